@@ -1,0 +1,387 @@
+"""Throughput of the CA-SGD outer iteration on GB300 (samples/s), with rooflines.
+
+A step is one training pass of the workload: `iters` CA-SGD outer iterations
+(sample+gather, Gram, recurrence, update) followed by one full-data loss evaluation,
+all in the kernels of libcasgd.so.  Default workload: logistic regression on a dense
+400,000 x 2,000 BF16 matrix (N(0,1)/sqrt(2000) entries, planted weights, 5% label
+flips), b=256, s=32 (Gram 8192 x 8192), eta=0.5, 50 outer iterations per step, seed 0,
+synthetic (the epsilon data set it stands in for is not available).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--config 1..5] [--s S]
+N > 1 runs under torchrun, one process per GPU: independent replicas (one GPU's
+problem per rank, no collective on the data path); value = samples of all ranks / max
+time.  `--impl reference` times the CPU oracle (the plain NumPy statement of the
+method) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth_inputs as si  # noqa: E402
+
+METRIC = "SGD samples/s per GB300 (CA-SGD); Gram TFLOP/s and % of roofline"
+STAGES = ("gather", "gram", "recurrence", "update")
+KERNEL_SOURCES = {"gram_tc": "k_gram_tc.cu", "gram_simt": "k_gram_simt.cu",
+                  "recurrence": "k_recur.cu", "update": "k_update.cu", "gather": "k_prep.cu"}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--s", type=int, default=None, help="override s (recipe 4 sweep)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload(cfg: int, s_override):
+    r = si.RECIPES[cfg]
+    s = s_override or r.s
+    iters = r.outer_iters(s=s)
+    return r, s, iters
+
+
+def workload_config(r, s, iters, S):
+    return {"workload": f"{si.LOSS_NAMES[r.loss]} CA-SGD, dense X {r.m}x{r.n} BF16, "
+                        f"b={r.b}, s={s} (Gram {S}x{S}), eta={r.eta}, {iters} outer iterations "
+                        f"+ 1 full-data loss per step, seed 0",
+            "m": r.m, "n": r.n, "b": r.b, "s": s, "S": S, "outer_iters_per_step": iters,
+            "loss": si.LOSS_NAMES[r.loss],
+            "l2_policy": f"inputs larger than L2: X is {r.m * ((r.n + 7) // 8 * 8) * 2 / 1e9:.2f} GB "
+                         "and each outer iteration gathers fresh random rows"}
+
+
+def alg_work(n, S, s, b, m):
+    """Algorithmic flops/bytes per outer iteration, per stage (strictly block-lower G)."""
+    frac = 1.0 - 1.0 / s
+    g_bytes = 2.0 * S * S * frac          # 4 bytes x S^2 (1-1/s) / 2 entries
+    return {
+        "gather": {"bytes": 2.0 * S * n * 2 + 4 * S + 2 * S + 4 * S, "flops": 2.0 * S * n},
+        "gram": {"flops": float(n) * S * S * frac, "bytes": 2.0 * S * n + g_bytes},
+        "recurrence": {"bytes": g_bytes + 10.0 * S, "flops": 2.0 * S * S * frac / 2},
+        "update": {"bytes": 2.0 * S * n + 4.0 * S + 8.0 * n, "flops": 2.0 * S * n},
+        "loss": {"bytes": 2.0 * m * ((n + 7) // 8 * 8) + 4.0 * m, "flops": 2.0 * m * n},
+    }
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def traffic_for(kernel: str, cfg: int):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path)).get(f"{kernel}@config{cfg}")
+    if not d:
+        return None
+    src = os.path.join(ROOT, "communication_avoiding_step_gb300", "csrc", KERNEL_SOURCES[kernel])
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return d["bytes_per_launch"] if d.get("source_sha256_16") == h else None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- CPU side ----
+def cpu_sample(cfg, s, budget_s=15.0, max_iters=8):
+    """Times the oracle's emulating-mode outer iteration on this host (bounded sample)."""
+    import oracle
+    r = si.RECIPES[cfg]
+    p = si.make_problem(cfg)
+    S = r.b * s
+    w = np.zeros(r.n, np.float32)
+    done, t_total = 0, 0.0
+    while done < max_iters and (t_total < budget_s or done == 0):
+        t0 = time.perf_counter()
+        w = oracle.outer_step(p.X, p.y, w, r.b, s, r.eta, r.loss, 0, done, mode="emulate")
+        t_total += time.perf_counter() - t0
+        done += 1
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": S * done / t_total, "unit": "samples/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} outer iteration(s) of the same workload (S={S}) in the oracle's "
+                      f"emulating mode (NumPy, BLAS on all host cores), {t_total:.2f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    r, s, iters = workload(args.config, args.s)
+    S = r.b * s
+    import oracle
+    p = si.make_problem(args.config)
+    w = np.zeros(r.n, np.float32)
+    k = 0
+    for _ in range(args.warmup):
+        w = oracle.outer_step(p.X, p.y, w, r.b, s, r.eta, r.loss, 0, k, mode="emulate")
+        k += 1
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        w = oracle.outer_step(p.X, p.y, w, r.b, s, r.eta, r.loss, 0, k, mode="emulate")
+        k += 1
+    dt = time.perf_counter() - t0
+    value = S * args.steps / dt
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    cfgd = workload_config(r, s, iters, S)
+    cfgd["reference_step"] = "one outer iteration (bounded sample of the workload)"
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "samples/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfgd,
+           "cpu_baseline": {"value": value, "unit": "samples/s", "cores": cores, "kind": "oracle",
+                            "sample": f"{args.steps} timed outer iterations, emulating mode"},
+           "e2e": {"value": value, "unit": "samples/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# --------------------------------------------------------------------- GPU side ----
+def run_ours(args):
+    import torch
+    import communication_avoiding_step_gb300 as casgd
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    casgd.load()
+
+    r, s, iters = workload(args.config, args.s)
+    S = r.b * s
+    p = si.make_problem(args.config)
+    X32 = torch.from_numpy(p.X).cuda()
+    y = torch.from_numpy(p.y).cuda()
+    data = casgd.Dataset.from_fp32(X32, y)
+    del X32
+    torch.cuda.synchronize()
+    params = casgd.Params(r.b, s, r.eta, r.loss, seed=rank)
+    ws = casgd.workspace(data, params)
+    w = torch.zeros(r.n, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(k0, events=None):
+        w.zero_()
+        hist, launches, kind = casgd.train(data, params, w, iters, ws, k0=k0,
+                                           loss_every=iters, stage_events=events)
+        return hist, launches, kind
+
+    k = 0
+    for _ in range(args.warmup):
+        step(k)
+        k += iters
+    n_ev = iters * casgd.STAGE_EVENTS
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+              for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches_total = 0
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            hist, launches, kind = step(k, events[i])
+            launches_total += launches
+            k += iters
+        end.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    elapsed = start.elapsed_time(end) / 1e3
+    if dist:
+        t = torch.tensor([elapsed], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    stage_ms = {st: 0.0 for st in STAGES}
+    for i in range(args.steps):
+        ev = events[i]
+        for it in range(iters):
+            b0 = it * casgd.STAGE_EVENTS
+            for si_, st in enumerate(STAGES):
+                stage_ms[st] += ev[b0 + si_].elapsed_time(ev[b0 + si_ + 1])
+    per_launch_ms = {st: stage_ms[st] / (args.steps * iters) for st in STAGES}
+    loss_ms = (elapsed * 1e3 - sum(stage_ms.values())) / args.steps  # loss + host gaps
+
+    samples = S * iters * args.steps * world
+    value = samples / elapsed
+    pk = peaks()
+    work = alg_work(r.n, S, s, r.b, r.m)
+    gram_name = "gram_tc" if kind == 1 else "gram_simt"
+    stages_out = {}
+    for st in STAGES:
+        t = per_launch_ms[st] / 1e3
+        ent = {"ms_per_launch": per_launch_ms[st],
+               "GB/s": work[st]["bytes"] / t / 1e9 if t > 0 else None}
+        if st == "gram":
+            ent["TFLOP/s"] = work[st]["flops"] / t / 1e12 if t > 0 else None
+            ent["kernel"] = gram_name
+        stages_out[st] = ent
+    dom = max(STAGES, key=lambda st: per_launch_ms[st])
+    t_dom = per_launch_ms[dom] / 1e3
+    if dom == "gram":
+        achieved = work["gram"]["flops"] / t_dom / 1e12
+        peak = pk["bf16_tflops_sustained"]
+        roof = {"kernel": gram_name, "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{pk['source']} bf16 dense, sustained (kernel timed inside "
+                               "a long step loop)",
+                "traffic": traffic_for(gram_name, args.config)}
+    else:
+        achieved = work[dom]["bytes"] / t_dom / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{pk['source']} HBM copy",
+                "traffic": traffic_for(dom, args.config)}
+    roof["units_per_launch"] = "one outer iteration (S rows)"
+
+    # ---- end to end: host buffers, copies inside the timed region ----------------
+    e2e = None
+    if not args.no_e2e:
+        Xh = data.X.cpu().pin_memory()
+        yh = data.y.cpu().pin_memory()
+        wh = torch.zeros(r.n).pin_memory()
+        w_out = torch.empty(r.n).pin_memory()
+        Xd = torch.empty_like(data.X)
+        yd = torch.empty_like(data.y)
+        data2 = casgd.Dataset(Xd, yd, r.n)
+        e_steps = max(2, min(args.steps, 5))
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(e_steps):
+            Xd.copy_(Xh, non_blocking=True)
+            yd.copy_(yh, non_blocking=True)
+            w.copy_(wh, non_blocking=True)
+            hist, _, _ = casgd.train(data2, params, w, iters, ws, k0=k, loss_every=iters)
+            w_out.copy_(w, non_blocking=True)
+            k += iters
+        t1.record(stream)
+        torch.cuda.synchronize()
+        e_el = t0.elapsed_time(t1) / 1e3
+        if dist:
+            t = torch.tensor([e_el], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_el = float(t.item())
+        e2e = {"value": S * iters * e_steps * world / e_el, "unit": "samples/s",
+               "h2d_bytes_per_step": Xh.numel() * 2 + yh.numel() * 4 + wh.numel() * 4,
+               "d2h_bytes_per_step": w_out.numel() * 4 + 8, "steps": e_steps}
+        del Xd, yd
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_sample(args.config, s)
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": value, "unit": "samples/s", "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup,
+               "ms_per_step": elapsed * 1e3 / args.steps, "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "config": workload_config(r, s, iters, S),
+               "parallelism": "replicas" if world > 1 else "single",
+               "gpu_launches": launches_total,
+               "roofline": roof, "stages": stages_out,
+               "loss_and_gaps_ms_per_step": loss_ms,
+               "gram_tflops": stages_out["gram"]["TFLOP/s"],
+               "final_loss": hist[0] if hist else None,
+               "clocks": clocks.summary(), "e2e": e2e, "cpu_baseline": cpu}
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

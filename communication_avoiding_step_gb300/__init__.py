@@ -1,0 +1,190 @@
+"""GB300-native mixed-precision communication-avoiding SGD (CA-SGD) for GLMs.
+
+Paper: Mixed-Precision Communication-Avoiding SGD for Generalized Linear Models on
+GPUs (abstract).  Every step of the outer iteration runs in the CUDA kernels of
+libcasgd.so (sm_103a); this module only marshals PyTorch tensors into the C ABI of
+include/casgd.h.  There is no CPU fallback: if the library is missing, `load()` and
+every call raise.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+
+import torch
+
+from ._native import (  # noqa: F401
+    CASGD_LOGISTIC, CASGD_LSQ, CASGD_POISSON, FLAG_GRAM_SIMT, FLAG_GRAM_TENSOR,
+    FLAG_TEST_STALL, FLAG_WRITE_DIAG_BLOCKS, STAGE_EVENTS, CasgdError, Data as _Data,
+    Params as _Params, Profile as _Profile, Taps as _Taps, check as _check, header_symbols,
+    load,
+)
+
+LOGISTIC, LSQ, POISSON = CASGD_LOGISTIC, CASGD_LSQ, CASGD_POISSON
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t) -> C.c_void_p | None:
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _need_cuda(t: torch.Tensor, name: str, dtype=None) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+@dataclass
+class Params:
+    b: int
+    s: int
+    eta: float
+    loss: int
+    seed: int = 0
+    flags: int = 0
+    timeout_us: int = 0
+
+    @property
+    def S(self) -> int:
+        return self.b * self.s
+
+    def c(self) -> _Params:
+        return _Params(self.b, self.s, self.eta, self.loss, self.seed, self.flags,
+                       self.timeout_us)
+
+
+class Dataset:
+    """BF16 data matrix X (m x ld, device) with n features and FP32 labels y."""
+
+    def __init__(self, X: torch.Tensor, y: torch.Tensor, n: int):
+        _need_cuda(X, "X", torch.bfloat16)
+        _need_cuda(y, "y", torch.float32)
+        if X.dim() != 2 or y.numel() != X.shape[0]:
+            raise ValueError("X must be m x ld and y must have m entries")
+        self.X, self.y, self.n = X, y, int(n)
+        self.m, self.ld = int(X.shape[0]), int(X.shape[1])
+
+    def c(self) -> _Data:
+        return _Data(self.m, self.n, self.ld, self.X.data_ptr(), self.y.data_ptr())
+
+    @classmethod
+    def from_fp32(cls, X32: torch.Tensor, y: torch.Tensor, stream=None) -> "Dataset":
+        """Stores an FP32 device matrix as BF16 (casgd_store_bf16), padded to ld % 8 == 0."""
+        X = store_bf16(X32, stream=stream)
+        return cls(X, y, X32.shape[1])
+
+
+def store_bf16(X32: torch.Tensor, ld: int | None = None, stream=None) -> torch.Tensor:
+    _need_cuda(X32, "X32", torch.float32)
+    m, n = X32.shape
+    ld = (n + 7) // 8 * 8 if ld is None else int(ld)
+    out = torch.empty((m, ld), dtype=torch.bfloat16, device=X32.device)
+    _check(load().casgd_store_bf16(_ptr(X32), m, n, n, _ptr(out), ld, _stream(stream)),
+           "casgd_store_bf16")
+    return out
+
+
+def sample_indices(m: int, count: int, seed: int, counter0: int, device="cuda",
+                   stream=None) -> torch.Tensor:
+    out = torch.empty(count, dtype=torch.int32, device=device)
+    _check(load().casgd_sample_indices(m, count, seed, counter0, _ptr(out), _stream(stream)),
+           "casgd_sample_indices")
+    return out
+
+
+def gram_elems(b: int, s: int, flags: int = 0) -> int:
+    return int(load().casgd_gram_elems(b, s, flags))
+
+
+def workspace_size(data: Dataset, params: Params) -> int:
+    nbytes = C.c_size_t(0)
+    _check(load().casgd_workspace_size(C.byref(data.c()), C.byref(params.c()), C.byref(nbytes)),
+           "casgd_workspace_size")
+    return int(nbytes.value)
+
+
+def workspace(data: Dataset, params: Params, stream=None) -> torch.Tensor:
+    """A fresh, initialised device workspace for (data, params)."""
+    nbytes = workspace_size(data, params)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=data.X.device)
+    _check(load().casgd_workspace_init(_ptr(ws), nbytes, _stream(stream)), "casgd_workspace_init")
+    return ws
+
+
+@dataclass
+class Taps:
+    idx_in: torch.Tensor | None = None
+    idx_out: torch.Tensor | None = None
+    G_out: torch.Tensor | None = None
+    r_out: torch.Tensor | None = None
+    alpha_out: torch.Tensor | None = None
+
+    def c(self) -> _Taps:
+        return _Taps(_ptr(self.idx_in), _ptr(self.idx_out), _ptr(self.G_out), _ptr(self.r_out),
+                     _ptr(self.alpha_out))
+
+    @classmethod
+    def alloc(cls, params: Params, device="cuda", G=True) -> "Taps":
+        S = params.S
+        return cls(
+            idx_out=torch.empty(S, dtype=torch.int32, device=device),
+            G_out=(torch.empty(gram_elems(params.b, params.s, params.flags), dtype=torch.float32,
+                               device=device) if G else None),
+            r_out=torch.empty(S, dtype=torch.int16, device=device),
+            alpha_out=torch.empty(S, dtype=torch.float32, device=device),
+        )
+
+
+def outer_step(data: Dataset, params: Params, w: torch.Tensor, k: int, ws: torch.Tensor,
+               taps: Taps | None = None, stream=None) -> None:
+    """One outer iteration k on w (FP32[n], updated in place).  Asynchronous."""
+    _need_cuda(w, "w", torch.float32)
+    t = C.byref(taps.c()) if taps is not None else None
+    _check(load().casgd_outer_step(C.byref(data.c()), C.byref(params.c()), _ptr(w), k, _ptr(ws),
+                                   ws.numel(), _stream(stream), t), "casgd_outer_step")
+
+
+def train(data: Dataset, params: Params, w: torch.Tensor, iters: int, ws: torch.Tensor,
+          k0: int = 0, loss_every: int = 0, stream=None, stage_events=None):
+    """`iters` outer iterations; returns (loss history list, launches, gram_kind).  Blocks."""
+    _need_cuda(w, "w", torch.float32)
+    nl = iters // loss_every if loss_every > 0 else 0
+    hist = (C.c_double * max(nl, 1))()
+    prof = _Profile()
+    ev_arr = None
+    if stage_events is not None:
+        ev_arr = (C.c_void_p * len(stage_events))(*[e.cuda_event for e in stage_events])
+        prof.stage_events = C.cast(ev_arr, C.POINTER(C.c_void_p))
+        prof.n_events = len(stage_events)
+    _check(load().casgd_train(C.byref(data.c()), C.byref(params.c()), _ptr(w), k0, iters,
+                              _ptr(ws), ws.numel(), _stream(stream), loss_every,
+                              hist if nl > 0 else None, C.byref(prof)), "casgd_train")
+    return [hist[i] for i in range(nl)], int(prof.launches), int(prof.gram_kind)
+
+
+def loss(data: Dataset, kind: int, w: torch.Tensor, ws: torch.Tensor, stream=None) -> float:
+    """Full-data loss f(w) (FP64 result).  Blocks."""
+    out = C.c_double(0.0)
+    _check(load().casgd_loss(C.byref(data.c()), kind, _ptr(w), _ptr(ws), ws.numel(),
+                             _stream(stream), C.byref(out)), "casgd_loss")
+    return float(out.value)
+
+
+def loss_async(data: Dataset, kind: int, w: torch.Tensor, ws: torch.Tensor,
+               out_dev: torch.Tensor, stream=None) -> None:
+    _need_cuda(out_dev, "out_dev", torch.float64)
+    _check(load().casgd_loss_async(C.byref(data.c()), kind, _ptr(w), _ptr(ws), ws.numel(),
+                                   _stream(stream), _ptr(out_dev)), "casgd_loss_async")
+
+
+def get_status(ws: torch.Tensor, stream=None) -> int:
+    """Sticky device status of ws (0 = ok); clears it.  Blocks."""
+    return int(load().casgd_get_status(_ptr(ws), _stream(stream)))

@@ -1,0 +1,344 @@
+// C ABI of libcasgd.so (declared in include/casgd.h): argument checks, workspace
+// layout, and the stream-ordered sequence of kernels for one CA-SGD outer iteration.
+//
+// Paper: Mixed-Precision Communication-Avoiding SGD for Generalized Linear Models on
+// GPUs (abstract).  Step order of one outer iteration: sample and gather the s
+// minibatches, form the Gram matrix and the BF16 margins, (sum G across processes --
+// absent on one GPU), run the inner recurrence, update the weights.
+#include <cstring>
+
+#include "casgd_internal.cuh"
+
+namespace casgd {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+constexpr int kLossSlots = 64;  // device slots for losses recorded by casgd_train
+
+struct Resolved {
+  Layout L;
+  Ctrl* ctrl;
+  int32_t* idx;
+  uint16_t* r;
+  float* yY;
+  float* alpha;
+  uint16_t* Y;
+  float* G;
+  float* upd;
+  double* loss_part;
+  double* loss_slots;
+};
+
+bool check_data(const casgd_data_t* d) {
+  if (!d || !d->X || !d->y) return false;
+  if (d->m < 1 || d->m >= (int64_t(1) << 31)) return false;
+  if (d->n < 1 || d->n > kMaxN) return false;
+  if (d->ld < d->n || (d->ld % 8) != 0) return false;
+  if ((reinterpret_cast<uintptr_t>(d->X) & 15u) != 0) return false;
+  return true;
+}
+
+bool check_params(const casgd_params_t* p) {
+  if (!p) return false;
+  if (p->b < 1 || p->s < 1 || p->s > kMaxS) return false;
+  if ((int64_t)p->b * p->s > kMaxSB) return false;
+  if (p->loss < CASGD_LOGISTIC || p->loss > CASGD_POISSON) return false;
+  if (!(p->eta == p->eta)) return false;  // NaN
+  return true;
+}
+
+int device_sms(int* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CASGD_ERR_CUDA;
+  if (cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return CASGD_ERR_CUDA;
+  return CASGD_OK;
+}
+
+Resolved resolve(void* ws, const Layout& L) {
+  char* base = static_cast<char*>(ws);
+  Resolved R;
+  R.L = L;
+  R.ctrl = reinterpret_cast<Ctrl*>(base);
+  R.idx = reinterpret_cast<int32_t*>(base + L.off_idx);
+  R.r = reinterpret_cast<uint16_t*>(base + L.off_r);
+  R.yY = reinterpret_cast<float*>(base + L.off_yY);
+  R.alpha = reinterpret_cast<float*>(base + L.off_alpha);
+  R.Y = reinterpret_cast<uint16_t*>(base + L.off_Y);
+  R.G = reinterpret_cast<float*>(base + L.off_G);
+  R.upd = reinterpret_cast<float*>(base + L.off_upd);
+  R.loss_part = reinterpret_cast<double*>(base + L.off_loss);
+  R.loss_slots = R.loss_part + kLossCtas;
+  return R;
+}
+
+int check_ws(void* ws, size_t ws_bytes, const Layout& L) {
+  if (!ws) return CASGD_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return CASGD_ERR_WORKSPACE;
+  if (ws_bytes < L.total) return CASGD_ERR_WORKSPACE;
+  return CASGD_OK;
+}
+
+// Layout for the loss alone (control block + partials), used when no params are known.
+size_t loss_only_bytes() {
+  return align_up(sizeof(Ctrl)) + align_up((size_t)(kLossCtas + kLossSlots) * sizeof(double));
+}
+
+int gram_choice(const casgd_params_t* p, int64_t S, int64_t n) {
+  const bool tc_ok = gram_tc_supported(S, n, p->b);
+  if (p->flags & CASGD_FLAG_GRAM_TENSOR) return tc_ok ? 1 : -1;
+  if (p->flags & CASGD_FLAG_GRAM_SIMT) return 2;
+  // Default: tensor cores where n is wide enough for the contraction to matter.
+  return (tc_ok && n > 32) ? 1 : 2;
+}
+
+int record(casgd_profile_t* prof, int64_t it, int e, cudaStream_t st) {
+  if (!prof || !prof->stage_events) return CASGD_OK;
+  const int64_t i = it * CASGD_STAGE_EVENTS + e;
+  if (i >= prof->n_events) return CASGD_OK;
+  if (cudaEventRecord(static_cast<cudaEvent_t>(prof->stage_events[i]), st) != cudaSuccess)
+    return CASGD_ERR_CUDA;
+  return CASGD_OK;
+}
+
+#define CK(expr)                                  \
+  do {                                            \
+    if ((expr) != cudaSuccess) return CASGD_ERR_CUDA; \
+  } while (0)
+
+int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, uint64_t k,
+                    void* ws, size_t ws_bytes, cudaStream_t st, const casgd_taps_t* taps,
+                    Ctx& c, casgd_profile_t* prof, int64_t it) {
+  const Layout L = make_layout(d->n, p->b, p->s, p->flags, c.num_sms);
+  int rc = check_ws(ws, ws_bytes, L);
+  if (rc != CASGD_OK) return rc;
+  Resolved R = resolve(ws, L);
+  const int choice = gram_choice(p, L.S, d->n);
+  if (choice < 0) return CASGD_ERR_UNSUPPORTED;
+  const bool diag = (p->flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
+  float* G = (taps && taps->G_out) ? taps->G_out : R.G;
+  const int32_t* idx_in = taps ? taps->idx_in : nullptr;
+  if (prof) prof->gram_kind = choice;
+
+  if ((rc = record(prof, it, 0, st)) != CASGD_OK) return rc;
+  CK(launch_gather(*d, *p, w, k, idx_in, R.idx, R.Y, L.ldY, R.r, R.yY, R.ctrl, c));
+  if ((rc = record(prof, it, 1, st)) != CASGD_OK) return rc;
+  if (choice == 1) {
+    CK(launch_gram_tc(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag, G, R.ctrl, p->timeout_us, c));
+  } else {
+    CK(launch_gram_simt(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag, G, c));
+  }
+  // (The sum of G over processes would sit here; on one GPU it is the identity.)
+  if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
+  CK(launch_recur(G, R.r, R.yY, R.alpha, p->b, p->s, p->eta, p->loss, p->flags,
+                  p->timeout_us, R.ctrl, c));
+  if ((rc = record(prof, it, 3, st)) != CASGD_OK) return rc;
+  CK(launch_update(R.Y, R.alpha, L.S, d->n, L.ldY, w, R.upd, L.upd_ctas, R.ctrl, c));
+  if ((rc = record(prof, it, 4, st)) != CASGD_OK) return rc;
+
+  if (taps) {
+    if (taps->idx_out)
+      CK(cudaMemcpyAsync(taps->idx_out, R.idx, L.S * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    if (taps->r_out)
+      CK(cudaMemcpyAsync(taps->r_out, R.r, L.S * sizeof(uint16_t), cudaMemcpyDeviceToDevice, st));
+    if (taps->alpha_out)
+      CK(cudaMemcpyAsync(taps->alpha_out, R.alpha, L.S * sizeof(float), cudaMemcpyDeviceToDevice, st));
+  }
+  return CASGD_OK;
+}
+
+int status_to_code(uint32_t st) {
+  if (st & ST_TIMEOUT) return CASGD_ERR_TIMEOUT;
+  if (st & ST_BAD_INDEX) return CASGD_ERR_BAD_INDEX;
+  if (st & ST_NONFINITE) return CASGD_ERR_NONFINITE;
+  return CASGD_OK;
+}
+
+int read_and_clear_status(Ctrl* ctrl, cudaStream_t st) {
+  uint32_t v = 0;
+  CK(cudaMemcpyAsync(&v, &ctrl->status, sizeof(v), cudaMemcpyDeviceToHost, st));
+  CK(cudaStreamSynchronize(st));
+  if (v != 0) {
+    CK(cudaMemsetAsync(&ctrl->status, 0, sizeof(uint32_t), st));
+    CK(cudaStreamSynchronize(st));
+  }
+  return status_to_code(v);
+}
+
+}  // namespace
+
+Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms) {
+  (void)num_sms;
+  Layout L;
+  L.S = (int64_t)b * s;
+  L.ldY = (n + 7) / 8 * 8;
+  L.gram_elems = gram_elems(b, s, (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0);
+  int64_t u = (L.S + 31) / 32;
+  L.upd_ctas = (int)(u > 320 ? 320 : u);
+  size_t off = align_up(sizeof(Ctrl));
+  L.off_loss = off;
+  off += align_up((size_t)(kLossCtas + kLossSlots) * sizeof(double));
+  L.off_idx = off;
+  off += align_up((size_t)L.S * sizeof(int32_t));
+  L.off_r = off;
+  off += align_up((size_t)L.S * sizeof(uint16_t));
+  L.off_yY = off;
+  off += align_up((size_t)L.S * sizeof(float));
+  L.off_alpha = off;
+  off += align_up((size_t)L.S * sizeof(float));
+  L.off_Y = off;
+  off += align_up((size_t)L.S * L.ldY * sizeof(uint16_t));
+  L.off_upd = off;
+  off += align_up((size_t)L.upd_ctas * L.ldY * sizeof(float));
+  L.off_G = off;
+  off += align_up((size_t)L.gram_elems * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+}  // namespace casgd
+
+using namespace casgd;
+
+extern "C" {
+
+const char* casgd_strerror(int code) {
+  switch (code) {
+    case CASGD_OK: return "ok";
+    case CASGD_ERR_ARG: return "invalid argument";
+    case CASGD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case CASGD_ERR_CUDA: return "CUDA runtime error";
+    case CASGD_ERR_NONFINITE: return "non-finite weight produced on the device";
+    case CASGD_ERR_TIMEOUT: return "an inter-CTA wait on the device exceeded its time bound";
+    case CASGD_ERR_BAD_INDEX: return "a given row index is outside [0, m)";
+    case CASGD_ERR_UNSUPPORTED: return "request not supported by this build";
+    default: return "unknown casgd status";
+  }
+}
+
+int casgd_version(void) { return CASGD_ABI_VERSION; }
+
+int64_t casgd_gram_elems(int32_t b, int32_t s, uint32_t flags) {
+  if (b < 1 || s < 1 || s > kMaxS || (int64_t)b * s > kMaxSB) return -1;
+  return gram_elems(b, s, (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0);
+}
+
+int casgd_workspace_size(const casgd_data_t* data, const casgd_params_t* params,
+                         size_t* bytes) {
+  if (!bytes || !check_params(params)) return CASGD_ERR_ARG;
+  if (!data || data->n < 1 || data->n > kMaxN) return CASGD_ERR_ARG;
+  *bytes = make_layout(data->n, params->b, params->s, params->flags, 0).total;
+  return CASGD_OK;
+}
+
+int casgd_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0 || ws_bytes < sizeof(Ctrl))
+    return CASGD_ERR_WORKSPACE;
+  if (cudaMemsetAsync(ws, 0, sizeof(Ctrl), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CASGD_ERR_CUDA;
+  return CASGD_OK;
+}
+
+int casgd_store_bf16(const float* src, int64_t m, int64_t n, int64_t ld_src, void* dst,
+                     int64_t ld_dst, void* stream) {
+  if (!src || !dst || m < 0 || n < 1 || ld_src < n || ld_dst < n || (ld_dst % 8) != 0)
+    return CASGD_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(dst) & 15u) != 0) return CASGD_ERR_ARG;
+  Ctx c{static_cast<cudaStream_t>(stream), 0, 0};
+  if (device_sms(&c.num_sms) != CASGD_OK) return CASGD_ERR_CUDA;
+  return launch_store_bf16(src, m, n, ld_src, static_cast<uint16_t*>(dst), ld_dst, c) ==
+                 cudaSuccess ? CASGD_OK : CASGD_ERR_CUDA;
+}
+
+int casgd_sample_indices(int64_t m, int64_t count, uint64_t seed, uint64_t counter0,
+                         int32_t* idx, void* stream) {
+  if (m < 1 || m >= (int64_t(1) << 31) || count < 0 || (count > 0 && !idx)) return CASGD_ERR_ARG;
+  Ctx c{static_cast<cudaStream_t>(stream), 0, 0};
+  if (device_sms(&c.num_sms) != CASGD_OK) return CASGD_ERR_CUDA;
+  return launch_sample(m, count, seed, counter0, idx, c) == cudaSuccess ? CASGD_OK
+                                                                        : CASGD_ERR_CUDA;
+}
+
+int casgd_outer_step(const casgd_data_t* data, const casgd_params_t* params, float* w,
+                     uint64_t k, void* ws, size_t ws_bytes, void* stream,
+                     const casgd_taps_t* taps) {
+  if (!check_data(data) || !check_params(params) || !w) return CASGD_ERR_ARG;
+  Ctx c{static_cast<cudaStream_t>(stream), 0, 0};
+  if (device_sms(&c.num_sms) != CASGD_OK) return CASGD_ERR_CUDA;
+  return outer_step_impl(data, params, w, k, ws, ws_bytes, c.stream, taps, c, nullptr, 0);
+}
+
+int casgd_loss_async(const casgd_data_t* data, int32_t loss, const float* w, void* ws,
+                     size_t ws_bytes, void* stream, double* out_dev) {
+  if (!check_data(data) || !w || !out_dev || loss < CASGD_LOGISTIC || loss > CASGD_POISSON)
+    return CASGD_ERR_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0 || ws_bytes < loss_only_bytes())
+    return CASGD_ERR_WORKSPACE;
+  Ctx c{static_cast<cudaStream_t>(stream), 0, 0};
+  if (device_sms(&c.num_sms) != CASGD_OK) return CASGD_ERR_CUDA;
+  Layout L = make_layout(data->n, 1, 1, 0, c.num_sms);
+  Resolved R = resolve(ws, L);
+  return launch_loss(*data, loss, w, R.loss_part, out_dev, R.ctrl, c) == cudaSuccess
+             ? CASGD_OK : CASGD_ERR_CUDA;
+}
+
+int casgd_loss(const casgd_data_t* data, int32_t loss, const float* w, void* ws,
+               size_t ws_bytes, void* stream, double* out) {
+  if (!out) return CASGD_ERR_ARG;
+  if (!check_data(data) || !w || loss < CASGD_LOGISTIC || loss > CASGD_POISSON)
+    return CASGD_ERR_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0 || ws_bytes < loss_only_bytes())
+    return CASGD_ERR_WORKSPACE;
+  Layout L = make_layout(data->n, 1, 1, 0, 0);
+  Resolved R = resolve(ws, L);
+  int rc = casgd_loss_async(data, loss, w, ws, ws_bytes, stream, R.loss_slots);
+  if (rc != CASGD_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CK(cudaMemcpyAsync(out, R.loss_slots, sizeof(double), cudaMemcpyDeviceToHost, st));
+  return read_and_clear_status(R.ctrl, st);
+}
+
+int casgd_train(const casgd_data_t* data, const casgd_params_t* params, float* w,
+                uint64_t k0, int32_t iters, void* ws, size_t ws_bytes, void* stream,
+                int32_t loss_every, double* loss_hist, casgd_profile_t* prof) {
+  if (!check_data(data) || !check_params(params) || !w || iters < 0 || loss_every < 0)
+    return CASGD_ERR_ARG;
+  if (loss_every > 0 && iters / loss_every > 0 && !loss_hist) return CASGD_ERR_ARG;
+  Ctx c{static_cast<cudaStream_t>(stream), 0, 0};
+  if (device_sms(&c.num_sms) != CASGD_OK) return CASGD_ERR_CUDA;
+  const Layout L = make_layout(data->n, params->b, params->s, params->flags, c.num_sms);
+  int rc = check_ws(ws, ws_bytes, L);
+  if (rc != CASGD_OK) return rc;
+  Resolved R = resolve(ws, L);
+  int slot = 0, flushed = 0;
+  for (int32_t it = 0; it < iters; ++it) {
+    rc = outer_step_impl(data, params, w, k0 + (uint64_t)it, ws, ws_bytes, c.stream, nullptr,
+                         c, prof, it);
+    if (rc != CASGD_OK) return rc;
+    if (loss_every > 0 && (it + 1) % loss_every == 0) {
+      CK(launch_loss(*data, params->loss, w, R.loss_part, R.loss_slots + slot, R.ctrl, c));
+      if (++slot == kLossSlots) {
+        CK(cudaMemcpyAsync(loss_hist + flushed, R.loss_slots, slot * sizeof(double),
+                           cudaMemcpyDeviceToHost, c.stream));
+        CK(cudaStreamSynchronize(c.stream));
+        flushed += slot;
+        slot = 0;
+      }
+    }
+  }
+  if (slot > 0)
+    CK(cudaMemcpyAsync(loss_hist + flushed, R.loss_slots, slot * sizeof(double),
+                       cudaMemcpyDeviceToHost, c.stream));
+  if (prof) prof->launches = c.launches;
+  return read_and_clear_status(R.ctrl, c.stream);
+}
+
+int casgd_get_status(void* ws, void* stream) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return CASGD_ERR_WORKSPACE;
+  return read_and_clear_status(static_cast<Ctrl*>(ws), static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,146 @@
+// Internal declarations shared by the CA-SGD kernels and the C-ABI layer.
+//
+// Paper: Mixed-Precision Communication-Avoiding SGD for Generalized Linear Models on
+// GPUs (abstract).  Kernel map (steps as numbered in include/casgd.h):
+//   k_prep.cu       a1 sampling, a2 gather into Y, a4 BF16 margins; BF16 storage
+//   k_gram_simt.cu  a3 Gram on CUDA cores (any n; used for narrow n)
+//   k_gram_tc.cu    a3 Gram on tcgen05 tensor cores with TMEM accumulators and TMA
+//   k_recur.cu      a6/a7 inner recurrence, persistent, flag-synchronised
+//   k_update.cu     a8 weight update, a9 full-data loss
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/casgd.h"
+
+namespace casgd {
+
+// Sticky device status bits (workspace word 0).
+enum : uint32_t {
+  ST_NONFINITE = 1u << 0,
+  ST_TIMEOUT = 1u << 1,
+  ST_BAD_INDEX = 1u << 2,
+};
+
+constexpr int kMaxS = 64;
+constexpr int64_t kMaxSB = 65536;
+constexpr int64_t kMaxN = 16384;
+constexpr int kLossCtas = 1024;     // upper bound on loss-kernel CTAs (partials)
+
+// Control block at the start of the workspace (256 bytes, zeroed per step where noted).
+struct Ctrl {
+  uint32_t status;        // sticky ST_* bits (cleared by casgd_get_status)
+  uint32_t abort;         // set by a waiter that timed out; others stop waiting
+  uint32_t next_unit;     // recurrence work queue (zeroed by the gather kernel)
+  uint32_t loss_done;     // loss kernel: CTAs finished (zeroed by the loss kernel's last CTA)
+  uint32_t upd_done;      // update kernel: CTAs finished
+  uint32_t pad0[3];
+  uint32_t block_done[kMaxS];  // recurrence: units finished per block (zeroed per step)
+};
+static_assert(sizeof(Ctrl) <= 512, "control block");
+
+// Byte layout of the workspace for one (data, params) pair.
+struct Layout {
+  int64_t S, ldY, gram_elems;
+  int upd_ctas;
+  size_t off_idx, off_r, off_yY, off_alpha, off_Y, off_G, off_upd, off_loss, total;
+};
+
+Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms);
+
+inline int64_t gram_elems(int64_t b, int64_t s, bool diag) {
+  int64_t nblk = diag ? s * (s + 1) / 2 : s * (s - 1) / 2;
+  return nblk * b * b;
+}
+
+__host__ __device__ inline int64_t packed_offset(int64_t j, int64_t t, int64_t b, bool diag) {
+  return (diag ? (j * (j + 1) / 2 + t) : (j * (j - 1) / 2 + t)) * b * b;
+}
+
+// ------------------------------------------------------------------ device helpers
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+// SplitMix64 output number `counter` of the stream started at state `seed`.
+__device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t counter) {
+  uint64_t z = seed + (counter + 1ull) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+__device__ __forceinline__ int32_t sample_row(uint64_t seed, uint64_t counter, uint32_t m) {
+  uint64_t h = splitmix64_at(seed, counter);
+  return (int32_t)(((h >> 32) * (uint64_t)m) >> 32);
+}
+
+// l'(z, y) for the three GLMs, FP32.
+__device__ __forceinline__ float loss_deriv(int kind, float z, float y) {
+  if (kind == CASGD_LOGISTIC) return -y / (1.0f + expf(y * z));
+  if (kind == CASGD_LSQ) return z - y;
+  return expf(z) - y;
+}
+
+// l(z, y), FP32; the logistic form avoids overflow: log(1+e^{-t}) = max(-t,0) + log1p(e^{-|t|}).
+__device__ __forceinline__ float loss_value(int kind, float z, float y) {
+  if (kind == CASGD_LOGISTIC) {
+    float t = y * z;
+    return fmaxf(-t, 0.0f) + log1pf(expf(-fabsf(t)));
+  }
+  if (kind == CASGD_LSQ) {
+    float d = z - y;
+    return 0.5f * d * d;
+  }
+  return expf(z) - y * z;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
+  return *reinterpret_cast<const volatile uint32_t*>(p);
+}
+
+// ------------------------------------------------------------------ launchers
+struct Ctx {
+  cudaStream_t stream;
+  int num_sms;
+  int64_t launches;
+};
+
+cudaError_t launch_store_bf16(const float* src, int64_t m, int64_t n, int64_t ld_src,
+                              uint16_t* dst, int64_t ld_dst, Ctx& c);
+cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t counter0,
+                          int32_t* idx, Ctx& c);
+cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const float* w,
+                          uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
+                          int64_t ldY, uint16_t* r, float* yY, Ctrl* ctrl, Ctx& c);
+cudaError_t launch_gram_simt(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
+                             int s, bool diag, float* G, Ctx& c);
+bool gram_tc_supported(int64_t S, int64_t n, int b);
+cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
+                           int s, bool diag, float* G, Ctrl* ctrl, uint32_t timeout_us,
+                           Ctx& c);
+cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, float* alpha,
+                         int b, int s, float eta, int loss, uint32_t flags,
+                         uint32_t timeout_us, Ctrl* ctrl, Ctx& c);
+cudaError_t launch_update(const uint16_t* Y, const float* alpha, int64_t S, int64_t n,
+                          int64_t ldY, float* w, float* part, int upd_ctas, Ctrl* ctrl,
+                          Ctx& c);
+int loss_ctas(int num_sms);
+cudaError_t launch_loss(const casgd_data_t& d, int loss, const float* w, double* part,
+                        double* out_dev, Ctrl* ctrl, Ctx& c);
+
+}  // namespace casgd

@@ -1,0 +1,157 @@
+// Steps a1 (sampling), a2 (gather) and a4 (BF16 margins), plus the BF16 storage step.
+//
+// Paper: Mixed-Precision Communication-Avoiding SGD for Generalized Linear Models on
+// GPUs (abstract): the recipe stores the input matrix and the margin vector in low
+// precision; each outer iteration works on s minibatches of b rows.
+//
+// The gather writes Y (S x ldY BF16, ldY = n rounded up to 8, zero padded) once per
+// outer iteration.  Y is small next to X and stays L2-resident for the Gram and update
+// kernels; it lets the Gram kernel fetch tiles with plain tiled TMA copies.
+#include <cuda_bf16.h>
+
+#include "casgd_internal.cuh"
+
+namespace casgd {
+
+namespace {
+
+__global__ void store_bf16_kernel(const float* __restrict__ src, int64_t m, int64_t n,
+                                  int64_t ld_src, uint16_t* __restrict__ dst, int64_t ld_dst) {
+  const int64_t vec_per_row = ld_dst / 8;
+  const int64_t total = m * vec_per_row;
+  for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < total;
+       v += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = v / vec_per_row;
+    const int64_t c0 = (v - row * vec_per_row) * 8;
+    const float* s = src + row * ld_src;
+    uint32_t packed[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const int64_t c = c0 + 2 * h;
+      const float a = (c < n) ? s[c] : 0.0f;
+      const float b = (c + 1 < n) ? s[c + 1] : 0.0f;
+      packed[h] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+    }
+    *reinterpret_cast<uint4*>(dst + row * ld_dst + c0) =
+        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  }
+}
+
+__global__ void sample_kernel(uint32_t m, int64_t count, uint64_t seed, uint64_t counter0,
+                              int32_t* __restrict__ idx) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count;
+       i += (int64_t)gridDim.x * blockDim.x)
+    idx[i] = sample_row(seed, counter0 + (uint64_t)i, m);
+}
+
+// One group of G lanes (G a power of two <= 32) per row of Y.  Lane g copies the
+// 16-byte vectors g, g+G, ... of the row and accumulates their FP32 dot with w; the
+// group then reduces with shuffles and its first lane stores the BF16 margin.
+__global__ void __launch_bounds__(256) gather_kernel(
+    const uint16_t* __restrict__ X, const float* __restrict__ y, int64_t m, int64_t n,
+    int64_t ld, const float* __restrict__ w, int64_t S, uint64_t seed, uint64_t counter0,
+    const int32_t* __restrict__ idx_in, int32_t* __restrict__ idx_out,
+    uint16_t* __restrict__ Y, int64_t ldY, uint16_t* __restrict__ r,
+    float* __restrict__ yY, Ctrl* ctrl, int s, int G) {
+  if (blockIdx.x == 0) {
+    if (threadIdx.x == 0) {
+      ctrl->next_unit = 0;
+      ctrl->abort = 0;
+    }
+    for (int j = threadIdx.x; j < kMaxS; j += blockDim.x) ctrl->block_done[j] = 0;
+  }
+  const int lane = threadIdx.x & 31;
+  const int g = lane & (G - 1);
+  const int rows_per_warp = 32 / G;
+  const int64_t p = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * rows_per_warp +
+                    lane / G;
+  const int64_t nvec = ldY / 8;
+  // Every lane of the warp must reach the shuffles, so out-of-range rows only mask.
+  const bool live = p < S;
+  int32_t row = 0;
+  bool valid = false;
+  if (live) {
+    if (idx_in) {
+      row = idx_in[p];
+      valid = (row >= 0 && (int64_t)row < m);
+      if (!valid && g == 0) atomicOr(&ctrl->status, ST_BAD_INDEX);
+    } else {
+      row = sample_row(seed, counter0 + (uint64_t)p, (uint32_t)m);
+      valid = true;
+    }
+  }
+  float acc = 0.0f;
+  if (live) {
+    const uint16_t* xr = X + (int64_t)(valid ? row : 0) * ld;
+    uint16_t* yr = Y + p * ldY;
+    for (int64_t v = g; v < nvec; v += G) {
+      const int64_t c0 = v * 8;
+      uint4 q = make_uint4(0, 0, 0, 0);
+      if (valid) q = __ldg(reinterpret_cast<const uint4*>(xr + c0));
+      uint32_t parts[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int64_t c = c0 + 2 * h;
+        uint32_t lo = parts[h] & 0xFFFFu, hi = parts[h] >> 16;
+        if (c >= n) lo = 0;
+        if (c + 1 >= n) hi = 0;
+        parts[h] = lo | (hi << 16);
+        if (c < n) acc = fmaf(bf16_bits_to_float(lo), __ldg(w + c), acc);
+        if (c + 1 < n) acc = fmaf(bf16_bits_to_float(hi), __ldg(w + c + 1), acc);
+      }
+      *reinterpret_cast<uint4*>(yr + c0) = make_uint4(parts[0], parts[1], parts[2], parts[3]);
+    }
+  }
+  for (int off = G >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);
+  if (live && g == 0) {
+    r[p] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+    yY[p] = valid ? __ldg(y + row) : 0.0f;
+    idx_out[p] = row;
+  }
+}
+
+int pow2_at_least(int64_t v, int cap) {
+  int g = 1;
+  while (g < v && g < cap) g <<= 1;
+  return g;
+}
+
+}  // namespace
+
+cudaError_t launch_store_bf16(const float* src, int64_t m, int64_t n, int64_t ld_src,
+                              uint16_t* dst, int64_t ld_dst, Ctx& c) {
+  const int64_t total = m * (ld_dst / 8);
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > (int64_t)c.num_sms * 16) blocks = (int64_t)c.num_sms * 16;
+  store_bf16_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>(src, m, n, ld_src, dst, ld_dst);
+  ++c.launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t counter0,
+                          int32_t* idx, Ctx& c) {
+  if (count == 0) return cudaSuccess;
+  int64_t blocks = (count + 255) / 256;
+  if (blocks > (int64_t)c.num_sms * 8) blocks = (int64_t)c.num_sms * 8;
+  sample_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>((uint32_t)m, count, seed, counter0, idx);
+  ++c.launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const float* w,
+                          uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
+                          int64_t ldY, uint16_t* r, float* yY, Ctrl* ctrl, Ctx& c) {
+  const int64_t S = (int64_t)p.b * p.s;
+  const int G = pow2_at_least(ldY / 8, 32);
+  const int64_t rows_per_cta = 8 * (32 / G);
+  const int64_t blocks = (S + rows_per_cta - 1) / rows_per_cta;
+  gather_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>(
+      static_cast<const uint16_t*>(d.X), d.y, d.m, d.n, d.ld, w, S, p.seed, k * (uint64_t)S,
+      idx_in, idx, Y, ldY, r, yY, ctrl, p.s, G);
+  ++c.launches;
+  return cudaGetLastError();
+}
+
+}  // namespace casgd

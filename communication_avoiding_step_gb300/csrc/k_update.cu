@@ -1,0 +1,190 @@
+// Step a8, the FP32 weight update w += Y^T alpha, and step a9, the full-data loss.
+//
+// Paper: Mixed-Precision Communication-Avoiding SGD for Generalized Linear Models on
+// GPUs (abstract): weight updates run in high precision; the method's accuracy claim
+// is stated on the training loss of logistic, linear and Poisson problems.
+//
+// Both are streaming reductions bound by HBM (the loss) or L2 (the update, whose Y was
+// written one step earlier).  Both reduce in a fixed order so that results do not
+// depend on scheduling: the update writes one FP32 partial row per CTA and a second
+// kernel sums them column by column; the loss keeps FP32 per-row values, FP64 per-CTA
+// partials, and the last CTA to finish sums the partials in CTA order.
+#include "casgd_internal.cuh"
+
+namespace casgd {
+
+namespace {
+
+constexpr int kMaxVecPerThread = 8;  // 16-byte vectors per thread: ldY <= 256*8*8
+
+// CTA p sums alpha_i * Y_i over its row range into part[p][:] (ldY floats).
+// Threads form TR row-lanes x TV vector-lanes (TV a power of two, TR = 256/TV).
+__global__ void __launch_bounds__(256) update_partial_kernel(
+    const uint16_t* __restrict__ Y, const float* __restrict__ alpha, int64_t S, int64_t ldY,
+    float* __restrict__ part, int TV) {
+  extern __shared__ float red[];  // [TR][TV*8] when TR > 1
+  const int64_t nvec = ldY / 8;
+  const int TR = 256 / TV;
+  const int tv = threadIdx.x % TV, tr = threadIdx.x / TV;
+  const int64_t r_lo = S * blockIdx.x / gridDim.x;
+  const int64_t r_hi = S * (blockIdx.x + 1) / gridDim.x;
+  float acc[kMaxVecPerThread][8];
+#pragma unroll
+  for (int v = 0; v < kMaxVecPerThread; ++v)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[v][e] = 0.0f;
+
+  for (int64_t i = r_lo + tr; i < r_hi; i += TR) {
+    const float a = __ldg(alpha + i);
+    const uint16_t* yr = Y + i * ldY;
+#pragma unroll
+    for (int v = 0; v < kMaxVecPerThread; ++v) {
+      const int64_t vec = tv + (int64_t)v * TV;
+      if (vec < nvec) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(yr + vec * 8));
+        const uint32_t pw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          acc[v][2 * h] = fmaf(a, bf16_bits_to_float(pw[h] & 0xFFFFu), acc[v][2 * h]);
+          acc[v][2 * h + 1] = fmaf(a, bf16_bits_to_float(pw[h] >> 16), acc[v][2 * h + 1]);
+        }
+      }
+    }
+  }
+
+  float* out = part + (int64_t)blockIdx.x * ldY;
+  if (TR == 1) {
+#pragma unroll
+    for (int v = 0; v < kMaxVecPerThread; ++v) {
+      const int64_t vec = tv + (int64_t)v * TV;
+      if (vec < nvec)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) out[vec * 8 + e] = acc[v][e];
+    }
+    return;
+  }
+  // TR > 1 means TV*8 >= ldY fits one vector per thread (v = 0 only).
+  for (int e = 0; e < 8; ++e) red[tr * TV * 8 + tv * 8 + e] = acc[0][e];
+  __syncthreads();
+  for (int col = threadIdx.x; col < TV * 8; col += 256) {
+    float sum = 0.0f;
+    for (int q = 0; q < TR; ++q) sum += red[q * TV * 8 + col];
+    if (col < ldY) out[col] = sum;
+  }
+}
+
+__global__ void update_reduce_kernel(const float* __restrict__ part, int P, int64_t n,
+                                     int64_t ldY, float* __restrict__ w, Ctrl* ctrl) {
+  const int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (c >= n) return;
+  float sum = 0.0f;
+  for (int p = 0; p < P; ++p) sum += part[(int64_t)p * ldY + c];
+  const float v = w[c] + sum;
+  w[c] = v;
+  if (!isfinite(v)) atomicOr(&ctrl->status, ST_NONFINITE);
+}
+
+// Loss: groups of G lanes per row (as in the gather), grid-stride over rows.
+__global__ void __launch_bounds__(256) loss_kernel(const uint16_t* __restrict__ X,
+                                                   const float* __restrict__ y, int64_t m,
+                                                   int64_t n, int64_t ld, int loss,
+                                                   const float* __restrict__ w,
+                                                   double* __restrict__ part,
+                                                   double* __restrict__ out, Ctrl* ctrl,
+                                                   int G) {
+  __shared__ double red[8];
+  __shared__ bool s_last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane & (G - 1);
+  const int rows_per_warp = 32 / G;
+  const int64_t nvec = (n + 7) / 8;
+  const int64_t rows_per_pass = (int64_t)gridDim.x * 8 * rows_per_warp;
+  double mine = 0.0;
+  for (int64_t base = ((int64_t)blockIdx.x * 8 + warp) * rows_per_warp; base < m;
+       base += rows_per_pass) {
+    const int64_t row = base + lane / G;
+    const bool live = row < m;
+    float acc = 0.0f;
+    if (live) {
+      const uint16_t* xr = X + row * ld;
+      for (int64_t v = g; v < nvec; v += G) {
+        const int64_t c0 = v * 8;
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(xr + c0));
+        const uint32_t pw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int64_t c = c0 + 2 * h;
+          if (c < n) acc = fmaf(bf16_bits_to_float(pw[h] & 0xFFFFu), __ldg(w + c), acc);
+          if (c + 1 < n) acc = fmaf(bf16_bits_to_float(pw[h] >> 16), __ldg(w + c + 1), acc);
+        }
+      }
+    }
+    for (int off = G >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);
+    if (live && g == 0) mine += (double)loss_value(loss, acc, __ldg(y + row));
+  }
+  for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
+  if (lane == 0) red[warp] = mine;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int q = 0; q < 8; ++q) t += red[q];
+    part[blockIdx.x] = t;
+    __threadfence();
+    const uint32_t done = atomicAdd(&ctrl->loss_done, 1u);
+    s_last = (done == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (s_last && threadIdx.x == 0) {
+    __threadfence();
+    double t = 0.0;
+    for (unsigned q = 0; q < gridDim.x; ++q) t += __ldcg(part + q);
+    *out = t / (double)m;
+    ctrl->loss_done = 0;
+  }
+}
+
+int pow2_at_least(int64_t v, int cap) {
+  int g = 1;
+  while (g < v && g < cap) g <<= 1;
+  return g;
+}
+
+}  // namespace
+
+cudaError_t launch_update(const uint16_t* Y, const float* alpha, int64_t S, int64_t n,
+                          int64_t ldY, float* w, float* part, int upd_ctas, Ctrl* ctrl,
+                          Ctx& c) {
+  const int64_t nvec = ldY / 8;
+  const int TV = pow2_at_least(nvec, 256);
+  const int TR = 256 / TV;
+  const size_t smem = TR > 1 ? (size_t)TR * TV * 8 * sizeof(float) : 0;
+  update_partial_kernel<<<upd_ctas, 256, smem, c.stream>>>(Y, alpha, S, ldY, part, TV);
+  ++c.launches;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const unsigned blocks = (unsigned)((n + 255) / 256);
+  update_reduce_kernel<<<blocks, 256, 0, c.stream>>>(part, upd_ctas, n, ldY, w, ctrl);
+  ++c.launches;
+  return cudaGetLastError();
+}
+
+int loss_ctas(int num_sms) {
+  int v = num_sms * 4;
+  return v > kLossCtas ? kLossCtas : v;
+}
+
+cudaError_t launch_loss(const casgd_data_t& d, int loss, const float* w, double* part,
+                        double* out_dev, Ctrl* ctrl, Ctx& c) {
+  const int G = pow2_at_least((d.n + 7) / 8, 32);
+  const int64_t rows_per_cta = 8 * (32 / G);
+  int64_t blocks = (d.m + rows_per_cta - 1) / rows_per_cta;
+  const int cap = loss_ctas(c.num_sms);
+  if (blocks > cap) blocks = cap;
+  loss_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>(static_cast<const uint16_t*>(d.X), d.y,
+                                                      d.m, d.n, d.ld, loss, w, part, out_dev,
+                                                      ctrl, G);
+  ++c.launches;
+  return cudaGetLastError();
+}
+
+}  // namespace casgd

@@ -1,0 +1,187 @@
+/*
+ * casgd.h -- C ABI of the GB300 (sm_103a) mixed-precision CA-SGD library (libcasgd.so).
+ *
+ * Method: "Mixed-Precision Communication-Avoiding SGD for Generalized Linear Models on
+ * GPUs" (abstract).  Communication-avoiding SGD batches s minibatch steps of b rows
+ * into one outer iteration whose only cross-process exchange is an sb x sb Gram
+ * matrix; the recipe keeps the data matrix and the margins in BF16, forms the Gram
+ * matrix from BF16 inputs with FP32 accumulation and runs the inner recurrence and
+ * the weight update in FP32.  One outer iteration (S = s*b) does:
+ *   a1  sample S row indices (counter-based, reproducible; see casgd_sample_indices)
+ *   a2  gather Y = X[idx,:] (S x n, BF16) and y_Y = y[idx]
+ *   a3  G = Y Y^T, BF16 products, FP32 accumulation; only blocks G_{j,t}, t < j
+ *   a4  r = Y w, FP32 accumulation, rounded once to BF16
+ *   a5  (sum of G over processes: absent on one GPU)
+ *   a6  for j = 0..s-1: z_j = r_j + sum_{t<j} G_{j,t} alpha_t,
+ *       alpha_j = -(eta/b) * l'(z_j, y_j)            (FP32)
+ *   a7  l' of the loss: logistic -y/(1+exp(y z)); least squares z-y; Poisson exp(z)-y
+ *   a8  w += Y^T alpha                                 (FP32)
+ *   a9  (separately) f(w) = (1/m) sum_i l(x_i.w, y_i)
+ * In exact arithmetic one outer iteration equals s plain minibatch-SGD steps.
+ *
+ * Conventions for every call:
+ *  - All arrays are allocated by the caller; the library allocates no device or
+ *    host memory and keeps no global state.  "device" pointers must be CUDA device
+ *    (or managed) memory of the current device; "host" pointers ordinary memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Every call is ordered on it; calls documented as "blocks" synchronize it.
+ *  - Argument errors are detected on the host before anything is launched and are
+ *    returned at once (CASGD_ERR_ARG, CASGD_ERR_WORKSPACE, CASGD_ERR_UNSUPPORTED).
+ *    A failed CUDA launch returns CASGD_ERR_CUDA.  Errors found on the device
+ *    (CASGD_ERR_NONFINITE, CASGD_ERR_TIMEOUT, CASGD_ERR_BAD_INDEX) are sticky bits in
+ *    the workspace, reported by casgd_get_status, casgd_train and casgd_loss.
+ *  - Limits: 1 <= m < 2^31; 1 <= n <= 16384; ld % 8 == 0 and ld >= n; X 16-byte
+ *    aligned; 1 <= b; 1 <= s <= 64; S = s*b <= 65536.
+ *  - The data matrix X is BF16 (raw 16-bit patterns), m x ld row-major; columns
+ *    n..ld-1 are never read as data.
+ */
+#ifndef CASGD_H
+#define CASGD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CASGD_ABI_VERSION 1
+
+/* GLM losses (the abstract: logistic, linear and Poisson problems). */
+enum { CASGD_LOGISTIC = 0, CASGD_LSQ = 1, CASGD_POISSON = 2 };
+
+/* Return codes. */
+enum {
+  CASGD_OK = 0,
+  CASGD_ERR_ARG = 1,          /* bad pointer, size, alignment or enum            */
+  CASGD_ERR_WORKSPACE = 2,    /* workspace missing, misaligned or too small       */
+  CASGD_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed             */
+  CASGD_ERR_NONFINITE = 4,    /* device: the update produced a NaN or Inf weight  */
+  CASGD_ERR_TIMEOUT = 5,      /* device: an inter-CTA wait ran past its bound     */
+  CASGD_ERR_BAD_INDEX = 6,    /* device: a caller-given row index outside [0, m)  */
+  CASGD_ERR_UNSUPPORTED = 7   /* valid request this build does not support        */
+};
+
+/* casgd_params_t.flags */
+#define CASGD_FLAG_WRITE_DIAG_BLOCKS 0x1u  /* also compute and store G_{j,j} (parity)   */
+#define CASGD_FLAG_GRAM_TENSOR       0x2u  /* force the tcgen05 tensor-core Gram kernel */
+#define CASGD_FLAG_GRAM_SIMT         0x4u  /* force the CUDA-core Gram kernel          */
+#define CASGD_FLAG_TEST_STALL        0x80000000u /* test only: the recurrence's first
+                                              block never signals completion, so every
+                                              waiter runs into its time bound and the
+                                              step ends with CASGD_ERR_TIMEOUT        */
+
+/* The data set (device pointers). */
+typedef struct {
+  int64_t m;         /* rows                                                    */
+  int64_t n;         /* features                                                */
+  int64_t ld;        /* row pitch of X in elements (multiple of 8, >= n)         */
+  const void* X;     /* device, BF16 bits, m x ld, 16-byte aligned              */
+  const float* y;    /* device, m labels (logistic: +-1; Poisson: counts)        */
+} casgd_data_t;
+
+/* Method parameters. */
+typedef struct {
+  int32_t b;           /* minibatch rows                                       */
+  int32_t s;           /* minibatch steps per outer iteration                  */
+  float eta;           /* step size; alpha = -(eta/b) l'                        */
+  int32_t loss;        /* CASGD_LOGISTIC / CASGD_LSQ / CASGD_POISSON            */
+  uint64_t seed;       /* sampling seed                                        */
+  uint32_t flags;      /* CASGD_FLAG_*                                         */
+  uint32_t timeout_us; /* bound on each inter-CTA wait; 0 = 1,000,000 us        */
+} casgd_params_t;
+
+/* Optional taps of one outer iteration (any member may be NULL; device memory). */
+typedef struct {
+  const int32_t* idx_in; /* S row indices to use instead of sampling; an index
+                            outside [0,m) sets CASGD_ERR_BAD_INDEX and its row is
+                            treated as zeros                                    */
+  int32_t* idx_out;      /* receives the S indices used                         */
+  float* G_out;          /* receives G in the packed block-lower layout:
+                            blocks (j,t) for t<j (t<=j with WRITE_DIAG_BLOCKS),
+                            j ascending then t ascending, each b x b row-major;
+                            casgd_gram_elems() floats                           */
+  uint16_t* r_out;       /* receives the S BF16 margins (bit patterns)          */
+  float* alpha_out;      /* receives the S FP32 step coefficients alpha         */
+} casgd_taps_t;
+
+/* Optional instrumentation of casgd_train (host struct). */
+typedef struct {
+  int64_t launches;      /* out: number of kernels the call launched            */
+  void** stage_events;   /* in: NULL, or cudaEvent_t handles; when given, event
+                            [it*CASGD_STAGE_EVENTS + e] is recorded on `stream`
+                            before stage e of outer iteration it (e = 0 gather,
+                            1 Gram, 2 recurrence, 3 update, 4 after update)     */
+  int32_t n_events;      /* in: length of stage_events                          */
+  int32_t gram_kind;     /* out: 1 = tcgen05 Gram kernel used, 2 = CUDA-core    */
+} casgd_profile_t;
+#define CASGD_STAGE_EVENTS 5
+
+/* Message for a return code (static string; never NULL). */
+const char* casgd_strerror(int code);
+
+/* CASGD_ABI_VERSION of the loaded library. */
+int casgd_version(void);
+
+/* Number of floats in the packed block-lower G for (b, s, flags); -1 on bad input. */
+int64_t casgd_gram_elems(int32_t b, int32_t s, uint32_t flags);
+
+/* Bytes of device workspace casgd_outer_step / casgd_train / casgd_loss need for
+ * (data, params); writes *bytes.  Host only, launches nothing.  The workspace must be
+ * 256-byte aligned and is owned by the caller; one workspace serves one stream at a
+ * time. */
+int casgd_workspace_size(const casgd_data_t* data, const casgd_params_t* params,
+                         size_t* bytes);
+
+/* Zero the control block of a workspace.  Call once on a fresh workspace (or
+ * zero-fill its first 512 bytes) before its first use; the library keeps it
+ * consistent afterwards.  Asynchronous. */
+int casgd_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Storage step of the recipe (the abstract: the input matrix is stored in low
+ * precision).  dst[i*ld_dst + c] = BF16 round-to-nearest-even of src[i*ld_src + c]
+ * for c < n, and 0 for n <= c < ld_dst.  src: device FP32 m x ld_src; dst: device
+ * BF16 bits m x ld_dst (ld_dst % 8 == 0, 16-byte aligned).  Asynchronous. */
+int casgd_store_bf16(const float* src, int64_t m, int64_t n, int64_t ld_src,
+                     void* dst, int64_t ld_dst, void* stream);
+
+/* Step a1 on its own.  idx[i] = ((h >> 32) * m) >> 32 where h is output number
+ * (counter0 + i) of SplitMix64 started from state `seed` (Steele, Lea & Flood 2014):
+ * h = mix(seed + (counter0 + i + 1) * 0x9E3779B97F4A7C15).  Outer iteration k uses
+ * counter0 = k*s*b, so plain SGD step q (counters q*b...) sees the same rows.
+ * idx: device int32[count].  Asynchronous. */
+int casgd_sample_indices(int64_t m, int64_t count, uint64_t seed, uint64_t counter0,
+                         int32_t* idx, void* stream);
+
+/* One outer iteration k (steps a1-a8) on w (device FP32[n], updated in place).
+ * ws: device workspace of ws_bytes (casgd_workspace_size).  taps: NULL or optional
+ * inputs/outputs for parity checks.  Asynchronous; device errors are sticky in ws. */
+int casgd_outer_step(const casgd_data_t* data, const casgd_params_t* params, float* w,
+                     uint64_t k, void* ws, size_t ws_bytes, void* stream,
+                     const casgd_taps_t* taps);
+
+/* `iters` outer iterations k = k0 .. k0+iters-1.  If loss_every > 0, f(w) is
+ * evaluated after every loss_every-th iteration and written to host
+ * loss_hist[iters/loss_every].  Blocks at the end (one stream synchronize) and
+ * returns the first sticky device error, which it clears.  prof may be NULL. */
+int casgd_train(const casgd_data_t* data, const casgd_params_t* params, float* w,
+                uint64_t k0, int32_t iters, void* ws, size_t ws_bytes, void* stream,
+                int32_t loss_every, double* loss_hist, casgd_profile_t* prof);
+
+/* Step a9: f(w) = (1/m) sum_i l(x_i . w, y_i) with x_i the BF16 rows, each row's
+ * dot product and loss in FP32, the sum in FP64.  Writes host *out; blocks. */
+int casgd_loss(const casgd_data_t* data, int32_t loss, const float* w, void* ws,
+               size_t ws_bytes, void* stream, double* out);
+
+/* Same as casgd_loss but asynchronous: the FP64 result goes to device *out_dev. */
+int casgd_loss_async(const casgd_data_t* data, int32_t loss, const float* w, void* ws,
+                     size_t ws_bytes, void* stream, double* out_dev);
+
+/* Blocks on `stream`, returns the sticky device status of ws (CASGD_OK or the
+ * highest-priority CASGD_ERR_* seen) and clears it. */
+int casgd_get_status(void* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CASGD_H */

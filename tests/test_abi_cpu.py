@@ -1,0 +1,104 @@
+"""The C-ABI library loads and exports every symbol include/casgd.h declares.
+
+No GPU here: only host-only entry points are called (messages, sizes) and argument
+checks that must reject a request before any CUDA call is made.
+"""
+import ctypes as C
+import subprocess
+
+import pytest
+
+import communication_avoiding_step_gb300 as casgd
+from communication_avoiding_step_gb300 import _native as nat
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return casgd.load()
+
+
+def test_every_header_symbol_is_exported(lib):
+    syms = nat.header_symbols()
+    assert len(syms) >= 12
+    out = subprocess.run(["nm", "-D", "--defined-only", nat.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for s in syms:
+        assert s in exported, s
+        assert hasattr(lib, s)
+    # and the binding declares a prototype for each of them
+    assert set(syms) == set(nat.SIGNATURES)
+
+
+def test_version_and_messages(lib):
+    assert lib.casgd_version() == 1
+    for code in range(8):
+        assert lib.casgd_strerror(code)
+    assert b"unknown" in lib.casgd_strerror(99)
+
+
+def test_gram_elems(lib):
+    assert lib.casgd_gram_elems(256, 32, 0) == 32 * 31 // 2 * 256 * 256
+    assert lib.casgd_gram_elems(256, 32, nat.FLAG_WRITE_DIAG_BLOCKS) == 32 * 33 // 2 * 256 * 256
+    assert lib.casgd_gram_elems(16, 1, 0) == 0
+    assert lib.casgd_gram_elems(0, 4, 0) == -1
+    assert lib.casgd_gram_elems(4096, 32, 0) == -1        # S over 65536
+    assert lib.casgd_gram_elems(1, 65, 0) == -1           # s over 64
+
+
+def test_workspace_size_host_only(lib):
+    d = nat.Data(1000, 2000, 2000, 0, 0)
+    p = nat.Params(256, 32, 0.5, 0, 0, 0, 0)
+    nbytes = C.c_size_t(0)
+    assert lib.casgd_workspace_size(C.byref(d), C.byref(p), C.byref(nbytes)) == 0
+    S = 256 * 32
+    g = 32 * 31 // 2 * 256 * 256 * 4
+    assert nbytes.value >= g + S * 2000 * 2 + S * 14
+    assert nbytes.value % 256 == 0
+    bad = nat.Params(256, 32, 0.5, 7, 0, 0, 0)
+    assert lib.casgd_workspace_size(C.byref(d), C.byref(bad), C.byref(nbytes)) == nat.CASGD_ERR_ARG
+
+
+def test_argument_errors_before_any_cuda_call(lib):
+    p = nat.Params(16, 4, 0.1, 0, 0, 0, 0)
+    fake = 1 << 20  # never dereferenced: every case fails validation first
+    cases = [
+        nat.Data(0, 64, 64, fake, fake),          # m = 0
+        nat.Data(100, 64, 60, fake, fake),        # ld < n
+        nat.Data(100, 64, 68, fake, fake),        # ld % 8 != 0
+        nat.Data(100, 64, 64, fake + 8, fake),    # X not 16-byte aligned
+        nat.Data(100, 20000, 20000, fake, fake),  # n over 16384
+        nat.Data(100, 64, 64, None, fake),        # null X
+    ]
+    for d in cases:
+        rc = lib.casgd_outer_step(C.byref(d), C.byref(p), C.c_void_p(fake), 0, C.c_void_p(fake),
+                                  1 << 30, None, None)
+        assert rc == nat.CASGD_ERR_ARG
+    good = nat.Data(100, 64, 64, fake, fake)
+    for bp in (nat.Params(0, 4, 0.1, 0, 0, 0, 0), nat.Params(16, 0, 0.1, 0, 0, 0, 0),
+               nat.Params(16, 65, 0.1, 0, 0, 0, 0), nat.Params(4096, 32, 0.1, 0, 0, 0, 0),
+               nat.Params(16, 4, 0.1, 3, 0, 0, 0), nat.Params(16, 4, float("nan"), 0, 0, 0, 0)):
+        rc = lib.casgd_outer_step(C.byref(good), C.byref(bp), C.c_void_p(fake), 0,
+                                  C.c_void_p(fake), 1 << 30, None, None)
+        assert rc == nat.CASGD_ERR_ARG
+    rc = lib.casgd_outer_step(C.byref(good), C.byref(p), None, 0, C.c_void_p(fake), 1 << 30,
+                              None, None)
+    assert rc == nat.CASGD_ERR_ARG
+    rc = lib.casgd_store_bf16(C.c_void_p(fake), 10, 9, 9, C.c_void_p(fake + 4), 16, None)
+    assert rc == nat.CASGD_ERR_ARG
+    rc = lib.casgd_sample_indices(0, 10, 0, 0, C.c_void_p(fake), None)
+    assert rc == nat.CASGD_ERR_ARG
+    assert lib.casgd_get_status(None, None) == nat.CASGD_ERR_WORKSPACE
+    assert lib.casgd_workspace_init(C.c_void_p(fake + 64), 4096, None) == nat.CASGD_ERR_WORKSPACE
+
+
+def test_product_path_has_no_oracle_dependency():
+    """The package and its build never import the oracle or the CPU reference."""
+    import os
+    import re
+    pkg = os.path.dirname(casgd.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(root, f)).read()
+                assert not re.search(r"\boracle\b", txt.replace("the oracle", "")), f

@@ -1,0 +1,234 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bars (the build's contract, from the method's stated tolerances):
+  * sampled row indices, BF16 storage: bit-exact;
+  * G within 1e-5 relative Frobenius of the oracle's emulating mode;
+  * BF16 margins r: equal, except rare one-ulp flips from a different FP32 summation
+    order (each within one BF16 ulp, at most 0.5% of entries);
+  * w after one outer iteration within 1e-4 relative L2 of the emulating mode, from
+    w = 0 and from a seeded non-zero w;
+  * loss kernel within 1e-5 relative of the oracle's FP64 loss on the same BF16 data;
+  * after a full run, the final loss (FP64 on the FP32 data) within 0.5% of FP64
+    plain minibatch SGD on the same rows.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth_inputs as si
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+GRAM_TOL = 1e-5
+W_TOL = 1e-4
+LOSS_TOL = 1e-5
+
+
+def _dev(p, casgd):
+    X32 = torch.from_numpy(p.X).cuda()
+    y = torch.from_numpy(p.y).cuda()
+    data = casgd.Dataset.from_fp32(X32, y)
+    del X32
+    return data
+
+
+def _run_step(casgd, data, params, w0, k=0, idx_in=None):
+    ws = casgd.workspace(data, params)
+    taps = casgd.Taps.alloc(params)
+    taps.idx_in = idx_in
+    w = torch.from_numpy(np.asarray(w0, dtype=np.float32).copy()).cuda()
+    casgd.outer_step(data, params, w, k, ws, taps)
+    st = casgd.get_status(ws)
+    return w.cpu().numpy(), taps, st
+
+
+def _rel(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300)
+
+
+def _bf16_ulp(v):
+    v = np.abs(np.asarray(v, np.float64))
+    e = np.floor(np.log2(np.maximum(v, 2.0**-126)))
+    return 2.0 ** (e - 7)
+
+
+# --------------------------------------------------------------- storage, a1 ----
+def test_store_bf16_bitexact(gpu_lib):
+    casgd = gpu_lib
+    rng = np.random.default_rng(0)
+    for m, n in ((1000, 37), (64, 8), (3, 1), (513, 130)):
+        X = (rng.standard_normal((m, n)) * 10.0 ** rng.integers(-30, 30, (m, n))).astype(np.float32)
+        X[0, 0] = np.float32(1.0 + 2.0**-8)  # a tie
+        out = casgd.store_bf16(torch.from_numpy(X).cuda())
+        got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        ld = (n + 7) // 8 * 8
+        assert got.shape == (m, ld)
+        want = oracle.bf16_round(X).view(np.uint32) >> 16
+        assert np.array_equal(got[:, :n].astype(np.uint32), want)
+        assert np.all(got[:, n:] == 0)
+
+
+def test_sample_indices_bitexact(gpu_lib):
+    casgd = gpu_lib
+    for m, count, seed, c0 in ((4096, 64, 0, 0), (400_000, 8192, 0, 49 * 8192),
+                               (2**31 - 1, 100_000, 2**64 - 1, 2**40 + 7), (1, 5, 3, 0),
+                               (11_000_000, 16384, 12345, 671 * 16384)):
+        got = casgd.sample_indices(m, count, seed, c0).cpu().numpy()
+        want = oracle.sample_indices(m, count, seed, c0)
+        assert np.array_equal(got, want), (m, count, seed, c0)
+
+
+# ------------------------------------------------------ one outer iteration ----
+CASES = [
+    # (name, problem factory, b, s, eta, loss)
+    ("recipe1", lambda: si.make_problem(1), None),
+    ("recipe2_m20000", lambda: si.make_problem(2, m=20000), None),
+    ("recipe3_m60000", lambda: si.make_problem(3, m=60000), None),
+    ("recipe4_m60000", lambda: si.make_problem(4, m=60000), None),
+    ("recipe5_m20000", lambda: si.make_problem(5, m=20000), None),
+    ("ragged_777x37_b24_s3", lambda: si.make_random(777, 37, si.LOGISTIC, seed=1), (24, 3, 0.3)),
+    ("ragged_500x5_b7_s5", lambda: si.make_random(500, 5, si.LSQ, seed=2), (7, 5, 0.05)),
+    ("ragged_3000x130_b100_s6", lambda: si.make_random(3000, 130, si.POISSON, seed=3),
+     (100, 6, 0.02)),
+    ("ragged_2000x200_b136_s1", lambda: si.make_random(2000, 200, si.LOGISTIC, seed=4),
+     (136, 1, 0.2)),
+]
+
+
+def _params(casgd, p, override, flags):
+    r = p.recipe
+    if override is None:
+        b, s, eta = r.b, r.s, r.eta
+    else:
+        b, s, eta = override
+    return casgd.Params(b, s, eta, p.recipe.loss, seed=0, flags=flags)
+
+
+@pytest.mark.parametrize("gram", ["simt", "tensor"])
+@pytest.mark.parametrize("name,factory,override", CASES, ids=[c[0] for c in CASES])
+def test_outer_step_parity(gpu_lib, name, factory, override, gram):
+    casgd = gpu_lib
+    p = factory()
+    flag = casgd.FLAG_GRAM_SIMT if gram == "simt" else casgd.FLAG_GRAM_TENSOR
+    params = _params(casgd, p, override, flag | casgd.FLAG_WRITE_DIAG_BLOCKS)
+    b, s = params.b, params.s
+    data = _dev(p, casgd)
+    for w0 in (np.zeros(p.n, np.float32), si.random_weights(p.n, seed=7, scale=0.5)):
+        try:
+            w_gpu, taps, st = _run_step(casgd, data, params, w0, k=3)
+        except casgd.CasgdError as e:
+            if gram == "tensor" and e.code == 7:
+                pytest.skip("tensor-core Gram does not take this shape")
+            raise
+        assert st == 0
+        ref = oracle.outer_step(p.X, p.y, w0, b, s, params.eta, p.recipe.loss, 0, 3,
+                                mode="emulate", return_parts=True)
+        # a1: indices bit-exact
+        assert np.array_equal(taps.idx_out.cpu().numpy(), ref["idx"])
+        # a4: margins
+        r_gpu = (taps.r_out.cpu().numpy().view(np.uint16).astype(np.uint32) << 16).view(np.float32)
+        diff = r_gpu != ref["r"]
+        assert diff.mean() <= 0.005
+        assert np.all(np.abs(r_gpu - ref["r"]) <= _bf16_ulp(ref["r"]) + 1e-38)
+        # a3: Gram, every block the kernel wrote (diagonal included)
+        G_gpu = taps.G_out.cpu().numpy()
+        if G_gpu.size <= 40_000_000:
+            G_ref = oracle.gram_packed(ref["Y"], b, s, diag=True, mode="emulate")
+            assert _rel(G_gpu, G_ref) <= GRAM_TOL
+        else:  # sampled blocks: first, last, and a few in between
+            rng = np.random.default_rng(0)
+            blocks = {(s - 1, 0), (s - 1, s - 1), (1, 0), (0, 0)}
+            for _ in range(6):
+                j = int(rng.integers(0, s))
+                blocks.add((j, int(rng.integers(0, j + 1))))
+            num = den = 0.0
+            for j, t in sorted(blocks):
+                o = oracle.packed_block_offset(j, t, b, True)
+                g_ref = oracle.gram_block(ref["Y"], b, j, t, "emulate").reshape(-1)
+                num += float(np.sum((G_gpu[o:o + b * b].astype(np.float64) - g_ref) ** 2))
+                den += float(np.sum(g_ref.astype(np.float64) ** 2))
+            assert math.sqrt(num / den) <= GRAM_TOL
+        # a6: alpha (diagnostic bound, looser than w because r may flip one ulp)
+        assert _rel(taps.alpha_out.cpu().numpy(), ref["alpha"]) <= 2e-3
+        # a8: the weights
+        assert _rel(w_gpu, ref["w"]) <= W_TOL
+
+
+def test_outer_step_given_indices_and_bad_index(gpu_lib):
+    casgd = gpu_lib
+    p = si.make_problem(1)
+    params = casgd.Params(16, 4, 0.1, si.LOGISTIC)
+    data = _dev(p, casgd)
+    idx = np.arange(64, dtype=np.int32) * 7 % p.m
+    w0 = si.random_weights(p.n, seed=3)
+    w_gpu, taps, st = _run_step(casgd, data, params, w0, idx_in=torch.from_numpy(idx).cuda())
+    assert st == 0
+    ref = oracle.outer_step(p.X, p.y, w0, 16, 4, 0.1, si.LOGISTIC, 0, 0, idx=idx)
+    assert _rel(w_gpu, ref) <= W_TOL
+    bad = idx.copy()
+    bad[5] = p.m          # one past the end
+    bad[9] = -1
+    _, _, st = _run_step(casgd, data, params, w0, idx_in=torch.from_numpy(bad).cuda())
+    assert st == 6        # CASGD_ERR_BAD_INDEX
+
+
+def test_deterministic(gpu_lib):
+    casgd = gpu_lib
+    p = si.make_problem(5, m=30000)
+    r = p.recipe
+    data = _dev(p, casgd)
+    params = casgd.Params(r.b, r.s, r.eta, r.loss)
+    outs = []
+    for _ in range(2):
+        ws = casgd.workspace(data, params)
+        w = torch.zeros(p.n, device="cuda")
+        casgd.train(data, params, w, 3, ws)
+        outs.append(w.cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
+
+
+# ---------------------------------------------------------------------- loss ----
+@pytest.mark.parametrize("kind,m,n", [(si.LOGISTIC, 10_001, 64), (si.LSQ, 5000, 28),
+                                      (si.POISSON, 3001, 512), (si.LOGISTIC, 777, 2000),
+                                      (si.LSQ, 1, 3)])
+def test_loss_kernel_parity(gpu_lib, kind, m, n):
+    casgd = gpu_lib
+    p = si.make_random(m, n, kind, seed=11)
+    data = _dev(p, casgd)
+    params = casgd.Params(1, 1, 0.1, kind)
+    ws = casgd.workspace(data, params)
+    for w in (np.zeros(n, np.float32), si.random_weights(n, seed=2, scale=1.0)):
+        got = casgd.loss(data, kind, torch.from_numpy(w).cuda(), ws)
+        want = oracle.full_loss(oracle.bf16_round(p.X), p.y, w, kind)
+        assert abs(got - want) <= LOSS_TOL * abs(want)
+
+
+# ------------------------------------------------------------ full training ----
+@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
+def test_final_loss_within_half_percent_of_fp64_sgd(gpu_lib, cid):
+    casgd = gpu_lib
+    p = si.make_problem(cid)
+    r = p.recipe
+    iters = r.outer_iters()
+    data = _dev(p, casgd)
+    params = casgd.Params(r.b, r.s, r.eta, r.loss)
+    ws = casgd.workspace(data, params)
+    w = torch.zeros(p.n, device="cuda")
+    hist, launches, _ = casgd.train(data, params, w, iters, ws, loss_every=iters)
+    assert len(hist) == 1
+    assert launches >= 4 * iters
+    w_gpu = w.cpu().numpy()
+    assert np.all(np.isfinite(w_gpu))
+    f_gpu = oracle.full_loss(p.X, p.y, w_gpu, r.loss)
+    w_sgd = oracle.plain_sgd(p.X, p.y, r.b, iters * r.s, r.eta, r.loss, 0, mode="fp64")
+    f_ref = oracle.full_loss(p.X, p.y, w_sgd, r.loss)
+    assert abs(f_gpu - f_ref) / f_ref < 0.005
+    # the device loss kernel agrees with the oracle on the BF16 data at the final w
+    assert abs(hist[-1] - oracle.full_loss(oracle.bf16_round(p.X), p.y, w_gpu, r.loss)) \
+        <= LOSS_TOL * abs(hist[-1])
