@@ -256,6 +256,10 @@ def run_ours(args):
     n_ev = iters * casgd.STAGE_EVENTS
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
               for _ in range(args.steps)]
+    for row in events:        # torch creates the CUDA event lazily, on first record
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     if dist:

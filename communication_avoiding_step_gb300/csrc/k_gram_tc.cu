@@ -1,14 +1,456 @@
-// Step a3 on tcgen05 tensor cores (sm_103a): not built yet in this revision; the
-// CUDA-core kernel serves every shape meanwhile.
+// Step a3 on the 5th-generation tensor cores of sm_103a: G_{j,t} = Y_j Y_t^T with BF16
+// operands and FP32 accumulation in tensor memory (TMEM).
+//
+// Paper: Mixed-Precision Communication-Avoiding SGD for Generalized Linear Models on
+// GPUs (abstract): matrix hardware with low-precision formats accelerates the Gram
+// GEMM, formed from low-precision inputs with high-precision accumulation.  Only the
+// blocks the inner recurrence reads (t < j), plus the diagonal on request, are formed.
+//
+// Design (persistent, one CTA per SM, 6 warps):
+//   warp 0      TMA producer: 128x64 (A) and 256x64 (B) BF16 tiles of Y, 128-byte
+//               swizzled, into a 4-stage shared-memory ring (48 KB per stage);
+//   warp 1      allocates 512 TMEM columns (two 128x256 FP32 accumulators) and one
+//               elected lane issues tcgen05.mma (M=128, N=256, K=16) per 16 columns of
+//               K, committing each stage back to the producer and each finished tile
+//               to the epilogue;
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one row per thread), masked
+//               stores of the rows/columns that belong to needed blocks into the packed
+//               block-lower G.  Two accumulators let the epilogue of one tile overlap
+//               the MMAs of the next.
+// Both operands are K-major slices of the same Y (rows are samples, K the features);
+// out-of-range rows and columns of K are zero-filled by TMA.  Tiles of the S x S
+// product are visited row-tile by row-tile, skipping tiles wholly above the needed
+// blocks.  Every wait is bounded: on timeout the kernel records ST_TIMEOUT, stops
+// issuing work, waits (bounded) for its own copies and MMAs in flight, frees TMEM and
+// returns.
+#include <cuda.h>
+
 #include "casgd_internal.cuh"
 
 namespace casgd {
 
-bool gram_tc_supported(int64_t, int64_t, int) { return false; }
+namespace {
 
-cudaError_t launch_gram_tc(const uint16_t*, int64_t, int64_t, int64_t, int, int, bool, float*,
-                           Ctrl*, uint32_t, Ctx&) {
-  return cudaErrorNotSupported;
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;  // 16 KB
+constexpr int kBBytes = BN * BK * 2;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kTmemCols = 512;
+constexpr int kThreads = 192;
+constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*align*/;
+
+struct TcArgs {
+  float* G;
+  Ctrl* ctrl;
+  int64_t S;
+  int n, b, nkb;
+  int TR, TC, ntiles;
+  bool diag;
+  uint64_t timeout_ns;
+};
+
+struct SharedCtl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile uint32_t abort;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: false (and the CTA's abort word set) if the phase does not complete in
+// time or another role of this CTA already gave up.
+__device__ bool mbar_wait(uint64_t* bar, uint32_t parity, SharedCtl* sc, const TcArgs& a) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (sc->abort) return false;
+    if (globaltimer_ns() - t0 > a.timeout_ns) {
+      sc->abort = 1;
+      atomicOr(&a.ctrl->status, ST_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, rows of 128 bytes, 128-byte swizzle,
+// 8-row groups 1024 bytes apart (the layout a 64-column BF16 TMA box with 128-byte
+// swizzle produces).  Bits: start>>4 [0,14), LBO>>4 [16,30), SBO>>4 [32,46), fixed
+// 0b001 [46,49), swizzle mode [61,64) = 2 (128-byte).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D FP32 (bits 4-5 = 1), A and B BF16 (bits 7-9 and
+// 10-12 = 1), both K-major (bits 15, 16 = 0), N>>3 at bits 17-22, M>>4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+        "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+        "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+        "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Number of needed column tiles in row tile `ra` (columns [0, count*BN) hold every
+// entry of a needed block in those rows).
+__device__ __forceinline__ int cols_needed(const TcArgs& a, int ra) {
+  int64_t last = (int64_t)ra * BM + BM - 1;
+  if (last > a.S - 1) last = a.S - 1;
+  const int64_t jmax = last / a.b;
+  const int64_t lim = (int64_t)a.b * (a.diag ? jmax + 1 : jmax);  // columns < lim needed
+  int64_t c = (lim + BN - 1) / BN;
+  return (int)(c < a.TC ? c : a.TC);
+}
+
+// Walks the linear tile index forward (tiles are visited in increasing order).
+struct TileCursor {
+  int ra = 0;
+  int base = 0;   // linear index of the first tile of row tile ra
+  int cnt = -1;   // tiles in row tile ra
+  __device__ void seek(const TcArgs& a, int tile, int& rr, int& cc) {
+    if (cnt < 0) cnt = cols_needed(a, 0);
+    while (tile >= base + cnt) {
+      base += cnt;
+      ++ra;
+      cnt = cols_needed(a, ra);
+    }
+    rr = ra;
+    cc = tile - base;
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gram_tc_kernel(const __grid_constant__ CUtensorMap tmY, TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  SharedCtl* sc = reinterpret_cast<SharedCtl*>(smem + (size_t)kStages * kStageBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sc->full[i], 1);
+      mbar_init(&sc->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sc->tfull[i], 1);
+      mbar_init(&sc->tempty[i], 4);
+    }
+    mbar_init(&sc->drain, 1);
+    sc->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sc->tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sc->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      TileCursor cur;
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;  // bit st: a load into stage st was issued; its parity below
+      uint32_t last_par = 0;
+      for (int tile = blockIdx.x; tile < a.ntiles && !sc->abort; tile += gridDim.x) {
+        int ra, ca;
+        cur.seek(a, tile, ra, ca);
+        for (int kb = 0; kb < a.nkb; ++kb) {
+          if (!mbar_wait(&sc->empty[stage], phase ^ 1u, sc, a)) break;
+          uint8_t* sa = smem + (size_t)stage * kStageBytes;
+          uint8_t* sb = sa + kABytes;
+          mbar_expect_tx(&sc->full[stage], kStageBytes);
+          tma_load_2d(smem_u32(sa), &tmY, &sc->full[stage], kb * BK, ra * BM);
+          tma_load_2d(smem_u32(sb), &tmY, &sc->full[stage], kb * BK, ca * BN);
+          tma_load_2d(smem_u32(sb + kBBytes / 2), &tmY, &sc->full[stage], kb * BK,
+                      ca * BN + BN / 2);
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: every issued copy has landed before the CTA may exit.
+      for (int st = 0; st < kStages; ++st)
+        if (issued & (1u << st)) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&sc->full[st], (last_par >> st) & 1u) &&
+                 globaltimer_ns() - t0 < a.timeout_ns) {
+          }
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t tphase[2] = {0, 0};
+      int iter = 0;
+      bool any = false;
+      for (int tile = blockIdx.x; tile < a.ntiles && !sc->abort; tile += gridDim.x, ++iter) {
+        const int acc = iter & 1;
+        if (!mbar_wait(&sc->tempty[acc], tphase[acc] ^ 1u, sc, a)) break;
+        tphase[acc] ^= 1u;
+        tc_fence_after();
+        const uint32_t tacc = tmem + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < a.nkb; ++kb) {
+          if (!mbar_wait(&sc->full[stage], phase, sc, a)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+          const uint64_t ad = sdesc_sw128(sa), bd = sdesc_sw128(sb);
+          const int krem = a.n - kb * BK;
+          const int ksteps = krem >= BK ? BK / 16 : (krem + 15) / 16;
+          for (int kk = 0; kk < ksteps; ++kk)
+            mma_bf16(tacc, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
+                     (kb > 0 || kk > 0) ? 1u : 0u);
+          any = true;
+          mma_commit(&sc->empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&sc->tfull[acc]);
+      }
+      if (any) {  // drain: all MMAs of this CTA complete before TMEM is freed
+        mma_commit(&sc->drain);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&sc->drain, 0) && globaltimer_ns() - t0 < a.timeout_ns) {
+        }
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    TileCursor cur;
+    uint32_t tphase[2] = {0, 0};
+    int iter = 0;
+    const bool vec_ok = (a.b % 4) == 0;
+    for (int tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++iter) {
+      int ra, ca;
+      cur.seek(a, tile, ra, ca);
+      const int acc = iter & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&sc->tfull[acc], tphase[acc], sc, a) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tphase[acc] ^= 1u;
+      tc_fence_after();
+      const int64_t p = (int64_t)ra * BM + quarter * 32 + lane;
+      const bool prow = p < a.S;
+      const int64_t jb = prow ? p / a.b : 0;
+      const int64_t ib = p - jb * a.b;
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t v[32];
+        __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
+        const int64_t q0 = (int64_t)ca * BN + ch * 32;
+        if (!prow || q0 >= a.S) continue;
+        const int64_t t0b = q0 / a.b;
+        const int64_t q1 = q0 + 31;
+        const int64_t t1b = q1 / a.b;
+        const bool whole = (q1 < a.S) && (t0b == t1b) && (t0b < jb || (a.diag && t0b == jb));
+        if (whole && vec_ok && ((q0 - t0b * a.b) % 4) == 0) {
+          float* dst = a.G + packed_offset(jb, t0b, a.b, a.diag) + ib * a.b + (q0 - t0b * a.b);
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + e) =
+                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                            __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int64_t q = q0 + e;
+            if (q >= a.S) break;
+            const int64_t tb = q / a.b;
+            if (tb < jb || (a.diag && tb == jb))
+              a.G[packed_offset(jb, tb, a.b, a.diag) + ib * a.b + (q - tb * a.b)] =
+                  __uint_as_float(v[e]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sc->tempty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+  if (threadIdx.x == 0 && sc->abort) atomicExch(&a.ctrl->abort, 1u);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+bool gram_tc_supported(int64_t S, int64_t n, int b) {
+  return S >= 1 && n >= 1 && b >= 1 && S <= kMaxSB && n <= kMaxN;
+}
+
+cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b, int s,
+                           bool diag, float* G, Ctrl* ctrl, uint32_t timeout_us, Ctx& c) {
+  (void)s;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap map;
+  const cuuint64_t gdim[2] = {(cuuint64_t)n, (cuuint64_t)S};
+  const cuuint64_t gstride[1] = {(cuuint64_t)ldY * 2};
+  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t estride[2] = {1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(Y), gdim, gstride,
+          box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+
+  TcArgs a;
+  a.G = G;
+  a.ctrl = ctrl;
+  a.S = S;
+  a.n = (int)n;
+  a.b = b;
+  a.nkb = (int)((n + BK - 1) / BK);
+  a.TR = (int)((S + BM - 1) / BM);
+  a.TC = (int)((S + BN - 1) / BN);
+  a.diag = diag;
+  a.timeout_ns = (uint64_t)(timeout_us ? timeout_us : 1000000u) * 1000ull;
+  // count the needed tiles on the host with the same rule the kernel walks
+  int64_t total = 0;
+  for (int ra = 0; ra < a.TR; ++ra) {
+    int64_t last = (int64_t)ra * BM + BM - 1;
+    if (last > S - 1) last = S - 1;
+    const int64_t jmax = last / b;
+    const int64_t lim = (int64_t)b * (diag ? jmax + 1 : jmax);
+    int64_t cc = (lim + BN - 1) / BN;
+    total += cc < a.TC ? cc : a.TC;
+  }
+  a.ntiles = (int)total;
+  if (a.ntiles == 0) return cudaSuccess;
+
+  cudaError_t e = cudaFuncSetAttribute(gram_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = a.ntiles < c.num_sms ? a.ntiles : c.num_sms;
+  gram_tc_kernel<<<grid, kThreads, kSmemBytes, c.stream>>>(map, a);
+  ++c.launches;
+  return cudaGetLastError();
 }
 
 }  // namespace casgd
