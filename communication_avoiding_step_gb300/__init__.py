@@ -188,3 +188,20 @@ def loss_async(data: Dataset, kind: int, w: torch.Tensor, ws: torch.Tensor,
 def get_status(ws: torch.Tensor, stream=None) -> int:
     """Sticky device status of ws (0 = ok); clears it.  Blocks."""
     return int(load().casgd_get_status(_ptr(ws), _stream(stream)))
+
+
+def update_static(Y: torch.Tensor, alpha: torch.Tensor, w: torch.Tensor, n: int,
+                  stream=None) -> None:
+    """w += Y^T alpha without a workspace and without allocating device memory.
+
+    For callers that cannot allocate where they apply an update; the scratch is a
+    fixed array inside the library (see casgd_update_static in include/casgd.h for the
+    size limit and the rule that overlapping calls must be serialised).  Y is the BF16
+    S x ldY matrix of the gathered rows, alpha FP32[S], w FP32[n] updated in place.
+    """
+    _need_cuda(Y, "Y", torch.bfloat16)
+    _need_cuda(alpha, "alpha", torch.float32)
+    _need_cuda(w, "w", torch.float32)
+    S, ldY = int(Y.shape[0]), int(Y.shape[1])
+    _check(load().casgd_update_static(_ptr(Y), S, int(n), ldY, _ptr(alpha), _ptr(w),
+                                      _stream(stream)), "casgd_update_static")

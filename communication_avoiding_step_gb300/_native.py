@@ -12,7 +12,7 @@ HEADER = os.path.join(ROOT, "include", "casgd.h")
 
 CASGD_LOGISTIC, CASGD_LSQ, CASGD_POISSON = 0, 1, 2
 (CASGD_OK, CASGD_ERR_ARG, CASGD_ERR_WORKSPACE, CASGD_ERR_CUDA, CASGD_ERR_NONFINITE,
- CASGD_ERR_TIMEOUT, CASGD_ERR_BAD_INDEX, CASGD_ERR_UNSUPPORTED) = range(8)
+ CASGD_ERR_TIMEOUT, CASGD_ERR_BAD_INDEX, CASGD_ERR_UNSUPPORTED, CASGD_ERR_SCRATCH_LIMIT) = range(9)
 FLAG_WRITE_DIAG_BLOCKS = 0x1
 FLAG_GRAM_TENSOR = 0x2
 FLAG_GRAM_SIMT = 0x4
@@ -61,6 +61,8 @@ SIGNATURES = {
     "casgd_loss_async": (C.c_int, [_P(Data), C.c_int32, C.c_void_p, C.c_void_p, C.c_size_t,
                                    C.c_void_p, C.c_void_p]),
     "casgd_get_status": (C.c_int, [C.c_void_p, C.c_void_p]),
+    "casgd_update_static": (C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_int64, C.c_void_p,
+                                      C.c_void_p, C.c_void_p]),
 }
 
 _lib = None

@@ -215,6 +215,7 @@ const char* casgd_strerror(int code) {
     case CASGD_ERR_TIMEOUT: return "an inter-CTA wait on the device exceeded its time bound";
     case CASGD_ERR_BAD_INDEX: return "a given row index is outside [0, m)";
     case CASGD_ERR_UNSUPPORTED: return "request not supported by this build";
+    case CASGD_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of casgd_update_static";
     default: return "unknown casgd status";
   }
 }

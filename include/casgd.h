@@ -59,7 +59,8 @@ enum {
   CASGD_ERR_NONFINITE = 4,    /* device: the update produced a NaN or Inf weight  */
   CASGD_ERR_TIMEOUT = 5,      /* device: an inter-CTA wait ran past its bound     */
   CASGD_ERR_BAD_INDEX = 6,    /* device: a caller-given row index outside [0, m)  */
-  CASGD_ERR_UNSUPPORTED = 7   /* valid request this build does not support        */
+  CASGD_ERR_UNSUPPORTED = 7,  /* valid request this build does not support        */
+  CASGD_ERR_SCRATCH_LIMIT = 8 /* too large for casgd_update_static's fixed scratch  */
 };
 
 /* casgd_params_t.flags */
@@ -176,6 +177,24 @@ int casgd_loss(const casgd_data_t* data, int32_t loss, const float* w, void* ws,
 /* Same as casgd_loss but asynchronous: the FP64 result goes to device *out_dev. */
 int casgd_loss_async(const casgd_data_t* data, int32_t loss, const float* w, void* ws,
                      size_t ws_bytes, void* stream, double* out_dev);
+
+/* Weight update w += Y^T alpha (step a8) that allocates nothing and takes no
+ * workspace.  The paper has no counterpart: this exists for callers that cannot
+ * allocate device memory where they apply an update (inside another framework's
+ * memory pool that forbids raw cudaMalloc, in loops that must not block on an
+ * allocator, or when they only own their input and output buffers).
+ *   Y      device BF16 bits, S x ldY row-major (ldY % 8 == 0, ldY >= n), 16-byte aligned
+ *   alpha  device FP32[S];  w  device FP32[n], updated in place
+ * Its scratch is a fixed array inside the library (4 MiB of partial sums plus a
+ * 512-byte control block) that every GPU loading the library holds until exit.  It
+ * fits P * ldY <= 1,048,576 floats with P = min(ceil(S/32), 320) (e.g. n <= 3272
+ * at P = 320); larger requests return CASGD_ERR_SCRATCH_LIMIT and run nothing.
+ * The first call on each device looks up the array's device address (make that
+ * first call before any stream capture).  Every call shares the array: calls whose
+ * work overlaps on the GPU (e.g. on two streams) race and must be serialised by the
+ * caller.  Non-finite results are not reported here (inspect w).  Asynchronous. */
+int casgd_update_static(const void* Y, int64_t S, int64_t n, int64_t ldY,
+                        const float* alpha, float* w, void* stream);
 
 /* Blocks on `stream`, returns the sticky device status of ws (CASGD_OK or the
  * highest-priority CASGD_ERR_* seen) and clears it. */
