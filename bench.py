@@ -162,6 +162,17 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def world_max(value: float, device) -> float:
+    """Max of a per-rank value over the process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # --------------------------------------------------------------------- CPU side ----
 def cpu_sample(cfg, s, budget_s=15.0, max_iters=8):
     """Times the oracle's emulating-mode outer iteration on this host (bounded sample)."""
@@ -276,11 +287,7 @@ def run_ours(args):
         torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    elapsed = start.elapsed_time(end) / 1e3
-    if dist:
-        t = torch.tensor([elapsed], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = world_max(start.elapsed_time(end) / 1e3, torch.device("cuda", local))
     stage_ms = {st: 0.0 for st in STAGES}
     for i in range(args.steps):
         ev = events[i]
@@ -347,11 +354,7 @@ def run_ours(args):
             k += iters
         t1.record(stream)
         torch.cuda.synchronize()
-        e_el = t0.elapsed_time(t1) / 1e3
-        if dist:
-            t = torch.tensor([e_el], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_el = float(t.item())
+        e_el = world_max(t0.elapsed_time(t1) / 1e3, torch.device("cuda", local))
         e2e = {"value": S * iters * e_steps * world / e_el, "unit": "samples/s",
                "h2d_bytes_per_step": Xh.numel() * 2 + yh.numel() * 4 + wh.numel() * 4,
                "d2h_bytes_per_step": w_out.numel() * 4 + 8, "steps": e_steps}
