@@ -25,6 +25,8 @@ struct Resolved {
   uint16_t* r;
   float* yY;
   float* alpha;
+  float* far;
+  uint32_t* far_done;
   uint16_t* Y;
   float* G;
   float* upd;
@@ -67,6 +69,8 @@ Resolved resolve(void* ws, const Layout& L) {
   R.r = reinterpret_cast<uint16_t*>(base + L.off_r);
   R.yY = reinterpret_cast<float*>(base + L.off_yY);
   R.alpha = reinterpret_cast<float*>(base + L.off_alpha);
+  R.far = reinterpret_cast<float*>(base + L.off_far);
+  R.far_done = reinterpret_cast<uint32_t*>(base + L.off_far + align_up((size_t)L.S * sizeof(float)));
   R.Y = reinterpret_cast<uint16_t*>(base + L.off_Y);
   R.G = reinterpret_cast<float*>(base + L.off_G);
   R.upd = reinterpret_cast<float*>(base + L.off_upd);
@@ -124,17 +128,18 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   if (prof) prof->gram_kind = choice;
 
   if ((rc = record(prof, it, 0, st)) != CASGD_OK) return rc;
-  CK(launch_gather(*d, *p, w, k, idx_in, R.idx, R.Y, L.ldY, R.r, R.yY, R.ctrl, c));
+  CK(launch_gather(*d, *p, w, k, idx_in, R.idx, R.Y, L.ldY, R.r, R.yY, R.ctrl, R.far_done, c));
   if ((rc = record(prof, it, 1, st)) != CASGD_OK) return rc;
   if (choice == 1) {
-    CK(launch_gram_tc(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag, G, R.ctrl, p->timeout_us, c));
+    CK(launch_gram_tc(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag,
+                      (p->flags & CASGD_FLAG_GRAM_NO_CLUSTER) != 0, G, R.ctrl, p->timeout_us, c));
   } else {
     CK(launch_gram_simt(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag, G, c));
   }
   // (The sum of G over processes would sit here; on one GPU it is the identity.)
   if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
-  CK(launch_recur(G, R.r, R.yY, R.alpha, p->b, p->s, p->eta, p->loss, p->flags,
-                  p->timeout_us, R.ctrl, c));
+  CK(launch_recur(G, R.r, R.yY, R.alpha, R.far, R.far_done, p->b, p->s, p->eta, p->loss,
+                  p->flags, p->timeout_us, R.ctrl, c));
   if ((rc = record(prof, it, 3, st)) != CASGD_OK) return rc;
   CK(launch_update(R.Y, R.alpha, L.S, d->n, L.ldY, w, R.upd, L.upd_ctas, R.ctrl, c));
   if ((rc = record(prof, it, 4, st)) != CASGD_OK) return rc;
@@ -189,6 +194,9 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms)
   off += align_up((size_t)L.S * sizeof(float));
   L.off_alpha = off;
   off += align_up((size_t)L.S * sizeof(float));
+  L.off_far = off;  // far-field sums FP32[S]; kMaxS completion counters; kMaxS x 4 trace
+  off += align_up((size_t)L.S * sizeof(float)) +
+         align_up(kMaxS * sizeof(uint32_t) + kMaxS * 4 * sizeof(uint64_t));
   L.off_Y = off;
   off += align_up((size_t)L.S * L.ldY * sizeof(uint16_t));
   L.off_upd = off;

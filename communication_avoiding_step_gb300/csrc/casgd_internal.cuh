@@ -5,7 +5,7 @@
 //   k_prep.cu       a1 sampling, a2 gather into Y, a4 BF16 margins; BF16 storage
 //   k_gram_simt.cu  a3 Gram on CUDA cores (any n; used for narrow n)
 //   k_gram_tc.cu    a3 Gram on tcgen05 tensor cores with TMEM accumulators and TMA
-//   k_recur.cu      a6/a7 inner recurrence, persistent, flag-synchronised
+//   k_recur.cu      a6/a7 inner recurrence: persistent chain + bulk CTAs, flag-synchronised
 //   k_update.cu     a8 weight update, a9 full-data loss
 #pragma once
 
@@ -32,12 +32,15 @@ constexpr int kLossCtas = 1024;     // upper bound on loss-kernel CTAs (partials
 // Control block at the start of the workspace (256 bytes, zeroed per step where noted).
 struct Ctrl {
   uint32_t status;        // sticky ST_* bits (cleared by casgd_get_status)
-  uint32_t abort;         // set by a waiter that timed out; others stop waiting
+  uint32_t abort;         // set by a waiter that timed out; others stop waiting.  The
+                          // gather kernel re-arms it each step only while no timeout is
+                          // recorded in `status`, so later steps fail fast.
   uint32_t next_unit;     // recurrence work queue (zeroed by the gather kernel)
   uint32_t loss_done;     // loss kernel: CTAs finished (zeroed by the loss kernel's last CTA)
-  uint32_t upd_done;      // update kernel: CTAs finished
-  uint32_t pad0[3];
-  uint32_t block_done[kMaxS];  // recurrence: units finished per block (zeroed per step)
+  uint32_t upd_done;      // (unused)
+  uint32_t diag;          // which wait timed out last: kind << 24 | block << 12 | value seen
+  uint32_t pad0[2];
+  uint32_t block_done[kMaxS];  // recurrence: chain CTAs done per phase (zeroed per step)
 };
 static_assert(sizeof(Ctrl) <= 512, "control block");
 
@@ -45,7 +48,7 @@ static_assert(sizeof(Ctrl) <= 512, "control block");
 struct Layout {
   int64_t S, ldY, gram_elems;
   int upd_ctas;
-  size_t off_idx, off_r, off_yY, off_alpha, off_Y, off_G, off_upd, off_loss, total;
+  size_t off_idx, off_r, off_yY, off_alpha, off_far, off_Y, off_G, off_upd, off_loss, total;
 };
 
 Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms);
@@ -126,16 +129,17 @@ cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t coun
                           int32_t* idx, Ctx& c);
 cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const float* w,
                           uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
-                          int64_t ldY, uint16_t* r, float* yY, Ctrl* ctrl, Ctx& c);
+                          int64_t ldY, uint16_t* r, float* yY, Ctrl* ctrl,
+                          uint32_t* far_done, Ctx& c);
 cudaError_t launch_gram_simt(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
                              int s, bool diag, float* G, Ctx& c);
 bool gram_tc_supported(int64_t S, int64_t n, int b);
 cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
-                           int s, bool diag, float* G, Ctrl* ctrl, uint32_t timeout_us,
-                           Ctx& c);
+                           int s, bool diag, bool no_cluster, float* G, Ctrl* ctrl,
+                           uint32_t timeout_us, Ctx& c);
 cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, float* alpha,
-                         int b, int s, float eta, int loss, uint32_t flags,
-                         uint32_t timeout_us, Ctrl* ctrl, Ctx& c);
+                         float* far, uint32_t* far_done, int b, int s, float eta, int loss,
+                         uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, Ctx& c);
 cudaError_t launch_update(const uint16_t* Y, const float* alpha, int64_t S, int64_t n,
                           int64_t ldY, float* w, float* part, int upd_ctas, Ctrl* ctrl,
                           Ctx& c);

@@ -17,6 +17,11 @@
 //               stores of the rows/columns that belong to needed blocks into the packed
 //               block-lower G.  Two accumulators let the epilogue of one tile overlap
 //               the MMAs of the next.
+// Cluster variant (kCl = 2, the default): the two CTAs of a cluster compute row tiles
+// 2g and 2g+1 against the same B tile; each loads one 128-row half of B and multicasts
+// it to both, so a CTA pulls 32 KB instead of 48 KB from L2 per 64 columns of K.  A
+// stage is refilled only after both CTAs' MMAs have read it (each MMA warp's commit
+// arrives on the stage's empty barrier in both CTAs).
 // Both operands are K-major slices of the same Y (rows are samples, K the features);
 // out-of-range rows and columns of K are zero-filled by TMA.  Tiles of the S x S
 // product are visited row-tile by row-tile, skipping tiles wholly above the needed
@@ -114,6 +119,28 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// The same copy written to the same offset in every CTA of `mask` (this GPU's memory).
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map,
+                                               uint64_t* bar, int32_t x, int32_t y,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
 // Shared-memory matrix descriptor: K-major operand, rows of 128 bytes, 128-byte swizzle,
 // 8-row groups 1024 bytes apart (the layout a 64-column BF16 TMA box with 128-byte
 // swizzle produces).  Bits: start>>4 [0,14), LBO>>4 [16,30), SBO>>4 [32,46), fixed
@@ -150,6 +177,16 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
+// Arrives on the barrier at the same offset in every CTA of `mask` once this thread's
+// earlier MMAs have completed.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -183,23 +220,34 @@ __device__ __forceinline__ int cols_needed(const TcArgs& a, int ra) {
   return (int)(c < a.TC ? c : a.TC);
 }
 
+// Column tiles of row group g (row tiles kCl*g .. kCl*g+kCl-1): those of its last row
+// tile, which needs the most (the count grows with the row).
+template <int kCl>
+__device__ __forceinline__ int group_cols(const TcArgs& a, int g) {
+  int last = kCl * g + kCl - 1;
+  if (last > a.TR - 1) last = a.TR - 1;
+  return cols_needed(a, last);
+}
+
 // Walks the linear tile index forward (tiles are visited in increasing order).
+template <int kCl>
 struct TileCursor {
-  int ra = 0;
-  int base = 0;   // linear index of the first tile of row tile ra
-  int cnt = -1;   // tiles in row tile ra
-  __device__ void seek(const TcArgs& a, int tile, int& rr, int& cc) {
-    if (cnt < 0) cnt = cols_needed(a, 0);
+  int g = 0;
+  int base = 0;   // linear index of the first tile of row group g
+  int cnt = -1;   // tiles in row group g
+  __device__ void seek(const TcArgs& a, int tile, int& rg, int& cc) {
+    if (cnt < 0) cnt = group_cols<kCl>(a, 0);
     while (tile >= base + cnt) {
       base += cnt;
-      ++ra;
-      cnt = cols_needed(a, ra);
+      ++g;
+      cnt = group_cols<kCl>(a, g);
     }
-    rr = ra;
+    rg = g;
     cc = tile - base;
   }
 };
 
+template <int kCl>
 __global__ void __launch_bounds__(kThreads, 1)
     gram_tc_kernel(const __grid_constant__ CUtensorMap tmY, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -207,11 +255,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~(uintptr_t)1023);
   SharedCtl* sc = reinterpret_cast<SharedCtl*>(smem + (size_t)kStages * kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = kCl == 2 ? (int)cluster_rank() : 0;
+  const int cid = blockIdx.x / kCl, ncl = gridDim.x / kCl;  // cluster id, clusters
+  constexpr uint16_t kMask = (uint16_t)((1u << kCl) - 1u);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sc->full[i], 1);
-      mbar_init(&sc->empty[i], 1);
+      mbar_init(&sc->empty[i], kCl);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sc->tfull[i], 1);
@@ -230,29 +281,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (kCl > 1) cluster_sync();  // peers' barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem = sc->tmem_base;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
-      TileCursor cur;
+      TileCursor<kCl> cur;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;  // bit st: a load into stage st was issued; its parity below
       uint32_t last_par = 0;
-      for (int tile = blockIdx.x; tile < a.ntiles && !sc->abort; tile += gridDim.x) {
-        int ra, ca;
-        cur.seek(a, tile, ra, ca);
+      for (int tile = cid; tile < a.ntiles && !sc->abort; tile += ncl) {
+        int rg, ca;
+        cur.seek(a, tile, rg, ca);
+        const int ra = kCl * rg + rank;
         for (int kb = 0; kb < a.nkb; ++kb) {
           if (!mbar_wait(&sc->empty[stage], phase ^ 1u, sc, a)) break;
           uint8_t* sa = smem + (size_t)stage * kStageBytes;
           uint8_t* sb = sa + kABytes;
+          // this CTA's A, and (with the peer) both halves of B: 48 KB land per stage
           mbar_expect_tx(&sc->full[stage], kStageBytes);
           tma_load_2d(smem_u32(sa), &tmY, &sc->full[stage], kb * BK, ra * BM);
-          tma_load_2d(smem_u32(sb), &tmY, &sc->full[stage], kb * BK, ca * BN);
-          tma_load_2d(smem_u32(sb + kBBytes / 2), &tmY, &sc->full[stage], kb * BK,
-                      ca * BN + BN / 2);
+          if (kCl == 1) {
+            tma_load_2d(smem_u32(sb), &tmY, &sc->full[stage], kb * BK, ca * BN);
+            tma_load_2d(smem_u32(sb + kBBytes / 2), &tmY, &sc->full[stage], kb * BK,
+                        ca * BN + BN / 2);
+          } else {
+            tma_load_2d_mc(smem_u32(sb + rank * (kBBytes / 2)), &tmY, &sc->full[stage],
+                           kb * BK, ca * BN + rank * (BN / 2), kMask);
+          }
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -278,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t tphase[2] = {0, 0};
       int iter = 0;
       bool any = false;
-      for (int tile = blockIdx.x; tile < a.ntiles && !sc->abort; tile += gridDim.x, ++iter) {
+      for (int tile = cid; tile < a.ntiles && !sc->abort; tile += ncl, ++iter) {
         const int acc = iter & 1;
         if (!mbar_wait(&sc->tempty[acc], tphase[acc] ^ 1u, sc, a)) break;
         tphase[acc] ^= 1u;
@@ -297,7 +356,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16(tacc, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
                      (kb > 0 || kk > 0) ? 1u : 0u);
           any = true;
-          mma_commit(&sc->empty[stage]);
+          if (kCl == 1)
+            mma_commit(&sc->empty[stage]);
+          else
+            mma_commit_mc(&sc->empty[stage], kMask);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -316,13 +378,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    TileCursor cur;
+    TileCursor<kCl> cur;
     uint32_t tphase[2] = {0, 0};
     int iter = 0;
     const bool vec_ok = (a.b % 4) == 0;
-    for (int tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++iter) {
-      int ra, ca;
-      cur.seek(a, tile, ra, ca);
+    for (int tile = cid; tile < a.ntiles; tile += ncl, ++iter) {
+      int rg, ca;
+      cur.seek(a, tile, rg, ca);
+      const int ra = kCl * rg + rank;
       const int acc = iter & 1;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&sc->tfull[acc], tphase[acc], sc, a) ? 1 : 0;
@@ -371,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (kCl > 1) cluster_sync();  // no peer copy or commit still targets this CTA
   tc_fence_after();
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -406,7 +470,8 @@ bool gram_tc_supported(int64_t S, int64_t n, int b) {
 }
 
 cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b, int s,
-                           bool diag, float* G, Ctrl* ctrl, uint32_t timeout_us, Ctx& c) {
+                           bool diag, bool no_cluster, float* G, Ctrl* ctrl, uint32_t timeout_us,
+                           Ctx& c) {
   (void)s;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
@@ -431,12 +496,17 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
   a.TC = (int)((S + BN - 1) / BN);
   a.diag = diag;
   a.timeout_ns = (uint64_t)(timeout_us ? timeout_us : 1000000u) * 1000ull;
+  if (S <= 0) return cudaSuccess;
+  const bool cluster = !no_cluster && a.TR > 1;
+  const int kcl = cluster ? 2 : 1;
   // count the needed tiles on the host with the same rule the kernel walks
   int64_t total = 0;
-  for (int ra = 0; ra < a.TR; ++ra) {
-    int64_t last = (int64_t)ra * BM + BM - 1;
-    if (last > S - 1) last = S - 1;
-    const int64_t jmax = last / b;
+  for (int g = 0; g * kcl < a.TR; ++g) {
+    int last = g * kcl + kcl - 1;
+    if (last > a.TR - 1) last = a.TR - 1;
+    int64_t lr = (int64_t)last * BM + BM - 1;
+    if (lr > S - 1) lr = S - 1;
+    const int64_t jmax = lr / b;
     const int64_t lim = (int64_t)b * (diag ? jmax + 1 : jmax);
     int64_t cc = (lim + BN - 1) / BN;
     total += cc < a.TC ? cc : a.TC;
@@ -444,13 +514,41 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
   a.ntiles = (int)total;
   if (a.ntiles == 0) return cudaSuccess;
 
-  cudaError_t e = cudaFuncSetAttribute(gram_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (!cluster) {
+    cudaError_t e = cudaFuncSetAttribute(gram_tc_kernel<1>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = a.ntiles < c.num_sms ? a.ntiles : c.num_sms;
+    gram_tc_kernel<1><<<grid, kThreads, kSmemBytes, c.stream>>>(map, a);
+    ++c.launches;
+    return cudaGetLastError();
+  }
+  cudaError_t e = cudaFuncSetAttribute(gram_tc_kernel<2>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int grid = a.ntiles < c.num_sms ? a.ntiles : c.num_sms;
-  gram_tc_kernel<<<grid, kThreads, kSmemBytes, c.stream>>>(map, a);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = c.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(2 * (unsigned)(c.num_sms / 2));
+  int max_clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&max_clusters, gram_tc_kernel<2>, &cfg) != cudaSuccess ||
+      max_clusters < 1)
+    max_clusters = c.num_sms / 2;
+  int clusters = a.ntiles < max_clusters ? a.ntiles : max_clusters;
+  cfg.gridDim = dim3(2 * (unsigned)clusters);
+  e = cudaLaunchKernelEx(&cfg, gram_tc_kernel<2>, map, a);
   ++c.launches;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace casgd

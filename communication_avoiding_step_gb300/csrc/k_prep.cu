@@ -53,13 +53,16 @@ __global__ void __launch_bounds__(256) gather_kernel(
     int64_t ld, const float* __restrict__ w, int64_t S, uint64_t seed, uint64_t counter0,
     const int32_t* __restrict__ idx_in, int32_t* __restrict__ idx_out,
     uint16_t* __restrict__ Y, int64_t ldY, uint16_t* __restrict__ r,
-    float* __restrict__ yY, Ctrl* ctrl, int s, int G) {
-  if (blockIdx.x == 0) {
+    float* __restrict__ yY, Ctrl* ctrl, uint32_t* far_done, int s, int G) {
+  if (blockIdx.x == 0) {  // per-step reset of the recurrence's queue and counters
     if (threadIdx.x == 0) {
       ctrl->next_unit = 0;
-      ctrl->abort = 0;
+      ctrl->abort = (ctrl->status & ST_TIMEOUT) ? 1u : 0u;  // stays set after a timeout
     }
-    for (int j = threadIdx.x; j < kMaxS; j += blockDim.x) ctrl->block_done[j] = 0;
+    for (int j = threadIdx.x; j < kMaxS; j += blockDim.x) {
+      ctrl->block_done[j] = 0;
+      far_done[j] = 0;
+    }
   }
   const int lane = threadIdx.x & 31;
   const int g = lane & (G - 1);
@@ -67,6 +70,7 @@ __global__ void __launch_bounds__(256) gather_kernel(
   const int64_t p = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * rows_per_warp +
                     lane / G;
   const int64_t nvec = ldY / 8;
+  const bool w_vec = (reinterpret_cast<uintptr_t>(w) & 15u) == 0;
   // Every lane of the warp must reach the shuffles, so out-of-range rows only mask.
   const bool live = p < S;
   int32_t row = 0;
@@ -85,11 +89,22 @@ __global__ void __launch_bounds__(256) gather_kernel(
   if (live) {
     const uint16_t* xr = X + (int64_t)(valid ? row : 0) * ld;
     uint16_t* yr = Y + p * ldY;
+#pragma unroll 4
     for (int64_t v = g; v < nvec; v += G) {
       const int64_t c0 = v * 8;
       uint4 q = make_uint4(0, 0, 0, 0);
       if (valid) q = __ldg(reinterpret_cast<const uint4*>(xr + c0));
       uint32_t parts[4] = {q.x, q.y, q.z, q.w};
+      float wv[8];
+      if (w_vec && c0 + 8 <= n) {
+        const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + c0));
+        const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + c0 + 4));
+        wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
+        wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) wv[e] = c0 + e < n ? __ldg(w + c0 + e) : 0.0f;
+      }
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         const int64_t c = c0 + 2 * h;
@@ -97,8 +112,8 @@ __global__ void __launch_bounds__(256) gather_kernel(
         if (c >= n) lo = 0;
         if (c + 1 >= n) hi = 0;
         parts[h] = lo | (hi << 16);
-        if (c < n) acc = fmaf(bf16_bits_to_float(lo), __ldg(w + c), acc);
-        if (c + 1 < n) acc = fmaf(bf16_bits_to_float(hi), __ldg(w + c + 1), acc);
+        if (c < n) acc = fmaf(bf16_bits_to_float(lo), wv[2 * h], acc);
+        if (c + 1 < n) acc = fmaf(bf16_bits_to_float(hi), wv[2 * h + 1], acc);
       }
       *reinterpret_cast<uint4*>(yr + c0) = make_uint4(parts[0], parts[1], parts[2], parts[3]);
     }
@@ -142,14 +157,15 @@ cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t coun
 
 cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const float* w,
                           uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
-                          int64_t ldY, uint16_t* r, float* yY, Ctrl* ctrl, Ctx& c) {
+                          int64_t ldY, uint16_t* r, float* yY, Ctrl* ctrl,
+                          uint32_t* far_done, Ctx& c) {
   const int64_t S = (int64_t)p.b * p.s;
   const int G = pow2_at_least(ldY / 8, 32);
   const int64_t rows_per_cta = 8 * (32 / G);
   const int64_t blocks = (S + rows_per_cta - 1) / rows_per_cta;
   gather_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>(
       static_cast<const uint16_t*>(d.X), d.y, d.m, d.n, d.ld, w, S, p.seed, k * (uint64_t)S,
-      idx_in, idx, Y, ldY, r, yY, ctrl, p.s, G);
+      idx_in, idx, Y, ldY, r, yY, ctrl, far_done, p.s, G);
   ++c.launches;
   return cudaGetLastError();
 }

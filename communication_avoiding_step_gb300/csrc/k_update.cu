@@ -34,19 +34,34 @@ __global__ void __launch_bounds__(256) update_partial_kernel(
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[v][e] = 0.0f;
 
-  for (int64_t i = r_lo + tr; i < r_hi; i += TR) {
-    const float a = __ldg(alpha + i);
-    const uint16_t* yr = Y + i * ldY;
+  // Rows are taken kUnroll at a time so that several 16-byte loads are in flight per
+  // thread; the FMA order per column stays row-ascending.
+  constexpr int kUnroll = 4;
+  for (int64_t i0 = r_lo + tr; i0 < r_hi; i0 += (int64_t)TR * kUnroll) {
+    float a[kUnroll];
+    const uint16_t* yr[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t i = i0 + (int64_t)u * TR;
+      a[u] = i < r_hi ? __ldg(alpha + i) : 0.0f;
+      yr[u] = Y + (i < r_hi ? i : r_lo) * ldY;
+    }
 #pragma unroll
     for (int v = 0; v < kMaxVecPerThread; ++v) {
       const int64_t vec = tv + (int64_t)v * TV;
       if (vec < nvec) {
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(yr + vec * 8));
-        const uint32_t pw[4] = {q.x, q.y, q.z, q.w};
+        uint4 q[kUnroll];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          acc[v][2 * h] = fmaf(a, bf16_bits_to_float(pw[h] & 0xFFFFu), acc[v][2 * h]);
-          acc[v][2 * h + 1] = fmaf(a, bf16_bits_to_float(pw[h] >> 16), acc[v][2 * h + 1]);
+        for (int u = 0; u < kUnroll; ++u)
+          q[u] = __ldg(reinterpret_cast<const uint4*>(yr[u] + vec * 8));
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const uint32_t pw[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            acc[v][2 * h] = fmaf(a[u], bf16_bits_to_float(pw[h] & 0xFFFFu), acc[v][2 * h]);
+            acc[v][2 * h + 1] = fmaf(a[u], bf16_bits_to_float(pw[h] >> 16), acc[v][2 * h + 1]);
+          }
         }
       }
     }
@@ -73,15 +88,38 @@ __global__ void __launch_bounds__(256) update_partial_kernel(
   }
 }
 
-__global__ void update_reduce_kernel(const float* __restrict__ part, int P, int64_t n,
-                                     int64_t ldY, float* __restrict__ w, Ctrl* ctrl) {
-  const int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  if (c >= n) return;
-  float sum = 0.0f;
-  for (int p = 0; p < P; ++p) sum += part[(int64_t)p * ldY + c];
-  const float v = w[c] + sum;
-  w[c] = v;
-  if (!isfinite(v)) atomicOr(&ctrl->status, ST_NONFINITE);
+// w[c] += sum_p part[p][c].  A CTA covers 32 columns with 8 warps; warp q sums the
+// partial rows p = q, q+8, ... of its column (eight loads in flight), and the eight
+// warp sums are combined in warp order: a fixed association, so the result is
+// deterministic.
+__global__ void __launch_bounds__(256) update_reduce_kernel(const float* __restrict__ part,
+                                                            int P, int64_t n, int64_t ldY,
+                                                            float* __restrict__ w, Ctrl* ctrl) {
+  __shared__ float red[8][32];
+  const int lane = threadIdx.x & 31, q = threadIdx.x >> 5;
+  const int64_t c = (int64_t)blockIdx.x * 32 + lane;
+  float acc = 0.0f;
+  if (c < n) {
+    int p = q;
+    for (; p + 56 < P; p += 64) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldg(part + (int64_t)(p + 8 * u) * ldY + c);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc += v[u];
+    }
+    for (; p < P; p += 8) acc += __ldg(part + (int64_t)p * ldY + c);
+  }
+  red[q][lane] = acc;
+  __syncthreads();
+  if (q == 0 && c < n) {
+    float sum = 0.0f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) sum += red[u][lane];
+    const float v = w[c] + sum;
+    w[c] = v;
+    if (!isfinite(v)) atomicOr(&ctrl->status, ST_NONFINITE);
+  }
 }
 
 // Loss: groups of G lanes per row (as in the gather), grid-stride over rows.
@@ -99,6 +137,9 @@ __global__ void __launch_bounds__(256) loss_kernel(const uint16_t* __restrict__ 
   const int rows_per_warp = 32 / G;
   const int64_t nvec = (n + 7) / 8;
   const int64_t rows_per_pass = (int64_t)gridDim.x * 8 * rows_per_warp;
+  constexpr int kBatch = 8;
+  // w read as float4 when it is 16-byte aligned and n is a multiple of 8
+  const bool w_vec = ((reinterpret_cast<uintptr_t>(w) & 15u) == 0) && (n % 8 == 0);
   double mine = 0.0;
   for (int64_t base = ((int64_t)blockIdx.x * 8 + warp) * rows_per_warp; base < m;
        base += rows_per_pass) {
@@ -107,15 +148,36 @@ __global__ void __launch_bounds__(256) loss_kernel(const uint16_t* __restrict__ 
     float acc = 0.0f;
     if (live) {
       const uint16_t* xr = X + row * ld;
-      for (int64_t v = g; v < nvec; v += G) {
-        const int64_t c0 = v * 8;
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(xr + c0));
-        const uint32_t pw[4] = {q.x, q.y, q.z, q.w};
+      // Issue up to kBatch 16-byte loads of the row before using any of them.
+      for (int64_t v0 = g; v0 < nvec; v0 += (int64_t)G * kBatch) {
+        uint4 q[kBatch];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int64_t c = c0 + 2 * h;
-          if (c < n) acc = fmaf(bf16_bits_to_float(pw[h] & 0xFFFFu), __ldg(w + c), acc);
-          if (c + 1 < n) acc = fmaf(bf16_bits_to_float(pw[h] >> 16), __ldg(w + c + 1), acc);
+        for (int u = 0; u < kBatch; ++u) {
+          const int64_t v = v0 + (int64_t)u * G;
+          q[u] = v < nvec ? __ldg(reinterpret_cast<const uint4*>(xr + v * 8))
+                          : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int64_t c0 = (v0 + (int64_t)u * G) * 8;
+          if (c0 >= n) break;
+          float wv[8];
+          if (w_vec) {
+            const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + c0));
+            const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + c0 + 4));
+            wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
+            wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) wv[e] = c0 + e < n ? __ldg(w + c0 + e) : 0.0f;
+          }
+          const uint32_t pw[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int64_t c = c0 + 2 * h;
+            if (c < n) acc = fmaf(bf16_bits_to_float(pw[h] & 0xFFFFu), wv[2 * h], acc);
+            if (c + 1 < n) acc = fmaf(bf16_bits_to_float(pw[h] >> 16), wv[2 * h + 1], acc);
+          }
         }
       }
     }
@@ -162,7 +224,7 @@ cudaError_t launch_update(const uint16_t* Y, const float* alpha, int64_t S, int6
   ++c.launches;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const unsigned blocks = (unsigned)((n + 255) / 256);
+  const unsigned blocks = (unsigned)((n + 31) / 32);
   update_reduce_kernel<<<blocks, 256, 0, c.stream>>>(part, upd_ctas, n, ldY, w, ctrl);
   ++c.launches;
   return cudaGetLastError();

@@ -67,6 +67,8 @@ enum {
 #define CASGD_FLAG_WRITE_DIAG_BLOCKS 0x1u  /* also compute and store G_{j,j} (parity)   */
 #define CASGD_FLAG_GRAM_TENSOR       0x2u  /* force the tcgen05 tensor-core Gram kernel */
 #define CASGD_FLAG_GRAM_SIMT         0x4u  /* force the CUDA-core Gram kernel          */
+#define CASGD_FLAG_GRAM_NO_CLUSTER   0x8u  /* tcgen05 Gram without 2-CTA clusters
+                                              (each CTA loads all of its B tile)      */
 #define CASGD_FLAG_TEST_STALL        0x80000000u /* test only: the recurrence's first
                                               block never signals completion, so every
                                               waiter runs into its time bound and the

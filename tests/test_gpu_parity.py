@@ -110,12 +110,13 @@ def _params(casgd, p, override, flags):
     return casgd.Params(b, s, eta, p.recipe.loss, seed=0, flags=flags)
 
 
-@pytest.mark.parametrize("gram", ["simt", "tensor"])
+@pytest.mark.parametrize("gram", ["simt", "tensor", "tensor_1cta"])
 @pytest.mark.parametrize("name,factory,override", CASES, ids=[c[0] for c in CASES])
 def test_outer_step_parity(gpu_lib, name, factory, override, gram):
     casgd = gpu_lib
     p = factory()
-    flag = casgd.FLAG_GRAM_SIMT if gram == "simt" else casgd.FLAG_GRAM_TENSOR
+    flag = {"simt": casgd.FLAG_GRAM_SIMT, "tensor": casgd.FLAG_GRAM_TENSOR,
+            "tensor_1cta": casgd.FLAG_GRAM_TENSOR | casgd.FLAG_GRAM_NO_CLUSTER}[gram]
     params = _params(casgd, p, override, flag | casgd.FLAG_WRITE_DIAG_BLOCKS)
     b, s = params.b, params.s
     data = _dev(p, casgd)
@@ -123,7 +124,7 @@ def test_outer_step_parity(gpu_lib, name, factory, override, gram):
         try:
             w_gpu, taps, st = _run_step(casgd, data, params, w0, k=3)
         except casgd.CasgdError as e:
-            if gram == "tensor" and e.code == 7:
+            if gram != "simt" and e.code == 7:
                 pytest.skip("tensor-core Gram does not take this shape")
             raise
         assert st == 0
