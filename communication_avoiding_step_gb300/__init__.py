@@ -14,7 +14,9 @@ from dataclasses import dataclass
 import torch
 
 from ._native import (  # noqa: F401
-    CASGD_LOGISTIC, CASGD_LSQ, CASGD_POISSON, FLAG_GRAM_NO_CLUSTER, FLAG_GRAM_SIMT,
+    CASGD_LOGISTIC, CASGD_LSQ, CASGD_POISSON, FLAG_GRAM_MULTICAST, FLAG_GRAM_NO_CLUSTER,
+    FLAG_GRAM_PAIR,
+    FLAG_GRAM_SIMT,
     FLAG_GRAM_TENSOR,
     FLAG_TEST_STALL, FLAG_WRITE_DIAG_BLOCKS, STAGE_EVENTS, CasgdError, Data as _Data,
     Params as _Params, Profile as _Profile, Taps as _Taps, check as _check, header_symbols,

@@ -17,6 +17,8 @@ FLAG_WRITE_DIAG_BLOCKS = 0x1
 FLAG_GRAM_TENSOR = 0x2
 FLAG_GRAM_SIMT = 0x4
 FLAG_GRAM_NO_CLUSTER = 0x8
+FLAG_GRAM_MULTICAST = 0x10
+FLAG_GRAM_PAIR = 0x20
 FLAG_TEST_STALL = 0x80000000
 STAGE_EVENTS = 5
 

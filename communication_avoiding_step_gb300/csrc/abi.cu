@@ -95,8 +95,9 @@ int gram_choice(const casgd_params_t* p, int64_t S, int64_t n) {
   const bool tc_ok = gram_tc_supported(S, n, p->b);
   if (p->flags & CASGD_FLAG_GRAM_TENSOR) return tc_ok ? 1 : -1;
   if (p->flags & CASGD_FLAG_GRAM_SIMT) return 2;
-  // Default: tensor cores where n is wide enough for the contraction to matter.
-  return (tc_ok && n > 32) ? 1 : 2;
+  // Default: tensor cores (measured faster than the CUDA-core kernel for every feature
+  // count here, n = 18 .. 2000, because writing G dominates for narrow n).
+  return tc_ok ? 1 : 2;
 }
 
 int record(casgd_profile_t* prof, int64_t it, int e, cudaStream_t st) {
@@ -128,11 +129,17 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   if (prof) prof->gram_kind = choice;
 
   if ((rc = record(prof, it, 0, st)) != CASGD_OK) return rc;
-  CK(launch_gather(*d, *p, w, k, idx_in, R.idx, R.Y, L.ldY, R.r, R.yY, R.ctrl, R.far_done, c));
+  CK(launch_gather(*d, *p, w, k, idx_in, R.idx, R.Y, L.ldY, R.r, R.yY, R.alpha, R.far, R.ctrl,
+                   R.far_done, c));
   if ((rc = record(prof, it, 1, st)) != CASGD_OK) return rc;
   if (choice == 1) {
-    CK(launch_gram_tc(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag,
-                      (p->flags & CASGD_FLAG_GRAM_NO_CLUSTER) != 0, G, R.ctrl, p->timeout_us, c));
+    // variant: forced by a flag, else CTA pairs for deep K (MMA-bound) and multicast
+    // clusters for shallow K (bound by writing G), as measured on the five workloads
+    const int mode = (p->flags & CASGD_FLAG_GRAM_NO_CLUSTER) ? 1
+                     : (p->flags & CASGD_FLAG_GRAM_MULTICAST) ? 2
+                     : (p->flags & CASGD_FLAG_GRAM_PAIR)      ? 0
+                     : (d->n >= 1024 ? 0 : 2);
+    CK(launch_gram_tc(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag, mode, G, R.ctrl, p->timeout_us, c));
   } else {
     CK(launch_gram_simt(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag, G, c));
   }

@@ -25,6 +25,10 @@ enum : uint32_t {
 };
 
 constexpr int kMaxS = 64;
+// alpha slots hold this bit pattern from the gather kernel until the recurrence writes
+// their value (a NaN payload no arithmetic produces: computed NaNs are 0x7FFFFFFF), so
+// a reader can wait on the values themselves.
+constexpr uint32_t kAlphaPending = 0x7FA1FA11u;
 constexpr int64_t kMaxSB = 65536;
 constexpr int64_t kMaxN = 16384;
 constexpr int kLossCtas = 1024;     // upper bound on loss-kernel CTAs (partials)
@@ -129,13 +133,13 @@ cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t coun
                           int32_t* idx, Ctx& c);
 cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const float* w,
                           uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
-                          int64_t ldY, uint16_t* r, float* yY, Ctrl* ctrl,
-                          uint32_t* far_done, Ctx& c);
+                          int64_t ldY, uint16_t* r, float* yY, float* alpha, float* far,
+                          Ctrl* ctrl, uint32_t* far_done, Ctx& c);
 cudaError_t launch_gram_simt(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
                              int s, bool diag, float* G, Ctx& c);
 bool gram_tc_supported(int64_t S, int64_t n, int b);
 cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
-                           int s, bool diag, bool no_cluster, float* G, Ctrl* ctrl,
+                           int s, bool diag, int mode, float* G, Ctrl* ctrl,
                            uint32_t timeout_us, Ctx& c);
 cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, float* alpha,
                          float* far, uint32_t* far_done, int b, int s, float eta, int loss,

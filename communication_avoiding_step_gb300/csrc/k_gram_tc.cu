@@ -17,7 +17,8 @@
 //               stores of the rows/columns that belong to needed blocks into the packed
 //               block-lower G.  Two accumulators let the epilogue of one tile overlap
 //               the MMAs of the next.
-// Cluster variant (kCl = 2, the default): the two CTAs of a cluster compute row tiles
+// Variants: the paired-SM kernel below (default); a single-CTA kernel (kCl = 1); and a
+// cluster variant (kCl = 2): the two CTAs of a cluster compute row tiles
 // 2g and 2g+1 against the same B tile; each loads one 128-row half of B and multicasts
 // it to both, so a CTA pulls 32 KB instead of 48 KB from L2 per 64 columns of K.  A
 // stage is refilled only after both CTAs' MMAs have read it (each MMA warp's commit
@@ -247,6 +248,47 @@ struct TileCursor {
   }
 };
 
+// Epilogue of one tile for one warp: TMEM lanes 32*quarter.. hold rows ra*BM + 32*quarter
+// + lane of the tile; the 256 accumulator columns of buffer `acc` are read 32 at a time
+// and the entries that belong to needed blocks are stored into the packed G.
+__device__ __forceinline__ void store_tile_rows(const TcArgs& a, uint32_t tmem, int acc,
+                                                int quarter, int lane, int ra, int ca) {
+  const bool vec_ok = (a.b % 4) == 0;
+  const int64_t p = (int64_t)ra * BM + quarter * 32 + lane;
+  const bool prow = p < a.S;
+  const int64_t jb = prow ? p / a.b : 0;
+  const int64_t ib = p - jb * a.b;
+  for (int ch = 0; ch < BN / 32; ++ch) {
+    uint32_t v[32];
+    __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
+    tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
+    const int64_t q0 = (int64_t)ca * BN + ch * 32;
+    if (!prow || q0 >= a.S) continue;
+    const int64_t t0b = q0 / a.b;
+    const int64_t q1 = q0 + 31;
+    const int64_t t1b = q1 / a.b;
+    const bool whole = (q1 < a.S) && (t0b == t1b) && (t0b < jb || (a.diag && t0b == jb));
+    if (whole && vec_ok && ((q0 - t0b * a.b) % 4) == 0) {
+      float* dst = a.G + packed_offset(jb, t0b, a.b, a.diag) + ib * a.b + (q0 - t0b * a.b);
+#pragma unroll
+      for (int e = 0; e < 32; e += 4)
+        *reinterpret_cast<float4*>(dst + e) =
+            make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                        __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int64_t q = q0 + e;
+        if (q >= a.S) break;
+        const int64_t tb = q / a.b;
+        if (tb < jb || (a.diag && tb == jb))
+          a.G[packed_offset(jb, tb, a.b, a.diag) + ib * a.b + (q - tb * a.b)] =
+              __uint_as_float(v[e]);
+      }
+    }
+  }
+}
+
 template <int kCl>
 __global__ void __launch_bounds__(kThreads, 1)
     gram_tc_kernel(const __grid_constant__ CUtensorMap tmY, TcArgs a) {
@@ -381,7 +423,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     TileCursor<kCl> cur;
     uint32_t tphase[2] = {0, 0};
     int iter = 0;
-    const bool vec_ok = (a.b % 4) == 0;
     for (int tile = cid; tile < a.ntiles; tile += ncl, ++iter) {
       int rg, ca;
       cur.seek(a, tile, rg, ca);
@@ -393,39 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tphase[acc] ^= 1u;
       tc_fence_after();
-      const int64_t p = (int64_t)ra * BM + quarter * 32 + lane;
-      const bool prow = p < a.S;
-      const int64_t jb = prow ? p / a.b : 0;
-      const int64_t ib = p - jb * a.b;
-      for (int ch = 0; ch < BN / 32; ++ch) {
-        uint32_t v[32];
-        __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
-        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
-        const int64_t q0 = (int64_t)ca * BN + ch * 32;
-        if (!prow || q0 >= a.S) continue;
-        const int64_t t0b = q0 / a.b;
-        const int64_t q1 = q0 + 31;
-        const int64_t t1b = q1 / a.b;
-        const bool whole = (q1 < a.S) && (t0b == t1b) && (t0b < jb || (a.diag && t0b == jb));
-        if (whole && vec_ok && ((q0 - t0b * a.b) % 4) == 0) {
-          float* dst = a.G + packed_offset(jb, t0b, a.b, a.diag) + ib * a.b + (q0 - t0b * a.b);
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + e) =
-                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                            __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int64_t q = q0 + e;
-            if (q >= a.S) break;
-            const int64_t tb = q / a.b;
-            if (tb < jb || (a.diag && tb == jb))
-              a.G[packed_offset(jb, tb, a.b, a.diag) + ib * a.b + (q - tb * a.b)] =
-                  __uint_as_float(v[e]);
-          }
-        }
-      }
+      store_tile_rows(a, tmem, acc, quarter, lane, ra, ca);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sc->tempty[acc]);
@@ -438,6 +447,228 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+  if (threadIdx.x == 0 && sc->abort) atomicExch(&a.ctrl->abort, 1u);
+}
+
+// ------------------------------------------------------------ paired-SM variant
+// A 2-CTA cluster computes a 256x256 tile with tcgen05.mma.cta_group::2 (M = 256): each
+// CTA loads its own 128 rows of A and its own 128-row half of B, so a stage costs a CTA
+// 32 KB of shared memory (six stages fit) and 32 KB of L2 reads for 128x256x64 of MMA
+// work.  The leader CTA (rank 0) issues the MMAs; its full barrier receives both CTAs'
+// copies (cta_group::2 TMA signals the leader's barrier); each commit multicasts to the
+// barriers of both CTAs; each CTA's TMEM holds its 128 rows of the accumulator and its
+// own epilogue warps store them.  Every tcgen05 operation of this kernel, the TMEM
+// allocation included, uses cta_group::2.
+constexpr int kStages2 = 7;                      // 7 x 32 KB + barriers fit in 227 KB
+constexpr int kHalfB = 128 * BK * 2;              // 16 KB
+constexpr int kStageBytes2 = kABytes + kHalfB;    // 32 KB per CTA per stage
+constexpr size_t kSmemBytes2 = (size_t)kStages2 * kStageBytes2 + 1024 + 1024;
+static_assert(kSmemBytes2 <= 232448, "dynamic shared memory per CTA");
+constexpr uint32_t kIdesc2 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                             ((uint32_t)(256 >> 4) << 24);
+
+struct SharedCtl2 {
+  uint64_t full[kStages2];   // leader: both CTAs' copies of a stage have landed
+  uint64_t empty[kStages2];  // both CTAs: the leader's MMAs have read a stage
+  uint64_t tfull[2];         // both CTAs: accumulator buffer complete
+  uint64_t tempty[2];        // leader: both CTAs' epilogues done with a buffer (8 warps)
+  uint64_t drain;            // leader: every MMA complete
+  uint32_t tmem_base;
+  volatile uint32_t abort;
+};
+
+__device__ __forceinline__ uint32_t mapa_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// TMA into this CTA's shared memory, completion signalled on a barrier that may live in
+// the peer CTA of the pair (a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc2), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+__device__ bool mbar_wait2(uint64_t* bar, uint32_t parity, SharedCtl2* sc, const TcArgs& a) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (sc->abort) return false;
+    if (globaltimer_ns() - t0 > a.timeout_ns) {
+      sc->abort = 1;
+      atomicOr(&a.ctrl->status, ST_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gram_tc2sm_kernel(const __grid_constant__ CUtensorMap tmY, TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  SharedCtl2* sc = reinterpret_cast<SharedCtl2*>(smem + (size_t)kStages2 * kStageBytes2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)cluster_rank();
+  const bool leader = rank == 0;
+  const int cid = blockIdx.x / 2, ncl = gridDim.x / 2;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages2; ++i) {
+      mbar_init(&sc->full[i], 1);
+      mbar_init(&sc->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sc->tfull[i], 1);
+      mbar_init(&sc->tempty[i], 8);
+    }
+    mbar_init(&sc->drain, 1);
+    sc->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {  // one warp of each CTA allocates collectively for the pair
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sc->tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = sc->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // -------------------------------------------------------- TMA producer (both CTAs)
+      TileCursor<2> cur;
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = cid; tile < a.ntiles && !sc->abort; tile += ncl) {
+        int rg, ca;
+        cur.seek(a, tile, rg, ca);
+        const int ra = 2 * rg + rank;
+        for (int kb = 0; kb < a.nkb; ++kb) {
+          if (!mbar_wait2(&sc->empty[stage], phase ^ 1u, sc, a)) break;
+          uint8_t* sa = smem + (size_t)stage * kStageBytes2;
+          uint8_t* sb = sa + kABytes;
+          if (leader) mbar_expect_tx(&sc->full[stage], 2 * kStageBytes2);  // both CTAs
+          const uint32_t bar = mapa_rank(smem_u32(&sc->full[stage]), 0);
+          tma_load_2d_pair(smem_u32(sa), &tmY, bar, kb * BK, ra * BM);
+          tma_load_2d_pair(smem_u32(sb), &tmY, bar, kb * BK, ca * BN + rank * (BN / 2));
+          if (++stage == kStages2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // -------------------------------------------------------- MMA issuer (leader)
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t tphase[2] = {0, 0};
+      int iter = 0;
+      bool any = false;
+      for (int tile = cid; tile < a.ntiles && !sc->abort; tile += ncl, ++iter) {
+        const int acc = iter & 1;
+        if (!mbar_wait2(&sc->tempty[acc], tphase[acc] ^ 1u, sc, a)) break;
+        tphase[acc] ^= 1u;
+        tc_fence_after();
+        const uint32_t tacc = tmem + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < a.nkb; ++kb) {
+          if (!mbar_wait2(&sc->full[stage], phase, sc, a)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes2);
+          const uint32_t sb = sa + kABytes;
+          const uint64_t ad = sdesc_sw128(sa), bd = sdesc_sw128(sb);
+          const int krem = a.n - kb * BK;
+          const int ksteps = krem >= BK ? BK / 16 : (krem + 15) / 16;
+          for (int kk = 0; kk < ksteps; ++kk)
+            mma_bf16_pair(tacc, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
+                          (kb > 0 || kk > 0) ? 1u : 0u);
+          any = true;
+          mma_commit_pair(&sc->empty[stage], 0x3);
+          if (++stage == kStages2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(&sc->tfull[acc], 0x3);
+      }
+      if (any) {  // drain: every MMA complete before the pair frees TMEM
+        mma_commit_pair(&sc->drain, 0x1);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&sc->drain, 0) && globaltimer_ns() - t0 < a.timeout_ns) {
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue (both CTAs)
+    const int quarter = warp & 3;
+    TileCursor<2> cur;
+    uint32_t tphase[2] = {0, 0};
+    int iter = 0;
+    for (int tile = cid; tile < a.ntiles; tile += ncl, ++iter) {
+      int rg, ca;
+      cur.seek(a, tile, rg, ca);
+      const int ra = 2 * rg + rank;
+      const int acc = iter & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait2(&sc->tfull[acc], tphase[acc], sc, a) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tphase[acc] ^= 1u;
+      tc_fence_after();
+      store_tile_rows(a, tmem, acc, quarter, lane, ra, ca);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_rank(smem_u32(&sc->tempty[acc]), 0));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the leader's MMAs and every copy into either CTA are finished
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
                  : "memory");
   }
@@ -470,7 +701,7 @@ bool gram_tc_supported(int64_t S, int64_t n, int b) {
 }
 
 cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b, int s,
-                           bool diag, bool no_cluster, float* G, Ctrl* ctrl, uint32_t timeout_us,
+                           bool diag, int mode, float* G, Ctrl* ctrl, uint32_t timeout_us,
                            Ctx& c) {
   (void)s;
   EncodeTiledFn enc = encode_fn();
@@ -497,8 +728,10 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
   a.diag = diag;
   a.timeout_ns = (uint64_t)(timeout_us ? timeout_us : 1000000u) * 1000ull;
   if (S <= 0) return cudaSuccess;
-  const bool cluster = !no_cluster && a.TR > 1;
-  const int kcl = cluster ? 2 : 1;
+  // mode 0: paired-SM MMA (default); 1: one CTA per tile; 2: 2-CTA clusters sharing B
+  // by multicast.  A single row tile always runs on one CTA.
+  if (a.TR <= 1) mode = 1;
+  const int kcl = mode == 1 ? 1 : 2;
   // count the needed tiles on the host with the same rule the kernel walks
   int64_t total = 0;
   for (int g = 0; g * kcl < a.TR; ++g) {
@@ -514,7 +747,7 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
   a.ntiles = (int)total;
   if (a.ntiles == 0) return cudaSuccess;
 
-  if (!cluster) {
+  if (mode == 1) {
     cudaError_t e = cudaFuncSetAttribute(gram_tc_kernel<1>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
@@ -524,9 +757,9 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
     ++c.launches;
     return cudaGetLastError();
   }
-  cudaError_t e = cudaFuncSetAttribute(gram_tc_kernel<2>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+  const void* fn = mode == 0 ? (const void*)gram_tc2sm_kernel : (const void*)gram_tc_kernel<2>;
+  const size_t smem = mode == 0 ? kSmemBytes2 : kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -535,18 +768,20 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = c.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(2 * (unsigned)(c.num_sms / 2));
   int max_clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&max_clusters, gram_tc_kernel<2>, &cfg) != cudaSuccess ||
-      max_clusters < 1)
+  if (cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg) != cudaSuccess || max_clusters < 1)
     max_clusters = c.num_sms / 2;
-  int clusters = a.ntiles < max_clusters ? a.ntiles : max_clusters;
+  const int clusters = a.ntiles < max_clusters ? a.ntiles : max_clusters;
   cfg.gridDim = dim3(2 * (unsigned)clusters);
-  e = cudaLaunchKernelEx(&cfg, gram_tc_kernel<2>, map, a);
+  if (mode == 0)
+    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel, map, a);
+  else
+    e = cudaLaunchKernelEx(&cfg, gram_tc_kernel<2>, map, a);
   ++c.launches;
   return e;
 }

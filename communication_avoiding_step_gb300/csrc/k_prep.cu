@@ -53,7 +53,8 @@ __global__ void __launch_bounds__(256) gather_kernel(
     int64_t ld, const float* __restrict__ w, int64_t S, uint64_t seed, uint64_t counter0,
     const int32_t* __restrict__ idx_in, int32_t* __restrict__ idx_out,
     uint16_t* __restrict__ Y, int64_t ldY, uint16_t* __restrict__ r,
-    float* __restrict__ yY, Ctrl* ctrl, uint32_t* far_done, int s, int G) {
+    float* __restrict__ yY, float* __restrict__ alpha, float* __restrict__ far, Ctrl* ctrl,
+    uint32_t* far_done, int s, int G) {
   if (blockIdx.x == 0) {  // per-step reset of the recurrence's queue and counters
     if (threadIdx.x == 0) {
       ctrl->next_unit = 0;
@@ -122,6 +123,8 @@ __global__ void __launch_bounds__(256) gather_kernel(
   if (live && g == 0) {
     r[p] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
     yY[p] = valid ? __ldg(y + row) : 0.0f;
+    alpha[p] = __uint_as_float(kAlphaPending);  // the recurrence waits on these values
+    far[p] = __uint_as_float(kAlphaPending);
     idx_out[p] = row;
   }
 }
@@ -157,15 +160,15 @@ cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t coun
 
 cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const float* w,
                           uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
-                          int64_t ldY, uint16_t* r, float* yY, Ctrl* ctrl,
-                          uint32_t* far_done, Ctx& c) {
+                          int64_t ldY, uint16_t* r, float* yY, float* alpha, float* far,
+                          Ctrl* ctrl, uint32_t* far_done, Ctx& c) {
   const int64_t S = (int64_t)p.b * p.s;
   const int G = pow2_at_least(ldY / 8, 32);
   const int64_t rows_per_cta = 8 * (32 / G);
   const int64_t blocks = (S + rows_per_cta - 1) / rows_per_cta;
   gather_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>(
       static_cast<const uint16_t*>(d.X), d.y, d.m, d.n, d.ld, w, S, p.seed, k * (uint64_t)S,
-      idx_in, idx, Y, ldY, r, yY, ctrl, far_done, p.s, G);
+      idx_in, idx, Y, ldY, r, yY, alpha, far, ctrl, far_done, p.s, G);
   ++c.launches;
   return cudaGetLastError();
 }

@@ -7,22 +7,23 @@
 // are independent once all earlier blocks are known; the s blocks form a serial chain.
 //
 // Design: one persistent cooperative launch (all CTAs co-resident) with two roles.
-//  * Chain CTAs (the first C CTAs) each own 8-row groups of every block and walk the
-//    phases j = 0..s-1 in order.  Phase j needs only the band
-//        band_j = sum_{t=j-B}^{j-1} G_{j,t} alpha_t      (B = 1 or 2 blocks)
-//    on top of far_j (below).  A chain CTA loads its rows of the band blocks into
-//    registers before it waits for alpha_{j-1}, so after the wait only alpha_{j-1}
-//    (from L2), a short dot product and l' remain on the critical path.
+//  * Chain CTAs (the first C CTAs): one warp per row, 8-row groups.  Phase j of a row
+//    needs only the band  sum_{t=j-B}^{j-1} G_{j,t} alpha_t  (B = 1 or 2 blocks) on top
+//    of far_j (below).  The warp loads its band rows of G, the older band alpha, r and
+//    y before it waits, then waits for alpha_{j-1} and far_j by loading exactly those
+//    values until none holds the pending pattern.
 //  * Bulk CTAs take units (block j >= B+1, 16 rows) from an atomic queue in increasing
 //    j and compute far_j = sum_{t<j-B} G_{j,t} alpha_t for their rows, streaming G with
-//    coalesced float4 reads as each alpha_t becomes available.  far_j is needed only B
+//    coalesced float4 reads; they wait on alpha_t the same way.  far_j is needed only B
 //    phases after its last input is known, so most of G is read off the critical path.
-// Completion is published with device-scope fences and atomic counters
-// (block_done[j]: chain CTAs finished with phase j; far_done[j]: bulk units of block j
-// finished) and read with acquire loads.  Every wait is bounded by `timeout_ns`; on
-// expiry the waiter records ST_TIMEOUT, which wait gave up (Ctrl::diag), and the abort
-// word, and every other waiter stops.  Sums are taken in a fixed order (far_j over t
-// ascending, then the band, then r), so results are deterministic.
+// Synchronisation is through the data: the gather kernel fills alpha and far with
+// kAlphaPending before this kernel runs, and a value is final once it differs from
+// that pattern (32-bit stores are single-copy atomic, and a reader uses only the value
+// it waited on, so no fences or counters are needed).  Warps of a chain CTA never wait
+// on each other.  Every wait is bounded by `timeout_ns`; on expiry the waiter records
+// ST_TIMEOUT, which wait gave up (Ctrl::diag) and the abort word, and every other
+// waiter stops.  Sums are taken in a fixed order (far_j over t ascending; then
+// r + far + band), so results are deterministic.
 #include "casgd_internal.cuh"
 
 namespace casgd {
@@ -33,6 +34,7 @@ constexpr int kThreads = 256;
 constexpr int kRows = 16;       // rows per bulk unit
 constexpr int kChainRows = 8;   // rows per chain group (a warp per row)
 constexpr int kPrefetch = 8;    // float4 of band G (and of alpha) a chain lane keeps in registers
+constexpr int kT = 4;           // bulk: blocks t handled per pass
 
 struct RecArgs {
   const float* G;
@@ -40,8 +42,7 @@ struct RecArgs {
   const float* yY;
   float* alpha;
   float* far;
-  uint32_t* far_done;
-  uint64_t* trace;  // [kMaxS][4] timestamps of chain CTA 0 (see chain_role)
+  uint64_t* trace;  // [kMaxS][4] timestamps of chain CTA 0, warp 0
   Ctrl* ctrl;
   uint64_t timeout_ns;
   int b, s, loss, U, Uc, C, B, bulk_units;
@@ -49,44 +50,7 @@ struct RecArgs {
   bool diag, stall_test, vec4;
 };
 
-// One thread waits until *p >= need; false on timeout or abort.  `where` is recorded
-// in Ctrl::diag when this wait is the one that gives up.
-__device__ bool spin_until(const uint32_t* p, uint32_t need, const RecArgs& a, bool backoff,
-                           uint32_t where) {
-  if (ld_acquire_u32(p) >= need) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    if (backoff) __nanosleep(128);
-    if (ld_acquire_u32(p) >= need) return true;
-    if (ld_volatile_u32(&a.ctrl->abort)) return false;
-    if (globaltimer_ns() - t0 > a.timeout_ns) {
-      atomicOr(&a.ctrl->status, ST_TIMEOUT);
-      atomicExch(&a.ctrl->diag, where | (ld_volatile_u32(p) & 0xFFFu));
-      atomicExch(&a.ctrl->abort, 1u);
-      return false;
-    }
-  }
-}
-
-// Release add: orders every write this CTA made before the preceding barrier (the
-// barrier makes them visible to thread 0, the release makes them visible device-wide)
-// before the counter changes.
-__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Whole-CTA wait: thread 0 spins; the barrier orders everyone's later reads.
-__device__ bool cta_wait(const uint32_t* p, uint32_t need, const RecArgs& a, bool backoff,
-                         uint32_t where) {
-  __shared__ int s_ok;
-  if (threadIdx.x == 0) s_ok = spin_until(p, need, a, backoff, where) ? 1 : 0;
-  __syncthreads();
-  const int ok = s_ok;
-  __syncthreads();
-  return ok != 0;
-}
-
-// Ctrl::diag codes: kind << 24 | block << 12 | counter value seen.
+// Ctrl::diag codes: kind << 24 | block << 12 (kind 2: chain wait, 3: bulk wait).
 __device__ __forceinline__ uint32_t where_code(uint32_t kind, int j) {
   return (kind << 24) | ((uint32_t)j << 12);
 }
@@ -98,18 +62,59 @@ __device__ __forceinline__ float dot4(float4 g, float4 v, float acc) {
   return fmaf(g.w, v.w, acc);
 }
 
+__device__ __forceinline__ bool pending1(float v) { return __float_as_uint(v) == kAlphaPending; }
+__device__ __forceinline__ bool pending4(float4 v) {
+  return pending1(v.x) || pending1(v.y) || pending1(v.z) || pending1(v.w);
+}
+
+__device__ __forceinline__ float4 ld_volatile_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.volatile.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float ld_volatile_f32(const float* p) {
+  return *reinterpret_cast<const volatile float*>(p);
+}
+
+// Records a timeout (status, diag, abort); returns false.
+__device__ bool give_up(const RecArgs& a, uint32_t where) {
+  atomicOr(&a.ctrl->status, ST_TIMEOUT);
+  atomicExch(&a.ctrl->diag, where);
+  atomicExch(&a.ctrl->abort, 1u);
+  return false;
+}
+
+// Bound check for a wait loop: false once the wait must end.
+__device__ __forceinline__ bool keep_waiting(const RecArgs& a, uint64_t t_start, uint32_t where) {
+  if (ld_volatile_u32(&a.ctrl->abort)) return false;
+  if (globaltimer_ns() - t_start > a.timeout_ns) return give_up(a, where);
+  return true;
+}
+
+// Scalar value wait (used where b is not a multiple of 4).
+__device__ bool wait_value(const float* p, float& v, const RecArgs& a, uint32_t where) {
+  v = ld_volatile_f32(p);
+  if (!pending1(v)) return true;
+  const uint64_t t_start = globaltimer_ns();
+  while (true) {
+    v = ld_volatile_f32(p);
+    if (!pending1(v)) return true;
+    if (!keep_waiting(a, t_start, where)) return false;
+  }
+}
+
 // ------------------------------------------------------------------ chain role
-// A warp per row (8 rows per group); a lane's columns are lane*4 + 128k.  Chain CTA c
-// owns the 8-row groups c, c+C, ... of every block.  Per phase, everything that does
-// not depend on alpha_{j-1} is issued as asynchronous loads before the wait (band rows
-// of G, alpha of the older band block, r and y of the row), the far part is checked
-// only after the wait (the bulk had B phases to produce it), and completion is
-// published by one release-add after the CTA barrier.
+// A warp per row; a lane's columns are lane*4 + 128k.  Chain CTA c owns the 8-row
+// groups c, c+C, ... of every block.
 __device__ void chain_role(const RecArgs& a, int c) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = a.vec4 ? (a.b + 127) / 128 : 0;  // float4 slots per band block
-  // Chain CTA 0 keeps a per-phase timeline (globaltimer ns): phase start, alpha_{j-1}
-  // ready, far part ready, alpha_j published.
+  // Chain CTA 0, warp 0 keeps a per-phase timeline (globaltimer ns): phase start, loads
+  // issued, alpha_{j-1} and far_j arrived, alpha_j stored.
   const bool tracer = (c == 0 && threadIdx.x == 0);
   for (int j = 0; j < a.s; ++j) {
     if (tracer) a.trace[4 * j] = globaltimer_ns();
@@ -119,99 +124,129 @@ __device__ void chain_role(const RecArgs& a, int c) {
     const bool has_far = j >= a.B + 1;
     for (int grp = c; grp < a.Uc; grp += a.C) {
       const int i = grp * kChainRows + warp;  // row within block j
-      const bool live = i < a.b;
-      const int64_t p = (int64_t)j * a.b + (live ? i : 0);
+      if (i >= a.b) continue;                 // warp-uniform
+      const int64_t p = (int64_t)j * a.b + i;
       const float* grow0 = a.G + (int64_t)i * a.b;
-      // (a) asynchronous loads that do not need alpha_{j-1}
+      // (a) loads that do not need alpha_{j-1}
       float4 gv[kPrefetch], av[kPrefetch];
 #pragma unroll
       for (int q = 0; q < kPrefetch; ++q) {
         gv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
         av[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (live && q < nq) {
+        if (q < nq) {
           const int t = t0 + q / nk, col = lane * 4 + 128 * (q % nk);
           if (col < a.b) {
             gv[q] = __ldg(reinterpret_cast<const float4*>(grow0 + packed_offset(j, t, a.b, a.diag) + col));
-            if (q < nq_old)
+            if (q < nq_old)  // seen complete by this lane in the previous phase
               av[q] = __ldcg(reinterpret_cast<const float4*>(a.alpha + (int64_t)t * a.b + col));
           }
         }
       }
-      float rj = 0.0f, yj = 0.0f;
-      if (live && lane == 0) {
-        rj = bf16_bits_to_float(a.r[p]);
+      uint32_t rbits = 0;  // converted after the wait, so the load does not stall the issue
+      float yj = 0.0f;
+      if (lane == 0) {
+        rbits = a.r[p];
         yj = a.yY[p];
       }
-      // (b) the critical wait: every chain CTA done with phase j-1
-      if (grp == c && j > 0 &&
-          !cta_wait(&a.ctrl->block_done[j - 1], (uint32_t)a.C, a, false, where_code(2, j)))
-        return;
       if (tracer) a.trace[4 * j + 1] = globaltimer_ns();
-      // (c) alpha_{j-1}
-      if (live) {
+      // (b) alpha_{j-1} and far_j: load them until none is pending
+      const float* aprev = a.alpha + (int64_t)(j - 1) * a.b;
+      bool pend = false;
+      float farv = 0.0f;
+      if (a.vec4 && j > 0) {
 #pragma unroll
         for (int q = 0; q < kPrefetch; ++q) {
-          if (q >= nq_old && q < nq) {
-            const int t = t0 + q / nk, col = lane * 4 + 128 * (q % nk);
-            if (col < a.b)
-              av[q] = __ldcg(reinterpret_cast<const float4*>(a.alpha + (int64_t)t * a.b + col));
+          const int col = lane * 4 + 128 * (q % nk);
+          if (q >= nq_old && q < nq && col < a.b) {
+            av[q] = ld_volatile_f4(aprev + col);
+            pend |= pending4(av[q]);
           }
         }
       }
-      // (d) far part (normally complete long before)
-      if (grp == c && has_far &&
-          !cta_wait(&a.far_done[j], (uint32_t)a.U, a, false, where_code(1, j)))
-        return;
+      if (has_far && lane == 0) {
+        farv = ld_volatile_f32(a.far + p);
+        pend |= pending1(farv);
+      }
+      bool ok = true;
+      if (__any_sync(0xffffffffu, pend)) {
+        const uint64_t t_start = globaltimer_ns();
+        while (true) {
+          __nanosleep(32);  // eases the load on the few L2 lines every chain warp polls
+          pend = false;
+          if (a.vec4 && j > 0) {
+#pragma unroll
+            for (int q = 0; q < kPrefetch; ++q) {
+              const int col = lane * 4 + 128 * (q % nk);
+              if (q >= nq_old && q < nq && col < a.b && pending4(av[q])) {
+                av[q] = ld_volatile_f4(aprev + col);
+                pend |= pending4(av[q]);
+              }
+            }
+          }
+          if (has_far && lane == 0 && pending1(farv)) {
+            farv = ld_volatile_f32(a.far + p);
+            pend |= pending1(farv);
+          }
+          if (!__any_sync(0xffffffffu, pend)) break;
+          ok = keep_waiting(a, t_start, where_code(2, j));
+          if (!__all_sync(0xffffffffu, ok)) return;
+        }
+      }
       if (tracer) a.trace[4 * j + 2] = globaltimer_ns();
       float acc = 0.0f;
-      if (live) {
-        if (a.vec4) {
+      if (a.vec4) {
 #pragma unroll
-          for (int q = 0; q < kPrefetch; ++q)
-            if (q < nq) acc = dot4(gv[q], av[q], acc);
-          for (int q = kPrefetch; q < nq; ++q) {  // beyond the register budget
-            const int t = t0 + q / nk, col = lane * 4 + 128 * (q % nk);
-            if (col < a.b)
-              acc = dot4(__ldg(reinterpret_cast<const float4*>(grow0 + packed_offset(j, t, a.b, a.diag) + col)),
-                         __ldcg(reinterpret_cast<const float4*>(a.alpha + (int64_t)t * a.b + col)),
-                         acc);
+        for (int q = 0; q < kPrefetch; ++q)
+          if (q < nq) acc = dot4(gv[q], av[q], acc);
+        for (int q = kPrefetch; q < nq; ++q) {  // beyond the register budget
+          const int t = t0 + q / nk, col = lane * 4 + 128 * (q % nk);
+          if (col < a.b) {
+            const float* src = a.alpha + (int64_t)t * a.b + col;
+            float4 v = ld_volatile_f4(src);
+            if (pending4(v)) {
+              const uint64_t t_start = globaltimer_ns();
+              while (pending4(v) && (ok = keep_waiting(a, t_start, where_code(2, j)))) v = ld_volatile_f4(src);
+            }
+            acc = dot4(__ldg(reinterpret_cast<const float4*>(grow0 + packed_offset(j, t, a.b, a.diag) + col)),
+                       v, acc);
           }
-        } else {
-          for (int t = t0; t < j; ++t) {
-            const float* al = a.alpha + (int64_t)t * a.b;
-            const float* grow = grow0 + packed_offset(j, t, a.b, a.diag);
-            for (int col = lane; col < a.b; col += 32)
-              acc = fmaf(__ldg(grow + col), __ldcg(al + col), acc);
+        }
+      } else {
+        for (int t = t0; t < j && ok; ++t) {
+          const float* al = a.alpha + (int64_t)t * a.b;
+          const float* grow = grow0 + packed_offset(j, t, a.b, a.diag);
+          for (int col = lane; col < a.b; col += 32) {
+            float v;
+            if (!(ok = wait_value(al + col, v, a, where_code(2, j)))) break;
+            acc = fmaf(__ldg(grow + col), v, acc);
           }
         }
       }
+      if (!__all_sync(0xffffffffu, ok)) return;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (live && lane == 0) {
-        float z = rj;
-        if (has_far) z += __ldcg(a.far + p);
-        z += acc;
-        a.alpha[p] = a.coef * loss_deriv(a.loss, z, yj);
+      if (lane == 0 && !(a.stall_test && j == 0)) {
+        const float z = bf16_bits_to_float(rbits) + farv + acc;
+        __stcg(a.alpha + p, a.coef * loss_deriv(a.loss, z, yj));
       }
     }
-    __syncthreads();
-    if (threadIdx.x == 0 && !(a.stall_test && j == 0)) red_release_add(&a.ctrl->block_done[j], 1u);
     if (tracer) a.trace[4 * j + 3] = globaltimer_ns();
   }
 }
 
 // ------------------------------------------------------------------- bulk role
 // Unit = (block j, 16 rows); each warp owns two rows; a lane's columns are lane*4 + 128k.
-// Phases complete in order, so one look at the newest counter a unit needs tells it
-// whether everything is already there (a unit claimed late then streams its blocks
-// without further polling).  Up to four blocks t are processed per pass with all their
-// loads issued together; each block's dot product is summed over columns first and
-// then added in t order, so the result does not depend on how passes were grouped.
+// The CTA waits as a whole: a final alpha value of phase q implies that phase q-1 is
+// complete (its row needed all of alpha_{q-1}), so thread 0 reads single values of the
+// next phases (spread over the values by CTA index, with a back-off while the next
+// phase is not done) and the CTA then processes every block known complete, up to kT
+// per pass with all their loads issued together, reading alpha with plain loads.  Each
+// block's dot product is summed over columns first and then added in t order, so the
+// result does not depend on timing.
 __device__ void bulk_role(const RecArgs& a) {
-  __shared__ int s_unit;
-  __shared__ int s_all;
-  constexpr int kT = 4;
+  __shared__ int s_unit, s_lead;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int probe_col = (int)((blockIdx.x * 37u) % (unsigned)a.b);
   while (true) {
     if (threadIdx.x == 0) {
       int u = (int)atomicAdd(&a.ctrl->next_unit, 1u);
@@ -227,17 +262,30 @@ __device__ void bulk_role(const RecArgs& a) {
     const int i0 = c * kRows + warp * 2;
     const bool has0 = i0 < a.b, has1 = i0 + 1 < a.b;
     const int t_end = j - a.B;  // far_j covers t < j - B
-    if (threadIdx.x == 0) s_all = ld_acquire_u32(&a.ctrl->block_done[t_end - 1]) >= (uint32_t)a.C;
-    __syncthreads();
-    int known = s_all ? t_end : 0;  // blocks of alpha known to be complete
-    __syncthreads();
     float acc0 = 0.0f, acc1 = 0.0f;
+    bool ok = true;
     for (int t = 0; t < t_end;) {
-      if (t >= known) {
-        if (!cta_wait(&a.ctrl->block_done[t], (uint32_t)a.C, a, true, where_code(3, j))) return;
-        known = t + 1;
+      if (threadIdx.x == 0) {
+        // leading run of complete phases t, t+1, ... (at most kT and t_end - t)
+        const int lim = min(kT, t_end - t);
+        int lead = 0;
+        while (lead < lim && !pending1(ld_volatile_f32(a.alpha + (int64_t)(t + lead + 1) * a.b + probe_col)))
+          ++lead;
+        if (lead == 0) {  // wait for phase t, polling one value of phase t+1
+          const float* pv = a.alpha + (int64_t)(t + 1) * a.b + probe_col;
+          const uint64_t t_start = globaltimer_ns();
+          while (pending1(ld_volatile_f32(pv))) {
+            __nanosleep(200);
+            if (!keep_waiting(a, t_start, where_code(3, j))) break;
+          }
+          lead = pending1(ld_volatile_f32(pv)) ? 0 : 1;
+        }
+        s_lead = lead;
       }
-      const int nt = min(min(known, t_end) - t, kT);
+      __syncthreads();
+      const int nt = s_lead;
+      __syncthreads();
+      if (nt == 0) { ok = false; break; }  // gave up (uniform)
       if (has0) {
         const float* g0 = a.G + (int64_t)i0 * a.b;
         float d0[kT] = {0.f, 0.f, 0.f, 0.f}, d1[kT] = {0.f, 0.f, 0.f, 0.f};
@@ -263,16 +311,13 @@ __device__ void bulk_role(const RecArgs& a) {
             }
           }
         } else {
-#pragma unroll
-          for (int u = 0; u < kT; ++u) {
-            if (u < nt) {
-              const float* gb = g0 + packed_offset(j, t + u, a.b, a.diag);
-              const float* al = a.alpha + (int64_t)(t + u) * a.b;
-              for (int col = lane; col < a.b; col += 32) {
-                const float av = __ldcg(al + col);
-                d0[u] = fmaf(__ldg(gb + col), av, d0[u]);
-                if (has1) d1[u] = fmaf(__ldg(gb + a.b + col), av, d1[u]);
-              }
+          for (int u = 0; u < nt; ++u) {
+            const float* gb = g0 + packed_offset(j, t + u, a.b, a.diag);
+            const float* al = a.alpha + (int64_t)(t + u) * a.b;
+            for (int col = lane; col < a.b; col += 32) {
+              const float v = __ldcg(al + col);
+              d0[u] = fmaf(__ldg(gb + col), v, d0[u]);
+              if (has1) d1[u] = fmaf(__ldg(gb + a.b + col), v, d1[u]);
             }
           }
         }
@@ -286,18 +331,19 @@ __device__ void bulk_role(const RecArgs& a) {
       }
       t += nt;
     }
+    if (has0) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      acc0 += __shfl_xor_sync(0xffffffffu, acc0, off);
-      acc1 += __shfl_xor_sync(0xffffffffu, acc1, off);
+      for (int off = 16; off > 0; off >>= 1) {
+        acc0 += __shfl_xor_sync(0xffffffffu, acc0, off);
+        acc1 += __shfl_xor_sync(0xffffffffu, acc1, off);
+      }
+      if (lane == 0 && ok) {
+        const int64_t p0 = (int64_t)j * a.b + i0;
+        __stcg(a.far + p0, acc0);
+        if (has1) __stcg(a.far + p0 + 1, acc1);
+      }
     }
-    if (lane == 0 && has0) {
-      const int64_t p0 = (int64_t)j * a.b + i0;
-      a.far[p0] = acc0;
-      if (has1) a.far[p0 + 1] = acc1;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) red_release_add(&a.far_done[j], 1u);
+    __syncthreads();  // every warp of the unit is done before the CTA claims the next
   }
 }
 
@@ -319,7 +365,6 @@ cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, flo
   a.yY = yY;
   a.alpha = alpha;
   a.far = far;
-  a.far_done = far_done;
   a.trace = reinterpret_cast<uint64_t*>(far_done + kMaxS);
   a.ctrl = ctrl;
   a.timeout_ns = (uint64_t)(timeout_us ? timeout_us : 1000000u) * 1000ull;

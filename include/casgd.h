@@ -67,8 +67,13 @@ enum {
 #define CASGD_FLAG_WRITE_DIAG_BLOCKS 0x1u  /* also compute and store G_{j,j} (parity)   */
 #define CASGD_FLAG_GRAM_TENSOR       0x2u  /* force the tcgen05 tensor-core Gram kernel */
 #define CASGD_FLAG_GRAM_SIMT         0x4u  /* force the CUDA-core Gram kernel          */
-#define CASGD_FLAG_GRAM_NO_CLUSTER   0x8u  /* tcgen05 Gram without 2-CTA clusters
-                                              (each CTA loads all of its B tile)      */
+#define CASGD_FLAG_GRAM_NO_CLUSTER   0x8u  /* tcgen05 Gram, one CTA per 128x256 tile  */
+#define CASGD_FLAG_GRAM_MULTICAST    0x10u /* tcgen05 Gram, 2-CTA clusters that share
+                                              the B tile by TMA multicast             */
+#define CASGD_FLAG_GRAM_PAIR         0x20u /* tcgen05 Gram, CTA pairs (cta_group::2,
+                                              256x256 tiles).  Without a variant flag
+                                              the library takes pairs for n >= 1024
+                                              and multicast clusters below            */
 #define CASGD_FLAG_TEST_STALL        0x80000000u /* test only: the recurrence's first
                                               block never signals completion, so every
                                               waiter runs into its time bound and the

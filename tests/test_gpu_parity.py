@@ -110,13 +110,15 @@ def _params(casgd, p, override, flags):
     return casgd.Params(b, s, eta, p.recipe.loss, seed=0, flags=flags)
 
 
-@pytest.mark.parametrize("gram", ["simt", "tensor", "tensor_1cta"])
+@pytest.mark.parametrize("gram", ["simt", "tensor", "tensor_1cta", "tensor_mc", "tensor_pair"])
 @pytest.mark.parametrize("name,factory,override", CASES, ids=[c[0] for c in CASES])
 def test_outer_step_parity(gpu_lib, name, factory, override, gram):
     casgd = gpu_lib
     p = factory()
     flag = {"simt": casgd.FLAG_GRAM_SIMT, "tensor": casgd.FLAG_GRAM_TENSOR,
-            "tensor_1cta": casgd.FLAG_GRAM_TENSOR | casgd.FLAG_GRAM_NO_CLUSTER}[gram]
+            "tensor_1cta": casgd.FLAG_GRAM_TENSOR | casgd.FLAG_GRAM_NO_CLUSTER,
+            "tensor_mc": casgd.FLAG_GRAM_TENSOR | casgd.FLAG_GRAM_MULTICAST,
+            "tensor_pair": casgd.FLAG_GRAM_TENSOR | casgd.FLAG_GRAM_PAIR}[gram]
     params = _params(casgd, p, override, flag | casgd.FLAG_WRITE_DIAG_BLOCKS)
     b, s = params.b, params.s
     data = _dev(p, casgd)
