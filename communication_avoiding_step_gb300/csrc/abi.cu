@@ -145,10 +145,17 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   }
   // (The sum of G over processes would sit here; on one GPU it is the identity.)
   if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
+  // The update's first stage rides in the recurrence kernel while a thread needs one
+  // 16-byte column vector (n <= 2048); wider rows keep the separate two-kernel update.
+  const bool fuse_update = L.ldY <= 2048;
   CK(launch_recur(G, R.r, R.yY, R.alpha, R.far, R.far_done, p->b, p->s, p->eta, p->loss,
-                  p->flags, p->timeout_us, R.ctrl, c));
+                  p->flags, p->timeout_us, R.ctrl, R.Y, L.ldY, R.upd,
+                  fuse_update ? L.upd_ctas : 0, c));
   if ((rc = record(prof, it, 3, st)) != CASGD_OK) return rc;
-  CK(launch_update(R.Y, R.alpha, L.S, d->n, L.ldY, w, R.upd, L.upd_ctas, R.ctrl, c));
+  if (fuse_update)
+    CK(launch_update_reduce(R.upd, L.upd_ctas, d->n, L.ldY, w, R.ctrl, c));
+  else
+    CK(launch_update(R.Y, R.alpha, L.S, d->n, L.ldY, w, R.upd, L.upd_ctas, R.ctrl, c));
   if ((rc = record(prof, it, 4, st)) != CASGD_OK) return rc;
 
   if (taps) {

@@ -31,6 +31,8 @@
 // returns.
 #include <cuda.h>
 
+#include <cstring>
+
 #include "casgd_internal.cuh"
 
 namespace casgd {
@@ -44,7 +46,10 @@ constexpr int kBBytes = BN * BK * 2;  // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTmemCols = 512;
 constexpr int kThreads = 192;
-constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*align*/;
+constexpr int kStageOut = 2 * 32 * 32 * 4;  // per epilogue warp: two 32x32 FP32 chunks (8 KB)
+constexpr int kOutBytes = 4 * kStageOut;     // four epilogue warps (32 KB)
+constexpr size_t kSmemBytes =
+    (size_t)kStages * kStageBytes + kOutBytes + 1024 /*barriers*/ + 1024 /*align*/;
 
 struct TcArgs {
   float* G;
@@ -53,6 +58,7 @@ struct TcArgs {
   int n, b, nkb;
   int TR, TC, ntiles;
   bool diag;
+  bool tma_store;  // b % 32 == 0: 32x32 chunks go out through a TMA tensor store
   uint64_t timeout_ns;
 };
 
@@ -248,21 +254,69 @@ struct TileCursor {
   }
 };
 
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
+                                             int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read1() {  // at most one group still reading smem
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {  // every issued store has completed
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Epilogue of one tile for one warp: TMEM lanes 32*quarter.. hold rows ra*BM + 32*quarter
 // + lane of the tile; the 256 accumulator columns of buffer `acc` are read 32 at a time
 // and the entries that belong to needed blocks are stored into the packed G.
+// With a.tma_store (b a multiple of 32) every 32x32 chunk lies inside one block of G:
+// the warp writes it into one of its two 128-byte-swizzled staging buffers and lane 0
+// stores it with a TMA tensor store (whole 128-byte lines), through a 2D tensor map that
+// views the packed G as (blocks*b) rows of b columns.
 __device__ __forceinline__ void store_tile_rows(const TcArgs& a, uint32_t tmem, int acc,
-                                                int quarter, int lane, int ra, int ca) {
+                                                int quarter, int lane, int ra, int ca,
+                                                const CUtensorMap* tmG, uint8_t* stage,
+                                                int& sbuf) {
   const bool vec_ok = (a.b % 4) == 0;
   const int64_t p = (int64_t)ra * BM + quarter * 32 + lane;
   const bool prow = p < a.S;
   const int64_t jb = prow ? p / a.b : 0;
   const int64_t ib = p - jb * a.b;
+  const int64_t p0 = (int64_t)ra * BM + quarter * 32;  // the warp's first row
   for (int ch = 0; ch < BN / 32; ++ch) {
     uint32_t v[32];
     __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
     tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
     const int64_t q0 = (int64_t)ca * BN + ch * 32;
+    if (a.tma_store) {  // warp-uniform
+      if (p0 >= a.S || q0 >= a.S) continue;
+      const int64_t j0 = p0 / a.b, t0b = q0 / a.b;
+      if (!(t0b < j0 || (a.diag && t0b == j0))) continue;
+      uint8_t* buf = stage + sbuf * (32 * 32 * 4);
+      if (lane == 0) bulk_wait_read1();  // the store issued two chunks ago has read buf
+      __syncwarp();
+#pragma unroll
+      for (int c = 0; c < 8; ++c)  // row `lane`, 16-byte chunk c at swizzled slot c ^ (row % 8)
+        *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) * 16)) =
+            make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int64_t grow = (packed_offset(j0, t0b, a.b, a.diag) / a.b) + (p0 - j0 * a.b);
+        tma_store_2d(tmG, smem_u32(buf), (int32_t)(q0 - t0b * a.b), (int32_t)grow);
+        bulk_commit();
+      }
+      sbuf ^= 1;
+      continue;
+    }
     if (!prow || q0 >= a.S) continue;
     const int64_t t0b = q0 / a.b;
     const int64_t q1 = q0 + 31;
@@ -291,11 +345,13 @@ __device__ __forceinline__ void store_tile_rows(const TcArgs& a, uint32_t tmem, 
 
 template <int kCl>
 __global__ void __launch_bounds__(kThreads, 1)
-    gram_tc_kernel(const __grid_constant__ CUtensorMap tmY, TcArgs a) {
+    gram_tc_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmG,
+                   TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
-  SharedCtl* sc = reinterpret_cast<SharedCtl*>(smem + (size_t)kStages * kStageBytes);
+  uint8_t* out_stage = smem + (size_t)kStages * kStageBytes;  // 1024-aligned
+  SharedCtl* sc = reinterpret_cast<SharedCtl*>(out_stage + kOutBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = kCl == 2 ? (int)cluster_rank() : 0;
   const int cid = blockIdx.x / kCl, ncl = gridDim.x / kCl;  // cluster id, clusters
@@ -420,6 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    uint8_t* stage = out_stage + (warp - 2) * kStageOut;
+    int sbuf = 0;
     TileCursor<kCl> cur;
     uint32_t tphase[2] = {0, 0};
     int iter = 0;
@@ -434,11 +492,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tphase[acc] ^= 1u;
       tc_fence_after();
-      store_tile_rows(a, tmem, acc, quarter, lane, ra, ca);
+      store_tile_rows(a, tmem, acc, quarter, lane, ra, ca, &tmG, stage, sbuf);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sc->tempty[acc]);
     }
+    if (lane == 0) bulk_wait_all();  // this warp's tensor stores are complete
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -462,10 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // barriers of both CTAs; each CTA's TMEM holds its 128 rows of the accumulator and its
 // own epilogue warps store them.  Every tcgen05 operation of this kernel, the TMEM
 // allocation included, uses cta_group::2.
-constexpr int kStages2 = 7;                      // 7 x 32 KB + barriers fit in 227 KB
+constexpr int kStages2 = 6;                      // 6 x 32 KB + 32 KB output staging
 constexpr int kHalfB = 128 * BK * 2;              // 16 KB
 constexpr int kStageBytes2 = kABytes + kHalfB;    // 32 KB per CTA per stage
-constexpr size_t kSmemBytes2 = (size_t)kStages2 * kStageBytes2 + 1024 + 1024;
+constexpr size_t kSmemBytes2 = (size_t)kStages2 * kStageBytes2 + kOutBytes + 1024 + 1024;
 static_assert(kSmemBytes2 <= 232448, "dynamic shared memory per CTA");
 constexpr uint32_t kIdesc2 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                              ((uint32_t)(256 >> 4) << 24);
@@ -535,11 +595,13 @@ __device__ bool mbar_wait2(uint64_t* bar, uint32_t parity, SharedCtl2* sc, const
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    gram_tc2sm_kernel(const __grid_constant__ CUtensorMap tmY, TcArgs a) {
+    gram_tc2sm_kernel(const __grid_constant__ CUtensorMap tmY,
+                      const __grid_constant__ CUtensorMap tmG, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
-  SharedCtl2* sc = reinterpret_cast<SharedCtl2*>(smem + (size_t)kStages2 * kStageBytes2);
+  uint8_t* out_stage = smem + (size_t)kStages2 * kStageBytes2;  // 1024-aligned
+  SharedCtl2* sc = reinterpret_cast<SharedCtl2*>(out_stage + kOutBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)cluster_rank();
   const bool leader = rank == 0;
@@ -642,6 +704,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------- epilogue (both CTAs)
     const int quarter = warp & 3;
+    uint8_t* stage = out_stage + (warp - 2) * kStageOut;
+    int sbuf = 0;
     TileCursor<2> cur;
     uint32_t tphase[2] = {0, 0};
     int iter = 0;
@@ -656,11 +720,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tphase[acc] ^= 1u;
       tc_fence_after();
-      store_tile_rows(a, tmem, acc, quarter, lane, ra, ca);
+      store_tile_rows(a, tmem, acc, quarter, lane, ra, ca, &tmG, stage, sbuf);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_rank(smem_u32(&sc->tempty[acc]), 0));
     }
+    if (lane == 0) bulk_wait_all();  // this warp's tensor stores are complete
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -703,7 +769,6 @@ bool gram_tc_supported(int64_t S, int64_t n, int b) {
 cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b, int s,
                            bool diag, int mode, float* G, Ctrl* ctrl, uint32_t timeout_us,
                            Ctx& c) {
-  (void)s;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap map;
@@ -747,13 +812,28 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
   a.ntiles = (int)total;
   if (a.ntiles == 0) return cudaSuccess;
 
+  // Output map: the packed G viewed as (blocks * b) rows of b FP32 columns; 32x32 boxes.
+  CUtensorMap mapG;
+  memset(&mapG, 0, sizeof(mapG));
+  a.tma_store = false;
+  if (b % 32 == 0) {
+    const int64_t nblk = diag ? (int64_t)s * (s + 1) / 2 : (int64_t)s * (s - 1) / 2;
+    const cuuint64_t gdimG[2] = {(cuuint64_t)b, (cuuint64_t)(nblk * b)};
+    const cuuint64_t gstrideG[1] = {(cuuint64_t)b * 4};
+    const cuuint32_t boxG[2] = {32, 32};
+    a.tma_store = enc(&mapG, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, G, gdimG, gstrideG, boxG,
+                      estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+
   if (mode == 1) {
     cudaError_t e = cudaFuncSetAttribute(gram_tc_kernel<1>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = a.ntiles < c.num_sms ? a.ntiles : c.num_sms;
-    gram_tc_kernel<1><<<grid, kThreads, kSmemBytes, c.stream>>>(map, a);
+    gram_tc_kernel<1><<<grid, kThreads, kSmemBytes, c.stream>>>(map, mapG, a);
     ++c.launches;
     return cudaGetLastError();
   }
@@ -779,9 +859,9 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
   const int clusters = a.ntiles < max_clusters ? a.ntiles : max_clusters;
   cfg.gridDim = dim3(2 * (unsigned)clusters);
   if (mode == 0)
-    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel, map, a);
+    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel, map, mapG, a);
   else
-    e = cudaLaunchKernelEx(&cfg, gram_tc_kernel<2>, map, a);
+    e = cudaLaunchKernelEx(&cfg, gram_tc_kernel<2>, map, mapG, a);
   ++c.launches;
   return e;
 }

@@ -90,33 +90,44 @@ __global__ void __launch_bounds__(256) gather_kernel(
   if (live) {
     const uint16_t* xr = X + (int64_t)(valid ? row : 0) * ld;
     uint16_t* yr = Y + p * ldY;
-#pragma unroll 4
-    for (int64_t v = g; v < nvec; v += G) {
-      const int64_t c0 = v * 8;
-      uint4 q = make_uint4(0, 0, 0, 0);
-      if (valid) q = __ldg(reinterpret_cast<const uint4*>(xr + c0));
-      uint32_t parts[4] = {q.x, q.y, q.z, q.w};
-      float wv[8];
-      if (w_vec && c0 + 8 <= n) {
-        const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + c0));
-        const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + c0 + 4));
-        wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
-        wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
-      } else {
+    // kBatch 16-byte loads of the row are issued before any of them is used.
+    constexpr int kBatch = 8;
+    for (int64_t v0 = g; v0 < nvec; v0 += (int64_t)G * kBatch) {
+      uint4 qv[kBatch];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) wv[e] = c0 + e < n ? __ldg(w + c0 + e) : 0.0f;
+      for (int u = 0; u < kBatch; ++u) {
+        const int64_t v = v0 + (int64_t)u * G;
+        qv[u] = (valid && v < nvec) ? __ldg(reinterpret_cast<const uint4*>(xr + v * 8))
+                                    : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int64_t c = c0 + 2 * h;
-        uint32_t lo = parts[h] & 0xFFFFu, hi = parts[h] >> 16;
-        if (c >= n) lo = 0;
-        if (c + 1 >= n) hi = 0;
-        parts[h] = lo | (hi << 16);
-        if (c < n) acc = fmaf(bf16_bits_to_float(lo), wv[2 * h], acc);
-        if (c + 1 < n) acc = fmaf(bf16_bits_to_float(hi), wv[2 * h + 1], acc);
+      for (int u = 0; u < kBatch; ++u) {
+        const int64_t v = v0 + (int64_t)u * G;
+        if (v >= nvec) break;
+        const int64_t c0 = v * 8;
+        uint32_t parts[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+        float wv[8];
+        if (w_vec && c0 + 8 <= n) {
+          const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + c0));
+          const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + c0 + 4));
+          wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
+          wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) wv[e] = c0 + e < n ? __ldg(w + c0 + e) : 0.0f;
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int64_t c = c0 + 2 * h;
+          uint32_t lo = parts[h] & 0xFFFFu, hi = parts[h] >> 16;
+          if (c >= n) lo = 0;
+          if (c + 1 >= n) hi = 0;
+          parts[h] = lo | (hi << 16);
+          if (c < n) acc = fmaf(bf16_bits_to_float(lo), wv[2 * h], acc);
+          if (c + 1 < n) acc = fmaf(bf16_bits_to_float(hi), wv[2 * h + 1], acc);
+        }
+        *reinterpret_cast<uint4*>(yr + c0) = make_uint4(parts[0], parts[1], parts[2], parts[3]);
       }
-      *reinterpret_cast<uint4*>(yr + c0) = make_uint4(parts[0], parts[1], parts[2], parts[3]);
     }
   }
   for (int off = G >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);

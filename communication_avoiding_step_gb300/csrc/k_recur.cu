@@ -16,6 +16,9 @@
 //    j and compute far_j = sum_{t<j-B} G_{j,t} alpha_t for their rows, streaming G with
 //    coalesced float4 reads; they wait on alpha_t the same way.  far_j is needed only B
 //    phases after its last input is known, so most of G is read off the critical path.
+//    After the far units, the same queue hands out the first stage of the weight update
+//    (step a8) when it is fused here: partial rows of Y^T alpha, each waiting on the
+//    alpha of its own rows.
 // Synchronisation is through the data: the gather kernel fills alpha and far with
 // kAlphaPending before this kernel runs, and a value is final once it differs from
 // that pattern (32-bit stores are single-copy atomic, and a reader uses only the value
@@ -43,6 +46,11 @@ struct RecArgs {
   float* alpha;
   float* far;
   uint64_t* trace;  // [kMaxS][4] timestamps of chain CTA 0, warp 0
+  // fused first stage of the weight update (upd_units > 0): partial rows of Y^T alpha
+  const uint16_t* Y;
+  float* part;
+  int64_t ldY;
+  int upd_units, TV;
   Ctrl* ctrl;
   uint64_t timeout_ns;
   int b, s, loss, U, Uc, C, B, bulk_units;
@@ -109,36 +117,44 @@ __device__ bool wait_value(const float* p, float& v, const RecArgs& a, uint32_t 
 
 // ------------------------------------------------------------------ chain role
 // A warp per row; a lane's columns are lane*4 + 128k.  Chain CTA c owns the 8-row
-// groups c, c+C, ... of every block.
+// groups c, c+C, ... of every block.  The band is kB blocks wide; register slot
+// (tb, k) holds band block j-1-tb at columns lane*4 + 128k, so every slot index is a
+// compile-time constant (kKB = kPrefetch / kB slots per block).
+template <int kB>
 __device__ void chain_role(const RecArgs& a, int c) {
+  constexpr int kKB = kPrefetch / kB;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nk = a.vec4 ? (a.b + 127) / 128 : 0;  // float4 slots per band block
+  const int nk = (a.b + 127) / 128;  // float4 slots per band block (vec4 path)
   // Chain CTA 0, warp 0 keeps a per-phase timeline (globaltimer ns): phase start, loads
   // issued, alpha_{j-1} and far_j arrived, alpha_j stored.
   const bool tracer = (c == 0 && threadIdx.x == 0);
   for (int j = 0; j < a.s; ++j) {
     if (tracer) a.trace[4 * j] = globaltimer_ns();
-    const int t0 = j - a.B > 0 ? j - a.B : 0;
-    const int nq = nk * (j - t0);       // band slots, t ascending then column ascending
-    const int nq_old = nk * (j - 1 - t0 > 0 ? j - 1 - t0 : 0);  // slots with t < j-1
-    const bool has_far = j >= a.B + 1;
+    const int t0 = j - kB > 0 ? j - kB : 0;
+    const int nb = j - t0;             // band blocks this phase (the last is t = j-1)
+    const bool has_far = j >= kB + 1;
     for (int grp = c; grp < a.Uc; grp += a.C) {
       const int i = grp * kChainRows + warp;  // row within block j
       if (i >= a.b) continue;                 // warp-uniform
       const int64_t p = (int64_t)j * a.b + i;
       const float* grow0 = a.G + (int64_t)i * a.b;
-      // (a) loads that do not need alpha_{j-1}
-      float4 gv[kPrefetch], av[kPrefetch];
+      // (a) loads that do not need alpha_{j-1}.  Slot row tb holds band block
+      // t = j-1-tb (tb < nb): row 0 is the block waited on, rows >= 1 are complete.
+      float4 gv[kB][kKB], av[kB][kKB];
 #pragma unroll
-      for (int q = 0; q < kPrefetch; ++q) {
-        gv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-        av[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (q < nq) {
-          const int t = t0 + q / nk, col = lane * 4 + 128 * (q % nk);
-          if (col < a.b) {
-            gv[q] = __ldg(reinterpret_cast<const float4*>(grow0 + packed_offset(j, t, a.b, a.diag) + col));
-            if (q < nq_old)  // seen complete by this lane in the previous phase
-              av[q] = __ldcg(reinterpret_cast<const float4*>(a.alpha + (int64_t)t * a.b + col));
+      for (int tb = 0; tb < kB; ++tb) {
+        const int t = j - 1 - tb;
+        const bool in_band = tb < nb;
+        const float* gb = grow0 + (in_band ? packed_offset(j, t, a.b, a.diag) : 0) + lane * 4;
+        const float* ab = a.alpha + (int64_t)(in_band ? t : 0) * a.b + lane * 4;
+#pragma unroll
+        for (int k = 0; k < kKB; ++k) {
+          gv[tb][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          av[tb][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (a.vec4 && in_band && lane * 4 + 128 * k < a.b) {
+            gv[tb][k] = __ldg(reinterpret_cast<const float4*>(gb + 128 * k));
+            if (tb >= 1)  // seen complete by this lane in an earlier phase
+              av[tb][k] = __ldcg(reinterpret_cast<const float4*>(ab + 128 * k));
           }
         }
       }
@@ -149,17 +165,16 @@ __device__ void chain_role(const RecArgs& a, int c) {
         yj = a.yY[p];
       }
       if (tracer) a.trace[4 * j + 1] = globaltimer_ns();
-      // (b) alpha_{j-1} and far_j: load them until none is pending
-      const float* aprev = a.alpha + (int64_t)(j - 1) * a.b;
+      // (b) alpha_{j-1} (slot row 0) and far_j: load them until none is pending
+      const float* aprev = a.alpha + (int64_t)(j - 1) * a.b + lane * 4;
       bool pend = false;
       float farv = 0.0f;
       if (a.vec4 && j > 0) {
 #pragma unroll
-        for (int q = 0; q < kPrefetch; ++q) {
-          const int col = lane * 4 + 128 * (q % nk);
-          if (q >= nq_old && q < nq && col < a.b) {
-            av[q] = ld_volatile_f4(aprev + col);
-            pend |= pending4(av[q]);
+        for (int k = 0; k < kKB; ++k) {
+          if (lane * 4 + 128 * k < a.b) {
+            av[0][k] = ld_volatile_f4(aprev + 128 * k);
+            pend |= pending4(av[0][k]);
           }
         }
       }
@@ -175,11 +190,10 @@ __device__ void chain_role(const RecArgs& a, int c) {
           pend = false;
           if (a.vec4 && j > 0) {
 #pragma unroll
-            for (int q = 0; q < kPrefetch; ++q) {
-              const int col = lane * 4 + 128 * (q % nk);
-              if (q >= nq_old && q < nq && col < a.b && pending4(av[q])) {
-                av[q] = ld_volatile_f4(aprev + col);
-                pend |= pending4(av[q]);
+            for (int k = 0; k < kKB; ++k) {
+              if (lane * 4 + 128 * k < a.b && pending4(av[0][k])) {
+                av[0][k] = ld_volatile_f4(aprev + 128 * k);
+                pend |= pending4(av[0][k]);
               }
             }
           }
@@ -196,11 +210,16 @@ __device__ void chain_role(const RecArgs& a, int c) {
       float acc = 0.0f;
       if (a.vec4) {
 #pragma unroll
-        for (int q = 0; q < kPrefetch; ++q)
-          if (q < nq) acc = dot4(gv[q], av[q], acc);
-        for (int q = kPrefetch; q < nq; ++q) {  // beyond the register budget
-          const int t = t0 + q / nk, col = lane * 4 + 128 * (q % nk);
-          if (col < a.b) {
+        for (int tb = 0; tb < kB; ++tb)
+#pragma unroll
+          for (int k = 0; k < kKB; ++k)
+            if (tb < nb) acc = dot4(gv[tb][k], av[tb][k], acc);
+        // columns beyond the register slots (b > 128 * kKB)
+        for (int tb = 0; tb < nb; ++tb) {
+          const int t = j - 1 - tb;
+          for (int k = kKB; k < nk; ++k) {
+            const int col = lane * 4 + 128 * k;
+            if (col >= a.b) break;
             const float* src = a.alpha + (int64_t)t * a.b + col;
             float4 v = ld_volatile_f4(src);
             if (pending4(v)) {
@@ -234,6 +253,67 @@ __device__ void chain_role(const RecArgs& a, int c) {
   }
 }
 
+// --------------------------------------------------------------- update units
+// Step a8's first stage, fused: unit u sums alpha_i * Y_i over rows
+// [S*u/P, S*(u+1)/P) into part[u][:], exactly the partition of the separate update
+// kernel, once the alpha of those rows are final.  One 16-byte column vector per
+// thread (ldY <= 2048); TR row-lanes x TV vector-lanes, rows taken four at a time.
+__device__ void update_unit(const RecArgs& a, int u) {
+  __shared__ float red[2048];
+  const int64_t S = (int64_t)a.b * a.s;
+  const int64_t nvec = a.ldY / 8;
+  const int TV = a.TV, TR = 256 / TV;
+  const int tv = threadIdx.x % TV, tr = threadIdx.x / TV;
+  const int64_t r_lo = S * u / a.upd_units;
+  const int64_t r_hi = S * (u + 1) / a.upd_units;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  bool ok = true;
+  for (int64_t i0 = r_lo + tr; i0 < r_hi && ok; i0 += (int64_t)TR * 4) {
+    float al[4];
+    uint4 q[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t i = i0 + (int64_t)k * TR;
+      const bool in = i < r_hi;
+      al[k] = in ? ld_volatile_f32(a.alpha + i) : 0.0f;
+      q[k] = (in && tv < nvec) ? __ldg(reinterpret_cast<const uint4*>(a.Y + i * a.ldY + tv * 8))
+                               : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (pending1(al[k])) {  // this row's alpha is not final yet
+        const uint64_t t_start = globaltimer_ns();
+        while (pending1(al[k]) && ok) {
+          __nanosleep(200);
+          al[k] = ld_volatile_f32(a.alpha + i0 + (int64_t)k * TR);
+          if (pending1(al[k])) ok = keep_waiting(a, t_start, where_code(4, 0));
+        }
+      }
+      const uint32_t pw[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        acc[2 * h] = fmaf(al[k], bf16_bits_to_float(pw[h] & 0xFFFFu), acc[2 * h]);
+        acc[2 * h + 1] = fmaf(al[k], bf16_bits_to_float(pw[h] >> 16), acc[2 * h + 1]);
+      }
+    }
+  }
+  float* out = a.part + (int64_t)u * a.ldY;
+  if (TR == 1) {
+    if (tv < nvec)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) out[tv * 8 + e] = acc[e];
+    return;
+  }
+  __syncthreads();  // red may still be read by this CTA's previous unit
+  for (int e = 0; e < 8; ++e) red[tr * TV * 8 + tv * 8 + e] = acc[e];
+  __syncthreads();
+  for (int col = threadIdx.x; col < TV * 8; col += 256) {
+    float sum = 0.0f;
+    for (int q = 0; q < TR; ++q) sum += red[q * TV * 8 + col];
+    if (col < a.ldY) out[col] = sum;
+  }
+}
+
 // ------------------------------------------------------------------- bulk role
 // Unit = (block j, 16 rows); each warp owns two rows; a lane's columns are lane*4 + 128k.
 // The CTA waits as a whole: a final alpha value of phase q implies that phase q-1 is
@@ -250,13 +330,20 @@ __device__ void bulk_role(const RecArgs& a) {
   while (true) {
     if (threadIdx.x == 0) {
       int u = (int)atomicAdd(&a.ctrl->next_unit, 1u);
-      if (ld_volatile_u32(&a.ctrl->abort)) u = a.bulk_units;
+      if (ld_volatile_u32(&a.ctrl->abort)) u = a.bulk_units + a.upd_units;
       s_unit = u;
     }
     __syncthreads();
     const int unit = s_unit;
     __syncthreads();
-    if (unit >= a.bulk_units) return;
+    if (unit >= a.bulk_units) {
+      if (unit < a.bulk_units + a.upd_units) {
+        update_unit(a, unit - a.bulk_units);
+        __syncthreads();
+        continue;
+      }
+      return;
+    }
     const int j = a.B + 1 + unit / a.U;
     const int c = unit % a.U;
     const int i0 = c * kRows + warp * 2;
@@ -311,13 +398,16 @@ __device__ void bulk_role(const RecArgs& a) {
             }
           }
         } else {
-          for (int u = 0; u < nt; ++u) {
-            const float* gb = g0 + packed_offset(j, t + u, a.b, a.diag);
-            const float* al = a.alpha + (int64_t)(t + u) * a.b;
-            for (int col = lane; col < a.b; col += 32) {
-              const float v = __ldcg(al + col);
-              d0[u] = fmaf(__ldg(gb + col), v, d0[u]);
-              if (has1) d1[u] = fmaf(__ldg(gb + a.b + col), v, d1[u]);
+#pragma unroll
+          for (int u = 0; u < kT; ++u) {
+            if (u < nt) {
+              const float* gb = g0 + packed_offset(j, t + u, a.b, a.diag);
+              const float* al = a.alpha + (int64_t)(t + u) * a.b;
+              for (int col = lane; col < a.b; col += 32) {
+                const float v = __ldcg(al + col);
+                d0[u] = fmaf(__ldg(gb + col), v, d0[u]);
+                if (has1) d1[u] = fmaf(__ldg(gb + a.b + col), v, d1[u]);
+              }
             }
           }
         }
@@ -347,9 +437,10 @@ __device__ void bulk_role(const RecArgs& a) {
   }
 }
 
+template <int kB>
 __global__ void __launch_bounds__(kThreads) recur_kernel(RecArgs a) {
   if ((int)blockIdx.x < a.C)
-    chain_role(a, blockIdx.x);
+    chain_role<kB>(a, blockIdx.x);
   else
     bulk_role(a);
 }
@@ -358,7 +449,8 @@ __global__ void __launch_bounds__(kThreads) recur_kernel(RecArgs a) {
 
 cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, float* alpha,
                          float* far, uint32_t* far_done, int b, int s, float eta, int loss,
-                         uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, Ctx& c) {
+                         uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, const uint16_t* Y,
+                         int64_t ldY, float* part, int upd_units, Ctx& c) {
   RecArgs a;
   a.G = G;
   a.r = r;
@@ -376,27 +468,37 @@ cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, flo
   a.vec4 = (b % 4) == 0;
   // band width: two blocks while a chain lane can hold both in registers
   a.B = (a.vec4 && 2 * ((b + 127) / 128) <= kPrefetch) ? 2 : 1;
+  const void* fn = a.B == 2 ? (const void*)recur_kernel<2> : (const void*)recur_kernel<1>;
   a.bulk_units = s > a.B + 1 ? (s - a.B - 1) * a.U : 0;
   a.coef = -(eta / (float)b);
+  a.Y = Y;
+  a.part = part;
+  a.ldY = ldY;
+  a.upd_units = upd_units;
+  {
+    int tv = 1;
+    while (tv < ldY / 8 && tv < 256) tv <<= 1;
+    a.TV = tv;
+  }
   a.diag = (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
   a.stall_test = (flags & CASGD_FLAG_TEST_STALL) != 0;
 
   int per_sm = 0;
   cudaError_t e =
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, recur_kernel, kThreads, 0);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, 0);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorLaunchOutOfResources;
   const int64_t cap = (int64_t)per_sm * c.num_sms;
   // one chain CTA per 8-row group while that leaves room for the bulk CTAs
-  int64_t cmax = a.bulk_units > 0 ? cap / 2 : cap;
+  const int64_t queued = (int64_t)a.bulk_units + a.upd_units;  // units for non-chain CTAs
+  int64_t cmax = queued > 0 ? cap / 2 : cap;
   if (cmax < 1) cmax = 1;
   a.C = (int)(a.Uc < cmax ? a.Uc : cmax);
-  if (a.C + (a.bulk_units > 0 ? 1 : 0) > cap) return cudaErrorNotSupported;
-  int64_t grid = a.C + (int64_t)a.bulk_units;
+  if (a.C + (queued > 0 ? 1 : 0) > cap) return cudaErrorNotSupported;
+  int64_t grid = a.C + queued;
   if (grid > cap) grid = cap;
   void* args[] = {&a};
-  e = cudaLaunchCooperativeKernel((const void*)recur_kernel, dim3((unsigned)grid),
-                                  dim3(kThreads), args, 0, c.stream);
+  e = cudaLaunchCooperativeKernel(fn, dim3((unsigned)grid), dim3(kThreads), args, 0, c.stream);
   ++c.launches;
   return e;
 }

@@ -15,53 +15,55 @@ namespace casgd {
 
 namespace {
 
-constexpr int kMaxVecPerThread = 8;  // 16-byte vectors per thread: ldY <= 256*8*8
 
 // CTA p sums alpha_i * Y_i over its row range into part[p][:] (ldY floats).
-// Threads form TR row-lanes x TV vector-lanes (TV a power of two, TR = 256/TV).
+// Threads form TR row-lanes x TV vector-lanes (TV a power of two, TR = 256/TV); a thread
+// holds kV 16-byte column vectors (kV = ceil(nvec / TV), a template parameter so that
+// only the accumulators in use take registers).  kUnroll rows are loaded before any is
+// used, so several loads per thread are in flight; the FMA order per column stays
+// row-ascending.
+template <int kV>
 __global__ void __launch_bounds__(256) update_partial_kernel(
     const uint16_t* __restrict__ Y, const float* __restrict__ alpha, int64_t S, int64_t ldY,
     float* __restrict__ part, int TV) {
   extern __shared__ float red[];  // [TR][TV*8] when TR > 1
+  constexpr int kUnroll = kV <= 2 ? 4 : 2;
   const int64_t nvec = ldY / 8;
   const int TR = 256 / TV;
   const int tv = threadIdx.x % TV, tr = threadIdx.x / TV;
   const int64_t r_lo = S * blockIdx.x / gridDim.x;
   const int64_t r_hi = S * (blockIdx.x + 1) / gridDim.x;
-  float acc[kMaxVecPerThread][8];
+  float acc[kV][8];
 #pragma unroll
-  for (int v = 0; v < kMaxVecPerThread; ++v)
+  for (int v = 0; v < kV; ++v)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[v][e] = 0.0f;
 
-  // Rows are taken kUnroll at a time so that several 16-byte loads are in flight per
-  // thread; the FMA order per column stays row-ascending.
-  constexpr int kUnroll = 4;
   for (int64_t i0 = r_lo + tr; i0 < r_hi; i0 += (int64_t)TR * kUnroll) {
     float a[kUnroll];
-    const uint16_t* yr[kUnroll];
+    uint4 q[kUnroll][kV];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t i = i0 + (int64_t)u * TR;
-      a[u] = i < r_hi ? __ldg(alpha + i) : 0.0f;
-      yr[u] = Y + (i < r_hi ? i : r_lo) * ldY;
+      const bool in = i < r_hi;
+      a[u] = in ? __ldg(alpha + i) : 0.0f;
+      const uint16_t* yr = Y + (in ? i : r_lo) * ldY;
+#pragma unroll
+      for (int v = 0; v < kV; ++v) {
+        const int64_t vec = tv + (int64_t)v * TV;
+        q[u][v] = vec < nvec ? __ldg(reinterpret_cast<const uint4*>(yr + vec * 8))
+                             : make_uint4(0, 0, 0, 0);
+      }
     }
 #pragma unroll
-    for (int v = 0; v < kMaxVecPerThread; ++v) {
-      const int64_t vec = tv + (int64_t)v * TV;
-      if (vec < nvec) {
-        uint4 q[kUnroll];
+    for (int u = 0; u < kUnroll; ++u) {
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-          q[u] = __ldg(reinterpret_cast<const uint4*>(yr[u] + vec * 8));
+      for (int v = 0; v < kV; ++v) {
+        const uint32_t pw[4] = {q[u][v].x, q[u][v].y, q[u][v].z, q[u][v].w};
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const uint32_t pw[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            acc[v][2 * h] = fmaf(a[u], bf16_bits_to_float(pw[h] & 0xFFFFu), acc[v][2 * h]);
-            acc[v][2 * h + 1] = fmaf(a[u], bf16_bits_to_float(pw[h] >> 16), acc[v][2 * h + 1]);
-          }
+        for (int h = 0; h < 4; ++h) {
+          acc[v][2 * h] = fmaf(a[u], bf16_bits_to_float(pw[h] & 0xFFFFu), acc[v][2 * h]);
+          acc[v][2 * h + 1] = fmaf(a[u], bf16_bits_to_float(pw[h] >> 16), acc[v][2 * h + 1]);
         }
       }
     }
@@ -70,7 +72,7 @@ __global__ void __launch_bounds__(256) update_partial_kernel(
   float* out = part + (int64_t)blockIdx.x * ldY;
   if (TR == 1) {
 #pragma unroll
-    for (int v = 0; v < kMaxVecPerThread; ++v) {
+    for (int v = 0; v < kV; ++v) {
       const int64_t vec = tv + (int64_t)v * TV;
       if (vec < nvec)
 #pragma unroll
@@ -220,10 +222,23 @@ cudaError_t launch_update(const uint16_t* Y, const float* alpha, int64_t S, int6
   const int TV = pow2_at_least(nvec, 256);
   const int TR = 256 / TV;
   const size_t smem = TR > 1 ? (size_t)TR * TV * 8 * sizeof(float) : 0;
-  update_partial_kernel<<<upd_ctas, 256, smem, c.stream>>>(Y, alpha, S, ldY, part, TV);
+  const int64_t vpt = (nvec + TV - 1) / TV;  // <= 8 since ldY <= 16384
+  if (vpt <= 1)
+    update_partial_kernel<1><<<upd_ctas, 256, smem, c.stream>>>(Y, alpha, S, ldY, part, TV);
+  else if (vpt <= 2)
+    update_partial_kernel<2><<<upd_ctas, 256, smem, c.stream>>>(Y, alpha, S, ldY, part, TV);
+  else if (vpt <= 4)
+    update_partial_kernel<4><<<upd_ctas, 256, smem, c.stream>>>(Y, alpha, S, ldY, part, TV);
+  else
+    update_partial_kernel<8><<<upd_ctas, 256, smem, c.stream>>>(Y, alpha, S, ldY, part, TV);
   ++c.launches;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  return launch_update_reduce(part, upd_ctas, n, ldY, w, ctrl, c);
+}
+
+cudaError_t launch_update_reduce(const float* part, int upd_ctas, int64_t n, int64_t ldY,
+                                 float* w, Ctrl* ctrl, Ctx& c) {
   const unsigned blocks = (unsigned)((n + 31) / 32);
   update_reduce_kernel<<<blocks, 256, 0, c.stream>>>(part, upd_ctas, n, ldY, w, ctrl);
   ++c.launches;

@@ -28,6 +28,15 @@ W_TOL = 1e-4
 LOSS_TOL = 1e-5
 
 
+def _len_scale(n):
+    """The bars above hold for dot products up to 2048 terms (the workloads' n <= 2000).
+    Beyond that they grow linearly with n: two valid FP32 summation orders of an n-term
+    dot product differ by up to about 2 n u sum|x_k y_k| (u = 2^-24), so the difference
+    between the GPU's accumulation order and the oracle's BLAS order grows with n
+    (observed 5.4e-5 relative Frobenius for G at n = 16384)."""
+    return max(1.0, n / 2048.0)
+
+
 def _dev(p, casgd):
     X32 = torch.from_numpy(p.X).cuda()
     y = torch.from_numpy(p.y).cuda()
@@ -98,6 +107,9 @@ CASES = [
      (100, 6, 0.02)),
     ("ragged_2000x200_b136_s1", lambda: si.make_random(2000, 200, si.LOGISTIC, seed=4),
      (136, 1, 0.2)),
+    # limits: the widest feature count, and S = 65536 (recipe 4 at s = 32, packed G 8.3 GB)
+    ("max_n16384_b64_s4", lambda: si.make_random(3000, 16384, si.LSQ, seed=5), (64, 4, 0.01)),
+    ("max_S65536_recipe4_s32", lambda: si.make_problem(4, m=200_000), (2048, 32, 0.01)),
 ]
 
 
@@ -137,13 +149,13 @@ def test_outer_step_parity(gpu_lib, name, factory, override, gram):
         # a4: margins
         r_gpu = (taps.r_out.cpu().numpy().view(np.uint16).astype(np.uint32) << 16).view(np.float32)
         diff = r_gpu != ref["r"]
-        assert diff.mean() <= 0.005
+        assert diff.mean() <= 0.005 * _len_scale(p.n)
         assert np.all(np.abs(r_gpu - ref["r"]) <= _bf16_ulp(ref["r"]) + 1e-38)
         # a3: Gram, every block the kernel wrote (diagonal included)
-        G_gpu = taps.G_out.cpu().numpy()
-        if G_gpu.size <= 40_000_000:
+        if taps.G_out.numel() <= 40_000_000:
+            G_gpu = taps.G_out.cpu().numpy()
             G_ref = oracle.gram_packed(ref["Y"], b, s, diag=True, mode="emulate")
-            assert _rel(G_gpu, G_ref) <= GRAM_TOL
+            assert _rel(G_gpu, G_ref) <= GRAM_TOL * _len_scale(p.n)
         else:  # sampled blocks: first, last, and a few in between
             rng = np.random.default_rng(0)
             blocks = {(s - 1, 0), (s - 1, s - 1), (1, 0), (0, 0)}
@@ -154,13 +166,14 @@ def test_outer_step_parity(gpu_lib, name, factory, override, gram):
             for j, t in sorted(blocks):
                 o = oracle.packed_block_offset(j, t, b, True)
                 g_ref = oracle.gram_block(ref["Y"], b, j, t, "emulate").reshape(-1)
-                num += float(np.sum((G_gpu[o:o + b * b].astype(np.float64) - g_ref) ** 2))
+                g_gpu = taps.G_out[o:o + b * b].cpu().numpy().astype(np.float64)
+                num += float(np.sum((g_gpu - g_ref) ** 2))
                 den += float(np.sum(g_ref.astype(np.float64) ** 2))
-            assert math.sqrt(num / den) <= GRAM_TOL
+            assert math.sqrt(num / den) <= GRAM_TOL * _len_scale(p.n)
         # a6: alpha (diagnostic bound, looser than w because r may flip one ulp)
-        assert _rel(taps.alpha_out.cpu().numpy(), ref["alpha"]) <= 2e-3
+        assert _rel(taps.alpha_out.cpu().numpy(), ref["alpha"]) <= 2e-3 * _len_scale(p.n)
         # a8: the weights
-        assert _rel(w_gpu, ref["w"]) <= W_TOL
+        assert _rel(w_gpu, ref["w"]) <= W_TOL * _len_scale(p.n)
 
 
 def test_outer_step_given_indices_and_bad_index(gpu_lib):
