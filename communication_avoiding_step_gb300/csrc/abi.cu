@@ -145,15 +145,14 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   }
   // (The sum of G over processes would sit here; on one GPU it is the identity.)
   if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
-  // The update's first stage rides in the recurrence kernel while a thread needs one
-  // 16-byte column vector (n <= 2048); wider rows keep the separate two-kernel update.
-  const bool fuse_update = L.ldY <= 2048;
+  // The update's first stage rides in the recurrence kernel (one partial row per block,
+  // s <= 64 <= upd_ctas rows of the partial buffer); the reduce adds the s rows to w.
+  const bool fuse_update = true;
   CK(launch_recur(G, R.r, R.yY, R.alpha, R.far, R.far_done, p->b, p->s, p->eta, p->loss,
-                  p->flags, p->timeout_us, R.ctrl, R.Y, L.ldY, R.upd,
-                  fuse_update ? L.upd_ctas : 0, c));
+                  p->flags, p->timeout_us, R.ctrl, R.Y, L.ldY, R.upd, fuse_update ? 1 : 0, c));
   if ((rc = record(prof, it, 3, st)) != CASGD_OK) return rc;
   if (fuse_update)
-    CK(launch_update_reduce(R.upd, L.upd_ctas, d->n, L.ldY, w, R.ctrl, c));
+    CK(launch_update_reduce(R.upd, p->s, d->n, L.ldY, w, R.ctrl, c));
   else
     CK(launch_update(R.Y, R.alpha, L.S, d->n, L.ldY, w, R.upd, L.upd_ctas, R.ctrl, c));
   if ((rc = record(prof, it, 4, st)) != CASGD_OK) return rc;
@@ -214,7 +213,10 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms)
   L.off_Y = off;
   off += align_up((size_t)L.S * L.ldY * sizeof(uint16_t));
   L.off_upd = off;
-  off += align_up((size_t)L.upd_ctas * L.ldY * sizeof(float));
+  // partial rows: upd_ctas for the two-kernel update, s for the update fused into the
+  // recurrence (one row per block)
+  const int64_t upd_rows = L.upd_ctas > s ? L.upd_ctas : s;
+  off += align_up((size_t)upd_rows * L.ldY * sizeof(float));
   L.off_G = off;
   off += align_up((size_t)L.gram_elems * sizeof(float));
   L.total = off;

@@ -141,12 +141,12 @@ bool gram_tc_supported(int64_t S, int64_t n, int b);
 cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
                            int s, bool diag, int mode, float* G, Ctrl* ctrl,
                            uint32_t timeout_us, Ctx& c);
-// upd_units > 0 fuses the first stage of the weight update (requires ldY <= 2048):
-// part[u][:] for u < upd_units, as launch_update's first kernel would write it.
+// fuse_update != 0 fuses the first stage of the weight update: part[j][:] for each of
+// the s blocks j (s partial rows of ldY floats), to be summed by launch_update_reduce.
 cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, float* alpha,
                          float* far, uint32_t* far_done, int b, int s, float eta, int loss,
                          uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, const uint16_t* Y,
-                         int64_t ldY, float* part, int upd_units, Ctx& c);
+                         int64_t ldY, float* part, int fuse_update, Ctx& c);
 cudaError_t launch_update_reduce(const float* part, int upd_ctas, int64_t n, int64_t ldY,
                                  float* w, Ctrl* ctrl, Ctx& c);
 cudaError_t launch_update(const uint16_t* Y, const float* alpha, int64_t S, int64_t n,

@@ -17,8 +17,8 @@
 //    coalesced float4 reads; they wait on alpha_t the same way.  far_j is needed only B
 //    phases after its last input is known, so most of G is read off the critical path.
 //    After the far units, the same queue hands out the first stage of the weight update
-//    (step a8) when it is fused here: partial rows of Y^T alpha, each waiting on the
-//    alpha of its own rows.
+//    (step a8) when it is fused here: per block j and 64-column chunk, the partial row
+//    of Y^T alpha over that block, each waiting on the alpha of its own rows.
 // Synchronisation is through the data: the gather kernel fills alpha and far with
 // kAlphaPending before this kernel runs, and a value is final once it differs from
 // that pattern (32-bit stores are single-copy atomic, and a reader uses only the value
@@ -254,39 +254,43 @@ __device__ void chain_role(const RecArgs& a, int c) {
 }
 
 // --------------------------------------------------------------- update units
-// Step a8's first stage, fused: unit u sums alpha_i * Y_i over rows
-// [S*u/P, S*(u+1)/P) into part[u][:], exactly the partition of the separate update
-// kernel, once the alpha of those rows are final.  One 16-byte column vector per
-// thread (ldY <= 2048); TR row-lanes x TV vector-lanes, rows taken four at a time.
+// Step a8's first stage, fused: unit (j, cc) sums alpha_i * Y_i over the b rows of block
+// j for the 64 columns cc*64 .. cc*64+63 into part[j][...] (one partial row per block;
+// the reduce kernel then adds the s rows to w).  Threads: 32 row-lanes x 8 column
+// vectors; each waits on the alpha of its own rows.  Units of block j become workable
+// as soon as phase j is done, so only the last block's units (spread over many CTAs)
+// run after the chain ends.  Fixed order: rows ascending per row-lane, then row-lanes
+// ascending in shared memory.
 __device__ void update_unit(const RecArgs& a, int u) {
-  __shared__ float red[2048];
-  const int64_t S = (int64_t)a.b * a.s;
-  const int64_t nvec = a.ldY / 8;
-  const int TV = a.TV, TR = 256 / TV;
-  const int tv = threadIdx.x % TV, tr = threadIdx.x / TV;
-  const int64_t r_lo = S * u / a.upd_units;
-  const int64_t r_hi = S * (u + 1) / a.upd_units;
+  __shared__ float red[32][64];
+  const int nchunk = (int)((a.ldY / 8 + 7) / 8);
+  const int j = u / nchunk, cc = u - j * nchunk;
+  const int tv = threadIdx.x & 7, tr = threadIdx.x >> 3;  // vector-lane, row-lane
+  const int64_t vec = (int64_t)cc * 8 + tv;
+  const bool vin = vec < a.ldY / 8;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   bool ok = true;
-  for (int64_t i0 = r_lo + tr; i0 < r_hi && ok; i0 += (int64_t)TR * 4) {
+  for (int i0 = tr; i0 < a.b && ok; i0 += 32 * 4) {
     float al[4];
     uint4 q[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int64_t i = i0 + (int64_t)k * TR;
-      const bool in = i < r_hi;
-      al[k] = in ? ld_volatile_f32(a.alpha + i) : 0.0f;
-      q[k] = (in && tv < nvec) ? __ldg(reinterpret_cast<const uint4*>(a.Y + i * a.ldY + tv * 8))
-                               : make_uint4(0, 0, 0, 0);
+      const int i = i0 + 32 * k;
+      const bool in = i < a.b;
+      const int64_t row = (int64_t)j * a.b + i;
+      al[k] = in ? ld_volatile_f32(a.alpha + row) : 0.0f;
+      q[k] = (in && vin) ? __ldg(reinterpret_cast<const uint4*>(a.Y + row * a.ldY + vec * 8))
+                         : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       if (pending1(al[k])) {  // this row's alpha is not final yet
+        const int64_t row = (int64_t)j * a.b + i0 + 32 * k;
         const uint64_t t_start = globaltimer_ns();
         while (pending1(al[k]) && ok) {
           __nanosleep(200);
-          al[k] = ld_volatile_f32(a.alpha + i0 + (int64_t)k * TR);
-          if (pending1(al[k])) ok = keep_waiting(a, t_start, where_code(4, 0));
+          al[k] = ld_volatile_f32(a.alpha + row);
+          if (pending1(al[k])) ok = keep_waiting(a, t_start, where_code(4, j));
         }
       }
       const uint32_t pw[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
@@ -297,20 +301,16 @@ __device__ void update_unit(const RecArgs& a, int u) {
       }
     }
   }
-  float* out = a.part + (int64_t)u * a.ldY;
-  if (TR == 1) {
-    if (tv < nvec)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) out[tv * 8 + e] = acc[e];
-    return;
-  }
   __syncthreads();  // red may still be read by this CTA's previous unit
-  for (int e = 0; e < 8; ++e) red[tr * TV * 8 + tv * 8 + e] = acc[e];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[tr][tv * 8 + e] = acc[e];
   __syncthreads();
-  for (int col = threadIdx.x; col < TV * 8; col += 256) {
+  if (threadIdx.x < 64) {
+    const int col = threadIdx.x;
     float sum = 0.0f;
-    for (int q = 0; q < TR; ++q) sum += red[q * TV * 8 + col];
-    if (col < a.ldY) out[col] = sum;
+    for (int r = 0; r < 32; ++r) sum += red[r][col];
+    const int64_t c = (int64_t)cc * 64 + col;
+    if (c < a.ldY) a.part[(int64_t)j * a.ldY + c] = sum;
   }
 }
 
@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(kThreads) recur_kernel(RecArgs a) {
 cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, float* alpha,
                          float* far, uint32_t* far_done, int b, int s, float eta, int loss,
                          uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, const uint16_t* Y,
-                         int64_t ldY, float* part, int upd_units, Ctx& c) {
+                         int64_t ldY, float* part, int upd_units /* nonzero: fuse */, Ctx& c) {
   RecArgs a;
   a.G = G;
   a.r = r;
@@ -474,12 +474,9 @@ cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, flo
   a.Y = Y;
   a.part = part;
   a.ldY = ldY;
-  a.upd_units = upd_units;
-  {
-    int tv = 1;
-    while (tv < ldY / 8 && tv < 256) tv <<= 1;
-    a.TV = tv;
-  }
+  // update units: s blocks x ceil(ldY / 64) column chunks (0 = update not fused)
+  a.upd_units = upd_units ? s * (int)((ldY / 8 + 7) / 8) : 0;
+  a.TV = 0;
   a.diag = (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
   a.stall_test = (flags & CASGD_FLAG_TEST_STALL) != 0;
 
