@@ -35,8 +35,10 @@ import synth_inputs as si  # noqa: E402
 
 METRIC = "SGD samples/s per GB300 (CA-SGD); Gram TFLOP/s and % of roofline"
 STAGES = ("gather", "gram", "recurrence", "update")
-KERNEL_SOURCES = {"gram_tc": "k_gram_tc.cu", "gram_simt": "k_gram_simt.cu",
-                  "recurrence": "k_recur.cu", "update": "k_update.cu", "gather": "k_prep.cu"}
+KERNEL_SOURCES = {"gram_tc": ("k_gram_tc.cu",), "gram_simt": ("k_gram_simt.cu",),
+                  "gram_recur": ("k_gram_tc.cu", "recur_roles.cuh"),
+                  "recurrence": ("k_recur.cu", "recur_roles.cuh"), "update": ("k_update.cu",),
+                  "gather": ("k_prep.cu",)}
 
 
 def parse():
@@ -93,6 +95,15 @@ def peaks():
             "source": "fallback"}
 
 
+def source_hash(kernel: str) -> str:
+    """First 16 hex digits of the SHA-256 of the kernel's source files, concatenated."""
+    hs = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        hs.update(open(os.path.join(ROOT, "communication_avoiding_step_gb300", "csrc", f),
+                       "rb").read())
+    return hs.hexdigest()[:16]
+
+
 def traffic_for(kernel: str, cfg: int):
     """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
@@ -101,8 +112,7 @@ def traffic_for(kernel: str, cfg: int):
     d = json.load(open(path)).get(f"{kernel}@config{cfg}")
     if not d:
         return None
-    src = os.path.join(ROOT, "communication_avoiding_step_gb300", "csrc", KERNEL_SOURCES[kernel])
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    h = source_hash(kernel)
     return d["bytes_per_launch"] if d.get("source_sha256_16") == h else None
 
 
@@ -302,7 +312,9 @@ def run_ours(args):
     value = samples / elapsed
     pk = peaks()
     work = alg_work(r.n, S, s, r.b, r.m)
-    gram_name = "gram_tc" if kind == 1 else "gram_simt"
+    # kind 3: the Gram, the recurrence and the update's first stage share one launch
+    # (its time is the "gram" stage; the "recurrence" stage is then empty)
+    gram_name = {1: "gram_tc", 2: "gram_simt", 3: "gram_recur"}[kind]
     stages_out = {}
     for st in STAGES:
         t = per_launch_ms[st] / 1e3

@@ -15,7 +15,7 @@ import torch
 
 from ._native import (  # noqa: F401
     CASGD_LOGISTIC, CASGD_LSQ, CASGD_POISSON, FLAG_GRAM_MULTICAST, FLAG_GRAM_NO_CLUSTER,
-    FLAG_GRAM_PAIR,
+    FLAG_GRAM_PAIR, FLAG_NO_FUSE, FLAG_TRACE_CHAIN,
     FLAG_GRAM_SIMT,
     FLAG_GRAM_TENSOR,
     FLAG_TEST_STALL, FLAG_WRITE_DIAG_BLOCKS, STAGE_EVENTS, CasgdError, Data as _Data,
@@ -191,6 +191,17 @@ def loss_async(data: Dataset, kind: int, w: torch.Tensor, ws: torch.Tensor,
 def get_status(ws: torch.Tensor, stream=None) -> int:
     """Sticky device status of ws (0 = ok); clears it.  Blocks."""
     return int(load().casgd_get_status(_ptr(ws), _stream(stream)))
+
+
+def chain_trace(data: Dataset, params: Params, ws: torch.Tensor, stream=None) -> list:
+    """Chain timeline of the last outer iteration run with FLAG_TRACE_CHAIN: per phase
+    j, globaltimer ns (start, loads issued, inputs final, alpha_j stored), then one
+    summary row (last tile of G stored, last far sum stored, last update partial
+    stored, 0).  Blocks."""
+    out = (C.c_uint64 * (4 * params.s + 4))()
+    _check(load().casgd_chain_trace(C.byref(data.c()), C.byref(params.c()), _ptr(ws), ws.numel(),
+                                    _stream(stream), out), "casgd_chain_trace")
+    return [tuple(out[4 * j + e] for e in range(4)) for j in range(params.s + 1)]
 
 
 def update_static(Y: torch.Tensor, alpha: torch.Tensor, w: torch.Tensor, n: int,

@@ -19,6 +19,8 @@ FLAG_GRAM_SIMT = 0x4
 FLAG_GRAM_NO_CLUSTER = 0x8
 FLAG_GRAM_MULTICAST = 0x10
 FLAG_GRAM_PAIR = 0x20
+FLAG_NO_FUSE = 0x40
+FLAG_TRACE_CHAIN = 0x100
 FLAG_TEST_STALL = 0x80000000
 STAGE_EVENTS = 5
 
@@ -64,6 +66,8 @@ SIGNATURES = {
     "casgd_loss_async": (C.c_int, [_P(Data), C.c_int32, C.c_void_p, C.c_void_p, C.c_size_t,
                                    C.c_void_p, C.c_void_p]),
     "casgd_get_status": (C.c_int, [C.c_void_p, C.c_void_p]),
+    "casgd_chain_trace": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p,
+                                    C.POINTER(C.c_uint64)]),
     "casgd_update_static": (C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_int64, C.c_void_p,
                                       C.c_void_p, C.c_void_p]),
 }

@@ -26,7 +26,8 @@ struct Resolved {
   float* yY;
   float* alpha;
   float* far;
-  uint32_t* far_done;
+  uint32_t* slab;   // the paired-SM Gram's per-32-row completion counters
+  uint64_t* trace;  // the recurrence's per-phase timeline
   uint16_t* Y;
   float* G;
   float* upd;
@@ -70,7 +71,8 @@ Resolved resolve(void* ws, const Layout& L) {
   R.yY = reinterpret_cast<float*>(base + L.off_yY);
   R.alpha = reinterpret_cast<float*>(base + L.off_alpha);
   R.far = reinterpret_cast<float*>(base + L.off_far);
-  R.far_done = reinterpret_cast<uint32_t*>(base + L.off_far + align_up((size_t)L.S * sizeof(float)));
+  R.slab = reinterpret_cast<uint32_t*>(base + L.off_far + align_up((size_t)L.S * sizeof(float)));
+  R.trace = reinterpret_cast<uint64_t*>(R.slab + kMaxSlabs);
   R.Y = reinterpret_cast<uint16_t*>(base + L.off_Y);
   R.G = reinterpret_cast<float*>(base + L.off_G);
   R.upd = reinterpret_cast<float*>(base + L.off_upd);
@@ -130,27 +132,41 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
 
   if ((rc = record(prof, it, 0, st)) != CASGD_OK) return rc;
   CK(launch_gather(*d, *p, w, k, idx_in, R.idx, R.Y, L.ldY, R.r, R.yY, R.alpha, R.far, R.ctrl,
-                   R.far_done, c));
+                   R.slab, c));
   if ((rc = record(prof, it, 1, st)) != CASGD_OK) return rc;
-  if (choice == 1) {
-    // variant: forced by a flag, else CTA pairs for deep K (MMA-bound) and multicast
-    // clusters for shallow K (bound by writing G), as measured on the five workloads
-    const int mode = (p->flags & CASGD_FLAG_GRAM_NO_CLUSTER) ? 1
-                     : (p->flags & CASGD_FLAG_GRAM_MULTICAST) ? 2
-                     : (p->flags & CASGD_FLAG_GRAM_PAIR)      ? 0
-                     : (d->n >= 1024 ? 0 : 2);
-    CK(launch_gram_tc(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag, mode, G, R.ctrl, p->timeout_us, c));
-  } else {
-    CK(launch_gram_simt(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag, G, c));
-  }
-  // (The sum of G over processes would sit here; on one GPU it is the identity.)
-  if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
-  // The update's first stage rides in the recurrence kernel (one partial row per block,
+  // variant: forced by a flag; else CTA pairs with the recurrence in the same launch
+  // while the chain's rows fit one warp each on half the SMs (b <= 512); else CTA pairs
+  // for deep K (MMA-bound) and multicast clusters for shallow K (bound by writing G),
+  // as measured on the five workloads
+  const bool fuse_default = !(p->flags & CASGD_FLAG_NO_FUSE) && p->b <= 512 &&
+                            gram_recur_fused_supported(L.S, d->n, p->b);
+  const int mode = (p->flags & CASGD_FLAG_GRAM_NO_CLUSTER) ? 1
+                   : (p->flags & CASGD_FLAG_GRAM_MULTICAST) ? 2
+                   : (p->flags & CASGD_FLAG_GRAM_PAIR)      ? 0
+                   : (fuse_default || d->n >= 1024) ? 0 : 2;
+  // The update's first stage rides in the recurrence (one partial row per block,
   // s <= 64 <= upd_ctas rows of the partial buffer); the reduce adds the s rows to w.
-  const bool fuse_update = true;
-  CK(launch_recur(G, R.r, R.yY, R.alpha, R.far, R.far_done, p->b, p->s, p->eta, p->loss,
-                  p->flags, p->timeout_us, R.ctrl, R.Y, L.ldY, R.upd, fuse_update ? 1 : 0, c));
+  const bool fused = choice == 1 && mode == 0 && !(p->flags & CASGD_FLAG_NO_FUSE) &&
+                     gram_recur_fused_supported(L.S, d->n, p->b);
+  if (fused) {
+    // Gram and recurrence in one launch.  (The sum of G over processes would split it:
+    // on one GPU it is the identity.)
+    CK(launch_gram_recur(R.Y, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss, p->flags, G, R.r,
+                         R.yY, R.alpha, R.far, R.trace, R.slab, R.upd, R.ctrl, p->timeout_us, c));
+    if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
+  } else {
+    if (choice == 1)
+      CK(launch_gram_tc(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag, mode, G, R.ctrl, p->timeout_us, c));
+    else
+      CK(launch_gram_simt(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag, G, c));
+    // (The sum of G over processes would sit here; on one GPU it is the identity.)
+    if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
+    CK(launch_recur(G, R.r, R.yY, R.alpha, R.far, R.trace, p->b, p->s, p->eta, p->loss,
+                    p->flags, p->timeout_us, R.ctrl, R.Y, L.ldY, R.upd, 1, c));
+  }
+  if (prof) prof->gram_kind = fused ? 3 : choice;
   if ((rc = record(prof, it, 3, st)) != CASGD_OK) return rc;
+  const bool fuse_update = true;
   if (fuse_update)
     CK(launch_update_reduce(R.upd, p->s, d->n, L.ldY, w, R.ctrl, c));
   else
@@ -207,9 +223,9 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms)
   off += align_up((size_t)L.S * sizeof(float));
   L.off_alpha = off;
   off += align_up((size_t)L.S * sizeof(float));
-  L.off_far = off;  // far-field sums FP32[S]; kMaxS completion counters; kMaxS x 4 trace
+  L.off_far = off;  // far sums FP32[S]; kMaxSlabs row counters; (kMaxS+1) x 4 trace
   off += align_up((size_t)L.S * sizeof(float)) +
-         align_up(kMaxS * sizeof(uint32_t) + kMaxS * 4 * sizeof(uint64_t));
+         align_up(kMaxSlabs * sizeof(uint32_t) + (kMaxS + 1) * 4 * sizeof(uint64_t));
   L.off_Y = off;
   off += align_up((size_t)L.S * L.ldY * sizeof(uint16_t));
   L.off_upd = off;
@@ -364,6 +380,23 @@ int casgd_train(const casgd_data_t* data, const casgd_params_t* params, float* w
 int casgd_get_status(void* ws, void* stream) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return CASGD_ERR_WORKSPACE;
   return read_and_clear_status(static_cast<Ctrl*>(ws), static_cast<cudaStream_t>(stream));
+}
+
+int casgd_chain_trace(const casgd_data_t* data, const casgd_params_t* params, void* ws,
+                      size_t ws_bytes, void* stream, uint64_t* out) {
+  if (!out || !check_params(params) || !data || data->n < 1 || data->n > kMaxN)
+    return CASGD_ERR_ARG;
+  const Layout L = make_layout(data->n, params->b, params->s, params->flags, 0);
+  int rc = check_ws(ws, ws_bytes, L);
+  if (rc != CASGD_OK) return rc;
+  Resolved R = resolve(ws, L);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CK(cudaMemcpyAsync(out, R.trace, (size_t)params->s * 4 * sizeof(uint64_t),
+                     cudaMemcpyDeviceToHost, st));
+  CK(cudaMemcpyAsync(out + (size_t)params->s * 4, R.trace + (size_t)kMaxS * 4,
+                     4 * sizeof(uint64_t), cudaMemcpyDeviceToHost, st));
+  CK(cudaStreamSynchronize(st));
+  return CASGD_OK;
 }
 
 }  // extern "C"

@@ -5,7 +5,8 @@
 //   k_prep.cu       a1 sampling, a2 gather into Y, a4 BF16 margins; BF16 storage
 //   k_gram_simt.cu  a3 Gram on CUDA cores (any n; used for narrow n)
 //   k_gram_tc.cu    a3 Gram on tcgen05 tensor cores with TMEM accumulators and TMA
-//   k_recur.cu      a6/a7 inner recurrence: persistent chain + bulk CTAs, flag-synchronised
+//   k_recur.cu      a6/a7 inner recurrence: persistent chain + bulk CTAs, data-synchronised
+//                   (roles in recur_roles.cuh; also run inside the paired-SM Gram launch)
 //   k_update.cu     a8 weight update, a9 full-data loss
 #pragma once
 
@@ -32,6 +33,8 @@ constexpr uint32_t kAlphaPending = 0x7FA1FA11u;
 constexpr int64_t kMaxSB = 65536;
 constexpr int64_t kMaxN = 16384;
 constexpr int kLossCtas = 1024;     // upper bound on loss-kernel CTAs (partials)
+// per-32-row completion counters of the paired-SM Gram (rows padded to 256-row groups)
+constexpr int64_t kMaxSlabs = (kMaxSB + 255) / 256 * 8;
 
 // Control block at the start of the workspace (256 bytes, zeroed per step where noted).
 struct Ctrl {
@@ -41,7 +44,7 @@ struct Ctrl {
                           // recorded in `status`, so later steps fail fast.
   uint32_t next_unit;     // recurrence work queue (zeroed by the gather kernel)
   uint32_t loss_done;     // loss kernel: CTAs finished (zeroed by the loss kernel's last CTA)
-  uint32_t upd_done;      // (unused)
+  uint32_t pad_q;         // (unused)
   uint32_t diag;          // which wait timed out last: kind << 24 | block << 12 | value seen
   uint32_t pad0[2];
   uint32_t block_done[kMaxS];  // recurrence: chain CTAs done per phase (zeroed per step)
@@ -64,6 +67,19 @@ inline int64_t gram_elems(int64_t b, int64_t s, bool diag) {
 
 __host__ __device__ inline int64_t packed_offset(int64_t j, int64_t t, int64_t b, bool diag) {
   return (diag ? (j * (j + 1) / 2 + t) : (j * (j - 1) / 2 + t)) * b * b;
+}
+
+// Column tiles (256 wide) that the paired-SM Gram computes for its 256-row group g:
+// those holding a needed entry (column block < row block, or <= with the diagonal) of
+// the group's last row, which needs the most.
+__host__ __device__ inline int pair_group_tiles(int64_t S, int64_t b, bool diag, int g) {
+  int64_t last = (int64_t)g * 256 + 255;
+  if (last > S - 1) last = S - 1;
+  const int64_t jmax = last / b;
+  const int64_t lim = b * (diag ? jmax + 1 : jmax);  // columns < lim are needed
+  const int64_t tc = (S + 255) / 256;
+  const int64_t c = (lim + 255) / 256;
+  return (int)(c < tc ? c : tc);
 }
 
 // ------------------------------------------------------------------ device helpers
@@ -134,7 +150,7 @@ cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t coun
 cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const float* w,
                           uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
                           int64_t ldY, uint16_t* r, float* yY, float* alpha, float* far,
-                          Ctrl* ctrl, uint32_t* far_done, Ctx& c);
+                          Ctrl* ctrl, uint32_t* slab, Ctx& c);
 cudaError_t launch_gram_simt(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
                              int s, bool diag, float* G, Ctx& c);
 bool gram_tc_supported(int64_t S, int64_t n, int b);
@@ -144,9 +160,19 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
 // fuse_update != 0 fuses the first stage of the weight update: part[j][:] for each of
 // the s blocks j (s partial rows of ldY floats), to be summed by launch_update_reduce.
 cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, float* alpha,
-                         float* far, uint32_t* far_done, int b, int s, float eta, int loss,
+                         float* far, uint64_t* trace, int b, int s, float eta, int loss,
                          uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, const uint16_t* Y,
                          int64_t ldY, float* part, int fuse_update, Ctx& c);
+// The paired-SM Gram and the recurrence (with the fused update stage) in one launch:
+// the Gram's epilogue releases per-32-row counters `slab` (zeroed by the gather kernel)
+// that the recurrence acquires before it reads rows of G.  cudaErrorNotSupported when
+// the shape does not fit the fused kernel (the caller then launches them separately).
+bool gram_recur_fused_supported(int64_t S, int64_t n, int b);
+cudaError_t launch_gram_recur(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
+                              int s, float eta, int loss, uint32_t flags, float* G,
+                              const uint16_t* r, const float* yY, float* alpha, float* far,
+                              uint64_t* trace, uint32_t* slab, float* part, Ctrl* ctrl,
+                              uint32_t timeout_us, Ctx& c);
 cudaError_t launch_update_reduce(const float* part, int upd_ctas, int64_t n, int64_t ldY,
                                  float* w, Ctrl* ctrl, Ctx& c);
 cudaError_t launch_update(const uint16_t* Y, const float* alpha, int64_t S, int64_t n,

@@ -34,6 +34,7 @@
 #include <cstring>
 
 #include "casgd_internal.cuh"
+#include "recur_roles.cuh"
 
 namespace casgd {
 
@@ -60,6 +61,7 @@ struct TcArgs {
   bool diag;
   bool tma_store;  // b % 32 == 0: 32x32 chunks go out through a TMA tensor store
   uint64_t timeout_ns;
+  uint32_t* slab;  // recurrence in the same launch: per-32-row tile counters (else null)
 };
 
 struct SharedCtl {
@@ -231,6 +233,7 @@ __device__ __forceinline__ int cols_needed(const TcArgs& a, int ra) {
 // tile, which needs the most (the count grows with the row).
 template <int kCl>
 __device__ __forceinline__ int group_cols(const TcArgs& a, int g) {
+  if (kCl == 2) return pair_group_tiles(a.S, a.b, a.diag, g);  // the count readers expect
   int last = kCl * g + kCl - 1;
   if (last > a.TR - 1) last = a.TR - 1;
   return cols_needed(a, last);
@@ -516,26 +519,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------ paired-SM variant
 // A 2-CTA cluster computes a 256x256 tile with tcgen05.mma.cta_group::2 (M = 256): each
 // CTA loads its own 128 rows of A and its own 128-row half of B, so a stage costs a CTA
-// 32 KB of shared memory (six stages fit) and 32 KB of L2 reads for 128x256x64 of MMA
-// work.  The leader CTA (rank 0) issues the MMAs; its full barrier receives both CTAs'
-// copies (cta_group::2 TMA signals the leader's barrier); each commit multicasts to the
+// 32 KB of shared memory and 32 KB of L2 reads for 128x256x64 of MMA work.  The leader
+// CTA (rank 0) issues the MMAs; its full barrier receives both CTAs' copies
+// (cta_group::2 TMA signals the leader's barrier); each commit multicasts to the
 // barriers of both CTAs; each CTA's TMEM holds its 128 rows of the accumulator and its
 // own epilogue warps store them.  Every tcgen05 operation of this kernel, the TMEM
 // allocation included, uses cta_group::2.
-constexpr int kStages2 = 6;                      // 6 x 32 KB + 32 KB output staging
+//
+// With kRecV > 0 the same launch also runs the inner recurrence (recur_roles.cuh) on
+// eight more warps per CTA (warps 6-13; kRecV: the chain's register layout, see
+// chain_variant).  After the stores of a tile are complete, each epilogue warp releases
+// the counter of its 32 rows, and the recurrence acquires the counters of the rows it
+// reads.  Row groups are visited in increasing order, so phase j of the recurrence can
+// start as soon as block row j of G is stored instead of after the whole Gram.  The
+// Gram warps never wait on the recurrence, so the Gram always completes; the
+// recurrence needs every CTA resident (the grid is the number of co-resident clusters).
 constexpr int kHalfB = 128 * BK * 2;              // 16 KB
 constexpr int kStageBytes2 = kABytes + kHalfB;    // 32 KB per CTA per stage
-constexpr size_t kSmemBytes2 = (size_t)kStages2 * kStageBytes2 + kOutBytes + 1024 + 1024;
-static_assert(kSmemBytes2 <= 232448, "dynamic shared memory per CTA");
+constexpr int kStagesPair = 6;                    // Gram alone: 6 x 32 KB + 32 KB staging
+constexpr int kStagesFused = 5;                   // with the recurrence's shared memory
+template <int kSt>
+constexpr size_t pair_smem_bytes() {
+  return (size_t)kSt * kStageBytes2 + kOutBytes + 1024 + 1024;
+}
+static_assert(pair_smem_bytes<kStagesPair>() <= 232448, "dynamic shared memory per CTA");
+static_assert(pair_smem_bytes<kStagesFused>() + 9 * 1024 <= 232448, "with the recurrence");
+constexpr int kFusedThreads = kThreads + kRecThreads;  // 6 Gram warps + 8 recurrence warps
 constexpr uint32_t kIdesc2 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                              ((uint32_t)(256 >> 4) << 24);
 
+template <int kSt>
 struct SharedCtl2 {
-  uint64_t full[kStages2];   // leader: both CTAs' copies of a stage have landed
-  uint64_t empty[kStages2];  // both CTAs: the leader's MMAs have read a stage
-  uint64_t tfull[2];         // both CTAs: accumulator buffer complete
-  uint64_t tempty[2];        // leader: both CTAs' epilogues done with a buffer (8 warps)
-  uint64_t drain;            // leader: every MMA complete
+  uint64_t full[kSt];   // leader: both CTAs' copies of a stage have landed
+  uint64_t empty[kSt];  // both CTAs: the leader's MMAs have read a stage
+  uint64_t tfull[2];    // both CTAs: accumulator buffer complete
+  uint64_t tempty[2];   // leader: both CTAs' epilogues done with a buffer (8 warps)
+  uint64_t drain;       // leader: every MMA complete
   uint32_t tmem_base;
   volatile uint32_t abort;
 };
@@ -580,7 +599,18 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
                : "memory");
 }
 
-__device__ bool mbar_wait2(uint64_t* bar, uint32_t parity, SharedCtl2* sc, const TcArgs& a) {
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait; a timeout also raises the workspace abort word at once, so waiters of
+// the recurrence (same launch or later) stop instead of running into their own bounds.
+template <int kSt>
+__device__ bool mbar_wait2(uint64_t* bar, uint32_t parity, SharedCtl2<kSt>* sc, const TcArgs& a) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -589,26 +619,28 @@ __device__ bool mbar_wait2(uint64_t* bar, uint32_t parity, SharedCtl2* sc, const
     if (globaltimer_ns() - t0 > a.timeout_ns) {
       sc->abort = 1;
       atomicOr(&a.ctrl->status, ST_TIMEOUT);
+      atomicExch(&a.ctrl->abort, 1u);
       return false;
     }
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int kSt, int kRecV>
+__global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
     gram_tc2sm_kernel(const __grid_constant__ CUtensorMap tmY,
-                      const __grid_constant__ CUtensorMap tmG, TcArgs a) {
+                      const __grid_constant__ CUtensorMap tmG, TcArgs a, RecArgs rec) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
-  uint8_t* out_stage = smem + (size_t)kStages2 * kStageBytes2;  // 1024-aligned
-  SharedCtl2* sc = reinterpret_cast<SharedCtl2*>(out_stage + kOutBytes);
+  uint8_t* out_stage = smem + (size_t)kSt * kStageBytes2;  // 1024-aligned
+  SharedCtl2<kSt>* sc = reinterpret_cast<SharedCtl2<kSt>*>(out_stage + kOutBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)cluster_rank();
   const bool leader = rank == 0;
-  const int cid = blockIdx.x / 2, ncl = gridDim.x / 2;
+  const int cid = (int)blockIdx.x / 2, ncl = (int)gridDim.x / 2;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages2; ++i) {
+    for (int i = 0; i < kSt; ++i) {
       mbar_init(&sc->full[i], 1);
       mbar_init(&sc->empty[i], 1);
     }
@@ -651,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t bar = mapa_rank(smem_u32(&sc->full[stage]), 0);
           tma_load_2d_pair(smem_u32(sa), &tmY, bar, kb * BK, ra * BM);
           tma_load_2d_pair(smem_u32(sb), &tmY, bar, kb * BK, ca * BN + rank * (BN / 2));
-          if (++stage == kStages2) {
+          if (++stage == kSt) {
             stage = 0;
             phase ^= 1u;
           }
@@ -686,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           (kb > 0 || kk > 0) ? 1u : 0u);
           any = true;
           mma_commit_pair(&sc->empty[stage], 0x3);
-          if (++stage == kStages2) {
+          if (++stage == kSt) {
             stage = 0;
             phase ^= 1u;
           }
@@ -701,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
+  } else if (warp < 6) {
     // ---------------------------------------------------------- epilogue (both CTAs)
     const int quarter = warp & 3;
     uint8_t* stage = out_stage + (warp - 2) * kStageOut;
@@ -724,9 +756,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_rank(smem_u32(&sc->tempty[acc]), 0));
+      if (kRecV) {
+        // publish this warp's 32 rows of the tile: its stores are complete and visible
+        if (a.tma_store) {
+          if (lane == 0) {
+            bulk_wait_all();
+            fence_proxy_async_global();
+          }
+        } else {
+          __threadfence();
+        }
+        __syncwarp();
+        if (lane == 0) {
+          red_release_add(a.slab + (int64_t)ra * 4 + quarter, 1u);
+          stamp_last(rec.trace, 0);
+        }
+      }
     }
     if (lane == 0) bulk_wait_all();  // this warp's tensor stores are complete
     __syncwarp();
+  } else if (kRecV) {
+    // ---------------------------------------------------------- recurrence (warps 6-13)
+    // the first C CTAs run chain groups, the others the bulk role
+    const int rt = threadIdx.x - kThreads;
+    if ((int)blockIdx.x < rec.C)
+      chain_role<kRecV == 1 ? 1 : 2, kRecV == 1 ? 8 : (kRecV == 2 ? 4 : 2), true>(
+          rec, blockIdx.x, rt);
+    else
+      bulk_role<true>(rec, rt);
   }
 
   tc_fence_before();
@@ -766,22 +823,27 @@ bool gram_tc_supported(int64_t S, int64_t n, int b) {
   return S >= 1 && n >= 1 && b >= 1 && S <= kMaxSB && n <= kMaxN;
 }
 
-cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b, int s,
-                           bool diag, int mode, float* G, Ctrl* ctrl, uint32_t timeout_us,
-                           Ctx& c) {
+namespace {
+
+struct TcPlan {
+  TcArgs a;
+  CUtensorMap map, mapG;
+};
+
+// Tensor maps and tile counts shared by every variant.  kcl: CTAs per row group.
+cudaError_t plan_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b, int s,
+                    bool diag, int kcl, float* G, Ctrl* ctrl, uint32_t timeout_us, TcPlan& P) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  CUtensorMap map;
   const cuuint64_t gdim[2] = {(cuuint64_t)n, (cuuint64_t)S};
   const cuuint64_t gstride[1] = {(cuuint64_t)ldY * 2};
   const cuuint32_t box[2] = {BK, BM};
   const cuuint32_t estride[2] = {1, 1};
-  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(Y), gdim, gstride,
+  if (enc(&P.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(Y), gdim, gstride,
           box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-
-  TcArgs a;
+  TcArgs& a = P.a;
   a.G = G;
   a.ctrl = ctrl;
   a.S = S;
@@ -792,14 +854,14 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
   a.TC = (int)((S + BN - 1) / BN);
   a.diag = diag;
   a.timeout_ns = (uint64_t)(timeout_us ? timeout_us : 1000000u) * 1000ull;
-  if (S <= 0) return cudaSuccess;
-  // mode 0: paired-SM MMA (default); 1: one CTA per tile; 2: 2-CTA clusters sharing B
-  // by multicast.  A single row tile always runs on one CTA.
-  if (a.TR <= 1) mode = 1;
-  const int kcl = mode == 1 ? 1 : 2;
+  a.slab = nullptr;
   // count the needed tiles on the host with the same rule the kernel walks
   int64_t total = 0;
   for (int g = 0; g * kcl < a.TR; ++g) {
+    if (kcl == 2) {
+      total += pair_group_tiles(S, b, diag, g);
+      continue;
+    }
     int last = g * kcl + kcl - 1;
     if (last > a.TR - 1) last = a.TR - 1;
     int64_t lr = (int64_t)last * BM + BM - 1;
@@ -810,58 +872,133 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
     total += cc < a.TC ? cc : a.TC;
   }
   a.ntiles = (int)total;
-  if (a.ntiles == 0) return cudaSuccess;
 
   // Output map: the packed G viewed as (blocks * b) rows of b FP32 columns; 32x32 boxes.
-  CUtensorMap mapG;
-  memset(&mapG, 0, sizeof(mapG));
+  memset(&P.mapG, 0, sizeof(P.mapG));
   a.tma_store = false;
-  if (b % 32 == 0) {
-    const int64_t nblk = diag ? (int64_t)s * (s + 1) / 2 : (int64_t)s * (s - 1) / 2;
+  const int64_t nblk = diag ? (int64_t)s * (s + 1) / 2 : (int64_t)s * (s - 1) / 2;
+  if (b % 32 == 0 && nblk > 0) {
     const cuuint64_t gdimG[2] = {(cuuint64_t)b, (cuuint64_t)(nblk * b)};
     const cuuint64_t gstrideG[1] = {(cuuint64_t)b * 4};
     const cuuint32_t boxG[2] = {32, 32};
-    a.tma_store = enc(&mapG, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, G, gdimG, gstrideG, boxG,
+    a.tma_store = enc(&P.mapG, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, G, gdimG, gstrideG, boxG,
                       estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_NONE,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   }
+  return cudaSuccess;
+}
 
-  if (mode == 1) {
-    cudaError_t e = cudaFuncSetAttribute(gram_tc_kernel<1>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    const int grid = a.ntiles < c.num_sms ? a.ntiles : c.num_sms;
-    gram_tc_kernel<1><<<grid, kThreads, kSmemBytes, c.stream>>>(map, mapG, a);
-    ++c.launches;
-    return cudaGetLastError();
-  }
-  const void* fn = mode == 0 ? (const void*)gram_tc2sm_kernel : (const void*)gram_tc_kernel<2>;
-  const size_t smem = mode == 0 ? kSmemBytes2 : kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+cudaLaunchConfig_t cluster2_config(unsigned threads, size_t smem, cudaStream_t st,
+                                   cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
-  cfg.stream = c.stream;
+  cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cfg;
+}
+
+}  // namespace
+
+cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b, int s,
+                           bool diag, int mode, float* G, Ctrl* ctrl, uint32_t timeout_us,
+                           Ctx& c) {
+  if (S <= 0) return cudaSuccess;
+  // mode 0: paired-SM MMA (default); 1: one CTA per tile; 2: 2-CTA clusters sharing B
+  // by multicast.  A single row tile always runs on one CTA.
+  if ((S + BM - 1) / BM <= 1) mode = 1;
+  const int kcl = mode == 1 ? 1 : 2;
+  TcPlan P;
+  cudaError_t e = plan_tc(Y, S, n, ldY, b, s, diag, kcl, G, ctrl, timeout_us, P);
+  if (e != cudaSuccess) return e;
+  TcArgs& a = P.a;
+  if (a.ntiles == 0) return cudaSuccess;
+
+  if (mode == 1) {
+    e = cudaFuncSetAttribute(gram_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = a.ntiles < c.num_sms ? a.ntiles : c.num_sms;
+    gram_tc_kernel<1><<<grid, kThreads, kSmemBytes, c.stream>>>(P.map, P.mapG, a);
+    ++c.launches;
+    return cudaGetLastError();
+  }
+  const void* fn = mode == 0 ? (const void*)gram_tc2sm_kernel<kStagesPair, 0>
+                             : (const void*)gram_tc_kernel<2>;
+  const size_t smem = mode == 0 ? pair_smem_bytes<kStagesPair>() : kSmemBytes;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster2_config(kThreads, smem, c.stream, attr);
   cfg.gridDim = dim3(2 * (unsigned)(c.num_sms / 2));
   int max_clusters = 0;
   if (cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg) != cudaSuccess || max_clusters < 1)
     max_clusters = c.num_sms / 2;
   const int clusters = a.ntiles < max_clusters ? a.ntiles : max_clusters;
   cfg.gridDim = dim3(2 * (unsigned)clusters);
-  if (mode == 0)
-    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel, map, mapG, a);
+  if (mode == 0) {
+    RecArgs none;
+    memset(&none, 0, sizeof(none));
+    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel<kStagesPair, 0>, P.map, P.mapG, a, none);
+  } else {
+    e = cudaLaunchKernelEx(&cfg, gram_tc_kernel<2>, P.map, P.mapG, a);
+  }
+  ++c.launches;
+  return e;
+}
+
+bool gram_recur_fused_supported(int64_t S, int64_t n, int b) {
+  // at least two row tiles (the paired kernel) and one block of G below the diagonal
+  return gram_tc_supported(S, n, b) && (S + BM - 1) / BM >= 2 && S / b >= 2;
+}
+
+cudaError_t launch_gram_recur(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
+                              int s, float eta, int loss, uint32_t flags, float* G,
+                              const uint16_t* r, const float* yY, float* alpha, float* far,
+                              uint64_t* trace, uint32_t* slab, float* part, Ctrl* ctrl,
+                              uint32_t timeout_us, Ctx& c) {
+  if (!gram_recur_fused_supported(S, n, b)) return cudaErrorNotSupported;
+  const bool diag = (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
+  TcPlan P;
+  cudaError_t e = plan_tc(Y, S, n, ldY, b, s, diag, 2, G, ctrl, timeout_us, P);
+  if (e != cudaSuccess) return e;
+  P.a.slab = slab;
+  RecArgs rec = make_rec_args(G, r, yY, alpha, far, trace, b, s, eta, loss, flags, timeout_us,
+                              ctrl, Y, ldY, part, 1);
+  rec.slab = slab;
+  const int v = chain_variant(rec);
+  const void* fn = v == 3   ? (const void*)gram_tc2sm_kernel<kStagesFused, 3>
+                   : v == 2 ? (const void*)gram_tc2sm_kernel<kStagesFused, 2>
+                            : (const void*)gram_tc2sm_kernel<kStagesFused, 1>;
+  const size_t smem = pair_smem_bytes<kStagesFused>();
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster2_config(kFusedThreads, smem, c.stream, attr);
+  cfg.gridDim = dim3(2 * (unsigned)(c.num_sms / 2));
+  int max_clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg);
+  if (e != cudaSuccess) return e;
+  // every CTA must be resident at once (the recurrence waits across CTAs); one chain
+  // group per 8-row group while at least one bulk group remains
+  if (max_clusters < 1) return cudaErrorNotSupported;
+  const int grid = 2 * max_clusters;
+  rec.C = rec.Uc < grid - 1 ? rec.Uc : grid - 1;
+  if (rec.C > grid / 2) rec.C = grid / 2;
+  if (rec.C < 1) return cudaErrorNotSupported;
+  cfg.gridDim = dim3((unsigned)grid);
+  if (v == 3)
+    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel<kStagesFused, 3>, P.map, P.mapG, P.a, rec);
+  else if (v == 2)
+    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel<kStagesFused, 2>, P.map, P.mapG, P.a, rec);
   else
-    e = cudaLaunchKernelEx(&cfg, gram_tc_kernel<2>, map, mapG, a);
+    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel<kStagesFused, 1>, P.map, P.mapG, P.a, rec);
   ++c.launches;
   return e;
 }

@@ -54,16 +54,18 @@ __global__ void __launch_bounds__(256) gather_kernel(
     const int32_t* __restrict__ idx_in, int32_t* __restrict__ idx_out,
     uint16_t* __restrict__ Y, int64_t ldY, uint16_t* __restrict__ r,
     float* __restrict__ yY, float* __restrict__ alpha, float* __restrict__ far, Ctrl* ctrl,
-    uint32_t* far_done, int s, int G) {
+    uint32_t* slab, int s, int G) {
   if (blockIdx.x == 0) {  // per-step reset of the recurrence's queue and counters
     if (threadIdx.x == 0) {
       ctrl->next_unit = 0;
       ctrl->abort = (ctrl->status & ST_TIMEOUT) ? 1u : 0u;  // stays set after a timeout
     }
-    for (int j = threadIdx.x; j < kMaxS; j += blockDim.x) {
-      ctrl->block_done[j] = 0;
-      far_done[j] = 0;
-    }
+    for (int j = threadIdx.x; j < kMaxS; j += blockDim.x) ctrl->block_done[j] = 0;
+    const int64_t nslab = (S + 255) / 256 * 8;  // the Gram's 32-row counters
+    for (int64_t j = threadIdx.x; j < nslab; j += blockDim.x) slab[j] = 0;
+    // summary row of the profiling timeline (it follows the counters)
+    uint64_t* summary = reinterpret_cast<uint64_t*>(slab + kMaxSlabs) + (int64_t)kMaxS * 4;
+    if (threadIdx.x < 4) summary[threadIdx.x] = 0;
   }
   const int lane = threadIdx.x & 31;
   const int g = lane & (G - 1);
@@ -172,14 +174,14 @@ cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t coun
 cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const float* w,
                           uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
                           int64_t ldY, uint16_t* r, float* yY, float* alpha, float* far,
-                          Ctrl* ctrl, uint32_t* far_done, Ctx& c) {
+                          Ctrl* ctrl, uint32_t* slab, Ctx& c) {
   const int64_t S = (int64_t)p.b * p.s;
   const int G = pow2_at_least(ldY / 8, 32);
   const int64_t rows_per_cta = 8 * (32 / G);
   const int64_t blocks = (S + rows_per_cta - 1) / rows_per_cta;
   gather_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>(
       static_cast<const uint16_t*>(d.X), d.y, d.m, d.n, d.ld, w, S, p.seed, k * (uint64_t)S,
-      idx_in, idx, Y, ldY, r, yY, alpha, far, ctrl, far_done, p.s, G);
+      idx_in, idx, Y, ldY, r, yY, alpha, far, ctrl, slab, p.s, G);
   ++c.launches;
   return cudaGetLastError();
 }

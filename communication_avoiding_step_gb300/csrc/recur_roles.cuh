@@ -1,0 +1,586 @@
+// Roles of the inner s-step recurrence (steps a6/a7) and of the fused first stage of
+// the weight update (a8), shared by the stand-alone recurrence kernel (k_recur.cu) and
+// the kernel that runs them beside the paired-SM Gram (k_gram_tc.cu).
+//
+// Paper: Mixed-Precision Communication-Avoiding SGD for Generalized Linear Models on
+// GPUs (abstract): the inner recurrence runs in high precision, from the BF16 margins
+// and the FP32 Gram matrix,
+//     z_j = r_j + sum_{t<j} G_{j,t} alpha_t,   alpha_j = -(eta/b) * l'(z_j, y_j).
+// alpha of one row depends only on that row's z, so rows are independent once all
+// earlier blocks are known; the s blocks form a serial chain.
+//
+// Two roles, each run by a group of 256 threads (a whole CTA in the stand-alone kernel,
+// warps 6-13 of a CTA in the fused one):
+//  * chain groups (the first C): one warp per row, 8-row groups.  Phase j of a row
+//    needs only the band  sum_{t=j-B}^{j-1} G_{j,t} alpha_t  (B = 1 or 2 blocks) on top
+//    of far_j (below).  The warp has its band rows of G in registers before it waits
+//    (loaded while it waited in the previous phase), then waits for alpha_{j-1} and
+//    far_j by loading exactly those values until none holds the pending pattern.
+//  * bulk groups take units (block j >= B+1, 16 rows) from an atomic queue in
+//    increasing j and compute far_j = sum_{t<j-B} G_{j,t} alpha_t for their rows,
+//    streaming G with coalesced float4 reads; they wait on alpha_t the same way.  far_j
+//    is needed only B phases after its last input is known, so most of G is read off
+//    the critical path.  After the far units the same queue hands out the first stage
+//    of the weight update when it is fused: per block j and 64-column chunk, the
+//    partial row of Y^T alpha over that block, each waiting on the alpha of its rows.
+// Synchronisation is through the data: the gather kernel fills alpha and far with
+// kAlphaPending before the recurrence runs, and a value is final once it differs from
+// that pattern (32-bit stores are single-copy atomic, and a reader uses only the value
+// it waited on, so no fences or counters are needed).  When the Gram runs in the same
+// launch (kFused), rows of G are additionally guarded by per-32-row counters that the
+// Gram's epilogue warps release once their stores of a tile are complete; a reader
+// acquires the counter of its rows before loading them, and loads G through L2 only.
+// Every wait is bounded by `timeout_ns`; on expiry the waiter records ST_TIMEOUT, which
+// wait gave up (Ctrl::diag) and the abort word, and every other waiter stops.  Sums
+// are taken in a fixed order (far_j over t ascending; then r + far + band), so results
+// are deterministic.
+#pragma once
+
+#include "casgd_internal.cuh"
+
+namespace casgd {
+
+constexpr int kRecThreads = 256;  // threads of one role group
+constexpr int kRecRows = 16;      // rows per bulk unit
+constexpr int kChainRows = 8;     // rows per chain group (a warp per row)
+
+struct RecArgs {
+  const float* G;
+  const uint16_t* r;
+  const float* yY;
+  float* alpha;
+  float* far;
+  uint64_t* trace;  // [kMaxS][4] timestamps of chain group 0, warp 0 (null: not traced)
+  // fused first stage of the weight update (upd_units > 0): partial rows of Y^T alpha
+  const uint16_t* Y;
+  float* part;
+  int64_t ldY;
+  int upd_units;
+  // Gram in the same launch: per-32-row completion counters of the paired-SM Gram
+  const uint32_t* slab;
+  int64_t S;
+  Ctrl* ctrl;
+  uint64_t timeout_ns;
+  int b, s, loss, U, Uc, C, B, bulk_units;
+  float coef;
+  bool diag, stall_test, vec4;
+};
+
+// Register layout of a chain lane: kB band blocks x kKB float4 slots per block.
+// 1: (1, 8) for b > 512 or b % 4 != 0; 2: (2, 4) for 256 < b <= 512; 3: (2, 2).
+inline int chain_variant(const RecArgs& a) {
+  const int nk = (a.b + 127) / 128;
+  if (a.B != 2) return 1;
+  return nk <= 2 ? 3 : 2;
+}
+
+// Fills every field but C (chosen by the launcher from its grid) and slab.
+RecArgs make_rec_args(const float* G, const uint16_t* r, const float* yY, float* alpha,
+                      float* far, uint64_t* trace, int b, int s, float eta, int loss,
+                      uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, const uint16_t* Y,
+                      int64_t ldY, float* part, int fuse_update);
+
+namespace {
+
+constexpr int kT = 4;         // bulk: blocks t handled per pass
+
+// Ctrl::diag codes: kind << 24 | block << 12 (2: chain wait, 3: bulk wait, 4: update
+// wait, 5: wait for rows of G, 6: wait for the CTA's own tiles).
+__device__ __forceinline__ uint32_t where_code(uint32_t kind, int j) {
+  return (kind << 24) | ((uint32_t)j << 12);
+}
+
+__device__ __forceinline__ float dot4(float4 g, float4 v, float acc) {
+  acc = fmaf(g.x, v.x, acc);
+  acc = fmaf(g.y, v.y, acc);
+  acc = fmaf(g.z, v.z, acc);
+  return fmaf(g.w, v.w, acc);
+}
+
+__device__ __forceinline__ bool pending1(float v) { return __float_as_uint(v) == kAlphaPending; }
+__device__ __forceinline__ bool pending4(float4 v) {
+  return pending1(v.x) || pending1(v.y) || pending1(v.z) || pending1(v.w);
+}
+
+__device__ __forceinline__ float4 ld_volatile_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.volatile.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float ld_volatile_f32(const float* p) {
+  return *reinterpret_cast<const volatile float*>(p);
+}
+
+// G is read through the read-only path when an earlier launch wrote it, and through L2
+// only when the Gram of the same launch is still writing other rows of it.
+template <bool kFused>
+__device__ __forceinline__ float4 ldG4(const float* p) {
+  if (kFused) return __ldcg(reinterpret_cast<const float4*>(p));
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+template <bool kFused>
+__device__ __forceinline__ float ldG1(const float* p) {
+  if (kFused) return __ldcg(p);
+  return __ldg(p);
+}
+
+// Barrier of one role group: the whole CTA, or named barrier 1 over warps 6-13.
+template <bool kFused>
+__device__ __forceinline__ void group_sync() {
+  if (kFused)
+    asm volatile("bar.sync 1, %0;" ::"r"(kRecThreads) : "memory");
+  else
+    __syncthreads();
+}
+
+// Profiling (tracing on): latest time an event of kind e happened (summary row of the
+// timeline: 0 last tile of G stored, 1 last far sum stored, 2 last update partial).
+__device__ __forceinline__ void stamp_last(uint64_t* trace, int e) {
+  if (trace)
+    atomicMax(reinterpret_cast<unsigned long long*>(trace + kMaxS * 4 + e),
+              (unsigned long long)globaltimer_ns());
+}
+
+// Records a timeout (status, diag, abort); returns false.
+__device__ bool give_up(const RecArgs& a, uint32_t where) {
+  atomicOr(&a.ctrl->status, ST_TIMEOUT);
+  atomicExch(&a.ctrl->diag, where);
+  atomicExch(&a.ctrl->abort, 1u);
+  return false;
+}
+
+// Bound check for a wait loop: false once the wait must end.
+__device__ __forceinline__ bool keep_waiting(const RecArgs& a, uint64_t t_start, uint32_t where) {
+  if (ld_volatile_u32(&a.ctrl->abort)) return false;
+  if (globaltimer_ns() - t_start > a.timeout_ns) return give_up(a, where);
+  return true;
+}
+
+// Scalar value wait (used where b is not a multiple of 4).
+__device__ bool wait_value(const float* p, float& v, const RecArgs& a, uint32_t where) {
+  v = ld_volatile_f32(p);
+  if (!pending1(v)) return true;
+  const uint64_t t_start = globaltimer_ns();
+  while (true) {
+    v = ld_volatile_f32(p);
+    if (!pending1(v)) return true;
+    if (!keep_waiting(a, t_start, where)) return false;
+  }
+}
+
+// Waits (acquire) until every tile of the Gram's 256-row group holding absolute row
+// `row` is stored: the counter of the row's 32-row slab reaches the group's tile count.
+__device__ bool wait_rows_of_G(const RecArgs& a, int64_t row, uint32_t where) {
+  const int64_t sl = row >> 5;
+  const uint32_t need = (uint32_t)pair_group_tiles(a.S, a.b, a.diag, (int)(sl >> 3));
+  if (ld_acquire_u32(a.slab + sl) >= need) return true;
+  const uint64_t t_start = globaltimer_ns();
+  while (true) {
+    __nanosleep(256);
+    if (ld_acquire_u32(a.slab + sl) >= need) return true;
+    if (!keep_waiting(a, t_start, where)) return false;
+  }
+}
+
+// ------------------------------------------------------------------ chain role
+// A warp per row; a lane's columns are lane*4 + 128k.  Chain group c owns the 8-row
+// groups c, c+C, ... of every block, so a warp's work is a sequence of items (phase j,
+// row i): phases ascending, then its groups.  The band is kB blocks wide; register slot
+// (tb, k) holds band block j-1-tb at columns lane*4 + 128k (k < kKB), so every slot
+// index is a compile-time constant.
+// Software pipeline: the band rows of G for the warp's next item are loaded while it
+// waits for the current item's alpha (once the Gram has stored them, when it runs in
+// the same launch), and the alpha vectors are kept in registers from item to item:
+// alpha_{j-2} of phase j is the alpha_{j-1} the warp waited for in phase j-1, and the
+// later items of a phase reuse the first item's.  So the only loads on the critical
+// path are the polls of alpha_{j-1} and far_j.  `rt` is the thread's index within the
+// role group.
+template <int kB, int kKB, bool kFused>
+__device__ void chain_role(const RecArgs& a, int c, int rt) {
+  const int warp = rt >> 5, lane = rt & 31;
+  const int nk = (a.b + 127) / 128;  // float4 slots per band block (vec4 path)
+  // With tracing on, chain group 0, warp 0 keeps a per-phase timeline (globaltimer ns):
+  // phase start, loads issued, alpha_{j-1} and far_j arrived, alpha_j stored.
+  const bool tracer = (c == 0 && rt == 0 && a.trace != nullptr);
+  // groups of this warp with a row inside the block (the last group may be partial)
+  int ng = 0;
+  for (int grp = c; grp < a.Uc; grp += a.C)
+    if (grp * kChainRows + warp < a.b) ++ng;
+  if (ng == 0) return;
+
+  // loads the band rows of G of item (j, i) into g (zeros outside the band)
+  auto load_band = [&](float4 (&g)[kB][kKB], int j, int i) {
+    const float* grow0 = a.G + (int64_t)i * a.b;
+    const int nb = j < kB ? j : kB;
+#pragma unroll
+    for (int tb = 0; tb < kB; ++tb) {
+      const float* gb = grow0 + (tb < nb ? packed_offset(j, j - 1 - tb, a.b, a.diag) : 0) + lane * 4;
+#pragma unroll
+      for (int k = 0; k < kKB; ++k) {
+        g[tb][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.vec4 && tb < nb && lane * 4 + 128 * k < a.b) g[tb][k] = ldG4<kFused>(gb + 128 * k);
+      }
+    }
+  };
+
+  float4 gv[kB][kKB], gn[kB][kKB], av[kB][kKB];
+#pragma unroll
+  for (int tb = 0; tb < kB; ++tb)
+#pragma unroll
+    for (int k = 0; k < kKB; ++k) av[tb][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  bool cur_loaded = false;  // gv holds the current item's band
+  int jprev = -1;
+  int j = 0, gi = 0;        // item: phase j, gi-th valid group of the warp
+  while (j < a.s) {
+    const int i = (c + gi * a.C) * kChainRows + warp;  // row within block j
+    const int64_t p = (int64_t)j * a.b + i;
+    const int nb = j < kB ? j : kB;  // band blocks this phase (the first is t = j-1)
+    const bool has_far = j >= kB + 1;
+    if (tracer && gi == 0) a.trace[4 * j] = globaltimer_ns();
+    if (!cur_loaded) {
+      if (kFused && j > 0) {  // this row of G is stored (block 0 reads none)
+        int ok0 = 1;
+        if (lane == 0) ok0 = wait_rows_of_G(a, p, where_code(5, j)) ? 1 : 0;
+        ok0 = __shfl_sync(0xffffffffu, ok0, 0);
+        __syncwarp();
+        if (!ok0) return;
+      }
+      load_band(gv, j, i);
+    }
+    uint32_t rbits = 0;  // converted after the wait, so the load does not stall the issue
+    float yj = 0.0f;
+    if (lane == 0) {
+      rbits = a.r[p];
+      yj = a.yY[p];
+    }
+    // the next item, and its band if its rows of G are already stored
+    int j2 = j, gi2 = gi + 1;
+    if (gi2 == ng) {
+      gi2 = 0;
+      ++j2;
+    }
+    bool next_loaded = false;
+    if (j2 < a.s && j2 > 0) {
+      const int i2 = (c + gi2 * a.C) * kChainRows + warp;
+      int ready = 1;
+      if (kFused) {
+        if (lane == 0) {
+          const int64_t sl = ((int64_t)j2 * a.b + i2) >> 5;
+          ready = ld_acquire_u32(a.slab + sl) >=
+                  (uint32_t)pair_group_tiles(a.S, a.b, a.diag, (int)(sl >> 3));
+        }
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        __syncwarp();
+      }
+      if (ready) {
+        load_band(gn, j2, i2);
+        next_loaded = true;
+      }
+    }
+    if (tracer && gi == 0) a.trace[4 * j + 1] = globaltimer_ns();
+    // alpha_{j-1} (slot row 0; polled once per phase) and far_j: load them until none
+    // is pending
+    bool pend = false;
+    const float* aprev = a.alpha + (int64_t)(j - 1) * a.b + lane * 4;
+    const bool poll_alpha = a.vec4 && j > 0 && j != jprev;
+    if (poll_alpha) {
+      if (kB == 2) {
+#pragma unroll
+        for (int k = 0; k < kKB; ++k) av[kB - 1][k] = av[0][k];  // alpha_{j-2}
+      }
+#pragma unroll
+      for (int k = 0; k < kKB; ++k) {
+        if (lane * 4 + 128 * k < a.b) {
+          av[0][k] = ld_volatile_f4(aprev + 128 * k);
+          pend |= pending4(av[0][k]);
+        }
+      }
+    }
+    float farv = 0.0f;
+    if (has_far && lane == 0) {
+      farv = ld_volatile_f32(a.far + p);
+      pend |= pending1(farv);
+    }
+    bool ok = true;
+    if (__any_sync(0xffffffffu, pend)) {
+      const uint64_t t_start = globaltimer_ns();
+      while (true) {
+        __nanosleep(32);  // eases the load on the few L2 lines every chain warp polls
+        pend = false;
+        if (poll_alpha) {
+#pragma unroll
+          for (int k = 0; k < kKB; ++k) {
+            if (lane * 4 + 128 * k < a.b && pending4(av[0][k])) {
+              av[0][k] = ld_volatile_f4(aprev + 128 * k);
+              pend |= pending4(av[0][k]);
+            }
+          }
+        }
+        if (has_far && lane == 0 && pending1(farv)) {
+          farv = ld_volatile_f32(a.far + p);
+          pend |= pending1(farv);
+        }
+        if (!__any_sync(0xffffffffu, pend)) break;
+        ok = keep_waiting(a, t_start, where_code(2, j));
+        if (!__all_sync(0xffffffffu, ok)) return;
+      }
+    }
+    if (tracer && gi == 0) a.trace[4 * j + 2] = globaltimer_ns();
+    float acc = 0.0f;
+    if (a.vec4) {
+#pragma unroll
+      for (int tb = 0; tb < kB; ++tb)
+#pragma unroll
+        for (int k = 0; k < kKB; ++k)
+          if (tb < nb) acc = dot4(gv[tb][k], av[tb][k], acc);
+      // columns beyond the register slots (b > 128 * kKB)
+      const float* grow0 = a.G + (int64_t)i * a.b;
+      for (int tb = 0; tb < nb; ++tb) {
+        const int t = j - 1 - tb;
+        for (int k = kKB; k < nk; ++k) {
+          const int col = lane * 4 + 128 * k;
+          if (col >= a.b) break;
+          const float* src = a.alpha + (int64_t)t * a.b + col;
+          float4 v = ld_volatile_f4(src);
+          if (pending4(v)) {
+            const uint64_t t_start = globaltimer_ns();
+            while (pending4(v) && (ok = keep_waiting(a, t_start, where_code(2, j)))) v = ld_volatile_f4(src);
+          }
+          acc = dot4(ldG4<kFused>(grow0 + packed_offset(j, t, a.b, a.diag) + col), v, acc);
+        }
+      }
+    } else {
+      const float* grow0 = a.G + (int64_t)i * a.b;
+      const int t0 = j - nb;
+      for (int t = t0; t < j && ok; ++t) {
+        const float* al = a.alpha + (int64_t)t * a.b;
+        const float* grow = grow0 + packed_offset(j, t, a.b, a.diag);
+        for (int col = lane; col < a.b; col += 32) {
+          float v;
+          if (!(ok = wait_value(al + col, v, a, where_code(2, j)))) break;
+          acc = fmaf(ldG1<kFused>(grow + col), v, acc);
+        }
+      }
+    }
+    if (!__all_sync(0xffffffffu, ok)) return;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0 && !(a.stall_test && j == 0)) {
+      const float z = bf16_bits_to_float(rbits) + farv + acc;
+      __stcg(a.alpha + p, a.coef * loss_deriv(a.loss, z, yj));
+    }
+    if (tracer && gi == ng - 1) a.trace[4 * j + 3] = globaltimer_ns();
+    // advance
+#pragma unroll
+    for (int tb = 0; tb < kB; ++tb)
+#pragma unroll
+      for (int k = 0; k < kKB; ++k) gv[tb][k] = gn[tb][k];
+    cur_loaded = next_loaded;
+    jprev = j;
+    j = j2;
+    gi = gi2;
+  }
+}
+
+// --------------------------------------------------------------- update units
+// Step a8's first stage, fused: unit (j, cc) sums alpha_i * Y_i over the b rows of block
+// j for the 64 columns cc*64 .. cc*64+63 into part[j][...] (one partial row per block;
+// the reduce kernel then adds the s rows to w).  Threads: 32 row-lanes x 8 column
+// vectors; each waits on the alpha of its own rows.  Units of block j become workable
+// as soon as phase j is done, so only the last block's units (spread over many groups)
+// run after the chain ends.  Fixed order: rows ascending per row-lane, then row-lanes
+// ascending in shared memory.  Y was written by an earlier launch.
+template <bool kFused>
+__device__ void update_unit(const RecArgs& a, int u, int rt) {
+  __shared__ float red[32][64];
+  const int nchunk = (int)((a.ldY / 8 + 7) / 8);
+  const int j = u / nchunk, cc = u - j * nchunk;
+  const int tv = rt & 7, tr = rt >> 3;  // vector-lane, row-lane
+  const int64_t vec = (int64_t)cc * 8 + tv;
+  const bool vin = vec < a.ldY / 8;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  bool ok = true;
+  for (int i0 = tr; i0 < a.b && ok; i0 += 32 * 4) {
+    float al[4];
+    uint4 q[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = i0 + 32 * k;
+      const bool in = i < a.b;
+      const int64_t row = (int64_t)j * a.b + i;
+      al[k] = in ? ld_volatile_f32(a.alpha + row) : 0.0f;
+      q[k] = (in && vin) ? __ldg(reinterpret_cast<const uint4*>(a.Y + row * a.ldY + vec * 8))
+                         : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (pending1(al[k])) {  // this row's alpha is not final yet
+        const int64_t row = (int64_t)j * a.b + i0 + 32 * k;
+        const uint64_t t_start = globaltimer_ns();
+        while (pending1(al[k]) && ok) {
+          __nanosleep(200);
+          al[k] = ld_volatile_f32(a.alpha + row);
+          if (pending1(al[k])) ok = keep_waiting(a, t_start, where_code(4, j));
+        }
+      }
+      const uint32_t pw[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        acc[2 * h] = fmaf(al[k], bf16_bits_to_float(pw[h] & 0xFFFFu), acc[2 * h]);
+        acc[2 * h + 1] = fmaf(al[k], bf16_bits_to_float(pw[h] >> 16), acc[2 * h + 1]);
+      }
+    }
+  }
+  group_sync<kFused>();  // red may still be read by this group's previous unit
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[tr][tv * 8 + e] = acc[e];
+  group_sync<kFused>();
+  if (rt < 64) {
+    const int col = rt;
+    float sum = 0.0f;
+    for (int r = 0; r < 32; ++r) sum += red[r][col];
+    const int64_t c = (int64_t)cc * 64 + col;
+    if (c < a.ldY) a.part[(int64_t)j * a.ldY + c] = sum;
+    if (col == 0) stamp_last(a.trace, 2);
+  }
+}
+
+// ------------------------------------------------------------------- bulk role
+// Unit = (block j, 16 rows); each warp owns two rows; a lane's columns are lane*4 + 128k.
+// The group waits as a whole: a final alpha value of phase q implies that phase q-1 is
+// complete (its row needed all of alpha_{q-1}), so thread 0 reads single values of the
+// next phases (spread over the values by CTA index, with a back-off while the next
+// phase is not done) and the group then processes every block known complete, up to kT
+// per pass with all their loads issued together, reading alpha with plain loads.  Each
+// block's dot product is summed over columns first and then added in t order, so the
+// result does not depend on timing.
+template <bool kFused>
+__device__ void bulk_role(const RecArgs& a, int rt) {
+  __shared__ int s_unit, s_lead;
+  const int warp = rt >> 5, lane = rt & 31;
+  const int probe_col = (int)((blockIdx.x * 37u) % (unsigned)a.b);
+  while (true) {
+    if (rt == 0) {
+      int u = (int)atomicAdd(&a.ctrl->next_unit, 1u);
+      if (ld_volatile_u32(&a.ctrl->abort)) u = a.bulk_units + a.upd_units;
+      s_unit = u;
+    }
+    group_sync<kFused>();
+    const int unit = s_unit;
+    group_sync<kFused>();
+    if (unit >= a.bulk_units) {
+      if (unit < a.bulk_units + a.upd_units) {
+        update_unit<kFused>(a, unit - a.bulk_units, rt);
+        group_sync<kFused>();
+        continue;
+      }
+      return;
+    }
+    const int j = a.B + 1 + unit / a.U;
+    const int c = unit % a.U;
+    const int i0 = c * kRecRows + warp * 2;
+    const bool has0 = i0 < a.b, has1 = i0 + 1 < a.b;
+    const int t_end = j - a.B;  // far_j covers t < j - B
+    float acc0 = 0.0f, acc1 = 0.0f;
+    bool ok = true;
+    for (int t = 0; t < t_end;) {
+      if (rt == 0) {
+        bool rows_ok = true;
+        if (kFused && t == 0) {  // the unit's rows of G are stored (first and last row)
+          const int64_t r0 = (int64_t)j * a.b + c * kRecRows;
+          const int last = min(c * kRecRows + kRecRows, a.b) - 1;
+          rows_ok = wait_rows_of_G(a, r0, where_code(5, j)) &&
+                    wait_rows_of_G(a, (int64_t)j * a.b + last, where_code(5, j));
+        }
+        // leading run of complete phases t, t+1, ... (at most kT and t_end - t)
+        const int lim = min(kT, t_end - t);
+        int lead = 0;
+        while (rows_ok && lead < lim &&
+               !pending1(ld_volatile_f32(a.alpha + (int64_t)(t + lead + 1) * a.b + probe_col)))
+          ++lead;
+        if (rows_ok && lead == 0) {  // wait for phase t, polling one value of phase t+1
+          const float* pv = a.alpha + (int64_t)(t + 1) * a.b + probe_col;
+          const uint64_t t_start = globaltimer_ns();
+          while (pending1(ld_volatile_f32(pv))) {
+            __nanosleep(200);
+            if (!keep_waiting(a, t_start, where_code(3, j))) break;
+          }
+          lead = pending1(ld_volatile_f32(pv)) ? 0 : 1;
+        }
+        s_lead = lead;
+      }
+      group_sync<kFused>();
+      const int nt = s_lead;
+      group_sync<kFused>();
+      if (nt == 0) { ok = false; break; }  // gave up (uniform)
+      if (has0) {
+        const float* g0 = a.G + (int64_t)i0 * a.b;
+        float d0[kT] = {0.f, 0.f, 0.f, 0.f}, d1[kT] = {0.f, 0.f, 0.f, 0.f};
+        if (a.vec4) {
+          for (int col = lane * 4; col < a.b; col += 128) {
+            float4 av[kT], x0[kT], x1[kT];
+#pragma unroll
+            for (int u = 0; u < kT; ++u) {
+              if (u < nt) {
+                const float* gb = g0 + packed_offset(j, t + u, a.b, a.diag) + col;
+                av[u] = __ldcg(reinterpret_cast<const float4*>(a.alpha + (int64_t)(t + u) * a.b + col));
+                x0[u] = ldG4<kFused>(gb);
+                x1[u] = has1 ? ldG4<kFused>(gb + a.b) : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < kT; ++u) {
+              if (u < nt) {
+                d0[u] = dot4(x0[u], av[u], d0[u]);
+                d1[u] = dot4(x1[u], av[u], d1[u]);
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < kT; ++u) {
+            if (u < nt) {
+              const float* gb = g0 + packed_offset(j, t + u, a.b, a.diag);
+              const float* al = a.alpha + (int64_t)(t + u) * a.b;
+              for (int col = lane; col < a.b; col += 32) {
+                const float v = __ldcg(al + col);
+                d0[u] = fmaf(ldG1<kFused>(gb + col), v, d0[u]);
+                if (has1) d1[u] = fmaf(ldG1<kFused>(gb + a.b + col), v, d1[u]);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kT; ++u) {
+          if (u < nt) {
+            acc0 += d0[u];
+            acc1 += d1[u];
+          }
+        }
+      }
+      t += nt;
+    }
+    if (has0) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        acc0 += __shfl_xor_sync(0xffffffffu, acc0, off);
+        acc1 += __shfl_xor_sync(0xffffffffu, acc1, off);
+      }
+      if (lane == 0 && ok) {
+        const int64_t p0 = (int64_t)j * a.b + i0;
+        __stcg(a.far + p0, acc0);
+        if (has1) __stcg(a.far + p0 + 1, acc1);
+        if (warp == 0) stamp_last(a.trace, 1);
+      }
+    }
+    group_sync<kFused>();  // every warp of the unit is done before the group claims the next
+  }
+}
+
+}  // namespace
+
+}  // namespace casgd

@@ -72,8 +72,25 @@ enum {
                                               the B tile by TMA multicast             */
 #define CASGD_FLAG_GRAM_PAIR         0x20u /* tcgen05 Gram, CTA pairs (cta_group::2,
                                               256x256 tiles).  Without a variant flag
-                                              the library takes pairs for n >= 1024
-                                              and multicast clusters below            */
+                                              the library takes pairs (sharing their
+                                              launch with the recurrence) for
+                                              b <= 512, else pairs for n >= 1024 and
+                                              multicast clusters below               */
+#define CASGD_FLAG_NO_FUSE           0x40u /* run the paired-SM Gram and the inner
+                                              recurrence as two launches.  Otherwise
+                                              they share one launch whenever the pair
+                                              variant is used (S >= 256, s >= 2): the
+                                              recurrence starts on block row j of G as
+                                              soon as the Gram has stored it; this
+                                              needs every CTA of the launch resident,
+                                              so a second fused step running on
+                                              another stream at the same time can make
+                                              both end with CASGD_ERR_TIMEOUT         */
+#define CASGD_FLAG_TRACE_CHAIN       0x100u /* profiling: the recurrence's first chain
+                                              warp records four globaltimer stamps per
+                                              phase in the workspace (see
+                                              casgd_chain_trace); off by default, as
+                                              the stamps slow that warp              */
 #define CASGD_FLAG_TEST_STALL        0x80000000u /* test only: the recurrence's first
                                               block never signals completion, so every
                                               waiter runs into its time bound and the
@@ -119,9 +136,13 @@ typedef struct {
   void** stage_events;   /* in: NULL, or cudaEvent_t handles; when given, event
                             [it*CASGD_STAGE_EVENTS + e] is recorded on `stream`
                             before stage e of outer iteration it (e = 0 gather,
-                            1 Gram, 2 recurrence, 3 update, 4 after update)     */
+                            1 Gram, 2 recurrence, 3 update, 4 after update;
+                            when the Gram and the recurrence share one launch,
+                            events 2 and 3 are both recorded after it)          */
   int32_t n_events;      /* in: length of stage_events                          */
-  int32_t gram_kind;     /* out: 1 = tcgen05 Gram kernel used, 2 = CUDA-core    */
+  int32_t gram_kind;     /* out: 1 = tcgen05 Gram kernel used, 2 = CUDA-core,
+                            3 = paired-SM tcgen05 Gram and recurrence in one
+                            launch                                              */
 } casgd_profile_t;
 #define CASGD_STAGE_EVENTS 5
 
@@ -206,6 +227,18 @@ int casgd_update_static(const void* Y, int64_t S, int64_t n, int64_t ldY,
 /* Blocks on `stream`, returns the sticky device status of ws (CASGD_OK or the
  * highest-priority CASGD_ERR_* seen) and clears it. */
 int casgd_get_status(void* ws, void* stream);
+
+/* Profiling: copies the chain timeline of the last outer iteration run with
+ * CASGD_FLAG_TRACE_CHAIN on ws (data and params as for that call) to host
+ * out[4*j + e], j < params->s: globaltimer nanoseconds when the first chain warp
+ * started phase j (e = 0), had issued its loads (1), saw alpha_{j-1} and far_j
+ * final (2) and had stored its alpha_j (3); then out[4*s + e]: when the last tile
+ * of G was stored (e = 0; only when the Gram shares the recurrence's launch), the
+ * last far sum (1) and the last fused update partial (2) were stored, 0 where none
+ * was; out[4*s + 3] = 0.  out holds 4*s + 4 values.  Blocks on `stream`.  Without
+ * the flag the stamps are stale or zero. */
+int casgd_chain_trace(const casgd_data_t* data, const casgd_params_t* params, void* ws,
+                      size_t ws_bytes, void* stream, uint64_t* out);
 
 #ifdef __cplusplus
 }

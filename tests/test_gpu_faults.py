@@ -54,6 +54,26 @@ def test_stalled_producer_times_out_and_context_survives(gpu_lib):
     assert torch.isfinite(w).all() and torch.count_nonzero(w).item() > 0
 
 
+def test_stall_in_fused_launch_times_out_and_context_survives(gpu_lib):
+    """The paired-SM Gram with the recurrence in the same launch (recipe 2 shape): the
+    Gram warps finish their tiles, every recurrence waiter runs into its bound."""
+    casgd = gpu_lib
+    p, data = _data(casgd, cid=2, m=20000)
+    r = p.recipe
+    stall = casgd.Params(r.b, r.s, r.eta, r.loss, flags=casgd.FLAG_TEST_STALL, timeout_us=20000)
+    ws = casgd.workspace(data, stall)
+    w = torch.zeros(p.n, device="cuda")
+    _, _, kind = casgd.train(data, casgd.Params(r.b, r.s, r.eta, r.loss), w, 1, ws)
+    assert kind == 3                                     # the fused launch ran
+    casgd.outer_step(data, stall, w, 0, ws)
+    assert casgd.get_status(ws) == 5                     # CASGD_ERR_TIMEOUT
+    assert casgd.get_status(ws) == 0
+    w.zero_()
+    casgd.outer_step(data, casgd.Params(r.b, r.s, r.eta, r.loss), w, 0, ws)
+    assert casgd.get_status(ws) == 0
+    assert torch.isfinite(w).all() and torch.count_nonzero(w).item() > 0
+
+
 def test_nonfinite_weights_reported(gpu_lib):
     casgd = gpu_lib
     p, data = _data(casgd, cid=5, m=5000)
