@@ -312,9 +312,10 @@ def run_ours(args):
     value = samples / elapsed
     pk = peaks()
     work = alg_work(r.n, S, s, r.b, r.m)
-    # kind 3: the Gram, the recurrence and the update's first stage share one launch
+    # kind 3/4: the Gram (4: of the next iteration), the recurrence and the update's
+    # first stage share one launch
     # (its time is the "gram" stage; the "recurrence" stage is then empty)
-    gram_name = {1: "gram_tc", 2: "gram_simt", 3: "gram_recur"}[kind]
+    gram_name = {1: "gram_tc", 2: "gram_simt", 3: "gram_recur", 4: "gram_recur"}[kind]
     stages_out = {}
     for st in STAGES:
         t = per_launch_ms[st] / 1e3

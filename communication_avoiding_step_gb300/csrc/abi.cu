@@ -30,6 +30,11 @@ struct Resolved {
   uint64_t* trace;  // the recurrence's per-phase timeline
   uint16_t* Y;
   float* G;
+  // second buffers of a multi-iteration run whose Gram runs one iteration ahead
+  uint16_t* Y2;
+  float* G2;
+  int32_t* idx2;
+  float* yY2;
   float* upd;
   double* loss_part;
   double* loss_slots;
@@ -72,9 +77,13 @@ Resolved resolve(void* ws, const Layout& L) {
   R.alpha = reinterpret_cast<float*>(base + L.off_alpha);
   R.far = reinterpret_cast<float*>(base + L.off_far);
   R.slab = reinterpret_cast<uint32_t*>(base + L.off_far + align_up((size_t)L.S * sizeof(float)));
-  R.trace = reinterpret_cast<uint64_t*>(R.slab + kMaxSlabs);
+  R.trace = timeline_of(R.slab);
   R.Y = reinterpret_cast<uint16_t*>(base + L.off_Y);
   R.G = reinterpret_cast<float*>(base + L.off_G);
+  R.Y2 = L.off_Y2 ? reinterpret_cast<uint16_t*>(base + L.off_Y2) : nullptr;
+  R.G2 = L.off_G2 ? reinterpret_cast<float*>(base + L.off_G2) : nullptr;
+  R.idx2 = L.off_idx2 ? reinterpret_cast<int32_t*>(base + L.off_idx2) : nullptr;
+  R.yY2 = L.off_yY2 ? reinterpret_cast<float*>(base + L.off_yY2) : nullptr;
   R.upd = reinterpret_cast<float*>(base + L.off_upd);
   R.loss_part = reinterpret_cast<double*>(base + L.off_loss);
   R.loss_slots = R.loss_part + kLossCtas;
@@ -102,6 +111,35 @@ int gram_choice(const casgd_params_t* p, int64_t S, int64_t n) {
   return tc_ok ? 1 : 2;
 }
 
+// Tensor-core variant (forced by a flag; else CTA pairs with the recurrence in the same
+// launch while the chain's rows fit one warp each on half the SMs, b <= 512; else CTA
+// pairs for deep K (MMA-bound) and multicast clusters for shallow K (bound by writing
+// G), as measured on the five workloads) and whether the recurrence shares its launch.
+struct GramPlan {
+  int choice;  // 1 tensor cores, 2 CUDA cores, -1 unsupported
+  int mode;    // tensor cores: 0 pairs, 1 single CTA, 2 multicast clusters
+  bool fused;  // pairs sharing their launch with the recurrence
+};
+
+GramPlan gram_plan(int64_t n, int32_t b, int32_t s, uint32_t flags) {
+  casgd_params_t p{};
+  p.b = b;
+  p.s = s;
+  p.flags = flags;
+  const int64_t S = (int64_t)b * s;
+  GramPlan g;
+  g.choice = gram_choice(&p, S, n);
+  const bool fuse_default = !(flags & CASGD_FLAG_NO_FUSE) && b <= 512 &&
+                            gram_recur_fused_supported(S, n, b);
+  g.mode = (flags & CASGD_FLAG_GRAM_NO_CLUSTER) ? 1
+           : (flags & CASGD_FLAG_GRAM_MULTICAST) ? 2
+           : (flags & CASGD_FLAG_GRAM_PAIR)      ? 0
+           : (fuse_default || n >= 1024) ? 0 : 2;
+  g.fused = g.choice == 1 && g.mode == 0 && !(flags & CASGD_FLAG_NO_FUSE) &&
+            gram_recur_fused_supported(S, n, b);
+  return g;
+}
+
 int record(casgd_profile_t* prof, int64_t it, int e, cudaStream_t st) {
   if (!prof || !prof->stage_events) return CASGD_OK;
   const int64_t i = it * CASGD_STAGE_EVENTS + e;
@@ -123,7 +161,8 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   int rc = check_ws(ws, ws_bytes, L);
   if (rc != CASGD_OK) return rc;
   Resolved R = resolve(ws, L);
-  const int choice = gram_choice(p, L.S, d->n);
+  const GramPlan gp = gram_plan(d->n, p->b, p->s, p->flags);
+  const int choice = gp.choice;
   if (choice < 0) return CASGD_ERR_UNSUPPORTED;
   const bool diag = (p->flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
   float* G = (taps && taps->G_out) ? taps->G_out : R.G;
@@ -132,27 +171,18 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
 
   if ((rc = record(prof, it, 0, st)) != CASGD_OK) return rc;
   CK(launch_gather(*d, *p, w, k, idx_in, R.idx, R.Y, L.ldY, R.r, R.yY, R.alpha, R.far, R.ctrl,
-                   R.slab, c));
+                   R.slab, GATHER_AND_MARGINS, c));
   if ((rc = record(prof, it, 1, st)) != CASGD_OK) return rc;
-  // variant: forced by a flag; else CTA pairs with the recurrence in the same launch
-  // while the chain's rows fit one warp each on half the SMs (b <= 512); else CTA pairs
-  // for deep K (MMA-bound) and multicast clusters for shallow K (bound by writing G),
-  // as measured on the five workloads
-  const bool fuse_default = !(p->flags & CASGD_FLAG_NO_FUSE) && p->b <= 512 &&
-                            gram_recur_fused_supported(L.S, d->n, p->b);
-  const int mode = (p->flags & CASGD_FLAG_GRAM_NO_CLUSTER) ? 1
-                   : (p->flags & CASGD_FLAG_GRAM_MULTICAST) ? 2
-                   : (p->flags & CASGD_FLAG_GRAM_PAIR)      ? 0
-                   : (fuse_default || d->n >= 1024) ? 0 : 2;
   // The update's first stage rides in the recurrence (one partial row per block,
   // s <= 64 <= upd_ctas rows of the partial buffer); the reduce adds the s rows to w.
-  const bool fused = choice == 1 && mode == 0 && !(p->flags & CASGD_FLAG_NO_FUSE) &&
-                     gram_recur_fused_supported(L.S, d->n, p->b);
+  const int mode = gp.mode;
+  const bool fused = gp.fused;
   if (fused) {
     // Gram and recurrence in one launch.  (The sum of G over processes would split it:
     // on one GPU it is the identity.)
-    CK(launch_gram_recur(R.Y, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss, p->flags, G, R.r,
-                         R.yY, R.alpha, R.far, R.trace, R.slab, R.upd, R.ctrl, p->timeout_us, c));
+    CK(launch_gram_recur(R.Y, G, false, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss, p->flags,
+                         G, R.Y, R.r, R.yY, R.alpha, R.far, R.slab, R.upd, w, R.ctrl,
+                         p->timeout_us, c));
     if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
   } else {
     if (choice == 1)
@@ -161,16 +191,12 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
       CK(launch_gram_simt(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag, G, c));
     // (The sum of G over processes would sit here; on one GPU it is the identity.)
     if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
-    CK(launch_recur(G, R.r, R.yY, R.alpha, R.far, R.trace, p->b, p->s, p->eta, p->loss,
-                    p->flags, p->timeout_us, R.ctrl, R.Y, L.ldY, R.upd, 1, c));
+    CK(launch_recur(G, R.r, R.yY, R.alpha, R.far, R.slab, p->b, p->s, p->eta, p->loss,
+                    p->flags, p->timeout_us, R.ctrl, R.Y, L.ldY, d->n, R.upd, w, c));
   }
   if (prof) prof->gram_kind = fused ? 3 : choice;
+  // the update (a8) finished inside the recurrence's launch
   if ((rc = record(prof, it, 3, st)) != CASGD_OK) return rc;
-  const bool fuse_update = true;
-  if (fuse_update)
-    CK(launch_update_reduce(R.upd, p->s, d->n, L.ldY, w, R.ctrl, c));
-  else
-    CK(launch_update(R.Y, R.alpha, L.S, d->n, L.ldY, w, R.upd, L.upd_ctas, R.ctrl, c));
   if ((rc = record(prof, it, 4, st)) != CASGD_OK) return rc;
 
   if (taps) {
@@ -180,6 +206,71 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
       CK(cudaMemcpyAsync(taps->r_out, R.r, L.S * sizeof(uint16_t), cudaMemcpyDeviceToDevice, st));
     if (taps->alpha_out)
       CK(cudaMemcpyAsync(taps->alpha_out, R.alpha, L.S * sizeof(float), cudaMemcpyDeviceToDevice, st));
+  }
+  return CASGD_OK;
+}
+
+// casgd_train with the paired-SM Gram sharing the recurrence's launch: the Gram of
+// iteration k+1 (whose rows are sampled ahead: only the margins need the current w)
+// runs in the launch of iteration k's recurrence, on double-buffered Y and G.  Every
+// value is computed as in outer_step_impl (same kernels' arithmetic), only the order of
+// independent work changes.  Stage events per iteration: 0 before the gather of the
+// next iteration's rows and this iteration's margins, 1 before the shared launch, 2, 3
+// and 4 after it (it ends with the update).
+int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, uint64_t k0,
+                    int32_t iters, const Layout& L, const Resolved& R, Ctx& c,
+                    casgd_profile_t* prof, int32_t loss_every, int& slot, int& flushed,
+                    double* loss_hist) {
+  uint16_t* Yb[2] = {R.Y, R.Y2};
+  float* Gb[2] = {R.G, R.G2};
+  int32_t* Ib[2] = {R.idx, R.idx2};
+  float* yb[2] = {R.yY, R.yY2};
+  const bool diag = (p->flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
+  const cudaStream_t st = c.stream;
+  int rc;
+  if (prof) prof->gram_kind = 4;
+  for (int32_t it = 0; it < iters; ++it) {
+    const int cur = it & 1, nxt = cur ^ 1;
+    const uint64_t k = k0 + (uint64_t)it;
+    if ((rc = record(prof, it, 0, st)) != CASGD_OK) return rc;
+    if (it == 0) {  // prologue: this iteration's rows and Gram
+      CK(launch_gather(*d, *p, w, k, nullptr, Ib[cur], Yb[cur], L.ldY, R.r, yb[cur], R.alpha,
+                       R.far, R.ctrl, R.slab, GATHER_ONLY, c));
+      CK(launch_gram_tc(Yb[cur], L.S, d->n, L.ldY, p->b, p->s, diag, 0, Gb[cur], R.ctrl,
+                        p->timeout_us, c));
+    }
+    if (it + 1 < iters)  // next iteration's rows (into the buffers the last launch
+                         // freed) and this iteration's margins, in one launch
+      CK(launch_gather_next_margins(*d, *p, w, k + 1, Ib[nxt], Yb[nxt], yb[nxt], Yb[cur],
+                                    L.ldY, R.r, R.alpha, R.far, R.ctrl, R.slab, c));
+    else
+      CK(launch_gather(*d, *p, w, k, nullptr, Ib[cur], Yb[cur], L.ldY, R.r, yb[cur], R.alpha,
+                       R.far, R.ctrl, R.slab, MARGINS_ONLY, c));
+    if ((rc = record(prof, it, 1, st)) != CASGD_OK) return rc;
+    // (The sum of G over processes would sit before this launch; on one GPU it is the
+    // identity.)
+    if (it + 1 < iters)
+      CK(launch_gram_recur(Yb[nxt], Gb[nxt], true, L.S, d->n, L.ldY, p->b, p->s, p->eta,
+                           p->loss, p->flags, Gb[cur], Yb[cur], R.r, yb[cur], R.alpha, R.far,
+                           R.slab, R.upd, w, R.ctrl, p->timeout_us, c));
+    else
+      CK(launch_recur(Gb[cur], R.r, yb[cur], R.alpha, R.far, R.slab, p->b, p->s, p->eta,
+                      p->loss, p->flags, p->timeout_us, R.ctrl, Yb[cur], L.ldY, d->n, R.upd, w,
+                      c));
+    // the update (a8) finished inside that launch
+    if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
+    if ((rc = record(prof, it, 3, st)) != CASGD_OK) return rc;
+    if ((rc = record(prof, it, 4, st)) != CASGD_OK) return rc;
+    if (loss_every > 0 && (it + 1) % loss_every == 0) {
+      CK(launch_loss(*d, p->loss, w, R.loss_part, R.loss_slots + slot, R.ctrl, c));
+      if (++slot == kLossSlots) {
+        CK(cudaMemcpyAsync(loss_hist + flushed, R.loss_slots, slot * sizeof(double),
+                           cudaMemcpyDeviceToHost, st));
+        CK(cudaStreamSynchronize(st));
+        flushed += slot;
+        slot = 0;
+      }
+    }
   }
   return CASGD_OK;
 }
@@ -223,9 +314,10 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms)
   off += align_up((size_t)L.S * sizeof(float));
   L.off_alpha = off;
   off += align_up((size_t)L.S * sizeof(float));
-  L.off_far = off;  // far sums FP32[S]; kMaxSlabs row counters; (kMaxS+1) x 4 trace
+  L.off_far = off;  // far sums FP32[S]; the counters area (see timeline_of)
   off += align_up((size_t)L.S * sizeof(float)) +
-         align_up(kMaxSlabs * sizeof(uint32_t) + (kMaxS + 1) * 4 * sizeof(uint64_t));
+         align_up((kMaxSlabs + kMaxUpdChunks) * sizeof(uint32_t) +
+                  (kMaxS + 1) * 4 * sizeof(uint64_t));
   L.off_Y = off;
   off += align_up((size_t)L.S * L.ldY * sizeof(uint16_t));
   L.off_upd = off;
@@ -235,6 +327,17 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms)
   off += align_up((size_t)upd_rows * L.ldY * sizeof(float));
   L.off_G = off;
   off += align_up((size_t)L.gram_elems * sizeof(float));
+  L.off_Y2 = L.off_G2 = L.off_idx2 = L.off_yY2 = 0;
+  if (gram_plan(n, b, s, flags).fused) {  // casgd_train runs the Gram one iteration ahead
+    L.off_idx2 = off;
+    off += align_up((size_t)L.S * sizeof(int32_t));
+    L.off_yY2 = off;
+    off += align_up((size_t)L.S * sizeof(float));
+    L.off_Y2 = off;
+    off += align_up((size_t)L.S * L.ldY * sizeof(uint16_t));
+    L.off_G2 = off;
+    off += align_up((size_t)L.gram_elems * sizeof(float));
+  }
   L.total = off;
   return L;
 }
@@ -355,6 +458,12 @@ int casgd_train(const casgd_data_t* data, const casgd_params_t* params, float* w
   if (rc != CASGD_OK) return rc;
   Resolved R = resolve(ws, L);
   int slot = 0, flushed = 0;
+  if (iters >= 2 && L.off_G2 != 0) {
+    rc = train_pipelined(data, params, w, k0, iters, L, R, c, prof, loss_every, slot, flushed,
+                         loss_hist);
+    if (rc != CASGD_OK) return rc;
+    iters = 0;  // done
+  }
   for (int32_t it = 0; it < iters; ++it) {
     rc = outer_step_impl(data, params, w, k0 + (uint64_t)it, ws, ws_bytes, c.stream, nullptr,
                          c, prof, it);

@@ -35,6 +35,14 @@ constexpr int64_t kMaxN = 16384;
 constexpr int kLossCtas = 1024;     // upper bound on loss-kernel CTAs (partials)
 // per-32-row completion counters of the paired-SM Gram (rows padded to 256-row groups)
 constexpr int64_t kMaxSlabs = (kMaxSB + 255) / 256 * 8;
+// per-64-column counters of the weight update's first stage (s partial rows each)
+constexpr int64_t kMaxUpdChunks = kMaxN / 64;
+// The counters area of the workspace: kMaxSlabs row counters, kMaxUpdChunks column
+// counters, then the profiling timeline ((kMaxS + 1) x 4 globaltimer stamps).
+__host__ __device__ inline uint32_t* upd_chunk_counters(uint32_t* slab) { return slab + kMaxSlabs; }
+__host__ __device__ inline uint64_t* timeline_of(uint32_t* slab) {
+  return reinterpret_cast<uint64_t*>(slab + kMaxSlabs + kMaxUpdChunks);
+}
 
 // Control block at the start of the workspace (256 bytes, zeroed per step where noted).
 struct Ctrl {
@@ -44,7 +52,7 @@ struct Ctrl {
                           // recorded in `status`, so later steps fail fast.
   uint32_t next_unit;     // recurrence work queue (zeroed by the gather kernel)
   uint32_t loss_done;     // loss kernel: CTAs finished (zeroed by the loss kernel's last CTA)
-  uint32_t pad_q;         // (unused)
+  uint32_t upd_next;      // recurrence: update-unit queue (zeroed by the gather kernel)
   uint32_t diag;          // which wait timed out last: kind << 24 | block << 12 | value seen
   uint32_t pad0[2];
   uint32_t block_done[kMaxS];  // recurrence: chain CTAs done per phase (zeroed per step)
@@ -55,7 +63,9 @@ static_assert(sizeof(Ctrl) <= 512, "control block");
 struct Layout {
   int64_t S, ldY, gram_elems;
   int upd_ctas;
-  size_t off_idx, off_r, off_yY, off_alpha, off_far, off_Y, off_G, off_upd, off_loss, total;
+  size_t off_idx, off_r, off_yY, off_alpha, off_far, off_Y, off_G, off_upd, off_loss;
+  size_t off_Y2, off_G2, off_idx2, off_yY2;  // 0: no second buffers
+  size_t total;
 };
 
 Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms);
@@ -147,32 +157,46 @@ cudaError_t launch_store_bf16(const float* src, int64_t m, int64_t n, int64_t ld
                               uint16_t* dst, int64_t ld_dst, Ctx& c);
 cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t counter0,
                           int32_t* idx, Ctx& c);
+// mode: GATHER_AND_MARGINS (sampled rows into Y, labels, indices, BF16 margins and the
+// recurrence's reset), GATHER_ONLY (rows, labels, indices), MARGINS_ONLY (margins of
+// the rows in Y and the reset).  The margins are bit-identical in every mode.
+enum { GATHER_AND_MARGINS = 0, GATHER_ONLY = 1, MARGINS_ONLY = 2 };
 cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const float* w,
                           uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
                           int64_t ldY, uint16_t* r, float* yY, float* alpha, float* far,
-                          Ctrl* ctrl, uint32_t* slab, Ctx& c);
+                          Ctrl* ctrl, uint32_t* slab, int mode, Ctx& c);
+// GATHER_ONLY for iteration k_next (into Y_next, yY_next, idx_next) and MARGINS_ONLY for
+// the rows in Y, in one launch (the two touch disjoint buffers).
+cudaError_t launch_gather_next_margins(const casgd_data_t& d, const casgd_params_t& p,
+                                       const float* w, uint64_t k_next, int32_t* idx_next,
+                                       uint16_t* Y_next, float* yY_next, const uint16_t* Y,
+                                       int64_t ldY, uint16_t* r, float* alpha, float* far,
+                                       Ctrl* ctrl, uint32_t* slab, Ctx& c);
 cudaError_t launch_gram_simt(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
                              int s, bool diag, float* G, Ctx& c);
 bool gram_tc_supported(int64_t S, int64_t n, int b);
 cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
                            int s, bool diag, int mode, float* G, Ctrl* ctrl,
                            uint32_t timeout_us, Ctx& c);
-// fuse_update != 0 fuses the first stage of the weight update: part[j][:] for each of
-// the s blocks j (s partial rows of ldY floats), to be summed by launch_update_reduce.
+// The recurrence with the weight update fused: part[j][:] for each of the s blocks j
+// (s partial rows of ldY floats), added to w (FP32[n]) by the last unit of each
+// 64-column chunk.  counters: the workspace's counters area (timeline_of).
 cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, float* alpha,
-                         float* far, uint64_t* trace, int b, int s, float eta, int loss,
+                         float* far, uint32_t* counters, int b, int s, float eta, int loss,
                          uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, const uint16_t* Y,
-                         int64_t ldY, float* part, int fuse_update, Ctx& c);
-// The paired-SM Gram and the recurrence (with the fused update stage) in one launch:
-// the Gram's epilogue releases per-32-row counters `slab` (zeroed by the gather kernel)
-// that the recurrence acquires before it reads rows of G.  cudaErrorNotSupported when
-// the shape does not fit the fused kernel (the caller then launches them separately).
+                         int64_t ldY, int64_t n, float* part, float* w, Ctx& c);
+// The paired-SM Gram (of rows Yg into Gg) and the recurrence (with the fused update
+// stage, on G and Y) in one launch.  next == false: the same iteration (Yg == Y,
+// Gg == G); the Gram's epilogue releases per-32-row counters `slab` (zeroed by the
+// margins step) that the recurrence acquires before it reads rows of G.  next == true:
+// the Gram is the next iteration's and G is complete.  cudaErrorNotSupported when the
+// shape does not fit the fused kernel (the caller then launches them separately).
 bool gram_recur_fused_supported(int64_t S, int64_t n, int b);
-cudaError_t launch_gram_recur(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
-                              int s, float eta, int loss, uint32_t flags, float* G,
-                              const uint16_t* r, const float* yY, float* alpha, float* far,
-                              uint64_t* trace, uint32_t* slab, float* part, Ctrl* ctrl,
-                              uint32_t timeout_us, Ctx& c);
+cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t S, int64_t n,
+                              int64_t ldY, int b, int s, float eta, int loss, uint32_t flags,
+                              const float* G, const uint16_t* Y, const uint16_t* r,
+                              const float* yY, float* alpha, float* far, uint32_t* slab,
+                              float* part, float* w, Ctrl* ctrl, uint32_t timeout_us, Ctx& c);
 cudaError_t launch_update_reduce(const float* part, int upd_ctas, int64_t n, int64_t ldY,
                                  float* w, Ctrl* ctrl, Ctx& c);
 cudaError_t launch_update(const uint16_t* Y, const float* alpha, int64_t S, int64_t n,

@@ -526,9 +526,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // own epilogue warps store them.  Every tcgen05 operation of this kernel, the TMEM
 // allocation included, uses cta_group::2.
 //
-// With kRecV > 0 the same launch also runs the inner recurrence (recur_roles.cuh) on
+// With kRecV > 0 the same launch also runs an inner recurrence (recur_roles.cuh) on
 // eight more warps per CTA (warps 6-13; kRecV: the chain's register layout, see
-// chain_variant).  After the stores of a tile are complete, each epilogue warp releases
+// chain_variant).  With kNext the Gram is the next outer iteration's (its rows were
+// sampled ahead; only the margins need the current w) and the recurrence reads this
+// iteration's complete G, so the two only share the SMs; otherwise both work on the
+// same iteration as follows.  After the stores of a tile are complete, each epilogue warp releases
 // the counter of its 32 rows, and the recurrence acquires the counters of the rows it
 // reads.  Row groups are visited in increasing order, so phase j of the recurrence can
 // start as soon as block row j of G is stored instead of after the whole Gram.  The
@@ -625,7 +628,7 @@ __device__ bool mbar_wait2(uint64_t* bar, uint32_t parity, SharedCtl2<kSt>* sc, 
   }
 }
 
-template <int kSt, int kRecV>
+template <int kSt, int kRecV, bool kNext>
 __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
     gram_tc2sm_kernel(const __grid_constant__ CUtensorMap tmY,
                       const __grid_constant__ CUtensorMap tmG, TcArgs a, RecArgs rec) {
@@ -756,7 +759,7 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_rank(smem_u32(&sc->tempty[acc]), 0));
-      if (kRecV) {
+      if (kRecV && !kNext) {
         // publish this warp's 32 rows of the tile: its stores are complete and visible
         if (a.tma_store) {
           if (lane == 0) {
@@ -771,6 +774,8 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
           red_release_add(a.slab + (int64_t)ra * 4 + quarter, 1u);
           stamp_last(rec.trace, 0);
         }
+      } else if (kRecV && lane == 0) {
+        stamp_last(rec.trace, 0);
       }
     }
     if (lane == 0) bulk_wait_all();  // this warp's tensor stores are complete
@@ -780,10 +785,10 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
     // the first C CTAs run chain groups, the others the bulk role
     const int rt = threadIdx.x - kThreads;
     if ((int)blockIdx.x < rec.C)
-      chain_role<kRecV == 1 ? 1 : 2, kRecV == 1 ? 8 : (kRecV == 2 ? 4 : 2), true>(
+      chain_role<kRecV == 1 ? 1 : 2, kRecV == 1 ? 8 : (kRecV == 2 ? 4 : 2), kNext ? 2 : 1>(
           rec, blockIdx.x, rt);
     else
-      bulk_role<true>(rec, rt);
+      bulk_role<kNext ? 2 : 1>(rec, rt, (int)blockIdx.x - rec.C < rec.upd_groups);
   }
 
   tc_fence_before();
@@ -929,7 +934,7 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
     ++c.launches;
     return cudaGetLastError();
   }
-  const void* fn = mode == 0 ? (const void*)gram_tc2sm_kernel<kStagesPair, 0>
+  const void* fn = mode == 0 ? (const void*)gram_tc2sm_kernel<kStagesPair, 0, false>
                              : (const void*)gram_tc_kernel<2>;
   const size_t smem = mode == 0 ? pair_smem_bytes<kStagesPair>() : kSmemBytes;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -945,7 +950,7 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
   if (mode == 0) {
     RecArgs none;
     memset(&none, 0, sizeof(none));
-    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel<kStagesPair, 0>, P.map, P.mapG, a, none);
+    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel<kStagesPair, 0, false>, P.map, P.mapG, a, none);
   } else {
     e = cudaLaunchKernelEx(&cfg, gram_tc_kernel<2>, P.map, P.mapG, a);
   }
@@ -958,32 +963,36 @@ bool gram_recur_fused_supported(int64_t S, int64_t n, int b) {
   return gram_tc_supported(S, n, b) && (S + BM - 1) / BM >= 2 && S / b >= 2;
 }
 
-cudaError_t launch_gram_recur(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
-                              int s, float eta, int loss, uint32_t flags, float* G,
-                              const uint16_t* r, const float* yY, float* alpha, float* far,
-                              uint64_t* trace, uint32_t* slab, float* part, Ctrl* ctrl,
-                              uint32_t timeout_us, Ctx& c) {
+cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t S, int64_t n,
+                              int64_t ldY, int b, int s, float eta, int loss, uint32_t flags,
+                              const float* G, const uint16_t* Y, const uint16_t* r,
+                              const float* yY, float* alpha, float* far, uint32_t* slab,
+                              float* part, float* w, Ctrl* ctrl, uint32_t timeout_us, Ctx& c) {
   if (!gram_recur_fused_supported(S, n, b)) return cudaErrorNotSupported;
   const bool diag = (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
   TcPlan P;
-  cudaError_t e = plan_tc(Y, S, n, ldY, b, s, diag, 2, G, ctrl, timeout_us, P);
+  cudaError_t e = plan_tc(Yg, S, n, ldY, b, s, diag, 2, Gg, ctrl, timeout_us, P);
   if (e != cudaSuccess) return e;
-  P.a.slab = slab;
-  RecArgs rec = make_rec_args(G, r, yY, alpha, far, trace, b, s, eta, loss, flags, timeout_us,
-                              ctrl, Y, ldY, part, 1);
-  rec.slab = slab;
+  P.a.slab = next ? nullptr : slab;
+  RecArgs rec = make_rec_args(G, r, yY, alpha, far, slab, b, s, eta, loss, flags, timeout_us,
+                              ctrl, Y, ldY, n, part, w);
+  rec.slab = next ? nullptr : slab;
   const int v = chain_variant(rec);
-  const void* fn = v == 3   ? (const void*)gram_tc2sm_kernel<kStagesFused, 3>
-                   : v == 2 ? (const void*)gram_tc2sm_kernel<kStagesFused, 2>
-                            : (const void*)gram_tc2sm_kernel<kStagesFused, 1>;
+  using Fn = void (*)(CUtensorMap, CUtensorMap, TcArgs, RecArgs);
+  const Fn table[2][3] = {
+      {gram_tc2sm_kernel<kStagesFused, 1, false>, gram_tc2sm_kernel<kStagesFused, 2, false>,
+       gram_tc2sm_kernel<kStagesFused, 3, false>},
+      {gram_tc2sm_kernel<kStagesFused, 1, true>, gram_tc2sm_kernel<kStagesFused, 2, true>,
+       gram_tc2sm_kernel<kStagesFused, 3, true>}};
+  const Fn fn = table[next ? 1 : 0][v - 1];
   const size_t smem = pair_smem_bytes<kStagesFused>();
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster2_config(kFusedThreads, smem, c.stream, attr);
   cfg.gridDim = dim3(2 * (unsigned)(c.num_sms / 2));
   int max_clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&max_clusters, (const void*)fn, &cfg);
   if (e != cudaSuccess) return e;
   // every CTA must be resident at once (the recurrence waits across CTAs); one chain
   // group per 8-row group while at least one bulk group remains
@@ -992,13 +1001,9 @@ cudaError_t launch_gram_recur(const uint16_t* Y, int64_t S, int64_t n, int64_t l
   rec.C = rec.Uc < grid - 1 ? rec.Uc : grid - 1;
   if (rec.C > grid / 2) rec.C = grid / 2;
   if (rec.C < 1) return cudaErrorNotSupported;
+  rec.upd_groups = update_groups(rec, grid - rec.C);
   cfg.gridDim = dim3((unsigned)grid);
-  if (v == 3)
-    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel<kStagesFused, 3>, P.map, P.mapG, P.a, rec);
-  else if (v == 2)
-    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel<kStagesFused, 2>, P.map, P.mapG, P.a, rec);
-  else
-    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel<kStagesFused, 1>, P.map, P.mapG, P.a, rec);
+  e = cudaLaunchKernelEx(&cfg, fn, P.map, P.mapG, P.a, rec);
   ++c.launches;
   return e;
 }

@@ -5,7 +5,7 @@
 // precision; each outer iteration works on s minibatches of b rows.
 //
 // The gather writes Y (S x ldY BF16, ldY = n rounded up to 8, zero padded) once per
-// outer iteration.  Y is small next to X and stays L2-resident for the Gram and update
+// outer iteration (in a multi-iteration run, one iteration ahead of its margins).  Y is small next to X and stays L2-resident for the Gram and update
 // kernels; it lets the Gram kernel fetch tiles with plain tiled TMA copies.
 #include <cuda_bf16.h>
 
@@ -45,53 +45,81 @@ __global__ void sample_kernel(uint32_t m, int64_t count, uint64_t seed, uint64_t
     idx[i] = sample_row(seed, counter0 + (uint64_t)i, m);
 }
 
-// One group of G lanes (G a power of two <= 32) per row of Y.  Lane g copies the
-// 16-byte vectors g, g+G, ... of the row and accumulates their FP32 dot with w; the
-// group then reduces with shuffles and its first lane stores the BF16 margin.
-__global__ void __launch_bounds__(256) gather_kernel(
-    const uint16_t* __restrict__ X, const float* __restrict__ y, int64_t m, int64_t n,
-    int64_t ld, const float* __restrict__ w, int64_t S, uint64_t seed, uint64_t counter0,
-    const int32_t* __restrict__ idx_in, int32_t* __restrict__ idx_out,
-    uint16_t* __restrict__ Y, int64_t ldY, uint16_t* __restrict__ r,
-    float* __restrict__ yY, float* __restrict__ alpha, float* __restrict__ far, Ctrl* ctrl,
-    uint32_t* slab, int s, int G) {
-  if (blockIdx.x == 0) {  // per-step reset of the recurrence's queue and counters
-    if (threadIdx.x == 0) {
-      ctrl->next_unit = 0;
-      ctrl->abort = (ctrl->status & ST_TIMEOUT) ? 1u : 0u;  // stays set after a timeout
-    }
-    for (int j = threadIdx.x; j < kMaxS; j += blockDim.x) ctrl->block_done[j] = 0;
-    const int64_t nslab = (S + 255) / 256 * 8;  // the Gram's 32-row counters
-    for (int64_t j = threadIdx.x; j < nslab; j += blockDim.x) slab[j] = 0;
-    // summary row of the profiling timeline (it follows the counters)
-    uint64_t* summary = reinterpret_cast<uint64_t*>(slab + kMaxSlabs) + (int64_t)kMaxS * 4;
-    if (threadIdx.x < 4) summary[threadIdx.x] = 0;
+// One group of G lanes (G a power of two <= 32) per row of Y.  Lane g reads the 16-byte
+// vectors g, g+G, ... of the row and accumulates their FP32 dot with w; the group then
+// reduces with shuffles and its first lane stores the BF16 margin.  Variants:
+//   kCopy && kMargin   gather the sampled rows of X into Y and form the margins (one
+//                      outer iteration at a time);
+//   kCopy && !kMargin  gather only (Y, labels, indices) for an iteration whose margins
+//                      are formed later, once its starting w is known;
+//   !kCopy && kMargin  margins of rows already in Y.
+// The margin arithmetic is the same in every variant (same lanes, vector order and
+// shuffle tree), so a margin does not depend on which variant formed it.  Variants with
+// kMargin also prepare the recurrence that follows (queues, counters, pending values).
+struct RowArgs {
+  const uint16_t* X;
+  const float* y;
+  int64_t m, n, ld;
+  const float* w;
+  int64_t S;
+  uint64_t seed, counter0;
+  const int32_t* idx_in;
+  int32_t* idx_out;
+  uint16_t* Y;
+  int64_t ldY;
+  uint16_t* r;
+  float* yY;
+  float* alpha;
+  float* far;
+  Ctrl* ctrl;
+  uint32_t* slab;
+  int G;
+};
+
+// The recurrence's per-step reset (one CTA).
+__device__ void reset_recurrence(const RowArgs& a) {
+  if (threadIdx.x == 0) {
+    a.ctrl->next_unit = 0;
+    a.ctrl->upd_next = 0;
+    a.ctrl->abort = (a.ctrl->status & ST_TIMEOUT) ? 1u : 0u;  // stays set after a timeout
   }
+  for (int j = threadIdx.x; j < kMaxS; j += blockDim.x) a.ctrl->block_done[j] = 0;
+  const int64_t nslab = (a.S + 255) / 256 * 8;  // the Gram's 32-row counters
+  for (int64_t j = threadIdx.x; j < nslab; j += blockDim.x) a.slab[j] = 0;
+  uint32_t* chunks = upd_chunk_counters(a.slab);  // the update's column counters
+  for (int64_t j = threadIdx.x; j < (a.ldY + 63) / 64; j += blockDim.x) chunks[j] = 0;
+  uint64_t* summary = timeline_of(a.slab) + (int64_t)kMaxS * 4;  // profiling summary row
+  if (threadIdx.x < 4) summary[threadIdx.x] = 0;
+}
+
+// The rows of block `blk` (8 warps, 32/G rows per warp).
+template <bool kCopy, bool kMargin>
+__device__ __forceinline__ void gather_rows(const RowArgs& a, int64_t blk) {
+  const int G = a.G;
   const int lane = threadIdx.x & 31;
   const int g = lane & (G - 1);
   const int rows_per_warp = 32 / G;
-  const int64_t p = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * rows_per_warp +
-                    lane / G;
-  const int64_t nvec = ldY / 8;
-  const bool w_vec = (reinterpret_cast<uintptr_t>(w) & 15u) == 0;
+  const int64_t p = (blk * (blockDim.x >> 5) + (threadIdx.x >> 5)) * rows_per_warp + lane / G;
+  const int64_t nvec = a.ldY / 8;
+  const bool w_vec = (reinterpret_cast<uintptr_t>(a.w) & 15u) == 0;
   // Every lane of the warp must reach the shuffles, so out-of-range rows only mask.
-  const bool live = p < S;
+  const bool live = p < a.S;
   int32_t row = 0;
-  bool valid = false;
-  if (live) {
-    if (idx_in) {
-      row = idx_in[p];
-      valid = (row >= 0 && (int64_t)row < m);
-      if (!valid && g == 0) atomicOr(&ctrl->status, ST_BAD_INDEX);
+  bool valid = !kCopy;  // rows already in Y are valid
+  if (kCopy && live) {
+    if (a.idx_in) {
+      row = a.idx_in[p];
+      valid = (row >= 0 && (int64_t)row < a.m);
+      if (!valid && g == 0) atomicOr(&a.ctrl->status, ST_BAD_INDEX);
     } else {
-      row = sample_row(seed, counter0 + (uint64_t)p, (uint32_t)m);
+      row = sample_row(a.seed, a.counter0 + (uint64_t)p, (uint32_t)a.m);
       valid = true;
     }
   }
   float acc = 0.0f;
   if (live) {
-    const uint16_t* xr = X + (int64_t)(valid ? row : 0) * ld;
-    uint16_t* yr = Y + p * ldY;
+    const uint16_t* xr = kCopy ? a.X + (int64_t)(valid ? row : 0) * a.ld : a.Y + p * a.ldY;
+    uint16_t* yr = a.Y + p * a.ldY;
     // kBatch 16-byte loads of the row are issued before any of them is used.
     constexpr int kBatch = 8;
     for (int64_t v0 = g; v0 < nvec; v0 += (int64_t)G * kBatch) {
@@ -109,36 +137,64 @@ __global__ void __launch_bounds__(256) gather_kernel(
         const int64_t c0 = v * 8;
         uint32_t parts[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
         float wv[8];
-        if (w_vec && c0 + 8 <= n) {
-          const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + c0));
-          const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + c0 + 4));
-          wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
-          wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
-        } else {
+        if (kMargin) {
+          if (w_vec && c0 + 8 <= a.n) {
+            const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.w + c0));
+            const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.w + c0 + 4));
+            wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
+            wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
+          } else {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) wv[e] = c0 + e < n ? __ldg(w + c0 + e) : 0.0f;
+            for (int e = 0; e < 8; ++e) wv[e] = c0 + e < a.n ? __ldg(a.w + c0 + e) : 0.0f;
+          }
         }
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           const int64_t c = c0 + 2 * h;
           uint32_t lo = parts[h] & 0xFFFFu, hi = parts[h] >> 16;
-          if (c >= n) lo = 0;
-          if (c + 1 >= n) hi = 0;
+          if (c >= a.n) lo = 0;
+          if (c + 1 >= a.n) hi = 0;
           parts[h] = lo | (hi << 16);
-          if (c < n) acc = fmaf(bf16_bits_to_float(lo), wv[2 * h], acc);
-          if (c + 1 < n) acc = fmaf(bf16_bits_to_float(hi), wv[2 * h + 1], acc);
+          if (kMargin) {
+            if (c < a.n) acc = fmaf(bf16_bits_to_float(lo), wv[2 * h], acc);
+            if (c + 1 < a.n) acc = fmaf(bf16_bits_to_float(hi), wv[2 * h + 1], acc);
+          }
         }
-        *reinterpret_cast<uint4*>(yr + c0) = make_uint4(parts[0], parts[1], parts[2], parts[3]);
+        if (kCopy)
+          *reinterpret_cast<uint4*>(yr + c0) = make_uint4(parts[0], parts[1], parts[2], parts[3]);
       }
     }
   }
-  for (int off = G >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);
+  if (kMargin)
+    for (int off = G >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);
   if (live && g == 0) {
-    r[p] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
-    yY[p] = valid ? __ldg(y + row) : 0.0f;
-    alpha[p] = __uint_as_float(kAlphaPending);  // the recurrence waits on these values
-    far[p] = __uint_as_float(kAlphaPending);
-    idx_out[p] = row;
+    if (kMargin) {
+      a.r[p] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+      a.alpha[p] = __uint_as_float(kAlphaPending);  // the recurrence waits on these values
+      a.far[p] = __uint_as_float(kAlphaPending);
+    }
+    if (kCopy) {
+      a.yY[p] = valid ? __ldg(a.y + row) : 0.0f;
+      a.idx_out[p] = row;
+    }
+  }
+}
+
+template <bool kCopy, bool kMargin>
+__global__ void __launch_bounds__(256) gather_kernel(RowArgs a) {
+  if (kMargin && blockIdx.x == 0) reset_recurrence(a);
+  gather_rows<kCopy, kMargin>(a, blockIdx.x);
+}
+
+// Two independent passes in one launch: blocks [0, nb_g) gather the next iteration's
+// rows (g), the others form this iteration's margins (mg) from its rows already in Y.
+__global__ void __launch_bounds__(256) gather_next_margins_kernel(RowArgs g, RowArgs mg,
+                                                                  int64_t nb_g) {
+  if ((int64_t)blockIdx.x < nb_g) {
+    gather_rows<true, false>(g, blockIdx.x);
+  } else {
+    if ((int64_t)blockIdx.x == nb_g) reset_recurrence(mg);
+    gather_rows<false, true>(mg, (int64_t)blockIdx.x - nb_g);
   }
 }
 
@@ -171,17 +227,66 @@ cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t coun
   return cudaGetLastError();
 }
 
+namespace {
+
+RowArgs row_args(const casgd_data_t& d, const casgd_params_t& p, const float* w, uint64_t k,
+                 const int32_t* idx_in, int32_t* idx, uint16_t* Y, int64_t ldY, uint16_t* r,
+                 float* yY, float* alpha, float* far, Ctrl* ctrl, uint32_t* slab) {
+  RowArgs a;
+  a.X = static_cast<const uint16_t*>(d.X);
+  a.y = d.y;
+  a.m = d.m;
+  a.n = d.n;
+  a.ld = d.ld;
+  a.w = w;
+  a.S = (int64_t)p.b * p.s;
+  a.seed = p.seed;
+  a.counter0 = k * (uint64_t)a.S;
+  a.idx_in = idx_in;
+  a.idx_out = idx;
+  a.Y = Y;
+  a.ldY = ldY;
+  a.r = r;
+  a.yY = yY;
+  a.alpha = alpha;
+  a.far = far;
+  a.ctrl = ctrl;
+  a.slab = slab;
+  a.G = pow2_at_least(ldY / 8, 32);
+  return a;
+}
+
+int64_t row_blocks(const RowArgs& a) {
+  const int64_t rows_per_cta = 8 * (32 / a.G);
+  return (a.S + rows_per_cta - 1) / rows_per_cta;
+}
+
+}  // namespace
+
 cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const float* w,
                           uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
                           int64_t ldY, uint16_t* r, float* yY, float* alpha, float* far,
-                          Ctrl* ctrl, uint32_t* slab, Ctx& c) {
-  const int64_t S = (int64_t)p.b * p.s;
-  const int G = pow2_at_least(ldY / 8, 32);
-  const int64_t rows_per_cta = 8 * (32 / G);
-  const int64_t blocks = (S + rows_per_cta - 1) / rows_per_cta;
-  gather_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>(
-      static_cast<const uint16_t*>(d.X), d.y, d.m, d.n, d.ld, w, S, p.seed, k * (uint64_t)S,
-      idx_in, idx, Y, ldY, r, yY, alpha, far, ctrl, slab, p.s, G);
+                          Ctrl* ctrl, uint32_t* slab, int mode, Ctx& c) {
+  const RowArgs a = row_args(d, p, w, k, idx_in, idx, Y, ldY, r, yY, alpha, far, ctrl, slab);
+  auto fn = mode == GATHER_AND_MARGINS ? gather_kernel<true, true>
+            : mode == GATHER_ONLY      ? gather_kernel<true, false>
+                                       : gather_kernel<false, true>;
+  fn<<<(unsigned)row_blocks(a), 256, 0, c.stream>>>(a);
+  ++c.launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_next_margins(const casgd_data_t& d, const casgd_params_t& p,
+                                       const float* w, uint64_t k_next, int32_t* idx_next,
+                                       uint16_t* Y_next, float* yY_next, const uint16_t* Y,
+                                       int64_t ldY, uint16_t* r, float* alpha, float* far,
+                                       Ctrl* ctrl, uint32_t* slab, Ctx& c) {
+  const RowArgs g = row_args(d, p, w, k_next, nullptr, idx_next, Y_next, ldY, nullptr, yY_next,
+                             nullptr, nullptr, ctrl, slab);
+  const RowArgs mg = row_args(d, p, w, 0, nullptr, nullptr, const_cast<uint16_t*>(Y), ldY, r,
+                              nullptr, alpha, far, ctrl, slab);
+  const int64_t nb = row_blocks(g);
+  gather_next_margins_kernel<<<(unsigned)(2 * nb), 256, 0, c.stream>>>(g, mg, nb);
   ++c.launches;
   return cudaGetLastError();
 }

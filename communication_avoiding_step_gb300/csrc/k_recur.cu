@@ -16,24 +16,27 @@ namespace {
 template <int kB, int kKB>
 __global__ void __launch_bounds__(kRecThreads) recur_kernel(RecArgs a) {
   if ((int)blockIdx.x < a.C)
-    chain_role<kB, kKB, false>(a, blockIdx.x, threadIdx.x);
+    chain_role<kB, kKB, 0>(a, blockIdx.x, threadIdx.x);
   else
-    bulk_role<false>(a, threadIdx.x);
+    bulk_role<0>(a, threadIdx.x, (int)blockIdx.x - a.C < a.upd_groups);
 }
 
 }  // namespace
 
 RecArgs make_rec_args(const float* G, const uint16_t* r, const float* yY, float* alpha,
-                      float* far, uint64_t* trace, int b, int s, float eta, int loss,
+                      float* far, uint32_t* counters, int b, int s, float eta, int loss,
                       uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, const uint16_t* Y,
-                      int64_t ldY, float* part, int fuse_update) {
+                      int64_t ldY, int64_t n, float* part, float* w) {
   RecArgs a;
   a.G = G;
   a.r = r;
   a.yY = yY;
   a.alpha = alpha;
   a.far = far;
-  a.trace = (flags & CASGD_FLAG_TRACE_CHAIN) ? trace : nullptr;
+  a.trace = (flags & CASGD_FLAG_TRACE_CHAIN) ? timeline_of(counters) : nullptr;
+  a.upd_chunks = upd_chunk_counters(counters);
+  a.w = w;
+  a.n = n;
   a.ctrl = ctrl;
   a.timeout_ns = (uint64_t)(timeout_us ? timeout_us : 1000000u) * 1000ull;
   a.b = b;
@@ -45,26 +48,28 @@ RecArgs make_rec_args(const float* G, const uint16_t* r, const float* yY, float*
   a.vec4 = (b % 4) == 0;
   // band width: two blocks while a chain lane can hold both in registers
   a.B = (a.vec4 && (b + 127) / 128 <= 4) ? 2 : 1;
-  a.bulk_units = s > a.B + 1 ? (s - a.B - 1) * a.U : 0;
+  a.bulk_units = 0;  // far units: (block, chunk of kT blocks) pairs x row units
+  for (int j = a.B + 1; j < s; ++j) a.bulk_units += a.U;
   a.coef = -(eta / (float)b);
   a.Y = Y;
   a.part = part;
   a.ldY = ldY;
-  // update units: s blocks x ceil(ldY / 64) column chunks (0 = update not fused)
-  a.upd_units = fuse_update ? s * (int)((ldY / 8 + 7) / 8) : 0;
+  // update units: s blocks x ceil(ldY / 64) column chunks
+  a.upd_units = s * (int)((ldY / 8 + 7) / 8);
   a.slab = nullptr;
   a.C = 0;
+  a.upd_groups = 0;
   a.diag = (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
   a.stall_test = (flags & CASGD_FLAG_TEST_STALL) != 0;
   return a;
 }
 
 cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, float* alpha,
-                         float* far, uint64_t* trace, int b, int s, float eta, int loss,
+                         float* far, uint32_t* counters, int b, int s, float eta, int loss,
                          uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, const uint16_t* Y,
-                         int64_t ldY, float* part, int fuse_update, Ctx& c) {
-  RecArgs a = make_rec_args(G, r, yY, alpha, far, trace, b, s, eta, loss, flags, timeout_us,
-                            ctrl, Y, ldY, part, fuse_update);
+                         int64_t ldY, int64_t n, float* part, float* w, Ctx& c) {
+  RecArgs a = make_rec_args(G, r, yY, alpha, far, counters, b, s, eta, loss, flags, timeout_us,
+                            ctrl, Y, ldY, n, part, w);
   const int v = chain_variant(a);
   const void* fn = v == 3   ? (const void*)recur_kernel<2, 2>
                    : v == 2 ? (const void*)recur_kernel<2, 4>
@@ -82,6 +87,7 @@ cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, flo
   if (a.C + (queued > 0 ? 1 : 0) > cap) return cudaErrorNotSupported;
   int64_t grid = a.C + queued;
   if (grid > cap) grid = cap;
+  a.upd_groups = update_groups(a, (int)(grid - a.C));
   void* args[] = {&a};
   e = cudaLaunchCooperativeKernel(fn, dim3((unsigned)grid), dim3(kRecThreads), args, 0, c.stream);
   ++c.launches;

@@ -10,24 +10,27 @@
 // earlier blocks are known; the s blocks form a serial chain.
 //
 // Two roles, each run by a group of 256 threads (a whole CTA in the stand-alone kernel,
-// warps 6-13 of a CTA in the fused one):
+// warps 6-13 of a CTA in the kernels shared with the Gram).  kMode: 0 own CTA, G
+// complete; 1 shared CTA, rows of G still being stored by the same launch; 2 shared
+// CTA, G complete (the launch computes the next iteration's Gram):
 //  * chain groups (the first C): one warp per row, 8-row groups.  Phase j of a row
 //    needs only the band  sum_{t=j-B}^{j-1} G_{j,t} alpha_t  (B = 1 or 2 blocks) on top
 //    of far_j (below).  The warp has its band rows of G in registers before it waits
 //    (loaded while it waited in the previous phase), then waits for alpha_{j-1} and
 //    far_j by loading exactly those values until none holds the pending pattern.
-//  * bulk groups take units (block j >= B+1, 16 rows) from an atomic queue in
-//    increasing j and compute far_j = sum_{t<j-B} G_{j,t} alpha_t for their rows,
-//    streaming G with coalesced float4 reads; they wait on alpha_t the same way.  far_j
-//    is needed only B phases after its last input is known, so most of G is read off
-//    the critical path.  After the far units the same queue hands out the first stage
+//  * bulk groups take units (block j >= B+1, chunk of 4 blocks t, 16 rows) from an
+//    atomic queue and compute partial sums of far_j = sum_{t<j-B} G_{j,t} alpha_t for
+//    their rows, streaming G with coalesced float4 reads; they wait on alpha_t the same
+//    way.  far_j is needed only B phases after its last input is known, so most of G is
+//    read off the critical path; the chain adds a row's partials in chunk order.  After the far units the same queue hands out the first stage
 //    of the weight update when it is fused: per block j and 64-column chunk, the
 //    partial row of Y^T alpha over that block, each waiting on the alpha of its rows.
 // Synchronisation is through the data: the gather kernel fills alpha and far with
 // kAlphaPending before the recurrence runs, and a value is final once it differs from
 // that pattern (32-bit stores are single-copy atomic, and a reader uses only the value
-// it waited on, so no fences or counters are needed).  When the Gram runs in the same
-// launch (kFused), rows of G are additionally guarded by per-32-row counters that the
+// it waited on, so no fences or counters are needed).  When the Gram of the same
+// iteration runs in the same launch (kMode 1), rows of G are guarded by per-32-row
+// counters that the
 // Gram's epilogue warps release once their stores of a tile are complete; a reader
 // acquires the counter of its rows before loading them, and loads G through L2 only.
 // Every wait is bounded by `timeout_ns`; on expiry the waiter records ST_TIMEOUT, which
@@ -56,12 +59,17 @@ struct RecArgs {
   float* part;
   int64_t ldY;
   int upd_units;
+  // the update's last stage: the last unit of a column chunk adds the s partial rows
+  uint32_t* upd_chunks;
+  float* w;
+  int64_t n;
   // Gram in the same launch: per-32-row completion counters of the paired-SM Gram
   const uint32_t* slab;
   int64_t S;
   Ctrl* ctrl;
   uint64_t timeout_ns;
   int b, s, loss, U, Uc, C, B, bulk_units;
+  int upd_groups;  // bulk groups that serve the update queue first
   float coef;
   bool diag, stall_test, vec4;
 };
@@ -74,15 +82,30 @@ inline int chain_variant(const RecArgs& a) {
   return nk <= 2 ? 3 : 2;
 }
 
-// Fills every field but C (chosen by the launcher from its grid) and slab.
+// Bulk groups that serve the update queue first, out of nbulk: the update's share of
+// the bytes the bulk role streams (Y for the update, the far blocks of G), at least one.
+inline int update_groups(const RecArgs& a, int nbulk) {
+  if (a.upd_units <= 0 || nbulk <= 1) return 0;
+  const double ub = (double)a.S * (double)a.ldY * 2.0;
+  const double nfar = (a.s > a.B + 1) ? 0.5 * (a.s - a.B - 1) * (a.s - a.B) : 0.0;
+  const double fb = nfar * (double)a.b * (double)a.b * 4.0;
+  int g = (int)(nbulk * ub / (ub + fb) + 0.5);
+  if (g < 1) g = 1;
+  if (g > nbulk - 1) g = nbulk - 1;
+  return g;
+}
+
+// Fills every field but C and upd_groups (chosen by the launcher from its grid) and slab.
+// counters: the workspace's counters area (timeline_of); w: FP32[n], updated in place.
 RecArgs make_rec_args(const float* G, const uint16_t* r, const float* yY, float* alpha,
-                      float* far, uint64_t* trace, int b, int s, float eta, int loss,
+                      float* far, uint32_t* counters, int b, int s, float eta, int loss,
                       uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, const uint16_t* Y,
-                      int64_t ldY, float* part, int fuse_update);
+                      int64_t ldY, int64_t n, float* part, float* w);
 
 namespace {
 
 constexpr int kT = 4;         // bulk: blocks t handled per pass
+constexpr int kUpdRows = 8;   // update unit: rows a thread loads per pass
 
 // Ctrl::diag codes: kind << 24 | block << 12 (2: chain wait, 3: bulk wait, 4: update
 // wait, 5: wait for rows of G, 6: wait for the CTA's own tiles).
@@ -117,21 +140,21 @@ __device__ __forceinline__ float ld_volatile_f32(const float* p) {
 
 // G is read through the read-only path when an earlier launch wrote it, and through L2
 // only when the Gram of the same launch is still writing other rows of it.
-template <bool kFused>
+template <bool kInFlight>
 __device__ __forceinline__ float4 ldG4(const float* p) {
-  if (kFused) return __ldcg(reinterpret_cast<const float4*>(p));
+  if (kInFlight) return __ldcg(reinterpret_cast<const float4*>(p));
   return __ldg(reinterpret_cast<const float4*>(p));
 }
-template <bool kFused>
+template <bool kInFlight>
 __device__ __forceinline__ float ldG1(const float* p) {
-  if (kFused) return __ldcg(p);
+  if (kInFlight) return __ldcg(p);
   return __ldg(p);
 }
 
 // Barrier of one role group: the whole CTA, or named barrier 1 over warps 6-13.
-template <bool kFused>
+template <bool kShared>
 __device__ __forceinline__ void group_sync() {
-  if (kFused)
+  if (kShared)
     asm volatile("bar.sync 1, %0;" ::"r"(kRecThreads) : "memory");
   else
     __syncthreads();
@@ -199,7 +222,7 @@ __device__ bool wait_rows_of_G(const RecArgs& a, int64_t row, uint32_t where) {
 // later items of a phase reuse the first item's.  So the only loads on the critical
 // path are the polls of alpha_{j-1} and far_j.  `rt` is the thread's index within the
 // role group.
-template <int kB, int kKB, bool kFused>
+template <int kB, int kKB, int kMode>
 __device__ void chain_role(const RecArgs& a, int c, int rt) {
   const int warp = rt >> 5, lane = rt & 31;
   const int nk = (a.b + 127) / 128;  // float4 slots per band block (vec4 path)
@@ -222,7 +245,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
 #pragma unroll
       for (int k = 0; k < kKB; ++k) {
         g[tb][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (a.vec4 && tb < nb && lane * 4 + 128 * k < a.b) g[tb][k] = ldG4<kFused>(gb + 128 * k);
+        if (a.vec4 && tb < nb && lane * 4 + 128 * k < a.b) g[tb][k] = ldG4<kMode == 1>(gb + 128 * k);
       }
     }
   };
@@ -242,7 +265,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
     const bool has_far = j >= kB + 1;
     if (tracer && gi == 0) a.trace[4 * j] = globaltimer_ns();
     if (!cur_loaded) {
-      if (kFused && j > 0) {  // this row of G is stored (block 0 reads none)
+      if (kMode == 1 && j > 0) {  // this row of G is stored (block 0 reads none)
         int ok0 = 1;
         if (lane == 0) ok0 = wait_rows_of_G(a, p, where_code(5, j)) ? 1 : 0;
         ok0 = __shfl_sync(0xffffffffu, ok0, 0);
@@ -267,7 +290,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
     if (j2 < a.s && j2 > 0) {
       const int i2 = (c + gi2 * a.C) * kChainRows + warp;
       int ready = 1;
-      if (kFused) {
+      if (kMode == 1) {
         if (lane == 0) {
           const int64_t sl = ((int64_t)j2 * a.b + i2) >> 5;
           ready = ld_acquire_u32(a.slab + sl) >=
@@ -350,7 +373,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
             const uint64_t t_start = globaltimer_ns();
             while (pending4(v) && (ok = keep_waiting(a, t_start, where_code(2, j)))) v = ld_volatile_f4(src);
           }
-          acc = dot4(ldG4<kFused>(grow0 + packed_offset(j, t, a.b, a.diag) + col), v, acc);
+          acc = dot4(ldG4<kMode == 1>(grow0 + packed_offset(j, t, a.b, a.diag) + col), v, acc);
         }
       }
     } else {
@@ -362,7 +385,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
         for (int col = lane; col < a.b; col += 32) {
           float v;
           if (!(ok = wait_value(al + col, v, a, where_code(2, j)))) break;
-          acc = fmaf(ldG1<kFused>(grow + col), v, acc);
+          acc = fmaf(ldG1<kMode == 1>(grow + col), v, acc);
         }
       }
     }
@@ -387,95 +410,160 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
 }
 
 // --------------------------------------------------------------- update units
-// Step a8's first stage, fused: unit (j, cc) sums alpha_i * Y_i over the b rows of block
-// j for the 64 columns cc*64 .. cc*64+63 into part[j][...] (one partial row per block;
-// the reduce kernel then adds the s rows to w).  Threads: 32 row-lanes x 8 column
-// vectors; each waits on the alpha of its own rows.  Units of block j become workable
-// as soon as phase j is done, so only the last block's units (spread over many groups)
-// run after the chain ends.  Fixed order: rows ascending per row-lane, then row-lanes
-// ascending in shared memory.  Y was written by an earlier launch.
-template <bool kFused>
+// Step a8, fused: unit (j, cc) sums alpha_i * Y_i over the b rows of block j for the 64
+// columns cc*64 .. cc*64+63 into part[j][...] (one partial row per block); the last
+// unit of a column chunk adds the chunk's s partial rows to w.  Threads: 32 row-lanes x 8 column
+// vectors.  The unit issues its first rows of Y, then waits as a whole for block j's
+// alpha: thread 0 polls one value of phase j+1 (a final value there implies all of
+// alpha_j is final), or warp 0 polls all of alpha_j for the last block, so a waiting
+// unit costs the memory system one load per back-off instead of one per row.  Units of
+// block j become workable as soon as phase j is done, so only the last block's units
+// (spread over many groups) run after the chain ends.  Fixed order: rows ascending per
+// row-lane, then row-lanes ascending in shared memory.  Y was written by an earlier
+// launch.
+template <int kMode>
 __device__ void update_unit(const RecArgs& a, int u, int rt) {
   __shared__ float red[32][64];
+  __shared__ int s_ready;
   const int nchunk = (int)((a.ldY / 8 + 7) / 8);
   const int j = u / nchunk, cc = u - j * nchunk;
   const int tv = rt & 7, tr = rt >> 3;  // vector-lane, row-lane
   const int64_t vec = (int64_t)cc * 8 + tv;
   const bool vin = vec < a.ldY / 8;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  bool ok = true;
-  for (int i0 = tr; i0 < a.b && ok; i0 += 32 * 4) {
-    float al[4];
-    uint4 q[4];
+  uint4 q[kUpdRows];
+  auto load_rows = [&](int i0) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kUpdRows; ++k) {
       const int i = i0 + 32 * k;
-      const bool in = i < a.b;
       const int64_t row = (int64_t)j * a.b + i;
-      al[k] = in ? ld_volatile_f32(a.alpha + row) : 0.0f;
-      q[k] = (in && vin) ? __ldg(reinterpret_cast<const uint4*>(a.Y + row * a.ldY + vec * 8))
-                         : make_uint4(0, 0, 0, 0);
+      q[k] = (i < a.b && vin)
+                 ? __ldg(reinterpret_cast<const uint4*>(a.Y + row * a.ldY + vec * 8))
+                 : make_uint4(0, 0, 0, 0);
     }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (pending1(al[k])) {  // this row's alpha is not final yet
-        const int64_t row = (int64_t)j * a.b + i0 + 32 * k;
-        const uint64_t t_start = globaltimer_ns();
-        while (pending1(al[k]) && ok) {
+  };
+  load_rows(tr);
+  if (rt < 32) {  // warp 0 waits for block j's alpha
+    bool ok = true;
+    const uint64_t t_start = globaltimer_ns();
+    if (j + 1 < a.s) {
+      if (rt == 0) {
+        const float* pv = a.alpha + (int64_t)(j + 1) * a.b + (int)((blockIdx.x * 37u) % (unsigned)a.b);
+        while (pending1(ld_volatile_f32(pv)) && ok) {
           __nanosleep(200);
-          al[k] = ld_volatile_f32(a.alpha + row);
-          if (pending1(al[k])) ok = keep_waiting(a, t_start, where_code(4, j));
+          ok = keep_waiting(a, t_start, where_code(4, j));
         }
       }
-      const uint32_t pw[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+    } else {
+      for (int i = rt; i < a.b && ok; i += 32) {
+        const float* pv = a.alpha + (int64_t)j * a.b + i;
+        while (pending1(ld_volatile_f32(pv)) && ok) {
+          __nanosleep(200);
+          ok = keep_waiting(a, t_start, where_code(4, j));
+        }
+      }
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (rt == 0) s_ready = ok ? 1 : 0;
+  }
+  group_sync<kMode != 0>();
+  const bool ready = s_ready != 0;  // rewritten only after the group syncs below
+  if (ready) {
+    for (int i0 = tr; i0 < a.b; i0 += 32 * kUpdRows) {
+      if (i0 != tr) load_rows(i0);
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        acc[2 * h] = fmaf(al[k], bf16_bits_to_float(pw[h] & 0xFFFFu), acc[2 * h]);
-        acc[2 * h + 1] = fmaf(al[k], bf16_bits_to_float(pw[h] >> 16), acc[2 * h + 1]);
+      for (int k = 0; k < kUpdRows; ++k) {
+        const int i = i0 + 32 * k;
+        const float al = i < a.b ? __ldcg(a.alpha + (int64_t)j * a.b + i) : 0.0f;
+        const uint32_t pw[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          acc[2 * h] = fmaf(al, bf16_bits_to_float(pw[h] & 0xFFFFu), acc[2 * h]);
+          acc[2 * h + 1] = fmaf(al, bf16_bits_to_float(pw[h] >> 16), acc[2 * h + 1]);
+        }
       }
     }
   }
-  group_sync<kFused>();  // red may still be read by this group's previous unit
 #pragma unroll
   for (int e = 0; e < 8; ++e) red[tr][tv * 8 + e] = acc[e];
-  group_sync<kFused>();
-  if (rt < 64) {
+  group_sync<kMode != 0>();
+  if (rt < 64 && ready) {
     const int col = rt;
     float sum = 0.0f;
     for (int r = 0; r < 32; ++r) sum += red[r][col];
     const int64_t c = (int64_t)cc * 64 + col;
     if (c < a.ldY) a.part[(int64_t)j * a.ldY + c] = sum;
     if (col == 0) stamp_last(a.trace, 2);
+    __threadfence();  // the partial row is visible before this unit is counted
+  }
+  // The last of the s units of column chunk cc adds the s partial rows to w, summing
+  // rows q, q+8, q+16, ... for each q < 8 and then the eight sums in q order.
+  group_sync<kMode != 0>();
+  if (rt == 0)
+    s_ready = ready && atomicAdd(a.upd_chunks + cc, 1u) == (unsigned)(a.s - 1) ? 2 : 0;
+  group_sync<kMode != 0>();
+  if (s_ready == 2 && rt < 64) {
+    __threadfence();
+    const int64_t c = (int64_t)cc * 64 + rt;
+    if (c < a.n) {
+      float sum = 0.0f;
+      for (int q = 0; q < 8; ++q) {
+        float acc_q = 0.0f;
+        for (int pr = q; pr < a.s; pr += 8) acc_q += __ldcg(a.part + (int64_t)pr * a.ldY + c);
+        sum += acc_q;
+      }
+      const float v = a.w[c] + sum;
+      a.w[c] = v;
+      if (!isfinite(v)) atomicOr(&a.ctrl->status, ST_NONFINITE);
+    }
   }
 }
 
 // ------------------------------------------------------------------- bulk role
-// Unit = (block j, 16 rows); each warp owns two rows; a lane's columns are lane*4 + 128k.
-// The group waits as a whole: a final alpha value of phase q implies that phase q-1 is
-// complete (its row needed all of alpha_{q-1}), so thread 0 reads single values of the
-// next phases (spread over the values by CTA index, with a back-off while the next
-// phase is not done) and the group then processes every block known complete, up to kT
-// per pass with all their loads issued together, reading alpha with plain loads.  Each
-// block's dot product is summed over columns first and then added in t order, so the
-// result does not depend on timing.
-template <bool kFused>
-__device__ void bulk_role(const RecArgs& a, int rt) {
+// Far units (block j, 16 rows) come first, in increasing j; each warp owns two rows; a
+// lane's columns are lane*4 + 128k.  The group waits as a whole: a final alpha value of
+// phase q implies that phase q-1 is complete (its row needed all of alpha_{q-1}), so
+// thread 0 reads single values of the next phases (spread over the values by CTA
+// index, with a back-off while the next phase is not done) and the group then
+// processes every block known complete, up to kT per pass with all their loads issued
+// together, reading alpha with plain loads.  Each block's dot product is summed over
+// columns first and then added in t order, so the result does not depend on timing.
+// The first upd_groups bulk groups (`upd_group`; their share of the bulk groups is the
+// update's share of the bulk role's bytes) serve the update units from their own queue,
+// in block order, so the update keeps pace with the chain instead of queueing behind
+// the far units; when no update units are left they turn to far units, and the other
+// groups turn to update units once the far units are gone.
+template <int kMode>
+__device__ void bulk_role(const RecArgs& a, int rt, bool upd_group) {
   __shared__ int s_unit, s_lead;
   const int warp = rt >> 5, lane = rt & 31;
   const int probe_col = (int)((blockIdx.x * 37u) % (unsigned)a.b);
+  bool far_left = true, upd_left = a.upd_units > 0;
   while (true) {
     if (rt == 0) {
-      int u = (int)atomicAdd(&a.ctrl->next_unit, 1u);
+      int u = a.bulk_units + a.upd_units;  // none left
+      for (int pass = 0; pass < 2; ++pass) {
+        const bool take_upd = (pass == 0) == upd_group;
+        if (take_upd && upd_left) {
+          const int v = (int)atomicAdd(&a.ctrl->upd_next, 1u);
+          if (v < a.upd_units) { u = a.bulk_units + v; break; }
+          upd_left = false;
+        } else if (!take_upd && far_left) {
+          const int v = (int)atomicAdd(&a.ctrl->next_unit, 1u);
+          if (v < a.bulk_units) { u = v; break; }
+          far_left = false;
+        }
+      }
       if (ld_volatile_u32(&a.ctrl->abort)) u = a.bulk_units + a.upd_units;
       s_unit = u;
     }
-    group_sync<kFused>();
+    group_sync<kMode != 0>();
     const int unit = s_unit;
-    group_sync<kFused>();
+    group_sync<kMode != 0>();
     if (unit >= a.bulk_units) {
       if (unit < a.bulk_units + a.upd_units) {
-        update_unit<kFused>(a, unit - a.bulk_units, rt);
-        group_sync<kFused>();
+        update_unit<kMode>(a, unit - a.bulk_units, rt);
+        group_sync<kMode != 0>();
         continue;
       }
       return;
@@ -490,7 +578,7 @@ __device__ void bulk_role(const RecArgs& a, int rt) {
     for (int t = 0; t < t_end;) {
       if (rt == 0) {
         bool rows_ok = true;
-        if (kFused && t == 0) {  // the unit's rows of G are stored (first and last row)
+        if (kMode == 1 && t == 0) {  // the unit's rows of G are stored (first and last row)
           const int64_t r0 = (int64_t)j * a.b + c * kRecRows;
           const int last = min(c * kRecRows + kRecRows, a.b) - 1;
           rows_ok = wait_rows_of_G(a, r0, where_code(5, j)) &&
@@ -513,9 +601,9 @@ __device__ void bulk_role(const RecArgs& a, int rt) {
         }
         s_lead = lead;
       }
-      group_sync<kFused>();
+      group_sync<kMode != 0>();
       const int nt = s_lead;
-      group_sync<kFused>();
+      group_sync<kMode != 0>();
       if (nt == 0) { ok = false; break; }  // gave up (uniform)
       if (has0) {
         const float* g0 = a.G + (int64_t)i0 * a.b;
@@ -528,8 +616,8 @@ __device__ void bulk_role(const RecArgs& a, int rt) {
               if (u < nt) {
                 const float* gb = g0 + packed_offset(j, t + u, a.b, a.diag) + col;
                 av[u] = __ldcg(reinterpret_cast<const float4*>(a.alpha + (int64_t)(t + u) * a.b + col));
-                x0[u] = ldG4<kFused>(gb);
-                x1[u] = has1 ? ldG4<kFused>(gb + a.b) : make_float4(0.f, 0.f, 0.f, 0.f);
+                x0[u] = ldG4<kMode == 1>(gb);
+                x1[u] = has1 ? ldG4<kMode == 1>(gb + a.b) : make_float4(0.f, 0.f, 0.f, 0.f);
               }
             }
 #pragma unroll
@@ -548,8 +636,8 @@ __device__ void bulk_role(const RecArgs& a, int rt) {
               const float* al = a.alpha + (int64_t)(t + u) * a.b;
               for (int col = lane; col < a.b; col += 32) {
                 const float v = __ldcg(al + col);
-                d0[u] = fmaf(ldG1<kFused>(gb + col), v, d0[u]);
-                if (has1) d1[u] = fmaf(ldG1<kFused>(gb + a.b + col), v, d1[u]);
+                d0[u] = fmaf(ldG1<kMode == 1>(gb + col), v, d0[u]);
+                if (has1) d1[u] = fmaf(ldG1<kMode == 1>(gb + a.b + col), v, d1[u]);
               }
             }
           }
@@ -577,7 +665,7 @@ __device__ void bulk_role(const RecArgs& a, int rt) {
         if (warp == 0) stamp_last(a.trace, 1);
       }
     }
-    group_sync<kFused>();  // every warp of the unit is done before the group claims the next
+    group_sync<kMode != 0>();  // every warp of the unit is done before the group claims the next
   }
 }
 

@@ -142,7 +142,8 @@ typedef struct {
   int32_t n_events;      /* in: length of stage_events                          */
   int32_t gram_kind;     /* out: 1 = tcgen05 Gram kernel used, 2 = CUDA-core,
                             3 = paired-SM tcgen05 Gram and recurrence in one
-                            launch                                              */
+                            launch, 4 = as 3 with the Gram one outer iteration
+                            ahead of the recurrence (casgd_train, iters >= 2)   */
 } casgd_profile_t;
 #define CASGD_STAGE_EVENTS 5
 
@@ -192,7 +193,12 @@ int casgd_outer_step(const casgd_data_t* data, const casgd_params_t* params, flo
 /* `iters` outer iterations k = k0 .. k0+iters-1.  If loss_every > 0, f(w) is
  * evaluated after every loss_every-th iteration and written to host
  * loss_hist[iters/loss_every].  Blocks at the end (one stream synchronize) and
- * returns the first sticky device error, which it clears.  prof may be NULL. */
+ * returns the first sticky device error, which it clears.  prof may be NULL.
+ * Where the paired-SM Gram shares its launch with the recurrence (see
+ * CASGD_FLAG_NO_FUSE) and iters >= 2, the Gram of iteration k+1 runs in the launch
+ * of iteration k's recurrence (its rows do not depend on w), on second Y and G
+ * buffers that casgd_workspace_size includes for such parameters; the results are
+ * bit-identical to iters calls of casgd_outer_step. */
 int casgd_train(const casgd_data_t* data, const casgd_params_t* params, float* w,
                 uint64_t k0, int32_t iters, void* ws, size_t ws_bytes, void* stream,
                 int32_t loss_every, double* loss_hist, casgd_profile_t* prof);

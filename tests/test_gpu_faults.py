@@ -74,6 +74,24 @@ def test_stall_in_fused_launch_times_out_and_context_survives(gpu_lib):
     assert torch.isfinite(w).all() and torch.count_nonzero(w).item() > 0
 
 
+def test_stall_in_pipelined_train_times_out(gpu_lib):
+    """casgd_train with the next Gram in the recurrence's launch: a stalled recurrence
+    ends the run with CASGD_ERR_TIMEOUT; the workspace works again afterwards."""
+    casgd = gpu_lib
+    p, data = _data(casgd, cid=2, m=20000)
+    r = p.recipe
+    stall = casgd.Params(r.b, r.s, r.eta, r.loss, flags=casgd.FLAG_TEST_STALL, timeout_us=20000)
+    ws = casgd.workspace(data, stall)
+    w = torch.zeros(p.n, device="cuda")
+    with pytest.raises(casgd.CasgdError) as e:
+        casgd.train(data, stall, w, 3, ws)
+    assert e.value.code == 5
+    w.zero_()
+    _, _, kind = casgd.train(data, casgd.Params(r.b, r.s, r.eta, r.loss), w, 2, ws)
+    assert kind == 4
+    assert torch.isfinite(w).all() and torch.count_nonzero(w).item() > 0
+
+
 def test_nonfinite_weights_reported(gpu_lib):
     casgd = gpu_lib
     p, data = _data(casgd, cid=5, m=5000)
