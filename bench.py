@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--s", type=int, default=None, help="override s (recipe 4 sweep)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flags", type=lambda v: int(v, 0), default=0,
+                    help="casgd_params_t.flags for profiling variants (e.g. 0x40: Gram and "
+                         "recurrence in separate launches)")
     return ap.parse_args()
 
 
@@ -131,10 +134,15 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            # the sampler is live (first line read) before the timed region starts
+            t_end = time.time() + 3.0
+            while not self.lines and time.time() < t_end:
+                time.sleep(0.01)
+            self.lines.clear()
         except OSError:
             self.proc = None
         return self
@@ -259,7 +267,7 @@ def run_ours(args):
     data = casgd.Dataset.from_fp32(X32, y)
     del X32
     torch.cuda.synchronize()
-    params = casgd.Params(r.b, s, r.eta, r.loss, seed=rank)
+    params = casgd.Params(r.b, s, r.eta, r.loss, seed=rank, flags=args.flags)
     ws = casgd.workspace(data, params)
     w = torch.zeros(r.n, device="cuda")
     stream = torch.cuda.current_stream()
@@ -382,7 +390,8 @@ def run_ours(args):
                "steps": args.steps, "warmup": args.warmup,
                "ms_per_step": elapsed * 1e3 / args.steps, "higher_is_better": True,
                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-               "config": workload_config(r, s, iters, S),
+               "config": dict(workload_config(r, s, iters, S),
+                              **({"flags": hex(args.flags)} if args.flags else {})),
                "parallelism": "replicas" if world > 1 else "single",
                "gpu_launches": launches_total,
                "roofline": roof, "stages": stages_out,
