@@ -51,26 +51,29 @@ def parse():
     ap.add_argument("--s", type=int, default=None, help="override s (recipe 4 sweep)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--m", type=int, default=None,
+                    help="override the row count (small profiling captures only)")
     ap.add_argument("--flags", type=lambda v: int(v, 0), default=0,
                     help="casgd_params_t.flags for profiling variants (e.g. 0x40: Gram and "
                          "recurrence in separate launches)")
     return ap.parse_args()
 
 
-def workload(cfg: int, s_override):
+def workload(cfg: int, s_override, m_override=None):
     r = si.RECIPES[cfg]
     s = s_override or r.s
-    iters = r.outer_iters(s=s)
+    iters = r.outer_iters(m=m_override, s=s)
     return r, s, iters
 
 
-def workload_config(r, s, iters, S):
-    return {"workload": f"{si.LOSS_NAMES[r.loss]} CA-SGD, dense X {r.m}x{r.n} BF16, "
+def workload_config(r, s, iters, S, m=None):
+    m = r.m if m is None else m
+    return {"workload": f"{si.LOSS_NAMES[r.loss]} CA-SGD, dense X {m}x{r.n} BF16, "
                         f"b={r.b}, s={s} (Gram {S}x{S}), eta={r.eta}, {iters} outer iterations "
                         f"+ 1 full-data loss per step, seed 0",
-            "m": r.m, "n": r.n, "b": r.b, "s": s, "S": S, "outer_iters_per_step": iters,
+            "m": m, "n": r.n, "b": r.b, "s": s, "S": S, "outer_iters_per_step": iters,
             "loss": si.LOSS_NAMES[r.loss],
-            "l2_policy": f"inputs larger than L2: X is {r.m * ((r.n + 7) // 8 * 8) * 2 / 1e9:.2f} GB "
+            "l2_policy": f"inputs larger than L2: X is {m * ((r.n + 7) // 8 * 8) * 2 / 1e9:.2f} GB "
                          "and each outer iteration gathers fresh random rows"}
 
 
@@ -259,9 +262,9 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     casgd.load()
 
-    r, s, iters = workload(args.config, args.s)
+    r, s, iters = workload(args.config, args.s, args.m)
     S = r.b * s
-    p = si.make_problem(args.config)
+    p = si.make_problem(args.config, m=args.m)
     X32 = torch.from_numpy(p.X).cuda()
     y = torch.from_numpy(p.y).cuda()
     data = casgd.Dataset.from_fp32(X32, y)
@@ -319,7 +322,7 @@ def run_ours(args):
     samples = S * iters * args.steps * world
     value = samples / elapsed
     pk = peaks()
-    work = alg_work(r.n, S, s, r.b, r.m)
+    work = alg_work(r.n, S, s, r.b, p.m)
     # kind 3/4: the Gram (4: of the next iteration), the recurrence and the update's
     # first stage share one launch
     # (its time is the "gram" stage; the "recurrence" stage is then empty)
@@ -390,7 +393,7 @@ def run_ours(args):
                "steps": args.steps, "warmup": args.warmup,
                "ms_per_step": elapsed * 1e3 / args.steps, "higher_is_better": True,
                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-               "config": dict(workload_config(r, s, iters, S),
+               "config": dict(workload_config(r, s, iters, S, p.m),
                               **({"flags": hex(args.flags)} if args.flags else {})),
                "parallelism": "replicas" if world > 1 else "single",
                "gpu_launches": launches_total,
