@@ -124,8 +124,10 @@ __global__ void __launch_bounds__(256) update_reduce_kernel(const float* __restr
   }
 }
 
-// Loss: groups of G lanes per row (as in the gather), grid-stride over rows.
-__global__ void __launch_bounds__(256) loss_kernel(const uint16_t* __restrict__ X,
+// Loss: groups of G lanes per row (as in the gather), grid-stride over rows; w is
+// staged in shared memory once per CTA, and each warp issues its next row's loads
+// before it sums the current row.
+__global__ void __launch_bounds__(256, 2) loss_kernel(const uint16_t* __restrict__ X,
                                                    const float* __restrict__ y, int64_t m,
                                                    int64_t n, int64_t ld, int loss,
                                                    const float* __restrict__ w,
@@ -140,51 +142,66 @@ __global__ void __launch_bounds__(256) loss_kernel(const uint16_t* __restrict__ 
   const int64_t nvec = (n + 7) / 8;
   const int64_t rows_per_pass = (int64_t)gridDim.x * 8 * rows_per_warp;
   constexpr int kBatch = 8;
-  // w read as float4 when it is 16-byte aligned and n is a multiple of 8
-  const bool w_vec = ((reinterpret_cast<uintptr_t>(w) & 15u) == 0) && (n % 8 == 0);
+  extern __shared__ __align__(16) float w_s[];  // w, zero padded to a multiple of 8
+  for (int64_t c = threadIdx.x; c < nvec * 8; c += blockDim.x) w_s[c] = c < n ? w[c] : 0.0f;
+  __syncthreads();
   double mine = 0.0;
-  for (int64_t base = ((int64_t)blockIdx.x * 8 + warp) * rows_per_warp; base < m;
-       base += rows_per_pass) {
-    const int64_t row = base + lane / G;
-    const bool live = row < m;
-    float acc = 0.0f;
-    if (live) {
-      const uint16_t* xr = X + row * ld;
+  // FP32 dot of row `row` with w from the kBatch vectors in q starting at vector v0
+  auto dot_batch = [&](const uint4 (&q)[kBatch], int64_t v0, float acc) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int64_t c0 = (v0 + (int64_t)u * G) * 8;
+      if (c0 >= n) break;
+      float wv[8];
+      const float4 w0 = *reinterpret_cast<const float4*>(w_s + c0);
+      const float4 w1 = *reinterpret_cast<const float4*>(w_s + c0 + 4);
+      wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
+      wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
+      const uint32_t pw[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int64_t c = c0 + 2 * h;
+        if (c < n) acc = fmaf(bf16_bits_to_float(pw[h] & 0xFFFFu), wv[2 * h], acc);
+        if (c + 1 < n) acc = fmaf(bf16_bits_to_float(pw[h] >> 16), wv[2 * h + 1], acc);
+      }
+    }
+    return acc;
+  };
+  auto load_batch = [&](uint4 (&q)[kBatch], int64_t row, int64_t v0) {
+    const uint16_t* xr = X + row * ld;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int64_t v = v0 + (int64_t)u * G;
+      q[u] = (row < m && v < nvec) ? __ldg(reinterpret_cast<const uint4*>(xr + v * 8))
+                                   : make_uint4(0, 0, 0, 0);
+    }
+  };
+  auto finish_row = [&](float acc, int64_t row) {
+    for (int off = G >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);
+    if (row < m && g == 0) mine += (double)loss_value(loss, acc, __ldg(y + row));
+  };
+  const int64_t first = ((int64_t)blockIdx.x * 8 + warp) * rows_per_warp + lane / G;
+  if (nvec <= (int64_t)G * kBatch) {
+    // one batch per row: the next row's loads are issued before this row is summed
+    uint4 q[kBatch], qn[kBatch];
+    load_batch(q, first, g);
+    for (int64_t row = first; row - lane / G < m; row += rows_per_pass) {
+      load_batch(qn, row + rows_per_pass, g);
+      finish_row(dot_batch(q, g, 0.0f), row);
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) q[u] = qn[u];
+    }
+  } else {
+    for (int64_t row = first; row - lane / G < m; row += rows_per_pass) {
+      float acc = 0.0f;
       // Issue up to kBatch 16-byte loads of the row before using any of them.
       for (int64_t v0 = g; v0 < nvec; v0 += (int64_t)G * kBatch) {
         uint4 q[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int64_t v = v0 + (int64_t)u * G;
-          q[u] = v < nvec ? __ldg(reinterpret_cast<const uint4*>(xr + v * 8))
-                          : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int64_t c0 = (v0 + (int64_t)u * G) * 8;
-          if (c0 >= n) break;
-          float wv[8];
-          if (w_vec) {
-            const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + c0));
-            const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + c0 + 4));
-            wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
-            wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) wv[e] = c0 + e < n ? __ldg(w + c0 + e) : 0.0f;
-          }
-          const uint32_t pw[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int64_t c = c0 + 2 * h;
-            if (c < n) acc = fmaf(bf16_bits_to_float(pw[h] & 0xFFFFu), wv[2 * h], acc);
-            if (c + 1 < n) acc = fmaf(bf16_bits_to_float(pw[h] >> 16), wv[2 * h + 1], acc);
-          }
-        }
+        load_batch(q, row, v0);
+        acc = dot_batch(q, v0, acc);
       }
+      finish_row(acc, row);
     }
-    for (int off = G >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);
-    if (live && g == 0) mine += (double)loss_value(loss, acc, __ldg(y + row));
   }
   for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
   if (lane == 0) red[warp] = mine;
@@ -255,11 +272,21 @@ cudaError_t launch_loss(const casgd_data_t& d, int loss, const float* w, double*
   const int G = pow2_at_least((d.n + 7) / 8, 32);
   const int64_t rows_per_cta = 8 * (32 / G);
   int64_t blocks = (d.m + rows_per_cta - 1) / rows_per_cta;
-  const int cap = loss_ctas(c.num_sms);
+  const size_t smem = (size_t)((d.n + 7) / 8 * 8) * sizeof(float);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(loss_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, loss_kernel, 256, smem);
+  if (e != cudaSuccess) return e;
+  int cap = (per_sm > 0 ? per_sm : 1) * c.num_sms;  // one resident wave
+  if (cap > loss_ctas(c.num_sms)) cap = loss_ctas(c.num_sms);
   if (blocks > cap) blocks = cap;
-  loss_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>(static_cast<const uint16_t*>(d.X), d.y,
-                                                      d.m, d.n, d.ld, loss, w, part, out_dev,
-                                                      ctrl, G);
+  loss_kernel<<<(unsigned)blocks, 256, smem, c.stream>>>(static_cast<const uint16_t*>(d.X), d.y,
+                                                         d.m, d.n, d.ld, loss, w, part, out_dev,
+                                                         ctrl, G);
   ++c.launches;
   return cudaGetLastError();
 }
