@@ -55,7 +55,6 @@ struct Ctrl {
   uint32_t upd_next;      // recurrence: update-unit queue (zeroed by the gather kernel)
   uint32_t diag;          // which wait timed out last: kind << 24 | block << 12 | value seen
   uint32_t pad0[2];
-  uint32_t block_done[kMaxS];  // recurrence: chain CTAs done per phase (zeroed per step)
 };
 static_assert(sizeof(Ctrl) <= 512, "control block");
 

@@ -785,7 +785,8 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
     // the first C CTAs run chain groups, the others the bulk role
     const int rt = threadIdx.x - kThreads;
     if ((int)blockIdx.x < rec.C)
-      chain_role<kRecV == 1 ? 1 : 2, kRecV == 1 ? 8 : (kRecV == 2 ? 4 : 2), kNext ? 2 : 1>(
+      chain_role<kRecV == 1 ? 1 : (kRecV == 2 ? 2 : 3), kRecV == 1 ? 8 : (kRecV == 2 ? 4 : 2),
+                 kNext ? 2 : 1>(
           rec, blockIdx.x, rt);
     else
       bulk_role<kNext ? 2 : 1>(rec, rt, (int)blockIdx.x - rec.C < rec.upd_groups);

@@ -83,7 +83,6 @@ __device__ void reset_recurrence(const RowArgs& a) {
     a.ctrl->upd_next = 0;
     a.ctrl->abort = (a.ctrl->status & ST_TIMEOUT) ? 1u : 0u;  // stays set after a timeout
   }
-  for (int j = threadIdx.x; j < kMaxS; j += blockDim.x) a.ctrl->block_done[j] = 0;
   const int64_t nslab = (a.S + 255) / 256 * 8;  // the Gram's 32-row counters
   for (int64_t j = threadIdx.x; j < nslab; j += blockDim.x) a.slab[j] = 0;
   uint32_t* chunks = upd_chunk_counters(a.slab);  // the update's column counters

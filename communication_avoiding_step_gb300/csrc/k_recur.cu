@@ -47,7 +47,8 @@ RecArgs make_rec_args(const float* G, const uint16_t* r, const float* yY, float*
   a.Uc = (b + kChainRows - 1) / kChainRows;
   a.vec4 = (b % 4) == 0;
   // band width: two blocks while a chain lane can hold both in registers
-  a.B = (a.vec4 && (b + 127) / 128 <= 4) ? 2 : 1;
+  // band width: as many blocks as a chain lane can hold in registers
+  a.B = !a.vec4 ? 1 : (b + 127) / 128 <= 2 ? 3 : (b + 127) / 128 <= 4 ? 2 : 1;
   a.bulk_units = 0;  // far units: (block, chunk of kT blocks) pairs x row units
   for (int j = a.B + 1; j < s; ++j) a.bulk_units += a.U;
   a.coef = -(eta / (float)b);
@@ -71,7 +72,7 @@ cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, flo
   RecArgs a = make_rec_args(G, r, yY, alpha, far, counters, b, s, eta, loss, flags, timeout_us,
                             ctrl, Y, ldY, n, part, w);
   const int v = chain_variant(a);
-  const void* fn = v == 3   ? (const void*)recur_kernel<2, 2>
+  const void* fn = v == 3   ? (const void*)recur_kernel<3, 2>
                    : v == 2 ? (const void*)recur_kernel<2, 4>
                             : (const void*)recur_kernel<1, 8>;
   int per_sm = 0;

@@ -14,7 +14,7 @@
 // complete; 1 shared CTA, rows of G still being stored by the same launch; 2 shared
 // CTA, G complete (the launch computes the next iteration's Gram):
 //  * chain groups (the first C): one warp per row, 8-row groups.  Phase j of a row
-//    needs only the band  sum_{t=j-B}^{j-1} G_{j,t} alpha_t  (B = 1 or 2 blocks) on top
+//    needs only the band  sum_{t=j-B}^{j-1} G_{j,t} alpha_t  (B = 1 to 3 blocks) on top
 //    of far_j (below).  The warp has its band rows of G in registers before it waits
 //    (loaded while it waited in the previous phase), then waits for alpha_{j-1} and
 //    far_j by loading exactly those values until none holds the pending pattern.
@@ -75,11 +75,11 @@ struct RecArgs {
 };
 
 // Register layout of a chain lane: kB band blocks x kKB float4 slots per block.
-// 1: (1, 8) for b > 512 or b % 4 != 0; 2: (2, 4) for 256 < b <= 512; 3: (2, 2).
+// 1: (1, 8) for b > 512 or b % 4 != 0; 2: (2, 4) for 256 < b <= 512; 3: (3, 2) for
+// b <= 256 (a wider band leaves the far sums one more phase of slack).
 inline int chain_variant(const RecArgs& a) {
-  const int nk = (a.b + 127) / 128;
-  if (a.B != 2) return 1;
-  return nk <= 2 ? 3 : 2;
+  if (a.B == 3) return 3;
+  return a.B == 2 ? 2 : 1;
 }
 
 // Bulk groups that serve the update queue first, out of nbulk: the update's share of
@@ -311,10 +311,11 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
     const float* aprev = a.alpha + (int64_t)(j - 1) * a.b + lane * 4;
     const bool poll_alpha = a.vec4 && j > 0 && j != jprev;
     if (poll_alpha) {
-      if (kB == 2) {
+      // slot row tb holds alpha_{j-1-tb}: shift the rows of the previous phase down
 #pragma unroll
-        for (int k = 0; k < kKB; ++k) av[kB - 1][k] = av[0][k];  // alpha_{j-2}
-      }
+      for (int tb = kB - 1; tb >= 1; --tb)
+#pragma unroll
+        for (int k = 0; k < kKB; ++k) av[tb][k] = av[tb - 1][k];
 #pragma unroll
       for (int k = 0; k < kKB; ++k) {
         if (lane * 4 + 128 * k < a.b) {

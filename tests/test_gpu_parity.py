@@ -319,3 +319,30 @@ def test_final_loss_within_half_percent_of_fp64_sgd(gpu_lib, cid):
     # the device loss kernel agrees with the oracle on the BF16 data at the final w
     assert abs(hist[-1] - oracle.full_loss(oracle.bf16_round(p.X), p.y, w_gpu, r.loss)) \
         <= LOSS_TOL * abs(hist[-1])
+
+
+def test_chain_trace_timeline(gpu_lib):
+    """The opt-in chain timeline (CASGD_FLAG_TRACE_CHAIN, casgd_chain_trace): per phase,
+    start <= loads issued <= inputs final <= alpha stored, phases in order, and the
+    summary row records the Gram's last tile, the last far sum and the last update
+    partial of a launch shared with the Gram (recipe 2 shape, one outer iteration)."""
+    casgd = gpu_lib
+    p = si.make_problem(2, m=20000)
+    r = p.recipe
+    data = _dev(p, casgd)
+    params = casgd.Params(r.b, r.s, r.eta, r.loss, flags=casgd.FLAG_TRACE_CHAIN)
+    ws = casgd.workspace(data, params)
+    w = torch.zeros(p.n, device="cuda")
+    casgd.outer_step(data, params, w, 0, ws)
+    assert casgd.get_status(ws) == 0
+    tr = np.array(casgd.chain_trace(data, params, ws), dtype=np.uint64).astype(np.int64)
+    assert tr.shape == (r.s + 1, 4)
+    ph = tr[: r.s]
+    assert np.all(ph > 0)
+    assert np.all(np.diff(ph, axis=1) >= 0)               # within a phase
+    assert np.all(ph[1:, 0] >= ph[:-1, 3])                # phases in order
+    gram_end, far_end, upd_end, zero = tr[r.s]
+    assert zero == 0 and gram_end > ph[0, 0] and far_end > ph[0, 0]
+    assert upd_end >= ph[r.s - 1, 3]                      # the last block's update follows it
+    span_us = (upd_end - ph[0, 0]) / 1e3
+    assert 1.0 < span_us < 1e5
