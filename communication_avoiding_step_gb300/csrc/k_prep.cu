@@ -147,16 +147,26 @@ __device__ __forceinline__ void gather_rows(const RowArgs& a, int64_t blk) {
             for (int e = 0; e < 8; ++e) wv[e] = c0 + e < a.n ? __ldg(a.w + c0 + e) : 0.0f;
           }
         }
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int64_t c = c0 + 2 * h;
-          uint32_t lo = parts[h] & 0xFFFFu, hi = parts[h] >> 16;
-          if (c >= a.n) lo = 0;
-          if (c + 1 >= a.n) hi = 0;
-          parts[h] = lo | (hi << 16);
+        if (c0 + 8 <= a.n) {  // the whole vector holds features: no masking
           if (kMargin) {
-            if (c < a.n) acc = fmaf(bf16_bits_to_float(lo), wv[2 * h], acc);
-            if (c + 1 < a.n) acc = fmaf(bf16_bits_to_float(hi), wv[2 * h + 1], acc);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              acc = fmaf(__uint_as_float(parts[h] << 16), wv[2 * h], acc);
+              acc = fmaf(__uint_as_float(parts[h] & 0xFFFF0000u), wv[2 * h + 1], acc);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int64_t c = c0 + 2 * h;
+            uint32_t lo = parts[h] & 0xFFFFu, hi = parts[h] >> 16;
+            if (c >= a.n) lo = 0;
+            if (c + 1 >= a.n) hi = 0;
+            parts[h] = lo | (hi << 16);
+            if (kMargin) {
+              if (c < a.n) acc = fmaf(bf16_bits_to_float(lo), wv[2 * h], acc);
+              if (c + 1 < a.n) acc = fmaf(bf16_bits_to_float(hi), wv[2 * h + 1], acc);
+            }
           }
         }
         if (kCopy)

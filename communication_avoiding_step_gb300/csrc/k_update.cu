@@ -158,11 +158,19 @@ __global__ void __launch_bounds__(256, 2) loss_kernel(const uint16_t* __restrict
       wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
       wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
       const uint32_t pw[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+      if (c0 + 8 <= n) {  // the whole vector holds features
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int64_t c = c0 + 2 * h;
-        if (c < n) acc = fmaf(bf16_bits_to_float(pw[h] & 0xFFFFu), wv[2 * h], acc);
-        if (c + 1 < n) acc = fmaf(bf16_bits_to_float(pw[h] >> 16), wv[2 * h + 1], acc);
+        for (int h = 0; h < 4; ++h) {
+          acc = fmaf(__uint_as_float(pw[h] << 16), wv[2 * h], acc);
+          acc = fmaf(__uint_as_float(pw[h] & 0xFFFF0000u), wv[2 * h + 1], acc);
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int64_t c = c0 + 2 * h;
+          if (c < n) acc = fmaf(bf16_bits_to_float(pw[h] & 0xFFFFu), wv[2 * h], acc);
+          if (c + 1 < n) acc = fmaf(bf16_bits_to_float(pw[h] >> 16), wv[2 * h + 1], acc);
+        }
       }
     }
     return acc;
