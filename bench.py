@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--s", type=int, default=None, help="override s (recipe 4 sweep)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sgd", action="store_true",
+                    help="skip the FP32 plain SGD comparison leg")
     ap.add_argument("--m", type=int, default=None,
                     help="override the row count (small profiling captures only)")
     ap.add_argument("--flags", type=lambda v: int(v, 0), default=0,
@@ -268,7 +270,8 @@ def run_ours(args):
     X32 = torch.from_numpy(p.X).cuda()
     y = torch.from_numpy(p.y).cuda()
     data = casgd.Dataset.from_fp32(X32, y)
-    del X32
+    if args.no_sgd:
+        del X32
     torch.cuda.synchronize()
     params = casgd.Params(r.b, s, r.eta, r.loss, seed=rank, flags=args.flags)
     ws = casgd.workspace(data, params)
@@ -355,6 +358,40 @@ def run_ours(args):
     roof["units_per_launch"] = "one outer iteration (S rows)"
 
     # ---- end to end: host buffers, copies inside the timed region ----------------
+    # ---- FP32 plain minibatch SGD on the same rows (the paper's comparison) -----
+    sgd = None
+    if not args.no_sgd:
+        sws = casgd.sgd_workspace(r.b)
+        wsg = torch.zeros(r.n, device="cuda")
+        sgd_params = casgd.Params(r.b, 1, r.eta, r.loss, seed=rank)
+        nsteps = iters * s  # one CA-SGD step's minibatches
+        casgd.sgd_fp32(X32, y, sgd_params, wsg, nsteps, sws, q0=0)  # warm-up
+        torch.cuda.synchronize()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for i in range(args.steps):
+            wsg.zero_()
+            casgd.sgd_fp32(X32, y, sgd_params, wsg, nsteps, sws, q0=(i + 1) * nsteps)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        sgd_elapsed = s0.elapsed_time(s1) / 1e3
+        # final loss on the rows of the last timed CA-SGD step, from w = 0
+        wsg.zero_()
+        casgd.sgd_fp32(X32, y, sgd_params, wsg, nsteps, sws, q0=(k - iters) * s)
+        f_sgd = casgd.loss(data, r.loss, wsg, ws)
+        st = casgd.get_status(sws)
+        value_sgd = S * iters * args.steps / sgd_elapsed
+        f_ca = hist[0] if hist else None
+        sgd = {"value": value_sgd, "unit": "samples/s",
+               "kind": "FP32 plain minibatch SGD on FP32 X (casgd_sgd_fp32), the same rows",
+               "steps_per_rep": nsteps, "ms_per_rep": sgd_elapsed * 1e3 / args.steps,
+               "ca_sgd_over_sgd": value / value_sgd if value_sgd > 0 else None,
+               "final_loss": f_sgd, "ca_sgd_final_loss": f_ca,
+               "final_loss_gap": abs(f_ca - f_sgd) / f_sgd if f_ca is not None else None,
+               "status": st}
+        del X32
+
     e2e = None
     if not args.no_e2e:
         Xh = data.X.cpu().pin_memory()
@@ -401,7 +438,8 @@ def run_ours(args):
                "loss_and_gaps_ms_per_step": loss_ms,
                "gram_tflops": stages_out["gram"]["TFLOP/s"],
                "final_loss": hist[0] if hist else None,
-               "clocks": clocks.summary(), "e2e": e2e, "cpu_baseline": cpu}
+               "clocks": clocks.summary(), "e2e": e2e, "cpu_baseline": cpu,
+               "fp32_sgd": sgd}
         print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()

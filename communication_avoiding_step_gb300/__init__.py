@@ -204,6 +204,26 @@ def chain_trace(data: Dataset, params: Params, ws: torch.Tensor, stream=None) ->
     return [tuple(out[4 * j + e] for e in range(4)) for j in range(params.s + 1)]
 
 
+def sgd_workspace(b: int, device="cuda") -> torch.Tensor:
+    """Zeroed workspace for sgd_fp32 with minibatch size b."""
+    nb = C.c_size_t(0)
+    _check(load().casgd_sgd_workspace_size(b, C.byref(nb)), "casgd_sgd_workspace_size")
+    return torch.zeros(nb.value, dtype=torch.uint8, device=device)
+
+
+def sgd_fp32(X: torch.Tensor, y: torch.Tensor, params: Params, w: torch.Tensor, steps: int,
+             ws: torch.Tensor, q0: int = 0, stream=None) -> None:
+    """FP32 plain minibatch SGD (steps q0 .. q0+steps-1) on FP32 X (m x n, row-major,
+    contiguous rows), the baseline CA-SGD is compared with.  Asynchronous."""
+    _need_cuda(X, "X", torch.float32)
+    _need_cuda(y, "y", torch.float32)
+    _need_cuda(w, "w", torch.float32)
+    m, n = X.shape
+    _check(load().casgd_sgd_fp32(_ptr(X), m, n, X.stride(0), _ptr(y), C.byref(params.c()),
+                                 _ptr(w), q0, steps, _ptr(ws), ws.numel(), _stream(stream)),
+           "casgd_sgd_fp32")
+
+
 def update_static(Y: torch.Tensor, alpha: torch.Tensor, w: torch.Tensor, n: int,
                   stream=None) -> None:
     """w += Y^T alpha without a workspace and without allocating device memory.

@@ -68,6 +68,10 @@ SIGNATURES = {
     "casgd_get_status": (C.c_int, [C.c_void_p, C.c_void_p]),
     "casgd_chain_trace": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p,
                                     C.POINTER(C.c_uint64)]),
+    "casgd_sgd_workspace_size": (C.c_int, [C.c_int32, C.POINTER(C.c_size_t)]),
+    "casgd_sgd_fp32": (C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_int64, C.c_void_p,
+                                 C.c_void_p, C.c_void_p, C.c_uint64, C.c_int32, C.c_void_p,
+                                 C.c_size_t, C.c_void_p]),
     "casgd_update_static": (C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_int64, C.c_void_p,
                                       C.c_void_p, C.c_void_p]),
 }

@@ -491,6 +491,30 @@ int casgd_get_status(void* ws, void* stream) {
   return read_and_clear_status(static_cast<Ctrl*>(ws), static_cast<cudaStream_t>(stream));
 }
 
+int casgd_sgd_workspace_size(int32_t b, size_t* bytes) {
+  if (!bytes || b < 1 || b > (1 << 20)) return CASGD_ERR_ARG;
+  *bytes = sgd_workspace_bytes(b);
+  return CASGD_OK;
+}
+
+int casgd_sgd_fp32(const float* X, int64_t m, int64_t n, int64_t ld, const float* y,
+                   const casgd_params_t* params, float* w, uint64_t q0, int32_t steps, void* ws,
+                   size_t ws_bytes, void* stream) {
+  if (!X || !y || !w || !params || m < 1 || m >= (int64_t(1) << 31) || n < 1 || n > kMaxN ||
+      ld < n || steps < 0)
+    return CASGD_ERR_ARG;
+  if (params->b < 1 || params->b > (1 << 20) || params->loss < CASGD_LOGISTIC ||
+      params->loss > CASGD_POISSON || !(params->eta == params->eta))
+    return CASGD_ERR_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0 ||
+      ws_bytes < sgd_workspace_bytes(params->b))
+    return CASGD_ERR_WORKSPACE;
+  Ctx c{static_cast<cudaStream_t>(stream), 0, 0};
+  if (device_sms(&c.num_sms) != CASGD_OK) return CASGD_ERR_CUDA;
+  CK(launch_sgd_fp32(X, m, n, ld, y, *params, w, q0, steps, ws, c));
+  return CASGD_OK;
+}
+
 int casgd_chain_trace(const casgd_data_t* data, const casgd_params_t* params, void* ws,
                       size_t ws_bytes, void* stream, uint64_t* out) {
   if (!out || !check_params(params) || !data || data->n < 1 || data->n > kMaxN)

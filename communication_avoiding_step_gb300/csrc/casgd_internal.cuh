@@ -8,6 +8,7 @@
 //   k_recur.cu      a6/a7 inner recurrence: persistent chain + bulk CTAs, data-synchronised
 //                   (roles in recur_roles.cuh; also run inside the paired-SM Gram launch)
 //   k_update.cu     a8 weight update, a9 full-data loss
+//   k_sgd.cu        FP32 plain minibatch SGD, the baseline CA-SGD is compared with
 #pragma once
 
 #include <cstddef>
@@ -202,6 +203,11 @@ cudaError_t launch_update(const uint16_t* Y, const float* alpha, int64_t S, int6
                           int64_t ldY, float* w, float* part, int upd_ctas, Ctrl* ctrl,
                           Ctx& c);
 int loss_ctas(int num_sms);
+// FP32 plain minibatch SGD (k_sgd.cu); ws: sgd_workspace_bytes(b), 256-byte aligned.
+size_t sgd_workspace_bytes(int b);
+cudaError_t launch_sgd_fp32(const float* X, int64_t m, int64_t n, int64_t ld, const float* y,
+                            const casgd_params_t& p, float* w, uint64_t q0, int steps, void* ws,
+                            Ctx& c);
 cudaError_t launch_loss(const casgd_data_t& d, int loss, const float* w, double* part,
                         double* out_dev, Ctrl* ctrl, Ctx& c);
 

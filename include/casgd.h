@@ -234,6 +234,24 @@ int casgd_update_static(const void* Y, int64_t S, int64_t n, int64_t ldY,
  * highest-priority CASGD_ERR_* seen) and clears it. */
 int casgd_get_status(void* ws, void* stream);
 
+/* Bytes of device workspace casgd_sgd_fp32 needs for minibatch size b (host only). */
+int casgd_sgd_workspace_size(int32_t b, size_t* bytes);
+
+/* FP32 plain minibatch SGD, the baseline the paper compares CA-SGD with (its speedup
+ * and its final-loss gap are stated against FP32 SGD).  Step q = q0 .. q0+steps-1
+ * samples the rows CA-SGD uses for the same minibatch (counters q*b .. q*b+b-1, see
+ * casgd_sample_indices) and does, in FP32,
+ *     z_i = x_i . w,   alpha_i = -(eta/b) l'(z_i, y_i),   w += sum_i alpha_i x_i.
+ *   X   device FP32 m x ld row-major (ld >= n; columns >= n are not read)
+ *   y   device FP32[m];  w  device FP32[n], updated in place
+ *   params: b, eta, loss, seed and timeout_us are used; s and flags are ignored.
+ *   ws  device workspace of ws_bytes >= casgd_sgd_workspace_size(b), 256-byte aligned;
+ *       device errors are sticky in it (casgd_get_status).
+ * One cooperative launch for all steps; asynchronous. */
+int casgd_sgd_fp32(const float* X, int64_t m, int64_t n, int64_t ld, const float* y,
+                   const casgd_params_t* params, float* w, uint64_t q0, int32_t steps, void* ws,
+                   size_t ws_bytes, void* stream);
+
 /* Profiling: copies the chain timeline of the last outer iteration run with
  * CASGD_FLAG_TRACE_CHAIN on ws (data and params as for that call) to host
  * out[4*j + e], j < params->s: globaltimer nanoseconds when the first chain warp

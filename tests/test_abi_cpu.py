@@ -89,6 +89,23 @@ def test_argument_errors_before_any_cuda_call(lib):
     rc = lib.casgd_sample_indices(0, 10, 0, 0, C.c_void_p(fake), None)
     assert rc == nat.CASGD_ERR_ARG
     assert lib.casgd_get_status(None, None) == nat.CASGD_ERR_WORKSPACE
+    # FP32 SGD: bad shapes, params and workspaces are rejected before any CUDA call
+    nb = C.c_size_t(0)
+    assert lib.casgd_sgd_workspace_size(256, C.byref(nb)) == 0 and nb.value >= 256 * 8
+    assert lib.casgd_sgd_workspace_size(0, C.byref(nb)) == nat.CASGD_ERR_ARG
+    sp = nat.Params(16, 1, 0.1, 0, 0, 0, 0)
+    for args in ((None, 100, 8, 8), (fake, 0, 8, 8), (fake, 100, 8, 4), (fake, 100, 0, 8)):
+        rc = lib.casgd_sgd_fp32(C.c_void_p(args[0]) if args[0] else None, args[1], args[2],
+                                args[3], C.c_void_p(fake), C.byref(sp), C.c_void_p(fake), 0, 5,
+                                C.c_void_p(fake), 1 << 20, None)
+        assert rc == nat.CASGD_ERR_ARG
+    rc = lib.casgd_sgd_fp32(C.c_void_p(fake), 100, 8, 8, C.c_void_p(fake),
+                            C.byref(nat.Params(16, 1, 0.1, 5, 0, 0, 0)), C.c_void_p(fake), 0, 5,
+                            C.c_void_p(fake), 1 << 20, None)
+    assert rc == nat.CASGD_ERR_ARG
+    rc = lib.casgd_sgd_fp32(C.c_void_p(fake), 100, 8, 8, C.c_void_p(fake), C.byref(sp),
+                            C.c_void_p(fake), 0, 5, C.c_void_p(fake + 64), 1 << 20, None)
+    assert rc == nat.CASGD_ERR_WORKSPACE
     assert lib.casgd_workspace_init(C.c_void_p(fake + 64), 4096, None) == nat.CASGD_ERR_WORKSPACE
 
 

@@ -346,3 +346,32 @@ def test_chain_trace_timeline(gpu_lib):
     assert upd_end >= ph[r.s - 1, 3]                      # the last block's update follows it
     span_us = (upd_end - ph[0, 0]) / 1e3
     assert 1.0 < span_us < 1e5
+
+
+SGD_CASES = [
+    # (name, factory, b, steps, eta)
+    ("recipe1", lambda: si.make_problem(1), 16, 40, 0.1),
+    ("recipe2_m20000", lambda: si.make_problem(2, m=20000), 256, 24, 0.5),
+    ("recipe5_m20000", lambda: si.make_problem(5, m=20000), 512, 10, 0.01),
+    ("ragged_777x37_b24", lambda: si.make_random(777, 37, si.LOGISTIC, seed=1), 24, 30, 0.3),
+    ("ragged_500x5_b7_lsq", lambda: si.make_random(500, 5, si.LSQ, seed=2), 7, 50, 0.05),
+]
+
+
+@pytest.mark.parametrize("name,factory,b,steps,eta", SGD_CASES, ids=[c[0] for c in SGD_CASES])
+def test_sgd_fp32_matches_oracle(gpu_lib, name, factory, b, steps, eta):
+    """FP32 plain minibatch SGD on the GPU against the oracle's FP32 plain SGD on the
+    same rows (sampled with the same counters), from a non-zero w, and continued from
+    a later step (q0)."""
+    casgd = gpu_lib
+    p = factory()
+    X = torch.from_numpy(p.X).cuda()
+    y = torch.from_numpy(p.y).cuda()
+    w0 = si.random_weights(p.n, seed=5)
+    params = casgd.Params(b, 1, eta, p.recipe.loss, seed=2)
+    ws = casgd.sgd_workspace(b)
+    w = torch.from_numpy(w0.copy()).cuda()
+    casgd.sgd_fp32(X, y, params, w, steps, ws, q0=3)
+    assert casgd.get_status(ws) == 0
+    want = oracle.plain_sgd(p.X, p.y, b, steps, eta, p.recipe.loss, 2, mode="fp32", w0=w0, q0=3)
+    assert _rel(w.cpu().numpy(), want) <= W_TOL * _len_scale(p.n)

@@ -316,3 +316,23 @@ def test_recipe1_loss_decreases():
                              loss_every=5)
     assert losses[-1] < math.log(2.0) - 0.05
     assert all(np.isfinite(losses))
+
+
+@pytest.mark.parametrize("kind", [LOGISTIC, LSQ, POISSON])
+def test_plain_sgd_fp32_close_to_fp64(kind):
+    """The FP32 plain SGD the paper compares against is the FP64 SGD up to FP32
+    rounding: after a few steps the two weight vectors agree to ~1e-5 relative (each
+    step's sums carry n*u relative error), while a dropped term, a wrong sign or a
+    transposed update would differ at order one."""
+    p = si.make_random(600, 37, kind, seed=11)
+    w64 = oracle.plain_sgd(p.X, p.y, 16, 12, 0.05, kind, 3, mode="fp64")
+    w32 = oracle.plain_sgd(p.X, p.y, 16, 12, 0.05, kind, 3, mode="fp32")
+    assert w32.dtype == np.float32
+    rel = np.linalg.norm(w32 - w64) / np.linalg.norm(w64)
+    assert 0.0 < rel < 1e-5
+    # and a single FP32 step equals the FP64 step rounded, to FP32 accuracy, at w = 0
+    w1 = oracle.plain_sgd(p.X, p.y, 16, 1, 0.05, kind, 3, mode="fp32")
+    idx = oracle.sample_indices(p.m, 16, 3, 0)
+    g0 = oracle.loss_grad(np.zeros(16), p.y[idx].astype(np.float64), kind)
+    ref = p.X[idx].astype(np.float64).T @ (-(0.05 / 16) * g0)
+    assert np.allclose(w1, ref, rtol=1e-5, atol=1e-7)
