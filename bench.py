@@ -37,6 +37,7 @@ METRIC = "SGD samples/s per GB300 (CA-SGD); Gram TFLOP/s and % of roofline"
 STAGES = ("gather", "gram", "recurrence", "update")
 KERNEL_SOURCES = {"gram_tc": ("k_gram_tc.cu",), "gram_simt": ("k_gram_simt.cu",),
                   "gram_recur": ("k_gram_tc.cu", "recur_roles.cuh"),
+                  "gram_recur_far": ("k_gram_tc.cu", "recur_roles.cuh"),
                   "recurrence": ("k_recur.cu", "recur_roles.cuh"), "update": ("k_update.cu",),
                   "gather": ("k_prep.cu",)}
 
@@ -326,10 +327,11 @@ def run_ours(args):
     value = samples / elapsed
     pk = peaks()
     work = alg_work(r.n, S, s, r.b, p.m)
-    # kind 3/4: the Gram (4: of the next iteration), the recurrence and the update's
-    # first stage share one launch
-    # (its time is the "gram" stage; the "recurrence" stage is then empty)
-    gram_name = {1: "gram_tc", 2: "gram_simt", 3: "gram_recur", 4: "gram_recur"}[kind]
+    # kind 3/4/5: the Gram (4: of the next iteration; 5: forming the far sums), the
+    # recurrence and the update share one launch (its time is the "gram" stage; the
+    # "recurrence" stage is then empty)
+    gram_name = {1: "gram_tc", 2: "gram_simt", 3: "gram_recur", 4: "gram_recur",
+                 5: "gram_recur_far"}[kind]
     stages_out = {}
     for st in STAGES:
         t = per_launch_ms[st] / 1e3

@@ -21,6 +21,8 @@ FLAG_GRAM_MULTICAST = 0x10
 FLAG_GRAM_PAIR = 0x20
 FLAG_NO_FUSE = 0x40
 FLAG_TRACE_CHAIN = 0x100
+FLAG_FAR_FROM_GRAM = 0x200
+FLAG_FULL_G = 0x400
 FLAG_TEST_STALL = 0x80000000
 STAGE_EVENTS = 5
 

@@ -35,6 +35,7 @@ struct Resolved {
   float* G2;
   int32_t* idx2;
   float* yY2;
+  float* fpart;  // far partial sums of the far-forming Gram (null: not laid out)
   float* upd;
   double* loss_part;
   double* loss_slots;
@@ -84,6 +85,7 @@ Resolved resolve(void* ws, const Layout& L) {
   R.G2 = L.off_G2 ? reinterpret_cast<float*>(base + L.off_G2) : nullptr;
   R.idx2 = L.off_idx2 ? reinterpret_cast<int32_t*>(base + L.off_idx2) : nullptr;
   R.yY2 = L.off_yY2 ? reinterpret_cast<float*>(base + L.off_yY2) : nullptr;
+  R.fpart = L.off_fpart ? reinterpret_cast<float*>(base + L.off_fpart) : nullptr;
   R.upd = reinterpret_cast<float*>(base + L.off_upd);
   R.loss_part = reinterpret_cast<double*>(base + L.off_loss);
   R.loss_slots = R.loss_part + kLossCtas;
@@ -111,14 +113,17 @@ int gram_choice(const casgd_params_t* p, int64_t S, int64_t n) {
   return tc_ok ? 1 : 2;
 }
 
-// Tensor-core variant (forced by a flag; else CTA pairs with the recurrence in the same
-// launch while the chain's rows fit one warp each on half the SMs, b <= 512; else CTA
-// pairs for deep K (MMA-bound) and multicast clusters for shallow K (bound by writing
-// G), as measured on the five workloads) and whether the recurrence shares its launch.
+// Tensor-core variant (forced by a flag; else CTA pairs forming the far sums in the
+// recurrence's launch for b a multiple of 256; else CTA pairs with the recurrence in the
+// same launch while the chain's rows fit one warp each on half the SMs, b <= 512; else
+// CTA pairs for deep K (MMA-bound) and multicast clusters for shallow K (bound by
+// writing G), as measured on the five workloads) and whether the recurrence shares its
+// launch.
 struct GramPlan {
   int choice;  // 1 tensor cores, 2 CUDA cores, -1 unsupported
   int mode;    // tensor cores: 0 pairs, 1 single CTA, 2 multicast clusters
   bool fused;  // pairs sharing their launch with the recurrence
+  bool far;    // ... and forming the far sums (CASGD_FLAG_FAR_FROM_GRAM)
 };
 
 GramPlan gram_plan(int64_t n, int32_t b, int32_t s, uint32_t flags) {
@@ -137,6 +142,20 @@ GramPlan gram_plan(int64_t n, int32_t b, int32_t s, uint32_t flags) {
            : (fuse_default || n >= 1024) ? 0 : 2;
   g.fused = g.choice == 1 && g.mode == 0 && !(flags & CASGD_FLAG_NO_FUSE) &&
             gram_recur_fused_supported(S, n, b);
+  // The far-forming Gram (pairs in the recurrence's launch, b % 256 == 0): the default
+  // wherever it applies (measured faster than storing G on all five workloads), forced
+  // by FAR_FROM_GRAM (which fails where it cannot apply), off with FULL_G or another
+  // variant flag.
+  const uint32_t other = CASGD_FLAG_GRAM_SIMT | CASGD_FLAG_GRAM_NO_CLUSTER |
+                         CASGD_FLAG_GRAM_MULTICAST | CASGD_FLAG_NO_FUSE | CASGD_FLAG_FULL_G;
+  const bool far_ok = g.choice == 1 && !(flags & other) && far_gram_supported(S, n, b);
+  g.far = far_ok;
+  if (g.far) {
+    g.mode = 0;
+    g.fused = true;
+  } else if (flags & CASGD_FLAG_FAR_FROM_GRAM) {
+    g.choice = -1;
+  }
   return g;
 }
 
@@ -170,8 +189,8 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   if (prof) prof->gram_kind = choice;
 
   if ((rc = record(prof, it, 0, st)) != CASGD_OK) return rc;
-  CK(launch_gather(*d, *p, w, k, idx_in, R.idx, R.Y, L.ldY, R.r, R.yY, R.alpha, R.far, R.ctrl,
-                   R.slab, GATHER_AND_MARGINS, c));
+  CK(launch_gather(*d, *p, w, k, idx_in, R.idx, R.Y, L.ldY, R.r, R.yY, R.alpha, R.far,
+                   gp.far ? R.fpart : nullptr, R.ctrl, R.slab, GATHER_AND_MARGINS, c));
   if ((rc = record(prof, it, 1, st)) != CASGD_OK) return rc;
   // The update's first stage rides in the recurrence (one partial row per block,
   // s <= 64 <= upd_ctas rows of the partial buffer); the reduce adds the s rows to w.
@@ -181,8 +200,8 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
     // Gram and recurrence in one launch.  (The sum of G over processes would split it:
     // on one GPU it is the identity.)
     CK(launch_gram_recur(R.Y, G, false, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss, p->flags,
-                         G, R.Y, R.r, R.yY, R.alpha, R.far, R.slab, R.upd, w, R.ctrl,
-                         p->timeout_us, c));
+                         G, R.Y, R.r, R.yY, R.alpha, R.far, R.slab, gp.far ? R.fpart : nullptr,
+                         R.upd, w, R.ctrl, p->timeout_us, c));
     if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
   } else {
     if (choice == 1)
@@ -194,7 +213,7 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
     CK(launch_recur(G, R.r, R.yY, R.alpha, R.far, R.slab, p->b, p->s, p->eta, p->loss,
                     p->flags, p->timeout_us, R.ctrl, R.Y, L.ldY, d->n, R.upd, w, c));
   }
-  if (prof) prof->gram_kind = fused ? 3 : choice;
+  if (prof) prof->gram_kind = gp.far ? 5 : fused ? 3 : choice;
   // the update (a8) finished inside the recurrence's launch
   if ((rc = record(prof, it, 3, st)) != CASGD_OK) return rc;
   if ((rc = record(prof, it, 4, st)) != CASGD_OK) return rc;
@@ -212,15 +231,18 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
 
 // casgd_train with the paired-SM Gram sharing the recurrence's launch: the Gram of
 // iteration k+1 (whose rows are sampled ahead: only the margins need the current w)
-// runs in the launch of iteration k's recurrence, on double-buffered Y and G.  Every
-// value is computed as in outer_step_impl (same kernels' arithmetic), only the order of
-// independent work changes.  Stage events per iteration: 0 before the gather of the
-// next iteration's rows and this iteration's margins, 1 before the shared launch, 2, 3
-// and 4 after it (it ends with the update).
+// runs in the launch of iteration k's recurrence, on double-buffered Y and G.  With the
+// far-forming Gram (far) the Gram of iteration k runs in iteration k's launch (its far
+// tiles need this iteration's alpha) and only Y is double-buffered: the rows of
+// iteration k+1 are still gathered in the launch that forms iteration k's margins.
+// Every value is computed as in outer_step_impl (same kernels' arithmetic), only the
+// order of independent work changes.  Stage events per iteration: 0 before the gather of
+// the next iteration's rows and this iteration's margins, 1 before the shared launch, 2,
+// 3 and 4 after it (it ends with the update).
 int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, uint64_t k0,
                     int32_t iters, const Layout& L, const Resolved& R, Ctx& c,
                     casgd_profile_t* prof, int32_t loss_every, int& slot, int& flushed,
-                    double* loss_hist) {
+                    double* loss_hist, bool far) {
   uint16_t* Yb[2] = {R.Y, R.Y2};
   float* Gb[2] = {R.G, R.G2};
   int32_t* Ib[2] = {R.idx, R.idx2};
@@ -228,31 +250,37 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   const bool diag = (p->flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
   const cudaStream_t st = c.stream;
   int rc;
-  if (prof) prof->gram_kind = 4;
+  float* fpart = far ? R.fpart : nullptr;
+  if (prof) prof->gram_kind = far ? 5 : 4;
   for (int32_t it = 0; it < iters; ++it) {
     const int cur = it & 1, nxt = cur ^ 1;
     const uint64_t k = k0 + (uint64_t)it;
     if ((rc = record(prof, it, 0, st)) != CASGD_OK) return rc;
-    if (it == 0) {  // prologue: this iteration's rows and Gram
+    if (it == 0) {  // prologue: this iteration's rows (and, one ahead, its Gram)
       CK(launch_gather(*d, *p, w, k, nullptr, Ib[cur], Yb[cur], L.ldY, R.r, yb[cur], R.alpha,
-                       R.far, R.ctrl, R.slab, GATHER_ONLY, c));
-      CK(launch_gram_tc(Yb[cur], L.S, d->n, L.ldY, p->b, p->s, diag, 0, Gb[cur], R.ctrl,
-                        p->timeout_us, c));
+                       R.far, nullptr, R.ctrl, R.slab, GATHER_ONLY, c));
+      if (!far)
+        CK(launch_gram_tc(Yb[cur], L.S, d->n, L.ldY, p->b, p->s, diag, 0, Gb[cur], R.ctrl,
+                          p->timeout_us, c));
     }
     if (it + 1 < iters)  // next iteration's rows (into the buffers the last launch
                          // freed) and this iteration's margins, in one launch
       CK(launch_gather_next_margins(*d, *p, w, k + 1, Ib[nxt], Yb[nxt], yb[nxt], Yb[cur],
-                                    L.ldY, R.r, R.alpha, R.far, R.ctrl, R.slab, c));
+                                    L.ldY, R.r, R.alpha, R.far, fpart, R.ctrl, R.slab, c));
     else
       CK(launch_gather(*d, *p, w, k, nullptr, Ib[cur], Yb[cur], L.ldY, R.r, yb[cur], R.alpha,
-                       R.far, R.ctrl, R.slab, MARGINS_ONLY, c));
+                       R.far, fpart, R.ctrl, R.slab, MARGINS_ONLY, c));
     if ((rc = record(prof, it, 1, st)) != CASGD_OK) return rc;
     // (The sum of G over processes would sit before this launch; on one GPU it is the
     // identity.)
-    if (it + 1 < iters)
+    if (far)
+      CK(launch_gram_recur(Yb[cur], R.G, false, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss,
+                           p->flags, R.G, Yb[cur], R.r, yb[cur], R.alpha, R.far, R.slab, fpart,
+                           R.upd, w, R.ctrl, p->timeout_us, c));
+    else if (it + 1 < iters)
       CK(launch_gram_recur(Yb[nxt], Gb[nxt], true, L.S, d->n, L.ldY, p->b, p->s, p->eta,
                            p->loss, p->flags, Gb[cur], Yb[cur], R.r, yb[cur], R.alpha, R.far,
-                           R.slab, R.upd, w, R.ctrl, p->timeout_us, c));
+                           R.slab, nullptr, R.upd, w, R.ctrl, p->timeout_us, c));
     else
       CK(launch_recur(Gb[cur], R.r, yb[cur], R.alpha, R.far, R.slab, p->b, p->s, p->eta,
                       p->loss, p->flags, p->timeout_us, R.ctrl, Yb[cur], L.ldY, d->n, R.upd, w,
@@ -327,16 +355,23 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms)
   off += align_up((size_t)upd_rows * L.ldY * sizeof(float));
   L.off_G = off;
   off += align_up((size_t)L.gram_elems * sizeof(float));
-  L.off_Y2 = L.off_G2 = L.off_idx2 = L.off_yY2 = 0;
-  if (gram_plan(n, b, s, flags).fused) {  // casgd_train runs the Gram one iteration ahead
+  L.off_Y2 = L.off_G2 = L.off_idx2 = L.off_yY2 = L.off_fpart = 0;
+  const GramPlan gp = gram_plan(n, b, s, flags);
+  if (gp.fused) {  // casgd_train gathers the rows (and runs the Gram) one iteration ahead
     L.off_idx2 = off;
     off += align_up((size_t)L.S * sizeof(int32_t));
     L.off_yY2 = off;
     off += align_up((size_t)L.S * sizeof(float));
     L.off_Y2 = off;
     off += align_up((size_t)L.S * L.ldY * sizeof(uint16_t));
-    L.off_G2 = off;
-    off += align_up((size_t)L.gram_elems * sizeof(float));
+    if (!gp.far) {
+      L.off_G2 = off;
+      off += align_up((size_t)L.gram_elems * sizeof(float));
+    }
+  }
+  if (gp.far) {
+    L.off_fpart = off;
+    off += align_up((size_t)L.S * s * far_partials_per_block(b, s) * sizeof(float));
   }
   L.total = off;
   return L;
@@ -458,9 +493,9 @@ int casgd_train(const casgd_data_t* data, const casgd_params_t* params, float* w
   if (rc != CASGD_OK) return rc;
   Resolved R = resolve(ws, L);
   int slot = 0, flushed = 0;
-  if (iters >= 2 && L.off_G2 != 0) {
+  if (iters >= 2 && L.off_Y2 != 0) {
     rc = train_pipelined(data, params, w, k0, iters, L, R, c, prof, loss_every, slot, flushed,
-                         loss_hist);
+                         loss_hist, L.off_fpart != 0);
     if (rc != CASGD_OK) return rc;
     iters = 0;  // done
   }

@@ -55,7 +55,9 @@ struct Ctrl {
   uint32_t loss_done;     // loss kernel: CTAs finished (zeroed by the loss kernel's last CTA)
   uint32_t upd_next;      // recurrence: update-unit queue (zeroed by the gather kernel)
   uint32_t diag;          // which wait timed out last: kind << 24 | block << 12 | value seen
-  uint32_t pad0[2];
+  uint32_t band_done;     // Gram in the recurrence's launch: tiles stored x 8 warps, as
+                          // released by its epilogue warps (zeroed by the margins step)
+  uint32_t pad0;
 };
 static_assert(sizeof(Ctrl) <= 512, "control block");
 
@@ -65,6 +67,7 @@ struct Layout {
   int upd_ctas;
   size_t off_idx, off_r, off_yY, off_alpha, off_far, off_Y, off_G, off_upd, off_loss;
   size_t off_Y2, off_G2, off_idx2, off_yY2;  // 0: no second buffers
+  size_t off_fpart;  // far partial sums FP32[S][s * npb] of the far-forming Gram (0: none)
   size_t total;
 };
 
@@ -90,6 +93,40 @@ __host__ __device__ inline int pair_group_tiles(int64_t S, int64_t b, bool diag,
   const int64_t tc = (S + 255) / 256;
   const int64_t c = (lim + 255) / 256;
   return (int)(c < tc ? c : tc);
+}
+
+// Band width B of the inner recurrence: phase j adds the blocks t = j-B .. j-1 itself
+// (their rows of G in a chain lane's registers), the far blocks t < j-B come from
+// partial sums formed off the critical path.  As many blocks as a lane holds: 3 for
+// b <= 256, 2 for b <= 512, else 1 (and 1 when b is not a multiple of 4).
+__host__ __device__ inline int band_width(int64_t b) {
+  if (b % 4 != 0) return 1;
+  const int64_t nk = (b + 127) / 128;
+  return nk <= 2 ? 3 : nk <= 4 ? 2 : 1;
+}
+
+// The paired-SM Gram that forms the far sums itself (b a multiple of 256): tiles of
+// its 256-row group g that it stores into G -- the band blocks t = j-B .. j-1 and, on
+// request, the diagonal block, b/256 column tiles each.
+__host__ __device__ inline int far_gram_stored_tiles(int64_t b, bool diag, int g) {
+  const int nb = (int)(b / 256);
+  const int j = g / nb;
+  const int B = band_width(b);
+  return nb * ((j < B ? j : B) + (diag ? 1 : 0));
+}
+
+// Far partial sums per row and block t of the far-forming Gram: the column tiles of a
+// block (b/256) are split into npb groups, each group's tiles summed into one partial
+// by one unit of work.  As many groups as keep a row's partials (s-1-B far blocks at
+// most) within the 64 a recurrence warp adds (two per lane): finer units spread the
+// partials that phase j waits on over more SMs.
+__host__ __device__ inline int far_partials_per_block(int64_t b, int s) {
+  const int nb = (int)(b / 256);
+  int nfb = s - 1 - band_width(b);
+  if (nfb < 1) nfb = 1;
+  for (int npb = nb; npb > 1; --npb)
+    if (nb % npb == 0 && npb * nfb <= 64) return npb;
+  return 1;
 }
 
 // ------------------------------------------------------------------ device helpers
@@ -159,19 +196,21 @@ cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t coun
                           int32_t* idx, Ctx& c);
 // mode: GATHER_AND_MARGINS (sampled rows into Y, labels, indices, BF16 margins and the
 // recurrence's reset), GATHER_ONLY (rows, labels, indices), MARGINS_ONLY (margins of
-// the rows in Y and the reset).  The margins are bit-identical in every mode.
+// the rows in Y and the reset).  The margins are bit-identical in every mode.  The reset
+// fills alpha, far and (fpart non-null) each row's far partials t < j-B with
+// kAlphaPending.
 enum { GATHER_AND_MARGINS = 0, GATHER_ONLY = 1, MARGINS_ONLY = 2 };
 cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const float* w,
                           uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
                           int64_t ldY, uint16_t* r, float* yY, float* alpha, float* far,
-                          Ctrl* ctrl, uint32_t* slab, int mode, Ctx& c);
+                          float* fpart, Ctrl* ctrl, uint32_t* slab, int mode, Ctx& c);
 // GATHER_ONLY for iteration k_next (into Y_next, yY_next, idx_next) and MARGINS_ONLY for
 // the rows in Y, in one launch (the two touch disjoint buffers).
 cudaError_t launch_gather_next_margins(const casgd_data_t& d, const casgd_params_t& p,
                                        const float* w, uint64_t k_next, int32_t* idx_next,
                                        uint16_t* Y_next, float* yY_next, const uint16_t* Y,
                                        int64_t ldY, uint16_t* r, float* alpha, float* far,
-                                       Ctrl* ctrl, uint32_t* slab, Ctx& c);
+                                       float* fpart, Ctrl* ctrl, uint32_t* slab, Ctx& c);
 cudaError_t launch_gram_simt(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
                              int s, bool diag, float* G, Ctx& c);
 bool gram_tc_supported(int64_t S, int64_t n, int b);
@@ -189,14 +228,21 @@ cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, flo
 // stage, on G and Y) in one launch.  next == false: the same iteration (Yg == Y,
 // Gg == G); the Gram's epilogue releases per-32-row counters `slab` (zeroed by the
 // margins step) that the recurrence acquires before it reads rows of G.  next == true:
-// the Gram is the next iteration's and G is complete.  cudaErrorNotSupported when the
-// shape does not fit the fused kernel (the caller then launches them separately).
+// the Gram is the next iteration's and G is complete.  fpart (next == false, b a
+// multiple of 256): the Gram stores only the band blocks (and the diagonal on request)
+// and forms the far sums itself into fpart FP32[S][s * npb] (npb =
+// far_partials_per_block; entries (j-B) * npb of each row of block j filled with
+// kAlphaPending by the margins step), which the recurrence adds.
+// cudaErrorNotSupported when the shape does not fit the fused kernel (the caller then
+// launches them separately).
 bool gram_recur_fused_supported(int64_t S, int64_t n, int b);
+bool far_gram_supported(int64_t S, int64_t n, int b);
 cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t S, int64_t n,
                               int64_t ldY, int b, int s, float eta, int loss, uint32_t flags,
                               const float* G, const uint16_t* Y, const uint16_t* r,
                               const float* yY, float* alpha, float* far, uint32_t* slab,
-                              float* part, float* w, Ctrl* ctrl, uint32_t timeout_us, Ctx& c);
+                              float* fpart, float* part, float* w, Ctrl* ctrl,
+                              uint32_t timeout_us, Ctx& c);
 cudaError_t launch_update_reduce(const float* part, int upd_ctas, int64_t n, int64_t ldY,
                                  float* w, Ctrl* ctrl, Ctx& c);
 cudaError_t launch_update(const uint16_t* Y, const float* alpha, int64_t S, int64_t n,

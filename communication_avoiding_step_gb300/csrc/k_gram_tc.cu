@@ -57,11 +57,19 @@ struct TcArgs {
   Ctrl* ctrl;
   int64_t S;
   int n, b, nkb;
-  int TR, TC, ntiles;
+  int TR, TC, ntiles;  // ntiles: work items (tiles; units of nb tiles when fpart is set)
   bool diag;
   bool tma_store;  // b % 32 == 0: 32x32 chunks go out through a TMA tensor store
   uint64_t timeout_ns;
   uint32_t* slab;  // recurrence in the same launch: per-32-row tile counters (else null)
+  // Far-forming mode (fpart set; b a multiple of 256): only the band blocks (and the
+  // diagonal on request) are stored; each far tile G_{j,t} (t < j-B) is multiplied by
+  // alpha_t once alpha_t is final, and each row's sum over column group c of block t
+  // (uq tiles) goes to fpart[row * fs + t * npb + c].
+  float* fpart;
+  const float* alpha;
+  int s, B, nb;      // steps, band width, 256-wide column tiles per block
+  int npb, uq, fs;   // column groups per block, tiles per group, fpart row stride
 };
 
 struct SharedCtl {
@@ -254,6 +262,65 @@ struct TileCursor {
     }
     rg = g;
     cc = tile - base;
+  }
+};
+
+// Work order of the far-forming mode: units of uq column tiles (one 256-row group g
+// against column group c of block t; npb groups of uq tiles per block).  First every
+// stored unit (they wait on nothing), by phase j ascending: the band blocks t = j-1
+// down to j-B, then the diagonal block (on request).  Then the far units by the phase j
+// that needs them, t ascending within a phase (alpha_t is final earliest for small t).
+// Within a block t, column groups outer, the row groups of block j inner.
+struct FarCursor {
+  int seg = 0, j = 0, base = 0, cnt = -1;  // seg 0: stored units, 1: far units
+  __device__ int count(const TcArgs& a) const {
+    const int nband = j < a.B ? j : a.B;
+    return a.nb * a.npb * (seg == 0 ? nband + (a.diag ? 1 : 0) : j - nband);
+  }
+  __device__ void seek(const TcArgs& a, int u, int& g, int& t, int& c, bool& far) {
+    if (cnt < 0) cnt = count(a);
+    while (u >= base + cnt) {
+      base += cnt;
+      if (++j == a.s) {
+        j = 0;
+        ++seg;
+      }
+      cnt = count(a);
+    }
+    const int per_t = a.nb * a.npb;
+    const int v = u - base;
+    const int tb = v / per_t;
+    const int r = v - tb * per_t;
+    c = r / a.nb;
+    g = j * a.nb + (r - c * a.nb);
+    const int nband = j < a.B ? j : a.B;
+    far = seg == 1;
+    t = far ? tb : (tb < nband ? j - 1 - tb : j);
+  }
+};
+
+// Work items of the paired kernel: single 256x256 tiles in row-group order, or (kFar)
+// the units above.  seek gives the row group, the first column tile, the number of
+// consecutive column tiles, the block t, the unit's partial index within the row
+// (t * npb + c) and whether the unit is far.
+template <bool kFar>
+struct WorkCursor {
+  TileCursor<2> tiles;
+  FarCursor units;
+  __device__ void seek(const TcArgs& a, int u, int& rg, int& ca0, int& nq, int& t, int& pidx,
+                       bool& far) {
+    if (kFar) {
+      int c;
+      units.seek(a, u, rg, t, c, far);
+      ca0 = t * a.nb + c * a.uq;
+      nq = a.uq;
+      pidx = t * a.npb + c;
+    } else {
+      tiles.seek(a, u, rg, ca0);
+      nq = 1;
+      t = pidx = 0;
+      far = false;
+    }
   }
 };
 
@@ -541,12 +608,13 @@ constexpr int kHalfB = 128 * BK * 2;              // 16 KB
 constexpr int kStageBytes2 = kABytes + kHalfB;    // 32 KB per CTA per stage
 constexpr int kStagesPair = 6;                    // Gram alone: 6 x 32 KB + 32 KB staging
 constexpr int kStagesFused = 5;                   // with the recurrence's shared memory
-template <int kSt>
+constexpr int kAlphaStage = 4 * BN * 4;  // far tiles: alpha of a tile, per epilogue warp
+template <int kSt, bool kFar = false>
 constexpr size_t pair_smem_bytes() {
-  return (size_t)kSt * kStageBytes2 + kOutBytes + 1024 + 1024;
+  return (size_t)kSt * kStageBytes2 + kOutBytes + 1024 + (kFar ? kAlphaStage : 0) + 1024;
 }
 static_assert(pair_smem_bytes<kStagesPair>() <= 232448, "dynamic shared memory per CTA");
-static_assert(pair_smem_bytes<kStagesFused>() + 9 * 1024 <= 232448, "with the recurrence");
+static_assert(pair_smem_bytes<kStagesFused, true>() + 9 * 1024 <= 232448, "with the recurrence");
 constexpr int kFusedThreads = kThreads + kRecThreads;  // 6 Gram warps + 8 recurrence warps
 constexpr uint32_t kIdesc2 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                              ((uint32_t)(256 >> 4) << 24);
@@ -628,7 +696,125 @@ __device__ bool mbar_wait2(uint64_t* bar, uint32_t parity, SharedCtl2<kSt>* sc, 
   }
 }
 
-template <int kSt, int kRecV, bool kNext>
+// Far tiles: waits until the 256 values of alpha that multiply the tile's columns are
+// final (loading them until none holds the pending pattern), then stages them in the
+// warp's shared-memory slot.  false when the wait ends without them: the workspace's
+// abort word was raised, or the bound ran out (recorded as a timeout; diag kind 7).
+__device__ __forceinline__ void load_alpha(const float* src, int lane, float4& v0, float4& v1) {
+  v0 = ld_volatile_f4(src + lane * 4);
+  v1 = ld_volatile_f4(src + 128 + lane * 4);
+}
+// v0, v1: this lane's values as loaded earlier (load_alpha), reloaded while pending.
+// While values are pending, lane 0 first polls one of them alone (with a back-off), and
+// the warp reloads its pending values only once that one is final: the chain stores a
+// block's alpha within a short time, and hundreds of waiting warps then put one load
+// each instead of 64 on the lines the chain writes.
+__device__ bool stage_alpha(const TcArgs& a, const float* src, float* dst, int lane,
+                            int where_j, float4 v0, float4 v1) {
+  if (__any_sync(0xffffffffu, pending4(v0) || pending4(v1))) {
+    const uint64_t t0 = globaltimer_ns();
+    // the probe: the first pending value of the lowest lane with one
+    const unsigned who = __ballot_sync(0xffffffffu, pending4(v0) || pending4(v1));
+    const int pl = __ffs(who) - 1;
+    const int pv = __shfl_sync(0xffffffffu, pending4(v0) ? 0 : 1, pl);
+    const float* probe = src + pv * 128 + pl * 4;
+    int fin = 0;  // the probe was seen final (warp-uniform)
+    while (true) {
+      if (!fin) {
+        if (lane == 0) fin = !pending4(ld_volatile_f4(probe));
+        fin = __shfl_sync(0xffffffffu, fin, 0);
+      }
+      if (fin) {
+        if (pending4(v0)) v0 = ld_volatile_f4(src + lane * 4);
+        if (pending4(v1)) v1 = ld_volatile_f4(src + 128 + lane * 4);
+        if (!__any_sync(0xffffffffu, pending4(v0) || pending4(v1))) break;
+      }
+      __nanosleep(fin ? 32 : 128);
+      int stop = 0;
+      if (lane == 0) {
+        if (ld_volatile_u32(&a.ctrl->abort)) {
+          stop = 1;
+        } else if (globaltimer_ns() - t0 > a.timeout_ns) {
+          atomicOr(&a.ctrl->status, ST_TIMEOUT);
+          atomicExch(&a.ctrl->diag, (7u << 24) | ((uint32_t)where_j << 12));
+          atomicExch(&a.ctrl->abort, 1u);
+          stop = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+  }
+  *reinterpret_cast<float4*>(dst + lane * 4) = v0;
+  *reinterpret_cast<float4*>(dst + 128 + lane * 4) = v1;
+  __syncwarp();
+  return true;
+}
+
+// tcgen05.ld of 32 columns without the wait; the registers are valid only after
+// tmem_wait_ld on the same array (which takes them as operands, so no use of them can
+// be scheduled before the wait).
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+        "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+        "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+        "=r"(v[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
+                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
+                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]),
+                 "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                 "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]),
+                 "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+               :
+               : "memory");
+}
+
+__device__ __forceinline__ void far_chunk(const uint32_t (&v)[32], const float* al,
+                                          float (&sum)[8]) {
+  const float4* a4 = reinterpret_cast<const float4*>(al);
+#pragma unroll
+  for (int e4 = 0; e4 < 8; ++e4) {
+    const float4 w = a4[e4];
+    const int o = (e4 & 1) * 4;
+    sum[o + 0] = fmaf(__uint_as_float(v[4 * e4 + 0]), w.x, sum[o + 0]);
+    sum[o + 1] = fmaf(__uint_as_float(v[4 * e4 + 1]), w.y, sum[o + 1]);
+    sum[o + 2] = fmaf(__uint_as_float(v[4 * e4 + 2]), w.z, sum[o + 2]);
+    sum[o + 3] = fmaf(__uint_as_float(v[4 * e4 + 3]), w.w, sum[o + 3]);
+  }
+}
+
+// Adds one far tile's products into the row's eight running sums: accumulator row
+// (TMEM lane 32*quarter + lane, buffer acc) times the staged alpha, columns ascending,
+// column e into sum e % 8.  The load of the next 32 columns is in flight while the
+// current ones are summed.
+__device__ __forceinline__ void far_tile_dot(uint32_t tmem, int acc, int quarter,
+                                             const float* al, float (&sum)[8]) {
+  const uint32_t base = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+  uint32_t va[32], vb[32];
+  __syncwarp();
+  tmem_ld32_issue(base, va);
+  tmem_wait_ld(va);
+#pragma unroll
+  for (int ch = 0; ch < BN / 32; ch += 2) {
+    tmem_ld32_issue(base + (uint32_t)(ch + 1) * 32, vb);
+    far_chunk(va, al + ch * 32, sum);
+    tmem_wait_ld(vb);
+    if (ch + 2 < BN / 32) tmem_ld32_issue(base + (uint32_t)(ch + 2) * 32, va);
+    far_chunk(vb, al + (ch + 1) * 32, sum);
+    if (ch + 2 < BN / 32) tmem_wait_ld(va);
+  }
+}
+
+template <int kSt, int kRecV, bool kNext, bool kFar>
 __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
     gram_tc2sm_kernel(const __grid_constant__ CUtensorMap tmY,
                       const __grid_constant__ CUtensorMap tmG, TcArgs a, RecArgs rec) {
@@ -671,24 +857,28 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // -------------------------------------------------------- TMA producer (both CTAs)
-      TileCursor<2> cur;
+      WorkCursor<kFar> cur;
       int stage = 0;
       uint32_t phase = 0;
-      for (int tile = cid; tile < a.ntiles && !sc->abort; tile += ncl) {
-        int rg, ca;
-        cur.seek(a, tile, rg, ca);
+      for (int u = cid; u < a.ntiles && !sc->abort; u += ncl) {
+        int rg, ca0, nq, t, pidx;
+        bool far;
+        cur.seek(a, u, rg, ca0, nq, t, pidx, far);
         const int ra = 2 * rg + rank;
-        for (int kb = 0; kb < a.nkb; ++kb) {
-          if (!mbar_wait2(&sc->empty[stage], phase ^ 1u, sc, a)) break;
-          uint8_t* sa = smem + (size_t)stage * kStageBytes2;
-          uint8_t* sb = sa + kABytes;
-          if (leader) mbar_expect_tx(&sc->full[stage], 2 * kStageBytes2);  // both CTAs
-          const uint32_t bar = mapa_rank(smem_u32(&sc->full[stage]), 0);
-          tma_load_2d_pair(smem_u32(sa), &tmY, bar, kb * BK, ra * BM);
-          tma_load_2d_pair(smem_u32(sb), &tmY, bar, kb * BK, ca * BN + rank * (BN / 2));
-          if (++stage == kSt) {
-            stage = 0;
-            phase ^= 1u;
+        for (int q = 0; q < nq && !sc->abort; ++q) {
+          const int ca = ca0 + q;
+          for (int kb = 0; kb < a.nkb; ++kb) {
+            if (!mbar_wait2(&sc->empty[stage], phase ^ 1u, sc, a)) break;
+            uint8_t* sa = smem + (size_t)stage * kStageBytes2;
+            uint8_t* sb = sa + kABytes;
+            if (leader) mbar_expect_tx(&sc->full[stage], 2 * kStageBytes2);  // both CTAs
+            const uint32_t bar = mapa_rank(smem_u32(&sc->full[stage]), 0);
+            tma_load_2d_pair(smem_u32(sa), &tmY, bar, kb * BK, ra * BM);
+            tma_load_2d_pair(smem_u32(sb), &tmY, bar, kb * BK, ca * BN + rank * (BN / 2));
+            if (++stage == kSt) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
       }
@@ -696,38 +886,43 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // -------------------------------------------------------- MMA issuer (leader)
+      WorkCursor<kFar> cur;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t tphase[2] = {0, 0};
-      int iter = 0;
-      bool any = false;
-      for (int tile = cid; tile < a.ntiles && !sc->abort; tile += ncl, ++iter) {
-        const int acc = iter & 1;
-        if (!mbar_wait2(&sc->tempty[acc], tphase[acc] ^ 1u, sc, a)) break;
-        tphase[acc] ^= 1u;
-        tc_fence_after();
-        const uint32_t tacc = tmem + (uint32_t)(acc * BN);
-        bool ok = true;
-        for (int kb = 0; kb < a.nkb; ++kb) {
-          if (!mbar_wait2(&sc->full[stage], phase, sc, a)) { ok = false; break; }
+      int iter = 0;  // tiles issued (accumulator buffer iter & 1)
+      bool any = false, ok = true;
+      for (int u = cid; u < a.ntiles && ok && !sc->abort; u += ncl) {
+        int rg, ca0, nq, t, pidx;
+        bool far;
+        cur.seek(a, u, rg, ca0, nq, t, pidx, far);
+        for (int q = 0; q < nq && ok; ++q, ++iter) {
+          const int acc = iter & 1;
+          if (!mbar_wait2(&sc->tempty[acc], tphase[acc] ^ 1u, sc, a)) { ok = false; break; }
+          tphase[acc] ^= 1u;
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes2);
-          const uint32_t sb = sa + kABytes;
-          const uint64_t ad = sdesc_sw128(sa), bd = sdesc_sw128(sb);
-          const int krem = a.n - kb * BK;
-          const int ksteps = krem >= BK ? BK / 16 : (krem + 15) / 16;
-          for (int kk = 0; kk < ksteps; ++kk)
-            mma_bf16_pair(tacc, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
-                          (kb > 0 || kk > 0) ? 1u : 0u);
-          any = true;
-          mma_commit_pair(&sc->empty[stage], 0x3);
-          if (++stage == kSt) {
-            stage = 0;
-            phase ^= 1u;
+          const uint32_t tacc = tmem + (uint32_t)(acc * BN);
+          for (int kb = 0; kb < a.nkb; ++kb) {
+            if (!mbar_wait2(&sc->full[stage], phase, sc, a)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes2);
+            const uint32_t sb = sa + kABytes;
+            const uint64_t ad = sdesc_sw128(sa), bd = sdesc_sw128(sb);
+            const int krem = a.n - kb * BK;
+            const int ksteps = krem >= BK ? BK / 16 : (krem + 15) / 16;
+            for (int kk = 0; kk < ksteps; ++kk)
+              mma_bf16_pair(tacc, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
+                            (kb > 0 || kk > 0) ? 1u : 0u);
+            any = true;
+            mma_commit_pair(&sc->empty[stage], 0x3);
+            if (++stage == kSt) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
+          if (!ok) break;
+          mma_commit_pair(&sc->tfull[acc], 0x3);
         }
-        if (!ok) break;
-        mma_commit_pair(&sc->tfull[acc], 0x3);
       }
       if (any) {  // drain: every MMA complete before the pair frees TMEM
         mma_commit_pair(&sc->drain, 0x1);
@@ -738,44 +933,80 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
     }
   } else if (warp < 6) {
     // ---------------------------------------------------------- epilogue (both CTAs)
+    // Stored tiles: masked or TMA stores into G, then (recurrence in the same launch,
+    // same iteration) the release of the warp's 32-row counter.  Far tiles (kFar): the
+    // row's products with alpha_t summed over the unit's tiles into fpart; once a wait
+    // for alpha has ended without it, the warp only drains its tiles (the Gram warps
+    // always finish their tiles, so every copy and MMA of the launch completes).
     const int quarter = warp & 3;
     uint8_t* stage = out_stage + (warp - 2) * kStageOut;
+    float* al_s = reinterpret_cast<float*>(out_stage + kOutBytes + 1024) + (warp - 2) * BN;
     int sbuf = 0;
-    TileCursor<2> cur;
+    WorkCursor<kFar> cur;
     uint32_t tphase[2] = {0, 0};
     int iter = 0;
-    for (int tile = cid; tile < a.ntiles; tile += ncl, ++iter) {
-      int rg, ca;
-      cur.seek(a, tile, rg, ca);
+    bool live = true, dead = false;  // live: the Gram's own waits succeed; dead: alpha gone
+    for (int u = cid; u < a.ntiles && live; u += ncl) {
+      int rg, ca0, nq, t, pidx;
+      bool far;
+      cur.seek(a, u, rg, ca0, nq, t, pidx, far);
       const int ra = 2 * rg + rank;
-      const int acc = iter & 1;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait2(&sc->tfull[acc], tphase[acc], sc, a) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      tphase[acc] ^= 1u;
-      tc_fence_after();
-      store_tile_rows(a, tmem, acc, quarter, lane, ra, ca, &tmG, stage, sbuf);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_rank(smem_u32(&sc->tempty[acc]), 0));
-      if (kRecV && !kNext) {
-        // publish this warp's 32 rows of the tile: its stores are complete and visible
-        if (a.tma_store) {
-          if (lane == 0) {
-            bulk_wait_all();
-            fence_proxy_async_global();
-          }
-        } else {
-          __threadfence();
+      float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // far: alpha of the unit's first column
+      const float* al_g = a.alpha + (int64_t)ca0 * BN;
+      float4 an0, an1;  // far: the next tile's alpha, loaded ahead
+      if (kFar && far && !dead) load_alpha(al_g, lane, an0, an1);
+      for (int q = 0; q < nq; ++q, ++iter) {
+        const int ca = ca0 + q;
+        const int acc = iter & 1;
+        if (kFar && far && !dead) {
+          dead = !stage_alpha(a, al_g + q * BN, al_s, lane, (ra * BM) / a.b, an0, an1);
+          if (!dead && q + 1 < nq) load_alpha(al_g + (q + 1) * BN, lane, an0, an1);
         }
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait2(&sc->tfull[acc], tphase[acc], sc, a) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          live = false;
+          break;
+        }
+        tphase[acc] ^= 1u;
+        tc_fence_after();
+        if (kFar && far) {
+          if (!dead) far_tile_dot(tmem, acc, quarter, al_s, sum);
+        } else {
+          store_tile_rows(a, tmem, acc, quarter, lane, ra, ca, &tmG, stage, sbuf);
+        }
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          red_release_add(a.slab + (int64_t)ra * 4 + quarter, 1u);
+        if (lane == 0) mbar_arrive_cluster(mapa_rank(smem_u32(&sc->tempty[acc]), 0));
+        if (kFar && far) continue;
+        if (kRecV && !kNext && q == nq - 1) {
+          // publish this warp's 32 rows of the unit's tiles: their stores are complete
+          // and visible
+          if (a.tma_store) {
+            if (lane == 0) {
+              bulk_wait_all();
+              fence_proxy_async_global();
+            }
+          } else {
+            __threadfence();
+          }
+          __syncwarp();
+          if (lane == 0) {
+            red_release_add(a.slab + (int64_t)ra * 4 + quarter, (uint32_t)nq);
+            red_release_add(&a.ctrl->band_done, (uint32_t)nq);
+            stamp_last(rec.trace, 0);
+          }
+        } else if (kRecV && lane == 0) {
           stamp_last(rec.trace, 0);
         }
-      } else if (kRecV && lane == 0) {
-        stamp_last(rec.trace, 0);
+      }
+      if (kFar && far && live && !dead) {
+        const int64_t p = (int64_t)ra * BM + quarter * 32 + lane;
+        __stcg(a.fpart + p * a.fs + pidx,
+               ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7])));
+        if (lane == 0) stamp_last(rec.trace, 1);
       }
     }
     if (lane == 0) bulk_wait_all();  // this warp's tensor stores are complete
@@ -784,12 +1015,12 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
     // ---------------------------------------------------------- recurrence (warps 6-13)
     // the first C CTAs run chain groups, the others the bulk role
     const int rt = threadIdx.x - kThreads;
+    constexpr int kMode = kNext ? 2 : (kFar ? 3 : 1);
     if ((int)blockIdx.x < rec.C)
       chain_role<kRecV == 1 ? 1 : (kRecV == 2 ? 2 : 3), kRecV == 1 ? 8 : (kRecV == 2 ? 4 : 2),
-                 kNext ? 2 : 1>(
-          rec, blockIdx.x, rt);
+                 kMode>(rec, blockIdx.x, rt);
     else
-      bulk_role<kNext ? 2 : 1>(rec, rt, (int)blockIdx.x - rec.C < rec.upd_groups);
+      bulk_role<kMode>(rec, rt, (int)blockIdx.x - rec.C < rec.upd_groups);
   }
 
   tc_fence_before();
@@ -861,6 +1092,13 @@ cudaError_t plan_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
   a.diag = diag;
   a.timeout_ns = (uint64_t)(timeout_us ? timeout_us : 1000000u) * 1000ull;
   a.slab = nullptr;
+  a.fpart = nullptr;
+  a.alpha = nullptr;
+  a.s = s;
+  a.B = band_width(b);
+  a.nb = b / 256;
+  a.npb = a.uq = 1;
+  a.fs = s;
   // count the needed tiles on the host with the same rule the kernel walks
   int64_t total = 0;
   for (int g = 0; g * kcl < a.TR; ++g) {
@@ -935,7 +1173,7 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
     ++c.launches;
     return cudaGetLastError();
   }
-  const void* fn = mode == 0 ? (const void*)gram_tc2sm_kernel<kStagesPair, 0, false>
+  const void* fn = mode == 0 ? (const void*)gram_tc2sm_kernel<kStagesPair, 0, false, false>
                              : (const void*)gram_tc_kernel<2>;
   const size_t smem = mode == 0 ? pair_smem_bytes<kStagesPair>() : kSmemBytes;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -951,7 +1189,8 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
   if (mode == 0) {
     RecArgs none;
     memset(&none, 0, sizeof(none));
-    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel<kStagesPair, 0, false>, P.map, P.mapG, a, none);
+    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel<kStagesPair, 0, false, false>, P.map, P.mapG, a,
+                           none);
   } else {
     e = cudaLaunchKernelEx(&cfg, gram_tc_kernel<2>, P.map, P.mapG, a);
   }
@@ -964,12 +1203,20 @@ bool gram_recur_fused_supported(int64_t S, int64_t n, int b) {
   return gram_tc_supported(S, n, b) && (S + BM - 1) / BM >= 2 && S / b >= 2;
 }
 
+bool far_gram_supported(int64_t S, int64_t n, int b) {
+  // whole 256x256 tiles inside one block pair (j, t)
+  return gram_recur_fused_supported(S, n, b) && b % 256 == 0;
+}
+
 cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t S, int64_t n,
                               int64_t ldY, int b, int s, float eta, int loss, uint32_t flags,
                               const float* G, const uint16_t* Y, const uint16_t* r,
                               const float* yY, float* alpha, float* far, uint32_t* slab,
-                              float* part, float* w, Ctrl* ctrl, uint32_t timeout_us, Ctx& c) {
+                              float* fpart, float* part, float* w, Ctrl* ctrl,
+                              uint32_t timeout_us, Ctx& c) {
   if (!gram_recur_fused_supported(S, n, b)) return cudaErrorNotSupported;
+  const bool far_gram = fpart != nullptr;
+  if (far_gram && (next || !far_gram_supported(S, n, b))) return cudaErrorNotSupported;
   const bool diag = (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
   TcPlan P;
   cudaError_t e = plan_tc(Yg, S, n, ldY, b, s, diag, 2, Gg, ctrl, timeout_us, P);
@@ -978,15 +1225,41 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
   RecArgs rec = make_rec_args(G, r, yY, alpha, far, slab, b, s, eta, loss, flags, timeout_us,
                               ctrl, Y, ldY, n, part, w);
   rec.slab = next ? nullptr : slab;
+  if (far_gram) {  // work items: units of uq tiles, nb * npb * (j + diag) for phase j
+    P.a.fpart = fpart;
+    P.a.alpha = alpha;
+    P.a.npb = far_partials_per_block(b, s);
+    P.a.uq = P.a.nb / P.a.npb;
+    P.a.fs = s * P.a.npb;
+    P.a.ntiles = P.a.nb * P.a.npb * (s * (s - 1) / 2 + (diag ? s : 0));
+    rec.fpart = fpart;
+    rec.fs = P.a.fs;
+    rec.npb = P.a.npb;
+    rec.far_gram = true;
+    rec.bulk_units = 0;  // no far units: the Gram forms the far sums
+  }
+  // what Ctrl::band_done reaches once every stored tile is stored (8 warps per tile)
+  if (!next) {
+    int64_t total = 0;
+    for (int g = 0; (int64_t)g * 256 < S; ++g)
+      total += far_gram ? far_gram_stored_tiles(b, diag, g) : pair_group_tiles(S, b, diag, g);
+    rec.band_total = (uint32_t)(8 * total);
+  }
   const int v = chain_variant(rec);
   using Fn = void (*)(CUtensorMap, CUtensorMap, TcArgs, RecArgs);
-  const Fn table[2][3] = {
-      {gram_tc2sm_kernel<kStagesFused, 1, false>, gram_tc2sm_kernel<kStagesFused, 2, false>,
-       gram_tc2sm_kernel<kStagesFused, 3, false>},
-      {gram_tc2sm_kernel<kStagesFused, 1, true>, gram_tc2sm_kernel<kStagesFused, 2, true>,
-       gram_tc2sm_kernel<kStagesFused, 3, true>}};
-  const Fn fn = table[next ? 1 : 0][v - 1];
-  const size_t smem = pair_smem_bytes<kStagesFused>();
+  const Fn table[3][3] = {
+      {gram_tc2sm_kernel<kStagesFused, 1, false, false>,
+       gram_tc2sm_kernel<kStagesFused, 2, false, false>,
+       gram_tc2sm_kernel<kStagesFused, 3, false, false>},
+      {gram_tc2sm_kernel<kStagesFused, 1, true, false>,
+       gram_tc2sm_kernel<kStagesFused, 2, true, false>,
+       gram_tc2sm_kernel<kStagesFused, 3, true, false>},
+      {gram_tc2sm_kernel<kStagesFused, 1, false, true>,
+       gram_tc2sm_kernel<kStagesFused, 2, false, true>,
+       gram_tc2sm_kernel<kStagesFused, 3, false, true>}};
+  const Fn fn = table[far_gram ? 2 : (next ? 1 : 0)][v - 1];
+  const size_t smem = far_gram ? pair_smem_bytes<kStagesFused, true>()
+                               : pair_smem_bytes<kStagesFused>();
   e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];

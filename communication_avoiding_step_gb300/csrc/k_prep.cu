@@ -71,6 +71,8 @@ struct RowArgs {
   float* yY;
   float* alpha;
   float* far;
+  float* fpart;  // far partials [S][fs] of the far-forming Gram (null: not used)
+  int fb, fs, fB, fnp;  // b, row stride s * npb, band width, partials per block
   Ctrl* ctrl;
   uint32_t* slab;
   int G;
@@ -81,6 +83,7 @@ __device__ void reset_recurrence(const RowArgs& a) {
   if (threadIdx.x == 0) {
     a.ctrl->next_unit = 0;
     a.ctrl->upd_next = 0;
+    a.ctrl->band_done = 0;
     a.ctrl->abort = (a.ctrl->status & ST_TIMEOUT) ? 1u : 0u;  // stays set after a timeout
   }
   const int64_t nslab = (a.S + 255) / 256 * 8;  // the Gram's 32-row counters
@@ -176,6 +179,10 @@ __device__ __forceinline__ void gather_rows(const RowArgs& a, int64_t blk) {
   }
   if (kMargin)
     for (int off = G >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);
+  if (kMargin && live && a.fpart) {  // the row's far partials t < j - B, spread over its lanes
+    const int nfar = ((int)(p / a.fb) - a.fB) * a.fnp;
+    for (int t = g; t < nfar; t += G) a.fpart[p * a.fs + t] = __uint_as_float(kAlphaPending);
+  }
   if (live && g == 0) {
     if (kMargin) {
       a.r[p] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
@@ -240,7 +247,8 @@ namespace {
 
 RowArgs row_args(const casgd_data_t& d, const casgd_params_t& p, const float* w, uint64_t k,
                  const int32_t* idx_in, int32_t* idx, uint16_t* Y, int64_t ldY, uint16_t* r,
-                 float* yY, float* alpha, float* far, Ctrl* ctrl, uint32_t* slab) {
+                 float* yY, float* alpha, float* far, float* fpart, Ctrl* ctrl,
+                 uint32_t* slab) {
   RowArgs a;
   a.X = static_cast<const uint16_t*>(d.X);
   a.y = d.y;
@@ -259,6 +267,11 @@ RowArgs row_args(const casgd_data_t& d, const casgd_params_t& p, const float* w,
   a.yY = yY;
   a.alpha = alpha;
   a.far = far;
+  a.fpart = fpart;
+  a.fb = p.b;
+  a.fnp = far_partials_per_block(p.b, p.s);
+  a.fs = p.s * a.fnp;
+  a.fB = band_width(p.b);
   a.ctrl = ctrl;
   a.slab = slab;
   a.G = pow2_at_least(ldY / 8, 32);
@@ -275,8 +288,9 @@ int64_t row_blocks(const RowArgs& a) {
 cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const float* w,
                           uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
                           int64_t ldY, uint16_t* r, float* yY, float* alpha, float* far,
-                          Ctrl* ctrl, uint32_t* slab, int mode, Ctx& c) {
-  const RowArgs a = row_args(d, p, w, k, idx_in, idx, Y, ldY, r, yY, alpha, far, ctrl, slab);
+                          float* fpart, Ctrl* ctrl, uint32_t* slab, int mode, Ctx& c) {
+  const RowArgs a =
+      row_args(d, p, w, k, idx_in, idx, Y, ldY, r, yY, alpha, far, fpart, ctrl, slab);
   auto fn = mode == GATHER_AND_MARGINS ? gather_kernel<true, true>
             : mode == GATHER_ONLY      ? gather_kernel<true, false>
                                        : gather_kernel<false, true>;
@@ -289,11 +303,11 @@ cudaError_t launch_gather_next_margins(const casgd_data_t& d, const casgd_params
                                        const float* w, uint64_t k_next, int32_t* idx_next,
                                        uint16_t* Y_next, float* yY_next, const uint16_t* Y,
                                        int64_t ldY, uint16_t* r, float* alpha, float* far,
-                                       Ctrl* ctrl, uint32_t* slab, Ctx& c) {
+                                       float* fpart, Ctrl* ctrl, uint32_t* slab, Ctx& c) {
   const RowArgs g = row_args(d, p, w, k_next, nullptr, idx_next, Y_next, ldY, nullptr, yY_next,
-                             nullptr, nullptr, ctrl, slab);
+                             nullptr, nullptr, nullptr, ctrl, slab);
   const RowArgs mg = row_args(d, p, w, 0, nullptr, nullptr, const_cast<uint16_t*>(Y), ldY, r,
-                              nullptr, alpha, far, ctrl, slab);
+                              nullptr, alpha, far, fpart, ctrl, slab);
   const int64_t nb = row_blocks(g);
   gather_next_margins_kernel<<<(unsigned)(2 * nb), 256, 0, c.stream>>>(g, mg, nb);
   ++c.launches;

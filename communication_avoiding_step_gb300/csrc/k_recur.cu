@@ -46,9 +46,7 @@ RecArgs make_rec_args(const float* G, const uint16_t* r, const float* yY, float*
   a.U = (b + kRecRows - 1) / kRecRows;
   a.Uc = (b + kChainRows - 1) / kChainRows;
   a.vec4 = (b % 4) == 0;
-  // band width: two blocks while a chain lane can hold both in registers
-  // band width: as many blocks as a chain lane can hold in registers
-  a.B = !a.vec4 ? 1 : (b + 127) / 128 <= 2 ? 3 : (b + 127) / 128 <= 4 ? 2 : 1;
+  a.B = band_width(b);  // as many blocks as a chain lane holds in registers
   a.bulk_units = 0;  // far units: (block, chunk of kT blocks) pairs x row units
   for (int j = a.B + 1; j < s; ++j) a.bulk_units += a.U;
   a.coef = -(eta / (float)b);
@@ -58,6 +56,10 @@ RecArgs make_rec_args(const float* G, const uint16_t* r, const float* yY, float*
   // update units: s blocks x ceil(ldY / 64) column chunks
   a.upd_units = s * (int)((ldY / 8 + 7) / 8);
   a.slab = nullptr;
+  a.fpart = nullptr;
+  a.fs = a.npb = 0;
+  a.band_total = 0;
+  a.far_gram = false;
   a.C = 0;
   a.upd_groups = 0;
   a.diag = (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;

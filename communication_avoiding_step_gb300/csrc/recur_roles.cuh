@@ -12,7 +12,9 @@
 // Two roles, each run by a group of 256 threads (a whole CTA in the stand-alone kernel,
 // warps 6-13 of a CTA in the kernels shared with the Gram).  kMode: 0 own CTA, G
 // complete; 1 shared CTA, rows of G still being stored by the same launch; 2 shared
-// CTA, G complete (the launch computes the next iteration's Gram):
+// CTA, G complete (the launch computes the next iteration's Gram); 3 shared CTA, the
+// Gram of the same launch stores only the band blocks and forms the far sums itself
+// (partial sums per row and block t, see below):
 //  * chain groups (the first C): one warp per row, 8-row groups.  Phase j of a row
 //    needs only the band  sum_{t=j-B}^{j-1} G_{j,t} alpha_t  (B = 1 to 3 blocks) on top
 //    of far_j (below).  The warp has its band rows of G in registers before it waits
@@ -21,7 +23,10 @@
 //  * bulk groups take units (block j >= B+1, chunk of 4 blocks t, 16 rows) from an
 //    atomic queue and compute partial sums of far_j = sum_{t<j-B} G_{j,t} alpha_t for
 //    their rows, streaming G with coalesced float4 reads; they wait on alpha_t the same
-//    way.  far_j is needed only B phases after its last input is known, so most of G is
+//    way.  In mode 3 there are no far units: the Gram's epilogue multiplies each far
+//    tile G_{j,t} by alpha_t as soon as alpha_t is final and stores one partial sum per
+//    row, block t and column group (npb groups per block); the chain adds a row's
+//    (j-B) * npb partials itself.  far_j is needed only B phases after its last input is known, so most of G is
 //    read off the critical path; the chain adds a row's partials in chunk order.  After the far units the same queue hands out the first stage
 //    of the weight update when it is fused: per block j and 64-column chunk, the
 //    partial row of Y^T alpha over that block, each waiting on the alpha of its rows.
@@ -65,6 +70,14 @@ struct RecArgs {
   int64_t n;
   // Gram in the same launch: per-32-row completion counters of the paired-SM Gram
   const uint32_t* slab;
+  // mode 3: far partial sums fpart[row * fs + t * npb + c], t < j - B, c < npb (column
+  // groups of block t), written by the Gram
+  const float* fpart;
+  int fs, npb;
+  // Gram in the same launch: Ctrl::band_done reaches band_total once every tile the Gram
+  // stores is stored (each epilogue warp adds its tiles after its 32-row counter)
+  uint32_t band_total;
+  bool far_gram;  // the Gram stores only the band (and diagonal) tiles
   int64_t S;
   Ctrl* ctrl;
   uint64_t timeout_ns;
@@ -195,11 +208,18 @@ __device__ bool wait_value(const float* p, float& v, const RecArgs& a, uint32_t 
   }
 }
 
+// Tiles the Gram stores for the 256-row group holding 32-row slab `sl`.
+__device__ __forceinline__ uint32_t slab_need(const RecArgs& a, int64_t sl) {
+  const int g = (int)(sl >> 3);
+  return (uint32_t)(a.far_gram ? far_gram_stored_tiles(a.b, a.diag, g)
+                               : pair_group_tiles(a.S, a.b, a.diag, g));
+}
+
 // Waits (acquire) until every tile of the Gram's 256-row group holding absolute row
 // `row` is stored: the counter of the row's 32-row slab reaches the group's tile count.
 __device__ bool wait_rows_of_G(const RecArgs& a, int64_t row, uint32_t where) {
   const int64_t sl = row >> 5;
-  const uint32_t need = (uint32_t)pair_group_tiles(a.S, a.b, a.diag, (int)(sl >> 3));
+  const uint32_t need = slab_need(a, sl);
   if (ld_acquire_u32(a.slab + sl) >= need) return true;
   const uint64_t t_start = globaltimer_ns();
   while (true) {
@@ -224,6 +244,10 @@ __device__ bool wait_rows_of_G(const RecArgs& a, int64_t row, uint32_t where) {
 // role group.
 template <int kB, int kKB, int kMode>
 __device__ void chain_role(const RecArgs& a, int c, int rt) {
+  constexpr bool kInFlight = kMode == 1 || kMode == 3;  // G stored by this launch
+  // the next item's row values are loaded with its band, except in the widest register
+  // layout (eight float4 slots per block), which has no registers to spare for them
+  constexpr bool kRowAhead = kKB < 8;
   const int warp = rt >> 5, lane = rt & 31;
   const int nk = (a.b + 127) / 128;  // float4 slots per band block (vec4 path)
   // With tracing on, chain group 0, warp 0 keeps a per-phase timeline (globaltimer ns):
@@ -245,9 +269,49 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
 #pragma unroll
       for (int k = 0; k < kKB; ++k) {
         g[tb][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (a.vec4 && tb < nb && lane * 4 + 128 * k < a.b) g[tb][k] = ldG4<kMode == 1>(gb + 128 * k);
+        if (a.vec4 && tb < nb && lane * 4 + 128 * k < a.b) g[tb][k] = ldG4<kInFlight>(gb + 128 * k);
       }
     }
+  };
+
+  // loads the row values of item (j, i): margin and label (lane 0) and far_j (lane 0;
+  // mode 3: the row's partials t = lane and t = lane + 32), possibly still pending
+  auto load_row = [&](int j, int i, uint32_t& rb, float& yv, float& f0, float& f1) {
+    const int64_t p = (int64_t)j * a.b + i;
+    rb = 0;
+    yv = f0 = f1 = 0.0f;
+    if (lane == 0) {
+      rb = a.r[p];
+      yv = a.yY[p];
+    }
+    if (j < kB + 1) return;
+    if (kMode == 3) {
+      const int nfar = (j - kB) * a.npb;
+      const float* fsrc = a.fpart + p * a.fs;
+      if (lane < nfar) f0 = ld_volatile_f32(fsrc + lane);
+      if (lane + 32 < nfar) f1 = ld_volatile_f32(fsrc + lane + 32);
+    } else if (lane == 0) {
+      f0 = ld_volatile_f32(a.far + p);
+    }
+  };
+  // Gram in the same launch: whether rows of item (j, i) are stored; once every stored
+  // tile is, no counter is read again
+  bool all_stored = !kInFlight;
+  auto rows_stored = [&](int j, int i) -> bool {
+    int ready = 1;
+    if (!all_stored) {
+      if (lane == 0) {
+        ready = ld_acquire_u32(&a.ctrl->band_done) >= a.band_total;
+        if (!ready) {
+          const int64_t sl = ((int64_t)j * a.b + i) >> 5;
+          ready = ld_acquire_u32(a.slab + sl) >= slab_need(a, sl) ? 2 : 0;
+        }
+      }
+      ready = __shfl_sync(0xffffffffu, ready, 0);
+      __syncwarp();
+      if (ready == 1) all_stored = true;
+    }
+    return ready != 0;
   };
 
   float4 gv[kB][kKB], gn[kB][kKB], av[kB][kKB];
@@ -256,6 +320,9 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
 #pragma unroll
     for (int k = 0; k < kKB; ++k) av[tb][k] = make_float4(0.f, 0.f, 0.f, 0.f);
   bool cur_loaded = false;  // gv holds the current item's band
+  bool row_loaded = false;  // rbits, yj, fv0, fv1 hold the current item's row values
+  uint32_t rbits = 0;       // converted after the wait, so the load does not stall the issue
+  float yj = 0.0f, fv0 = 0.0f, fv1 = 0.0f;
   int jprev = -1;
   int j = 0, gi = 0;        // item: phase j, gi-th valid group of the warp
   while (j < a.s) {
@@ -264,8 +331,9 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
     const int nb = j < kB ? j : kB;  // band blocks this phase (the first is t = j-1)
     const bool has_far = j >= kB + 1;
     if (tracer && gi == 0) a.trace[4 * j] = globaltimer_ns();
+    if (!row_loaded) load_row(j, i, rbits, yj, fv0, fv1);
     if (!cur_loaded) {
-      if (kMode == 1 && j > 0) {  // this row of G is stored (block 0 reads none)
+      if (kInFlight && j > 0 && !rows_stored(j, i)) {  // block 0 reads no row of G
         int ok0 = 1;
         if (lane == 0) ok0 = wait_rows_of_G(a, p, where_code(5, j)) ? 1 : 0;
         ok0 = __shfl_sync(0xffffffffu, ok0, 0);
@@ -274,39 +342,26 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
       }
       load_band(gv, j, i);
     }
-    uint32_t rbits = 0;  // converted after the wait, so the load does not stall the issue
-    float yj = 0.0f;
-    if (lane == 0) {
-      rbits = a.r[p];
-      yj = a.yY[p];
-    }
-    // the next item, and its band if its rows of G are already stored
+    // the next item: its row values, and its band if its rows of G are already stored
     int j2 = j, gi2 = gi + 1;
     if (gi2 == ng) {
       gi2 = 0;
       ++j2;
     }
     bool next_loaded = false;
-    if (j2 < a.s && j2 > 0) {
+    uint32_t rbits_n = 0;
+    float yj_n = 0.0f, fv0_n = 0.0f, fv1_n = 0.0f;
+    if (j2 < a.s) {
       const int i2 = (c + gi2 * a.C) * kChainRows + warp;
-      int ready = 1;
-      if (kMode == 1) {
-        if (lane == 0) {
-          const int64_t sl = ((int64_t)j2 * a.b + i2) >> 5;
-          ready = ld_acquire_u32(a.slab + sl) >=
-                  (uint32_t)pair_group_tiles(a.S, a.b, a.diag, (int)(sl >> 3));
-        }
-        ready = __shfl_sync(0xffffffffu, ready, 0);
-        __syncwarp();
-      }
-      if (ready) {
+      if (kRowAhead) load_row(j2, i2, rbits_n, yj_n, fv0_n, fv1_n);
+      if (j2 > 0 && rows_stored(j2, i2)) {
         load_band(gn, j2, i2);
         next_loaded = true;
       }
     }
     if (tracer && gi == 0) a.trace[4 * j + 1] = globaltimer_ns();
-    // alpha_{j-1} (slot row 0; polled once per phase) and far_j: load them until none
-    // is pending
+    // alpha_{j-1} (slot row 0; polled once per phase) and far_j (mode 3: the row's
+    // j-B partial sums, two per lane): load them until none is pending
     bool pend = false;
     const float* aprev = a.alpha + (int64_t)(j - 1) * a.b + lane * 4;
     const bool poll_alpha = a.vec4 && j > 0 && j != jprev;
@@ -324,9 +379,16 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
         }
       }
     }
-    float farv = 0.0f;
-    if (has_far && lane == 0) {
-      farv = ld_volatile_f32(a.far + p);
+    // far_j as loaded with the row values (lane 0; mode 3: partials t = lane and
+    // t = lane + 32), reloaded below while pending
+    float farv = kMode == 3 ? 0.0f : fv0;
+    float fp0 = fv0, fp1 = fv1;
+    const int nfar = (j - kB) * a.npb;  // partials of the row (has_far), at most 64
+    const float* fsrc = kMode == 3 ? a.fpart + p * a.fs : nullptr;
+    if (kMode == 3) {
+      if (has_far && lane < nfar) pend |= pending1(fp0);
+      if (has_far && lane + 32 < nfar) pend |= pending1(fp1);
+    } else if (has_far && lane == 0) {
       pend |= pending1(farv);
     }
     bool ok = true;
@@ -344,7 +406,16 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
             }
           }
         }
-        if (has_far && lane == 0 && pending1(farv)) {
+        if (kMode == 3) {
+          if (has_far && lane < nfar && pending1(fp0)) {
+            fp0 = ld_volatile_f32(fsrc + lane);
+            pend |= pending1(fp0);
+          }
+          if (has_far && lane + 32 < nfar && pending1(fp1)) {
+            fp1 = ld_volatile_f32(fsrc + lane + 32);
+            pend |= pending1(fp1);
+          }
+        } else if (has_far && lane == 0 && pending1(farv)) {
           farv = ld_volatile_f32(a.far + p);
           pend |= pending1(farv);
         }
@@ -361,20 +432,33 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
 #pragma unroll
         for (int k = 0; k < kKB; ++k)
           if (tb < nb) acc = dot4(gv[tb][k], av[tb][k], acc);
-      // columns beyond the register slots (b > 128 * kKB)
+      // columns beyond the register slots (b > 128 * kKB): kX float4 of G and of alpha
+      // per lane requested together, then summed in column order
       const float* grow0 = a.G + (int64_t)i * a.b;
-      for (int tb = 0; tb < nb; ++tb) {
+      for (int tb = 0; tb < nb && ok; ++tb) {
         const int t = j - 1 - tb;
-        for (int k = kKB; k < nk; ++k) {
-          const int col = lane * 4 + 128 * k;
-          if (col >= a.b) break;
-          const float* src = a.alpha + (int64_t)t * a.b + col;
-          float4 v = ld_volatile_f4(src);
-          if (pending4(v)) {
-            const uint64_t t_start = globaltimer_ns();
-            while (pending4(v) && (ok = keep_waiting(a, t_start, where_code(2, j)))) v = ld_volatile_f4(src);
+        const float* gsrc = grow0 + packed_offset(j, t, a.b, a.diag);
+        const float* asrc = a.alpha + (int64_t)t * a.b;
+        constexpr int kX = 2;
+        for (int k0 = kKB; k0 < nk && ok; k0 += kX) {
+          float4 gx[kX], vx[kX];
+#pragma unroll
+          for (int u = 0; u < kX; ++u) {
+            const int col = lane * 4 + 128 * (k0 + u);
+            const bool in = k0 + u < nk && col < a.b;
+            gx[u] = in ? ldG4<kInFlight>(gsrc + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+            vx[u] = in ? ld_volatile_f4(asrc + col) : make_float4(0.f, 0.f, 0.f, 0.f);
           }
-          acc = dot4(ldG4<kMode == 1>(grow0 + packed_offset(j, t, a.b, a.diag) + col), v, acc);
+#pragma unroll
+          for (int u = 0; u < kX; ++u) {
+            if (pending4(vx[u])) {
+              const float* src = asrc + lane * 4 + 128 * (k0 + u);
+              const uint64_t t_start = globaltimer_ns();
+              while (pending4(vx[u]) && (ok = keep_waiting(a, t_start, where_code(2, j))))
+                vx[u] = ld_volatile_f4(src);
+            }
+            acc = dot4(gx[u], vx[u], acc);
+          }
         }
       }
     } else {
@@ -386,13 +470,19 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
         for (int col = lane; col < a.b; col += 32) {
           float v;
           if (!(ok = wait_value(al + col, v, a, where_code(2, j)))) break;
-          acc = fmaf(ldG1<kMode == 1>(grow + col), v, acc);
+          acc = fmaf(ldG1<kInFlight>(grow + col), v, acc);
         }
       }
     }
     if (!__all_sync(0xffffffffu, ok)) return;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (kMode == 3) {  // far_j: the row's partials, lane sums then a fixed tree
+      float fs = fp0 + fp1;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) fs += __shfl_xor_sync(0xffffffffu, fs, off);
+      farv = fs;
+    }
     if (lane == 0 && !(a.stall_test && j == 0)) {
       const float z = bf16_bits_to_float(rbits) + farv + acc;
       __stcg(a.alpha + p, a.coef * loss_deriv(a.loss, z, yj));
@@ -404,6 +494,11 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
 #pragma unroll
       for (int k = 0; k < kKB; ++k) gv[tb][k] = gn[tb][k];
     cur_loaded = next_loaded;
+    row_loaded = kRowAhead;
+    rbits = rbits_n;
+    yj = yj_n;
+    fv0 = fv0_n;
+    fv1 = fv1_n;
     jprev = j;
     j = j2;
     gi = gi2;
@@ -536,6 +631,7 @@ __device__ void update_unit(const RecArgs& a, int u, int rt) {
 // groups turn to update units once the far units are gone.
 template <int kMode>
 __device__ void bulk_role(const RecArgs& a, int rt, bool upd_group) {
+  constexpr bool kInFlight = kMode == 1 || kMode == 3;
   __shared__ int s_unit, s_lead;
   const int warp = rt >> 5, lane = rt & 31;
   const int probe_col = (int)((blockIdx.x * 37u) % (unsigned)a.b);
@@ -579,7 +675,7 @@ __device__ void bulk_role(const RecArgs& a, int rt, bool upd_group) {
     for (int t = 0; t < t_end;) {
       if (rt == 0) {
         bool rows_ok = true;
-        if (kMode == 1 && t == 0) {  // the unit's rows of G are stored (first and last row)
+        if (kInFlight && t == 0) {  // the unit's rows of G are stored (first and last row)
           const int64_t r0 = (int64_t)j * a.b + c * kRecRows;
           const int last = min(c * kRecRows + kRecRows, a.b) - 1;
           rows_ok = wait_rows_of_G(a, r0, where_code(5, j)) &&
@@ -617,8 +713,8 @@ __device__ void bulk_role(const RecArgs& a, int rt, bool upd_group) {
               if (u < nt) {
                 const float* gb = g0 + packed_offset(j, t + u, a.b, a.diag) + col;
                 av[u] = __ldcg(reinterpret_cast<const float4*>(a.alpha + (int64_t)(t + u) * a.b + col));
-                x0[u] = ldG4<kMode == 1>(gb);
-                x1[u] = has1 ? ldG4<kMode == 1>(gb + a.b) : make_float4(0.f, 0.f, 0.f, 0.f);
+                x0[u] = ldG4<kInFlight>(gb);
+                x1[u] = has1 ? ldG4<kInFlight>(gb + a.b) : make_float4(0.f, 0.f, 0.f, 0.f);
               }
             }
 #pragma unroll
@@ -637,8 +733,8 @@ __device__ void bulk_role(const RecArgs& a, int rt, bool upd_group) {
               const float* al = a.alpha + (int64_t)(t + u) * a.b;
               for (int col = lane; col < a.b; col += 32) {
                 const float v = __ldcg(al + col);
-                d0[u] = fmaf(ldG1<kMode == 1>(gb + col), v, d0[u]);
-                if (has1) d1[u] = fmaf(ldG1<kMode == 1>(gb + a.b + col), v, d1[u]);
+                d0[u] = fmaf(ldG1<kInFlight>(gb + col), v, d0[u]);
+                if (has1) d1[u] = fmaf(ldG1<kInFlight>(gb + a.b + col), v, d1[u]);
               }
             }
           }

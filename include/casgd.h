@@ -72,10 +72,12 @@ enum {
                                               the B tile by TMA multicast             */
 #define CASGD_FLAG_GRAM_PAIR         0x20u /* tcgen05 Gram, CTA pairs (cta_group::2,
                                               256x256 tiles).  Without a variant flag
-                                              the library takes pairs (sharing their
-                                              launch with the recurrence) for
-                                              b <= 512, else pairs for n >= 1024 and
-                                              multicast clusters below               */
+                                              the library takes pairs forming the far
+                                              sums (FAR_FROM_GRAM) for b a multiple of
+                                              256, else pairs sharing their launch
+                                              with the recurrence for b <= 512, else
+                                              pairs for n >= 1024 and multicast
+                                              clusters below                         */
 #define CASGD_FLAG_NO_FUSE           0x40u /* run the paired-SM Gram and the inner
                                               recurrence as two launches.  Otherwise
                                               they share one launch whenever the pair
@@ -91,6 +93,29 @@ enum {
                                               phase in the workspace (see
                                               casgd_chain_trace); off by default, as
                                               the stamps slow that warp              */
+#define CASGD_FLAG_FAR_FROM_GRAM     0x200u /* the paired-SM Gram of the same launch
+                                              forms the far sums of the inner
+                                              recurrence itself: each tile of G_{j,t}
+                                              with t < j-B (B = 3 for b <= 256, 2 for
+                                              b <= 512, else 1) is multiplied by
+                                              alpha_t in the tile's epilogue, straight
+                                              from the tensor-memory accumulator, once
+                                              alpha_t is final, and only the band
+                                              blocks t = j-B .. j-1 (and G_{j,j} with
+                                              WRITE_DIAG_BLOCKS) are stored: G beyond
+                                              the band never reaches memory.  Same
+                                              sums as the stored-G path in another
+                                              order (per row: partials per block t
+                                              and column group, then t ascending).
+                                              The default wherever it applies (b a
+                                              multiple of 256, s >= 2, S >= 256);
+                                              this flag forces it: with another
+                                              variant flag, FULL_G or a shape it does
+                                              not take, CASGD_ERR_UNSUPPORTED          */
+#define CASGD_FLAG_FULL_G            0x400u /* store every block G_{j,t}, t < j, and
+                                              form the far sums from memory (the
+                                              recurrence's bulk groups) even where the
+                                              far-forming Gram applies                 */
 #define CASGD_FLAG_TEST_STALL        0x80000000u /* test only: the recurrence's first
                                               block never signals completion, so every
                                               waiter runs into its time bound and the
@@ -125,7 +150,8 @@ typedef struct {
   float* G_out;          /* receives G in the packed block-lower layout:
                             blocks (j,t) for t<j (t<=j with WRITE_DIAG_BLOCKS),
                             j ascending then t ascending, each b x b row-major;
-                            casgd_gram_elems() floats                           */
+                            casgd_gram_elems() floats (with FAR_FROM_GRAM only
+                            the band and diagonal blocks are written)           */
   uint16_t* r_out;       /* receives the S BF16 margins (bit patterns)          */
   float* alpha_out;      /* receives the S FP32 step coefficients alpha         */
 } casgd_taps_t;
@@ -143,7 +169,9 @@ typedef struct {
   int32_t gram_kind;     /* out: 1 = tcgen05 Gram kernel used, 2 = CUDA-core,
                             3 = paired-SM tcgen05 Gram and recurrence in one
                             launch, 4 = as 3 with the Gram one outer iteration
-                            ahead of the recurrence (casgd_train, iters >= 2)   */
+                            ahead of the recurrence (casgd_train, iters >= 2),
+                            5 = as 3 with the far sums formed by the Gram
+                            (CASGD_FLAG_FAR_FROM_GRAM)                          */
 } casgd_profile_t;
 #define CASGD_STAGE_EVENTS 5
 

@@ -55,21 +55,24 @@ def test_stalled_producer_times_out_and_context_survives(gpu_lib):
 
 
 def test_stall_in_fused_launch_times_out_and_context_survives(gpu_lib):
-    """The paired-SM Gram with the recurrence in the same launch (recipe 2 shape): the
-    Gram warps finish their tiles, every recurrence waiter runs into its bound."""
+    """The paired-SM Gram storing G with the recurrence in the same launch (recipe 2
+    shape): the Gram warps finish their tiles, every recurrence waiter runs into its
+    bound."""
     casgd = gpu_lib
     p, data = _data(casgd, cid=2, m=20000)
     r = p.recipe
-    stall = casgd.Params(r.b, r.s, r.eta, r.loss, flags=casgd.FLAG_TEST_STALL, timeout_us=20000)
+    full = casgd.FLAG_FULL_G
+    stall = casgd.Params(r.b, r.s, r.eta, r.loss, flags=full | casgd.FLAG_TEST_STALL,
+                         timeout_us=20000)
     ws = casgd.workspace(data, stall)
     w = torch.zeros(p.n, device="cuda")
-    _, _, kind = casgd.train(data, casgd.Params(r.b, r.s, r.eta, r.loss), w, 1, ws)
+    _, _, kind = casgd.train(data, casgd.Params(r.b, r.s, r.eta, r.loss, flags=full), w, 1, ws)
     assert kind == 3                                     # the fused launch ran
     casgd.outer_step(data, stall, w, 0, ws)
     assert casgd.get_status(ws) == 5                     # CASGD_ERR_TIMEOUT
     assert casgd.get_status(ws) == 0
     w.zero_()
-    casgd.outer_step(data, casgd.Params(r.b, r.s, r.eta, r.loss), w, 0, ws)
+    casgd.outer_step(data, casgd.Params(r.b, r.s, r.eta, r.loss, flags=full), w, 0, ws)
     assert casgd.get_status(ws) == 0
     assert torch.isfinite(w).all() and torch.count_nonzero(w).item() > 0
 
@@ -80,15 +83,42 @@ def test_stall_in_pipelined_train_times_out(gpu_lib):
     casgd = gpu_lib
     p, data = _data(casgd, cid=2, m=20000)
     r = p.recipe
-    stall = casgd.Params(r.b, r.s, r.eta, r.loss, flags=casgd.FLAG_TEST_STALL, timeout_us=20000)
+    full = casgd.FLAG_FULL_G
+    stall = casgd.Params(r.b, r.s, r.eta, r.loss, flags=full | casgd.FLAG_TEST_STALL,
+                         timeout_us=20000)
     ws = casgd.workspace(data, stall)
     w = torch.zeros(p.n, device="cuda")
     with pytest.raises(casgd.CasgdError) as e:
         casgd.train(data, stall, w, 3, ws)
     assert e.value.code == 5
     w.zero_()
-    _, _, kind = casgd.train(data, casgd.Params(r.b, r.s, r.eta, r.loss), w, 2, ws)
+    _, _, kind = casgd.train(data, casgd.Params(r.b, r.s, r.eta, r.loss, flags=full), w, 2, ws)
     assert kind == 4
+    assert torch.isfinite(w).all() and torch.count_nonzero(w).item() > 0
+
+
+def test_stall_in_far_forming_launch_times_out(gpu_lib):
+    """CASGD_FLAG_FAR_FROM_GRAM: the Gram's epilogue waits on alpha itself.  With alpha_0
+    never stored, those waits and the recurrence's run into their bound; the Gram warps
+    still drain every tile, and the workspace works again afterwards."""
+    casgd = gpu_lib
+    p, data = _data(casgd, cid=2, m=20000)
+    r = p.recipe
+    far = casgd.FLAG_FAR_FROM_GRAM
+    stall = casgd.Params(r.b, r.s, r.eta, r.loss, flags=far | casgd.FLAG_TEST_STALL,
+                         timeout_us=20000)
+    ws = casgd.workspace(data, stall)
+    w = torch.zeros(p.n, device="cuda")
+    casgd.outer_step(data, stall, w, 0, ws)
+    assert casgd.get_status(ws) == 5                     # CASGD_ERR_TIMEOUT
+    assert casgd.get_status(ws) == 0
+    with pytest.raises(casgd.CasgdError) as e:
+        casgd.train(data, stall, w, 3, ws)
+    assert e.value.code == 5
+    w.zero_()
+    ok = casgd.Params(r.b, r.s, r.eta, r.loss, flags=far)
+    _, _, kind = casgd.train(data, ok, w, 2, ws)
+    assert kind == 5
     assert torch.isfinite(w).all() and torch.count_nonzero(w).item() > 0
 
 

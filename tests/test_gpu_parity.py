@@ -134,7 +134,9 @@ def test_outer_step_parity(gpu_lib, name, factory, override, gram):
             "tensor_pair": casgd.FLAG_GRAM_TENSOR | casgd.FLAG_GRAM_PAIR,
             "tensor_pair_nofuse": casgd.FLAG_GRAM_TENSOR | casgd.FLAG_GRAM_PAIR
             | casgd.FLAG_NO_FUSE}[gram]
-    params = _params(casgd, p, override, flag | casgd.FLAG_WRITE_DIAG_BLOCKS)
+    # FULL_G: every block of G is stored (the far-forming Gram has its own test)
+    params = _params(casgd, p, override,
+                     flag | casgd.FLAG_WRITE_DIAG_BLOCKS | casgd.FLAG_FULL_G)
     b, s = params.b, params.s
     data = _dev(p, casgd)
     for w0 in (np.zeros(p.n, np.float32), si.random_weights(p.n, seed=7, scale=0.5)):
@@ -202,8 +204,8 @@ def test_fused_launch_equals_separate_launches(gpu_lib, name, factory, override)
     w0 = si.random_weights(p.n, seed=3)
     out = []
     for extra in (0, casgd.FLAG_NO_FUSE):
-        params = _params(casgd, p, override,
-                         casgd.FLAG_GRAM_TENSOR | casgd.FLAG_GRAM_PAIR | extra)
+        params = _params(casgd, p, override, casgd.FLAG_GRAM_TENSOR | casgd.FLAG_GRAM_PAIR
+                         | casgd.FLAG_FULL_G | extra)
         w, taps, st = _run_step(casgd, data, params, w0, k=3)
         assert st == 0
         G = taps.G_out.cpu().numpy() if taps.G_out.numel() <= 40_000_000 else None
@@ -226,12 +228,13 @@ PIPE_CASES = [
 @pytest.mark.parametrize("name,factory,override", PIPE_CASES, ids=[c[0] for c in PIPE_CASES])
 def test_train_pipeline_equals_outer_steps(gpu_lib, name, factory, override):
     """casgd_train computes the next iteration's Gram in the launch of the current
-    recurrence; every value must still be exactly what one outer iteration at a time
-    computes: bit-identical w after 3 iterations from a non-zero w, and after 1."""
+    recurrence (stored G); every value must still be exactly what one outer iteration
+    at a time computes: bit-identical w after 3 iterations from a non-zero w, and
+    after 1."""
     casgd = gpu_lib
     p = factory()
     data = _dev(p, casgd)
-    params = _params(casgd, p, override, 0)
+    params = _params(casgd, p, override, casgd.FLAG_FULL_G)
     w0 = si.random_weights(p.n, seed=7)
     for iters in (3, 1):
         ws = casgd.workspace(data, params)
@@ -245,6 +248,145 @@ def test_train_pipeline_equals_outer_steps(gpu_lib, name, factory, override):
         a = w_step.cpu().numpy()
         b_ = w_train.cpu().numpy()
         assert np.array_equal(a.view(np.uint32), b_.view(np.uint32)), (iters, _rel(b_, a))
+
+
+# ------------------------------------ far sums formed by the Gram (no far G) ----
+def _band_width(b):
+    """The recurrence's band width for a block size b (a multiple of 4): the blocks a
+    chain lane holds in registers (documented with CASGD_FLAG_FAR_FROM_GRAM)."""
+    return 3 if b <= 256 else 2 if b <= 512 else 1
+
+
+FAR_CASES = [
+    # the recipes' own block sizes (b = 256 .. 2048) and feature counts (18 .. 2000)
+    ("recipe2_m20000", lambda: si.make_problem(2, m=20000), None),
+    ("recipe3_m60000", lambda: si.make_problem(3, m=60000), None),
+    ("recipe4_m60000", lambda: si.make_problem(4, m=60000), None),
+    ("recipe5_m20000", lambda: si.make_problem(5, m=20000), None),
+    # a ragged K tail (n = 130) and the fewest blocks with a far block (s = 5, b = 256)
+    ("ragged_3000x130_b256_s5", lambda: si.make_random(3000, 130, si.POISSON, seed=3),
+     (256, 5, 0.02)),
+    ("ragged_2500x70_b512_s3", lambda: si.make_random(2500, 70, si.LOGISTIC, seed=8),
+     (512, 3, 0.3)),
+    # more than 32 far blocks per row (a chain lane adds two partials)
+    ("s40_b256_12000x64", lambda: si.make_random(12000, 64, si.LSQ, seed=9), (256, 40, 0.01)),
+    # the largest S (65536) at recipe 4's shape
+    ("max_S65536_recipe4_s32", lambda: si.make_problem(4, m=200_000), (2048, 32, 0.01)),
+]
+
+
+@pytest.mark.parametrize("name,factory,override", FAR_CASES, ids=[c[0] for c in FAR_CASES])
+def test_far_from_gram_parity(gpu_lib, name, factory, override):
+    """CASGD_FLAG_FAR_FROM_GRAM: the far sums come from the Gram's accumulators and only
+    the band and diagonal blocks of G are stored.  Against the oracle: indices, margins,
+    every stored block, alpha and w, with the bars of the stored-G path."""
+    casgd = gpu_lib
+    p = factory()
+    params = _params(casgd, p, override,
+                     casgd.FLAG_FAR_FROM_GRAM | casgd.FLAG_WRITE_DIAG_BLOCKS)
+    b, s = params.b, params.s
+    B = _band_width(b)
+    data = _dev(p, casgd)
+    for w0 in (np.zeros(p.n, np.float32), si.random_weights(p.n, seed=7, scale=0.5)):
+        w_gpu, taps, st = _run_step(casgd, data, params, w0, k=3)
+        assert st == 0
+        ref = oracle.outer_step(p.X, p.y, w0, b, s, params.eta, p.recipe.loss, 0, 3,
+                                mode="emulate", return_parts=True)
+        assert np.array_equal(taps.idx_out.cpu().numpy(), ref["idx"])
+        r_gpu = (taps.r_out.cpu().numpy().view(np.uint16).astype(np.uint32) << 16).view(np.float32)
+        assert (r_gpu != ref["r"]).mean() <= 0.005 * _len_scale(p.n)
+        assert np.all(np.abs(r_gpu - ref["r"]) <= _bf16_ulp(ref["r"]) + 1e-38)
+        stored = [(j, t) for j in range(s) for t in range(max(0, j - B), j + 1)]
+        if len(stored) * b * b > 20_000_000:  # sampled: first, last and a few between
+            rng = np.random.default_rng(1)
+            keep = {stored[0], stored[-1], (1, 0)}
+            for i in rng.choice(len(stored), 6, replace=False):
+                keep.add(stored[int(i)])
+            stored = sorted(keep)
+        num = den = 0.0
+        for j, t in stored:
+            o = oracle.packed_block_offset(j, t, b, True)
+            g_ref = oracle.gram_block(ref["Y"], b, j, t, "emulate").reshape(-1)
+            g_gpu = taps.G_out[o:o + b * b].cpu().numpy().astype(np.float64)
+            num += float(np.sum((g_gpu - g_ref) ** 2))
+            den += float(np.sum(g_ref.astype(np.float64) ** 2))
+        assert math.sqrt(num / den) <= GRAM_TOL * _len_scale(p.n)
+        assert _rel(taps.alpha_out.cpu().numpy(), ref["alpha"]) <= 2e-3 * _len_scale(p.n)
+        assert _rel(w_gpu, ref["w"]) <= W_TOL * _len_scale(p.n)
+
+
+FAR_PIPE_CASES = [
+    ("recipe2_m20000", lambda: si.make_problem(2, m=20000), None),
+    ("recipe3_m60000", lambda: si.make_problem(3, m=60000), None),
+    ("ragged_3000x130_b256_s5", lambda: si.make_random(3000, 130, si.POISSON, seed=3),
+     (256, 5, 0.02)),
+]
+
+
+@pytest.mark.parametrize("name,factory,override", FAR_PIPE_CASES,
+                         ids=[c[0] for c in FAR_PIPE_CASES])
+def test_far_from_gram_train_equals_outer_steps(gpu_lib, name, factory, override):
+    """casgd_train with the far-forming Gram gathers the next iteration's rows in the
+    launch that forms this iteration's margins; the values are those of one outer
+    iteration at a time: bit-identical w after 3 iterations and after 1, and the same
+    again on a second run (the far sums are taken in a fixed order)."""
+    casgd = gpu_lib
+    p = factory()
+    data = _dev(p, casgd)
+    params = _params(casgd, p, override, casgd.FLAG_FAR_FROM_GRAM)
+    w0 = si.random_weights(p.n, seed=7)
+    for iters in (3, 1):
+        ws = casgd.workspace(data, params)
+        w_step = torch.from_numpy(w0.copy()).cuda()
+        for k in range(iters):
+            casgd.outer_step(data, params, w_step, 5 + k, ws)
+        assert casgd.get_status(ws) == 0
+        a = w_step.cpu().numpy()
+        for _ in range(2):
+            w_train = torch.from_numpy(w0.copy()).cuda()
+            _, _, kind = casgd.train(data, params, w_train, iters, ws, k0=5)
+            assert kind == 5
+            b_ = w_train.cpu().numpy()
+            assert np.array_equal(a.view(np.uint32), b_.view(np.uint32)), (iters, _rel(b_, a))
+
+
+def test_far_from_gram_is_the_default(gpu_lib):
+    """Without variant flags the far-forming Gram runs wherever it applies (b a multiple
+    of 256), bit-identical to forcing it; FULL_G runs the stored-G launches instead."""
+    casgd = gpu_lib
+    p = si.make_random(3000, 130, si.POISSON, seed=3)
+    data = _dev(p, casgd)
+    w0 = si.random_weights(p.n, seed=7)
+    out = {}
+    for name, fl in (("default", 0), ("forced", casgd.FLAG_FAR_FROM_GRAM),
+                     ("full", casgd.FLAG_FULL_G)):
+        params = casgd.Params(256, 5, 0.02, si.POISSON, flags=fl)
+        ws = casgd.workspace(data, params)
+        w = torch.from_numpy(w0.copy()).cuda()
+        _, _, kind = casgd.train(data, params, w, 2, ws, k0=1)
+        out[name] = (kind, w.cpu().numpy())
+    assert out["default"][0] == 5 and out["forced"][0] == 5 and out["full"][0] == 4
+    assert np.array_equal(out["default"][1].view(np.uint32), out["forced"][1].view(np.uint32))
+    assert _rel(out["full"][1], out["default"][1]) <= 1e-5
+
+
+def test_far_from_gram_unsupported_shapes(gpu_lib):
+    """The flag needs b a multiple of 256, s >= 2 and the paired kernel in the same
+    launch; anything else is CASGD_ERR_UNSUPPORTED and launches nothing."""
+    casgd = gpu_lib
+    p = si.make_random(3000, 130, si.LOGISTIC, seed=3)
+    data = _dev(p, casgd)
+    for b, s, extra in ((100, 6, 0), (256, 1, 0), (256, 4, casgd.FLAG_NO_FUSE),
+                        (256, 4, casgd.FLAG_GRAM_SIMT), (256, 4, casgd.FLAG_GRAM_MULTICAST),
+                        (256, 4, casgd.FLAG_FULL_G)):
+        params = casgd.Params(b, s, 0.1, si.LOGISTIC, flags=casgd.FLAG_FAR_FROM_GRAM | extra)
+        ws = casgd.workspace(data, params)
+        w = torch.zeros(p.n, device="cuda")
+        with pytest.raises(casgd.CasgdError) as e:
+            casgd.outer_step(data, params, w, 0, ws)
+        assert e.value.code == 7
+        torch.cuda.synchronize()
+        assert torch.count_nonzero(w).item() == 0
 
 
 def test_outer_step_given_indices_and_bad_index(gpu_lib):
