@@ -18,6 +18,7 @@ not printed anywhere on the pages: parity unpinned for those numbers.
 from .casgd import (  # noqa: F401
     LOGISTIC, LSQ, POISSON,
     splitmix64, sample_indices, bf16_round,
+    perm_width, feistel, epoch_keys, permuted_indices, draw_indices,
     loss_value, loss_grad, full_loss,
     gram_block, gram_packed, packed_block_offset,
     outer_step, train, plain_sgd,

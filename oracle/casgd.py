@@ -25,7 +25,9 @@ Readings of points the abstract leaves open (each is listed in the design notes)
                iteration k uses generator counter c = k*s*b + j*b + i, i.e. the c-th
                output h of SplitMix64 seeded with `seed`, reduced to [0, m) as
                ((h >> 32) * m) >> 32.  Step q of plain SGD uses counters q*b .. q*b+b-1,
-               so CA-SGD and plain SGD see the same rows.
+               so CA-SGD and plain SGD see the same rows.  Variant (without
+               replacement): counter c is position c mod m of epoch c div m of a keyed
+               pseudorandom permutation of the rows (permuted_indices).
   losses       logistic l = log(1 + exp(-y z)), y in {-1, +1}; least squares
                l = (z - y)^2 / 2; Poisson (log link) l = exp(z) - y z, the log(y!)
                constant left out.  No regulariser, no intercept; f = mean over rows.
@@ -76,6 +78,76 @@ def sample_indices(m: int, count: int, seed: int, counter0: int) -> np.ndarray:
         raise ValueError("m must be in [1, 2^31)")
     h = splitmix64(seed, np.arange(count, dtype=_U64) + _U64(counter0))
     return ((h >> _U64(32)) * _U64(m) >> _U64(32)).astype(np.int64)
+
+
+# Sampling without replacement (a variant: every row once per epoch of m draws).
+# A keyed pseudorandom permutation of [0, m) built from published pieces:
+#   * a balanced Feistel network (Luby & Rackoff, "How to construct pseudorandom
+#     permutations from pseudorandom functions", SIAM J. Comput. 1988) on d-bit values,
+#     d the smallest even width with 2^d >= m (at least 2): halves of h = d/2 bits,
+#     four rounds (L, R) -> (R, L xor F_r(R));
+#   * round function F_r(R) = the low h bits of SplitMix64 output number R of the stream
+#     started at state K_{e,r}, the round key K_{e,r} = SplitMix64 output number 4e + r
+#     of the stream started at seed xor 0x6A09E667F3BCC908 (a fixed constant that keeps
+#     the keys apart from the with-replacement stream);
+#   * cycle walking (Black & Rogaway, "Ciphers with arbitrary finite domains", CT-RSA
+#     2002): apply the d-bit permutation until the value falls in [0, m); this is a
+#     permutation of [0, m) because the walk stays on the cycle of its start.
+_PERM_SEED_XOR = 0x6A09E667F3BCC908
+_PERM_ROUNDS = 4
+
+
+def perm_width(m: int) -> int:
+    """d: the smallest even bit width with 2^d >= m, at least 2."""
+    d = 2
+    while (1 << d) < m:
+        d += 2
+    return d
+
+
+def feistel(x, d: int, keys) -> np.ndarray:
+    """The d-bit Feistel permutation with the given round keys, on uint64 values."""
+    h = d // 2
+    mask = _U64((1 << h) - 1)
+    x = np.asarray(x, dtype=_U64)
+    L, R = x >> _U64(h), x & mask
+    for k in keys:
+        L, R = R, L ^ (splitmix64(int(k), R) & mask)
+    return (L << _U64(h)) | R
+
+
+def epoch_keys(seed: int, e: int) -> list:
+    """Round keys K_{e,0..3} of epoch e."""
+    base = (seed ^ _PERM_SEED_XOR) & 0xFFFFFFFFFFFFFFFF
+    return [int(splitmix64(base, _PERM_ROUNDS * e + r)) for r in range(_PERM_ROUNDS)]
+
+
+def permuted_indices(m: int, count: int, seed: int, counter0: int) -> np.ndarray:
+    """Row indices for counters counter0 .. counter0+count-1 without replacement within
+    each epoch: counter c is position c mod m of the permutation of epoch c div m."""
+    if not (0 < m < 2**31):
+        raise ValueError("m must be in [1, 2^31)")
+    d = perm_width(m)
+    c = np.arange(count, dtype=np.int64) + int(counter0)
+    out = np.empty(count, dtype=np.int64)
+    for e in np.unique(c // m):
+        sel = (c // m) == e
+        keys = epoch_keys(seed, int(e))
+        y = feistel(c[sel] % m, d, keys)
+        while True:  # cycle walking
+            over = y >= _U64(m)
+            if not over.any():
+                break
+            y[over] = feistel(y[over], d, keys)
+        out[sel] = y.astype(np.int64)
+    return out
+
+
+def draw_indices(m: int, count: int, seed: int, counter0: int, permuted: bool = False):
+    """sample_indices (with replacement) or permuted_indices (without)."""
+    if permuted:
+        return permuted_indices(m, count, seed, counter0)
+    return sample_indices(m, count, seed, counter0)
 
 
 # ----------------------------------------------------------------------------------
@@ -212,7 +284,7 @@ def gather_rows(X, idx, mode: str, storage: str | None = None) -> np.ndarray:
 
 def outer_step(X, y, w, b: int, s: int, eta: float, kind: int, seed: int, k: int,
                mode: str = "emulate", storage: str | None = None, idx=None,
-               return_parts: bool = False):
+               return_parts: bool = False, permuted: bool = False):
     """One CA-SGD outer iteration: s minibatch SGD steps of b rows, batched.
 
     Derivation (pins the recurrence).  Minibatch SGD on f(w) = (1/m) sum l(x.w, y)
@@ -233,7 +305,7 @@ def outer_step(X, y, w, b: int, s: int, eta: float, kind: int, seed: int, k: int
     m = X.shape[0]
     S = s * b
     if idx is None:
-        idx = sample_indices(m, S, seed, k * S)
+        idx = draw_indices(m, S, seed, k * S, permuted)
     idx = np.asarray(idx, dtype=np.int64)
     Y = gather_rows(X, idx, mode, storage)
     yY = np.asarray(y, dtype=np.float32)[idx].astype(ft)
@@ -263,7 +335,7 @@ def outer_step(X, y, w, b: int, s: int, eta: float, kind: int, seed: int, k: int
 
 def train(X, y, b: int, s: int, eta: float, kind: int, seed: int, iters: int,
           mode: str = "emulate", storage: str | None = None, w0=None, k0: int = 0,
-          loss_every: int = 0, loss_X=None):
+          loss_every: int = 0, loss_X=None, permuted: bool = False):
     """`iters` outer iterations k = k0 .. k0+iters-1 from w0 (zeros by default).
 
     Returns (w, losses) where losses holds f(w) (FP64, on `loss_X` or X) after every
@@ -273,7 +345,8 @@ def train(X, y, b: int, s: int, eta: float, kind: int, seed: int, iters: int,
     w = np.zeros(X.shape[1], dtype=np.float32) if w0 is None else np.asarray(w0)
     losses = []
     for it in range(iters):
-        w = outer_step(X, y, w, b, s, eta, kind, seed, k0 + it, mode=mode, storage=storage)
+        w = outer_step(X, y, w, b, s, eta, kind, seed, k0 + it, mode=mode, storage=storage,
+                       permuted=permuted)
         if mode == "emulate":
             w = np.asarray(w, dtype=np.float32)
         if loss_every and (it + 1) % loss_every == 0:
@@ -282,7 +355,7 @@ def train(X, y, b: int, s: int, eta: float, kind: int, seed: int, iters: int,
 
 
 def plain_sgd(X, y, b: int, steps: int, eta: float, kind: int, seed: int,
-              mode: str = "fp64", w0=None, q0: int = 0):
+              mode: str = "fp64", w0=None, q0: int = 0, permuted: bool = False):
     """Plain minibatch SGD, one step per minibatch, on the same rows as CA-SGD.
 
     Step q (q = q0 .. q0+steps-1) uses counters q*b .. q*b+b-1 and does
@@ -296,7 +369,7 @@ def plain_sgd(X, y, b: int, steps: int, eta: float, kind: int, seed: int,
     coef = -(ft(eta) / ft(b))
     yv = np.asarray(y, dtype=np.float32)
     for q in range(q0, q0 + steps):
-        idx = sample_indices(m, b, seed, q * b)
+        idx = draw_indices(m, b, seed, q * b, permuted)
         Yq = X[idx].astype(ft)
         g = loss_grad(Yq @ w, yv[idx].astype(ft), kind)
         w = w + Yq.T @ (coef * g)

@@ -15,6 +15,8 @@ _orig_gram_block = oc.gram_block
 _orig_loss_grad = oc.loss_grad
 _orig_splitmix = oc.splitmix64
 _orig_bf16 = oc.bf16_round
+_orig_feistel = oc.feistel
+_orig_epoch_keys = oc.epoch_keys
 
 
 def _drop_first_term(Y, b, j, t, mode="emulate"):
@@ -48,6 +50,30 @@ def _bf16_truncate(x):
     return u.view(np.float32)
 
 
+def _no_cycle_walk(m, count, seed, counter0):
+    d = oc.perm_width(m)
+    c = np.arange(count, dtype=np.int64) + int(counter0)
+    out = np.empty(count, dtype=np.int64)
+    for e in np.unique(c // m):
+        sel = (c // m) == e
+        out[sel] = oc.feistel(c[sel] % m, d, oc.epoch_keys(seed, int(e))).astype(np.int64)
+    return out
+
+
+def _keys_ignore_epoch(seed, e):
+    return _orig_epoch_keys(seed, 0)
+
+
+def _feistel_no_swap(x, d, keys):
+    h = d // 2
+    mask = np.uint64((1 << h) - 1)
+    x = np.asarray(x, dtype=np.uint64)
+    L, R = x >> np.uint64(h), x & mask
+    for k in keys:
+        L = L ^ (_orig_splitmix(int(k), R) & mask)  # halves never swap: R passes through
+    return (L << np.uint64(h)) | R
+
+
 CASES = [
     ("recurrence drops t=0", [("gram_block", _drop_first_term)],
      lambda: pins.test_ca_sgd_equals_s_sgd_steps_fp64(oracle.LSQ)),
@@ -61,6 +87,12 @@ CASES = [
      pins.test_splitmix64_known_answers),
     ("BF16 truncation instead of RNE", [("bf16_round", _bf16_truncate)],
      pins.test_bf16_round_edge_cases),
+    ("permutation without cycle walking", [("permuted_indices", _no_cycle_walk)],
+     pins.test_permuted_indices_visit_every_row_once_per_epoch),
+    ("permutation keys ignore the epoch", [("epoch_keys", _keys_ignore_epoch)],
+     pins.test_permuted_epochs_and_seeds_differ),
+    ("Feistel halves never swap", [("feistel", _feistel_no_swap)],
+     pins.test_permuted_uniform_chi2),
 ]
 
 

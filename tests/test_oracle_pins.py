@@ -79,6 +79,91 @@ def test_sample_indices_uniform_chi2():
 
 
 # ---------------------------------------------------------------------- bf16 ----
+# --------------------------------------------- sampling without replacement ----
+def test_perm_width():
+    """d is the smallest even width with 2^d >= m (at least 2)."""
+    for m, d in ((1, 2), (4, 2), (5, 4), (16, 4), (17, 6), (64, 6), (65, 8),
+                 (4096, 12), (4097, 14), (11_000_000, 24), (2**31 - 1, 32)):
+        assert oracle.perm_width(m) == d, m
+
+
+def test_feistel_is_a_bijection_on_its_domain():
+    """Any round keys give a permutation of [0, 2^d) (Luby-Rackoff structure)."""
+    for d in (2, 4, 6, 10, 12):
+        for seed, e in ((0, 0), (7, 3), (2**64 - 1, 1000)):
+            keys = oracle.epoch_keys(seed, e)
+            y = oracle.feistel(np.arange(2**d, dtype=np.uint64), d, keys)
+            assert np.array_equal(np.sort(y), np.arange(2**d, dtype=np.uint64)), (d, seed, e)
+            assert not np.array_equal(y, np.arange(2**d, dtype=np.uint64))
+
+
+def test_permuted_indices_visit_every_row_once_per_epoch():
+    """Brute force: the m draws of each epoch are a permutation of the m rows (cycle
+    walking keeps the values below m), at every epoch and for widths that are and are
+    not powers of two."""
+    for m in (1, 2, 3, 5, 16, 17, 100, 1000, 4097):
+        for seed in (0, 7, 2**64 - 1):
+            for e in (0, 1, 3):
+                idx = oracle.permuted_indices(m, m, seed, e * m)
+                assert np.array_equal(np.sort(idx), np.arange(m)), (m, seed, e)
+    # a range that starts inside an epoch and spans three more: each whole epoch once
+    m = 37
+    idx = oracle.permuted_indices(m, 5 * m, 3, 2 * m + 11)
+    c = np.arange(5 * m) + 2 * m + 11
+    for e in (3, 4, 5):
+        assert np.array_equal(np.sort(idx[c // m == e]), np.arange(m))
+
+
+def test_permuted_indices_are_a_function_of_the_counter():
+    m = 1009
+    whole = oracle.permuted_indices(m, 3000, 5, 123)
+    parts = np.concatenate([oracle.permuted_indices(m, 1000, 5, 123 + 1000 * i)
+                            for i in range(3)])
+    assert np.array_equal(whole, parts)
+    assert whole.min() >= 0 and whole.max() < m
+
+
+def test_permuted_epochs_and_seeds_differ():
+    """Different epochs and seeds give (nearly) unrelated permutations; none is close to
+    the identity (a random permutation has one fixed point on average)."""
+    m = 1000
+    p00 = oracle.permuted_indices(m, m, 0, 0)
+    p01 = oracle.permuted_indices(m, m, 0, m)
+    p10 = oracle.permuted_indices(m, m, 1, 0)
+    for a, b_ in ((p00, p01), (p00, p10), (p01, p10)):
+        assert np.mean(a == b_) < 0.02
+    for a in (p00, p01, p10):
+        assert np.mean(a == np.arange(m)) < 0.02
+
+
+def test_permuted_uniform_chi2():
+    """Over many epochs, the row drawn at a fixed position, and the position at which a
+    fixed row is drawn, are uniform (chi-square, 10 rows, 4000 epochs)."""
+    scipy_stats = pytest.importorskip("scipy.stats")
+    m, E = 10, 4000
+    idx = oracle.permuted_indices(m, m * E, 2024, 0).reshape(E, m)
+    first = np.bincount(idx[:, 0], minlength=m)
+    where0 = np.bincount(np.argmax(idx == 0, axis=1), minlength=m)
+    for counts in (first, where0):
+        _, pv = scipy_stats.chisquare(counts)
+        assert pv > 1e-4, counts
+
+
+def test_ca_sgd_equals_s_sgd_steps_permuted_fp64():
+    """The identity CA-SGD == s SGD steps holds for the permuted rows too (both sides
+    draw the same rows for the same counters)."""
+    p = si.make_random(120, 8, LSQ, seed=12)
+    w0 = si.random_weights(8, seed=5, scale=0.3)
+    b, s, eta, seed = 7, 5, 0.2, 3
+    w_ca = w0.astype(np.float64)
+    for k in range(4):  # 140 draws: past the first epoch of 120 rows
+        w_ca = oracle.outer_step(p.X, p.y, w_ca, b, s, eta, LSQ, seed, k, mode="fp64",
+                                 permuted=True)
+    w_sgd = oracle.plain_sgd(p.X, p.y, b, 4 * s, eta, LSQ, seed, mode="fp64", w0=w0,
+                             permuted=True)
+    assert np.linalg.norm(w_ca - w_sgd) <= 1e-12 * np.linalg.norm(w_sgd)
+
+
 def test_bf16_round_edge_cases():
     f = np.float32
     one = 1.0
