@@ -15,7 +15,8 @@ import torch
 
 from ._native import (  # noqa: F401
     CASGD_LOGISTIC, CASGD_LSQ, CASGD_POISSON, FLAG_GRAM_MULTICAST, FLAG_GRAM_NO_CLUSTER,
-    FLAG_FAR_FROM_GRAM, FLAG_FULL_G, FLAG_GRAM_PAIR, FLAG_NO_FUSE, FLAG_TRACE_CHAIN,
+    FLAG_FAR_FROM_GRAM, FLAG_FULL_G, FLAG_GRAM_PAIR, FLAG_SAMPLE_PERMUTED, FLAG_NO_FUSE,
+    FLAG_TRACE_CHAIN,
     FLAG_GRAM_SIMT,
     FLAG_GRAM_TENSOR,
     FLAG_TEST_STALL, FLAG_WRITE_DIAG_BLOCKS, STAGE_EVENTS, CasgdError, Data as _Data,
@@ -96,10 +97,12 @@ def store_bf16(X32: torch.Tensor, ld: int | None = None, stream=None) -> torch.T
 
 
 def sample_indices(m: int, count: int, seed: int, counter0: int, device="cuda",
-                   stream=None) -> torch.Tensor:
+                   stream=None, permuted: bool = False) -> torch.Tensor:
+    """Row indices for sampler counters counter0 .. counter0+count-1: with replacement,
+    or (permuted) without replacement within each epoch of m draws."""
     out = torch.empty(count, dtype=torch.int32, device=device)
-    _check(load().casgd_sample_indices(m, count, seed, counter0, _ptr(out), _stream(stream)),
-           "casgd_sample_indices")
+    name = "casgd_sample_indices_permuted" if permuted else "casgd_sample_indices"
+    _check(getattr(load(), name)(m, count, seed, counter0, _ptr(out), _stream(stream)), name)
     return out
 
 

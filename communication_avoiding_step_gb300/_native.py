@@ -23,6 +23,7 @@ FLAG_NO_FUSE = 0x40
 FLAG_TRACE_CHAIN = 0x100
 FLAG_FAR_FROM_GRAM = 0x200
 FLAG_FULL_G = 0x400
+FLAG_SAMPLE_PERMUTED = 0x800
 FLAG_TEST_STALL = 0x80000000
 STAGE_EVENTS = 5
 
@@ -57,6 +58,8 @@ SIGNATURES = {
     "casgd_store_bf16": (C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_int64, C.c_void_p,
                                    C.c_int64, C.c_void_p]),
     "casgd_sample_indices": (C.c_int, [C.c_int64, C.c_int64, C.c_uint64, C.c_uint64,
+                                       C.c_void_p, C.c_void_p]),
+    "casgd_sample_indices_permuted": (C.c_int, [C.c_int64, C.c_int64, C.c_uint64, C.c_uint64,
                                        C.c_void_p, C.c_void_p]),
     "casgd_outer_step": (C.c_int, [_P(Data), _P(Params), C.c_void_p, C.c_uint64, C.c_void_p,
                                    C.c_size_t, C.c_void_p, _P(Taps)]),

@@ -437,8 +437,19 @@ int casgd_sample_indices(int64_t m, int64_t count, uint64_t seed, uint64_t count
   if (m < 1 || m >= (int64_t(1) << 31) || count < 0 || (count > 0 && !idx)) return CASGD_ERR_ARG;
   Ctx c{static_cast<cudaStream_t>(stream), 0, 0};
   if (device_sms(&c.num_sms) != CASGD_OK) return CASGD_ERR_CUDA;
-  return launch_sample(m, count, seed, counter0, idx, c) == cudaSuccess ? CASGD_OK
-                                                                        : CASGD_ERR_CUDA;
+  return launch_sample(m, count, seed, counter0, false, idx, c) == cudaSuccess
+             ? CASGD_OK
+             : CASGD_ERR_CUDA;
+}
+
+int casgd_sample_indices_permuted(int64_t m, int64_t count, uint64_t seed, uint64_t counter0,
+                                  int32_t* idx, void* stream) {
+  if (m < 1 || m >= (int64_t(1) << 31) || count < 0 || (count > 0 && !idx)) return CASGD_ERR_ARG;
+  Ctx c{static_cast<cudaStream_t>(stream), 0, 0};
+  if (device_sms(&c.num_sms) != CASGD_OK) return CASGD_ERR_CUDA;
+  return launch_sample(m, count, seed, counter0, true, idx, c) == cudaSuccess
+             ? CASGD_OK
+             : CASGD_ERR_CUDA;
 }
 
 int casgd_outer_step(const casgd_data_t* data, const casgd_params_t* params, float* w,

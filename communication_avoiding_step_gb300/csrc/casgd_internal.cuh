@@ -147,6 +147,53 @@ __device__ __forceinline__ int32_t sample_row(uint64_t seed, uint64_t counter, u
   return (int32_t)(((h >> 32) * (uint64_t)m) >> 32);
 }
 
+// Sampling without replacement: counter c is position c mod m of epoch c div m of a
+// keyed pseudorandom permutation of [0, m).  The permutation is a four-round balanced
+// Feistel network on d-bit values (Luby & Rackoff 1988; d the smallest even width with
+// 2^d >= m, at least 2), its round function the low d/2 bits of SplitMix64 output
+// number R of the stream started at the round key, the key of epoch e and round r
+// being SplitMix64 output number 4e + r of the stream started at seed xor
+// 0x6A09E667F3BCC908; values outside [0, m) are walked along their cycle until they
+// fall inside (Black & Rogaway 2002), which ends because the start lies on the cycle.
+constexpr uint64_t kPermSeedXor = 0x6A09E667F3BCC908ull;
+__host__ __device__ inline int perm_width(int64_t m) {
+  int d = 2;
+  while ((int64_t(1) << d) < m) d += 2;
+  return d;
+}
+
+__device__ __forceinline__ uint64_t feistel4(uint64_t x, int h, const uint64_t (&key)[4]) {
+  const uint64_t mask = (1ull << h) - 1ull;
+  uint64_t L = x >> h, R = x & mask;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const uint64_t t = L ^ (splitmix64_at(key[r], R) & mask);
+    L = R;
+    R = t;
+  }
+  return (L << h) | R;
+}
+
+// d = perm_width(m)
+__device__ __forceinline__ int32_t permuted_row(uint64_t seed, uint64_t counter, uint32_t m,
+                                                int d) {
+  const uint64_t e = counter / m;
+  const uint64_t q = counter - e * m;
+  uint64_t key[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) key[r] = splitmix64_at(seed ^ kPermSeedXor, 4ull * e + r);
+  uint64_t y = feistel4(q, d / 2, key);
+  while (y >= m) y = feistel4(y, d / 2, key);
+  return (int32_t)y;
+}
+
+// The row of sampler counter `counter`: with replacement (perm_d == 0) or the permuted
+// draw (perm_d = perm_width(m)).
+__device__ __forceinline__ int32_t draw_row(uint64_t seed, uint64_t counter, uint32_t m,
+                                            int perm_d) {
+  return perm_d ? permuted_row(seed, counter, m, perm_d) : sample_row(seed, counter, m);
+}
+
 // l'(z, y) for the three GLMs, FP32.
 __device__ __forceinline__ float loss_deriv(int kind, float z, float y) {
   if (kind == CASGD_LOGISTIC) return -y / (1.0f + expf(y * z));
@@ -192,8 +239,9 @@ struct Ctx {
 
 cudaError_t launch_store_bf16(const float* src, int64_t m, int64_t n, int64_t ld_src,
                               uint16_t* dst, int64_t ld_dst, Ctx& c);
+// permuted: without replacement (per-epoch permutation), else with replacement
 cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t counter0,
-                          int32_t* idx, Ctx& c);
+                          bool permuted, int32_t* idx, Ctx& c);
 // mode: GATHER_AND_MARGINS (sampled rows into Y, labels, indices, BF16 margins and the
 // recurrence's reset), GATHER_ONLY (rows, labels, indices), MARGINS_ONLY (margins of
 // the rows in Y and the reset).  The margins are bit-identical in every mode.  The reset

@@ -39,10 +39,10 @@ __global__ void store_bf16_kernel(const float* __restrict__ src, int64_t m, int6
 }
 
 __global__ void sample_kernel(uint32_t m, int64_t count, uint64_t seed, uint64_t counter0,
-                              int32_t* __restrict__ idx) {
+                              int perm_d, int32_t* __restrict__ idx) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count;
        i += (int64_t)gridDim.x * blockDim.x)
-    idx[i] = sample_row(seed, counter0 + (uint64_t)i, m);
+    idx[i] = draw_row(seed, counter0 + (uint64_t)i, m, perm_d);
 }
 
 // One group of G lanes (G a power of two <= 32) per row of Y.  Lane g reads the 16-byte
@@ -76,6 +76,7 @@ struct RowArgs {
   Ctrl* ctrl;
   uint32_t* slab;
   int G;
+  int perm_d;  // sampling: 0 with replacement, else perm_width(m) (per-epoch permutation)
 };
 
 // The recurrence's per-step reset (one CTA).
@@ -114,7 +115,7 @@ __device__ __forceinline__ void gather_rows(const RowArgs& a, int64_t blk) {
       valid = (row >= 0 && (int64_t)row < a.m);
       if (!valid && g == 0) atomicOr(&a.ctrl->status, ST_BAD_INDEX);
     } else {
-      row = sample_row(a.seed, a.counter0 + (uint64_t)p, (uint32_t)a.m);
+      row = draw_row(a.seed, a.counter0 + (uint64_t)p, (uint32_t)a.m, a.perm_d);
       valid = true;
     }
   }
@@ -234,11 +235,12 @@ cudaError_t launch_store_bf16(const float* src, int64_t m, int64_t n, int64_t ld
 }
 
 cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t counter0,
-                          int32_t* idx, Ctx& c) {
+                          bool permuted, int32_t* idx, Ctx& c) {
   if (count == 0) return cudaSuccess;
   int64_t blocks = (count + 255) / 256;
   if (blocks > (int64_t)c.num_sms * 8) blocks = (int64_t)c.num_sms * 8;
-  sample_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>((uint32_t)m, count, seed, counter0, idx);
+  sample_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>((uint32_t)m, count, seed, counter0,
+                                                        permuted ? perm_width(m) : 0, idx);
   ++c.launches;
   return cudaGetLastError();
 }
@@ -275,6 +277,7 @@ RowArgs row_args(const casgd_data_t& d, const casgd_params_t& p, const float* w,
   a.ctrl = ctrl;
   a.slab = slab;
   a.G = pow2_at_least(ldY / 8, 32);
+  a.perm_d = (p.flags & CASGD_FLAG_SAMPLE_PERMUTED) ? perm_width(d.m) : 0;
   return a;
 }
 

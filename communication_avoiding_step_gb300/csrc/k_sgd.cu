@@ -34,6 +34,7 @@ struct SgdArgs {
   Ctrl* ctrl;
   uint64_t seed, q0;
   int steps, b, loss;
+  int perm_d;  // sampling: 0 with replacement, else perm_width(m)
   float coef;
   uint64_t timeout_ns;
 };
@@ -88,8 +89,8 @@ __global__ void __launch_bounds__(kSgdThreads, 1) sgd_kernel(SgdArgs a) {
     for (int c = threadIdx.x; c < ldw; c += kSgdThreads) w_s[c] = c < a.n ? __ldcg(a.w + c) : 0.0f;
     __syncthreads();
     for (int i = gwarp; i < a.b; i += nwarps) {
-      const int32_t row = sample_row(a.seed, (a.q0 + (uint64_t)q) * (uint64_t)a.b + (uint64_t)i,
-                                     (uint32_t)a.m);
+      const int32_t row = draw_row(a.seed, (a.q0 + (uint64_t)q) * (uint64_t)a.b + (uint64_t)i,
+                                   (uint32_t)a.m, a.perm_d);
       const float* x = a.X + (int64_t)row * a.ld;
       float acc = 0.0f;
       if (vec) {
@@ -134,8 +135,8 @@ __global__ void __launch_bounds__(kSgdThreads, 1) sgd_kernel(SgdArgs a) {
     for (int i = threadIdx.x; i < a.b; i += kSgdThreads) {
       al_s[i] = __ldcg(a.alpha + i);
       // the row index is a pure function of the counter: recomputed, not read back
-      idx_s[i] = sample_row(a.seed, (a.q0 + (uint64_t)q) * (uint64_t)a.b + (uint64_t)i,
-                            (uint32_t)a.m);
+      idx_s[i] = draw_row(a.seed, (a.q0 + (uint64_t)q) * (uint64_t)a.b + (uint64_t)i,
+                          (uint32_t)a.m, a.perm_d);
     }
     __syncthreads();
     const int col_in = threadIdx.x % kColsPerCta, grp = threadIdx.x / kColsPerCta;
@@ -193,6 +194,7 @@ cudaError_t launch_sgd_fp32(const float* X, int64_t m, int64_t n, int64_t ld, co
   a.alpha = reinterpret_cast<float*>(base + 768);
   a.idx = reinterpret_cast<int32_t*>(base + 768 + ((size_t)p.b * 4 + 255) / 256 * 256);
   a.seed = p.seed;
+  a.perm_d = (p.flags & CASGD_FLAG_SAMPLE_PERMUTED) ? perm_width(m) : 0;
   a.q0 = q0;
   a.steps = steps;
   a.b = p.b;

@@ -116,6 +116,13 @@ enum {
                                               form the far sums from memory (the
                                               recurrence's bulk groups) even where the
                                               far-forming Gram applies                 */
+#define CASGD_FLAG_SAMPLE_PERMUTED   0x800u /* sample without replacement: counter c
+                                              draws position c mod m of epoch c div m
+                                              of a keyed permutation of the m rows
+                                              (casgd_sample_indices_permuted), so each
+                                              run of m draws from an epoch boundary
+                                              visits every row once.  Also honoured
+                                              by casgd_sgd_fp32                       */
 #define CASGD_FLAG_TEST_STALL        0x80000000u /* test only: the recurrence's first
                                               block never signals completion, so every
                                               waiter runs into its time bound and the
@@ -211,6 +218,18 @@ int casgd_store_bf16(const float* src, int64_t m, int64_t n, int64_t ld_src,
 int casgd_sample_indices(int64_t m, int64_t count, uint64_t seed, uint64_t counter0,
                          int32_t* idx, void* stream);
 
+/* Step a1 without replacement (CASGD_FLAG_SAMPLE_PERMUTED; the abstract leaves the
+ * sampling scheme open).  Counter c = counter0 + i draws position q = c mod m of the
+ * permutation of epoch e = c div m: d = the smallest even width with 2^d >= m (at
+ * least 2); the round keys K_r = SplitMix64 output number 4e + r (r = 0..3) of the
+ * stream started at seed ^ 0x6A09E667F3BCC908; the d-bit balanced Feistel network
+ * (Luby & Rackoff 1988) maps (L, R) = (x >> d/2, x & mask) four times to
+ * (R, L ^ (SplitMix64 output number R of the stream started at K_r) & mask); applied to
+ * q and then again while the value is >= m (cycle walking, Black & Rogaway 2002).
+ * m in [1, 2^31); idx: device int32[count].  Asynchronous. */
+int casgd_sample_indices_permuted(int64_t m, int64_t count, uint64_t seed, uint64_t counter0,
+                                  int32_t* idx, void* stream);
+
 /* One outer iteration k (steps a1-a8) on w (device FP32[n], updated in place).
  * ws: device workspace of ws_bytes (casgd_workspace_size).  taps: NULL or optional
  * inputs/outputs for parity checks.  Asynchronous; device errors are sticky in ws. */
@@ -272,7 +291,8 @@ int casgd_sgd_workspace_size(int32_t b, size_t* bytes);
  *     z_i = x_i . w,   alpha_i = -(eta/b) l'(z_i, y_i),   w += sum_i alpha_i x_i.
  *   X   device FP32 m x ld row-major (ld >= n; columns >= n are not read)
  *   y   device FP32[m];  w  device FP32[n], updated in place
- *   params: b, eta, loss, seed and timeout_us are used; s and flags are ignored.
+ *   params: b, eta, loss, seed, timeout_us and the SAMPLE_PERMUTED flag are used;
+ *       s and the other flags are ignored.
  *   ws  device workspace of ws_bytes >= casgd_sgd_workspace_size(b), 256-byte aligned;
  *       device errors are sticky in it (casgd_get_status).
  * One cooperative launch for all steps; asynchronous. */

@@ -93,6 +93,49 @@ def test_sample_indices_bitexact(gpu_lib):
         assert np.array_equal(got, want), (m, count, seed, c0)
 
 
+def test_sample_indices_permuted_bitexact(gpu_lib):
+    """Sampling without replacement: the device's keyed permutation equals the oracle's
+    bit for bit, across epoch boundaries and for the largest row count; a whole epoch
+    visits every row once."""
+    casgd = gpu_lib
+    for m, count, seed, c0 in ((4096, 4096, 0, 0), (400_000, 8192, 0, 49 * 8192),
+                               (2**31 - 1, 100_000, 2**64 - 1, 2**40 + 7), (1, 5, 3, 0),
+                               (11_000_000, 16384, 12345, 671 * 16384), (37, 200, 3, 85),
+                               (1000, 3000, 9, 0), (5_000_000, 16384, 0, 305 * 16384)):
+        got = casgd.sample_indices(m, count, seed, c0, permuted=True).cpu().numpy()
+        want = oracle.permuted_indices(m, count, seed, c0)
+        assert np.array_equal(got, want), (m, count, seed, c0)
+    whole = casgd.sample_indices(4096, 4096, 11, 4096 * 7, permuted=True).cpu().numpy()
+    assert np.array_equal(np.sort(whole), np.arange(4096))
+
+
+PERM_CASES = [
+    ("recipe1", lambda: si.make_problem(1), None),
+    ("recipe2_m20000", lambda: si.make_problem(2, m=20000), None),
+    ("ragged_777x37_b24_s3", lambda: si.make_random(777, 37, si.LOGISTIC, seed=1), (24, 3, 0.3)),
+]
+
+
+@pytest.mark.parametrize("name,factory,override", PERM_CASES, ids=[c[0] for c in PERM_CASES])
+def test_outer_step_permuted_sampling(gpu_lib, name, factory, override):
+    """CASGD_FLAG_SAMPLE_PERMUTED: the rows of an outer iteration are the oracle's
+    permuted draws (bit-exact, an iteration that crosses an epoch boundary included),
+    and w matches the oracle on them."""
+    casgd = gpu_lib
+    p = factory()
+    params = _params(casgd, p, override, casgd.FLAG_SAMPLE_PERMUTED)
+    b, s = params.b, params.s
+    data = _dev(p, casgd)
+    w0 = si.random_weights(p.n, seed=7, scale=0.5)
+    k = p.m // (b * s)  # counters k*S .. k*S+S-1: past m (across it where S does not divide m)
+    w_gpu, taps, st = _run_step(casgd, data, params, w0, k=k)
+    assert st == 0
+    ref = oracle.outer_step(p.X, p.y, w0, b, s, params.eta, p.recipe.loss, 0, k,
+                            mode="emulate", return_parts=True, permuted=True)
+    assert np.array_equal(taps.idx_out.cpu().numpy(), ref["idx"])
+    assert _rel(w_gpu, ref["w"]) <= W_TOL * _len_scale(p.n)
+
+
 # ------------------------------------------------------ one outer iteration ----
 CASES = [
     # (name, problem factory, b, s, eta, loss)
@@ -516,4 +559,21 @@ def test_sgd_fp32_matches_oracle(gpu_lib, name, factory, b, steps, eta):
     casgd.sgd_fp32(X, y, params, w, steps, ws, q0=3)
     assert casgd.get_status(ws) == 0
     want = oracle.plain_sgd(p.X, p.y, b, steps, eta, p.recipe.loss, 2, mode="fp32", w0=w0, q0=3)
+    assert _rel(w.cpu().numpy(), want) <= W_TOL * _len_scale(p.n)
+
+
+def test_sgd_fp32_permuted_sampling(gpu_lib):
+    """The FP32 SGD baseline draws the same permuted rows as CA-SGD."""
+    casgd = gpu_lib
+    p = si.make_random(777, 37, si.LOGISTIC, seed=1)
+    X = torch.from_numpy(p.X).cuda()
+    y = torch.from_numpy(p.y).cuda()
+    w0 = si.random_weights(p.n, seed=5)
+    params = casgd.Params(24, 1, 0.3, p.recipe.loss, seed=2, flags=casgd.FLAG_SAMPLE_PERMUTED)
+    ws = casgd.sgd_workspace(24)
+    w = torch.from_numpy(w0.copy()).cuda()
+    casgd.sgd_fp32(X, y, params, w, 70, ws, q0=3)  # 1680 draws: past two epochs
+    assert casgd.get_status(ws) == 0
+    want = oracle.plain_sgd(p.X, p.y, 24, 70, 0.3, p.recipe.loss, 2, mode="fp32", w0=w0, q0=3,
+                            permuted=True)
     assert _rel(w.cpu().numpy(), want) <= W_TOL * _len_scale(p.n)
