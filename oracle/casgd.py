@@ -284,7 +284,8 @@ def gather_rows(X, idx, mode: str, storage: str | None = None) -> np.ndarray:
 
 def outer_step(X, y, w, b: int, s: int, eta: float, kind: int, seed: int, k: int,
                mode: str = "emulate", storage: str | None = None, idx=None,
-               return_parts: bool = False, permuted: bool = False):
+               return_parts: bool = False, permuted: bool = False,
+               margins: str = "bf16", gram: str = "fp32"):
     """One CA-SGD outer iteration: s minibatch SGD steps of b rows, batched.
 
     Derivation (pins the recurrence).  Minibatch SGD on f(w) = (1/m) sum l(x.w, y)
@@ -299,6 +300,11 @@ def outer_step(X, y, w, b: int, s: int, eta: float, kind: int, seed: int, k: int
          with G_{j,t} = Y_j Y_t^T;
       5. w = w_0 + Y^T a.
     Returns w (mode dtype), or a dict with idx, Y, r, alpha, w when return_parts.
+
+    Two other precision choices of the emulating mode (the abstract studies several
+    and lists none; these vary one each): margins="fp32" keeps r as its FP32 sum (no
+    BF16 rounding); gram="bf16" rounds every entry of G to BF16 (nearest even) before
+    the recurrence uses it, as when G is summed across processes in BF16.
     """
     ft = _mode_dtype(mode)
     X = np.asarray(X)
@@ -314,7 +320,7 @@ def outer_step(X, y, w, b: int, s: int, eta: float, kind: int, seed: int, k: int
         else np.asarray(w, dtype=np.float64)
 
     r = Y @ w0
-    if mode == "emulate":
+    if mode == "emulate" and margins == "bf16":
         r = bf16_round(r)                       # margins stored in low precision
 
     coef = -(ft(eta) / ft(b))
@@ -324,7 +330,10 @@ def outer_step(X, y, w, b: int, s: int, eta: float, kind: int, seed: int, k: int
         z = r[rows].astype(ft)
         for t in range(j):
             cols = slice(t * b, (t + 1) * b)
-            z = z + gram_block(Y, b, j, t, mode) @ alpha[cols]
+            G_jt = gram_block(Y, b, j, t, mode)
+            if mode == "emulate" and gram == "bf16":
+                G_jt = bf16_round(G_jt)
+            z = z + G_jt @ alpha[cols]
         alpha[rows] = coef * loss_grad(z, yY[rows], kind)
 
     w_new = w0 + Y.T @ alpha

@@ -17,6 +17,7 @@ _orig_splitmix = oc.splitmix64
 _orig_bf16 = oc.bf16_round
 _orig_feistel = oc.feistel
 _orig_epoch_keys = oc.epoch_keys
+_orig_outer_step = oc.outer_step
 
 
 def _drop_first_term(Y, b, j, t, mode="emulate"):
@@ -74,6 +75,16 @@ def _feistel_no_swap(x, d, keys):
     return (L << np.uint64(h)) | R
 
 
+def _margins_choice_ignored(*args, **kw):
+    kw.pop("margins", None)
+    return _orig_outer_step(*args, **kw)
+
+
+def _gram_choice_ignored(*args, **kw):
+    kw.pop("gram", None)
+    return _orig_outer_step(*args, **kw)
+
+
 CASES = [
     ("recurrence drops t=0", [("gram_block", _drop_first_term)],
      lambda: pins.test_ca_sgd_equals_s_sgd_steps_fp64(oracle.LSQ)),
@@ -93,6 +104,10 @@ CASES = [
      pins.test_permuted_epochs_and_seeds_differ),
     ("Feistel halves never swap", [("feistel", _feistel_no_swap)],
      pins.test_permuted_uniform_chi2),
+    ("FP32-margin variant still rounds", [("outer_step", _margins_choice_ignored)],
+     pins.test_precision_variants_of_the_emulating_mode),
+    ("BF16-G variant leaves G in FP32", [("outer_step", _gram_choice_ignored)],
+     pins.test_precision_variants_of_the_emulating_mode),
 ]
 
 

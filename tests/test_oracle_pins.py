@@ -376,6 +376,33 @@ def test_update_is_w0_plus_Yt_alpha():
     assert np.allclose(parts["w"], direct, rtol=1e-14, atol=1e-15)
 
 
+def test_precision_variants_of_the_emulating_mode():
+    """margins="fp32": r is the FP32 sum itself, which the recipe's r is the BF16
+    rounding of; gram="bf16": the same recurrence fed bf16_round(G), so with one block
+    (s = 1: no G) it changes nothing and with G it moves w by less than BF16's relative
+    step.  Both variants stay within BF16 rounding of the FP64 iterate on the same
+    BF16 data, and FP32 margins are the closer of the two margin choices."""
+    p = si.make_random(500, 31, LOGISTIC, seed=13)
+    w0 = si.random_weights(31, seed=6, scale=0.5)
+    b, s, eta = 8, 6, 0.4
+    base = oracle.outer_step(p.X, p.y, w0, b, s, eta, LOGISTIC, 1, 2, return_parts=True)
+    m32 = oracle.outer_step(p.X, p.y, w0, b, s, eta, LOGISTIC, 1, 2, return_parts=True,
+                            margins="fp32")
+    assert np.array_equal(oracle.bf16_round(m32["r"]), base["r"])
+    assert not np.array_equal(m32["r"], base["r"])
+    ref = oracle.outer_step(p.X, p.y, w0, b, s, eta, LOGISTIC, 1, 2, mode="fp64",
+                            storage="bf16")
+    e_bf = np.linalg.norm(base["w"] - ref)
+    e_32 = np.linalg.norm(m32["w"] - ref)
+    assert e_32 < e_bf <= 1e-2 * np.linalg.norm(ref)
+    one = oracle.outer_step(p.X, p.y, w0, 48, 1, eta, LOGISTIC, 1, 2)
+    assert np.array_equal(one, oracle.outer_step(p.X, p.y, w0, 48, 1, eta, LOGISTIC, 1, 2,
+                                                 gram="bf16"))
+    gb = oracle.outer_step(p.X, p.y, w0, b, s, eta, LOGISTIC, 1, 2, gram="bf16")
+    d = np.linalg.norm(gb - base["w"]) / np.linalg.norm(base["w"])
+    assert 0 < d < 2.0**-8
+
+
 def test_emulate_close_to_fp64_on_bf16_storage():
     p = si.make_problem(1)
     r = p.recipe
