@@ -16,7 +16,7 @@ import torch
 from ._native import (  # noqa: F401
     CASGD_LOGISTIC, CASGD_LSQ, CASGD_POISSON, FLAG_GRAM_MULTICAST, FLAG_GRAM_NO_CLUSTER,
     FLAG_FAR_FROM_GRAM, FLAG_FULL_G, FLAG_GRAM_PAIR, FLAG_SAMPLE_PERMUTED, FLAG_NO_FUSE,
-    FLAG_TRACE_CHAIN,
+    FLAG_TRACE_CHAIN, FLAG_MARGINS_FP32, FLAG_G_BF16,
     FLAG_GRAM_SIMT,
     FLAG_GRAM_TENSOR,
     FLAG_TEST_STALL, FLAG_WRITE_DIAG_BLOCKS, STAGE_EVENTS, CasgdError, Data as _Data,
@@ -144,7 +144,9 @@ class Taps:
             idx_out=torch.empty(S, dtype=torch.int32, device=device),
             G_out=(torch.empty(gram_elems(params.b, params.s, params.flags), dtype=torch.float32,
                                device=device) if G else None),
-            r_out=torch.empty(S, dtype=torch.int16, device=device),
+            # BF16 bit patterns, or FP32 values (two int16 each) with FLAG_MARGINS_FP32
+            r_out=torch.empty(2 * S if params.flags & FLAG_MARGINS_FP32 else S,
+                              dtype=torch.int16, device=device),
             alpha_out=torch.empty(S, dtype=torch.float32, device=device),
         )
 

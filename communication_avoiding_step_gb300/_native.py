@@ -24,6 +24,8 @@ FLAG_TRACE_CHAIN = 0x100
 FLAG_FAR_FROM_GRAM = 0x200
 FLAG_FULL_G = 0x400
 FLAG_SAMPLE_PERMUTED = 0x800
+FLAG_MARGINS_FP32 = 0x1000
+FLAG_G_BF16 = 0x2000
 FLAG_TEST_STALL = 0x80000000
 STAGE_EVENTS = 5
 

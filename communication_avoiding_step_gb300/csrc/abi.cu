@@ -22,7 +22,7 @@ struct Resolved {
   Layout L;
   Ctrl* ctrl;
   int32_t* idx;
-  uint16_t* r;
+  float* r;  // margins as FP32 values (BF16-representable in the recipe)
   float* yY;
   float* alpha;
   float* far;
@@ -73,7 +73,7 @@ Resolved resolve(void* ws, const Layout& L) {
   R.L = L;
   R.ctrl = reinterpret_cast<Ctrl*>(base);
   R.idx = reinterpret_cast<int32_t*>(base + L.off_idx);
-  R.r = reinterpret_cast<uint16_t*>(base + L.off_r);
+  R.r = reinterpret_cast<float*>(base + L.off_r);
   R.yY = reinterpret_cast<float*>(base + L.off_yY);
   R.alpha = reinterpret_cast<float*>(base + L.off_alpha);
   R.far = reinterpret_cast<float*>(base + L.off_far);
@@ -205,9 +205,11 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
     if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
   } else {
     if (choice == 1)
-      CK(launch_gram_tc(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag, mode, G, R.ctrl, p->timeout_us, c));
+      CK(launch_gram_tc(R.Y, L.S, d->n, L.ldY, p->b, p->s, p->flags, mode, G, R.ctrl,
+                        p->timeout_us, c));
     else
-      CK(launch_gram_simt(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag, G, c));
+      CK(launch_gram_simt(R.Y, L.S, d->n, L.ldY, p->b, p->s, diag,
+                          (p->flags & CASGD_FLAG_G_BF16) != 0, G, c));
     // (The sum of G over processes would sit here; on one GPU it is the identity.)
     if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
     CK(launch_recur(G, R.r, R.yY, R.alpha, R.far, R.slab, p->b, p->s, p->eta, p->loss,
@@ -221,8 +223,12 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   if (taps) {
     if (taps->idx_out)
       CK(cudaMemcpyAsync(taps->idx_out, R.idx, L.S * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
-    if (taps->r_out)
-      CK(cudaMemcpyAsync(taps->r_out, R.r, L.S * sizeof(uint16_t), cudaMemcpyDeviceToDevice, st));
+    if (taps->r_out) {
+      if (p->flags & CASGD_FLAG_MARGINS_FP32)
+        CK(cudaMemcpyAsync(taps->r_out, R.r, L.S * sizeof(float), cudaMemcpyDeviceToDevice, st));
+      else  // the BF16 bit patterns of the (BF16-valued) margins
+        CK(launch_bf16_bits(R.r, L.S, taps->r_out, c));
+    }
     if (taps->alpha_out)
       CK(cudaMemcpyAsync(taps->alpha_out, R.alpha, L.S * sizeof(float), cudaMemcpyDeviceToDevice, st));
   }
@@ -247,7 +253,6 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   float* Gb[2] = {R.G, R.G2};
   int32_t* Ib[2] = {R.idx, R.idx2};
   float* yb[2] = {R.yY, R.yY2};
-  const bool diag = (p->flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
   const cudaStream_t st = c.stream;
   int rc;
   float* fpart = far ? R.fpart : nullptr;
@@ -260,7 +265,7 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
       CK(launch_gather(*d, *p, w, k, nullptr, Ib[cur], Yb[cur], L.ldY, R.r, yb[cur], R.alpha,
                        R.far, nullptr, R.ctrl, R.slab, GATHER_ONLY, c));
       if (!far)
-        CK(launch_gram_tc(Yb[cur], L.S, d->n, L.ldY, p->b, p->s, diag, 0, Gb[cur], R.ctrl,
+        CK(launch_gram_tc(Yb[cur], L.S, d->n, L.ldY, p->b, p->s, p->flags, 0, Gb[cur], R.ctrl,
                           p->timeout_us, c));
     }
     if (it + 1 < iters)  // next iteration's rows (into the buffers the last launch
@@ -336,8 +341,8 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms)
   off += align_up((size_t)(kLossCtas + kLossSlots) * sizeof(double));
   L.off_idx = off;
   off += align_up((size_t)L.S * sizeof(int32_t));
-  L.off_r = off;
-  off += align_up((size_t)L.S * sizeof(uint16_t));
+  L.off_r = off;  // margins FP32[S] (BF16 values, or FP32 sums with MARGINS_FP32)
+  off += align_up((size_t)L.S * sizeof(float));
   L.off_yY = off;
   off += align_up((size_t)L.S * sizeof(float));
   L.off_alpha = off;

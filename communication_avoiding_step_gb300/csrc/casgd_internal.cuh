@@ -13,6 +13,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/casgd.h"
@@ -134,6 +135,11 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
 }
 
+// x rounded to the nearest BF16 value (ties to even), as FP32 (CASGD_FLAG_G_BF16)
+__device__ __forceinline__ float round_bf16(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
 // SplitMix64 output number `counter` of the stream started at state `seed`.
 __device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t counter) {
   uint64_t z = seed + (counter + 1ull) * 0x9E3779B97F4A7C15ull;
@@ -239,6 +245,8 @@ struct Ctx {
 
 cudaError_t launch_store_bf16(const float* src, int64_t m, int64_t n, int64_t ld_src,
                               uint16_t* dst, int64_t ld_dst, Ctx& c);
+// dst[i] = the BF16 bits of src[i] (values already BF16-representable: exact)
+cudaError_t launch_bf16_bits(const float* src, int64_t count, uint16_t* dst, Ctx& c);
 // permuted: without replacement (per-epoch permutation), else with replacement
 cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t counter0,
                           bool permuted, int32_t* idx, Ctx& c);
@@ -250,25 +258,26 @@ cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t coun
 enum { GATHER_AND_MARGINS = 0, GATHER_ONLY = 1, MARGINS_ONLY = 2 };
 cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const float* w,
                           uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
-                          int64_t ldY, uint16_t* r, float* yY, float* alpha, float* far,
+                          int64_t ldY, float* r, float* yY, float* alpha, float* far,
                           float* fpart, Ctrl* ctrl, uint32_t* slab, int mode, Ctx& c);
 // GATHER_ONLY for iteration k_next (into Y_next, yY_next, idx_next) and MARGINS_ONLY for
 // the rows in Y, in one launch (the two touch disjoint buffers).
 cudaError_t launch_gather_next_margins(const casgd_data_t& d, const casgd_params_t& p,
                                        const float* w, uint64_t k_next, int32_t* idx_next,
                                        uint16_t* Y_next, float* yY_next, const uint16_t* Y,
-                                       int64_t ldY, uint16_t* r, float* alpha, float* far,
+                                       int64_t ldY, float* r, float* alpha, float* far,
                                        float* fpart, Ctrl* ctrl, uint32_t* slab, Ctx& c);
+// g_bf16: every stored entry rounded to BF16 (CASGD_FLAG_G_BF16)
 cudaError_t launch_gram_simt(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
-                             int s, bool diag, float* G, Ctx& c);
+                             int s, bool diag, bool g_bf16, float* G, Ctx& c);
 bool gram_tc_supported(int64_t S, int64_t n, int b);
 cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
-                           int s, bool diag, int mode, float* G, Ctrl* ctrl,
+                           int s, uint32_t flags, int mode, float* G, Ctrl* ctrl,
                            uint32_t timeout_us, Ctx& c);
 // The recurrence with the weight update fused: part[j][:] for each of the s blocks j
 // (s partial rows of ldY floats), added to w (FP32[n]) by the last unit of each
 // 64-column chunk.  counters: the workspace's counters area (timeline_of).
-cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, float* alpha,
+cudaError_t launch_recur(const float* G, const float* r, const float* yY, float* alpha,
                          float* far, uint32_t* counters, int b, int s, float eta, int loss,
                          uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, const uint16_t* Y,
                          int64_t ldY, int64_t n, float* part, float* w, Ctx& c);
@@ -287,7 +296,7 @@ bool gram_recur_fused_supported(int64_t S, int64_t n, int b);
 bool far_gram_supported(int64_t S, int64_t n, int b);
 cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t S, int64_t n,
                               int64_t ldY, int b, int s, float eta, int loss, uint32_t flags,
-                              const float* G, const uint16_t* Y, const uint16_t* r,
+                              const float* G, const uint16_t* Y, const float* r,
                               const float* yY, float* alpha, float* far, uint32_t* slab,
                               float* fpart, float* part, float* w, Ctrl* ctrl,
                               uint32_t timeout_us, Ctx& c);

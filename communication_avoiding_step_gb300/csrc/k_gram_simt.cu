@@ -21,7 +21,8 @@ constexpr int kKC = 32;
 
 __global__ void __launch_bounds__(256) gram_simt_kernel(const uint16_t* __restrict__ Y,
                                                         int64_t S, int64_t ldY, int b,
-                                                        bool diag, float* __restrict__ G) {
+                                                        bool diag, bool g_bf16,
+                                                        float* __restrict__ G) {
   const int64_t R0 = (int64_t)blockIdx.y * kTile;
   const int64_t C0 = (int64_t)blockIdx.x * kTile;
   if (R0 >= S || C0 >= S) return;
@@ -80,7 +81,8 @@ __global__ void __launch_bounds__(256) gram_simt_kernel(const uint16_t* __restri
       if (q >= S) continue;
       const int64_t tb = q / b;
       if (tb > jb || (tb == jb && !diag)) continue;
-      G[packed_offset(jb, tb, b, diag) + (p - jb * b) * b + (q - tb * b)] = acc[i][e];
+      G[packed_offset(jb, tb, b, diag) + (p - jb * b) * b + (q - tb * b)] =
+          g_bf16 ? round_bf16(acc[i][e]) : acc[i][e];
     }
   }
 }
@@ -88,12 +90,12 @@ __global__ void __launch_bounds__(256) gram_simt_kernel(const uint16_t* __restri
 }  // namespace
 
 cudaError_t launch_gram_simt(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
-                             int s, bool diag, float* G, Ctx& c) {
+                             int s, bool diag, bool g_bf16, float* G, Ctx& c) {
   (void)n;
   (void)s;
   const int64_t T = (S + kTile - 1) / kTile;
   dim3 grid((unsigned)T, (unsigned)T);
-  gram_simt_kernel<<<grid, 256, 0, c.stream>>>(Y, S, ldY, b, diag, G);
+  gram_simt_kernel<<<grid, 256, 0, c.stream>>>(Y, S, ldY, b, diag, g_bf16, G);
   ++c.launches;
   return cudaGetLastError();
 }

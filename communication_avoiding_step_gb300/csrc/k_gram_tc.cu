@@ -59,6 +59,7 @@ struct TcArgs {
   int n, b, nkb;
   int TR, TC, ntiles;  // ntiles: work items (tiles; units of nb tiles when fpart is set)
   bool diag;
+  bool g_bf16;     // entries rounded to BF16 before they are stored or used
   bool tma_store;  // b % 32 == 0: 32x32 chunks go out through a TMA tensor store
   uint64_t timeout_ns;
   uint32_t* slab;  // recurrence in the same launch: per-32-row tile counters (else null)
@@ -365,6 +366,10 @@ __device__ __forceinline__ void store_tile_rows(const TcArgs& a, uint32_t tmem, 
     uint32_t v[32];
     __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
     tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
+    if (a.g_bf16) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(round_bf16(__uint_as_float(v[e])));
+    }
     const int64_t q0 = (int64_t)ca * BN + ch * 32;
     if (a.tma_store) {  // warp-uniform
       if (p0 >= a.S || q0 >= a.S) continue;
@@ -778,17 +783,23 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32]) {
                : "memory");
 }
 
-__device__ __forceinline__ void far_chunk(const uint32_t (&v)[32], const float* al,
+// An accumulator entry as the recurrence uses it: FP32, or rounded to BF16 (G_BF16).
+__device__ __forceinline__ float far_entry(uint32_t bits, bool g_bf16) {
+  const float g = __uint_as_float(bits);
+  return g_bf16 ? round_bf16(g) : g;
+}
+
+__device__ __forceinline__ void far_chunk(const uint32_t (&v)[32], const float* al, bool g_bf16,
                                           float (&sum)[8]) {
   const float4* a4 = reinterpret_cast<const float4*>(al);
 #pragma unroll
   for (int e4 = 0; e4 < 8; ++e4) {
     const float4 w = a4[e4];
     const int o = (e4 & 1) * 4;
-    sum[o + 0] = fmaf(__uint_as_float(v[4 * e4 + 0]), w.x, sum[o + 0]);
-    sum[o + 1] = fmaf(__uint_as_float(v[4 * e4 + 1]), w.y, sum[o + 1]);
-    sum[o + 2] = fmaf(__uint_as_float(v[4 * e4 + 2]), w.z, sum[o + 2]);
-    sum[o + 3] = fmaf(__uint_as_float(v[4 * e4 + 3]), w.w, sum[o + 3]);
+    sum[o + 0] = fmaf(far_entry(v[4 * e4 + 0], g_bf16), w.x, sum[o + 0]);
+    sum[o + 1] = fmaf(far_entry(v[4 * e4 + 1], g_bf16), w.y, sum[o + 1]);
+    sum[o + 2] = fmaf(far_entry(v[4 * e4 + 2], g_bf16), w.z, sum[o + 2]);
+    sum[o + 3] = fmaf(far_entry(v[4 * e4 + 3], g_bf16), w.w, sum[o + 3]);
   }
 }
 
@@ -797,7 +808,7 @@ __device__ __forceinline__ void far_chunk(const uint32_t (&v)[32], const float* 
 // column e into sum e % 8.  The load of the next 32 columns is in flight while the
 // current ones are summed.
 __device__ __forceinline__ void far_tile_dot(uint32_t tmem, int acc, int quarter,
-                                             const float* al, float (&sum)[8]) {
+                                             const float* al, bool g_bf16, float (&sum)[8]) {
   const uint32_t base = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
   uint32_t va[32], vb[32];
   __syncwarp();
@@ -806,10 +817,10 @@ __device__ __forceinline__ void far_tile_dot(uint32_t tmem, int acc, int quarter
 #pragma unroll
   for (int ch = 0; ch < BN / 32; ch += 2) {
     tmem_ld32_issue(base + (uint32_t)(ch + 1) * 32, vb);
-    far_chunk(va, al + ch * 32, sum);
+    far_chunk(va, al + ch * 32, g_bf16, sum);
     tmem_wait_ld(vb);
     if (ch + 2 < BN / 32) tmem_ld32_issue(base + (uint32_t)(ch + 2) * 32, va);
-    far_chunk(vb, al + (ch + 1) * 32, sum);
+    far_chunk(vb, al + (ch + 1) * 32, g_bf16, sum);
     if (ch + 2 < BN / 32) tmem_wait_ld(va);
   }
 }
@@ -973,7 +984,7 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
         tphase[acc] ^= 1u;
         tc_fence_after();
         if (kFar && far) {
-          if (!dead) far_tile_dot(tmem, acc, quarter, al_s, sum);
+          if (!dead) far_tile_dot(tmem, acc, quarter, al_s, a.g_bf16, sum);
         } else {
           store_tile_rows(a, tmem, acc, quarter, lane, ra, ca, &tmG, stage, sbuf);
         }
@@ -1069,7 +1080,9 @@ struct TcPlan {
 
 // Tensor maps and tile counts shared by every variant.  kcl: CTAs per row group.
 cudaError_t plan_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b, int s,
-                    bool diag, int kcl, float* G, Ctrl* ctrl, uint32_t timeout_us, TcPlan& P) {
+                    uint32_t flags, int kcl, float* G, Ctrl* ctrl, uint32_t timeout_us,
+                    TcPlan& P) {
+  const bool diag = (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t gdim[2] = {(cuuint64_t)n, (cuuint64_t)S};
@@ -1090,6 +1103,7 @@ cudaError_t plan_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
   a.TR = (int)((S + BM - 1) / BM);
   a.TC = (int)((S + BN - 1) / BN);
   a.diag = diag;
+  a.g_bf16 = (flags & CASGD_FLAG_G_BF16) != 0;
   a.timeout_ns = (uint64_t)(timeout_us ? timeout_us : 1000000u) * 1000ull;
   a.slab = nullptr;
   a.fpart = nullptr;
@@ -1151,7 +1165,7 @@ cudaLaunchConfig_t cluster2_config(unsigned threads, size_t smem, cudaStream_t s
 }  // namespace
 
 cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b, int s,
-                           bool diag, int mode, float* G, Ctrl* ctrl, uint32_t timeout_us,
+                           uint32_t flags, int mode, float* G, Ctrl* ctrl, uint32_t timeout_us,
                            Ctx& c) {
   if (S <= 0) return cudaSuccess;
   // mode 0: paired-SM MMA (default); 1: one CTA per tile; 2: 2-CTA clusters sharing B
@@ -1159,7 +1173,7 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
   if ((S + BM - 1) / BM <= 1) mode = 1;
   const int kcl = mode == 1 ? 1 : 2;
   TcPlan P;
-  cudaError_t e = plan_tc(Y, S, n, ldY, b, s, diag, kcl, G, ctrl, timeout_us, P);
+  cudaError_t e = plan_tc(Y, S, n, ldY, b, s, flags, kcl, G, ctrl, timeout_us, P);
   if (e != cudaSuccess) return e;
   TcArgs& a = P.a;
   if (a.ntiles == 0) return cudaSuccess;
@@ -1210,7 +1224,7 @@ bool far_gram_supported(int64_t S, int64_t n, int b) {
 
 cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t S, int64_t n,
                               int64_t ldY, int b, int s, float eta, int loss, uint32_t flags,
-                              const float* G, const uint16_t* Y, const uint16_t* r,
+                              const float* G, const uint16_t* Y, const float* r,
                               const float* yY, float* alpha, float* far, uint32_t* slab,
                               float* fpart, float* part, float* w, Ctrl* ctrl,
                               uint32_t timeout_us, Ctx& c) {
@@ -1219,7 +1233,7 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
   if (far_gram && (next || !far_gram_supported(S, n, b))) return cudaErrorNotSupported;
   const bool diag = (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
   TcPlan P;
-  cudaError_t e = plan_tc(Yg, S, n, ldY, b, s, diag, 2, Gg, ctrl, timeout_us, P);
+  cudaError_t e = plan_tc(Yg, S, n, ldY, b, s, flags, 2, Gg, ctrl, timeout_us, P);
   if (e != cudaSuccess) return e;
   P.a.slab = next ? nullptr : slab;
   RecArgs rec = make_rec_args(G, r, yY, alpha, far, slab, b, s, eta, loss, flags, timeout_us,

@@ -38,6 +38,13 @@ __global__ void store_bf16_kernel(const float* __restrict__ src, int64_t m, int6
   }
 }
 
+__global__ void bf16_bits_kernel(const float* __restrict__ src, int64_t count,
+                                 uint16_t* __restrict__ dst) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count;
+       i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(src[i]));
+}
+
 __global__ void sample_kernel(uint32_t m, int64_t count, uint64_t seed, uint64_t counter0,
                               int perm_d, int32_t* __restrict__ idx) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count;
@@ -67,7 +74,7 @@ struct RowArgs {
   int32_t* idx_out;
   uint16_t* Y;
   int64_t ldY;
-  uint16_t* r;
+  float* r;  // margins: BF16-rounded FP32 values, or the FP32 sums (r_fp32)
   float* yY;
   float* alpha;
   float* far;
@@ -77,6 +84,7 @@ struct RowArgs {
   uint32_t* slab;
   int G;
   int perm_d;  // sampling: 0 with replacement, else perm_width(m) (per-epoch permutation)
+  bool r_fp32;  // margins kept in FP32 (CASGD_FLAG_MARGINS_FP32), r then holds floats
 };
 
 // The recurrence's per-step reset (one CTA).
@@ -186,7 +194,7 @@ __device__ __forceinline__ void gather_rows(const RowArgs& a, int64_t blk) {
   }
   if (live && g == 0) {
     if (kMargin) {
-      a.r[p] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+      a.r[p] = a.r_fp32 ? acc : round_bf16(acc);
       a.alpha[p] = __uint_as_float(kAlphaPending);  // the recurrence waits on these values
       a.far[p] = __uint_as_float(kAlphaPending);
     }
@@ -234,6 +242,15 @@ cudaError_t launch_store_bf16(const float* src, int64_t m, int64_t n, int64_t ld
   return cudaGetLastError();
 }
 
+cudaError_t launch_bf16_bits(const float* src, int64_t count, uint16_t* dst, Ctx& c) {
+  if (count == 0) return cudaSuccess;
+  int64_t blocks = (count + 255) / 256;
+  if (blocks > (int64_t)c.num_sms * 8) blocks = (int64_t)c.num_sms * 8;
+  bf16_bits_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>(src, count, dst);
+  ++c.launches;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t counter0,
                           bool permuted, int32_t* idx, Ctx& c) {
   if (count == 0) return cudaSuccess;
@@ -248,7 +265,7 @@ cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t coun
 namespace {
 
 RowArgs row_args(const casgd_data_t& d, const casgd_params_t& p, const float* w, uint64_t k,
-                 const int32_t* idx_in, int32_t* idx, uint16_t* Y, int64_t ldY, uint16_t* r,
+                 const int32_t* idx_in, int32_t* idx, uint16_t* Y, int64_t ldY, float* r,
                  float* yY, float* alpha, float* far, float* fpart, Ctrl* ctrl,
                  uint32_t* slab) {
   RowArgs a;
@@ -278,6 +295,7 @@ RowArgs row_args(const casgd_data_t& d, const casgd_params_t& p, const float* w,
   a.slab = slab;
   a.G = pow2_at_least(ldY / 8, 32);
   a.perm_d = (p.flags & CASGD_FLAG_SAMPLE_PERMUTED) ? perm_width(d.m) : 0;
+  a.r_fp32 = (p.flags & CASGD_FLAG_MARGINS_FP32) != 0;
   return a;
 }
 
@@ -290,7 +308,7 @@ int64_t row_blocks(const RowArgs& a) {
 
 cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const float* w,
                           uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
-                          int64_t ldY, uint16_t* r, float* yY, float* alpha, float* far,
+                          int64_t ldY, float* r, float* yY, float* alpha, float* far,
                           float* fpart, Ctrl* ctrl, uint32_t* slab, int mode, Ctx& c) {
   const RowArgs a =
       row_args(d, p, w, k, idx_in, idx, Y, ldY, r, yY, alpha, far, fpart, ctrl, slab);
@@ -305,7 +323,7 @@ cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const 
 cudaError_t launch_gather_next_margins(const casgd_data_t& d, const casgd_params_t& p,
                                        const float* w, uint64_t k_next, int32_t* idx_next,
                                        uint16_t* Y_next, float* yY_next, const uint16_t* Y,
-                                       int64_t ldY, uint16_t* r, float* alpha, float* far,
+                                       int64_t ldY, float* r, float* alpha, float* far,
                                        float* fpart, Ctrl* ctrl, uint32_t* slab, Ctx& c) {
   const RowArgs g = row_args(d, p, w, k_next, nullptr, idx_next, Y_next, ldY, nullptr, yY_next,
                              nullptr, nullptr, nullptr, ctrl, slab);

@@ -23,7 +23,7 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(RecArgs a) {
 
 }  // namespace
 
-RecArgs make_rec_args(const float* G, const uint16_t* r, const float* yY, float* alpha,
+RecArgs make_rec_args(const float* G, const float* r, const float* yY, float* alpha,
                       float* far, uint32_t* counters, int b, int s, float eta, int loss,
                       uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, const uint16_t* Y,
                       int64_t ldY, int64_t n, float* part, float* w) {
@@ -67,7 +67,7 @@ RecArgs make_rec_args(const float* G, const uint16_t* r, const float* yY, float*
   return a;
 }
 
-cudaError_t launch_recur(const float* G, const uint16_t* r, const float* yY, float* alpha,
+cudaError_t launch_recur(const float* G, const float* r, const float* yY, float* alpha,
                          float* far, uint32_t* counters, int b, int s, float eta, int loss,
                          uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, const uint16_t* Y,
                          int64_t ldY, int64_t n, float* part, float* w, Ctx& c) {

@@ -54,7 +54,7 @@ constexpr int kChainRows = 8;     // rows per chain group (a warp per row)
 
 struct RecArgs {
   const float* G;
-  const uint16_t* r;
+  const float* r;  // margins (BF16 values in the recipe)
   const float* yY;
   float* alpha;
   float* far;
@@ -110,7 +110,7 @@ inline int update_groups(const RecArgs& a, int nbulk) {
 
 // Fills every field but C and upd_groups (chosen by the launcher from its grid) and slab.
 // counters: the workspace's counters area (timeline_of); w: FP32[n], updated in place.
-RecArgs make_rec_args(const float* G, const uint16_t* r, const float* yY, float* alpha,
+RecArgs make_rec_args(const float* G, const float* r, const float* yY, float* alpha,
                       float* far, uint32_t* counters, int b, int s, float eta, int loss,
                       uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, const uint16_t* Y,
                       int64_t ldY, int64_t n, float* part, float* w);
@@ -281,7 +281,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
     rb = 0;
     yv = f0 = f1 = 0.0f;
     if (lane == 0) {
-      rb = a.r[p];
+      rb = __float_as_uint(a.r[p]);
       yv = a.yY[p];
     }
     if (j < kB + 1) return;
@@ -484,7 +484,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
       farv = fs;
     }
     if (lane == 0 && !(a.stall_test && j == 0)) {
-      const float z = bf16_bits_to_float(rbits) + farv + acc;
+      const float z = __uint_as_float(rbits) + farv + acc;
       __stcg(a.alpha + p, a.coef * loss_deriv(a.loss, z, yj));
     }
     if (tracer && gi == ng - 1) a.trace[4 * j + 3] = globaltimer_ns();

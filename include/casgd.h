@@ -123,6 +123,16 @@ enum {
                                               run of m draws from an epoch boundary
                                               visits every row once.  Also honoured
                                               by casgd_sgd_fp32                       */
+#define CASGD_FLAG_MARGINS_FP32      0x1000u /* precision variant: keep the margins r
+                                              as their FP32 sums (no rounding to BF16);
+                                              the r_out tap then receives S FP32
+                                              values (4*S bytes)                      */
+#define CASGD_FLAG_G_BF16            0x2000u /* precision variant: round every entry of
+                                              G to BF16 (nearest even) after its FP32
+                                              accumulation and before the recurrence
+                                              uses it, as when G is summed across
+                                              processes in BF16; stored blocks (and the
+                                              G_out tap) hold the rounded values      */
 #define CASGD_FLAG_TEST_STALL        0x80000000u /* test only: the recurrence's first
                                               block never signals completion, so every
                                               waiter runs into its time bound and the
@@ -159,7 +169,9 @@ typedef struct {
                             j ascending then t ascending, each b x b row-major;
                             casgd_gram_elems() floats (with FAR_FROM_GRAM only
                             the band and diagonal blocks are written)           */
-  uint16_t* r_out;       /* receives the S BF16 margins (bit patterns)          */
+  uint16_t* r_out;       /* receives the S BF16 margins (bit patterns); with
+                            CASGD_FLAG_MARGINS_FP32 the S FP32 margins (4*S
+                            bytes)                                              */
   float* alpha_out;      /* receives the S FP32 step coefficients alpha         */
 } casgd_taps_t;
 

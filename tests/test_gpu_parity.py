@@ -432,6 +432,72 @@ def test_far_from_gram_unsupported_shapes(gpu_lib):
         assert torch.count_nonzero(w).item() == 0
 
 
+# ------------------------------------------------- precision variants (f3) ----
+PREC_CASES = [
+    # far-forming Gram (b = 256), stored-G pair launch (b = 100), CUDA-core Gram
+    ("recipe2_m20000", lambda: si.make_problem(2, m=20000), None, 0),
+    ("ragged_3000x130_b100_s6", lambda: si.make_random(3000, 130, si.POISSON, seed=3),
+     (100, 6, 0.02), 0),
+    ("ragged_777x37_b24_s3_simt", lambda: si.make_random(777, 37, si.LOGISTIC, seed=1),
+     (24, 3, 0.3), "simt"),
+]
+
+
+@pytest.mark.parametrize("variant", ["margins_fp32", "g_bf16", "both"])
+@pytest.mark.parametrize("name,factory,override,gram", PREC_CASES,
+                         ids=[c[0] for c in PREC_CASES])
+def test_precision_variants_parity(gpu_lib, name, factory, override, gram, variant):
+    """CASGD_FLAG_MARGINS_FP32 / CASGD_FLAG_G_BF16 against the oracle's emulating mode
+    with the same choice: FP32 margins within FP32 summation order, G blocks the BF16
+    rounding of the oracle's (one-ulp flips where the FP32 sums straddle a rounding
+    boundary), alpha and w with the recipe's bars; and each variant changes w."""
+    casgd = gpu_lib
+    p = factory()
+    fl = casgd.FLAG_WRITE_DIAG_BLOCKS | (casgd.FLAG_GRAM_SIMT if gram == "simt" else 0)
+    m32 = variant in ("margins_fp32", "both")
+    gbf = variant in ("g_bf16", "both")
+    vfl = (casgd.FLAG_MARGINS_FP32 if m32 else 0) | (casgd.FLAG_G_BF16 if gbf else 0)
+    params = _params(casgd, p, override, fl | vfl)
+    b, s = params.b, params.s
+    data = _dev(p, casgd)
+    w0 = si.random_weights(p.n, seed=7, scale=0.5)
+    w_gpu, taps, st = _run_step(casgd, data, params, w0, k=3)
+    assert st == 0
+    ref = oracle.outer_step(p.X, p.y, w0, b, s, params.eta, p.recipe.loss, 0, 3,
+                            mode="emulate", return_parts=True,
+                            margins="fp32" if m32 else "bf16", gram="bf16" if gbf else "fp32")
+    assert np.array_equal(taps.idx_out.cpu().numpy(), ref["idx"])
+    if m32:
+        r_gpu = taps.r_out.cpu().numpy().view(np.float32)
+        assert r_gpu.shape == ref["r"].shape
+        assert np.all(np.abs(r_gpu - ref["r"]) <= 1e-5 * np.abs(ref["r"]) + 1e-6)
+    else:
+        r_gpu = (taps.r_out.cpu().numpy().view(np.uint16).astype(np.uint32) << 16).view(np.float32)
+        assert np.all(np.abs(r_gpu - ref["r"]) <= _bf16_ulp(ref["r"]) + 1e-38)
+    # blocks every path stores: the diagonal and the first band block
+    for j in range(s):
+        for t in ([j - 1, j] if j > 0 else [j]):
+            o = oracle.packed_block_offset(j, t, b, True)
+            g_ref = oracle.gram_block(ref["Y"], b, j, t, "emulate").reshape(-1)
+            g_gpu = taps.G_out[o:o + b * b].cpu().numpy()
+            if gbf:
+                # the GPU rounds its own FP32 sum, within the summation-order bound
+                # d = 2 n u sum_k |y_ik y_tk| of the oracle's: |g - g_ref| <= d + ulp/2
+                Yj = np.abs(ref["Y"][j * b:(j + 1) * b].astype(np.float64))
+                Yt = np.abs(ref["Y"][t * b:(t + 1) * b].astype(np.float64))
+                d = (2.0 * p.n * 2.0**-24) * (Yj @ Yt.T).reshape(-1)
+                g64 = g_ref.astype(np.float64)
+                assert np.all(np.abs(g_gpu - g64) <= d + 0.5 * _bf16_ulp(np.abs(g64) + d) + 1e-30)
+                assert np.mean(g_gpu != oracle.bf16_round(g_ref)) <= 0.01
+                assert np.array_equal(oracle.bf16_round(g_gpu), g_gpu)  # BF16 values
+            else:
+                assert _rel(g_gpu, g_ref) <= GRAM_TOL * _len_scale(p.n)
+    assert _rel(taps.alpha_out.cpu().numpy(), ref["alpha"]) <= 2e-3 * _len_scale(p.n)
+    assert _rel(w_gpu, ref["w"]) <= W_TOL * _len_scale(p.n)
+    w_rec, _, st = _run_step(casgd, data, _params(casgd, p, override, fl), w0, k=3)
+    assert st == 0 and not np.array_equal(w_rec, w_gpu)
+
+
 def test_outer_step_given_indices_and_bad_index(gpu_lib):
     casgd = gpu_lib
     p = si.make_problem(1)
