@@ -331,7 +331,7 @@ def run_ours(args):
     # recurrence and the update share one launch (its time is the "gram" stage; the
     # "recurrence" stage is then empty)
     gram_name = {1: "gram_tc", 2: "gram_simt", 3: "gram_recur", 4: "gram_recur",
-                 5: "gram_recur_far"}[kind]
+                 5: "gram_recur_far", 6: "gram_recur_far"}[kind]
     stages_out = {}
     for st in STAGES:
         t = per_launch_ms[st] / 1e3

@@ -238,9 +238,9 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
 // casgd_train with the paired-SM Gram sharing the recurrence's launch: the Gram of
 // iteration k+1 (whose rows are sampled ahead: only the margins need the current w)
 // runs in the launch of iteration k's recurrence, on double-buffered Y and G.  With the
-// far-forming Gram (far) the Gram of iteration k runs in iteration k's launch (its far
-// tiles need this iteration's alpha) and only Y is double-buffered: the rows of
-// iteration k+1 are still gathered in the launch that forms iteration k's margins.
+// far-forming Gram (far) the launch of iteration k forms iteration k's far sums (they
+// need this iteration's alpha) and stores the band of iteration k+1, so the recurrence
+// starts on a complete band; the first iteration's band comes from a prologue launch.
 // Every value is computed as in outer_step_impl (same kernels' arithmetic), only the
 // order of independent work changes.  Stage events per iteration: 0 before the gather of
 // the next iteration's rows and this iteration's margins, 1 before the shared launch, 2,
@@ -256,15 +256,18 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   const cudaStream_t st = c.stream;
   int rc;
   float* fpart = far ? R.fpart : nullptr;
-  if (prof) prof->gram_kind = far ? 5 : 4;
+  if (prof) prof->gram_kind = far ? 6 : 4;
   for (int32_t it = 0; it < iters; ++it) {
     const int cur = it & 1, nxt = cur ^ 1;
     const uint64_t k = k0 + (uint64_t)it;
     if ((rc = record(prof, it, 0, st)) != CASGD_OK) return rc;
-    if (it == 0) {  // prologue: this iteration's rows (and, one ahead, its Gram)
+    if (it == 0) {  // prologue: this iteration's rows and its Gram (far: its band)
       CK(launch_gather(*d, *p, w, k, nullptr, Ib[cur], Yb[cur], L.ldY, R.r, yb[cur], R.alpha,
                        R.far, nullptr, R.ctrl, R.slab, GATHER_ONLY, c));
-      if (!far)
+      if (far)
+        CK(launch_gram_band(Yb[cur], Gb[cur], L.S, d->n, L.ldY, p->b, p->s, p->flags, R.ctrl,
+                            p->timeout_us, c));
+      else
         CK(launch_gram_tc(Yb[cur], L.S, d->n, L.ldY, p->b, p->s, p->flags, 0, Gb[cur], R.ctrl,
                           p->timeout_us, c));
     }
@@ -278,10 +281,11 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
     if ((rc = record(prof, it, 1, st)) != CASGD_OK) return rc;
     // (The sum of G over processes would sit before this launch; on one GPU it is the
     // identity.)
-    if (far)
-      CK(launch_gram_recur(Yb[cur], R.G, false, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss,
-                           p->flags, R.G, Yb[cur], R.r, yb[cur], R.alpha, R.far, R.slab, fpart,
-                           R.upd, w, R.ctrl, p->timeout_us, c));
+    if (far)  // this iteration's far sums; the next iteration's band (if any) into Gb[nxt]
+      CK(launch_gram_recur(it + 1 < iters ? Yb[nxt] : nullptr, Gb[nxt], true, L.S, d->n, L.ldY,
+                           p->b, p->s, p->eta, p->loss, p->flags, Gb[cur], Yb[cur], R.r,
+                           yb[cur], R.alpha, R.far, R.slab, fpart, R.upd, w, R.ctrl,
+                           p->timeout_us, c));
     else if (it + 1 < iters)
       CK(launch_gram_recur(Yb[nxt], Gb[nxt], true, L.S, d->n, L.ldY, p->b, p->s, p->eta,
                            p->loss, p->flags, Gb[cur], Yb[cur], R.r, yb[cur], R.alpha, R.far,
@@ -349,14 +353,15 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms)
   off += align_up((size_t)L.S * sizeof(float));
   L.off_far = off;  // far sums FP32[S]; the counters area (see timeline_of)
   off += align_up((size_t)L.S * sizeof(float)) +
-         align_up((kMaxSlabs + kMaxUpdChunks) * sizeof(uint32_t) +
+         align_up((kMaxSlabs + kMaxUpdChunks + kMaxUpdBlocks) * sizeof(uint32_t) +
                   (kMaxS + 1) * 4 * sizeof(uint64_t));
   L.off_Y = off;
   off += align_up((size_t)L.S * L.ldY * sizeof(uint16_t));
   L.off_upd = off;
-  // partial rows: upd_ctas for the two-kernel update, s for the update fused into the
-  // recurrence (one row per block)
-  const int64_t upd_rows = L.upd_ctas > s ? L.upd_ctas : s;
+  // partial rows: upd_ctas for the two-kernel update, s * R for the update fused into
+  // the recurrence (one row per block and row part)
+  const int64_t upd_fused = (int64_t)s * upd_row_parts(b, L.ldY);
+  const int64_t upd_rows = L.upd_ctas > upd_fused ? L.upd_ctas : upd_fused;
   off += align_up((size_t)upd_rows * L.ldY * sizeof(float));
   L.off_G = off;
   off += align_up((size_t)L.gram_elems * sizeof(float));
@@ -369,10 +374,8 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms)
     off += align_up((size_t)L.S * sizeof(float));
     L.off_Y2 = off;
     off += align_up((size_t)L.S * L.ldY * sizeof(uint16_t));
-    if (!gp.far) {
-      L.off_G2 = off;
-      off += align_up((size_t)L.gram_elems * sizeof(float));
-    }
+    L.off_G2 = off;  // the far-forming Gram stores the next iteration's band into it
+    off += align_up((size_t)L.gram_elems * sizeof(float));
   }
   if (gp.far) {
     L.off_fpart = off;
@@ -502,7 +505,8 @@ int casgd_train(const casgd_data_t* data, const casgd_params_t* params, float* w
   if (!check_data(data) || !check_params(params) || !w || iters < 0 || loss_every < 0)
     return CASGD_ERR_ARG;
   if (loss_every > 0 && iters / loss_every > 0 && !loss_hist) return CASGD_ERR_ARG;
-  Ctx c{static_cast<cudaStream_t>(stream), 0, 0};
+  LaunchCache cache;  // occupancy of the kernels the loop repeats, found once per call
+  Ctx c{static_cast<cudaStream_t>(stream), 0, 0, &cache};
   if (device_sms(&c.num_sms) != CASGD_OK) return CASGD_ERR_CUDA;
   const Layout L = make_layout(data->n, params->b, params->s, params->flags, c.num_sms);
   int rc = check_ws(ws, ws_bytes, L);

@@ -37,13 +37,19 @@ constexpr int64_t kMaxN = 16384;
 constexpr int kLossCtas = 1024;     // upper bound on loss-kernel CTAs (partials)
 // per-32-row completion counters of the paired-SM Gram (rows padded to 256-row groups)
 constexpr int64_t kMaxSlabs = (kMaxSB + 255) / 256 * 8;
-// per-64-column counters of the weight update's first stage (s partial rows each)
+// per-64-column counters of the weight update (the next block whose sum is added to w)
 constexpr int64_t kMaxUpdChunks = kMaxN / 64;
+// per-(block, 64-column chunk) arrival counters of the update's row parts
+constexpr int64_t kMaxUpdBlocks = kMaxS * kMaxUpdChunks;
 // The counters area of the workspace: kMaxSlabs row counters, kMaxUpdChunks column
-// counters, then the profiling timeline ((kMaxS + 1) x 4 globaltimer stamps).
+// counters, kMaxUpdBlocks block counters, then the profiling timeline ((kMaxS + 1) x 4
+// globaltimer stamps).
 __host__ __device__ inline uint32_t* upd_chunk_counters(uint32_t* slab) { return slab + kMaxSlabs; }
+__host__ __device__ inline uint32_t* upd_block_counters(uint32_t* slab) {
+  return slab + kMaxSlabs + kMaxUpdChunks;
+}
 __host__ __device__ inline uint64_t* timeline_of(uint32_t* slab) {
-  return reinterpret_cast<uint64_t*>(slab + kMaxSlabs + kMaxUpdChunks);
+  return reinterpret_cast<uint64_t*>(slab + kMaxSlabs + kMaxUpdChunks + kMaxUpdBlocks);
 }
 
 // Control block at the start of the workspace (256 bytes, zeroed per step where noted).
@@ -128,6 +134,19 @@ __host__ __device__ inline int far_partials_per_block(int64_t b, int s) {
   for (int npb = nb; npb > 1; --npb)
     if (nb % npb == 0 && npb * nfb <= 64) return npb;
   return 1;
+}
+
+// Row parts of a block in the update fused into the recurrence's launch: units (block,
+// 64-column chunk, row part) with at least ~32 units per block (the last block's units
+// run after the chain and set the launch's tail; every unit has a fixed latency, so more
+// units than the groups clear while the chain runs lengthen it), parts of at least 64
+// rows.  Used where the far sums come from the Gram (the bulk groups only update).
+__host__ __device__ inline int upd_row_parts(int64_t b, int64_t ldY) {
+  const int64_t nchunk = (ldY / 8 + 7) / 8;
+  int64_t R = (32 + nchunk - 1) / nchunk;
+  const int64_t cap = b / 64 > 1 ? b / 64 : 1;
+  if (R > cap) R = cap;
+  return (int)(R < 1 ? 1 : R);
 }
 
 // ------------------------------------------------------------------ device helpers
@@ -232,16 +251,56 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   return v;
 }
 
+__device__ __forceinline__ void red_release_add_u32(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
   return *reinterpret_cast<const volatile uint32_t*>(p);
 }
 
 // ------------------------------------------------------------------ launchers
+// Launch parameters of the kernels one call launches repeatedly (occupancy results, with
+// the dynamic shared memory attribute set), found once per call: the queries cost host
+// time, and in casgd_train's loop that time would fall between the launches.  Owned by
+// the calling C-ABI function, never global.
+struct LaunchCache {
+  static constexpr int kSlots = 16;
+  const void* fn[kSlots] = {};
+  int value[kSlots] = {};
+  int n = 0;
+  bool find(const void* f, int& v) const {
+    for (int i = 0; i < n; ++i)
+      if (fn[i] == f) {
+        v = value[i];
+        return true;
+      }
+    return false;
+  }
+  void put(const void* f, int v) {
+    if (n < kSlots) {
+      fn[n] = f;
+      value[n] = v;
+      ++n;
+    }
+  }
+};
+
 struct Ctx {
   cudaStream_t stream;
   int num_sms;
   int64_t launches;
+  LaunchCache* cache = nullptr;
 };
+
+// query(&v) once per kernel `fn` and Ctx cache (every time without a cache).
+template <class Query>
+cudaError_t cached_query(Ctx& c, const void* fn, Query query, int& v) {
+  if (c.cache && c.cache->find(fn, v)) return cudaSuccess;
+  const cudaError_t e = query(v);
+  if (e == cudaSuccess && c.cache) c.cache->put(fn, v);
+  return e;
+}
 
 cudaError_t launch_store_bf16(const float* src, int64_t m, int64_t n, int64_t ld_src,
                               uint16_t* dst, int64_t ld_dst, Ctx& c);
@@ -274,9 +333,10 @@ bool gram_tc_supported(int64_t S, int64_t n, int b);
 cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
                            int s, uint32_t flags, int mode, float* G, Ctrl* ctrl,
                            uint32_t timeout_us, Ctx& c);
-// The recurrence with the weight update fused: part[j][:] for each of the s blocks j
-// (s partial rows of ldY floats), added to w (FP32[n]) by the last unit of each
-// 64-column chunk.  counters: the workspace's counters area (timeline_of).
+// The recurrence with the weight update fused: partial rows part[j * R + rq][:] (ldY
+// floats) per block j and row part rq (R = upd_row_parts), added to w (FP32[n]) by the
+// last unit of each 64-column chunk.  counters: the workspace's counters area
+// (timeline_of).
 cudaError_t launch_recur(const float* G, const float* r, const float* yY, float* alpha,
                          float* far, uint32_t* counters, int b, int s, float eta, int loss,
                          uint32_t flags, uint32_t timeout_us, Ctrl* ctrl, const uint16_t* Y,
@@ -285,15 +345,23 @@ cudaError_t launch_recur(const float* G, const float* r, const float* yY, float*
 // stage, on G and Y) in one launch.  next == false: the same iteration (Yg == Y,
 // Gg == G); the Gram's epilogue releases per-32-row counters `slab` (zeroed by the
 // margins step) that the recurrence acquires before it reads rows of G.  next == true:
-// the Gram is the next iteration's and G is complete.  fpart (next == false, b a
-// multiple of 256): the Gram stores only the band blocks (and the diagonal on request)
-// and forms the far sums itself into fpart FP32[S][s * npb] (npb =
+// the Gram is the next iteration's and G is complete.  fpart (b a multiple of 256): the
+// Gram forms the far sums itself into fpart FP32[S][s * npb] (npb =
 // far_partials_per_block; entries (j-B) * npb of each row of block j filled with
-// kAlphaPending by the margins step), which the recurrence adds.
+// kAlphaPending by the margins step), which the recurrence adds, from its tiles of this
+// iteration (rows Y), and stores only band blocks (and the diagonal on request): with
+// next == false this iteration's (Yg == Y, Gg == G), with next == true the next
+// iteration's (rows Yg into Gg; Yg null: none) while the recurrence reads this
+// iteration's complete band from G.
 // cudaErrorNotSupported when the shape does not fit the fused kernel (the caller then
 // launches them separately).
 bool gram_recur_fused_supported(int64_t S, int64_t n, int b);
 bool far_gram_supported(int64_t S, int64_t n, int b);
+// The band blocks (and the diagonal on request) of the far-forming Gram alone, from rows
+// Y into G: the band of a run's first iteration.
+cudaError_t launch_gram_band(const uint16_t* Y, float* G, int64_t S, int64_t n, int64_t ldY,
+                             int b, int s, uint32_t flags, Ctrl* ctrl, uint32_t timeout_us,
+                             Ctx& c);
 cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t S, int64_t n,
                               int64_t ldY, int b, int s, float eta, int loss, uint32_t flags,
                               const float* G, const uint16_t* Y, const float* r,

@@ -71,6 +71,9 @@ struct TcArgs {
   const float* alpha;
   int s, B, nb;      // steps, band width, 256-wide column tiles per block
   int npb, uq, fs;   // column groups per block, tiles per group, fpart row stride
+  bool stored_last;  // the stored units are the next iteration's band (see FarCursor)
+  int n_stored;      // stored units in this launch
+  int far_head;      // stored_last: far units before the stored ones
 };
 
 struct SharedCtl {
@@ -267,26 +270,26 @@ struct TileCursor {
 };
 
 // Work order of the far-forming mode: units of uq column tiles (one 256-row group g
-// against column group c of block t; npb groups of uq tiles per block).  First every
-// stored unit (they wait on nothing), by phase j ascending: the band blocks t = j-1
-// down to j-B, then the diagonal block (on request).  Then the far units by the phase j
-// that needs them, t ascending within a phase (alpha_t is final earliest for small t).
-// Within a block t, column groups outer, the row groups of block j inner.
-struct FarCursor {
-  int seg = 0, j = 0, base = 0, cnt = -1;  // seg 0: stored units, 1: far units
-  __device__ int count(const TcArgs& a) const {
+// against column group c of block t; npb groups of uq tiles per block).  Far units come
+// by the phase j that needs them, t ascending within a phase (alpha_t is final earliest
+// for small t); stored units (the band blocks t = j-1 down to j-B, then the diagonal on
+// request) by phase.  Within a block t: column groups outer, row groups of block j inner.
+// Same iteration: every stored unit first (they wait on nothing and the recurrence
+// starts on them).  Band of the next iteration (stored_last): the first far_head far
+// units (one round over the pairs), then the stored units, which fill the MMAs while
+// the first far tiles wait for alpha, then the other far units.
+struct UnitWalk {  // forward walk over the far units (far) or the stored units
+  int j = 0, base = 0, cnt = -1;
+  __device__ int count(const TcArgs& a, bool far) const {
     const int nband = j < a.B ? j : a.B;
-    return a.nb * a.npb * (seg == 0 ? nband + (a.diag ? 1 : 0) : j - nband);
+    return a.nb * a.npb * (far ? j - nband : nband + (a.diag ? 1 : 0));
   }
-  __device__ void seek(const TcArgs& a, int u, int& g, int& t, int& c, bool& far) {
-    if (cnt < 0) cnt = count(a);
+  __device__ void seek(const TcArgs& a, bool far, int u, int& g, int& t, int& c) {
+    if (cnt < 0) cnt = count(a, far);
     while (u >= base + cnt) {
       base += cnt;
-      if (++j == a.s) {
-        j = 0;
-        ++seg;
-      }
-      cnt = count(a);
+      ++j;
+      cnt = count(a, far);
     }
     const int per_t = a.nb * a.npb;
     const int v = u - base;
@@ -295,8 +298,31 @@ struct FarCursor {
     c = r / a.nb;
     g = j * a.nb + (r - c * a.nb);
     const int nband = j < a.B ? j : a.B;
-    far = seg == 1;
     t = far ? tb : (tb < nband ? j - 1 - tb : j);
+  }
+};
+
+struct FarCursor {
+  UnitWalk far_w, st_w;
+  __device__ void seek(const TcArgs& a, int u, int& g, int& t, int& c, bool& far) {
+    int lf;  // index among the far units, or -1
+    int ls = -1;
+    if (!a.stored_last) {
+      lf = u < a.n_stored ? -1 : u - a.n_stored;
+      if (lf < 0) ls = u;
+    } else if (u < a.far_head) {
+      lf = u;
+    } else if (u < a.far_head + a.n_stored) {
+      lf = -1;
+      ls = u - a.far_head;
+    } else {
+      lf = u - a.n_stored;
+    }
+    far = lf >= 0;
+    if (far)
+      far_w.seek(a, true, lf, g, t, c);
+    else
+      st_w.seek(a, false, ls, g, t, c);
   }
 };
 
@@ -679,9 +705,6 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 // Bounded wait; a timeout also raises the workspace abort word at once, so waiters of
 // the recurrence (same launch or later) stop instead of running into their own bounds.
@@ -828,7 +851,8 @@ __device__ __forceinline__ void far_tile_dot(uint32_t tmem, int acc, int quarter
 template <int kSt, int kRecV, bool kNext, bool kFar>
 __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
     gram_tc2sm_kernel(const __grid_constant__ CUtensorMap tmY,
-                      const __grid_constant__ CUtensorMap tmG, TcArgs a, RecArgs rec) {
+                      const __grid_constant__ CUtensorMap tmG,
+                      const __grid_constant__ CUtensorMap tmYf, TcArgs a, RecArgs rec) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -876,6 +900,8 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
         bool far;
         cur.seek(a, u, rg, ca0, nq, t, pidx, far);
         const int ra = 2 * rg + rank;
+        // far tiles read this iteration's rows; the others the Gram's own rows
+        const CUtensorMap* map = (kFar && far) ? &tmYf : &tmY;
         for (int q = 0; q < nq && !sc->abort; ++q) {
           const int ca = ca0 + q;
           for (int kb = 0; kb < a.nkb; ++kb) {
@@ -884,8 +910,8 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
             uint8_t* sb = sa + kABytes;
             if (leader) mbar_expect_tx(&sc->full[stage], 2 * kStageBytes2);  // both CTAs
             const uint32_t bar = mapa_rank(smem_u32(&sc->full[stage]), 0);
-            tma_load_2d_pair(smem_u32(sa), &tmY, bar, kb * BK, ra * BM);
-            tma_load_2d_pair(smem_u32(sb), &tmY, bar, kb * BK, ca * BN + rank * (BN / 2));
+            tma_load_2d_pair(smem_u32(sa), map, bar, kb * BK, ra * BM);
+            tma_load_2d_pair(smem_u32(sb), map, bar, kb * BK, ca * BN + rank * (BN / 2));
             if (++stage == kSt) {
               stage = 0;
               phase ^= 1u;
@@ -1005,8 +1031,8 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
           }
           __syncwarp();
           if (lane == 0) {
-            red_release_add(a.slab + (int64_t)ra * 4 + quarter, (uint32_t)nq);
-            red_release_add(&a.ctrl->band_done, (uint32_t)nq);
+            red_release_add_u32(a.slab + (int64_t)ra * 4 + quarter, (uint32_t)nq);
+            red_release_add_u32(&a.ctrl->band_done, (uint32_t)nq);
             stamp_last(rec.trace, 0);
           }
         } else if (kRecV && lane == 0) {
@@ -1026,7 +1052,10 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
     // ---------------------------------------------------------- recurrence (warps 6-13)
     // the first C CTAs run chain groups, the others the bulk role
     const int rt = threadIdx.x - kThreads;
-    constexpr int kMode = kNext ? 2 : (kFar ? 3 : 1);
+    // 1: same iteration, G stored; 2: next iteration's Gram, G complete; 3: same
+    // iteration, far sums from the Gram; 4: far sums from the Gram, band complete (the
+    // Gram stores the next iteration's band)
+    constexpr int kMode = kFar ? (kNext ? 4 : 3) : (kNext ? 2 : 1);
     if ((int)blockIdx.x < rec.C)
       chain_role<kRecV == 1 ? 1 : (kRecV == 2 ? 2 : 3), kRecV == 1 ? 8 : (kRecV == 2 ? 4 : 2),
                  kMode>(rec, blockIdx.x, rt);
@@ -1113,6 +1142,8 @@ cudaError_t plan_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
   a.nb = b / 256;
   a.npb = a.uq = 1;
   a.fs = s;
+  a.stored_last = false;
+  a.n_stored = a.far_head = 0;
   // count the needed tiles on the host with the same rule the kernel walks
   int64_t total = 0;
   for (int g = 0; g * kcl < a.TR; ++g) {
@@ -1190,21 +1221,24 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
   const void* fn = mode == 0 ? (const void*)gram_tc2sm_kernel<kStagesPair, 0, false, false>
                              : (const void*)gram_tc_kernel<2>;
   const size_t smem = mode == 0 ? pair_smem_bytes<kStagesPair>() : kSmemBytes;
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster2_config(kThreads, smem, c.stream, attr);
   cfg.gridDim = dim3(2 * (unsigned)(c.num_sms / 2));
   int max_clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg) != cudaSuccess || max_clusters < 1)
-    max_clusters = c.num_sms / 2;
+  e = cached_query(c, fn, [&](int& v) {
+    cudaError_t r = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (r != cudaSuccess) return r;
+    if (cudaOccupancyMaxActiveClusters(&v, fn, &cfg) != cudaSuccess || v < 1) v = c.num_sms / 2;
+    return cudaSuccess;
+  }, max_clusters);
+  if (e != cudaSuccess) return e;
   const int clusters = a.ntiles < max_clusters ? a.ntiles : max_clusters;
   cfg.gridDim = dim3(2 * (unsigned)clusters);
   if (mode == 0) {
     RecArgs none;
     memset(&none, 0, sizeof(none));
-    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel<kStagesPair, 0, false, false>, P.map, P.mapG, a,
-                           none);
+    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel<kStagesPair, 0, false, false>, P.map, P.mapG,
+                           P.map, a, none);
   } else {
     e = cudaLaunchKernelEx(&cfg, gram_tc_kernel<2>, P.map, P.mapG, a);
   }
@@ -1222,6 +1256,68 @@ bool far_gram_supported(int64_t S, int64_t n, int b) {
   return gram_recur_fused_supported(S, n, b) && b % 256 == 0;
 }
 
+namespace {
+
+// Units of the far-forming order: far (t < j-B) and stored (band, and the diagonal on
+// request), nb * npb of each per block pair (j, t).
+void far_unit_counts(const TcArgs& a, int64_t& far_units, int64_t& stored_units) {
+  int64_t nfar = 0, nst = 0;
+  for (int j = 0; j < a.s; ++j) {
+    const int nband = j < a.B ? j : a.B;
+    nfar += j - nband;
+    nst += nband + (a.diag ? 1 : 0);
+  }
+  far_units = (int64_t)a.nb * a.npb * nfar;
+  stored_units = (int64_t)a.nb * a.npb * nst;
+}
+
+void set_far_fields(TcArgs& a, int b, int s, float* fpart, const float* alpha) {
+  a.fpart = fpart;
+  a.alpha = alpha;
+  a.npb = far_partials_per_block(b, s);
+  a.uq = a.nb / a.npb;
+  a.fs = s * a.npb;
+}
+
+}  // namespace
+
+cudaError_t launch_gram_band(const uint16_t* Y, float* G, int64_t S, int64_t n, int64_t ldY,
+                             int b, int s, uint32_t flags, Ctrl* ctrl, uint32_t timeout_us,
+                             Ctx& c) {
+  if (!far_gram_supported(S, n, b)) return cudaErrorNotSupported;
+  TcPlan P;
+  cudaError_t e = plan_tc(Y, S, n, ldY, b, s, flags, 2, G, ctrl, timeout_us, P);
+  if (e != cudaSuccess) return e;
+  set_far_fields(P.a, b, s, nullptr, nullptr);
+  int64_t nfar, nst;
+  far_unit_counts(P.a, nfar, nst);
+  P.a.n_stored = (int)nst;
+  P.a.ntiles = (int)nst;  // the stored units only (they come first)
+  if (P.a.ntiles == 0) return cudaSuccess;
+  const auto fn = gram_tc2sm_kernel<kStagesFused, 0, false, true>;
+  const size_t smem = pair_smem_bytes<kStagesFused, true>();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster2_config(kThreads, smem, c.stream, attr);
+  cfg.gridDim = dim3(2 * (unsigned)(c.num_sms / 2));
+  int max_clusters = 0;
+  e = cached_query(c, (const void*)fn, [&](int& v) {
+    cudaError_t r = cudaFuncSetAttribute((const void*)fn,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (r != cudaSuccess) return r;
+    if (cudaOccupancyMaxActiveClusters(&v, (const void*)fn, &cfg) != cudaSuccess || v < 1)
+      v = c.num_sms / 2;
+    return cudaSuccess;
+  }, max_clusters);
+  if (e != cudaSuccess) return e;
+  const int clusters = P.a.ntiles < max_clusters ? P.a.ntiles : max_clusters;
+  cfg.gridDim = dim3(2 * (unsigned)clusters);
+  RecArgs none;
+  memset(&none, 0, sizeof(none));
+  e = cudaLaunchKernelEx(&cfg, fn, P.map, P.mapG, P.map, P.a, none);
+  ++c.launches;
+  return e;
+}
+
 cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t S, int64_t n,
                               int64_t ldY, int b, int s, float eta, int loss, uint32_t flags,
                               const float* G, const uint16_t* Y, const float* r,
@@ -1230,27 +1326,41 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
                               uint32_t timeout_us, Ctx& c) {
   if (!gram_recur_fused_supported(S, n, b)) return cudaErrorNotSupported;
   const bool far_gram = fpart != nullptr;
-  if (far_gram && (next || !far_gram_supported(S, n, b))) return cudaErrorNotSupported;
+  if (far_gram && !far_gram_supported(S, n, b)) return cudaErrorNotSupported;
+  if (!far_gram && !Yg) return cudaErrorInvalidValue;
   const bool diag = (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
   TcPlan P;
-  cudaError_t e = plan_tc(Yg, S, n, ldY, b, s, flags, 2, Gg, ctrl, timeout_us, P);
+  cudaError_t e = plan_tc(Yg ? Yg : Y, S, n, ldY, b, s, flags, 2, Gg, ctrl, timeout_us, P);
   if (e != cudaSuccess) return e;
+  // far tiles read this iteration's rows (the Gram's own rows unless next)
+  CUtensorMap mapYf = P.map;
+  if (far_gram && next) {
+    TcPlan Pf;
+    e = plan_tc(Y, S, n, ldY, b, s, flags, 2, Gg, ctrl, timeout_us, Pf);
+    if (e != cudaSuccess) return e;
+    mapYf = Pf.map;
+  }
   P.a.slab = next ? nullptr : slab;
   RecArgs rec = make_rec_args(G, r, yY, alpha, far, slab, b, s, eta, loss, flags, timeout_us,
                               ctrl, Y, ldY, n, part, w);
   rec.slab = next ? nullptr : slab;
-  if (far_gram) {  // work items: units of uq tiles, nb * npb * (j + diag) for phase j
-    P.a.fpart = fpart;
-    P.a.alpha = alpha;
-    P.a.npb = far_partials_per_block(b, s);
-    P.a.uq = P.a.nb / P.a.npb;
-    P.a.fs = s * P.a.npb;
-    P.a.ntiles = P.a.nb * P.a.npb * (s * (s - 1) / 2 + (diag ? s : 0));
+  if (far_gram) {  // work items: units of uq tiles
+    set_far_fields(P.a, b, s, fpart, alpha);
+    int64_t nfar, nst;
+    far_unit_counts(P.a, nfar, nst);
+    // next: the next iteration's band (none without its rows) after one round of far
+    // units (far_head is set once the grid is known)
+    P.a.stored_last = next;
+    P.a.n_stored = (int)((!next || Yg) ? nst : 0);
+    P.a.ntiles = (int)(nfar + P.a.n_stored);
+    P.a.far_head = 0;
     rec.fpart = fpart;
     rec.fs = P.a.fs;
     rec.npb = P.a.npb;
     rec.far_gram = true;
     rec.bulk_units = 0;  // no far units: the Gram forms the far sums
+    rec.upd_R = upd_row_parts(b, ldY);  // the bulk groups only update: row parts
+    rec.upd_units = s * (int)((ldY / 8 + 7) / 8) * rec.upd_R;
   }
   // what Ctrl::band_done reaches once every stored tile is stored (8 warps per tile)
   if (!next) {
@@ -1260,8 +1370,8 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
     rec.band_total = (uint32_t)(8 * total);
   }
   const int v = chain_variant(rec);
-  using Fn = void (*)(CUtensorMap, CUtensorMap, TcArgs, RecArgs);
-  const Fn table[3][3] = {
+  using Fn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, TcArgs, RecArgs);
+  const Fn table[4][3] = {
       {gram_tc2sm_kernel<kStagesFused, 1, false, false>,
        gram_tc2sm_kernel<kStagesFused, 2, false, false>,
        gram_tc2sm_kernel<kStagesFused, 3, false, false>},
@@ -1270,17 +1380,23 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
        gram_tc2sm_kernel<kStagesFused, 3, true, false>},
       {gram_tc2sm_kernel<kStagesFused, 1, false, true>,
        gram_tc2sm_kernel<kStagesFused, 2, false, true>,
-       gram_tc2sm_kernel<kStagesFused, 3, false, true>}};
-  const Fn fn = table[far_gram ? 2 : (next ? 1 : 0)][v - 1];
+       gram_tc2sm_kernel<kStagesFused, 3, false, true>},
+      {gram_tc2sm_kernel<kStagesFused, 1, true, true>,
+       gram_tc2sm_kernel<kStagesFused, 2, true, true>,
+       gram_tc2sm_kernel<kStagesFused, 3, true, true>}};
+  const Fn fn = table[(far_gram ? 2 : 0) + (next ? 1 : 0)][v - 1];
   const size_t smem = far_gram ? pair_smem_bytes<kStagesFused, true>()
                                : pair_smem_bytes<kStagesFused>();
-  e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster2_config(kFusedThreads, smem, c.stream, attr);
   cfg.gridDim = dim3(2 * (unsigned)(c.num_sms / 2));
   int max_clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&max_clusters, (const void*)fn, &cfg);
+  e = cached_query(c, (const void*)fn, [&](int& v) {
+    cudaError_t r = cudaFuncSetAttribute((const void*)fn,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (r != cudaSuccess) return r;
+    return cudaOccupancyMaxActiveClusters(&v, (const void*)fn, &cfg);
+  }, max_clusters);
   if (e != cudaSuccess) return e;
   // every CTA must be resident at once (the recurrence waits across CTAs); one chain
   // group per 8-row group while at least one bulk group remains
@@ -1290,8 +1406,12 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
   if (rec.C > grid / 2) rec.C = grid / 2;
   if (rec.C < 1) return cudaErrorNotSupported;
   rec.upd_groups = update_groups(rec, grid - rec.C);
+  if (far_gram && next) {
+    const int nfar = P.a.ntiles - P.a.n_stored;
+    P.a.far_head = nfar < grid / 2 ? nfar : grid / 2;
+  }
   cfg.gridDim = dim3((unsigned)grid);
-  e = cudaLaunchKernelEx(&cfg, fn, P.map, P.mapG, P.a, rec);
+  e = cudaLaunchKernelEx(&cfg, fn, P.map, P.mapG, mapYf, P.a, rec);
   ++c.launches;
   return e;
 }

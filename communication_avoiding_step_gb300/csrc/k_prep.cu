@@ -80,6 +80,7 @@ struct RowArgs {
   float* far;
   float* fpart;  // far partials [S][fs] of the far-forming Gram (null: not used)
   int fb, fs, fB, fnp;  // b, row stride s * npb, band width, partials per block
+  int steps;            // s
   Ctrl* ctrl;
   uint32_t* slab;
   int G;
@@ -97,8 +98,11 @@ __device__ void reset_recurrence(const RowArgs& a) {
   }
   const int64_t nslab = (a.S + 255) / 256 * 8;  // the Gram's 32-row counters
   for (int64_t j = threadIdx.x; j < nslab; j += blockDim.x) a.slab[j] = 0;
+  const int64_t nchunk = (a.ldY + 63) / 64;
   uint32_t* chunks = upd_chunk_counters(a.slab);  // the update's column counters
-  for (int64_t j = threadIdx.x; j < (a.ldY + 63) / 64; j += blockDim.x) chunks[j] = 0;
+  for (int64_t j = threadIdx.x; j < nchunk; j += blockDim.x) chunks[j] = 0;
+  uint32_t* blocks = upd_block_counters(a.slab);  // and its (block, chunk) counters
+  for (int64_t j = threadIdx.x; j < a.steps * nchunk; j += blockDim.x) blocks[j] = 0;
   uint64_t* summary = timeline_of(a.slab) + (int64_t)kMaxS * 4;  // profiling summary row
   if (threadIdx.x < 4) summary[threadIdx.x] = 0;
 }
@@ -288,6 +292,7 @@ RowArgs row_args(const casgd_data_t& d, const casgd_params_t& p, const float* w,
   a.far = far;
   a.fpart = fpart;
   a.fb = p.b;
+  a.steps = p.s;
   a.fnp = far_partials_per_block(p.b, p.s);
   a.fs = p.s * a.fnp;
   a.fB = band_width(p.b);

@@ -35,6 +35,7 @@ RecArgs make_rec_args(const float* G, const float* r, const float* yY, float* al
   a.far = far;
   a.trace = (flags & CASGD_FLAG_TRACE_CHAIN) ? timeline_of(counters) : nullptr;
   a.upd_chunks = upd_chunk_counters(counters);
+  a.upd_blocks = upd_block_counters(counters);
   a.w = w;
   a.n = n;
   a.ctrl = ctrl;
@@ -53,7 +54,9 @@ RecArgs make_rec_args(const float* G, const float* r, const float* yY, float* al
   a.Y = Y;
   a.part = part;
   a.ldY = ldY;
-  // update units: s blocks x ceil(ldY / 64) column chunks
+  // update units: s blocks x ceil(ldY / 64) column chunks (x R row parts where the far
+  // sums come from the Gram: launch_gram_recur)
+  a.upd_R = 1;
   a.upd_units = s * (int)((ldY / 8 + 7) / 8);
   a.slab = nullptr;
   a.fpart = nullptr;
@@ -78,7 +81,9 @@ cudaError_t launch_recur(const float* G, const float* r, const float* yY, float*
                    : v == 2 ? (const void*)recur_kernel<2, 4>
                             : (const void*)recur_kernel<1, 8>;
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kRecThreads, 0);
+  cudaError_t e = cached_query(c, fn, [&](int& v) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, fn, kRecThreads, 0);
+  }, per_sm);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorLaunchOutOfResources;
   const int64_t cap = (int64_t)per_sm * c.num_sms;

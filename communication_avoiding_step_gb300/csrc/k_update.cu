@@ -281,13 +281,15 @@ cudaError_t launch_loss(const casgd_data_t& d, int loss, const float* w, double*
   const int64_t rows_per_cta = 8 * (32 / G);
   int64_t blocks = (d.m + rows_per_cta - 1) / rows_per_cta;
   const size_t smem = (size_t)((d.n + 7) / 8 * 8) * sizeof(float);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(loss_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-  }
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, loss_kernel, 256, smem);
+  cudaError_t e = cached_query(c, (const void*)loss_kernel, [&](int& v) {
+    if (smem > 48 * 1024) {
+      cudaError_t r = cudaFuncSetAttribute(loss_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (r != cudaSuccess) return r;
+    }
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, loss_kernel, 256, smem);
+  }, per_sm);
   if (e != cudaSuccess) return e;
   int cap = (per_sm > 0 ? per_sm : 1) * c.num_sms;  // one resident wave
   if (cap > loss_ctas(c.num_sms)) cap = loss_ctas(c.num_sms);

@@ -14,7 +14,8 @@
 // complete; 1 shared CTA, rows of G still being stored by the same launch; 2 shared
 // CTA, G complete (the launch computes the next iteration's Gram); 3 shared CTA, the
 // Gram of the same launch stores only the band blocks and forms the far sums itself
-// (partial sums per row and block t, see below):
+// (partial sums per row and block t, see below); 4 as 3 with the band already
+// complete (the launch's Gram stores the next iteration's band):
 //  * chain groups (the first C): one warp per row, 8-row groups.  Phase j of a row
 //    needs only the band  sum_{t=j-B}^{j-1} G_{j,t} alpha_t  (B = 1 to 3 blocks) on top
 //    of far_j (below).  The warp has its band rows of G in registers before it waits
@@ -64,8 +65,11 @@ struct RecArgs {
   float* part;
   int64_t ldY;
   int upd_units;
-  // the update's last stage: the last unit of a column chunk adds the s partial rows
+  int upd_R;  // row parts per block (upd_row_parts)
+  // the update's last stage: the last row part of (block, column chunk) sums the parts
+  // and adds them to w in block order (upd_chunks: the next block per chunk)
   uint32_t* upd_chunks;
+  uint32_t* upd_blocks;
   float* w;
   int64_t n;
   // Gram in the same launch: per-32-row completion counters of the paired-SM Gram
@@ -245,6 +249,7 @@ __device__ bool wait_rows_of_G(const RecArgs& a, int64_t row, uint32_t where) {
 template <int kB, int kKB, int kMode>
 __device__ void chain_role(const RecArgs& a, int c, int rt) {
   constexpr bool kInFlight = kMode == 1 || kMode == 3;  // G stored by this launch
+  constexpr bool kFarParts = kMode >= 3;                // far sums from the Gram's partials
   // the next item's row values are loaded with its band, except in the widest register
   // layout (eight float4 slots per block), which has no registers to spare for them
   constexpr bool kRowAhead = kKB < 8;
@@ -285,7 +290,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
       yv = a.yY[p];
     }
     if (j < kB + 1) return;
-    if (kMode == 3) {
+    if (kFarParts) {
       const int nfar = (j - kB) * a.npb;
       const float* fsrc = a.fpart + p * a.fs;
       if (lane < nfar) f0 = ld_volatile_f32(fsrc + lane);
@@ -381,11 +386,11 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
     }
     // far_j as loaded with the row values (lane 0; mode 3: partials t = lane and
     // t = lane + 32), reloaded below while pending
-    float farv = kMode == 3 ? 0.0f : fv0;
+    float farv = kFarParts ? 0.0f : fv0;
     float fp0 = fv0, fp1 = fv1;
     const int nfar = (j - kB) * a.npb;  // partials of the row (has_far), at most 64
-    const float* fsrc = kMode == 3 ? a.fpart + p * a.fs : nullptr;
-    if (kMode == 3) {
+    const float* fsrc = kFarParts ? a.fpart + p * a.fs : nullptr;
+    if (kFarParts) {
       if (has_far && lane < nfar) pend |= pending1(fp0);
       if (has_far && lane + 32 < nfar) pend |= pending1(fp1);
     } else if (has_far && lane == 0) {
@@ -406,7 +411,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
             }
           }
         }
-        if (kMode == 3) {
+        if (kFarParts) {
           if (has_far && lane < nfar && pending1(fp0)) {
             fp0 = ld_volatile_f32(fsrc + lane);
             pend |= pending1(fp0);
@@ -477,7 +482,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
     if (!__all_sync(0xffffffffu, ok)) return;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (kMode == 3) {  // far_j: the row's partials, lane sums then a fixed tree
+    if (kFarParts) {  // far_j: the row's partials, lane sums then a fixed tree
       float fs = fp0 + fp1;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) fs += __shfl_xor_sync(0xffffffffu, fs, off);
@@ -506,26 +511,37 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
 }
 
 // --------------------------------------------------------------- update units
-// Step a8, fused: unit (j, cc) sums alpha_i * Y_i over the b rows of block j for the 64
-// columns cc*64 .. cc*64+63 into part[j][...] (one partial row per block); the last
-// unit of a column chunk adds the chunk's s partial rows to w.  Threads: 32 row-lanes x 8 column
-// vectors.  The unit issues its first rows of Y, then waits as a whole for block j's
-// alpha: thread 0 polls one value of phase j+1 (a final value there implies all of
-// alpha_j is final), or warp 0 polls all of alpha_j for the last block, so a waiting
-// unit costs the memory system one load per back-off instead of one per row.  Units of
-// block j become workable as soon as phase j is done, so only the last block's units
-// (spread over many groups) run after the chain ends.  Fixed order: rows ascending per
-// row-lane, then row-lanes ascending in shared memory.  Y was written by an earlier
-// launch.
+// Step a8, fused: unit (j, cc, rq) sums alpha_i * Y_i over row part rq (of R) of block j
+// for the 64 columns cc*64 .. cc*64+63 into partial row j*R + rq.  Two ways to finish:
+//  * modes 0-2 (R = 1; the bulk groups also stream G, so no unit may wait on another):
+//    the last of the s units of a column chunk adds the chunk's s partial rows to w,
+//    rows q, q+8, q+16, ... for each q < 8, then the eight sums in q order;
+//  * modes 3-4 (far sums from the Gram; the bulk groups only update): the last of the R
+//    units of (j, cc) sums the R partial rows (four interleaved sums) and adds the
+//    block's sum to w once block j-1's has been added (a per-chunk turn counter), so w
+//    receives the block sums in block order and only the last block's small addition
+//    follows the chain.
+// Threads: 32 row-lanes x 8 column vectors.  The unit issues its first rows of Y, then
+// waits as a whole for its rows of alpha_j: lane 0 of warp 0 polls one value with a
+// back-off (of phase j+1, or the part's last row for the last block), then warp 0 loads
+// the part's values until none is pending.  Fixed
+// order: rows ascending per row-lane, then row-lanes ascending in shared memory.  Y was
+// written by an earlier launch.
 template <int kMode>
 __device__ void update_unit(const RecArgs& a, int u, int rt) {
   __shared__ float red[32][64];
-  __shared__ int s_ready;
+  // one flag per stage, each written by thread 0 and read by the group after a barrier;
+  // the next write of a flag comes after at least two more barriers of the group
+  __shared__ int s_ready, s_last, s_turn;
   const int nchunk = (int)((a.ldY / 8 + 7) / 8);
-  const int j = u / nchunk, cc = u - j * nchunk;
+  const int per_j = nchunk * a.upd_R;
+  const int j = u / per_j, cc = (u - j * per_j) / a.upd_R;
+  const int rq = u - j * per_j - cc * a.upd_R;
+  const int r0 = (int)((int64_t)rq * a.b / a.upd_R), r1 = (int)((int64_t)(rq + 1) * a.b / a.upd_R);
   const int tv = rt & 7, tr = rt >> 3;  // vector-lane, row-lane
   const int64_t vec = (int64_t)cc * 8 + tv;
   const bool vin = vec < a.ldY / 8;
+  const float* al_j = a.alpha + (int64_t)j * a.b;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   uint4 q[kUpdRows];
   auto load_rows = [&](int i0) {
@@ -533,29 +549,47 @@ __device__ void update_unit(const RecArgs& a, int u, int rt) {
     for (int k = 0; k < kUpdRows; ++k) {
       const int i = i0 + 32 * k;
       const int64_t row = (int64_t)j * a.b + i;
-      q[k] = (i < a.b && vin)
+      q[k] = (i < r1 && vin)
                  ? __ldg(reinterpret_cast<const uint4*>(a.Y + row * a.ldY + vec * 8))
                  : make_uint4(0, 0, 0, 0);
     }
   };
-  load_rows(tr);
-  if (rt < 32) {  // warp 0 waits for block j's alpha
+  load_rows(r0 + tr);
+  if (rt < 32) {  // warp 0 waits for the part's alpha
     bool ok = true;
     const uint64_t t_start = globaltimer_ns();
-    if (j + 1 < a.s) {
-      if (rt == 0) {
-        const float* pv = a.alpha + (int64_t)(j + 1) * a.b + (int)((blockIdx.x * 37u) % (unsigned)a.b);
-        while (pending1(ld_volatile_f32(pv)) && ok) {
-          __nanosleep(200);
-          ok = keep_waiting(a, t_start, where_code(4, j));
-        }
+    if (rt == 0) {
+      // one value polled with a back-off: of phase j+1 (final there implies alpha_j
+      // complete; the update of block j is off the critical path), or for the last
+      // block its own last row
+      const float* pv = j + 1 < a.s
+                            ? a.alpha + (int64_t)(j + 1) * a.b + (int)((blockIdx.x * 37u) % (unsigned)a.b)
+                            : al_j + r1 - 1;
+      while (pending1(ld_volatile_f32(pv)) && ok) {
+        __nanosleep(200);
+        ok = keep_waiting(a, t_start, where_code(4, j));
       }
-    } else {
-      for (int i = rt; i < a.b && ok; i += 32) {
-        const float* pv = a.alpha + (int64_t)j * a.b + i;
-        while (pending1(ld_volatile_f32(pv)) && ok) {
-          __nanosleep(200);
-          ok = keep_waiting(a, t_start, where_code(4, j));
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    // the part's own values, four per lane in flight (modes 0-2 rely on the probe of
+    // phase j+1 for every block but the last, as the far units do)
+    if (kMode >= 3 || j + 1 == a.s) {
+      for (int i = r0 + rt; i < r1 && ok; i += 32 * 4) {
+        float v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          v[k] = i + 32 * k < r1 ? ld_volatile_f32(al_j + i + 32 * k) : 0.0f;
+        bool pend = pending1(v[0]) || pending1(v[1]) || pending1(v[2]) || pending1(v[3]);
+        while (pend && ok) {
+          __nanosleep(64);
+          pend = false;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (pending1(v[k])) {
+              v[k] = ld_volatile_f32(al_j + i + 32 * k);
+              pend |= pending1(v[k]);
+            }
+          if (pend) ok = keep_waiting(a, t_start, where_code(4, j));
         }
       }
     }
@@ -565,12 +599,12 @@ __device__ void update_unit(const RecArgs& a, int u, int rt) {
   group_sync<kMode != 0>();
   const bool ready = s_ready != 0;  // rewritten only after the group syncs below
   if (ready) {
-    for (int i0 = tr; i0 < a.b; i0 += 32 * kUpdRows) {
-      if (i0 != tr) load_rows(i0);
+    for (int i0 = r0 + tr; i0 < r1; i0 += 32 * kUpdRows) {
+      if (i0 != r0 + tr) load_rows(i0);
 #pragma unroll
       for (int k = 0; k < kUpdRows; ++k) {
         const int i = i0 + 32 * k;
-        const float al = i < a.b ? __ldcg(a.alpha + (int64_t)j * a.b + i) : 0.0f;
+        const float al = i < r1 ? __ldcg(al_j + i) : 0.0f;
         const uint32_t pw[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -583,36 +617,70 @@ __device__ void update_unit(const RecArgs& a, int u, int rt) {
 #pragma unroll
   for (int e = 0; e < 8; ++e) red[tr][tv * 8 + e] = acc[e];
   group_sync<kMode != 0>();
+  const int64_t c = (int64_t)cc * 64 + (rt & 63);
   if (rt < 64 && ready) {
-    const int col = rt;
     float sum = 0.0f;
-    for (int r = 0; r < 32; ++r) sum += red[r][col];
-    const int64_t c = (int64_t)cc * 64 + col;
-    if (c < a.ldY) a.part[(int64_t)j * a.ldY + c] = sum;
-    if (col == 0) stamp_last(a.trace, 2);
+    for (int r = 0; r < 32; ++r) sum += red[r][rt];
+    if (c < a.ldY) a.part[((int64_t)j * a.upd_R + rq) * a.ldY + c] = sum;
+    if (rt == 0) stamp_last(a.trace, 2);
     __threadfence();  // the partial row is visible before this unit is counted
   }
-  // The last of the s units of column chunk cc adds the s partial rows to w, summing
-  // rows q, q+8, q+16, ... for each q < 8 and then the eight sums in q order.
-  group_sync<kMode != 0>();
-  if (rt == 0)
-    s_ready = ready && atomicAdd(a.upd_chunks + cc, 1u) == (unsigned)(a.s - 1) ? 2 : 0;
-  group_sync<kMode != 0>();
-  if (s_ready == 2 && rt < 64) {
-    __threadfence();
-    const int64_t c = (int64_t)cc * 64 + rt;
-    if (c < a.n) {
+  if (kMode <= 2) {
+    // the last of the s units of column chunk cc adds the chunk's s partial rows to w
+    group_sync<kMode != 0>();
+    if (rt == 0)
+      s_last = ready && atomicAdd(a.upd_chunks + cc, 1u) == (unsigned)(a.s - 1) ? 1 : 0;
+    group_sync<kMode != 0>();
+    if (s_last && rt < 64 && c < a.n) {
+      __threadfence();
       float sum = 0.0f;
-      for (int q = 0; q < 8; ++q) {
+      for (int q8 = 0; q8 < 8; ++q8) {
         float acc_q = 0.0f;
-        for (int pr = q; pr < a.s; pr += 8) acc_q += __ldcg(a.part + (int64_t)pr * a.ldY + c);
+        for (int pr = q8; pr < a.s; pr += 8) acc_q += __ldcg(a.part + (int64_t)pr * a.ldY + c);
         sum += acc_q;
       }
       const float v = a.w[c] + sum;
       a.w[c] = v;
       if (!isfinite(v)) atomicOr(&a.ctrl->status, ST_NONFINITE);
     }
+    return;
   }
+  // the last row part of (j, cc): the block's sum, then its turn to add to w
+  group_sync<kMode != 0>();
+  if (rt == 0)
+    s_last = ready && atomicAdd(a.upd_blocks + (int64_t)j * nchunk + cc, 1u) ==
+                          (unsigned)(a.upd_R - 1)
+                 ? 1
+                 : 0;
+  group_sync<kMode != 0>();
+  if (!s_last) return;  // group-uniform
+  float bsum = 0.0f;
+  if (rt < 64 && c < a.n) {
+    __threadfence();
+    float p4[4] = {0.f, 0.f, 0.f, 0.f};  // parts rq, rq+4, ... in four sums, then combined
+    for (int r = 0; r < a.upd_R; ++r)
+      p4[r & 3] += __ldcg(a.part + ((int64_t)j * a.upd_R + r) * a.ldY + c);
+    bsum = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+  }
+  if (rt == 0) {  // wait for block j-1's addition to this chunk
+    bool ok = true;
+    const uint64_t t_start = globaltimer_ns();
+    while (ld_acquire_u32(a.upd_chunks + cc) != (uint32_t)j && ok) {
+      __nanosleep(64);
+      ok = keep_waiting(a, t_start, where_code(4, j));
+    }
+    s_turn = ok ? 1 : 0;
+  }
+  group_sync<kMode != 0>();
+  if (!s_turn) return;  // group-uniform
+  if (rt < 64 && c < a.n) {
+    const float v = __ldcg(a.w + c) + bsum;
+    a.w[c] = v;
+    if (j == a.s - 1 && !isfinite(v)) atomicOr(&a.ctrl->status, ST_NONFINITE);
+    __threadfence();
+  }
+  group_sync<kMode != 0>();
+  if (rt == 0) red_release_add_u32(a.upd_chunks + cc, 1u);  // block j+1's turn
 }
 
 // ------------------------------------------------------------------- bulk role

@@ -190,7 +190,9 @@ typedef struct {
                             launch, 4 = as 3 with the Gram one outer iteration
                             ahead of the recurrence (casgd_train, iters >= 2),
                             5 = as 3 with the far sums formed by the Gram
-                            (CASGD_FLAG_FAR_FROM_GRAM)                          */
+                            (CASGD_FLAG_FAR_FROM_GRAM), 6 = as 5 with the
+                            next iteration's band stored by the same launch
+                            (casgd_train, iters >= 2)                           */
 } casgd_profile_t;
 #define CASGD_STAGE_EVENTS 5
 

@@ -118,7 +118,7 @@ def test_stall_in_far_forming_launch_times_out(gpu_lib):
     w.zero_()
     ok = casgd.Params(r.b, r.s, r.eta, r.loss, flags=far)
     _, _, kind = casgd.train(data, ok, w, 2, ws)
-    assert kind == 5
+    assert kind == 6
     assert torch.isfinite(w).all() and torch.count_nonzero(w).item() > 0
 
 
