@@ -1404,6 +1404,14 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
   const int grid = 2 * max_clusters;
   rec.C = rec.Uc < grid - 1 ? rec.Uc : grid - 1;
   if (rec.C > grid / 2) rec.C = grid / 2;
+  // Far sums from the Gram: the bulk groups only update, so where a chain warp would
+  // take more than two rows per phase (b > 8 * grid), chain CTAs may take all but 24 of
+  // the CTAs, two row groups each (measured: b = 2048, 180 -> 128-150 us per launch).
+  constexpr int kUpdateCtas = 24;
+  if (far_gram && rec.Uc > grid && grid > 2 * kUpdateCtas) {
+    const int want = (rec.Uc + 1) / 2;
+    rec.C = want < grid - kUpdateCtas ? want : grid - kUpdateCtas;
+  }
   if (rec.C < 1) return cudaErrorNotSupported;
   rec.upd_groups = update_groups(rec, grid - rec.C);
   if (far_gram && next) {
