@@ -36,6 +36,7 @@ struct Resolved {
   int32_t* idx2;
   float* yY2;
   float* fpart;  // far partial sums of the far-forming Gram (null: not laid out)
+  float* w_acc;  // its update's running sum (null: not laid out)
   float* upd;
   double* loss_part;
   double* loss_slots;
@@ -86,6 +87,7 @@ Resolved resolve(void* ws, const Layout& L) {
   R.idx2 = L.off_idx2 ? reinterpret_cast<int32_t*>(base + L.off_idx2) : nullptr;
   R.yY2 = L.off_yY2 ? reinterpret_cast<float*>(base + L.off_yY2) : nullptr;
   R.fpart = L.off_fpart ? reinterpret_cast<float*>(base + L.off_fpart) : nullptr;
+  R.w_acc = L.off_wacc ? reinterpret_cast<float*>(base + L.off_wacc) : nullptr;
   R.upd = reinterpret_cast<float*>(base + L.off_upd);
   R.loss_part = reinterpret_cast<double*>(base + L.off_loss);
   R.loss_slots = R.loss_part + kLossCtas;
@@ -189,8 +191,12 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   if (prof) prof->gram_kind = choice;
 
   if ((rc = record(prof, it, 0, st)) != CASGD_OK) return rc;
-  CK(launch_gather(*d, *p, w, k, idx_in, R.idx, R.Y, L.ldY, R.r, R.yY, R.alpha, R.far,
-                   gp.far ? R.fpart : nullptr, R.ctrl, R.slab, GATHER_AND_MARGINS, c));
+  if (gp.far)  // the rows and the reset; the margins are formed in the shared launch
+    CK(launch_gather_reset(*d, *p, k, idx_in, R.idx, R.Y, R.yY, true, L.ldY, R.r, R.alpha,
+                           R.far, R.fpart, R.ctrl, R.slab, c));
+  else
+    CK(launch_gather(*d, *p, w, k, idx_in, R.idx, R.Y, L.ldY, R.r, R.yY, R.alpha, R.far,
+                     nullptr, R.ctrl, R.slab, GATHER_AND_MARGINS, c));
   if ((rc = record(prof, it, 1, st)) != CASGD_OK) return rc;
   // The update's first stage rides in the recurrence (one partial row per block,
   // s <= 64 <= upd_ctas rows of the partial buffer); the reduce adds the s rows to w.
@@ -201,7 +207,7 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
     // on one GPU it is the identity.)
     CK(launch_gram_recur(R.Y, G, false, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss, p->flags,
                          G, R.Y, R.r, R.yY, R.alpha, R.far, R.slab, gp.far ? R.fpart : nullptr,
-                         R.upd, w, R.ctrl, p->timeout_us, c));
+                         R.upd, w, gp.far ? R.w_acc : nullptr, R.ctrl, p->timeout_us, c));
     if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
   } else {
     if (choice == 1)
@@ -271,8 +277,11 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
         CK(launch_gram_tc(Yb[cur], L.S, d->n, L.ldY, p->b, p->s, p->flags, 0, Gb[cur], R.ctrl,
                           p->timeout_us, c));
     }
-    if (it + 1 < iters)  // next iteration's rows (into the buffers the last launch
-                         // freed) and this iteration's margins, in one launch
+    if (far)  // next iteration's rows and this iteration's reset (margins in-launch)
+      CK(launch_gather_reset(*d, *p, k + 1, nullptr, Ib[nxt], Yb[nxt], yb[nxt], it + 1 < iters,
+                             L.ldY, R.r, R.alpha, R.far, fpart, R.ctrl, R.slab, c));
+    else if (it + 1 < iters)  // next iteration's rows (into the buffers the last launch
+                              // freed) and this iteration's margins, in one launch
       CK(launch_gather_next_margins(*d, *p, w, k + 1, Ib[nxt], Yb[nxt], yb[nxt], Yb[cur],
                                     L.ldY, R.r, R.alpha, R.far, fpart, R.ctrl, R.slab, c));
     else
@@ -284,12 +293,12 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
     if (far)  // this iteration's far sums; the next iteration's band (if any) into Gb[nxt]
       CK(launch_gram_recur(it + 1 < iters ? Yb[nxt] : nullptr, Gb[nxt], true, L.S, d->n, L.ldY,
                            p->b, p->s, p->eta, p->loss, p->flags, Gb[cur], Yb[cur], R.r,
-                           yb[cur], R.alpha, R.far, R.slab, fpart, R.upd, w, R.ctrl,
+                           yb[cur], R.alpha, R.far, R.slab, fpart, R.upd, w, R.w_acc, R.ctrl,
                            p->timeout_us, c));
     else if (it + 1 < iters)
       CK(launch_gram_recur(Yb[nxt], Gb[nxt], true, L.S, d->n, L.ldY, p->b, p->s, p->eta,
                            p->loss, p->flags, Gb[cur], Yb[cur], R.r, yb[cur], R.alpha, R.far,
-                           R.slab, nullptr, R.upd, w, R.ctrl, p->timeout_us, c));
+                           R.slab, nullptr, R.upd, w, nullptr, R.ctrl, p->timeout_us, c));
     else
       CK(launch_recur(Gb[cur], R.r, yb[cur], R.alpha, R.far, R.slab, p->b, p->s, p->eta,
                       p->loss, p->flags, p->timeout_us, R.ctrl, Yb[cur], L.ldY, d->n, R.upd, w,
@@ -377,9 +386,12 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms)
     L.off_G2 = off;  // the far-forming Gram stores the next iteration's band into it
     off += align_up((size_t)L.gram_elems * sizeof(float));
   }
+  L.off_wacc = 0;
   if (gp.far) {
     L.off_fpart = off;
     off += align_up((size_t)L.S * s * far_partials_per_block(b, s) * sizeof(float));
+    L.off_wacc = off;
+    off += align_up((size_t)n * sizeof(float));
   }
   L.total = off;
   return L;

@@ -75,6 +75,7 @@ struct Layout {
   size_t off_idx, off_r, off_yY, off_alpha, off_far, off_Y, off_G, off_upd, off_loss;
   size_t off_Y2, off_G2, off_idx2, off_yY2;  // 0: no second buffers
   size_t off_fpart;  // far partial sums FP32[S][s * npb] of the far-forming Gram (0: none)
+  size_t off_wacc;   // its update's running sum FP32[n] (0: none)
   size_t total;
 };
 
@@ -319,6 +320,14 @@ cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const 
                           uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
                           int64_t ldY, float* r, float* yY, float* alpha, float* far,
                           float* fpart, Ctrl* ctrl, uint32_t* slab, int mode, Ctx& c);
+// Rows of iteration k_rows (into Yg, yY, idx; skipped without `gather`) and, in the same
+// launch, this iteration's recurrence reset without margins (alpha, far, r and the far
+// partials pending; counters and queues zeroed): for the far-forming Gram, whose launch
+// forms the margins itself.
+cudaError_t launch_gather_reset(const casgd_data_t& d, const casgd_params_t& p, uint64_t k_rows,
+                                const int32_t* idx_in, int32_t* idx, uint16_t* Yg, float* yY,
+                                bool gather, int64_t ldY, float* r, float* alpha, float* far,
+                                float* fpart, Ctrl* ctrl, uint32_t* slab, Ctx& c);
 // GATHER_ONLY for iteration k_next (into Y_next, yY_next, idx_next) and MARGINS_ONLY for
 // the rows in Y, in one launch (the two touch disjoint buffers).
 cudaError_t launch_gather_next_margins(const casgd_data_t& d, const casgd_params_t& p,
@@ -362,11 +371,14 @@ bool far_gram_supported(int64_t S, int64_t n, int b);
 cudaError_t launch_gram_band(const uint16_t* Y, float* G, int64_t S, int64_t n, int64_t ldY,
                              int b, int s, uint32_t flags, Ctrl* ctrl, uint32_t timeout_us,
                              Ctx& c);
+// w_acc (with fpart): FP32[n] scratch; the launch then forms the margins itself (r reset
+// to pending by launch_gather_reset) from Y and w, and w receives the update only with the
+// last block.
 cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t S, int64_t n,
                               int64_t ldY, int b, int s, float eta, int loss, uint32_t flags,
-                              const float* G, const uint16_t* Y, const float* r,
+                              const float* G, const uint16_t* Y, float* r,
                               const float* yY, float* alpha, float* far, uint32_t* slab,
-                              float* fpart, float* part, float* w, Ctrl* ctrl,
+                              float* fpart, float* part, float* w, float* w_acc, Ctrl* ctrl,
                               uint32_t timeout_us, Ctx& c);
 cudaError_t launch_update_reduce(const float* part, int upd_ctas, int64_t n, int64_t ldY,
                                  float* w, Ctrl* ctrl, Ctx& c);

@@ -1320,9 +1320,9 @@ cudaError_t launch_gram_band(const uint16_t* Y, float* G, int64_t S, int64_t n, 
 
 cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t S, int64_t n,
                               int64_t ldY, int b, int s, float eta, int loss, uint32_t flags,
-                              const float* G, const uint16_t* Y, const float* r,
+                              const float* G, const uint16_t* Y, float* r,
                               const float* yY, float* alpha, float* far, uint32_t* slab,
-                              float* fpart, float* part, float* w, Ctrl* ctrl,
+                              float* fpart, float* part, float* w, float* w_acc, Ctrl* ctrl,
                               uint32_t timeout_us, Ctx& c) {
   if (!gram_recur_fused_supported(S, n, b)) return cudaErrorNotSupported;
   const bool far_gram = fpart != nullptr;
@@ -1361,6 +1361,18 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
     rec.bulk_units = 0;  // no far units: the Gram forms the far sums
     rec.upd_R = upd_row_parts(b, ldY);  // the bulk groups only update: row parts
     rec.upd_units = s * (int)((ldY / 8 + 7) / 8) * rec.upd_R;
+    if (w_acc) {  // the bulk groups form the margins first (mG lanes per row, 4 passes)
+      int G = 1;
+      while (G < ldY / 8 && G < 32) G <<= 1;
+      rec.margins = true;
+      rec.mG = G;
+      rec.mrows = 8 * (32 / G) * 4;
+      rec.bulk_units = (int)((S + rec.mrows - 1) / rec.mrows);
+      rec.r_w = r;
+      rec.wm = w;
+      rec.wm_vec = (reinterpret_cast<uintptr_t>(w) & 15u) == 0;
+      rec.w_acc = w_acc;
+    }
   }
   // what Ctrl::band_done reaches once every stored tile is stored (8 warps per tile)
   if (!next) {
@@ -1413,7 +1425,7 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
     rec.C = want < grid - kUpdateCtas ? want : grid - kUpdateCtas;
   }
   if (rec.C < 1) return cudaErrorNotSupported;
-  rec.upd_groups = update_groups(rec, grid - rec.C);
+  rec.upd_groups = rec.margins ? 0 : update_groups(rec, grid - rec.C);
   if (far_gram && next) {
     const int nfar = P.a.ntiles - P.a.n_stored;
     P.a.far_head = nfar < grid / 2 ? nfar : grid / 2;

@@ -215,6 +215,39 @@ __global__ void __launch_bounds__(256) gather_kernel(RowArgs a) {
   gather_rows<kCopy, kMargin>(a, blockIdx.x);
 }
 
+// The recurrence's per-row reset where the margins are formed in the recurrence's launch
+// (the far-forming Gram): alpha, far, r and each row's far partials hold kAlphaPending.
+// Block `blk` of nr: a grid-stride pass over the S rows and, in storage order (so the
+// stores coalesce), over the S x fs far-partial slots (those t < (j-B) * npb of a row).
+__device__ void reset_rows(const RowArgs& a, int64_t blk, int64_t nr) {
+  const float pend = __uint_as_float(kAlphaPending);
+  const int64_t stride = nr * blockDim.x;
+  for (int64_t p = blk * blockDim.x + threadIdx.x; p < a.S; p += stride) {
+    a.alpha[p] = pend;
+    a.far[p] = pend;
+    a.r[p] = pend;
+  }
+  if (!a.fpart) return;
+  const int64_t total = a.S * a.fs;
+  for (int64_t e = blk * blockDim.x + threadIdx.x; e < total; e += stride) {
+    const int64_t p = e / a.fs;
+    const int t = (int)(e - p * a.fs);
+    if (t < ((int)(p / a.fb) - a.fB) * a.fnp) a.fpart[e] = pend;
+  }
+}
+
+// Blocks [0, nb_g) gather rows (g: the next iteration's, or this one's for a single
+// step), the others reset this iteration's recurrence state (mg).
+__global__ void __launch_bounds__(256) gather_reset_kernel(RowArgs g, RowArgs mg, int64_t nb_g) {
+  if ((int64_t)blockIdx.x < nb_g) {
+    gather_rows<true, false>(g, blockIdx.x);
+  } else {
+    const int64_t blk = (int64_t)blockIdx.x - nb_g;
+    if (blk == 0) reset_recurrence(mg);
+    reset_rows(mg, blk, (int64_t)gridDim.x - nb_g);
+  }
+}
+
 // Two independent passes in one launch: blocks [0, nb_g) gather the next iteration's
 // rows (g), the others form this iteration's margins (mg) from its rows already in Y.
 __global__ void __launch_bounds__(256) gather_next_margins_kernel(RowArgs g, RowArgs mg,
@@ -321,6 +354,23 @@ cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const 
             : mode == GATHER_ONLY      ? gather_kernel<true, false>
                                        : gather_kernel<false, true>;
   fn<<<(unsigned)row_blocks(a), 256, 0, c.stream>>>(a);
+  ++c.launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_reset(const casgd_data_t& d, const casgd_params_t& p, uint64_t k_rows,
+                                const int32_t* idx_in, int32_t* idx, uint16_t* Yg, float* yY,
+                                bool gather, int64_t ldY, float* r, float* alpha, float* far,
+                                float* fpart, Ctrl* ctrl, uint32_t* slab, Ctx& c) {
+  const RowArgs g = row_args(d, p, nullptr, k_rows, idx_in, idx, Yg, ldY, nullptr, yY, nullptr,
+                             nullptr, nullptr, ctrl, slab);
+  const RowArgs mg = row_args(d, p, nullptr, 0, nullptr, nullptr, nullptr, ldY, r, nullptr, alpha,
+                              far, fpart, ctrl, slab);
+  const int64_t nb = gather ? row_blocks(g) : 0;
+  const int64_t work = mg.fpart ? mg.S * mg.fs : mg.S;  // reset slots
+  int64_t nr = (work + 255) / 256;
+  if (nr > (int64_t)c.num_sms * 4) nr = (int64_t)c.num_sms * 4;
+  gather_reset_kernel<<<(unsigned)(nb + nr), 256, 0, c.stream>>>(g, mg, nb);
   ++c.launches;
   return cudaGetLastError();
 }

@@ -62,6 +62,12 @@ RecArgs make_rec_args(const float* G, const float* r, const float* yY, float* al
   a.fpart = nullptr;
   a.fs = a.npb = 0;
   a.band_total = 0;
+  a.margins = a.wm_vec = false;
+  a.r_fp32 = (flags & CASGD_FLAG_MARGINS_FP32) != 0;
+  a.mrows = a.mG = 0;
+  a.r_w = nullptr;
+  a.wm = nullptr;
+  a.w_acc = nullptr;
   a.far_gram = false;
   a.C = 0;
   a.upd_groups = 0;

@@ -81,6 +81,15 @@ struct RecArgs {
   // Gram in the same launch: Ctrl::band_done reaches band_total once every tile the Gram
   // stores is stored (each epilogue warp adds its tiles after its 32-row counter)
   uint32_t band_total;
+  // Margins formed in this launch (with the far-forming Gram): the bulk groups' first
+  // units (bulk_units of them, mrows rows each, mG lanes per row) write r (pending until
+  // then) from Y and w; the update then adds its block sums into w_acc and only the last
+  // block's into w, which the margins read.
+  bool margins, r_fp32, wm_vec;  // wm_vec: w 16-byte aligned
+  int mrows, mG;
+  float* r_w;
+  const float* wm;  // w as the launch starts (w_k), read by the margin units
+  float* w_acc;
   bool far_gram;  // the Gram stores only the band (and diagonal) tiles
   int64_t S;
   Ctrl* ctrl;
@@ -286,7 +295,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
     rb = 0;
     yv = f0 = f1 = 0.0f;
     if (lane == 0) {
-      rb = __float_as_uint(a.r[p]);
+      rb = __float_as_uint(ld_volatile_f32(a.r + p));  // pending while formed in this launch
       yv = a.yY[p];
     }
     if (j < kB + 1) return;
@@ -396,6 +405,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
     } else if (has_far && lane == 0) {
       pend |= pending1(farv);
     }
+    if (lane == 0) pend |= pending1(__uint_as_float(rbits));
     bool ok = true;
     if (__any_sync(0xffffffffu, pend)) {
       const uint64_t t_start = globaltimer_ns();
@@ -410,6 +420,10 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
               pend |= pending4(av[0][k]);
             }
           }
+        }
+        if (lane == 0 && pending1(__uint_as_float(rbits))) {
+          rbits = __float_as_uint(ld_volatile_f32(a.r + p));
+          pend |= pending1(__uint_as_float(rbits));
         }
         if (kFarParts) {
           if (has_far && lane < nfar && pending1(fp0)) {
@@ -674,13 +688,73 @@ __device__ void update_unit(const RecArgs& a, int u, int rt) {
   group_sync<kMode != 0>();
   if (!s_turn) return;  // group-uniform
   if (rt < 64 && c < a.n) {
-    const float v = __ldcg(a.w + c) + bsum;
-    a.w[c] = v;
+    // with the margins in this launch, w keeps w_k until the last block: the running
+    // sum lives in w_acc (block 0 starts from w)
+    const float* src = (a.w_acc && j > 0) ? a.w_acc : a.w;
+    float* dst = (a.w_acc && j + 1 < a.s) ? a.w_acc : a.w;
+    const float v = __ldcg(src + c) + bsum;
+    dst[c] = v;
     if (j == a.s - 1 && !isfinite(v)) atomicOr(&a.ctrl->status, ST_NONFINITE);
     __threadfence();
   }
   group_sync<kMode != 0>();
   if (rt == 0) red_release_add_u32(a.upd_chunks + cc, 1u);  // block j+1's turn
+}
+
+// -------------------------------------------------------------- margin units
+// Step a4 in the recurrence's launch (with the far-forming Gram): unit u forms the
+// margins of rows u*mrows .. of Y with w (the launch's w_k: the update writes w only with
+// the last block).  mG lanes per row (a power of two covering the row's 16-byte vectors
+// up to 32), 32/mG rows per warp and pass; lane g sums the vectors g, g+mG, ... in FP32,
+// eight elements each in column order, the row's lanes then add by a shuffle tree, and
+// its first lane stores the margin (rounded once to BF16, or FP32 with MARGINS_FP32).
+__device__ void margin_unit(const RecArgs& a, int u, int rt) {
+  const int G = a.mG;
+  const int warp = rt >> 5, lane = rt & 31;
+  const int g = lane & (G - 1);
+  const int rows_pass = 8 * (32 / G);
+  const int64_t nvec = a.ldY / 8;
+  const int64_t p_end = (int64_t)(u + 1) * a.mrows < a.S ? (int64_t)(u + 1) * a.mrows : a.S;
+  for (int64_t p0 = (int64_t)u * a.mrows; p0 < p_end; p0 += rows_pass) {
+    const int64_t p = p0 + warp * (32 / G) + lane / G;
+    const bool live = p < p_end;
+    const uint16_t* yr = a.Y + (live ? p : 0) * a.ldY;
+    float acc = 0.0f;
+    constexpr int kBatch = 8;
+    for (int64_t v0 = g; v0 < nvec; v0 += (int64_t)G * kBatch) {
+      uint4 q[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int64_t v = v0 + (int64_t)k * G;
+        q[k] = (live && v < nvec) ? __ldg(reinterpret_cast<const uint4*>(yr + v * 8))
+                                  : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int64_t c0 = (v0 + (int64_t)k * G) * 8;
+        if (c0 >= a.n) break;
+        const uint32_t pw[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+        float wv[8];
+        if (a.wm_vec && c0 + 8 <= a.n) {
+          const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.wm + c0));
+          const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.wm + c0 + 4));
+          wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
+          wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) wv[e] = c0 + e < a.n ? __ldg(a.wm + c0 + e) : 0.0f;
+        }
+        // elements in column order; past n the row holds zeros (stored padding)
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          acc = fmaf(bf16_bits_to_float(pw[h] & 0xFFFFu), wv[2 * h], acc);
+          acc = fmaf(bf16_bits_to_float(pw[h] >> 16), wv[2 * h + 1], acc);
+        }
+      }
+    }
+    for (int off = G >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);
+    if (live && g == 0) __stcg(a.r_w + p, a.r_fp32 ? acc : round_bf16(acc));
+  }
 }
 
 // ------------------------------------------------------------------- bulk role
@@ -732,6 +806,11 @@ __device__ void bulk_role(const RecArgs& a, int rt, bool upd_group) {
         continue;
       }
       return;
+    }
+    if (a.margins) {  // the bulk units are margin units
+      margin_unit(a, unit, rt);
+      group_sync<kMode != 0>();
+      continue;
     }
     const int j = a.B + 1 + unit / a.U;
     const int c = unit % a.U;
