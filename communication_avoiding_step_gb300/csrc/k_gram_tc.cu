@@ -1361,12 +1361,12 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
     rec.bulk_units = 0;  // no far units: the Gram forms the far sums
     rec.upd_R = upd_row_parts(b, ldY);  // the bulk groups only update: row parts
     rec.upd_units = s * (int)((ldY / 8 + 7) / 8) * rec.upd_R;
-    if (w_acc) {  // the bulk groups form the margins first (mG lanes per row, 4 passes)
+    if (w_acc) {  // the bulk groups form the margins first (mG lanes per row, 2 passes)
       int G = 1;
       while (G < ldY / 8 && G < 32) G <<= 1;
       rec.margins = true;
       rec.mG = G;
-      rec.mrows = 8 * (32 / G) * 4;
+      rec.mrows = 8 * (32 / G) * 2;
       rec.bulk_units = (int)((S + rec.mrows - 1) / rec.mrows);
       rec.r_w = r;
       rec.wm = w;
