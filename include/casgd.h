@@ -258,8 +258,11 @@ int casgd_outer_step(const casgd_data_t* data, const casgd_params_t* params, flo
  * Where the paired-SM Gram shares its launch with the recurrence (see
  * CASGD_FLAG_NO_FUSE) and iters >= 2, the Gram of iteration k+1 runs in the launch
  * of iteration k's recurrence (its rows do not depend on w), on second Y and G
- * buffers that casgd_workspace_size includes for such parameters; the results are
- * bit-identical to iters calls of casgd_outer_step. */
+ * buffers that casgd_workspace_size includes for such parameters; with the far-
+ * forming Gram (CASGD_FLAG_FAR_FROM_GRAM, the default for b a multiple of 256) the
+ * launch of iteration k forms iteration k's far sums and margins and stores the band
+ * of iteration k+1, after a launch that gathers iteration k+1's rows.  Either way the
+ * results are bit-identical to iters calls of casgd_outer_step. */
 int casgd_train(const casgd_data_t* data, const casgd_params_t* params, float* w,
                 uint64_t k0, int32_t iters, void* ws, size_t ws_bytes, void* stream,
                 int32_t loss_every, double* loss_hist, casgd_profile_t* prof);
