@@ -248,7 +248,8 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
 // need this iteration's alpha) and stores the band of iteration k+1, so the recurrence
 // starts on a complete band; the first iteration's band comes from a prologue launch.
 // Every value is computed as in outer_step_impl (same kernels' arithmetic), only the
-// order of independent work changes.  Stage events per iteration: 0 before the gather of
+// order of independent work changes.  The loop's gather and shared launches use
+// programmatic dependent launch (Ctx::pdl).  Stage events per iteration: 0 before the gather of
 // the next iteration's rows and this iteration's margins, 1 before the shared launch, 2,
 // 3 and 4 after it (it ends with the update).
 int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, uint64_t k0,
@@ -263,6 +264,10 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   int rc;
   float* fpart = far ? R.fpart : nullptr;
   if (prof) prof->gram_kind = far ? 6 : 4;
+  // the gather launches and the shared launches of the loop overlap each other's start
+  // and end (programmatic dependent launch); each waits for its predecessor's completion
+  // before it touches memory, so the results are those of plain stream order
+  c.pdl = true;
   for (int32_t it = 0; it < iters; ++it) {
     const int cur = it & 1, nxt = cur ^ 1;
     const uint64_t k = k0 + (uint64_t)it;

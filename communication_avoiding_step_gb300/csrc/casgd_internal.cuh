@@ -260,6 +260,20 @@ __device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
   return *reinterpret_cast<const volatile uint32_t*>(p);
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic stream
+// serialization attribute may be scheduled before the previous kernel of its stream has
+// finished; wait_prior_grid() returns once that kernel has completed and its memory
+// operations are visible, so it precedes every global access of such a kernel.  For a
+// kernel launched without the attribute it returns at once.  allow_next_grid() lets the
+// next kernel of the stream be scheduled (it still waits for this one's completion at
+// its own wait_prior_grid()); without it that happens when this grid's blocks exit.
+__device__ __forceinline__ void wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_next_grid() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ launchers
 // Launch parameters of the kernels one call launches repeatedly (occupancy results, with
 // the dynamic shared memory attribute set), found once per call: the queries cost host
@@ -292,7 +306,21 @@ struct Ctx {
   int num_sms;
   int64_t launches;
   LaunchCache* cache = nullptr;
+  // launch the kernels of casgd_train's loop (the gather and the shared launch) with
+  // programmatic stream serialization: each may be scheduled while the one before it
+  // ends, and waits for it in wait_prior_grid() before touching memory
+  bool pdl = false;
 };
+
+// Adds the programmatic stream serialization attribute to cfg when c.pdl (attr must
+// have room for one more entry).
+inline void add_pdl_attr(const Ctx& c, cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr) {
+  if (!c.pdl) return;
+  attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  ++cfg.numAttrs;
+}
 
 // query(&v) once per kernel `fn` and Ctx cache (every time without a cache).
 template <class Query>

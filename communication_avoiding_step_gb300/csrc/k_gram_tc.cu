@@ -888,6 +888,9 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = sc->tmem_base;
+  // Launched behind the gather (casgd_train), the setup above overlaps its end; every
+  // global access follows this wait.
+  wait_prior_grid();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1067,6 +1070,7 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
   __syncthreads();
   cluster_sync();  // the leader's MMAs and every copy into either CTA are finished
   tc_fence_after();
+  allow_next_grid();
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
@@ -1399,7 +1403,7 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
   const Fn fn = table[(far_gram ? 2 : 0) + (next ? 1 : 0)][v - 1];
   const size_t smem = far_gram ? pair_smem_bytes<kStagesFused, true>()
                                : pair_smem_bytes<kStagesFused>();
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = cluster2_config(kFusedThreads, smem, c.stream, attr);
   cfg.gridDim = dim3(2 * (unsigned)(c.num_sms / 2));
   int max_clusters = 0;
@@ -1431,6 +1435,11 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
     P.a.far_head = nfar < grid / 2 ? nfar : grid / 2;
   }
   cfg.gridDim = dim3((unsigned)grid);
+  // Scheduled early behind the gather, a CTA waits in wait_prior_grid() (a hardware
+  // wait, no spin) until the gather has completed; the gather blocks are all running
+  // by then (they allow this launch only once each has started), so every CTA of this
+  // grid is still resident once they leave.
+  add_pdl_attr(c, cfg, attr);
   e = cudaLaunchKernelEx(&cfg, fn, P.map, P.mapG, mapYf, P.a, rec);
   ++c.launches;
   return e;

@@ -211,14 +211,16 @@ __device__ __forceinline__ void gather_rows(const RowArgs& a, int64_t blk) {
 
 template <bool kCopy, bool kMargin>
 __global__ void __launch_bounds__(256) gather_kernel(RowArgs a) {
+  wait_prior_grid();
+  allow_next_grid();
   if (kMargin && blockIdx.x == 0) reset_recurrence(a);
   gather_rows<kCopy, kMargin>(a, blockIdx.x);
 }
 
 // The recurrence's per-row reset where the margins are formed in the recurrence's launch
 // (the far-forming Gram): alpha, far, r and each row's far partials hold kAlphaPending.
-// Block `blk` of nr: a grid-stride pass over the S rows and, in storage order (so the
-// stores coalesce), over the S x fs far-partial slots (those t < (j-B) * npb of a row).
+// Block `blk` of nr: a grid-stride pass over the S rows, then one warp per row over its
+// far-partial slots t < (j-B) * npb, which are contiguous (the stores coalesce).
 __device__ void reset_rows(const RowArgs& a, int64_t blk, int64_t nr) {
   const float pend = __uint_as_float(kAlphaPending);
   const int64_t stride = nr * blockDim.x;
@@ -228,17 +230,20 @@ __device__ void reset_rows(const RowArgs& a, int64_t blk, int64_t nr) {
     a.r[p] = pend;
   }
   if (!a.fpart) return;
-  const int64_t total = a.S * a.fs;
-  for (int64_t e = blk * blockDim.x + threadIdx.x; e < total; e += stride) {
-    const int64_t p = e / a.fs;
-    const int t = (int)(e - p * a.fs);
-    if (t < ((int)(p / a.fb) - a.fB) * a.fnp) a.fpart[e] = pend;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = nr * (blockDim.x >> 5);
+  for (int64_t p = blk * (blockDim.x >> 5) + (threadIdx.x >> 5); p < a.S; p += warps) {
+    const int nfar = ((int)(p / a.fb) - a.fB) * a.fnp;
+    float* row = a.fpart + p * a.fs;
+    for (int t = lane; t < nfar; t += 32) row[t] = pend;
   }
 }
 
 // Blocks [0, nb_g) gather rows (g: the next iteration's, or this one's for a single
 // step), the others reset this iteration's recurrence state (mg).
 __global__ void __launch_bounds__(256) gather_reset_kernel(RowArgs g, RowArgs mg, int64_t nb_g) {
+  wait_prior_grid();  // the previous launch reads the buffers this one writes
+  allow_next_grid();  // the next launch may take SMs as this one's blocks leave
   if ((int64_t)blockIdx.x < nb_g) {
     gather_rows<true, false>(g, blockIdx.x);
   } else {
@@ -252,6 +257,8 @@ __global__ void __launch_bounds__(256) gather_reset_kernel(RowArgs g, RowArgs mg
 // rows (g), the others form this iteration's margins (mg) from its rows already in Y.
 __global__ void __launch_bounds__(256) gather_next_margins_kernel(RowArgs g, RowArgs mg,
                                                                   int64_t nb_g) {
+  wait_prior_grid();
+  allow_next_grid();
   if ((int64_t)blockIdx.x < nb_g) {
     gather_rows<true, false>(g, blockIdx.x);
   } else {
@@ -337,6 +344,17 @@ RowArgs row_args(const casgd_data_t& d, const casgd_params_t& p, const float* w,
   return a;
 }
 
+// 256-thread blocks on c's stream, with the programmatic serialization attribute when
+// c.pdl (attr: room for it)
+cudaLaunchConfig_t plain_config(unsigned blocks, const Ctx& c, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = c.stream;
+  add_pdl_attr(c, cfg, attr);
+  return cfg;
+}
+
 int64_t row_blocks(const RowArgs& a) {
   const int64_t rows_per_cta = 8 * (32 / a.G);
   return (a.S + rows_per_cta - 1) / rows_per_cta;
@@ -370,9 +388,11 @@ cudaError_t launch_gather_reset(const casgd_data_t& d, const casgd_params_t& p, 
   const int64_t work = mg.fpart ? mg.S * mg.fs : mg.S;  // reset slots
   int64_t nr = (work + 255) / 256;
   if (nr > (int64_t)c.num_sms * 4) nr = (int64_t)c.num_sms * 4;
-  gather_reset_kernel<<<(unsigned)(nb + nr), 256, 0, c.stream>>>(g, mg, nb);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = plain_config((unsigned)(nb + nr), c, attr);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gather_reset_kernel, g, mg, nb);
   ++c.launches;
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_gather_next_margins(const casgd_data_t& d, const casgd_params_t& p,
@@ -385,9 +405,11 @@ cudaError_t launch_gather_next_margins(const casgd_data_t& d, const casgd_params
   const RowArgs mg = row_args(d, p, w, 0, nullptr, nullptr, const_cast<uint16_t*>(Y), ldY, r,
                               nullptr, alpha, far, fpart, ctrl, slab);
   const int64_t nb = row_blocks(g);
-  gather_next_margins_kernel<<<(unsigned)(2 * nb), 256, 0, c.stream>>>(g, mg, nb);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = plain_config((unsigned)(2 * nb), c, attr);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gather_next_margins_kernel, g, mg, nb);
   ++c.launches;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace casgd
