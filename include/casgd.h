@@ -183,7 +183,10 @@ typedef struct {
                             before stage e of outer iteration it (e = 0 gather,
                             1 Gram, 2 recurrence, 3 update, 4 after update;
                             when the Gram and the recurrence share one launch,
-                            events 2 and 3 are both recorded after it)          */
+                            events 2 and 3 are both recorded after it).  An
+                            event between two launches keeps them from
+                            overlapping (see casgd_train), so a timed loop
+                            with events runs slower than one without        */
   int32_t n_events;      /* in: length of stage_events                          */
   int32_t gram_kind;     /* out: 1 = tcgen05 Gram kernel used, 2 = CUDA-core,
                             3 = paired-SM tcgen05 Gram and recurrence in one
@@ -261,7 +264,10 @@ int casgd_outer_step(const casgd_data_t* data, const casgd_params_t* params, flo
  * buffers that casgd_workspace_size includes for such parameters; with the far-
  * forming Gram (CASGD_FLAG_FAR_FROM_GRAM, the default for b a multiple of 256) the
  * launch of iteration k forms iteration k's far sums and margins and stores the band
- * of iteration k+1, after a launch that gathers iteration k+1's rows.  Either way the
+ * of iteration k+1, after a launch that gathers iteration k+1's rows.  The loop's
+ * launches use programmatic dependent launch: each may be scheduled while the one
+ * before it ends and waits for that one's completion before it touches memory, so
+ * work the caller enqueues on `stream` keeps plain stream order.  Either way the
  * results are bit-identical to iters calls of casgd_outer_step. */
 int casgd_train(const casgd_data_t* data, const casgd_params_t* params, float* w,
                 uint64_t k0, int32_t iters, void* ws, size_t ws_bytes, void* stream,
