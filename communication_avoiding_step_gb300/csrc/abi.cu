@@ -190,6 +190,9 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   const int32_t* idx_in = taps ? taps->idx_in : nullptr;
   if (prof) prof->gram_kind = choice;
 
+  // the shared launch may be scheduled while the gather ends (programmatic dependent
+  // launch; it waits for the gather's completion before it touches memory)
+  c.pdl = true;
   if ((rc = record(prof, it, 0, st)) != CASGD_OK) return rc;
   if (gp.far)  // the rows and the reset; the margins are formed in the shared launch
     CK(launch_gather_reset(*d, *p, k, idx_in, R.idx, R.Y, R.yY, true, L.ldY, R.r, R.alpha,
