@@ -248,13 +248,14 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
 // iteration k+1 (whose rows are sampled ahead: only the margins need the current w)
 // runs in the launch of iteration k's recurrence, on double-buffered Y and G.  With the
 // far-forming Gram (far) the launch of iteration k forms iteration k's far sums (they
-// need this iteration's alpha) and stores the band of iteration k+1, so the recurrence
-// starts on a complete band; the first iteration's band comes from a prologue launch.
-// Every value is computed as in outer_step_impl (same kernels' arithmetic), only the
-// order of independent work changes.  The loop's gather and shared launches use
-// programmatic dependent launch (Ctx::pdl).  Stage events per iteration: 0 before the gather of
-// the next iteration's rows and this iteration's margins, 1 before the shared launch, 2,
-// 3 and 4 after it (it ends with the update).
+// need this iteration's alpha), its margins and update, and stores the band of iteration
+// k+1, so the recurrence starts on a complete band; the first iteration's band comes
+// from a prologue launch.  Every value is computed as in outer_step_impl (same kernels'
+// arithmetic), only the order of independent work changes.  The loop's gather and
+// shared launches use programmatic dependent launch (Ctx::pdl).  Stage events per
+// iteration: 0 before the gather of the next iteration's rows (with the stored-G Gram
+// also this iteration's margins), 1 before the shared launch, 2, 3 and 4 after it (it
+// ends with the update).
 int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, uint64_t k0,
                     int32_t iters, const Layout& L, const Resolved& R, Ctx& c,
                     casgd_profile_t* prof, int32_t loss_every, int& slot, int& flushed,

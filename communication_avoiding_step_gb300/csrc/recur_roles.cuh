@@ -21,28 +21,30 @@
 //    of far_j (below).  The warp has its band rows of G in registers before it waits
 //    (loaded while it waited in the previous phase), then waits for alpha_{j-1} and
 //    far_j by loading exactly those values until none holds the pending pattern.
-//  * bulk groups take units (block j >= B+1, chunk of 4 blocks t, 16 rows) from an
-//    atomic queue and compute partial sums of far_j = sum_{t<j-B} G_{j,t} alpha_t for
-//    their rows, streaming G with coalesced float4 reads; they wait on alpha_t the same
-//    way.  In mode 3 there are no far units: the Gram's epilogue multiplies each far
-//    tile G_{j,t} by alpha_t as soon as alpha_t is final and stores one partial sum per
-//    row, block t and column group (npb groups per block); the chain adds a row's
-//    (j-B) * npb partials itself.  far_j is needed only B phases after its last input is known, so most of G is
-//    read off the critical path; the chain adds a row's partials in chunk order.  After the far units the same queue hands out the first stage
-//    of the weight update when it is fused: per block j and 64-column chunk, the
-//    partial row of Y^T alpha over that block, each waiting on the alpha of its rows.
-// Synchronisation is through the data: the gather kernel fills alpha and far with
-// kAlphaPending before the recurrence runs, and a value is final once it differs from
-// that pattern (32-bit stores are single-copy atomic, and a reader uses only the value
-// it waited on, so no fences or counters are needed).  When the Gram of the same
-// iteration runs in the same launch (kMode 1), rows of G are guarded by per-32-row
-// counters that the
-// Gram's epilogue warps release once their stores of a tile are complete; a reader
-// acquires the counter of its rows before loading them, and loads G through L2 only.
-// Every wait is bounded by `timeout_ns`; on expiry the waiter records ST_TIMEOUT, which
-// wait gave up (Ctrl::diag) and the abort word, and every other waiter stops.  Sums
-// are taken in a fixed order (far_j over t ascending; then r + far + band), so results
-// are deterministic.
+//  * bulk groups take units from atomic queues.  Modes 0-2: far units (block j >= B+1,
+//    16 rows) whose sum far_j = sum_{t<j-B} G_{j,t} alpha_t runs over t in runs of up to
+//    four phases whose alpha is already final, streaming G with coalesced float4 reads.
+//    Modes 3 and 4 have no far units: the Gram's epilogue multiplies each far tile
+//    G_{j,t} by alpha_t once alpha_t is final and stores one partial sum per row, block
+//    t and column group (npb groups per block), and the chain adds a row's (j-B) * npb
+//    partials itself, in a fixed order; there the bulk units are margin units
+//    (r = Y w for a run of rows, before the chain needs them).  A second queue hands
+//    out the first stage of the weight update: per block j and 64-column chunk (and
+//    row part), the partial row of Y^T alpha over that block, once its alpha is final.
+//    far_j is needed only B phases after its last input is known, so most of the far
+//    work is off the critical path.
+// Synchronisation is through the data: the launch before the recurrence fills alpha and
+// far (and r and the far partials where those are formed in the launch) with
+// kAlphaPending, and a value is final once it differs from that pattern (32-bit stores
+// are single-copy atomic, and a reader uses only the value it waited on, so no fences
+// or counters are needed).  When the Gram of the same iteration runs in the same launch
+// and stores the rows a reader needs (modes 1 and 3), those rows are guarded by
+// per-32-row counters that the Gram's epilogue warps release once their stores of a
+// tile are complete; a reader acquires the counter of its rows before loading them, and
+// loads G through L2 only.  Every wait is bounded by `timeout_ns`; on expiry the waiter
+// records ST_TIMEOUT, which wait gave up (Ctrl::diag) and the abort word, and every
+// other waiter stops.  Sums are taken in a fixed order (far_j over t ascending, or the
+// partials two per lane and then a fixed shuffle tree; then r + far + band), so results are deterministic.
 #pragma once
 
 #include "casgd_internal.cuh"
