@@ -13,6 +13,10 @@ N > 1 runs under torchrun, one process per GPU: independent replicas (one GPU's
 problem per rank, no collective on the data path); value = samples of all ranks / max
 time.  `--impl reference` times the CPU oracle (the plain NumPy statement of the
 method) on the host cores, on a bounded sample of the same workload.
+
+`value` comes from K steps called as a user calls them; a second pass of K steps with
+CUDA events between the launches gives the per-stage times and the roofline (the
+events themselves cost stream time, so that pass is reported apart).
 """
 from __future__ import annotations
 
