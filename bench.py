@@ -202,8 +202,9 @@ def world_max(value: float, device) -> float:
 
 
 # --------------------------------------------------------------------- CPU side ----
-def cpu_sample(cfg, s, budget_s=15.0, max_iters=8):
-    """Times the oracle's emulating-mode outer iteration on this host (bounded sample)."""
+def cpu_sample(cfg, s, budget_s=15.0, max_iters=50):
+    """Times the oracle's emulating-mode outer iteration on this host (bounded sample:
+    up to one step's 50 outer iterations, stopping once budget_s seconds are spent)."""
     import oracle
     r = si.RECIPES[cfg]
     p = si.make_problem(cfg)
