@@ -59,6 +59,43 @@ def test_workspace_size_host_only(lib):
     assert lib.casgd_workspace_size(C.byref(d), C.byref(bad), C.byref(nbytes)) == nat.CASGD_ERR_ARG
 
 
+def _ws_bytes(lib, n, b, s, flags):
+    nbytes = C.c_size_t(0)
+    d = nat.Data(1000, n, (n + 7) // 8 * 8, 0, 0)
+    p = nat.Params(b, s, 0.1, 0, 0, flags, 0)
+    assert lib.casgd_workspace_size(C.byref(d), C.byref(p), C.byref(nbytes)) == 0
+    return nbytes.value
+
+
+def _a(x):  # 256-byte sections
+    return (x + 255) // 256 * 256
+
+
+def test_workspace_sections_of_the_gram_paths(lib):
+    # b = 256, s = 32, n = 2000: the stored-G launch shared with the recurrence (FULL_G)
+    # adds a second idx, y_Y, Y and G for casgd_train's iteration-ahead Gram; the
+    # far-forming default adds to that the far partials (one column group per block:
+    # S x s floats) and the update's running sum w_acc (n floats)
+    n, b, s = 2000, 256, 32
+    S, ld = b * s, 2000
+    G = s * (s - 1) // 2 * b * b * 4
+    no_fuse = _ws_bytes(lib, n, b, s, nat.FLAG_NO_FUSE)
+    full_g = _ws_bytes(lib, n, b, s, nat.FLAG_FULL_G)
+    far = _ws_bytes(lib, n, b, s, 0)
+    assert full_g - no_fuse == 2 * _a(S * 4) + _a(S * ld * 2) + _a(G)
+    assert far - full_g == _a(S * s * 1 * 4) + _a(n * 4)
+    # b = 1024, s = 16, n = 18: the stored G is not shared with the recurrence there
+    # (b > 512), so only the far-forming path has second buffers; four column groups
+    # per block keep a row's far partials within 64
+    n, b, s = 18, 1024, 16
+    S, ld = b * s, 24
+    G = s * (s - 1) // 2 * b * b * 4
+    full_g = _ws_bytes(lib, n, b, s, nat.FLAG_FULL_G)
+    far = _ws_bytes(lib, n, b, s, 0)
+    assert far - full_g == (2 * _a(S * 4) + _a(S * ld * 2) + _a(G) + _a(S * s * 4 * 4)
+                            + _a(n * 4))
+
+
 def test_argument_errors_before_any_cuda_call(lib):
     p = nat.Params(16, 4, 0.1, 0, 0, 0, 0)
     fake = 1 << 20  # never dereferenced: every case fails validation first
