@@ -888,8 +888,8 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = sc->tmem_base;
-  // Launched behind the gather (casgd_train), the setup above overlaps its end; every
-  // global access follows this wait.
+  // Launched behind the gather (programmatic dependent launch), the setup above
+  // overlaps the gather's end; every global access follows this wait.
   wait_prior_grid();
 
   if (warp == 0) {
