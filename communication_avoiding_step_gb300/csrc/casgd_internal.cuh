@@ -306,9 +306,9 @@ struct Ctx {
   int num_sms;
   int64_t launches;
   LaunchCache* cache = nullptr;
-  // launch the kernels of casgd_train's loop (the gather and the shared launch) with
-  // programmatic stream serialization: each may be scheduled while the one before it
-  // ends, and waits for it in wait_prior_grid() before touching memory
+  // launch the gather and the shared launch of an outer iteration (casgd_outer_step,
+  // casgd_train) with programmatic stream serialization: each may be scheduled while
+  // the one before it ends, and waits for it in wait_prior_grid() before touching memory
   bool pdl = false;
 };
 
