@@ -60,6 +60,10 @@ def parse():
                     help="skip the FP32 plain SGD comparison leg")
     ap.add_argument("--m", type=int, default=None,
                     help="override the row count (small profiling captures only)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads' lines (recipes 3, 4 with s = 4..32, 5)")
+    ap.add_argument("--config-steps", type=int, default=3,
+                    help="timed steps of each other workload (after 1 warm-up step)")
     ap.add_argument("--flags", type=lambda v: int(v, 0), default=0,
                     help="casgd_params_t.flags for profiling variants (e.g. 0x40: Gram and "
                          "recurrence in separate launches)")
@@ -106,6 +110,20 @@ def peaks():
                 "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
             "source": "fallback"}
+
+
+def tensor_peak(pk: dict, clk: dict):
+    """The dense BF16 peak a kernel timed in this run is held to: the burst figure,
+    unless the clock record of the timed region shows the power cap or an SM clock well
+    below its maximum (then the seconds-long sustained figure).  Returns (peak, which)."""
+    reasons = clk.get("reasons") or []
+    sm, mx = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    low = sm is not None and mx is not None and sm < 0.9 * mx
+    if "sw_power_cap" in reasons or low:
+        why = "sw_power_cap active" if "sw_power_cap" in reasons else f"SM clock {sm:.0f} of {mx:.0f} MHz"
+        return pk["bf16_tflops_sustained"], f"sustained ({why} in the timed region)"
+    return pk["bf16_tflops"], ("burst (timed region at full SM clock, no power cap)"
+                               if sm is not None else "burst (clocks not sampled)")
 
 
 def source_hash(kernel: str) -> str:
@@ -256,6 +274,125 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------- GPU side ----
+GRAM_NAMES = {1: "gram_tc", 2: "gram_simt", 3: "gram_recur", 4: "gram_recur",
+              5: "gram_recur_far", 6: "gram_recur_far"}
+
+
+def stage_times(torch, casgd, data, params, ws, w, iters, steps, k, stream):
+    """Per-launch stage times (ms) from `steps` steps with CUDA events between the
+    launches; returns (stage_ms_per_launch, total_ms, k, last loss history)."""
+    n_ev = iters * casgd.STAGE_EVENTS
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
+    for row in events:        # torch creates the CUDA event lazily, on first record
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    hist = None
+    for i in range(steps):
+        w.zero_()
+        hist, _, _ = casgd.train(data, params, w, iters, ws, k0=k, loss_every=iters,
+                                 stage_events=events[i])
+        k += iters
+    s1.record(stream)
+    torch.cuda.synchronize()
+    stage_ms = {st: 0.0 for st in STAGES}
+    for i in range(steps):
+        ev = events[i]
+        for it in range(iters):
+            b0 = it * casgd.STAGE_EVENTS
+            for si_, st in enumerate(STAGES):
+                stage_ms[st] += ev[b0 + si_].elapsed_time(ev[b0 + si_ + 1])
+    per_launch = {st: stage_ms[st] / (steps * iters) for st in STAGES}
+    return per_launch, s0.elapsed_time(s1), sum(stage_ms.values()), k, hist
+
+
+def chain_phase_floor(torch, casgd, data, params, k):
+    """The fastest phase of the recurrence's chain in one traced outer iteration (ns
+    between alpha_{j-1} and alpha_j stored, j >= 1), or None."""
+    import dataclasses
+    pt = dataclasses.replace(params, flags=params.flags | casgd.FLAG_TRACE_CHAIN)
+    ws = casgd.workspace(data, pt)
+    w = torch.zeros(data.n, device="cuda")
+    casgd.train(data, pt, w, 2, ws, k0=k)
+    tr = casgd.chain_trace(data, pt, ws)
+    st = [row[3] for row in tr[:params.s]]
+    d = [b - a for a, b in zip(st[:-1], st[1:]) if a and b and b > a]
+    del ws
+    return min(d) if d else None
+
+
+def extra_configs(args, torch, casgd, rank, pk):
+    """The other workloads of the method (recipes 3, 4 at s = 4, 8, 16, 32, and 5): one
+    warm-up and `config_steps` timed steps each, as a user calls them, then as many steps
+    with events between the launches for the dominant launch's time."""
+    out = {}
+    pl = [(3, None), (4, 4), (4, 8), (4, 16), (4, 32), (5, None)]
+    stream = torch.cuda.current_stream()
+    for cfg, s_ov in pl:
+        r, s, iters = workload(cfg, s_ov)
+        S = r.b * s
+        p = si.make_problem(cfg)
+        X32 = torch.from_numpy(p.X).cuda()
+        y = torch.from_numpy(p.y).cuda()
+        data = casgd.Dataset.from_fp32(X32, y)
+        del X32
+        params = casgd.Params(r.b, s, r.eta, r.loss, seed=rank)
+        ws = casgd.workspace(data, params)
+        w = torch.zeros(r.n, device="cuda")
+        k = 0
+        w.zero_()
+        casgd.train(data, params, w, iters, ws, k0=k, loss_every=iters)
+        k += iters
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        kind = None
+        for _ in range(args.config_steps):
+            w.zero_()
+            hist, _, kind = casgd.train(data, params, w, iters, ws, k0=k, loss_every=iters)
+            k += iters
+        t1.record(stream)
+        torch.cuda.synchronize()
+        el = t0.elapsed_time(t1) / 1e3
+        per_launch, _, _, k, _ = stage_times(torch, casgd, data, params, ws, w, iters,
+                                             args.config_steps, k, stream)
+        work = alg_work(r.n, S, s, r.b, p.m)
+        t_g = per_launch["gram"] / 1e3
+        name = GRAM_NAMES[kind]
+        ent = {"workload": workload_config(r, s, iters, S)["workload"],
+               "value": S * iters * args.config_steps / el, "unit": "samples/s",
+               "ms_per_step": el * 1e3 / args.config_steps, "steps": args.config_steps,
+               "dominant_kernel": name, "dominant_ms_per_launch": per_launch["gram"],
+               "other_ms_per_iteration": {st: per_launch[st] for st in STAGES if st != "gram"},
+               "final_loss": hist[0] if hist else None}
+        tf = work["gram"]["flops"] / t_g / 1e12
+        tb = work["gram"]["bytes"] / t_g / 1e9
+        ent["tensor"] = {"achieved_TFLOP/s": tf, "frac": tf / pk["bf16_tflops"],
+                         "peak": pk["bf16_tflops"], "peak_source": f"{pk['source']} bf16 burst"}
+        ent["hbm_by_algorithmic_bytes"] = {
+            "achieved_GB/s": tb, "frac": tb / pk["hbm_gbs"], "peak": pk["hbm_gbs"],
+            "note": "bytes of the stored-G algorithm (Y read, G written); the far-forming "
+                    "launch never moves G below the band, so this can exceed 1"}
+        floor = chain_phase_floor(torch, casgd, data, params, k) if kind in (5, 6) else None
+        if floor:
+            t_lat = s * floor / 1e9
+            ent["latency"] = {"bound": "chain", "phase_floor_us": floor / 1e3,
+                              "bound_us": t_lat * 1e6, "frac": t_lat / t_g,
+                              "note": "s phases x the fastest measured chain phase (alpha_j "
+                                      "stored after alpha_{j-1}, one traced iteration)"}
+        bound = "tensor" if ent["tensor"]["frac"] >= (ent.get("latency") or {}).get("frac", 0) \
+            else "chain latency"
+        ent["bound"] = bound
+        out[f"config{cfg}" + (f"_s{s}" if cfg == 4 else "")] = ent
+        del ws, data, w
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import communication_avoiding_step_gb300 as casgd
@@ -350,8 +487,7 @@ def run_ours(args):
     # kind 3/4/5: the Gram (4: of the next iteration; 5: forming the far sums), the
     # recurrence and the update share one launch (its time is the "gram" stage; the
     # "recurrence" stage is then empty)
-    gram_name = {1: "gram_tc", 2: "gram_simt", 3: "gram_recur", 4: "gram_recur",
-                 5: "gram_recur_far", 6: "gram_recur_far"}[kind]
+    gram_name = GRAM_NAMES[kind]
     stages_out = {}
     for st in STAGES:
         t = per_launch_ms[st] / 1e3
@@ -365,11 +501,10 @@ def run_ours(args):
     t_dom = per_launch_ms[dom] / 1e3
     if dom == "gram":
         achieved = work["gram"]["flops"] / t_dom / 1e12
-        peak = pk["bf16_tflops_sustained"]
+        peak, which = tensor_peak(pk, clocks.summary())
         roof = {"kernel": gram_name, "bound": "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": f"{pk['source']} bf16 dense, sustained (kernel timed inside "
-                               "a long step loop)",
+                "peak_source": f"{pk['source']} bf16 dense, {which}",
                 "traffic": traffic_for(gram_name, args.config)}
     else:
         achieved = work[dom]["bytes"] / t_dom / 1e9
@@ -462,6 +597,12 @@ def run_ours(args):
                          "step's compute (two device buffers)"}
         del Xd, yd, dsets
 
+    configs = None
+    if not args.no_configs and args.m is None and args.flags == 0:
+        del data, ws
+        torch.cuda.empty_cache()
+        configs = extra_configs(args, torch, casgd, rank, pk)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_sample(args.config, s)
@@ -481,7 +622,7 @@ def run_ours(args):
                "gram_tflops": stages_out["gram"]["TFLOP/s"],
                "final_loss": hist[0] if hist else None,
                "clocks": clocks.summary(), "e2e": e2e, "cpu_baseline": cpu,
-               "fp32_sgd": sgd}
+               "fp32_sgd": sgd, "configs": configs}
         print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()

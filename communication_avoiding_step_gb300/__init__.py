@@ -8,13 +8,14 @@ every call raise.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes as C
 from dataclasses import dataclass
 
 import torch
 
 from ._native import (  # noqa: F401
-    CASGD_LOGISTIC, CASGD_LSQ, CASGD_POISSON, FLAG_GRAM_MULTICAST, FLAG_GRAM_NO_CLUSTER,
+    CASGD_LOGISTIC, CASGD_LSQ, CASGD_POISSON, ExchangeFn as _ExchangeFn, FLAG_GRAM_NO_CLUSTER,
     FLAG_FAR_FROM_GRAM, FLAG_FULL_G, FLAG_GRAM_PAIR, FLAG_SAMPLE_PERMUTED, FLAG_NO_FUSE,
     FLAG_TRACE_CHAIN, FLAG_MARGINS_FP32, FLAG_G_BF16,
     FLAG_GRAM_SIMT,
@@ -238,9 +239,119 @@ def update_static(Y: torch.Tensor, alpha: torch.Tensor, w: torch.Tensor, n: int,
     size limit and the rule that overlapping calls must be serialised).  Y is the BF16
     S x ldY matrix of the gathered rows, alpha FP32[S], w FP32[n] updated in place.
     """
+    # The library cannot see buffer lengths: refuse shapes that would let it read or
+    # write past a tensor before anything is called.
+    if not isinstance(Y, torch.Tensor) or Y.dim() != 2:
+        raise ValueError("Y must be a 2-D S x ldY tensor")
+    S, ldY = int(Y.shape[0]), int(Y.shape[1])
+    n = int(n)
+    if not 1 <= n <= ldY:
+        raise ValueError(f"n must be in [1, ldY = {ldY}], got {n}")
+    if not isinstance(alpha, torch.Tensor) or alpha.numel() < S:
+        raise ValueError(f"alpha must hold at least S = {S} values")
+    if not isinstance(w, torch.Tensor) or w.numel() < n:
+        raise ValueError(f"w must hold at least n = {n} values")
     _need_cuda(Y, "Y", torch.bfloat16)
     _need_cuda(alpha, "alpha", torch.float32)
     _need_cuda(w, "w", torch.float32)
-    S, ldY = int(Y.shape[0]), int(Y.shape[1])
-    _check(load().casgd_update_static(_ptr(Y), S, int(n), ldY, _ptr(alpha), _ptr(w),
+    _check(load().casgd_update_static(_ptr(Y), S, n, ldY, _ptr(alpha), _ptr(w),
                                       _stream(stream)), "casgd_update_static")
+
+
+# ----------------------------------------------------- feature-sharded outer iteration
+def exchange_elems(b: int, s: int, flags: int = 0) -> int:
+    """Floats of the exchange buffer: the packed block-lower G, then S margins."""
+    v = int(load().casgd_exchange_elems(b, s, flags))
+    if v < 0:
+        raise ValueError("invalid (b, s, flags)")
+    return v
+
+
+def workspace_sharded(data: Dataset, params: Params, stream=None) -> torch.Tensor:
+    """A fresh, initialised workspace for the sharded calls on this process's slice."""
+    nbytes = C.c_size_t(0)
+    _check(load().casgd_workspace_size_sharded(C.byref(data.c()), C.byref(params.c()),
+                                               C.byref(nbytes)), "casgd_workspace_size_sharded")
+    ws = torch.empty(int(nbytes.value), dtype=torch.uint8, device=data.X.device)
+    _check(load().casgd_workspace_init(_ptr(ws), ws.numel(), _stream(stream)),
+           "casgd_workspace_init")
+    return ws
+
+
+def exchange_buffer(params: Params, device="cuda") -> torch.Tensor:
+    """The caller-owned FP32 exchange buffer (torch allocations are 256-byte aligned)."""
+    return torch.zeros(exchange_elems(params.b, params.s, params.flags), dtype=torch.float32,
+                       device=device)
+
+
+def outer_step_local(data: Dataset, params: Params, w: torch.Tensor, k: int, ws: torch.Tensor,
+                     xbuf: torch.Tensor, taps: Taps | None = None, stream=None) -> None:
+    """First half of sharded outer iteration k: this slice's partial G and margins into
+    xbuf.  Sum xbuf over the processes, then call outer_step_finish.  Asynchronous."""
+    _need_cuda(w, "w", torch.float32)
+    _need_cuda(xbuf, "xbuf", torch.float32)
+    if xbuf.numel() < exchange_elems(params.b, params.s, params.flags):
+        raise ValueError("xbuf is smaller than exchange_elems(b, s, flags)")
+    t = C.byref(taps.c()) if taps is not None else None
+    _check(load().casgd_outer_step_local(C.byref(data.c()), C.byref(params.c()), _ptr(w), k,
+                                         _ptr(ws), ws.numel(), _stream(stream), _ptr(xbuf), t),
+           "casgd_outer_step_local")
+
+
+def outer_step_finish(data: Dataset, params: Params, w: torch.Tensor, ws: torch.Tensor,
+                      xbuf: torch.Tensor, taps: Taps | None = None, stream=None) -> None:
+    """Second half: the recurrence on the summed xbuf and this slice's update of w."""
+    _need_cuda(w, "w", torch.float32)
+    _need_cuda(xbuf, "xbuf", torch.float32)
+    if xbuf.numel() < exchange_elems(params.b, params.s, params.flags):
+        raise ValueError("xbuf is smaller than exchange_elems(b, s, flags)")
+    t = C.byref(taps.c()) if taps is not None else None
+    _check(load().casgd_outer_step_finish(C.byref(data.c()), C.byref(params.c()), _ptr(w),
+                                          _ptr(ws), ws.numel(), _stream(stream), _ptr(xbuf), t),
+           "casgd_outer_step_finish")
+
+
+def make_exchange(xbuf: torch.Tensor, all_reduce):
+    """The exchange hook the C loop calls once per outer iteration, as a Python callable
+    (ctx, buf, count, stream) -> int: it sums xbuf[:count] in place over the processes
+    with all_reduce (for example torch.distributed.all_reduce, which on an NCCL process
+    group is ncclAllReduce with ncclSum), ordered on the library's stream.  Returns 0, or
+    1 when the buffer is not xbuf or all_reduce raised (the loop then stops with
+    CASGD_ERR_EXCHANGE)."""
+    def hook(ctx, buf, count, stream_ptr):
+        try:
+            if buf != xbuf.data_ptr() or not 0 <= count <= xbuf.numel():
+                return 1
+            view = xbuf[:count]
+            ctxm = (torch.cuda.stream(torch.cuda.ExternalStream(stream_ptr))
+                    if xbuf.is_cuda and stream_ptr else contextlib.nullcontext())
+            with ctxm:
+                all_reduce(view)
+            return 0
+        except Exception:  # noqa: BLE001 -- reported to the C loop as a failed exchange
+            return 1
+    return hook
+
+
+def train_sharded(data: Dataset, params: Params, w: torch.Tensor, iters: int, ws: torch.Tensor,
+                  xbuf: torch.Tensor, all_reduce, k0: int = 0, stream=None, stage_events=None):
+    """`iters` feature-sharded outer iterations on this process's slice (data: its columns
+    of X and the full y; w: its slice).  all_reduce(t) must sum the FP32 tensor t in
+    place over the processes (None: one process, the identity).  Blocks; returns
+    (launches, gram_kind)."""
+    _need_cuda(w, "w", torch.float32)
+    _need_cuda(xbuf, "xbuf", torch.float32)
+    if xbuf.numel() < exchange_elems(params.b, params.s, params.flags):
+        raise ValueError("xbuf is smaller than exchange_elems(b, s, flags)")
+    hook = _ExchangeFn(make_exchange(xbuf, all_reduce if all_reduce is not None
+                                     else (lambda t: None)))
+    prof = _Profile()
+    ev_arr = None
+    if stage_events is not None:
+        ev_arr = (C.c_void_p * len(stage_events))(*[e.cuda_event for e in stage_events])
+        prof.stage_events = C.cast(ev_arr, C.POINTER(C.c_void_p))
+        prof.n_events = len(stage_events)
+    _check(load().casgd_train_sharded(C.byref(data.c()), C.byref(params.c()), _ptr(w), k0, iters,
+                                      _ptr(ws), ws.numel(), _stream(stream), _ptr(xbuf), hook,
+                                      None, C.byref(prof)), "casgd_train_sharded")
+    return int(prof.launches), int(prof.gram_kind)

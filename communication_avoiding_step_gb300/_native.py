@@ -12,12 +12,12 @@ HEADER = os.path.join(ROOT, "include", "casgd.h")
 
 CASGD_LOGISTIC, CASGD_LSQ, CASGD_POISSON = 0, 1, 2
 (CASGD_OK, CASGD_ERR_ARG, CASGD_ERR_WORKSPACE, CASGD_ERR_CUDA, CASGD_ERR_NONFINITE,
- CASGD_ERR_TIMEOUT, CASGD_ERR_BAD_INDEX, CASGD_ERR_UNSUPPORTED, CASGD_ERR_SCRATCH_LIMIT) = range(9)
+ CASGD_ERR_TIMEOUT, CASGD_ERR_BAD_INDEX, CASGD_ERR_UNSUPPORTED, CASGD_ERR_SCRATCH_LIMIT,
+ CASGD_ERR_EXCHANGE) = range(10)
 FLAG_WRITE_DIAG_BLOCKS = 0x1
 FLAG_GRAM_TENSOR = 0x2
 FLAG_GRAM_SIMT = 0x4
 FLAG_GRAM_NO_CLUSTER = 0x8
-FLAG_GRAM_MULTICAST = 0x10
 FLAG_GRAM_PAIR = 0x20
 FLAG_NO_FUSE = 0x40
 FLAG_TRACE_CHAIN = 0x100
@@ -51,6 +51,9 @@ class Profile(C.Structure):
 
 
 _P = C.POINTER
+# int (*casgd_exchange_fn)(void* ctx, float* buf, int64_t count, void* stream)
+ExchangeFn = C.CFUNCTYPE(C.c_int, C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p)
+
 SIGNATURES = {
     "casgd_strerror": (C.c_char_p, [C.c_int]),
     "casgd_version": (C.c_int, []),
@@ -81,6 +84,16 @@ SIGNATURES = {
                                  C.c_size_t, C.c_void_p]),
     "casgd_update_static": (C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_int64, C.c_void_p,
                                       C.c_void_p, C.c_void_p]),
+    "casgd_exchange_elems": (C.c_int64, [C.c_int32, C.c_int32, C.c_uint32]),
+    "casgd_workspace_size_sharded": (C.c_int, [_P(Data), _P(Params), _P(C.c_size_t)]),
+    "casgd_outer_step_local": (C.c_int, [_P(Data), _P(Params), C.c_void_p, C.c_uint64,
+                                         C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p,
+                                         _P(Taps)]),
+    "casgd_outer_step_finish": (C.c_int, [_P(Data), _P(Params), C.c_void_p, C.c_void_p,
+                                          C.c_size_t, C.c_void_p, C.c_void_p, _P(Taps)]),
+    "casgd_train_sharded": (C.c_int, [_P(Data), _P(Params), C.c_void_p, C.c_uint64, C.c_int32,
+                                      C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p,
+                                      ExchangeFn, C.c_void_p, _P(Profile)]),
 }
 
 _lib = None

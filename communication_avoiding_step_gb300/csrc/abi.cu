@@ -51,8 +51,16 @@ bool check_data(const casgd_data_t* d) {
   return true;
 }
 
+constexpr uint32_t kKnownFlags =
+    CASGD_FLAG_WRITE_DIAG_BLOCKS | CASGD_FLAG_GRAM_TENSOR | CASGD_FLAG_GRAM_SIMT |
+    CASGD_FLAG_GRAM_NO_CLUSTER | CASGD_FLAG_GRAM_PAIR | CASGD_FLAG_NO_FUSE |
+    CASGD_FLAG_TRACE_CHAIN | CASGD_FLAG_FAR_FROM_GRAM | CASGD_FLAG_FULL_G |
+    CASGD_FLAG_SAMPLE_PERMUTED | CASGD_FLAG_MARGINS_FP32 | CASGD_FLAG_G_BF16 |
+    CASGD_FLAG_TEST_STALL;
+
 bool check_params(const casgd_params_t* p) {
   if (!p) return false;
+  if (p->flags & ~kKnownFlags) return false;
   if (p->b < 1 || p->s < 1 || p->s > kMaxS) return false;
   if ((int64_t)p->b * p->s > kMaxSB) return false;
   if (p->loss < CASGD_LOGISTIC || p->loss > CASGD_POISSON) return false;
@@ -116,14 +124,12 @@ int gram_choice(const casgd_params_t* p, int64_t S, int64_t n) {
 }
 
 // Tensor-core variant (forced by a flag; else CTA pairs forming the far sums in the
-// recurrence's launch for b a multiple of 256; else CTA pairs with the recurrence in the
-// same launch while the chain's rows fit one warp each on half the SMs, b <= 512; else
-// CTA pairs for deep K (MMA-bound) and multicast clusters for shallow K (bound by
-// writing G), as measured on the five workloads) and whether the recurrence shares its
-// launch.
+// recurrence's launch for b a multiple of 256; else CTA pairs, sharing their launch with
+// the recurrence while the chain's rows fit one warp each on half the SMs, b <= 512) and
+// whether the recurrence shares its launch.
 struct GramPlan {
   int choice;  // 1 tensor cores, 2 CUDA cores, -1 unsupported
-  int mode;    // tensor cores: 0 pairs, 1 single CTA, 2 multicast clusters
+  int mode;    // tensor cores: 0 pairs, 1 single CTA
   bool fused;  // pairs sharing their launch with the recurrence
   bool far;    // ... and forming the far sums (CASGD_FLAG_FAR_FROM_GRAM)
 };
@@ -136,20 +142,19 @@ GramPlan gram_plan(int64_t n, int32_t b, int32_t s, uint32_t flags) {
   const int64_t S = (int64_t)b * s;
   GramPlan g;
   g.choice = gram_choice(&p, S, n);
-  const bool fuse_default = !(flags & CASGD_FLAG_NO_FUSE) && b <= 512 &&
-                            gram_recur_fused_supported(S, n, b);
-  g.mode = (flags & CASGD_FLAG_GRAM_NO_CLUSTER) ? 1
-           : (flags & CASGD_FLAG_GRAM_MULTICAST) ? 2
-           : (flags & CASGD_FLAG_GRAM_PAIR)      ? 0
-           : (fuse_default || n >= 1024) ? 0 : 2;
-  g.fused = g.choice == 1 && g.mode == 0 && !(flags & CASGD_FLAG_NO_FUSE) &&
+  g.mode = (flags & CASGD_FLAG_GRAM_NO_CLUSTER) ? 1 : 0;
+  // Without a variant flag the recurrence shares the pairs' launch for b <= 512 or deep K
+  // (n >= 1024); wide blocks over shallow K run the Gram and the recurrence as two
+  // launches (measured faster there: writing G bounds the Gram).
+  const bool fuse_shape = b <= 512 || n >= 1024 || (flags & CASGD_FLAG_GRAM_PAIR);
+  g.fused = g.choice == 1 && g.mode == 0 && !(flags & CASGD_FLAG_NO_FUSE) && fuse_shape &&
             gram_recur_fused_supported(S, n, b);
   // The far-forming Gram (pairs in the recurrence's launch, b % 256 == 0): the default
   // wherever it applies (measured faster than storing G on all five workloads), forced
   // by FAR_FROM_GRAM (which fails where it cannot apply), off with FULL_G or another
   // variant flag.
   const uint32_t other = CASGD_FLAG_GRAM_SIMT | CASGD_FLAG_GRAM_NO_CLUSTER |
-                         CASGD_FLAG_GRAM_MULTICAST | CASGD_FLAG_NO_FUSE | CASGD_FLAG_FULL_G;
+                         CASGD_FLAG_NO_FUSE | CASGD_FLAG_FULL_G;
   const bool far_ok = g.choice == 1 && !(flags & other) && far_gram_supported(S, n, b);
   g.far = far_ok;
   if (g.far) {
@@ -348,9 +353,96 @@ int read_and_clear_status(Ctrl* ctrl, cudaStream_t st) {
   return status_to_code(v);
 }
 
+// ---------------------------------------------------- feature-sharded outer iteration
+// The abstract's distributed setting: each process holds a slice of the features
+// (columns of X and of w), every process draws the same rows, and the only exchange of
+// an outer iteration is one sum over the processes of the sb x sb Gram matrix (with the
+// margins), in FP32.  The far sums of the recurrence need the summed G, so these calls
+// store G (the packed block-lower layout) into the caller's exchange buffer, followed
+// by the S partial margins as FP32 sums (rounded once to BF16 only after the sum).
+constexpr uint32_t kShardedUnsupported = CASGD_FLAG_FAR_FROM_GRAM | CASGD_FLAG_G_BF16;
+
+uint32_t sharded_flags(uint32_t f) { return f | CASGD_FLAG_FULL_G | CASGD_FLAG_NO_FUSE; }
+
+Layout sharded_layout(int64_t n, const casgd_params_t* p) {
+  return make_layout(n, p->b, p->s, sharded_flags(p->flags), 0, false);
+}
+
+int64_t exchange_elems_of(const casgd_params_t* p) {
+  return gram_elems(p->b, p->s, (p->flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0) +
+         (int64_t)p->b * p->s;
+}
+
+int check_xbuf(const float* xbuf) {
+  if (!xbuf || (reinterpret_cast<uintptr_t>(xbuf) % kAlign) != 0) return CASGD_ERR_ARG;
+  return CASGD_OK;
+}
+
+int sharded_local_impl(const casgd_data_t* d, const casgd_params_t* p, const float* w,
+                       uint64_t k, void* ws, size_t ws_bytes, float* xbuf,
+                       const casgd_taps_t* taps, Ctx& c) {
+  if (p->flags & kShardedUnsupported) return CASGD_ERR_UNSUPPORTED;
+  const Layout L = sharded_layout(d->n, p);
+  int rc = check_ws(ws, ws_bytes, L);
+  if (rc != CASGD_OK) return rc;
+  if ((rc = check_xbuf(xbuf)) != CASGD_OK) return rc;
+  const Resolved R = resolve(ws, L);
+  casgd_params_t q = *p;
+  q.flags = sharded_flags(p->flags) | CASGD_FLAG_MARGINS_FP32;  // partial margins: FP32 sums
+  const GramPlan gp = gram_plan(d->n, p->b, p->s, q.flags);
+  if (gp.choice < 0) return CASGD_ERR_UNSUPPORTED;
+  float* G = xbuf;
+  float* r_part = xbuf + L.gram_elems;
+  c.pdl = false;
+  // rows, labels, indices, this slice's partial margins and the recurrence's reset
+  CK(launch_gather(*d, q, w, k, taps ? taps->idx_in : nullptr, R.idx, R.Y, L.ldY, r_part, R.yY,
+                   R.alpha, R.far, nullptr, R.ctrl, R.slab, GATHER_AND_MARGINS, c));
+  if (gp.choice == 1)
+    CK(launch_gram_tc(R.Y, L.S, d->n, L.ldY, p->b, p->s, q.flags, gp.mode, G, R.ctrl,
+                      p->timeout_us, c));
+  else
+    CK(launch_gram_simt(R.Y, L.S, d->n, L.ldY, p->b, p->s,
+                        (p->flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0, false, G, c));
+  if (taps && taps->idx_out)
+    CK(cudaMemcpyAsync(taps->idx_out, R.idx, L.S * sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                       c.stream));
+  return CASGD_OK;
+}
+
+int sharded_finish_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, void* ws,
+                        size_t ws_bytes, const float* xbuf, const casgd_taps_t* taps, Ctx& c) {
+  if (p->flags & kShardedUnsupported) return CASGD_ERR_UNSUPPORTED;
+  const Layout L = sharded_layout(d->n, p);
+  int rc = check_ws(ws, ws_bytes, L);
+  if (rc != CASGD_OK) return rc;
+  if ((rc = check_xbuf(xbuf)) != CASGD_OK) return rc;
+  const Resolved R = resolve(ws, L);
+  const uint32_t flags = sharded_flags(p->flags);
+  const bool r_fp32 = (p->flags & CASGD_FLAG_MARGINS_FP32) != 0;
+  c.pdl = false;
+  // the summed margins, rounded once (the recipe) or kept in FP32 (MARGINS_FP32)
+  CK(launch_sharded_margins(xbuf + L.gram_elems, L.S, r_fp32, R.r, c));
+  // recurrence on the summed G (identical on every process), then this slice's update
+  CK(launch_recur(xbuf, R.r, R.yY, R.alpha, R.far, R.slab, p->b, p->s, p->eta, p->loss, flags,
+                  p->timeout_us, R.ctrl, R.Y, L.ldY, d->n, R.upd, w, c));
+  if (taps) {
+    if (taps->r_out) {
+      if (r_fp32)
+        CK(cudaMemcpyAsync(taps->r_out, R.r, L.S * sizeof(float), cudaMemcpyDeviceToDevice,
+                           c.stream));
+      else
+        CK(launch_bf16_bits(R.r, L.S, taps->r_out, c));
+    }
+    if (taps->alpha_out)
+      CK(cudaMemcpyAsync(taps->alpha_out, R.alpha, L.S * sizeof(float),
+                         cudaMemcpyDeviceToDevice, c.stream));
+  }
+  return CASGD_OK;
+}
+
 }  // namespace
 
-Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms) {
+Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms, bool with_G) {
   (void)num_sms;
   Layout L;
   L.S = (int64_t)b * s;
@@ -381,8 +473,8 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms)
   const int64_t upd_fused = (int64_t)s * upd_row_parts(b, L.ldY);
   const int64_t upd_rows = L.upd_ctas > upd_fused ? L.upd_ctas : upd_fused;
   off += align_up((size_t)upd_rows * L.ldY * sizeof(float));
-  L.off_G = off;
-  off += align_up((size_t)L.gram_elems * sizeof(float));
+  L.off_G = with_G ? off : 0;
+  if (with_G) off += align_up((size_t)L.gram_elems * sizeof(float));
   L.off_Y2 = L.off_G2 = L.off_idx2 = L.off_yY2 = L.off_fpart = 0;
   const GramPlan gp = gram_plan(n, b, s, flags);
   if (gp.fused) {  // casgd_train gathers the rows (and runs the Gram) one iteration ahead
@@ -423,6 +515,7 @@ const char* casgd_strerror(int code) {
     case CASGD_ERR_BAD_INDEX: return "a given row index is outside [0, m)";
     case CASGD_ERR_UNSUPPORTED: return "request not supported by this build";
     case CASGD_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of casgd_update_static";
+    case CASGD_ERR_EXCHANGE: return "the caller's exchange (sum over processes) reported a failure";
     default: return "unknown casgd status";
   }
 }
@@ -560,6 +653,77 @@ int casgd_train(const casgd_data_t* data, const casgd_params_t* params, float* w
                        cudaMemcpyDeviceToHost, c.stream));
   if (prof) prof->launches = c.launches;
   return read_and_clear_status(R.ctrl, c.stream);
+}
+
+int64_t casgd_exchange_elems(int32_t b, int32_t s, uint32_t flags) {
+  casgd_params_t p{};
+  p.b = b;
+  p.s = s;
+  p.flags = flags;
+  p.eta = 0.0f;
+  if (!check_params(&p)) return -1;
+  return exchange_elems_of(&p);
+}
+
+int casgd_workspace_size_sharded(const casgd_data_t* data, const casgd_params_t* params,
+                                 size_t* bytes) {
+  if (!bytes || !check_params(params)) return CASGD_ERR_ARG;
+  if (!data || data->n < 1 || data->n > kMaxN) return CASGD_ERR_ARG;
+  if (params->flags & kShardedUnsupported) return CASGD_ERR_UNSUPPORTED;
+  *bytes = sharded_layout(data->n, params).total;
+  return CASGD_OK;
+}
+
+int casgd_outer_step_local(const casgd_data_t* data, const casgd_params_t* params,
+                           const float* w, uint64_t k, void* ws, size_t ws_bytes, void* stream,
+                           float* xbuf, const casgd_taps_t* taps) {
+  if (!check_data(data) || !check_params(params) || !w) return CASGD_ERR_ARG;
+  Ctx c{static_cast<cudaStream_t>(stream), 0, 0};
+  if (device_sms(&c.num_sms) != CASGD_OK) return CASGD_ERR_CUDA;
+  return sharded_local_impl(data, params, w, k, ws, ws_bytes, xbuf, taps, c);
+}
+
+int casgd_outer_step_finish(const casgd_data_t* data, const casgd_params_t* params, float* w,
+                            void* ws, size_t ws_bytes, void* stream, const float* xbuf,
+                            const casgd_taps_t* taps) {
+  if (!check_data(data) || !check_params(params) || !w) return CASGD_ERR_ARG;
+  Ctx c{static_cast<cudaStream_t>(stream), 0, 0};
+  if (device_sms(&c.num_sms) != CASGD_OK) return CASGD_ERR_CUDA;
+  return sharded_finish_impl(data, params, w, ws, ws_bytes, xbuf, taps, c);
+}
+
+int casgd_train_sharded(const casgd_data_t* data, const casgd_params_t* params, float* w,
+                        uint64_t k0, int32_t iters, void* ws, size_t ws_bytes, void* stream,
+                        float* xbuf, casgd_exchange_fn exchange, void* exchange_ctx,
+                        casgd_profile_t* prof) {
+  if (!check_data(data) || !check_params(params) || !w || iters < 0 || !exchange)
+    return CASGD_ERR_ARG;
+  LaunchCache cache;
+  Ctx c{static_cast<cudaStream_t>(stream), 0, 0, &cache};
+  if (device_sms(&c.num_sms) != CASGD_OK) return CASGD_ERR_CUDA;
+  const int64_t count = exchange_elems_of(params);
+  if (params->flags & kShardedUnsupported) return CASGD_ERR_UNSUPPORTED;
+  int rc = check_ws(ws, ws_bytes, sharded_layout(data->n, params));
+  if (rc != CASGD_OK) return rc;
+  if ((rc = check_xbuf(xbuf)) != CASGD_OK) return rc;
+  for (int32_t it = 0; it < iters; ++it) {
+    if ((rc = record(prof, it, 0, c.stream)) != CASGD_OK) return rc;
+    rc = sharded_local_impl(data, params, w, k0 + (uint64_t)it, ws, ws_bytes, xbuf, nullptr, c);
+    if (rc != CASGD_OK) return rc;
+    if ((rc = record(prof, it, 1, c.stream)) != CASGD_OK) return rc;
+    // the one exchange of the outer iteration, issued by the caller on `stream`
+    if (exchange(exchange_ctx, xbuf, count, stream) != 0) return CASGD_ERR_EXCHANGE;
+    if ((rc = record(prof, it, 2, c.stream)) != CASGD_OK) return rc;
+    rc = sharded_finish_impl(data, params, w, ws, ws_bytes, xbuf, nullptr, c);
+    if (rc != CASGD_OK) return rc;
+    if ((rc = record(prof, it, 3, c.stream)) != CASGD_OK) return rc;
+    if ((rc = record(prof, it, 4, c.stream)) != CASGD_OK) return rc;
+  }
+  if (prof) {
+    prof->launches = c.launches;
+    prof->gram_kind = 7;
+  }
+  return read_and_clear_status(static_cast<Ctrl*>(ws), c.stream);
 }
 
 int casgd_get_status(void* ws, void* stream) {

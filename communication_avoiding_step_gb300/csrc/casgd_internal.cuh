@@ -79,7 +79,10 @@ struct Layout {
   size_t total;
 };
 
-Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms);
+// with_G: false for the feature-sharded calls, whose G lives in the caller's exchange
+// buffer
+Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms,
+                   bool with_G = true);
 
 inline int64_t gram_elems(int64_t b, int64_t s, bool diag) {
   int64_t nblk = diag ? s * (s + 1) / 2 : s * (s - 1) / 2;
@@ -335,6 +338,10 @@ cudaError_t launch_store_bf16(const float* src, int64_t m, int64_t n, int64_t ld
                               uint16_t* dst, int64_t ld_dst, Ctx& c);
 // dst[i] = the BF16 bits of src[i] (values already BF16-representable: exact)
 cudaError_t launch_bf16_bits(const float* src, int64_t count, uint16_t* dst, Ctx& c);
+// dst[i] = src[i] rounded once to BF16 (as FP32), or src[i] itself (fp32): the summed
+// partial margins of a feature-sharded outer iteration as the recurrence reads them
+cudaError_t launch_sharded_margins(const float* src, int64_t count, bool fp32, float* dst,
+                                   Ctx& c);
 // permuted: without replacement (per-epoch permutation), else with replacement
 cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t counter0,
                           bool permuted, int32_t* idx, Ctx& c);

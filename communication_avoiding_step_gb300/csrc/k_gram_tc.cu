@@ -17,12 +17,9 @@
 //               stores of the rows/columns that belong to needed blocks into the packed
 //               block-lower G.  Two accumulators let the epilogue of one tile overlap
 //               the MMAs of the next.
-// Variants: the paired-SM kernel below (default); a single-CTA kernel (kCl = 1); and a
-// cluster variant (kCl = 2): the two CTAs of a cluster compute row tiles
-// 2g and 2g+1 against the same B tile; each loads one 128-row half of B and multicasts
-// it to both, so a CTA pulls 32 KB instead of 48 KB from L2 per 64 columns of K.  A
-// stage is refilled only after both CTAs' MMAs have read it (each MMA warp's commit
-// arrives on the stage's empty barrier in both CTAs).
+// Variants: the paired-SM kernel below (default) and this single-CTA kernel.  Every
+// TMA copy lands in the shared memory of the CTA that issues it (no cluster multicast),
+// so the same code runs unchanged in processes that each drive their own GPU.
 // Both operands are K-major slices of the same Y (rows are samples, K the features);
 // out-of-range rows and columns of K are zero-filled by TMA.  Tiles of the S x S
 // product are visited row-tile by row-tile, skipping tiles wholly above the needed
@@ -34,6 +31,7 @@
 #include <cstring>
 
 #include "casgd_internal.cuh"
+#include "ptx_async.cuh"
 #include "recur_roles.cuh"
 
 namespace casgd {
@@ -86,35 +84,6 @@ struct SharedCtl {
   volatile uint32_t abort;
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Bounded wait: false (and the CTA's abort word set) if the phase does not complete in
 // time or another role of this CTA already gave up.
 __device__ bool mbar_wait(uint64_t* bar, uint32_t parity, SharedCtl* sc, const TcArgs& a) {
@@ -137,17 +106,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-      : "memory");
-}
-
-// The same copy written to the same offset in every CTA of `mask` (this GPU's memory).
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map,
-                                               uint64_t* bar, int32_t x, int32_t y,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
       : "memory");
 }
 
@@ -198,16 +156,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// Arrives on the barrier at the same offset in every CTA of `mask` once this thread's
-// earlier MMAs have completed.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -241,8 +189,9 @@ __device__ __forceinline__ int cols_needed(const TcArgs& a, int ra) {
   return (int)(c < a.TC ? c : a.TC);
 }
 
-// Column tiles of row group g (row tiles kCl*g .. kCl*g+kCl-1): those of its last row
-// tile, which needs the most (the count grows with the row).
+// Column tiles of row group g (row tiles kCl*g .. kCl*g+kCl-1; kCl = 1 for the
+// single-CTA kernel, 2 for CTA pairs): those of its last row tile, which needs the
+// most (the count grows with the row).
 template <int kCl>
 __device__ __forceinline__ int group_cols(const TcArgs& a, int g) {
   if (kCl == 2) return pair_group_tiles(a.S, a.b, a.diag, g);  // the count readers expect
@@ -444,7 +393,8 @@ __device__ __forceinline__ void store_tile_rows(const TcArgs& a, uint32_t tmem, 
   }
 }
 
-template <int kCl>
+// Single-CTA variant: one CTA per 128x256 tile, A and both halves of B loaded by the
+// CTA itself (48 KB per stage).
 __global__ void __launch_bounds__(kThreads, 1)
     gram_tc_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmG,
                    TcArgs a) {
@@ -454,14 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* out_stage = smem + (size_t)kStages * kStageBytes;  // 1024-aligned
   SharedCtl* sc = reinterpret_cast<SharedCtl*>(out_stage + kOutBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = kCl == 2 ? (int)cluster_rank() : 0;
-  const int cid = blockIdx.x / kCl, ncl = gridDim.x / kCl;  // cluster id, clusters
-  constexpr uint16_t kMask = (uint16_t)((1u << kCl) - 1u);
+  const int cid = blockIdx.x, ncl = gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sc->full[i], 1);
-      mbar_init(&sc->empty[i], kCl);
+      mbar_init(&sc->empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sc->tfull[i], 1);
@@ -480,14 +428,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (kCl > 1) cluster_sync();  // peers' barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem = sc->tmem_base;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
-      TileCursor<kCl> cur;
+      TileCursor<1> cur;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;  // bit st: a load into stage st was issued; its parity below
@@ -495,22 +442,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = cid; tile < a.ntiles && !sc->abort; tile += ncl) {
         int rg, ca;
         cur.seek(a, tile, rg, ca);
-        const int ra = kCl * rg + rank;
+        const int ra = rg;
         for (int kb = 0; kb < a.nkb; ++kb) {
           if (!mbar_wait(&sc->empty[stage], phase ^ 1u, sc, a)) break;
           uint8_t* sa = smem + (size_t)stage * kStageBytes;
           uint8_t* sb = sa + kABytes;
-          // this CTA's A, and (with the peer) both halves of B: 48 KB land per stage
+          // the tile's A and both halves of B: 48 KB land per stage
           mbar_expect_tx(&sc->full[stage], kStageBytes);
           tma_load_2d(smem_u32(sa), &tmY, &sc->full[stage], kb * BK, ra * BM);
-          if (kCl == 1) {
-            tma_load_2d(smem_u32(sb), &tmY, &sc->full[stage], kb * BK, ca * BN);
-            tma_load_2d(smem_u32(sb + kBBytes / 2), &tmY, &sc->full[stage], kb * BK,
-                        ca * BN + BN / 2);
-          } else {
-            tma_load_2d_mc(smem_u32(sb + rank * (kBBytes / 2)), &tmY, &sc->full[stage],
-                           kb * BK, ca * BN + rank * (BN / 2), kMask);
-          }
+          tma_load_2d(smem_u32(sb), &tmY, &sc->full[stage], kb * BK, ca * BN);
+          tma_load_2d(smem_u32(sb + kBBytes / 2), &tmY, &sc->full[stage], kb * BK,
+                      ca * BN + BN / 2);
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -555,10 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16(tacc, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
                      (kb > 0 || kk > 0) ? 1u : 0u);
           any = true;
-          if (kCl == 1)
-            mma_commit(&sc->empty[stage]);
-          else
-            mma_commit_mc(&sc->empty[stage], kMask);
+          mma_commit(&sc->empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -579,13 +518,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     uint8_t* stage = out_stage + (warp - 2) * kStageOut;
     int sbuf = 0;
-    TileCursor<kCl> cur;
+    TileCursor<1> cur;
     uint32_t tphase[2] = {0, 0};
     int iter = 0;
     for (int tile = cid; tile < a.ntiles; tile += ncl, ++iter) {
       int rg, ca;
       cur.seek(a, tile, rg, ca);
-      const int ra = kCl * rg + rank;
+      const int ra = rg;
       const int acc = iter & 1;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&sc->tfull[acc], tphase[acc], sc, a) ? 1 : 0;
@@ -604,7 +543,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (kCl > 1) cluster_sync();  // no peer copy or commit still targets this CTA
   tc_fence_after();
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -1203,9 +1141,10 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
                            uint32_t flags, int mode, float* G, Ctrl* ctrl, uint32_t timeout_us,
                            Ctx& c) {
   if (S <= 0) return cudaSuccess;
-  // mode 0: paired-SM MMA (default); 1: one CTA per tile; 2: 2-CTA clusters sharing B
-  // by multicast.  A single row tile always runs on one CTA.
+  // mode 0: paired-SM MMA (default); 1: one CTA per tile.  A single row tile always runs
+  // on one CTA.
   if ((S + BM - 1) / BM <= 1) mode = 1;
+  if (mode != 0 && mode != 1) return cudaErrorInvalidValue;
   const int kcl = mode == 1 ? 1 : 2;
   TcPlan P;
   cudaError_t e = plan_tc(Y, S, n, ldY, b, s, flags, kcl, G, ctrl, timeout_us, P);
@@ -1214,17 +1153,16 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
   if (a.ntiles == 0) return cudaSuccess;
 
   if (mode == 1) {
-    e = cudaFuncSetAttribute(gram_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(gram_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = a.ntiles < c.num_sms ? a.ntiles : c.num_sms;
-    gram_tc_kernel<1><<<grid, kThreads, kSmemBytes, c.stream>>>(P.map, P.mapG, a);
+    gram_tc_kernel<<<grid, kThreads, kSmemBytes, c.stream>>>(P.map, P.mapG, a);
     ++c.launches;
     return cudaGetLastError();
   }
-  const void* fn = mode == 0 ? (const void*)gram_tc2sm_kernel<kStagesPair, 0, false, false>
-                             : (const void*)gram_tc_kernel<2>;
-  const size_t smem = mode == 0 ? pair_smem_bytes<kStagesPair>() : kSmemBytes;
+  const void* fn = (const void*)gram_tc2sm_kernel<kStagesPair, 0, false, false>;
+  const size_t smem = pair_smem_bytes<kStagesPair>();
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster2_config(kThreads, smem, c.stream, attr);
   cfg.gridDim = dim3(2 * (unsigned)(c.num_sms / 2));
@@ -1238,14 +1176,10 @@ cudaError_t launch_gram_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY,
   if (e != cudaSuccess) return e;
   const int clusters = a.ntiles < max_clusters ? a.ntiles : max_clusters;
   cfg.gridDim = dim3(2 * (unsigned)clusters);
-  if (mode == 0) {
-    RecArgs none;
-    memset(&none, 0, sizeof(none));
-    e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel<kStagesPair, 0, false, false>, P.map, P.mapG,
-                           P.map, a, none);
-  } else {
-    e = cudaLaunchKernelEx(&cfg, gram_tc_kernel<2>, P.map, P.mapG, a);
-  }
+  RecArgs none;
+  memset(&none, 0, sizeof(none));
+  e = cudaLaunchKernelEx(&cfg, gram_tc2sm_kernel<kStagesPair, 0, false, false>, P.map, P.mapG,
+                         P.map, a, none);
   ++c.launches;
   return e;
 }

@@ -45,6 +45,15 @@ __global__ void bf16_bits_kernel(const float* __restrict__ src, int64_t count,
     dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(src[i]));
 }
 
+// The summed margins of a feature-sharded outer iteration (FP32 partial sums, added
+// over the ranks) as the recurrence reads them: rounded once to BF16, or kept (fp32).
+__global__ void sharded_margins_kernel(const float* __restrict__ src, int64_t count, bool fp32,
+                                       float* __restrict__ dst) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count;
+       i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = fp32 ? src[i] : round_bf16(src[i]);
+}
+
 __global__ void sample_kernel(uint32_t m, int64_t count, uint64_t seed, uint64_t counter0,
                               int perm_d, int32_t* __restrict__ idx) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count;
@@ -291,6 +300,16 @@ cudaError_t launch_bf16_bits(const float* src, int64_t count, uint16_t* dst, Ctx
   int64_t blocks = (count + 255) / 256;
   if (blocks > (int64_t)c.num_sms * 8) blocks = (int64_t)c.num_sms * 8;
   bf16_bits_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>(src, count, dst);
+  ++c.launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sharded_margins(const float* src, int64_t count, bool fp32, float* dst,
+                                   Ctx& c) {
+  if (count == 0) return cudaSuccess;
+  int64_t blocks = (count + 255) / 256;
+  if (blocks > (int64_t)c.num_sms * 8) blocks = (int64_t)c.num_sms * 8;
+  sharded_margins_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>(src, count, fp32, dst);
   ++c.launches;
   return cudaGetLastError();
 }

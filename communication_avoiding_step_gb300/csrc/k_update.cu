@@ -10,6 +10,7 @@
 // kernel sums them column by column; the loss keeps FP32 per-row values, FP64 per-CTA
 // partials, and the last CTA to finish sums the partials in CTA order.
 #include "casgd_internal.cuh"
+#include "ptx_async.cuh"
 
 namespace casgd {
 
@@ -124,111 +125,179 @@ __global__ void __launch_bounds__(256) update_reduce_kernel(const float* __restr
   }
 }
 
-// Loss: groups of G lanes per row (as in the gather), grid-stride over rows; w is
-// staged in shared memory once per CTA, and each warp issues its next row's loads
-// before it sums the current row.
-__global__ void __launch_bounds__(256, 2) loss_kernel(const uint16_t* __restrict__ X,
-                                                   const float* __restrict__ y, int64_t m,
-                                                   int64_t n, int64_t ld, int loss,
-                                                   const float* __restrict__ w,
-                                                   double* __restrict__ part,
-                                                   double* __restrict__ out, Ctrl* ctrl,
-                                                   int G) {
-  __shared__ double red[8];
-  __shared__ bool s_last;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane & (G - 1);
-  const int rows_per_warp = 32 / G;
-  const int64_t nvec = (n + 7) / 8;
-  const int64_t rows_per_pass = (int64_t)gridDim.x * 8 * rows_per_warp;
-  constexpr int kBatch = 8;
-  extern __shared__ __align__(16) float w_s[];  // w, zero padded to a multiple of 8
-  for (int64_t c = threadIdx.x; c < nvec * 8; c += blockDim.x) w_s[c] = c < n ? w[c] : 0.0f;
-  __syncthreads();
-  double mine = 0.0;
-  // FP32 dot of row `row` with w from the kBatch vectors in q starting at vector v0
-  auto dot_batch = [&](const uint4 (&q)[kBatch], int64_t v0, float acc) {
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int64_t c0 = (v0 + (int64_t)u * G) * 8;
-      if (c0 >= n) break;
-      float wv[8];
-      const float4 w0 = *reinterpret_cast<const float4*>(w_s + c0);
-      const float4 w1 = *reinterpret_cast<const float4*>(w_s + c0 + 4);
-      wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
-      wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
-      const uint32_t pw[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-      if (c0 + 8 <= n) {  // the whole vector holds features
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          acc = fmaf(__uint_as_float(pw[h] << 16), wv[2 * h], acc);
-          acc = fmaf(__uint_as_float(pw[h] & 0xFFFF0000u), wv[2 * h + 1], acc);
-        }
-      } else {
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int64_t c = c0 + 2 * h;
-          if (c < n) acc = fmaf(bf16_bits_to_float(pw[h] & 0xFFFFu), wv[2 * h], acc);
-          if (c + 1 < n) acc = fmaf(bf16_bits_to_float(pw[h] >> 16), wv[2 * h + 1], acc);
-        }
-      }
-    }
-    return acc;
-  };
-  auto load_batch = [&](uint4 (&q)[kBatch], int64_t row, int64_t v0) {
-    const uint16_t* xr = X + row * ld;
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int64_t v = v0 + (int64_t)u * G;
-      q[u] = (row < m && v < nvec) ? __ldg(reinterpret_cast<const uint4*>(xr + v * 8))
-                                   : make_uint4(0, 0, 0, 0);
-    }
-  };
-  auto finish_row = [&](float acc, int64_t row) {
-    for (int off = G >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);
-    if (row < m && g == 0) mine += (double)loss_value(loss, acc, __ldg(y + row));
-  };
-  const int64_t first = ((int64_t)blockIdx.x * 8 + warp) * rows_per_warp + lane / G;
-  if (nvec <= (int64_t)G * kBatch) {
-    // one batch per row: the next row's loads are issued before this row is summed
-    uint4 q[kBatch], qn[kBatch];
-    load_batch(q, first, g);
-    for (int64_t row = first; row - lane / G < m; row += rows_per_pass) {
-      load_batch(qn, row + rows_per_pass, g);
-      finish_row(dot_batch(q, g, 0.0f), row);
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) q[u] = qn[u];
-    }
-  } else {
-    for (int64_t row = first; row - lane / G < m; row += rows_per_pass) {
-      float acc = 0.0f;
-      // Issue up to kBatch 16-byte loads of the row before using any of them.
-      for (int64_t v0 = g; v0 < nvec; v0 += (int64_t)G * kBatch) {
-        uint4 q[kBatch];
-        load_batch(q, row, v0);
-        acc = dot_batch(q, v0, acc);
-      }
-      finish_row(acc, row);
+// Loss: the rows are streamed, never gathered -- each CTA owns a contiguous range of
+// rows, and because X is row-major with a 16-byte-multiple pitch, R consecutive rows are
+// one contiguous block that a single bulk copy (cp.async.bulk) moves into shared memory.
+// A producer lane keeps nst such stages in flight (a shared-memory ring with full/empty
+// barriers), so the bytes in flight per SM do not cost registers; eight consumer warps
+// take G lanes per row from the landed stage: lane g sums the row's 16-byte vectors g,
+// g+G, ... with w (staged in shared memory once), the row's lanes add by a shuffle tree,
+// and the row's loss is added in FP64.  Per row the FP32 dot product has the same order
+// as the margins.  Every wait is bounded; on expiry the CTA records ST_TIMEOUT, stops
+// consuming, and its producer waits (bounded) for its copies in flight before exiting.
+constexpr int kLossWarps = 8;                        // consumer warps
+constexpr int kLossThreads = 32 * (kLossWarps + 1);  // + one producer warp
+constexpr int kLossMaxStages = 8;
+constexpr uint32_t kLossStageBytes = 32 * 1024;
+
+struct LossArgs {
+  const uint16_t* X;
+  const float* y;
+  int64_t m, n, ld;
+  int loss, G;
+  int R;            // rows per stage
+  int nst;          // stages in the ring
+  uint32_t stage;   // bytes per stage slot (multiple of 128)
+  const float* w;
+  double* part;
+  double* out;
+  Ctrl* ctrl;
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ bool loss_wait(uint64_t* bar, uint32_t parity, const LossArgs& a,
+                                          volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > a.timeout_ns) {
+      *abort_flag = 1;
+      atomicOr(&a.ctrl->status, ST_TIMEOUT);
+      return false;
     }
   }
-  for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
-  if (lane == 0) red[warp] = mine;
+  return true;
+}
+
+__global__ void __launch_bounds__(kLossThreads, 1) loss_kernel(LossArgs a) {
+  extern __shared__ __align__(128) uint8_t loss_smem[];
+  __shared__ uint64_t full[kLossMaxStages], empty[kLossMaxStages];
+  __shared__ double red[kLossWarps];
+  __shared__ volatile int s_abort;
+  __shared__ bool s_last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t ldv = a.ld / 8;                         // 16-byte vectors per row
+  float* w_s = reinterpret_cast<float*>(loss_smem);     // ld floats, zero past n
+  uint8_t* ring = loss_smem + ((a.ld * 4 + 127) / 128) * 128;
+  const int64_t r_lo = a.m * blockIdx.x / gridDim.x;
+  const int64_t r_hi = a.m * (blockIdx.x + 1) / gridDim.x;
+  const int64_t nchunk = (r_hi - r_lo + a.R - 1) / a.R;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.nst; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kLossWarps);
+    }
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  for (int64_t c = threadIdx.x; c < a.ld; c += blockDim.x) w_s[c] = c < a.n ? a.w[c] : 0.0f;
+  __syncthreads();
+
+  double mine = 0.0;
+  if (warp == kLossWarps) {
+    // ---------------------------------------------------------------- producer lane
+    if (lane == 0) {
+      int64_t issued = 0;
+      for (int64_t ch = 0; ch < nchunk && !s_abort; ++ch) {
+        const int st = (int)(ch % a.nst);
+        const uint32_t ph = (uint32_t)((ch / a.nst) & 1);
+        if (!loss_wait(&empty[st], ph ^ 1u, a, &s_abort)) break;
+        const int64_t row0 = r_lo + ch * a.R;
+        const int64_t rows = r_hi - row0 < a.R ? r_hi - row0 : a.R;
+        const uint32_t bytes = (uint32_t)(rows * a.ld * 2);
+        mbar_expect_tx(&full[st], bytes);
+        bulk_load(ring + (size_t)st * a.stage, a.X + row0 * a.ld, bytes, &full[st]);
+        issued = ch + 1;
+      }
+      // every copy issued has landed before the CTA may exit
+      for (int64_t ch = issued - a.nst < 0 ? 0 : issued - a.nst; ch < issued; ++ch) {
+        const int st = (int)(ch % a.nst);
+        const uint32_t ph = (uint32_t)((ch / a.nst) & 1);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&full[st], ph) && globaltimer_ns() - t0 < a.timeout_ns) {
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- consumer warps
+    const int G = a.G;
+    const int g = lane & (G - 1);
+    const int rows_per_pass = kLossWarps * (32 / G);
+    const int my = warp * (32 / G) + lane / G;  // row slot within a pass
+    // the label of this lane's row in pass q0 of chunk ch (0 past the range): loaded one
+    // pass ahead, so its latency hides behind the stage wait and the previous pass
+    auto label = [&](int64_t ch, int q0) -> float {
+      const int64_t row = r_lo + ch * a.R + q0 + my;
+      const int64_t end = r_lo + (ch + 1) * a.R < r_hi ? r_lo + (ch + 1) * a.R : r_hi;
+      return (g == 0 && ch < nchunk && row < end) ? __ldg(a.y + row) : 0.0f;
+    };
+    float ycur = label(0, 0);
+    for (int64_t ch = 0; ch < nchunk; ++ch) {
+      const int st = (int)(ch % a.nst);
+      const uint32_t ph = (uint32_t)((ch / a.nst) & 1);
+      int ok = 1;
+      if (lane == 0) ok = loss_wait(&full[st], ph, a, &s_abort) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const int64_t row0 = r_lo + ch * a.R;
+      const int rows = (int)(r_hi - row0 < a.R ? r_hi - row0 : a.R);
+      const uint8_t* stg = ring + (size_t)st * a.stage;
+      for (int q0 = 0; q0 < rows; q0 += rows_per_pass) {  // warp-uniform
+        const int q = q0 + my;
+        const bool live = q < rows;
+        const float ynext = q0 + rows_per_pass < rows ? label(ch, q0 + rows_per_pass)
+                                                      : label(ch + 1, 0);
+        const uint4* xr = reinterpret_cast<const uint4*>(stg + (size_t)(live ? q : 0) * a.ld * 2);
+        float acc = 0.0f;
+        for (int64_t v = g; live && v < ldv; v += G) {
+          const int64_t c0 = v * 8;
+          if (c0 >= a.n) break;
+          const uint4 xv = xr[v];
+          const float4 w0 = *reinterpret_cast<const float4*>(w_s + c0);
+          const float4 w1 = *reinterpret_cast<const float4*>(w_s + c0 + 4);
+          const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          const uint32_t pw[4] = {xv.x, xv.y, xv.z, xv.w};
+          if (c0 + 8 <= a.n) {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              acc = fmaf(__uint_as_float(pw[h] << 16), wv[2 * h], acc);
+              acc = fmaf(__uint_as_float(pw[h] & 0xFFFF0000u), wv[2 * h + 1], acc);
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int64_t cc = c0 + 2 * h;
+              if (cc < a.n) acc = fmaf(bf16_bits_to_float(pw[h] & 0xFFFFu), wv[2 * h], acc);
+              if (cc + 1 < a.n) acc = fmaf(bf16_bits_to_float(pw[h] >> 16), wv[2 * h + 1], acc);
+            }
+          }
+        }
+        for (int off = G >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);
+        if (live && g == 0) mine += (double)loss_value(a.loss, acc, ycur);
+        ycur = ynext;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
+    }
+    for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
+    if (lane == 0) red[warp] = mine;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     double t = 0.0;
-    for (int q = 0; q < 8; ++q) t += red[q];
-    part[blockIdx.x] = t;
+    for (int q = 0; q < kLossWarps; ++q) t += red[q];
+    a.part[blockIdx.x] = t;
     __threadfence();
-    const uint32_t done = atomicAdd(&ctrl->loss_done, 1u);
+    const uint32_t done = atomicAdd(&a.ctrl->loss_done, 1u);
     s_last = (done == gridDim.x - 1);
   }
   __syncthreads();
   if (s_last && threadIdx.x == 0) {
     __threadfence();
     double t = 0.0;
-    for (unsigned q = 0; q < gridDim.x; ++q) t += __ldcg(part + q);
-    *out = t / (double)m;
-    ctrl->loss_done = 0;
+    for (unsigned q = 0; q < gridDim.x; ++q) t += __ldcg(a.part + q);
+    *a.out = t / (double)a.m;
+    a.ctrl->loss_done = 0;
   }
 }
 
@@ -271,32 +340,48 @@ cudaError_t launch_update_reduce(const float* part, int upd_ctas, int64_t n, int
 }
 
 int loss_ctas(int num_sms) {
-  int v = num_sms * 4;
+  int v = num_sms;
   return v > kLossCtas ? kLossCtas : v;
 }
 
 cudaError_t launch_loss(const casgd_data_t& d, int loss, const float* w, double* part,
                         double* out_dev, Ctrl* ctrl, Ctx& c) {
-  const int G = pow2_at_least((d.n + 7) / 8, 32);
-  const int64_t rows_per_cta = 8 * (32 / G);
-  int64_t blocks = (d.m + rows_per_cta - 1) / rows_per_cta;
-  const size_t smem = (size_t)((d.n + 7) / 8 * 8) * sizeof(float);
-  int per_sm = 0;
+  LossArgs a;
+  a.X = static_cast<const uint16_t*>(d.X);
+  a.y = d.y;
+  a.m = d.m;
+  a.n = d.n;
+  a.ld = d.ld;
+  a.loss = loss;
+  a.G = pow2_at_least(d.ld / 8, 32);
+  a.w = w;
+  a.part = part;
+  a.out = out_dev;
+  a.ctrl = ctrl;
+  a.timeout_ns = 1000000000ull;
+  // stages of at least one row, 128-byte aligned slots; as many as fit beside w
+  const size_t row_bytes = (size_t)d.ld * 2;
+  size_t stage = row_bytes > kLossStageBytes ? row_bytes : kLossStageBytes;
+  stage = (stage + 127) / 128 * 128;
+  a.R = (int)(stage / row_bytes);
+  a.stage = (uint32_t)stage;
+  const size_t w_bytes = ((size_t)d.ld * 4 + 127) / 128 * 128;
+  const size_t budget = 200 * 1024;
+  int nst = (int)((budget - w_bytes) / stage);
+  if (nst > 6) nst = 6;
+  if (nst < 2) return cudaErrorInvalidValue;  // (n <= 16384 keeps at least 3 stages)
+  a.nst = nst;
+  const size_t smem = w_bytes + (size_t)nst * stage;
+  int dummy = 0;
   cudaError_t e = cached_query(c, (const void*)loss_kernel, [&](int& v) {
-    if (smem > 48 * 1024) {
-      cudaError_t r = cudaFuncSetAttribute(loss_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (r != cudaSuccess) return r;
-    }
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, loss_kernel, 256, smem);
-  }, per_sm);
+    v = 1;
+    return cudaFuncSetAttribute(loss_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(220 * 1024));
+  }, dummy);
   if (e != cudaSuccess) return e;
-  int cap = (per_sm > 0 ? per_sm : 1) * c.num_sms;  // one resident wave
-  if (cap > loss_ctas(c.num_sms)) cap = loss_ctas(c.num_sms);
-  if (blocks > cap) blocks = cap;
-  loss_kernel<<<(unsigned)blocks, 256, smem, c.stream>>>(static_cast<const uint16_t*>(d.X), d.y,
-                                                         d.m, d.n, d.ld, loss, w, part, out_dev,
-                                                         ctrl, G);
+  int64_t blocks = loss_ctas(c.num_sms);
+  if (blocks > d.m) blocks = d.m;
+  loss_kernel<<<(unsigned)blocks, kLossThreads, smem, c.stream>>>(a);
   ++c.launches;
   return cudaGetLastError();
 }

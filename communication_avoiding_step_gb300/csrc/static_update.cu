@@ -18,6 +18,8 @@
 // partial rows are overwritten completely on every call; the status word is cleared
 // at the start of each call.  Calls whose kernels overlap on the GPU (for instance on
 // two streams at once) race on the array and must be serialised by the caller.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "casgd_internal.cuh"
@@ -32,22 +34,57 @@ constexpr int kMaxDevices = 64;
 // The fixed scratch: a control block followed by the partial rows.
 static __device__ __align__(256) float g_static_update_scratch[kStaticCtrlFloats + kStaticPartials];
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
 std::mutex g_addr_mutex;
 void* g_addr[kMaxDevices] = {};
+unsigned long long g_ctx_id[kMaxDevices] = {};  // context the address belongs to
+
+// Unique id (over the process's life) of the calling thread's current context, from the
+// driver API through the runtime's entry-point lookup; 0 if it cannot be found.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  if (!get_cur || !get_id) {
+    void* p1 = nullptr;
+    void* p2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p1, 12000, cudaEnableDefault,
+                                         &q1) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &p2, 12000, cudaEnableDefault, &q2) !=
+            cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess)
+      return 0;
+    get_cur = reinterpret_cast<CtxGetCurrentFn>(p1);
+    get_id = reinterpret_cast<CtxGetIdFn>(p2);
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_cur(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 // Device address of the scratch on the current device.  Host code only sees a host-side
-// stand-in under the array's name, so the address is looked up once per device with
-// that device current (the first call on each device does it).
+// stand-in under the array's name, so the address is looked up with that device current
+// (cudaGetSymbolAddress) the first time a call runs in a context of that device, and
+// kept with the context's unique id: a device reset (cudaDeviceReset) or a new primary
+// context in this process gives a new id, so the address is looked up again instead of
+// pointing into the old context's memory.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CASGD_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return CASGD_ERR_UNSUPPORTED;
+  const unsigned long long id = current_context_id();  // 0: no context bound yet
   std::lock_guard<std::mutex> lock(g_addr_mutex);
-  if (!g_addr[dev]) {
+  if (!g_addr[dev] || id == 0 || g_ctx_id[dev] != id) {
     void* p = nullptr;
+    // (binds the device's primary context first if the thread had none)
     if (cudaGetSymbolAddress(&p, g_static_update_scratch) != cudaSuccess || !p)
       return CASGD_ERR_CUDA;
     g_addr[dev] = p;
+    g_ctx_id[dev] = id ? id : current_context_id();
   }
   *out = g_addr[dev];
   return CASGD_OK;

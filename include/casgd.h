@@ -21,8 +21,12 @@
  *
  * Conventions for every call:
  *  - All arrays are allocated by the caller; the library allocates no device or
- *    host memory and keeps no global state.  "device" pointers must be CUDA device
- *    (or managed) memory of the current device; "host" pointers ordinary memory.
+ *    host memory.  It keeps no state between calls, with one exception: the fixed
+ *    scratch array of casgd_update_static (see there).  "device" pointers must be
+ *    CUDA device (or managed) memory of the current device; "host" pointers ordinary
+ *    memory.
+ *  - Flag bits not defined below are rejected with CASGD_ERR_ARG (bit 0x10 named a
+ *    Gram variant this build no longer has).
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
  *    Every call is ordered on it; calls documented as "blocks" synchronize it.
  *  - Argument errors are detected on the host before anything is launched and are
@@ -60,7 +64,8 @@ enum {
   CASGD_ERR_TIMEOUT = 5,      /* device: an inter-CTA wait ran past its bound     */
   CASGD_ERR_BAD_INDEX = 6,    /* device: a caller-given row index outside [0, m)  */
   CASGD_ERR_UNSUPPORTED = 7,  /* valid request this build does not support        */
-  CASGD_ERR_SCRATCH_LIMIT = 8 /* too large for casgd_update_static's fixed scratch  */
+  CASGD_ERR_SCRATCH_LIMIT = 8, /* too large for casgd_update_static's fixed scratch */
+  CASGD_ERR_EXCHANGE = 9       /* the caller's exchange hook returned non-zero      */
 };
 
 /* casgd_params_t.flags */
@@ -68,16 +73,14 @@ enum {
 #define CASGD_FLAG_GRAM_TENSOR       0x2u  /* force the tcgen05 tensor-core Gram kernel */
 #define CASGD_FLAG_GRAM_SIMT         0x4u  /* force the CUDA-core Gram kernel          */
 #define CASGD_FLAG_GRAM_NO_CLUSTER   0x8u  /* tcgen05 Gram, one CTA per 128x256 tile  */
-#define CASGD_FLAG_GRAM_MULTICAST    0x10u /* tcgen05 Gram, 2-CTA clusters that share
-                                              the B tile by TMA multicast             */
 #define CASGD_FLAG_GRAM_PAIR         0x20u /* tcgen05 Gram, CTA pairs (cta_group::2,
                                               256x256 tiles).  Without a variant flag
                                               the library takes pairs forming the far
                                               sums (FAR_FROM_GRAM) for b a multiple of
-                                              256, else pairs sharing their launch
-                                              with the recurrence for b <= 512, else
-                                              pairs for n >= 1024 and multicast
-                                              clusters below                         */
+                                              256, else pairs; these share their launch
+                                              with the recurrence for b <= 512 or
+                                              n >= 1024 (with this flag: always), else
+                                              run as a launch of their own            */
 #define CASGD_FLAG_NO_FUSE           0x40u /* run the paired-SM Gram and the inner
                                               recurrence as two launches.  Otherwise
                                               they share one launch whenever the pair
@@ -195,7 +198,8 @@ typedef struct {
                             5 = as 3 with the far sums formed by the Gram
                             (CASGD_FLAG_FAR_FROM_GRAM), 6 = as 5 with the
                             next iteration's band stored by the same launch
-                            (casgd_train, iters >= 2)                           */
+                            (casgd_train, iters >= 2), 7 = the feature-sharded
+                            calls of casgd_train_sharded                        */
 } casgd_profile_t;
 #define CASGD_STAGE_EVENTS 5
 
@@ -293,12 +297,83 @@ int casgd_loss_async(const casgd_data_t* data, int32_t loss, const float* w, voi
  * 512-byte control block) that every GPU loading the library holds until exit.  It
  * fits P * ldY <= 1,048,576 floats with P = min(ceil(S/32), 320) (e.g. n <= 3272
  * at P = 320); larger requests return CASGD_ERR_SCRATCH_LIMIT and run nothing.
- * The first call on each device looks up the array's device address (make that
- * first call before any stream capture).  Every call shares the array: calls whose
+ * The first call in each CUDA context of a device (the first call on the device, and
+ * the first after a cudaDeviceReset) looks up the array's device address; make that
+ * call before any stream capture.  Every call shares the array: calls whose
  * work overlaps on the GPU (e.g. on two streams) race and must be serialised by the
  * caller.  Non-finite results are not reported here (inspect w).  Asynchronous. */
 int casgd_update_static(const void* Y, int64_t S, int64_t n, int64_t ldY,
                         const float* alpha, float* w, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Feature-sharded outer iteration: the setting the paper measures.  The abstract's
+ * method exists to replace the s AllReduces of s minibatch-SGD steps by a single
+ * AllReduce of the sb x sb Gram matrix per outer iteration, communicated in high
+ * precision.  With the features split over P processes (process p holds columns
+ * c_p .. c_{p+1}-1 of X and the same slice of w), every process draws the same S rows,
+ * forms its partial Gram G_p = Y_p Y_p^T and partial margins r_p = Y_p w_p, and the
+ * sums G = sum_p G_p, r = sum_p r_p give every process the quantities of the
+ * unsharded step (G_{j,t} and r_j are dot products over the features).  The recurrence
+ * then runs identically on every process and each updates its own slice of w.
+ *
+ * An outer iteration is casgd_outer_step_local, then the caller's in-place FP32 sum of
+ * the exchange buffer over the processes (for example ncclAllReduce(ncclSum) on
+ * `stream`), then casgd_outer_step_finish.  The exchange buffer (caller-owned device
+ * FP32, 256-byte aligned, casgd_exchange_elems floats) holds the packed block-lower G
+ * (casgd_gram_elems floats, the layout of casgd_taps_t.G_out) followed by the S
+ * margins as FP32 partial sums; finish rounds the summed margins once to BF16 (or keeps
+ * them in FP32 with CASGD_FLAG_MARGINS_FP32).  With one process the sum is the identity
+ * and the result is that of casgd_outer_step with CASGD_FLAG_FULL_G up to FP32
+ * summation order.  The far-forming Gram (CASGD_FLAG_FAR_FROM_GRAM) and
+ * CASGD_FLAG_G_BF16 are CASGD_ERR_UNSUPPORTED here: the far sums need the summed G, and
+ * the buffer is summed in FP32.  Losses need every feature: they are not formed here.
+ * ---------------------------------------------------------------------------------- */
+
+/* Floats in the exchange buffer for (b, s, flags): the packed block-lower G
+ * (with the diagonal blocks under CASGD_FLAG_WRITE_DIAG_BLOCKS) followed by S = s*b
+ * margins; -1 on bad input.  Host only. */
+int64_t casgd_exchange_elems(int32_t b, int32_t s, uint32_t flags);
+
+/* Bytes of device workspace the sharded calls need for this process's slice (data->n
+ * = its feature count); G is not part of it (it lives in the exchange buffer).  Host
+ * only.  Initialise a fresh workspace with casgd_workspace_init. */
+int casgd_workspace_size_sharded(const casgd_data_t* data, const casgd_params_t* params,
+                                 size_t* bytes);
+
+/* First half of outer iteration k on this process's slice.  data: X_p (m x ld_p BF16,
+ * the slice's columns) and the full label vector y (the same on every process); w:
+ * device FP32[n_p], this slice of the weights (read only here).  Samples the S rows
+ * (the same on every process for the same seed and k), gathers them, and writes G_p and
+ * r_p into xbuf (device, 256-byte aligned, casgd_exchange_elems floats).  taps: NULL,
+ * or idx_in / idx_out as in casgd_outer_step (other members ignored).  Asynchronous. */
+int casgd_outer_step_local(const casgd_data_t* data, const casgd_params_t* params,
+                           const float* w, uint64_t k, void* ws, size_t ws_bytes, void* stream,
+                           float* xbuf, const casgd_taps_t* taps);
+
+/* Second half, after xbuf holds the sums over the processes: the inner recurrence on
+ * the summed G and margins (steps a6, a7) and this slice's update w_p += Y_p^T alpha
+ * (a8).  data, params, ws: as for the matching casgd_outer_step_local call, with no
+ * other call on ws in between.  taps: NULL, or r_out / alpha_out as in
+ * casgd_outer_step (other members ignored).  Asynchronous; device errors are sticky in
+ * ws. */
+int casgd_outer_step_finish(const casgd_data_t* data, const casgd_params_t* params, float* w,
+                            void* ws, size_t ws_bytes, void* stream, const float* xbuf,
+                            const casgd_taps_t* taps);
+
+/* The caller's exchange: sum buf[0 .. count-1] (device FP32) in place over the
+ * processes, ordered on `stream` (it may enqueue work there and return at once).
+ * Returns 0 on success. */
+typedef int (*casgd_exchange_fn)(void* ctx, float* buf, int64_t count, void* stream);
+
+/* `iters` sharded outer iterations k = k0 .. k0+iters-1: local, exchange(ctx, xbuf,
+ * casgd_exchange_elems(...), stream), finish.  A non-zero exchange return ends the
+ * loop with CASGD_ERR_EXCHANGE.  Blocks at the end and returns the first sticky device
+ * error, which it clears.  prof may be NULL (stage events: 0 before local, 1 before the
+ * exchange, 2 before finish, 3 and 4 after it). */
+int casgd_train_sharded(const casgd_data_t* data, const casgd_params_t* params, float* w,
+                        uint64_t k0, int32_t iters, void* ws, size_t ws_bytes, void* stream,
+                        float* xbuf, casgd_exchange_fn exchange, void* exchange_ctx,
+                        casgd_profile_t* prof);
 
 /* Blocks on `stream`, returns the sticky device status of ws (CASGD_OK or the
  * highest-priority CASGD_ERR_* seen) and clears it. */

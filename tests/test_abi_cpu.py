@@ -59,6 +59,19 @@ def test_workspace_size_host_only(lib):
     assert lib.casgd_workspace_size(C.byref(d), C.byref(bad), C.byref(nbytes)) == nat.CASGD_ERR_ARG
 
 
+def test_unknown_flag_bits_rejected(lib):
+    # bit 0x10 named the cluster-multicast Gram, which the library no longer has
+    d = nat.Data(1000, 2000, 2000, 0, 0)
+    nbytes = C.c_size_t(0)
+    for flags in (0x10, 0x4000, 0x40000000):
+        p = nat.Params(256, 32, 0.5, 0, 0, flags, 0)
+        assert lib.casgd_workspace_size(C.byref(d), C.byref(p), C.byref(nbytes)) == nat.CASGD_ERR_ARG
+    known = (nat.FLAG_WRITE_DIAG_BLOCKS | nat.FLAG_GRAM_TENSOR | nat.FLAG_GRAM_PAIR
+             | nat.FLAG_FULL_G | nat.FLAG_G_BF16 | nat.FLAG_MARGINS_FP32)
+    p = nat.Params(256, 32, 0.5, 0, 0, known, 0)
+    assert lib.casgd_workspace_size(C.byref(d), C.byref(p), C.byref(nbytes)) == 0
+
+
 def _ws_bytes(lib, n, b, s, flags):
     nbytes = C.c_size_t(0)
     d = nat.Data(1000, n, (n + 7) // 8 * 8, 0, 0)
@@ -156,3 +169,30 @@ def test_product_path_has_no_oracle_dependency():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 txt = open(os.path.join(root, f)).read()
                 assert not re.search(r"\boracle\b", txt.replace("the oracle", "")), f
+
+
+def test_update_static_refuses_bad_shapes_before_calling_the_library(monkeypatch):
+    """The C side cannot see buffer lengths, so the binding refuses a Y that is not
+    2-D, an n outside [1, ldY], a short alpha or a short w before the library is
+    touched (checked here with CPU tensors and a library stand-in that fails if used)."""
+    import torch
+
+    def no_library():
+        raise AssertionError("the library was called")
+
+    monkeypatch.setattr(casgd, "load", no_library)
+    Y = torch.zeros((64, 16), dtype=torch.bfloat16)
+    a = torch.zeros(64)
+    w = torch.zeros(16)
+    bad = [
+        (torch.zeros(64 * 16, dtype=torch.bfloat16), a, w, 16),   # Y not 2-D
+        (Y, a, w, 17),                                             # n > ldY
+        (Y, a, w, 0),                                              # n < 1
+        (Y, torch.zeros(63), w, 16),                               # alpha shorter than S
+        (Y, a, torch.zeros(15), 16),                               # w shorter than n
+    ]
+    for Yb, ab, wb, n in bad:
+        with pytest.raises(ValueError):
+            casgd.update_static(Yb, ab, wb, n)
+    with pytest.raises(ValueError, match="CUDA"):                  # right shapes, host memory
+        casgd.update_static(Y, a, w, 16)

@@ -52,3 +52,16 @@ def test_source_hash_tracks_the_kernel_sources():
     h = bench.source_hash("gram_recur_far")
     assert len(h) == 16 and int(h, 16) >= 0
     assert h == bench.source_hash("gram_recur_far")  # deterministic
+
+
+def test_tensor_peak_is_burst_unless_the_clock_record_says_otherwise():
+    pk = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    full = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert bench.tensor_peak(pk, full)[0] == 1900.0
+    capped = dict(full, reasons=["sw_power_cap"])
+    peak, which = bench.tensor_peak(pk, capped)
+    assert peak == 1700.0 and "sw_power_cap" in which
+    slow = {"sm_mhz": 1460.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert bench.tensor_peak(pk, slow)[0] == 1700.0
+    unsampled = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+    assert bench.tensor_peak(pk, unsampled)[0] == 1900.0

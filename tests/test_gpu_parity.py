@@ -165,7 +165,7 @@ def _params(casgd, p, override, flags):
     return casgd.Params(b, s, eta, p.recipe.loss, seed=0, flags=flags)
 
 
-@pytest.mark.parametrize("gram", ["simt", "tensor", "tensor_1cta", "tensor_mc", "tensor_pair",
+@pytest.mark.parametrize("gram", ["simt", "tensor", "tensor_1cta", "tensor_pair",
                                   "tensor_pair_nofuse"])
 @pytest.mark.parametrize("name,factory,override", CASES, ids=[c[0] for c in CASES])
 def test_outer_step_parity(gpu_lib, name, factory, override, gram):
@@ -173,7 +173,6 @@ def test_outer_step_parity(gpu_lib, name, factory, override, gram):
     p = factory()
     flag = {"simt": casgd.FLAG_GRAM_SIMT, "tensor": casgd.FLAG_GRAM_TENSOR,
             "tensor_1cta": casgd.FLAG_GRAM_TENSOR | casgd.FLAG_GRAM_NO_CLUSTER,
-            "tensor_mc": casgd.FLAG_GRAM_TENSOR | casgd.FLAG_GRAM_MULTICAST,
             "tensor_pair": casgd.FLAG_GRAM_TENSOR | casgd.FLAG_GRAM_PAIR,
             "tensor_pair_nofuse": casgd.FLAG_GRAM_TENSOR | casgd.FLAG_GRAM_PAIR
             | casgd.FLAG_NO_FUSE}[gram]
@@ -421,7 +420,7 @@ def test_far_from_gram_unsupported_shapes(gpu_lib):
     p = si.make_random(3000, 130, si.LOGISTIC, seed=3)
     data = _dev(p, casgd)
     for b, s, extra in ((100, 6, 0), (256, 1, 0), (256, 4, casgd.FLAG_NO_FUSE),
-                        (256, 4, casgd.FLAG_GRAM_SIMT), (256, 4, casgd.FLAG_GRAM_MULTICAST),
+                        (256, 4, casgd.FLAG_GRAM_SIMT), (256, 4, casgd.FLAG_GRAM_NO_CLUSTER),
                         (256, 4, casgd.FLAG_FULL_G)):
         params = casgd.Params(b, s, 0.1, si.LOGISTIC, flags=casgd.FLAG_FAR_FROM_GRAM | extra)
         ws = casgd.workspace(data, params)

@@ -77,6 +77,47 @@ def test_feature_sharded_outer_step_equals_single_process(kind):
     assert np.linalg.norm(w - ref) <= 1e-12 * np.linalg.norm(ref)
 
 
+def _exchange_hook(rank, world, port, out_q):
+    """The library's exchange hook (make_exchange), as casgd_train_sharded calls it once
+    per outer iteration, summing a rank's buffer over a gloo group in place."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import communication_avoiding_step_gb300 as casgd
+        xbuf = torch.arange(10, dtype=torch.float32) * (rank + 1)
+        hook = casgd.make_exchange(xbuf, dist.all_reduce)
+        rc_ok = hook(None, xbuf.data_ptr(), 7, None)            # sums the first 7 floats
+        rc_bad_ptr = hook(None, xbuf.data_ptr() + 4, 7, None)   # not the buffer: refused
+        rc_bad_len = hook(None, xbuf.data_ptr(), 11, None)      # longer than the buffer
+
+        def failing(t):
+            raise RuntimeError("peer lost")
+
+        rc_fail = casgd.make_exchange(xbuf, failing)(None, xbuf.data_ptr(), 7, None)
+        out_q.put((rank, rc_ok, rc_bad_ptr, rc_bad_len, rc_fail, xbuf.numpy().copy()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_exchange_hook_sums_over_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_exchange_hook, args=(r, 2, port, q)) for r in range(2)]
+    for pr in procs:
+        pr.start()
+    got = {v[0]: v[1:] for v in (q.get(timeout=120) for _ in range(2))}
+    for pr in procs:
+        pr.join(timeout=60)
+        assert pr.exitcode == 0
+    for rank, (rc_ok, rc_bad_ptr, rc_bad_len, rc_fail, buf) in got.items():
+        assert (rc_ok, rc_bad_ptr, rc_bad_len, rc_fail) == (0, 1, 1, 1)
+        want = np.arange(10, dtype=np.float32) * (rank + 1)
+        want[:7] = np.arange(7, dtype=np.float32) * 3          # 1x + 2x over the two ranks
+        assert np.array_equal(buf, want)
+
+
 def _bench_reduce(rank, world, port, out_q):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)

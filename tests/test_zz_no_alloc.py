@@ -1,18 +1,22 @@
-"""casgd_update_static: the allocation-free weight update, checked against the regular
-outer iteration's update.
+"""casgd_update_static: the weight update w += Y^T alpha for callers that cannot
+allocate device memory where they apply it (code inside another framework's memory
+pool that forbids raw cudaMalloc, loops that must not block on an allocator, or
+embedders that own only their input and output buffers).  Its scratch is a fixed array
+inside the library, shared by every call.
 
-Some callers cannot allocate device memory where they apply an update, so this entry
-point keeps its scratch in a fixed array inside the library.  The test runs the
-regular casgd_outer_step (which uses a caller workspace), rebuilds the gathered rows Y
-from its sampled indices, applies casgd_update_static to the starting weights with the
-same alpha, and compares the results -- on two calls in a row, so the second call runs
-on scratch the first one left behind.  This file is collected last on purpose.
+Checked three ways, each on two calls in a row (so the second call runs on the scratch
+the first one left behind):
+  * against the regular casgd_outer_step's update (the same alpha and rows);
+  * against the oracle's FP32 update Y^T alpha on the oracle's own rows and alpha;
+  * requests larger than the scratch are refused before anything runs, with real
+    device buffers.
+This file is collected last on purpose: a run that stops at the first failure has then
+already run every other test.
 """
-import ctypes as C
-
 import numpy as np
 import pytest
 
+import oracle
 import synth_inputs as si
 
 pytestmark = pytest.mark.gpu
@@ -50,12 +54,48 @@ def test_update_static_matches_outer_step(gpu_lib, cid, m):
         w_start = w_ref
 
 
-def test_update_static_rejects_oversized_requests(gpu_lib):
+@pytest.mark.parametrize("cid,m", [(5, 20000), (1, 4096)])
+def test_update_static_matches_oracle(gpu_lib, cid, m):
+    """The oracle's emulating-mode outer iteration gives Y (BF16 values), alpha and
+    w = w0 + Y^T alpha in FP32; the allocation-free update applied to the same Y, alpha
+    and w0 must land within the w bar of the parity tests."""
     casgd = gpu_lib
-    lib = casgd.load()
-    fake = C.c_void_p(1 << 20)          # never touched: the size check comes first
-    rc = lib.casgd_update_static(fake, 65536, 16384, 16384, fake, fake, None)
-    assert rc == 8                      # CASGD_ERR_SCRATCH_LIMIT
-    assert b"fixed scratch" in lib.casgd_strerror(8)
-    rc = lib.casgd_update_static(fake, 65536, 3280, 3280, fake, fake, None)
-    assert rc == 8
+    p = si.make_problem(cid, m=m)
+    r = p.recipe
+    w0 = si.random_weights(p.n, seed=5, scale=0.2)
+    for k in range(2):                        # two calls in a row
+        parts = oracle.outer_step(p.X, p.y, w0, r.b, r.s, r.eta, r.loss, 0, k,
+                                  mode="emulate", return_parts=True)
+        ld = (p.n + 7) // 8 * 8
+        Yh = np.zeros((parts["Y"].shape[0], ld), np.float32)
+        Yh[:, :p.n] = parts["Y"]                          # BF16 values: exact in BF16
+        Y = torch.from_numpy(Yh).to(torch.bfloat16).cuda()
+        alpha = torch.from_numpy(np.asarray(parts["alpha"], np.float32)).cuda()
+        w = torch.from_numpy(w0.copy()).cuda()
+        casgd.update_static(Y, alpha, w, p.n)
+        torch.cuda.synchronize()
+        assert _rel(w.cpu().numpy(), parts["w"]) <= W_TOL
+        w0 = np.asarray(parts["w"], np.float32)
+
+
+def test_update_static_rejects_oversized_requests(gpu_lib):
+    """P * ldY > 1,048,576 partial floats (P = min(ceil(S/32), 320)) is refused with
+    CASGD_ERR_SCRATCH_LIMIT and w stays as it was.  Real device buffers of the stated
+    sizes are passed, so nothing would read past them even if a check moved."""
+    casgd = gpu_lib
+    S, ld = 320 * 32, 3280                    # P = 320: 320 * 3280 = 1,049,600 floats
+    Y = torch.zeros((S, ld), dtype=torch.bfloat16, device="cuda")
+    alpha = torch.ones(S, dtype=torch.float32, device="cuda")
+    w = torch.full((ld,), 2.0, dtype=torch.float32, device="cuda")
+    with pytest.raises(casgd.CasgdError) as e:
+        casgd.update_static(Y, alpha, w, ld)
+    assert e.value.code == 8                  # CASGD_ERR_SCRATCH_LIMIT
+    assert b"fixed scratch" in casgd.load().casgd_strerror(8)
+    torch.cuda.synchronize()
+    assert torch.all(w == 2.0).item()
+    # one column less fits: P * ldY = 320 * 3272 <= 1,048,576
+    Y2 = torch.zeros((S, 3272), dtype=torch.bfloat16, device="cuda")
+    w2 = torch.full((3272,), 2.0, dtype=torch.float32, device="cuda")
+    casgd.update_static(Y2, alpha, w2, 3272)  # Y = 0: w unchanged, and no error
+    torch.cuda.synchronize()
+    assert torch.all(w2 == 2.0).item()
