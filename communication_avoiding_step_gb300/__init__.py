@@ -17,7 +17,7 @@ import torch
 from ._native import (  # noqa: F401
     CASGD_LOGISTIC, CASGD_LSQ, CASGD_POISSON, ExchangeFn as _ExchangeFn, FLAG_GRAM_NO_CLUSTER,
     FLAG_FAR_FROM_GRAM, FLAG_FULL_G, FLAG_GRAM_PAIR, FLAG_SAMPLE_PERMUTED, FLAG_NO_FUSE,
-    FLAG_TRACE_CHAIN, FLAG_MARGINS_FP32, FLAG_G_BF16,
+    FLAG_TRACE_CHAIN, FLAG_MARGINS_FP32, FLAG_G_BF16, FLAG_GATHER_ROWS,
     FLAG_GRAM_SIMT,
     FLAG_GRAM_TENSOR,
     FLAG_TEST_STALL, FLAG_WRITE_DIAG_BLOCKS, STAGE_EVENTS, CasgdError, Data as _Data,

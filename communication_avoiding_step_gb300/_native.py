@@ -26,6 +26,7 @@ FLAG_FULL_G = 0x400
 FLAG_SAMPLE_PERMUTED = 0x800
 FLAG_MARGINS_FP32 = 0x1000
 FLAG_G_BF16 = 0x2000
+FLAG_GATHER_ROWS = 0x4000
 FLAG_TEST_STALL = 0x80000000
 STAGE_EVENTS = 5
 

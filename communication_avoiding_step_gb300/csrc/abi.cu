@@ -56,7 +56,7 @@ constexpr uint32_t kKnownFlags =
     CASGD_FLAG_GRAM_NO_CLUSTER | CASGD_FLAG_GRAM_PAIR | CASGD_FLAG_NO_FUSE |
     CASGD_FLAG_TRACE_CHAIN | CASGD_FLAG_FAR_FROM_GRAM | CASGD_FLAG_FULL_G |
     CASGD_FLAG_SAMPLE_PERMUTED | CASGD_FLAG_MARGINS_FP32 | CASGD_FLAG_G_BF16 |
-    CASGD_FLAG_TEST_STALL;
+    CASGD_FLAG_GATHER_ROWS | CASGD_FLAG_TEST_STALL;
 
 bool check_params(const casgd_params_t* p) {
   if (!p) return false;
@@ -180,6 +180,17 @@ int record(casgd_profile_t* prof, int64_t it, int e, cudaStream_t st) {
     if ((expr) != cudaSuccess) return CASGD_ERR_CUDA; \
   } while (0)
 
+// The sampled rows of the data set as the gathering launch reads them.
+RowSource row_source(const casgd_data_t* d, const casgd_params_t* p) {
+  RowSource rs;
+  rs.X = static_cast<const uint16_t*>(d->X);
+  rs.ld = d->ld;
+  rs.m = (uint32_t)d->m;
+  rs.seed = p->seed;
+  rs.perm_d = (p->flags & CASGD_FLAG_SAMPLE_PERMUTED) ? perm_width(d->m) : 0;
+  return rs;
+}
+
 int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, uint64_t k,
                     void* ws, size_t ws_bytes, cudaStream_t st, const casgd_taps_t* taps,
                     Ctx& c, casgd_profile_t* prof, int64_t it) {
@@ -199,9 +210,16 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   // launch; it waits for the gather's completion before it touches memory)
   c.pdl = true;
   if ((rc = record(prof, it, 0, st)) != CASGD_OK) return rc;
-  if (gp.far)  // the rows and the reset; the margins are formed in the shared launch
-    CK(launch_gather_reset(*d, *p, k, idx_in, R.idx, R.Y, R.yY, true, L.ldY, R.r, R.alpha,
-                           R.far, R.fpart, R.ctrl, R.slab, c));
+  // With CASGD_FLAG_GATHER_ROWS the far-forming launch reads its rows straight from X
+  // (drawing the sampled indices itself), unless the caller gives the indices; otherwise
+  // the rows are gathered into Y first.
+  const bool gather = gp.far && !idx_in && (p->flags & CASGD_FLAG_GATHER_ROWS);
+  const RowSource rs = row_source(d, p);
+  const uint64_t ctr = k * (uint64_t)L.S;
+  if (gp.far)  // the indices and labels (rows into Y only with given indices) and the
+               // reset; the margins are formed in the shared launch
+    CK(launch_gather_reset(*d, *p, k, idx_in, R.idx, gather ? nullptr : R.Y, R.yY, true, L.ldY,
+                           R.r, R.alpha, R.far, R.fpart, R.ctrl, R.slab, c));
   else
     CK(launch_gather(*d, *p, w, k, idx_in, R.idx, R.Y, L.ldY, R.r, R.yY, R.alpha, R.far,
                      nullptr, R.ctrl, R.slab, GATHER_AND_MARGINS, c));
@@ -215,7 +233,8 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
     // on one GPU it is the identity.)
     CK(launch_gram_recur(R.Y, G, false, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss, p->flags,
                          G, R.Y, R.r, R.yY, R.alpha, R.far, R.slab, gp.far ? R.fpart : nullptr,
-                         R.upd, w, gp.far ? R.w_acc : nullptr, R.ctrl, p->timeout_us, c));
+                         R.upd, w, gp.far ? R.w_acc : nullptr, R.ctrl, p->timeout_us,
+                         /*g_band=*/G == R.G, gather ? &rs : nullptr, ctr, ctr, c));
     if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
   } else {
     if (choice == 1)
@@ -272,6 +291,12 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   const cudaStream_t st = c.stream;
   int rc;
   float* fpart = far ? R.fpart : nullptr;
+  // with CASGD_FLAG_GATHER_ROWS the far-forming loop reads every row straight from X (no
+  // Y); its launches draw the sampled indices themselves, the gather launches only the
+  // indices and labels
+  const RowSource rs = row_source(d, p);
+  const bool gather = far && (p->flags & CASGD_FLAG_GATHER_ROWS);
+  const RowSource* rsp = gather ? &rs : nullptr;
   if (prof) prof->gram_kind = far ? 6 : 4;
   // the gather launches and the shared launches of the loop overlap each other's start
   // and end (programmatic dependent launch); each waits for its predecessor's completion
@@ -282,18 +307,20 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
     const uint64_t k = k0 + (uint64_t)it;
     if ((rc = record(prof, it, 0, st)) != CASGD_OK) return rc;
     if (it == 0) {  // prologue: this iteration's rows and its Gram (far: its band)
-      CK(launch_gather(*d, *p, w, k, nullptr, Ib[cur], Yb[cur], L.ldY, R.r, yb[cur], R.alpha,
-                       R.far, nullptr, R.ctrl, R.slab, GATHER_ONLY, c));
+      CK(launch_gather(*d, *p, w, k, nullptr, Ib[cur], gather ? nullptr : Yb[cur], L.ldY, R.r,
+                       yb[cur], R.alpha, R.far, nullptr, R.ctrl, R.slab, GATHER_ONLY, c));
       if (far)
-        CK(launch_gram_band(Yb[cur], Gb[cur], L.S, d->n, L.ldY, p->b, p->s, p->flags, R.ctrl,
-                            p->timeout_us, c));
+        CK(launch_gram_band(gather ? nullptr : Yb[cur], Gb[cur], L.S, d->n, L.ldY, p->b, p->s,
+                            p->flags, R.ctrl, p->timeout_us, rsp, k * (uint64_t)L.S, c));
       else
         CK(launch_gram_tc(Yb[cur], L.S, d->n, L.ldY, p->b, p->s, p->flags, 0, Gb[cur], R.ctrl,
                           p->timeout_us, c));
     }
-    if (far)  // next iteration's rows and this iteration's reset (margins in-launch)
-      CK(launch_gather_reset(*d, *p, k + 1, nullptr, Ib[nxt], Yb[nxt], yb[nxt], it + 1 < iters,
-                             L.ldY, R.r, R.alpha, R.far, fpart, R.ctrl, R.slab, c));
+    if (far)  // next iteration's rows (gathering: its indices and labels only) and this
+              // iteration's reset (margins in-launch)
+      CK(launch_gather_reset(*d, *p, k + 1, nullptr, Ib[nxt], gather ? nullptr : Yb[nxt],
+                             yb[nxt], it + 1 < iters, L.ldY, R.r, R.alpha, R.far, fpart, R.ctrl,
+                             R.slab, c));
     else if (it + 1 < iters)  // next iteration's rows (into the buffers the last launch
                               // freed) and this iteration's margins, in one launch
       CK(launch_gather_next_margins(*d, *p, w, k + 1, Ib[nxt], Yb[nxt], yb[nxt], Yb[cur],
@@ -305,14 +332,18 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
     // (The sum of G over processes would sit before this launch; on one GPU it is the
     // identity.)
     if (far)  // this iteration's far sums; the next iteration's band (if any) into Gb[nxt]
-      CK(launch_gram_recur(it + 1 < iters ? Yb[nxt] : nullptr, Gb[nxt], true, L.S, d->n, L.ldY,
-                           p->b, p->s, p->eta, p->loss, p->flags, Gb[cur], Yb[cur], R.r,
-                           yb[cur], R.alpha, R.far, R.slab, fpart, R.upd, w, R.w_acc, R.ctrl,
-                           p->timeout_us, c));
+      CK(launch_gram_recur(gather ? nullptr : (it + 1 < iters ? Yb[nxt] : nullptr), Gb[nxt],
+                           true, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss, p->flags,
+                           Gb[cur], gather ? nullptr : Yb[cur], R.r, yb[cur], R.alpha, R.far,
+                           R.slab, fpart, R.upd, w, R.w_acc, R.ctrl, p->timeout_us,
+                           /*g_band=*/true, rsp,
+                           it + 1 < iters ? (k + 1) * (uint64_t)L.S : kNoRows,
+                           k * (uint64_t)L.S, c));
     else if (it + 1 < iters)
       CK(launch_gram_recur(Yb[nxt], Gb[nxt], true, L.S, d->n, L.ldY, p->b, p->s, p->eta,
                            p->loss, p->flags, Gb[cur], Yb[cur], R.r, yb[cur], R.alpha, R.far,
-                           R.slab, nullptr, R.upd, w, nullptr, R.ctrl, p->timeout_us, c));
+                           R.slab, nullptr, R.upd, w, nullptr, R.ctrl, p->timeout_us, false,
+                           nullptr, 0, 0, c));
     else
       CK(launch_recur(Gb[cur], R.r, yb[cur], R.alpha, R.far, R.slab, p->b, p->s, p->eta,
                       p->loss, p->flags, p->timeout_us, R.ctrl, Yb[cur], L.ldY, d->n, R.upd, w,
@@ -446,8 +477,15 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms,
   (void)num_sms;
   Layout L;
   L.S = (int64_t)b * s;
-  L.ldY = (n + 7) / 8 * 8;
-  L.gram_elems = gram_elems(b, s, (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0);
+  // Y's pitch: whole 128-byte lines for wide rows (the Gram's TMA reads of a row segment
+  // then touch one L2 line instead of two: measured 132 -> 128 us per shared launch at
+  // n = 2000), 16-byte vectors for narrow ones
+  L.ldY = n >= 128 ? (n + 63) / 64 * 64 : (n + 7) / 8 * 8;
+  const bool diag = (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
+  const GramPlan gp = gram_plan(n, b, s, flags);
+  // the far-forming Gram keeps only the band blocks (band layout); the others store
+  // every block of the packed block-lower G
+  L.gram_elems = g_layout_elems(b, s, diag, gp.far ? band_width(b) : 0);
   int64_t u = (L.S + 31) / 32;
   L.upd_ctas = (int)(u > 320 ? 320 : u);
   size_t off = align_up(sizeof(Ctrl));
@@ -476,14 +514,15 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms,
   L.off_G = with_G ? off : 0;
   if (with_G) off += align_up((size_t)L.gram_elems * sizeof(float));
   L.off_Y2 = L.off_G2 = L.off_idx2 = L.off_yY2 = L.off_fpart = 0;
-  const GramPlan gp = gram_plan(n, b, s, flags);
   if (gp.fused) {  // casgd_train gathers the rows (and runs the Gram) one iteration ahead
     L.off_idx2 = off;
     off += align_up((size_t)L.S * sizeof(int32_t));
     L.off_yY2 = off;
     off += align_up((size_t)L.S * sizeof(float));
-    L.off_Y2 = off;
-    off += align_up((size_t)L.S * L.ldY * sizeof(uint16_t));
+    if (!(gp.far && (flags & CASGD_FLAG_GATHER_ROWS))) {  // (gathering from X: no second Y)
+      L.off_Y2 = off;
+      off += align_up((size_t)L.S * L.ldY * sizeof(uint16_t));
+    }
     L.off_G2 = off;  // the far-forming Gram stores the next iteration's band into it
     off += align_up((size_t)L.gram_elems * sizeof(float));
   }
@@ -627,7 +666,7 @@ int casgd_train(const casgd_data_t* data, const casgd_params_t* params, float* w
   if (rc != CASGD_OK) return rc;
   Resolved R = resolve(ws, L);
   int slot = 0, flushed = 0;
-  if (iters >= 2 && L.off_Y2 != 0) {
+  if (iters >= 2 && L.off_G2 != 0) {  // the second buffers of the pipelined loop exist
     rc = train_pipelined(data, params, w, k0, iters, L, R, c, prof, loss_every, slot, flushed,
                          loss_hist, L.off_fpart != 0);
     if (rc != CASGD_OK) return rc;

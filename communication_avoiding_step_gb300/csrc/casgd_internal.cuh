@@ -93,6 +93,32 @@ __host__ __device__ inline int64_t packed_offset(int64_t j, int64_t t, int64_t b
   return (diag ? (j * (j + 1) / 2 + t) : (j * (j - 1) / 2 + t)) * b * b;
 }
 
+// Blocks before block row j in the band layout of band width B: sum over j' < j of
+// min(j', B), plus one diagonal block per row with diag.
+__host__ __device__ inline int64_t band_blocks_before(int64_t j, int64_t B, bool diag) {
+  const int64_t lower = j <= B ? j * (j - 1) / 2 : B * (B - 1) / 2 + (j - B) * B;
+  return lower + (diag ? j : 0);
+}
+
+// Offset (elements) of block (j, t) of G in one of two layouts.  gB = 0: the packed
+// block-lower layout (every block t < j, or t <= j with diag; j ascending, then t).
+// gB = B > 0: the band layout the far-forming Gram keeps internally -- only the blocks
+// the recurrence reads from memory, t = j - min(j, B) .. j-1 ascending, then G_{j,j}
+// with diag -- so its buffers grow with s * B instead of s^2 / 2.  Each block b x b,
+// row-major.
+__host__ __device__ inline int64_t g_block_offset(int64_t j, int64_t t, int64_t b, bool diag,
+                                                  int gB) {
+  if (gB == 0) return packed_offset(j, t, b, diag);
+  const int64_t nb = j < gB ? j : gB;
+  return (band_blocks_before(j, gB, diag) + (t - (j - nb))) * b * b;
+}
+
+// Floats of G in either layout (gB as above).
+inline int64_t g_layout_elems(int64_t b, int64_t s, bool diag, int gB) {
+  if (gB == 0) return gram_elems(b, s, diag);
+  return band_blocks_before(s, gB, diag) * b * b;
+}
+
 // Column tiles (256 wide) that the paired-SM Gram computes for its 256-row group g:
 // those holding a needed entry (column block < row block, or <= with the diagonal) of
 // the group's last row, which needs the most.
@@ -278,6 +304,19 @@ __device__ __forceinline__ void allow_next_grid() {
 }
 
 // ------------------------------------------------------------------ launchers
+// Rows of an outer iteration read straight from X (the far-forming launch that gathers
+// its own operands): row p of the iteration whose first sampler counter is c0 is row
+// draw_row(seed, c0 + p, m, perm_d) of X (pitch ld elements).
+struct RowSource {
+  const uint16_t* X;
+  int64_t ld;
+  uint32_t m;
+  uint64_t seed;
+  int perm_d;
+};
+// A sampler counter that names no rows (a launch without the next iteration's band).
+constexpr uint64_t kNoRows = ~0ull;
+
 // Launch parameters of the kernels one call launches repeatedly (occupancy results, with
 // the dynamic shared memory attribute set), found once per call: the queries cost host
 // time, and in casgd_train's loop that time would fall between the launches.  Owned by
@@ -349,13 +388,15 @@ cudaError_t launch_sample(int64_t m, int64_t count, uint64_t seed, uint64_t coun
 // recurrence's reset), GATHER_ONLY (rows, labels, indices), MARGINS_ONLY (margins of
 // the rows in Y and the reset).  The margins are bit-identical in every mode.  The reset
 // fills alpha, far and (fpart non-null) each row's far partials t < j-B with
-// kAlphaPending.
+// kAlphaPending.  GATHER_ONLY with Y null: the indices and labels only (the rows are read
+// from X by the launch that gathers its own operands).
 enum { GATHER_AND_MARGINS = 0, GATHER_ONLY = 1, MARGINS_ONLY = 2 };
 cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const float* w,
                           uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
                           int64_t ldY, float* r, float* yY, float* alpha, float* far,
                           float* fpart, Ctrl* ctrl, uint32_t* slab, int mode, Ctx& c);
-// Rows of iteration k_rows (into Yg, yY, idx; skipped without `gather`) and, in the same
+// Rows of iteration k_rows (into Yg, yY, idx; skipped without `gather`; Yg null: the
+// indices and labels only) and, in the same
 // launch, this iteration's recurrence reset without margins (alpha, far, r and the far
 // partials pending; counters and queues zeroed): for the far-forming Gram, whose launch
 // forms the margins itself.
@@ -402,19 +443,26 @@ cudaError_t launch_recur(const float* G, const float* r, const float* yY, float*
 bool gram_recur_fused_supported(int64_t S, int64_t n, int b);
 bool far_gram_supported(int64_t S, int64_t n, int b);
 // The band blocks (and the diagonal on request) of the far-forming Gram alone, from rows
-// Y into G: the band of a run's first iteration.
+// Y into G (band layout): the band of a run's first iteration.
+// rs (non-null): the rows are read from X instead of Y (Y unused), those of the iteration
+// whose first sampler counter is ctr.
 cudaError_t launch_gram_band(const uint16_t* Y, float* G, int64_t S, int64_t n, int64_t ldY,
                              int b, int s, uint32_t flags, Ctrl* ctrl, uint32_t timeout_us,
-                             Ctx& c);
+                             const RowSource* rs, uint64_t ctr, Ctx& c);
 // w_acc (with fpart): FP32[n] scratch; the launch then forms the margins itself (r reset
 // to pending by launch_gather_reset) from Y and w, and w receives the update only with the
-// last block.
+// last block.  g_band (with fpart): Gg and G use the band layout (g_block_offset with
+// gB = band_width(b)), else the packed block-lower layout.  rs (non-null, with fpart):
+// every row is read from X instead of Yg / Y -- the Gram's own rows those of the
+// iteration starting at sampler counter ctr_g, this iteration's (far tiles, margins,
+// update) those starting at ctr_f.
 cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t S, int64_t n,
                               int64_t ldY, int b, int s, float eta, int loss, uint32_t flags,
                               const float* G, const uint16_t* Y, float* r,
                               const float* yY, float* alpha, float* far, uint32_t* slab,
                               float* fpart, float* part, float* w, float* w_acc, Ctrl* ctrl,
-                              uint32_t timeout_us, Ctx& c);
+                              uint32_t timeout_us, bool g_band, const RowSource* rs,
+                              uint64_t ctr_g, uint64_t ctr_f, Ctx& c);
 cudaError_t launch_update_reduce(const float* part, int upd_ctas, int64_t n, int64_t ldY,
                                  float* w, Ctrl* ctrl, Ctx& c);
 cudaError_t launch_update(const uint16_t* Y, const float* alpha, int64_t S, int64_t n,

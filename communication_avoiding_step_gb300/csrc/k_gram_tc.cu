@@ -59,6 +59,7 @@ struct TcArgs {
   bool diag;
   bool g_bf16;     // entries rounded to BF16 before they are stored or used
   bool tma_store;  // b % 32 == 0: 32x32 chunks go out through a TMA tensor store
+  int gB;          // layout of G: 0 packed block-lower, B > 0 band layout (g_block_offset)
   uint64_t timeout_ns;
   uint32_t* slab;  // recurrence in the same launch: per-32-row tile counters (else null)
   // Far-forming mode (fpart set; b a multiple of 256): only the band blocks (and the
@@ -72,6 +73,13 @@ struct TcArgs {
   bool stored_last;  // the stored units are the next iteration's band (see FarCursor)
   int n_stored;      // stored units in this launch
   int far_head;      // stored_last: far units before the stored ones
+  // Rows read straight from X (kernels with kGather): row p of the Gram's own rows is
+  // row draw_row(seed, ctr_g + p) of X, row p of the far tiles' rows (this iteration's)
+  // draw_row(seed, ctr_f + p) -- the sampler is a pure function of its counter, so the
+  // producer draws the indices itself and Y never exists
+  uint64_t seed, ctr_g, ctr_f;
+  uint32_t m;
+  int perm_d;
 };
 
 struct SharedCtl {
@@ -360,7 +368,7 @@ __device__ __forceinline__ void store_tile_rows(const TcArgs& a, uint32_t tmem, 
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        const int64_t grow = (packed_offset(j0, t0b, a.b, a.diag) / a.b) + (p0 - j0 * a.b);
+        const int64_t grow = (g_block_offset(j0, t0b, a.b, a.diag, a.gB) / a.b) + (p0 - j0 * a.b);
         tma_store_2d(tmG, smem_u32(buf), (int32_t)(q0 - t0b * a.b), (int32_t)grow);
         bulk_commit();
       }
@@ -373,7 +381,7 @@ __device__ __forceinline__ void store_tile_rows(const TcArgs& a, uint32_t tmem, 
     const int64_t t1b = q1 / a.b;
     const bool whole = (q1 < a.S) && (t0b == t1b) && (t0b < jb || (a.diag && t0b == jb));
     if (whole && vec_ok && ((q0 - t0b * a.b) % 4) == 0) {
-      float* dst = a.G + packed_offset(jb, t0b, a.b, a.diag) + ib * a.b + (q0 - t0b * a.b);
+      float* dst = a.G + g_block_offset(jb, t0b, a.b, a.diag, a.gB) + ib * a.b + (q0 - t0b * a.b);
 #pragma unroll
       for (int e = 0; e < 32; e += 4)
         *reinterpret_cast<float4*>(dst + e) =
@@ -386,7 +394,7 @@ __device__ __forceinline__ void store_tile_rows(const TcArgs& a, uint32_t tmem, 
         if (q >= a.S) break;
         const int64_t tb = q / a.b;
         if (tb < jb || (a.diag && tb == jb))
-          a.G[packed_offset(jb, tb, a.b, a.diag) + ib * a.b + (q - tb * a.b)] =
+          a.G[g_block_offset(jb, tb, a.b, a.diag, a.gB) + ib * a.b + (q - tb * a.b)] =
               __uint_as_float(v[e]);
       }
     }
@@ -616,6 +624,21 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Four rows r0..r3 of a 2D tensor (columns x .. x+63 of each, the map's box being one row
+// high) into consecutive 128-byte rows of this CTA's shared memory, 128-byte swizzled by
+// their shared-memory address (so four copies to dst, dst+512, ... build the same tile a
+// 128-row box copy would); completion counted on a barrier that may be the pair leader's.
+__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t r0,
+                                                 int32_t r1, int32_t r2, int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4"
+      ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(r0), "r"(r1), "r"(r2),
+      "r"(r3)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                               uint32_t accumulate) {
   asm volatile(
@@ -786,7 +809,7 @@ __device__ __forceinline__ void far_tile_dot(uint32_t tmem, int acc, int quarter
   }
 }
 
-template <int kSt, int kRecV, bool kNext, bool kFar>
+template <int kSt, int kRecV, bool kNext, bool kFar, bool kGather = false>
 __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
     gram_tc2sm_kernel(const __grid_constant__ CUtensorMap tmY,
                       const __grid_constant__ CUtensorMap tmG,
@@ -830,7 +853,59 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
   // overlaps the gather's end; every global access follows this wait.
   wait_prior_grid();
 
-  if (warp == 0) {
+  if (warp == 0 && kGather) {
+    // ------------------------------------------------ row-gathering producer (both CTAs)
+    // The whole warp: per tile, lane L draws the X rows of A rows 4L..4L+3 and of B rows
+    // 4L..4L+3 (of this CTA's half) from the sampler, then per 64 columns of K issues one
+    // four-row gather of each into the stage (lane 0 waits for the stage and, in the
+    // leader, arms its barrier for both CTAs' bytes first).  Every tile is whole: S is a
+    // multiple of 256 on this path.
+    WorkCursor<kFar> cur;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool live = true;
+    for (int u = cid; u < a.ntiles && live; u += ncl) {
+      live = __shfl_sync(0xffffffffu, sc->abort ? 0 : 1, 0) != 0;
+      if (!live) break;
+      int rg, ca0, nq, t, pidx;
+      bool far;
+      cur.seek(a, u, rg, ca0, nq, t, pidx, far);
+      const int ra = 2 * rg + rank;
+      const uint64_t c0 = (kFar && far) ? a.ctr_f : a.ctr_g;  // this iteration's or the Gram's
+      int32_t ar[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        ar[i] = draw_row(a.seed, c0 + (uint64_t)(ra * BM + 4 * lane + i), a.m, a.perm_d);
+      for (int q = 0; q < nq && live; ++q) {
+        const int ca = ca0 + q;
+        int32_t br[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          br[i] = draw_row(a.seed, c0 + (uint64_t)(ca * BN + rank * (BN / 2) + 4 * lane + i), a.m,
+                           a.perm_d);
+        for (int kb = 0; kb < a.nkb; ++kb) {
+          int ok = 1;
+          if (lane == 0) {
+            ok = mbar_wait2(&sc->empty[stage], phase ^ 1u, sc, a) ? 1 : 0;
+            if (ok && leader) mbar_expect_tx(&sc->full[stage], 2 * kStageBytes2);  // both CTAs
+          }
+          if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            live = false;
+            break;
+          }
+          const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes2);
+          const uint32_t sb = sa + kABytes;
+          const uint32_t bar = mapa_rank(smem_u32(&sc->full[stage]), 0);
+          tma_gather4_pair(sa + lane * 512, &tmY, bar, kb * BK, ar[0], ar[1], ar[2], ar[3]);
+          tma_gather4_pair(sb + lane * 512, &tmY, bar, kb * BK, br[0], br[1], br[2], br[3]);
+          if (++stage == kSt) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       // -------------------------------------------------------- TMA producer (both CTAs)
       WorkCursor<kFar> cur;
@@ -1001,7 +1076,7 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
       chain_role<kRecV == 1 ? 1 : (kRecV == 2 ? 2 : 3), kRecV == 1 ? 8 : (kRecV == 2 ? 4 : 2),
                  kMode>(rec, blockIdx.x, rt);
     else
-      bulk_role<kMode>(rec, rt, (int)blockIdx.x - rec.C < rec.upd_groups);
+      bulk_role<kMode, kGather>(rec, rt, (int)blockIdx.x - rec.C < rec.upd_groups);
   }
 
   tc_fence_before();
@@ -1050,9 +1125,10 @@ struct TcPlan {
 };
 
 // Tensor maps and tile counts shared by every variant.  kcl: CTAs per row group.
+// gB: layout of G (0 packed block-lower; band_width(b) for the band layout).
 cudaError_t plan_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b, int s,
                     uint32_t flags, int kcl, float* G, Ctrl* ctrl, uint32_t timeout_us,
-                    TcPlan& P) {
+                    TcPlan& P, int gB = 0) {
   const bool diag = (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
@@ -1060,9 +1136,11 @@ cudaError_t plan_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
   const cuuint64_t gstride[1] = {(cuuint64_t)ldY * 2};
   const cuuint32_t box[2] = {BK, BM};
   const cuuint32_t estride[2] = {1, 1};
-  if (enc(&P.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(Y), gdim, gstride,
-          box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  memset(&P.map, 0, sizeof(P.map));
+  if (Y && enc(&P.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(Y), gdim,
+               gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+                   CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   TcArgs& a = P.a;
   a.G = G;
@@ -1086,6 +1164,10 @@ cudaError_t plan_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
   a.fs = s;
   a.stored_last = false;
   a.n_stored = a.far_head = 0;
+  a.gB = gB;
+  a.seed = a.ctr_g = a.ctr_f = 0;
+  a.m = 0;
+  a.perm_d = 0;
   // count the needed tiles on the host with the same rule the kernel walks
   int64_t total = 0;
   for (int g = 0; g * kcl < a.TR; ++g) {
@@ -1104,10 +1186,11 @@ cudaError_t plan_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
   }
   a.ntiles = (int)total;
 
-  // Output map: the packed G viewed as (blocks * b) rows of b FP32 columns; 32x32 boxes.
+  // Output map: G (either layout) viewed as (blocks * b) rows of b FP32 columns; 32x32
+  // boxes.
   memset(&P.mapG, 0, sizeof(P.mapG));
   a.tma_store = false;
-  const int64_t nblk = diag ? (int64_t)s * (s + 1) / 2 : (int64_t)s * (s - 1) / 2;
+  const int64_t nblk = g_layout_elems(b, s, diag, gB) / ((int64_t)b * b);
   if (b % 32 == 0 && nblk > 0) {
     const cuuint64_t gdimG[2] = {(cuuint64_t)b, (cuuint64_t)(nblk * b)};
     const cuuint64_t gstrideG[1] = {(cuuint64_t)b * 4};
@@ -1117,6 +1200,29 @@ cudaError_t plan_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
                       CU_TENSOR_MAP_L2_PROMOTION_NONE,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   }
+  return cudaSuccess;
+}
+
+// The map the row-gathering producer reads X through: X viewed as m rows of n BF16
+// columns (pitch ld), a box of 64 columns by one row (tile::gather4 takes four of them),
+// 128-byte swizzle, columns from n on read as zeros.  Sets the sampler fields of a.
+cudaError_t plan_gather(const RowSource& rs, int64_t n, uint64_t ctr_g, uint64_t ctr_f,
+                        TcPlan& P) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t gdim[2] = {(cuuint64_t)n, (cuuint64_t)rs.m};
+  const cuuint64_t gstride[1] = {(cuuint64_t)rs.ld * 2};
+  const cuuint32_t box[2] = {BK, 1};
+  const cuuint32_t estride[2] = {1, 1};
+  if (enc(&P.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(rs.X), gdim,
+          gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  P.a.seed = rs.seed;
+  P.a.ctr_g = ctr_g;
+  P.a.ctr_f = ctr_f;
+  P.a.m = rs.m;
+  P.a.perm_d = rs.perm_d;
   return cudaSuccess;
 }
 
@@ -1221,18 +1327,21 @@ void set_far_fields(TcArgs& a, int b, int s, float* fpart, const float* alpha) {
 
 cudaError_t launch_gram_band(const uint16_t* Y, float* G, int64_t S, int64_t n, int64_t ldY,
                              int b, int s, uint32_t flags, Ctrl* ctrl, uint32_t timeout_us,
-                             Ctx& c) {
+                             const RowSource* rs, uint64_t ctr, Ctx& c) {
   if (!far_gram_supported(S, n, b)) return cudaErrorNotSupported;
   TcPlan P;
-  cudaError_t e = plan_tc(Y, S, n, ldY, b, s, flags, 2, G, ctrl, timeout_us, P);
+  cudaError_t e = plan_tc(rs ? nullptr : Y, S, n, ldY, b, s, flags, 2, G, ctrl, timeout_us, P,
+                          band_width(b));
   if (e != cudaSuccess) return e;
+  if (rs && (e = plan_gather(*rs, n, ctr, ctr, P)) != cudaSuccess) return e;
   set_far_fields(P.a, b, s, nullptr, nullptr);
   int64_t nfar, nst;
   far_unit_counts(P.a, nfar, nst);
   P.a.n_stored = (int)nst;
   P.a.ntiles = (int)nst;  // the stored units only (they come first)
   if (P.a.ntiles == 0) return cudaSuccess;
-  const auto fn = gram_tc2sm_kernel<kStagesFused, 0, false, true>;
+  const auto fn = rs ? gram_tc2sm_kernel<kStagesFused, 0, false, true, true>
+                     : gram_tc2sm_kernel<kStagesFused, 0, false, true>;
   const size_t smem = pair_smem_bytes<kStagesFused, true>();
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster2_config(kThreads, smem, c.stream, attr);
@@ -1261,18 +1370,25 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
                               const float* G, const uint16_t* Y, float* r,
                               const float* yY, float* alpha, float* far, uint32_t* slab,
                               float* fpart, float* part, float* w, float* w_acc, Ctrl* ctrl,
-                              uint32_t timeout_us, Ctx& c) {
+                              uint32_t timeout_us, bool g_band, const RowSource* rs,
+                              uint64_t ctr_g, uint64_t ctr_f, Ctx& c) {
   if (!gram_recur_fused_supported(S, n, b)) return cudaErrorNotSupported;
   const bool far_gram = fpart != nullptr;
   if (far_gram && !far_gram_supported(S, n, b)) return cudaErrorNotSupported;
   if (!far_gram && !Yg) return cudaErrorInvalidValue;
+  if (rs && !far_gram) return cudaErrorInvalidValue;  // only the far-forming launch gathers
+  const bool gather = rs != nullptr;
   const bool diag = (flags & CASGD_FLAG_WRITE_DIAG_BLOCKS) != 0;
   TcPlan P;
-  cudaError_t e = plan_tc(Yg ? Yg : Y, S, n, ldY, b, s, flags, 2, Gg, ctrl, timeout_us, P);
+  const int gB = (far_gram && g_band) ? band_width(b) : 0;  // layout of Gg and G
+  cudaError_t e = plan_tc(gather ? nullptr : (Yg ? Yg : Y), S, n, ldY, b, s, flags, 2, Gg, ctrl,
+                          timeout_us, P, gB);
   if (e != cudaSuccess) return e;
-  // far tiles read this iteration's rows (the Gram's own rows unless next)
+  if (gather && (e = plan_gather(*rs, n, ctr_g, ctr_f, P)) != cudaSuccess) return e;
+  // far tiles read this iteration's rows (the Gram's own rows unless next; gathering, the
+  // same map of X with this iteration's sampler counters)
   CUtensorMap mapYf = P.map;
-  if (far_gram && next) {
+  if (far_gram && next && !gather) {
     TcPlan Pf;
     e = plan_tc(Y, S, n, ldY, b, s, flags, 2, Gg, ctrl, timeout_us, Pf);
     if (e != cudaSuccess) return e;
@@ -1281,6 +1397,15 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
   P.a.slab = next ? nullptr : slab;
   RecArgs rec = make_rec_args(G, r, yY, alpha, far, slab, b, s, eta, loss, flags, timeout_us,
                               ctrl, Y, ldY, n, part, w);
+  rec.gB = gB;
+  if (gather) {  // margins and update read this iteration's rows from X
+    rec.X = rs->X;
+    rec.ldx = rs->ld;
+    rec.xseed = rs->seed;
+    rec.xctr = ctr_f;
+    rec.xm = rs->m;
+    rec.xperm = rs->perm_d;
+  }
   rec.slab = next ? nullptr : slab;
   if (far_gram) {  // work items: units of uq tiles
     set_far_fields(P.a, b, s, fpart, alpha);
@@ -1289,7 +1414,8 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
     // next: the next iteration's band (none without its rows) after one round of far
     // units (far_head is set once the grid is known)
     P.a.stored_last = next;
-    P.a.n_stored = (int)((!next || Yg) ? nst : 0);
+    const bool g_rows = gather ? ctr_g != kNoRows : Yg != nullptr;  // the Gram has rows
+    P.a.n_stored = (int)((!next || g_rows) ? nst : 0);
     P.a.ntiles = (int)(nfar + P.a.n_stored);
     P.a.far_head = 0;
     rec.fpart = fpart;
@@ -1334,7 +1460,15 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
       {gram_tc2sm_kernel<kStagesFused, 1, true, true>,
        gram_tc2sm_kernel<kStagesFused, 2, true, true>,
        gram_tc2sm_kernel<kStagesFused, 3, true, true>}};
-  const Fn fn = table[(far_gram ? 2 : 0) + (next ? 1 : 0)][v - 1];
+  const Fn gtable[2][3] = {
+      {gram_tc2sm_kernel<kStagesFused, 1, false, true, true>,
+       gram_tc2sm_kernel<kStagesFused, 2, false, true, true>,
+       gram_tc2sm_kernel<kStagesFused, 3, false, true, true>},
+      {gram_tc2sm_kernel<kStagesFused, 1, true, true, true>,
+       gram_tc2sm_kernel<kStagesFused, 2, true, true, true>,
+       gram_tc2sm_kernel<kStagesFused, 3, true, true, true>}};
+  const Fn fn = gather ? gtable[next ? 1 : 0][v - 1]
+                       : table[(far_gram ? 2 : 0) + (next ? 1 : 0)][v - 1];
   const size_t smem = far_gram ? pair_smem_bytes<kStagesFused, true>()
                                : pair_smem_bytes<kStagesFused>();
   cudaLaunchAttribute attr[2];

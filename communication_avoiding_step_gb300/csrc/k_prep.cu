@@ -4,12 +4,14 @@
 // GPUs (abstract): the recipe stores the input matrix and the margin vector in low
 // precision; each outer iteration works on s minibatches of b rows.
 //
-// The gather writes Y (S x ldY BF16, ldY = n rounded up to 8, zero padded) once per
+// The gather writes Y (S x ldY BF16, ldY = n rounded up to 64, or to 8 below 128
+// columns, zero padded) once per
 // outer iteration (in a multi-iteration run, one iteration ahead of its margins).  Y is small next to X and stays L2-resident for the Gram and update
 // kernels; it lets the Gram kernel fetch tiles with plain tiled TMA copies.
 #include <cuda_bf16.h>
 
 #include "casgd_internal.cuh"
+#include "ptx_async.cuh"
 
 namespace casgd {
 
@@ -141,7 +143,9 @@ __device__ __forceinline__ void gather_rows(const RowArgs& a, int64_t blk) {
     }
   }
   float acc = 0.0f;
-  if (live) {
+  // (a.Y null: the rows are not copied -- the Gram and the units read them from X --
+  // only the indices and labels are gathered)
+  if (live && a.Y) {
     const uint16_t* xr = kCopy ? a.X + (int64_t)(valid ? row : 0) * a.ld : a.Y + p * a.ldY;
     uint16_t* yr = a.Y + p * a.ldY;
     // kBatch 16-byte loads of the row are issued before any of them is used.
@@ -151,8 +155,11 @@ __device__ __forceinline__ void gather_rows(const RowArgs& a, int64_t blk) {
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
         const int64_t v = v0 + (int64_t)u * G;
-        qv[u] = (valid && v < nvec) ? __ldg(reinterpret_cast<const uint4*>(xr + v * 8))
-                                    : make_uint4(0, 0, 0, 0);
+        // vectors past n are never read (X holds only round_up(n, 8) columns of data);
+        // Y's padding is written as zeros
+        qv[u] = (valid && v < nvec && v * 8 < a.n)
+                    ? __ldg(reinterpret_cast<const uint4*>(xr + v * 8))
+                    : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
@@ -248,13 +255,93 @@ __device__ void reset_rows(const RowArgs& a, int64_t blk, int64_t nr) {
   }
 }
 
+// Wide rows (ldY*2 >= 512 bytes) of block `blk`, RB of them, moved whole by bulk copies:
+// the indices and labels first (one thread per row), then one cp.async.bulk per valid
+// row from X into shared memory (the row's round_up(n, 8) columns), the columns from n on
+// zeroed there (and the whole row for an index outside [0, m)), and one bulk store per
+// row into Y.  The bytes in flight cost no registers, so a CTA keeps RB rows moving.
+// Every wait is bounded (a timeout records ST_TIMEOUT).
+__device__ void gather_rows_bulk(const RowArgs& a, int64_t blk, int RB, uint8_t* sm) {
+  __shared__ uint64_t bar;
+  __shared__ int32_t s_row[256];
+  const int64_t p0 = blk * RB;
+  const int nrow = (int)(a.S - p0 < RB ? a.S - p0 : RB);
+  const uint32_t pitch = (uint32_t)(a.ldY * 2);            // bytes per row in Y and in sm
+  const uint32_t ncopy = (uint32_t)(((a.n + 7) / 8) * 16);  // bytes of data per row
+  int32_t row = 0;
+  bool valid = false;
+  if ((int)threadIdx.x < nrow) {
+    const int64_t p = p0 + threadIdx.x;
+    if (a.idx_in) {
+      row = a.idx_in[p];
+      valid = row >= 0 && (int64_t)row < a.m;
+      if (!valid) atomicOr(&a.ctrl->status, ST_BAD_INDEX);
+    } else {
+      row = draw_row(a.seed, a.counter0 + (uint64_t)p, (uint32_t)a.m, a.perm_d);
+      valid = true;
+    }
+    s_row[threadIdx.x] = valid ? row : -1;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {  // the rows' copies first ...
+    uint32_t total = 0;
+    for (int i = 0; i < nrow; ++i) total += s_row[i] >= 0 ? ncopy : 0u;
+    mbar_expect_tx(&bar, total);
+    for (int i = 0; i < nrow; ++i)
+      if (s_row[i] >= 0)
+        bulk_load(sm + (size_t)i * pitch, a.X + (int64_t)s_row[i] * a.ld, ncopy, &bar);
+  }
+  if ((int)threadIdx.x < nrow) {  // ... then the labels and indices, while the rows land
+    const int64_t p = p0 + threadIdx.x;
+    a.yY[p] = valid ? __ldg(a.y + row) : 0.0f;
+    a.idx_out[p] = row;
+  }
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(&bar, 0)) {
+    if (globaltimer_ns() - t0 > 1000000000ull) {  // (copies of this CTA alone: not expected)
+      if (threadIdx.x == 0) atomicOr(&a.ctrl->status, ST_TIMEOUT);
+      // keep the shared memory until the copies land (bounded), store nothing
+      while (!mbar_try_wait(&bar, 0) && globaltimer_ns() - t0 < 2000000000ull) {
+      }
+      return;
+    }
+  }
+  // zero the columns that are not data: from n on (all of an invalid row)
+  for (int i = 0; i < nrow; ++i) {
+    uint16_t* r = reinterpret_cast<uint16_t*>(sm + (size_t)i * pitch);
+    const int64_t c0 = s_row[i] >= 0 ? a.n : 0;
+    for (int64_t cc = c0 + threadIdx.x; cc < a.ldY; cc += blockDim.x) r[cc] = 0;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the bulk stores
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nrow; ++i)
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                       reinterpret_cast<uint64_t>(a.Y + (p0 + i) * a.ldY)),
+                   "r"(smem_u32(sm + (size_t)i * pitch)), "r"(pitch)
+                   : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // stored before the CTA leaves
+  }
+}
+
 // Blocks [0, nb_g) gather rows (g: the next iteration's, or this one's for a single
-// step), the others reset this iteration's recurrence state (mg).
-__global__ void __launch_bounds__(256) gather_reset_kernel(RowArgs g, RowArgs mg, int64_t nb_g) {
+// step), the others reset this iteration's recurrence state (mg).  rb > 0: wide rows by
+// bulk copies, rb per block (dynamic shared memory rb * ldY * 2 bytes).
+__global__ void __launch_bounds__(256) gather_reset_kernel(RowArgs g, RowArgs mg, int64_t nb_g,
+                                                           int rb) {
+  extern __shared__ __align__(128) uint8_t gather_smem[];
   wait_prior_grid();  // the previous launch reads the buffers this one writes
   allow_next_grid();  // the next launch may take SMs as this one's blocks leave
   if ((int64_t)blockIdx.x < nb_g) {
-    gather_rows<true, false>(g, blockIdx.x);
+    if (rb > 0)
+      gather_rows_bulk(g, blockIdx.x, rb, gather_smem);
+    else
+      gather_rows<true, false>(g, blockIdx.x);
   } else {
     const int64_t blk = (int64_t)blockIdx.x - nb_g;
     if (blk == 0) reset_recurrence(mg);
@@ -385,8 +472,8 @@ cudaError_t launch_gather(const casgd_data_t& d, const casgd_params_t& p, const 
                           uint64_t k, const int32_t* idx_in, int32_t* idx, uint16_t* Y,
                           int64_t ldY, float* r, float* yY, float* alpha, float* far,
                           float* fpart, Ctrl* ctrl, uint32_t* slab, int mode, Ctx& c) {
-  const RowArgs a =
-      row_args(d, p, w, k, idx_in, idx, Y, ldY, r, yY, alpha, far, fpart, ctrl, slab);
+  RowArgs a = row_args(d, p, w, k, idx_in, idx, Y, ldY, r, yY, alpha, far, fpart, ctrl, slab);
+  if (!Y && mode == GATHER_ONLY) a.G = 1;  // indices and labels only: one thread per row
   auto fn = mode == GATHER_AND_MARGINS ? gather_kernel<true, true>
             : mode == GATHER_ONLY      ? gather_kernel<true, false>
                                        : gather_kernel<false, true>;
@@ -399,17 +486,33 @@ cudaError_t launch_gather_reset(const casgd_data_t& d, const casgd_params_t& p, 
                                 const int32_t* idx_in, int32_t* idx, uint16_t* Yg, float* yY,
                                 bool gather, int64_t ldY, float* r, float* alpha, float* far,
                                 float* fpart, Ctrl* ctrl, uint32_t* slab, Ctx& c) {
-  const RowArgs g = row_args(d, p, nullptr, k_rows, idx_in, idx, Yg, ldY, nullptr, yY, nullptr,
-                             nullptr, nullptr, ctrl, slab);
+  RowArgs g = row_args(d, p, nullptr, k_rows, idx_in, idx, Yg, ldY, nullptr, yY, nullptr,
+                       nullptr, nullptr, ctrl, slab);
+  if (!Yg) g.G = 1;  // indices and labels only (the rows are read from X later): one thread per row
+  // wide rows move by bulk copies, 32 KB of rows per block (at most 256)
+  int rb = 0;
+  if (Yg && ldY * 2 >= 512) {
+    rb = (int)((32 * 1024) / (ldY * 2));
+    if (rb < 1) rb = 1;
+    if (rb > 256) rb = 256;
+  }
   const RowArgs mg = row_args(d, p, nullptr, 0, nullptr, nullptr, nullptr, ldY, r, nullptr, alpha,
                               far, fpart, ctrl, slab);
-  const int64_t nb = gather ? row_blocks(g) : 0;
+  const int64_t nb = gather ? (rb > 0 ? (g.S + rb - 1) / rb : row_blocks(g)) : 0;
   const int64_t work = mg.fpart ? mg.S * mg.fs : mg.S;  // reset slots
   int64_t nr = (work + 255) / 256;
   if (nr > (int64_t)c.num_sms * 4) nr = (int64_t)c.num_sms * 4;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = plain_config((unsigned)(nb + nr), c, attr);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gather_reset_kernel, g, mg, nb);
+  const size_t smem = rb > 0 ? (size_t)rb * ldY * 2 : 0;
+  cfg.dynamicSmemBytes = smem;
+  if (smem > 48 * 1024) {
+    const cudaError_t ea = cudaFuncSetAttribute(gather_reset_kernel,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)smem);
+    if (ea != cudaSuccess) return ea;
+  }
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gather_reset_kernel, g, mg, nb, rb);
   ++c.launches;
   return e;
 }

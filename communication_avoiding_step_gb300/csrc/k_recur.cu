@@ -29,6 +29,12 @@ RecArgs make_rec_args(const float* G, const float* r, const float* yY, float* al
                       int64_t ldY, int64_t n, float* part, float* w) {
   RecArgs a;
   a.G = G;
+  a.gB = 0;  // packed block-lower G (the far-forming launch sets the band layout)
+  a.X = nullptr;  // rows from Y (the far-forming launch may read them from X instead)
+  a.ldx = 0;
+  a.xseed = a.xctr = 0;
+  a.xm = 0;
+  a.xperm = 0;
   a.r = r;
   a.yY = yY;
   a.alpha = alpha;

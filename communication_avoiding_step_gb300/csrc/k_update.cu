@@ -135,10 +135,12 @@ __global__ void __launch_bounds__(256) update_reduce_kernel(const float* __restr
 // and the row's loss is added in FP64.  Per row the FP32 dot product has the same order
 // as the margins.  Every wait is bounded; on expiry the CTA records ST_TIMEOUT, stops
 // consuming, and its producer waits (bounded) for its copies in flight before exiting.
-constexpr int kLossWarps = 8;                        // consumer warps
+constexpr int kLossWarps = 16;                       // consumer warps
 constexpr int kLossThreads = 32 * (kLossWarps + 1);  // + one producer warp
 constexpr int kLossMaxStages = 8;
-constexpr uint32_t kLossStageBytes = 32 * 1024;
+constexpr uint32_t kLossStageBytes = 64 * 1024;
+constexpr int kLabelAhead = 8;                 // passes a label is copied ahead of its use
+constexpr int kLabelSlots = kLabelAhead + 1;   // ring slots per row slot of a pass
 
 struct LossArgs {
   const uint16_t* X;
@@ -148,6 +150,7 @@ struct LossArgs {
   int R;            // rows per stage
   int nst;          // stages in the ring
   uint32_t stage;   // bytes per stage slot (multiple of 128)
+  uint32_t lring;   // bytes of the label ring (rows per pass x kLabelSlots floats)
   const float* w;
   double* part;
   double* out;
@@ -179,7 +182,8 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_kernel(LossArgs a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t ldv = a.ld / 8;                         // 16-byte vectors per row
   float* w_s = reinterpret_cast<float*>(loss_smem);     // ld floats, zero past n
-  uint8_t* ring = loss_smem + ((a.ld * 4 + 127) / 128) * 128;
+  float* label_ring = reinterpret_cast<float*>(loss_smem + ((a.ld * 4 + 127) / 128) * 128);
+  uint8_t* ring = reinterpret_cast<uint8_t*>(label_ring) + a.lring;
   const int64_t r_lo = a.m * blockIdx.x / gridDim.x;
   const int64_t r_hi = a.m * (blockIdx.x + 1) / gridDim.x;
   const int64_t nchunk = (r_hi - r_lo + a.R - 1) / a.R;
@@ -225,14 +229,27 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_kernel(LossArgs a) {
     const int g = lane & (G - 1);
     const int rows_per_pass = kLossWarps * (32 / G);
     const int my = warp * (32 / G) + lane / G;  // row slot within a pass
-    // the label of this lane's row in pass q0 of chunk ch (0 past the range): loaded one
-    // pass ahead, so its latency hides behind the stage wait and the previous pass
-    auto label = [&](int64_t ch, int q0) -> float {
-      const int64_t row = r_lo + ch * a.R + q0 + my;
+    const int nfull = (int)(a.n / 8);             // vectors wholly inside the n columns
+    // Labels: pass P of the CTA is pass P % ppc of chunk P / ppc.  Lane g == 0 of each row
+    // slot copies its row's label kLabelAhead passes ahead into the slot's shared-memory
+    // ring with a 4-byte cp.async (one commit group per pass, empty where the row does
+    // not exist), so the label's memory latency never stalls a pass.  The ring has one
+    // slot more than the distance: the copy for pass P + kLabelAhead goes into the slot
+    // pass P - 1 read, never into the one the current pass is reading.
+    const int ppc = (a.R + rows_per_pass - 1) / rows_per_pass;
+    float* lring = label_ring + (size_t)my * kLabelSlots;
+    auto issue_label = [&](int64_t P) {
+      const int64_t ch = P / ppc;
+      const int64_t row = r_lo + ch * a.R + (P - ch * ppc) * rows_per_pass + my;
       const int64_t end = r_lo + (ch + 1) * a.R < r_hi ? r_lo + (ch + 1) * a.R : r_hi;
-      return (g == 0 && ch < nchunk && row < end) ? __ldg(a.y + row) : 0.0f;
+      if (g == 0 && ch < nchunk && row < end)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                         smem_u32(lring + (P % kLabelSlots))),
+                     "l"(a.y + row)
+                     : "memory");
+      asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    float ycur = label(0, 0);
+    for (int64_t P = 0; P < kLabelAhead; ++P) issue_label(P);
     for (int64_t ch = 0; ch < nchunk; ++ch) {
       const int st = (int)(ch % a.nst);
       const uint32_t ph = (uint32_t)((ch / a.nst) & 1);
@@ -242,43 +259,79 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_kernel(LossArgs a) {
       const int64_t row0 = r_lo + ch * a.R;
       const int rows = (int)(r_hi - row0 < a.R ? r_hi - row0 : a.R);
       const uint8_t* stg = ring + (size_t)st * a.stage;
-      for (int q0 = 0; q0 < rows; q0 += rows_per_pass) {  // warp-uniform
-        const int q = q0 + my;
+      for (int pp = 0; pp * rows_per_pass < rows; ++pp) {  // warp-uniform
+        const int64_t P = ch * ppc + pp;
+        const int q = pp * rows_per_pass + my;
         const bool live = q < rows;
-        const float ynext = q0 + rows_per_pass < rows ? label(ch, q0 + rows_per_pass)
-                                                      : label(ch + 1, 0);
         const uint4* xr = reinterpret_cast<const uint4*>(stg + (size_t)(live ? q : 0) * a.ld * 2);
-        float acc = 0.0f;
-        for (int64_t v = g; live && v < ldv; v += G) {
-          const int64_t c0 = v * 8;
-          if (c0 >= a.n) break;
-          const uint4 xv = xr[v];
-          const float4 w0 = *reinterpret_cast<const float4*>(w_s + c0);
-          const float4 w1 = *reinterpret_cast<const float4*>(w_s + c0 + 4);
-          const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        // eight independent sums (element e of every vector into sum e), then a fixed tree
+        float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        auto add_full = [&](const uint4 xv, const float (&wv)[8]) {
           const uint32_t pw[4] = {xv.x, xv.y, xv.z, xv.w};
-          if (c0 + 8 <= a.n) {
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              acc = fmaf(__uint_as_float(pw[h] << 16), wv[2 * h], acc);
-              acc = fmaf(__uint_as_float(pw[h] & 0xFFFF0000u), wv[2 * h + 1], acc);
-            }
-          } else {
+          for (int h = 0; h < 4; ++h) {
+            sum[2 * h] = fmaf(__uint_as_float(pw[h] << 16), wv[2 * h], sum[2 * h]);
+            sum[2 * h + 1] = fmaf(__uint_as_float(pw[h] & 0xFFFF0000u), wv[2 * h + 1], sum[2 * h + 1]);
+          }
+        };
+        auto add_vec = [&](const uint4 xv, const float (&wv)[8], int64_t c0) {
+          uint32_t pw[4] = {xv.x, xv.y, xv.z, xv.w};
+          if (c0 + 8 > a.n) {  // columns from n on are not data: zero them
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
               const int64_t cc = c0 + 2 * h;
-              if (cc < a.n) acc = fmaf(bf16_bits_to_float(pw[h] & 0xFFFFu), wv[2 * h], acc);
-              if (cc + 1 < a.n) acc = fmaf(bf16_bits_to_float(pw[h] >> 16), wv[2 * h + 1], acc);
+              if (cc >= a.n) pw[h] = 0;
+              else if (cc + 1 >= a.n) pw[h] &= 0xFFFFu;
             }
           }
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            sum[2 * h] = fmaf(__uint_as_float(pw[h] << 16), wv[2 * h], sum[2 * h]);
+            sum[2 * h + 1] = fmaf(__uint_as_float(pw[h] & 0xFFFF0000u), wv[2 * h + 1], sum[2 * h + 1]);
+          }
+        };
+        // whole vectors (no masking), two at a time; then the partial last vector
+        if (live) {
+          int v = g;
+          for (; v + G < nfull; v += 2 * G) {
+            const uint4 x0 = xr[v], x1 = xr[v + G];
+            const float4* wa = reinterpret_cast<const float4*>(w_s + v * 8);
+            const float4* wb = reinterpret_cast<const float4*>(w_s + (v + G) * 8);
+            const float4 a0 = wa[0], a1 = wa[1], b0 = wb[0], b1 = wb[1];
+            const float wva[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float wvb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            add_full(x0, wva);
+            add_full(x1, wvb);
+          }
+          for (; v < nfull; v += G) {
+            const float4* wa = reinterpret_cast<const float4*>(w_s + v * 8);
+            const float4 a0 = wa[0], a1 = wa[1];
+            const float wva[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            add_full(xr[v], wva);
+          }
+          if (v == nfull && nfull * 8 < a.n) {  // this lane holds the partial vector
+            const float4* wa = reinterpret_cast<const float4*>(w_s + v * 8);
+            const float4 a0 = wa[0], a1 = wa[1];
+            const float wva[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            add_vec(xr[v], wva, (int64_t)v * 8);
+          }
         }
+        float acc = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
         for (int off = G >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);
-        if (live && g == 0) mine += (double)loss_value(a.loss, acc, ycur);
-        ycur = ynext;
+        // this pass's label: every group but the newest kLabelAhead - 1 has landed
+        asm volatile("cp.async.wait_group %0;" ::"n"(kLabelAhead - 1) : "memory");
+        if (live && g == 0) mine += (double)loss_value(a.loss, acc, lring[P % kLabelSlots]);
+        issue_label(P + kLabelAhead);  // into the slot pass P - 1 read
+      }
+      // passes the last chunk does not have keep the pass count (and the ring) in step
+      for (int pp = (rows + rows_per_pass - 1) / rows_per_pass; pp < ppc; ++pp) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(kLabelAhead - 1) : "memory");
+        issue_label(ch * ppc + pp + kLabelAhead);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // no label copy outlives the CTA
     for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
     if (lane == 0) red[warp] = mine;
   }
@@ -353,7 +406,10 @@ cudaError_t launch_loss(const casgd_data_t& d, int loss, const float* w, double*
   a.n = d.n;
   a.ld = d.ld;
   a.loss = loss;
-  a.G = pow2_at_least(d.ld / 8, 32);
+  // G lanes per row, each with at most eight of the row's 16-byte vectors where that
+  // fits in 32 lanes
+  const int64_t nv = (d.n + 7) / 8;
+  a.G = pow2_at_least((nv + 7) / 8, 32);
   a.w = w;
   a.part = part;
   a.out = out_dev;
@@ -366,22 +422,25 @@ cudaError_t launch_loss(const casgd_data_t& d, int loss, const float* w, double*
   a.R = (int)(stage / row_bytes);
   a.stage = (uint32_t)stage;
   const size_t w_bytes = ((size_t)d.ld * 4 + 127) / 128 * 128;
-  const size_t budget = 200 * 1024;
-  int nst = (int)((budget - w_bytes) / stage);
-  if (nst > 6) nst = 6;
-  if (nst < 2) return cudaErrorInvalidValue;  // (n <= 16384 keeps at least 3 stages)
+  const size_t rows_per_pass = (size_t)kLossWarps * (32 / a.G);
+  a.lring = (uint32_t)((rows_per_pass * kLabelSlots * 4 + 127) / 128 * 128);
+  const size_t budget = 216 * 1024;
+  int nst = (int)((budget - w_bytes - a.lring) / stage);
+  if (nst > 4) nst = 4;
+  if (nst < 2) return cudaErrorInvalidValue;  // (n <= 16384 keeps at least 2 stages)
   a.nst = nst;
-  const size_t smem = w_bytes + (size_t)nst * stage;
+  const size_t smem = w_bytes + a.lring + (size_t)nst * stage;
+  void (*const fn)(LossArgs) = loss_kernel;
   int dummy = 0;
-  cudaError_t e = cached_query(c, (const void*)loss_kernel, [&](int& v) {
+  cudaError_t e = cached_query(c, (const void*)fn, [&](int& v) {
     v = 1;
-    return cudaFuncSetAttribute(loss_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)(220 * 1024));
+    return cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(224 * 1024));
   }, dummy);
   if (e != cudaSuccess) return e;
   int64_t blocks = loss_ctas(c.num_sms);
   if (blocks > d.m) blocks = d.m;
-  loss_kernel<<<(unsigned)blocks, kLossThreads, smem, c.stream>>>(a);
+  fn<<<(unsigned)blocks, kLossThreads, smem, c.stream>>>(a);
   ++c.launches;
   return cudaGetLastError();
 }

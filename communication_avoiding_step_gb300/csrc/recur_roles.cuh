@@ -57,6 +57,7 @@ constexpr int kChainRows = 8;     // rows per chain group (a warp per row)
 
 struct RecArgs {
   const float* G;
+  int gB;          // layout of G: 0 packed block-lower, B > 0 band layout (g_block_offset)
   const float* r;  // margins (BF16 values in the recipe)
   const float* yY;
   float* alpha;
@@ -64,6 +65,14 @@ struct RecArgs {
   uint64_t* trace;  // [kMaxS][4] timestamps of chain group 0, warp 0 (null: not traced)
   // fused first stage of the weight update (upd_units > 0): partial rows of Y^T alpha
   const uint16_t* Y;
+  // Rows of Y read straight from X (X non-null; the far-forming launch that gathers its
+  // operands itself): row p of Y is row draw_row(xseed, xctr + p, xm, xperm) of X, whose
+  // pitch is ldx; columns of X from n on are never read
+  const uint16_t* X;
+  int64_t ldx;
+  uint64_t xseed, xctr;
+  uint32_t xm;
+  int xperm;
   float* part;
   int64_t ldY;
   int upd_units;
@@ -281,7 +290,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
     const int nb = j < kB ? j : kB;
 #pragma unroll
     for (int tb = 0; tb < kB; ++tb) {
-      const float* gb = grow0 + (tb < nb ? packed_offset(j, j - 1 - tb, a.b, a.diag) : 0) + lane * 4;
+      const float* gb = grow0 + (tb < nb ? g_block_offset(j, j - 1 - tb, a.b, a.diag, a.gB) : 0) + lane * 4;
 #pragma unroll
       for (int k = 0; k < kKB; ++k) {
         g[tb][k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -458,7 +467,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
       const float* grow0 = a.G + (int64_t)i * a.b;
       for (int tb = 0; tb < nb && ok; ++tb) {
         const int t = j - 1 - tb;
-        const float* gsrc = grow0 + packed_offset(j, t, a.b, a.diag);
+        const float* gsrc = grow0 + g_block_offset(j, t, a.b, a.diag, a.gB);
         const float* asrc = a.alpha + (int64_t)t * a.b;
         constexpr int kX = 2;
         for (int k0 = kKB; k0 < nk && ok; k0 += kX) {
@@ -487,7 +496,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
       const int t0 = j - nb;
       for (int t = t0; t < j && ok; ++t) {
         const float* al = a.alpha + (int64_t)t * a.b;
-        const float* grow = grow0 + packed_offset(j, t, a.b, a.diag);
+        const float* grow = grow0 + g_block_offset(j, t, a.b, a.diag, a.gB);
         for (int col = lane; col < a.b; col += 32) {
           float v;
           if (!(ok = wait_value(al + col, v, a, where_code(2, j)))) break;
@@ -543,7 +552,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
 // the part's values until none is pending.  Fixed
 // order: rows ascending per row-lane, then row-lanes ascending in shared memory.  Y was
 // written by an earlier launch.
-template <int kMode>
+template <int kMode, bool kFromX>
 __device__ void update_unit(const RecArgs& a, int u, int rt) {
   __shared__ float red[32][64];
   // one flag per stage, each written by thread 0 and read by the group after a barrier;
@@ -560,14 +569,19 @@ __device__ void update_unit(const RecArgs& a, int u, int rt) {
   const float* al_j = a.alpha + (int64_t)j * a.b;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   uint4 q[kUpdRows];
+  // (reading X: vectors from column n on are skipped, and the columns past n of the last
+  // vector only reach partial-row columns that are never added to w)
+  const bool xin = kFromX ? vec * 8 < a.n : vin;
   auto load_rows = [&](int i0) {
 #pragma unroll
     for (int k = 0; k < kUpdRows; ++k) {
       const int i = i0 + 32 * k;
       const int64_t row = (int64_t)j * a.b + i;
-      q[k] = (i < r1 && vin)
-                 ? __ldg(reinterpret_cast<const uint4*>(a.Y + row * a.ldY + vec * 8))
-                 : make_uint4(0, 0, 0, 0);
+      const uint16_t* src =
+          kFromX ? a.X + (int64_t)draw_row(a.xseed, a.xctr + (uint64_t)row, a.xm, a.xperm) * a.ldx
+                 : a.Y + row * a.ldY;
+      q[k] = (i < r1 && xin) ? __ldg(reinterpret_cast<const uint4*>(src + vec * 8))
+                             : make_uint4(0, 0, 0, 0);
     }
   };
   load_rows(r0 + tr);
@@ -710,6 +724,7 @@ __device__ void update_unit(const RecArgs& a, int u, int rt) {
 // up to 32), 32/mG rows per warp and pass; lane g sums the vectors g, g+mG, ... in FP32,
 // eight elements each in column order, the row's lanes then add by a shuffle tree, and
 // its first lane stores the margin (rounded once to BF16, or FP32 with MARGINS_FP32).
+template <bool kFromX>
 __device__ void margin_unit(const RecArgs& a, int u, int rt) {
   const int G = a.mG;
   const int warp = rt >> 5, lane = rt & 31;
@@ -720,7 +735,10 @@ __device__ void margin_unit(const RecArgs& a, int u, int rt) {
   for (int64_t p0 = (int64_t)u * a.mrows; p0 < p_end; p0 += rows_pass) {
     const int64_t p = p0 + warp * (32 / G) + lane / G;
     const bool live = p < p_end;
-    const uint16_t* yr = a.Y + (live ? p : 0) * a.ldY;
+    const uint16_t* yr =
+        kFromX ? a.X + (int64_t)draw_row(a.xseed, a.xctr + (uint64_t)(live ? p : 0), a.xm,
+                                         a.xperm) * a.ldx
+               : a.Y + (live ? p : 0) * a.ldY;
     float acc = 0.0f;
     constexpr int kBatch = 8;
     for (int64_t v0 = g; v0 < nvec; v0 += (int64_t)G * kBatch) {
@@ -728,14 +746,23 @@ __device__ void margin_unit(const RecArgs& a, int u, int rt) {
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         const int64_t v = v0 + (int64_t)k * G;
-        q[k] = (live && v < nvec) ? __ldg(reinterpret_cast<const uint4*>(yr + v * 8))
-                                  : make_uint4(0, 0, 0, 0);
+        q[k] = (live && v < nvec && (!kFromX || v * 8 < a.n))
+                   ? __ldg(reinterpret_cast<const uint4*>(yr + v * 8))
+                   : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         const int64_t c0 = (v0 + (int64_t)k * G) * 8;
         if (c0 >= a.n) break;
-        const uint32_t pw[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+        uint32_t pw[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+        if (kFromX && c0 + 8 > a.n) {  // columns from n on: zero (X's padding is not data)
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int64_t c = c0 + 2 * h;
+            if (c >= a.n) pw[h] = 0;
+            else if (c + 1 >= a.n) pw[h] &= 0xFFFFu;
+          }
+        }
         float wv[8];
         if (a.wm_vec && c0 + 8 <= a.n) {
           const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.wm + c0));
@@ -773,7 +800,7 @@ __device__ void margin_unit(const RecArgs& a, int u, int rt) {
 // in block order, so the update keeps pace with the chain instead of queueing behind
 // the far units; when no update units are left they turn to far units, and the other
 // groups turn to update units once the far units are gone.
-template <int kMode>
+template <int kMode, bool kFromX = false>
 __device__ void bulk_role(const RecArgs& a, int rt, bool upd_group) {
   constexpr bool kInFlight = kMode == 1 || kMode == 3;
   __shared__ int s_unit, s_lead;
@@ -803,14 +830,14 @@ __device__ void bulk_role(const RecArgs& a, int rt, bool upd_group) {
     group_sync<kMode != 0>();
     if (unit >= a.bulk_units) {
       if (unit < a.bulk_units + a.upd_units) {
-        update_unit<kMode>(a, unit - a.bulk_units, rt);
+        update_unit<kMode, kFromX>(a, unit - a.bulk_units, rt);
         group_sync<kMode != 0>();
         continue;
       }
       return;
     }
     if (a.margins) {  // the bulk units are margin units
-      margin_unit(a, unit, rt);
+      margin_unit<kFromX>(a, unit, rt);
       group_sync<kMode != 0>();
       continue;
     }

@@ -136,6 +136,19 @@ enum {
                                               uses it, as when G is summed across
                                               processes in BF16; stored blocks (and the
                                               G_out tap) hold the rounded values      */
+#define CASGD_FLAG_GATHER_ROWS       0x4000u /* the far-forming launch reads its rows
+                                              straight from X: the Gram's producer warp
+                                              draws the sampled indices itself and loads
+                                              four rows per tile::gather4 TMA copy, and
+                                              the margin and update units read X rows
+                                              through the same sampler, so the rows are
+                                              never gathered into a copy Y (only the
+                                              indices and labels are).  Same results bit
+                                              for bit; measured 4x slower on GB300 at
+                                              n = 2000 (one small TMA copy per four rows
+                                              and 64 columns), so off by default.
+                                              Ignored where the far-forming Gram does
+                                              not apply or indices are given (idx_in)  */
 #define CASGD_FLAG_TEST_STALL        0x80000000u /* test only: the recurrence's first
                                               block never signals completion, so every
                                               waiter runs into its time bound and the

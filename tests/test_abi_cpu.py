@@ -52,8 +52,8 @@ def test_workspace_size_host_only(lib):
     nbytes = C.c_size_t(0)
     assert lib.casgd_workspace_size(C.byref(d), C.byref(p), C.byref(nbytes)) == 0
     S = 256 * 32
-    g = 32 * 31 // 2 * 256 * 256 * 4
-    assert nbytes.value >= g + S * 2000 * 2 + S * 14
+    g = 2 * 90 * 256 * 256 * 4   # two band-layout G buffers of the far-forming default
+    assert nbytes.value >= g + 2 * S * 2048 * 2 + S * 14
     assert nbytes.value % 256 == 0
     bad = nat.Params(256, 32, 0.5, 7, 0, 0, 0)
     assert lib.casgd_workspace_size(C.byref(d), C.byref(bad), C.byref(nbytes)) == nat.CASGD_ERR_ARG
@@ -63,7 +63,7 @@ def test_unknown_flag_bits_rejected(lib):
     # bit 0x10 named the cluster-multicast Gram, which the library no longer has
     d = nat.Data(1000, 2000, 2000, 0, 0)
     nbytes = C.c_size_t(0)
-    for flags in (0x10, 0x4000, 0x40000000):
+    for flags in (0x10, 0x8000, 0x40000000):
         p = nat.Params(256, 32, 0.5, 0, 0, flags, 0)
         assert lib.casgd_workspace_size(C.byref(d), C.byref(p), C.byref(nbytes)) == nat.CASGD_ERR_ARG
     known = (nat.FLAG_WRITE_DIAG_BLOCKS | nat.FLAG_GRAM_TENSOR | nat.FLAG_GRAM_PAIR
@@ -84,29 +84,43 @@ def _a(x):  # 256-byte sections
     return (x + 255) // 256 * 256
 
 
+def _band_blocks(s, B):
+    return sum(min(j, B) for j in range(s))
+
+
 def test_workspace_sections_of_the_gram_paths(lib):
     # b = 256, s = 32, n = 2000: the stored-G launch shared with the recurrence (FULL_G)
     # adds a second idx, y_Y, Y and G for casgd_train's iteration-ahead Gram; the
-    # far-forming default adds to that the far partials (one column group per block:
-    # S x s floats) and the update's running sum w_acc (n floats)
+    # far-forming default keeps both G buffers in the band layout (the B = 3 blocks
+    # below the diagonal of each block row: 90 of the 496 blocks) and adds the far
+    # partials (one column group per block: S x s floats) and the update's running sum
+    # w_acc (n floats)
     n, b, s = 2000, 256, 32
-    S, ld = b * s, 2000
+    S, ld = b * s, 2048          # Y rows padded to whole 128-byte lines
     G = s * (s - 1) // 2 * b * b * 4
+    Gb = _band_blocks(s, 3) * b * b * 4
+    assert _band_blocks(s, 3) == 90
     no_fuse = _ws_bytes(lib, n, b, s, nat.FLAG_NO_FUSE)
     full_g = _ws_bytes(lib, n, b, s, nat.FLAG_FULL_G)
     far = _ws_bytes(lib, n, b, s, 0)
     assert full_g - no_fuse == 2 * _a(S * 4) + _a(S * ld * 2) + _a(G)
-    assert far - full_g == _a(S * s * 1 * 4) + _a(n * 4)
+    assert far - full_g == 2 * _a(Gb) - 2 * _a(G) + _a(S * s * 1 * 4) + _a(n * 4)
     # b = 1024, s = 16, n = 18: the stored G is not shared with the recurrence there
-    # (b > 512), so only the far-forming path has second buffers; four column groups
-    # per block keep a row's far partials within 64
+    # (b > 512), so only the far-forming path has second buffers; its band is one block
+    # wide; four column groups per block keep a row's far partials within 64
     n, b, s = 18, 1024, 16
     S, ld = b * s, 24
     G = s * (s - 1) // 2 * b * b * 4
+    Gb = _band_blocks(s, 1) * b * b * 4
     full_g = _ws_bytes(lib, n, b, s, nat.FLAG_FULL_G)
     far = _ws_bytes(lib, n, b, s, 0)
-    assert far - full_g == (2 * _a(S * 4) + _a(S * ld * 2) + _a(G) + _a(S * s * 4 * 4)
-                            + _a(n * 4))
+    assert far - full_g == (2 * _a(S * 4) + _a(S * ld * 2) + 2 * _a(Gb) - _a(G)
+                            + _a(S * s * 4 * 4) + _a(n * 4))
+    # least squares 11,000,000 x 28 at b = 2048, s = 32 (S = 65536): 31 band blocks of
+    # 16 MiB per buffer instead of 496 (8.3 GB) in the packed block-lower layout
+    far = _ws_bytes(lib, 28, 2048, 32, 0)
+    full_g = _ws_bytes(lib, 28, 2048, 32, nat.FLAG_FULL_G)
+    assert far < 1.2e9 < 8.3e9 < full_g
 
 
 def test_argument_errors_before_any_cuda_call(lib):

@@ -413,6 +413,47 @@ def test_far_from_gram_is_the_default(gpu_lib):
     assert _rel(out["full"][1], out["default"][1]) <= 1e-5
 
 
+@pytest.mark.parametrize("cid,m,flags", [(2, 20000, 0), (5, 20000, 0),
+                                         (5, 20000, "permuted"), (3, 60000, 0)])
+def test_far_gram_gathers_rows_like_copied_rows(gpu_lib, cid, m, flags):
+    """With CASGD_FLAG_GATHER_ROWS the far-forming launch reads its rows straight from X
+    (the Gram's producer draws the sampled indices and gathers four rows per TMA copy; the
+    margin and update units read X the same way).  By default, and with the indices given,
+    the rows are first copied into Y and read from there.  All three are the same
+    arithmetic on the same values, so one outer iteration agrees bit for bit (indices,
+    alpha and w), and so does a pipelined casgd_train of three iterations."""
+    casgd = gpu_lib
+    p = si.make_problem(cid, m=m)
+    r = p.recipe
+    fl = casgd.FLAG_SAMPLE_PERMUTED if flags == "permuted" else 0
+    pg = casgd.Params(r.b, r.s, r.eta, r.loss, seed=5, flags=fl | casgd.FLAG_GATHER_ROWS)
+    pc = casgd.Params(r.b, r.s, r.eta, r.loss, seed=5, flags=fl)
+    data = _dev(p, casgd)
+    w0 = si.random_weights(p.n, seed=8, scale=0.3)
+    w_g, taps_g, st = _run_step(casgd, data, pg, w0, k=2)            # rows from X
+    assert st == 0
+    w_c, taps_c, st = _run_step(casgd, data, pc, w0, k=2)            # rows copied into Y
+    assert st == 0
+    w_i, taps_i, st = _run_step(casgd, data, pg, w0, k=2, idx_in=taps_g.idx_out)  # given
+    assert st == 0
+    for w_, t_ in ((w_c, taps_c), (w_i, taps_i)):
+        assert np.array_equal(t_.idx_out.cpu().numpy(), taps_g.idx_out.cpu().numpy())
+        assert np.array_equal(t_.alpha_out.cpu().numpy().view(np.uint32),
+                              taps_g.alpha_out.cpu().numpy().view(np.uint32))
+        assert np.array_equal(w_.view(np.uint32), w_g.view(np.uint32))
+    ref = oracle.outer_step(p.X, p.y, w0, r.b, r.s, r.eta, r.loss, 5, 2, mode="emulate",
+                            permuted=bool(fl))
+    assert _rel(w_g, ref) <= W_TOL
+    out = []
+    for params in (pg, pc):
+        ws = casgd.workspace(data, params)
+        w = torch.from_numpy(w0.copy()).cuda()
+        _, _, kind = casgd.train(data, params, w, 3, ws, k0=1)
+        assert kind == 6 and casgd.get_status(ws) == 0
+        out.append(w.cpu().numpy())
+    assert np.array_equal(out[0].view(np.uint32), out[1].view(np.uint32))
+
+
 def test_far_from_gram_unsupported_shapes(gpu_lib):
     """The flag needs b a multiple of 256, s >= 2 and the paired kernel in the same
     launch; anything else is CASGD_ERR_UNSUPPORTED and launches nothing."""
