@@ -325,23 +325,51 @@ __device__ void gather_rows_bulk(const RowArgs& a, int64_t blk, int RB, uint8_t*
                    "r"(smem_u32(sm + (size_t)i * pitch)), "r"(pitch)
                    : "memory");
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // stored before the CTA leaves
+    // the stores have read shared memory before the CTA leaves (their writes complete
+    // with the grid, before the next launch's wait for it returns)
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   }
 }
 
-// Blocks [0, nb_g) gather rows (g: the next iteration's, or this one's for a single
-// step), the others reset this iteration's recurrence state (mg).  rb > 0: wide rows by
-// bulk copies, rb per block (dynamic shared memory rb * ldY * 2 bytes).
-__global__ void __launch_bounds__(256) gather_reset_kernel(RowArgs g, RowArgs mg, int64_t nb_g,
-                                                           int rb) {
+// The per-row part of the reset for rows [p_lo, p_hi) (as reset_rows).
+__device__ void reset_row_range(const RowArgs& a, int64_t p_lo, int64_t p_hi) {
+  const float pend = __uint_as_float(kAlphaPending);
+  for (int64_t p = p_lo + threadIdx.x; p < p_hi; p += blockDim.x) {
+    a.alpha[p] = pend;
+    a.far[p] = pend;
+    a.r[p] = pend;
+  }
+  if (!a.fpart) return;
+  const int lane = threadIdx.x & 31;
+  for (int64_t p = p_lo + (threadIdx.x >> 5); p < p_hi; p += blockDim.x >> 5) {
+    const int nfar = ((int)(p / a.fb) - a.fB) * a.fnp;
+    float* row = a.fpart + p * a.fs;
+    for (int t = lane; t < nfar; t += 32) row[t] = pend;
+  }
+}
+
+// Wide rows by bulk copies: block `blk` gathers rows [blk*rb, blk*rb + rb) of g and
+// resets the same rows of this iteration's recurrence state (mg); block 0 also the
+// counters and queues.  Few registers, so several blocks share an SM (their rows'
+// bytes in flight add up).
+__global__ void __launch_bounds__(256, 4) gather_bulk_reset_kernel(RowArgs g, RowArgs mg, int rb) {
   extern __shared__ __align__(128) uint8_t gather_smem[];
   wait_prior_grid();  // the previous launch reads the buffers this one writes
   allow_next_grid();  // the next launch may take SMs as this one's blocks leave
+  const int64_t blk = blockIdx.x;
+  if (blk == 0) reset_recurrence(mg);
+  const int64_t p_lo = blk * rb;
+  reset_row_range(mg, p_lo, p_lo + rb < mg.S ? p_lo + rb : mg.S);
+  gather_rows_bulk(g, blk, rb, gather_smem);
+}
+
+// Blocks [0, nb_g) gather rows (g: the next iteration's, or this one's for a single
+// step), the others reset this iteration's recurrence state (mg).
+__global__ void __launch_bounds__(256) gather_reset_kernel(RowArgs g, RowArgs mg, int64_t nb_g) {
+  wait_prior_grid();  // the previous launch reads the buffers this one writes
+  allow_next_grid();  // the next launch may take SMs as this one's blocks leave
   if ((int64_t)blockIdx.x < nb_g) {
-    if (rb > 0)
-      gather_rows_bulk(g, blockIdx.x, rb, gather_smem);
-    else
-      gather_rows<true, false>(g, blockIdx.x);
+    gather_rows<true, false>(g, blockIdx.x);
   } else {
     const int64_t blk = (int64_t)blockIdx.x - nb_g;
     if (blk == 0) reset_recurrence(mg);
@@ -498,21 +526,27 @@ cudaError_t launch_gather_reset(const casgd_data_t& d, const casgd_params_t& p, 
   }
   const RowArgs mg = row_args(d, p, nullptr, 0, nullptr, nullptr, nullptr, ldY, r, nullptr, alpha,
                               far, fpart, ctrl, slab);
-  const int64_t nb = gather ? (rb > 0 ? (g.S + rb - 1) / rb : row_blocks(g)) : 0;
+  cudaLaunchAttribute attr[1];
+  if (gather && rb > 0 && g.S == mg.S) {  // bulk rows; each block resets its own rows
+    cudaLaunchConfig_t cfg = plain_config((unsigned)((g.S + rb - 1) / rb), c, attr);
+    const size_t smem = (size_t)rb * ldY * 2;
+    cfg.dynamicSmemBytes = smem;
+    if (smem > 48 * 1024) {
+      const cudaError_t ea = cudaFuncSetAttribute(gather_bulk_reset_kernel,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  (int)smem);
+      if (ea != cudaSuccess) return ea;
+    }
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gather_bulk_reset_kernel, g, mg, rb);
+    ++c.launches;
+    return e;
+  }
+  const int64_t nb = gather ? row_blocks(g) : 0;
   const int64_t work = mg.fpart ? mg.S * mg.fs : mg.S;  // reset slots
   int64_t nr = (work + 255) / 256;
   if (nr > (int64_t)c.num_sms * 4) nr = (int64_t)c.num_sms * 4;
-  cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = plain_config((unsigned)(nb + nr), c, attr);
-  const size_t smem = rb > 0 ? (size_t)rb * ldY * 2 : 0;
-  cfg.dynamicSmemBytes = smem;
-  if (smem > 48 * 1024) {
-    const cudaError_t ea = cudaFuncSetAttribute(gather_reset_kernel,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)smem);
-    if (ea != cudaSuccess) return ea;
-  }
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gather_reset_kernel, g, mg, nb, rb);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gather_reset_kernel, g, mg, nb);
   ++c.launches;
   return e;
 }

@@ -181,7 +181,11 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_kernel(LossArgs a) {
   __shared__ bool s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t ldv = a.ld / 8;                         // 16-byte vectors per row
-  float* w_s = reinterpret_cast<float*>(loss_smem);     // ld floats, zero past n
+  // w in two planes of ld/2 floats: plane 0 holds columns 8v..8v+3 of each 16-byte
+  // vector v at 4v, plane 1 columns 8v+4..8v+7, so a warp's 16-byte reads of w for
+  // consecutive vectors are contiguous (zero past n)
+  float* w_s = reinterpret_cast<float*>(loss_smem);
+  float* w_s1 = w_s + a.ld / 2;
   float* label_ring = reinterpret_cast<float*>(loss_smem + ((a.ld * 4 + 127) / 128) * 128);
   uint8_t* ring = reinterpret_cast<uint8_t*>(label_ring) + a.lring;
   const int64_t r_lo = a.m * blockIdx.x / gridDim.x;
@@ -195,7 +199,8 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_kernel(LossArgs a) {
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  for (int64_t c = threadIdx.x; c < a.ld; c += blockDim.x) w_s[c] = c < a.n ? a.w[c] : 0.0f;
+  for (int64_t c = threadIdx.x; c < a.ld; c += blockDim.x)
+    ((c & 4) ? w_s1 : w_s)[(c >> 3) * 4 + (c & 3)] = c < a.n ? a.w[c] : 0.0f;
   __syncthreads();
 
   double mine = 0.0;
@@ -295,23 +300,24 @@ __global__ void __launch_bounds__(kLossThreads, 1) loss_kernel(LossArgs a) {
           int v = g;
           for (; v + G < nfull; v += 2 * G) {
             const uint4 x0 = xr[v], x1 = xr[v + G];
-            const float4* wa = reinterpret_cast<const float4*>(w_s + v * 8);
-            const float4* wb = reinterpret_cast<const float4*>(w_s + (v + G) * 8);
-            const float4 a0 = wa[0], a1 = wa[1], b0 = wb[0], b1 = wb[1];
+            const float4 a0 = *reinterpret_cast<const float4*>(w_s + v * 4);
+            const float4 a1 = *reinterpret_cast<const float4*>(w_s1 + v * 4);
+            const float4 b0 = *reinterpret_cast<const float4*>(w_s + (v + G) * 4);
+            const float4 b1 = *reinterpret_cast<const float4*>(w_s1 + (v + G) * 4);
             const float wva[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             const float wvb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
             add_full(x0, wva);
             add_full(x1, wvb);
           }
           for (; v < nfull; v += G) {
-            const float4* wa = reinterpret_cast<const float4*>(w_s + v * 8);
-            const float4 a0 = wa[0], a1 = wa[1];
+            const float4 a0 = *reinterpret_cast<const float4*>(w_s + v * 4);
+            const float4 a1 = *reinterpret_cast<const float4*>(w_s1 + v * 4);
             const float wva[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             add_full(xr[v], wva);
           }
           if (v == nfull && nfull * 8 < a.n) {  // this lane holds the partial vector
-            const float4* wa = reinterpret_cast<const float4*>(w_s + v * 8);
-            const float4 a0 = wa[0], a1 = wa[1];
+            const float4 a0 = *reinterpret_cast<const float4*>(w_s + v * 4);
+            const float4 a1 = *reinterpret_cast<const float4*>(w_s1 + v * 4);
             const float wva[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             add_vec(xr[v], wva, (int64_t)v * 8);
           }
