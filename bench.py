@@ -8,10 +8,11 @@ flips), b=256, s=32 (Gram 8192 x 8192), eta=0.5, 50 outer iterations per step, s
 synthetic (the epsilon data set it stands in for is not available).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--config 1..5] [--s S]
+                       [--config 1..5] [--s S] [--sharded]
 N > 1 runs under torchrun, one process per GPU: independent replicas (one GPU's
 problem per rank, no collective on the data path); value = samples of all ranks / max
-time.  `--impl reference` times the CPU oracle (the plain NumPy statement of the
+time.  `--sharded` instead splits one problem's features over the ranks, with one FP32
+all-reduce (NCCL) of the Gram matrix and the margins per outer iteration.  `--impl reference` times the CPU oracle (the plain NumPy statement of the
 method) on the host cores, on a bounded sample of the same workload.
 
 `value` comes from K steps called as a user calls them; a second pass of K steps with
@@ -60,6 +61,10 @@ def parse():
                     help="skip the FP32 plain SGD comparison leg")
     ap.add_argument("--m", type=int, default=None,
                     help="override the row count (small profiling captures only)")
+    ap.add_argument("--sharded", action="store_true",
+                    help="the paper's feature-sharded setting: each rank holds a slice of the "
+                         "columns, one FP32 all-reduce of G and the margins per outer iteration "
+                         "(torch.distributed, NCCL); strong scaling (one problem)")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the other workloads' lines (recipes 3, 4 with s = 4..32, 5)")
     ap.add_argument("--config-steps", type=int, default=3,
@@ -393,6 +398,76 @@ def extra_configs(args, torch, casgd, rank, pk):
     return out
 
 
+def run_sharded(args):
+    """Feature-sharded CA-SGD over the ranks of a torchrun job (one rank: the exchange is
+    the identity).  Every rank draws the same rows; rank q holds columns
+    [q*n/N, (q+1)*n/N) of X and of w.  A step = `iters` outer iterations; value = the
+    problem's samples per second (every rank works on the same samples)."""
+    import torch
+    import communication_avoiding_step_gb300 as casgd
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    casgd.load()
+    r, s, iters = workload(args.config, args.s, args.m)
+    S = r.b * s
+    p = si.make_problem(args.config, m=args.m)
+    c0, c1 = r.n * rank // world, r.n * (rank + 1) // world
+    X32 = torch.from_numpy(np.ascontiguousarray(p.X[:, c0:c1])).cuda()
+    data = casgd.Dataset.from_fp32(X32, torch.from_numpy(p.y).cuda())
+    del X32
+    params = casgd.Params(r.b, s, r.eta, r.loss, seed=0, flags=args.flags)
+    ws = casgd.workspace_sharded(data, params)
+    xbuf = casgd.exchange_buffer(params)
+    w = torch.zeros(c1 - c0, device="cuda")
+    all_reduce = dist.all_reduce if dist else None
+    k = 0
+    for _ in range(args.warmup):
+        w.zero_()
+        casgd.train_sharded(data, params, w, iters, ws, xbuf, all_reduce, k0=k)
+        k += iters
+    stream = torch.cuda.current_stream()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches = 0
+    with ClockSampler(local) as clocks:
+        t0.record(stream)
+        for _ in range(args.steps):
+            w.zero_()
+            n_l, _ = casgd.train_sharded(data, params, w, iters, ws, xbuf, all_reduce, k0=k)
+            launches += n_l
+            k += iters
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    elapsed = world_max(t0.elapsed_time(t1) / 1e3, torch.device("cuda", local))
+    if rank == 0:
+        xb = xbuf.numel() * 4
+        out = {"metric": METRIC, "value": S * iters * args.steps / elapsed, "unit": "samples/s",
+               "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+               "ms_per_step": elapsed * 1e3 / args.steps, "higher_is_better": True,
+               "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+               "data": "synthetic",
+               "config": dict(workload_config(r, s, iters, S, p.m),
+                              sharded=f"features split over {world} rank(s); one FP32 "
+                                      f"all-reduce of {xb / 1e6:.1f} MB per outer iteration"),
+               "parallelism": f"feature-sharded x{world}", "gpu_launches": launches,
+               "clocks": clocks.summary()}
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
 def run_ours(args):
     import torch
     import communication_avoiding_step_gb300 as casgd
@@ -632,6 +707,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.sharded:
+        run_sharded(args)
     else:
         run_ours(args)
 

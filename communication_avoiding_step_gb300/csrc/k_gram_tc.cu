@@ -80,7 +80,25 @@ struct TcArgs {
   uint64_t seed, ctr_g, ctr_f;
   uint32_t m;
   int perm_d;
+  // Weighted deal of the work items to the CTA pairs: the first pc pairs (those whose
+  // CTAs also run the recurrence's chain) take wa items for every wb the other pairs
+  // take (wa <= wb; wa == wb: plain round robin)
+  int pc, wa, wb;
 };
+
+// The kq-th work item of pair cid of ncl, in increasing order: items are dealt in rounds
+// of pc*wa + (ncl-pc)*wb; sub-round s < wa of a round gives one item to every pair (in
+// pair order), sub-rounds wa..wb-1 one to every pair from pc on.
+__device__ __forceinline__ int unit_of(const TcArgs& a, int cid, int ncl, int kq) {
+  if (a.wa == a.wb) return cid + kq * ncl;
+  const bool chain = cid < a.pc;
+  const int W = chain ? a.wa : a.wb;
+  const int r = kq / W, sub = kq - r * W;
+  const int R = a.pc * a.wa + (ncl - a.pc) * a.wb;
+  const int off = sub < a.wa ? sub * ncl : a.wa * ncl + (sub - a.wa) * (ncl - a.pc);
+  const int pos = sub < a.wa ? cid : cid - a.pc;
+  return r * R + off + pos;
+}
 
 struct SharedCtl {
   uint64_t full[kStages];
@@ -593,6 +611,9 @@ constexpr size_t pair_smem_bytes() {
 static_assert(pair_smem_bytes<kStagesPair>() <= 232448, "dynamic shared memory per CTA");
 static_assert(pair_smem_bytes<kStagesFused, true>() + 9 * 1024 <= 232448, "with the recurrence");
 constexpr int kFusedThreads = kThreads + kRecThreads;  // 6 Gram warps + 8 recurrence warps
+// Gram items per round of a pair that also runs the chain, and of the other pairs
+constexpr int kChainPairShare = 1;
+constexpr int kOtherPairShare = 1;
 constexpr uint32_t kIdesc2 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                              ((uint32_t)(256 >> 4) << 24);
 
@@ -718,7 +739,9 @@ __device__ bool stage_alpha(const TcArgs& a, const float* src, float* dst, int l
         if (pending4(v1)) v1 = ld_volatile_f4(src + 128 + lane * 4);
         if (!__any_sync(0xffffffffu, pending4(v0) || pending4(v1))) break;
       }
-      __nanosleep(fin ? 32 : 128);
+      // long sleeps while the probe is pending: hundreds of waiting warps polling the lines
+      // the chain writes slowed the launch (measured: 128 ns 132 us, 512 ns 128 us)
+      __nanosleep(fin ? 64 : 512);
       int stop = 0;
       if (lane == 0) {
         if (ld_volatile_u32(&a.ctrl->abort)) {
@@ -864,7 +887,8 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool live = true;
-    for (int u = cid; u < a.ntiles && live; u += ncl) {
+    for (int kq = 0, u = unit_of(a, cid, ncl, 0); u < a.ntiles && live;
+         u = unit_of(a, cid, ncl, ++kq)) {
       live = __shfl_sync(0xffffffffu, sc->abort ? 0 : 1, 0) != 0;
       if (!live) break;
       int rg, ca0, nq, t, pidx;
@@ -911,7 +935,8 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
       WorkCursor<kFar> cur;
       int stage = 0;
       uint32_t phase = 0;
-      for (int u = cid; u < a.ntiles && !sc->abort; u += ncl) {
+      for (int kq = 0, u = unit_of(a, cid, ncl, 0); u < a.ntiles && !sc->abort;
+           u = unit_of(a, cid, ncl, ++kq)) {
         int rg, ca0, nq, t, pidx;
         bool far;
         cur.seek(a, u, rg, ca0, nq, t, pidx, far);
@@ -945,7 +970,8 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
       uint32_t tphase[2] = {0, 0};
       int iter = 0;  // tiles issued (accumulator buffer iter & 1)
       bool any = false, ok = true;
-      for (int u = cid; u < a.ntiles && ok && !sc->abort; u += ncl) {
+      for (int kq = 0, u = unit_of(a, cid, ncl, 0); u < a.ntiles && ok && !sc->abort;
+           u = unit_of(a, cid, ncl, ++kq)) {
         int rg, ca0, nq, t, pidx;
         bool far;
         cur.seek(a, u, rg, ca0, nq, t, pidx, far);
@@ -999,7 +1025,8 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
     uint32_t tphase[2] = {0, 0};
     int iter = 0;
     bool live = true, dead = false;  // live: the Gram's own waits succeed; dead: alpha gone
-    for (int u = cid; u < a.ntiles && live; u += ncl) {
+    for (int kq = 0, u = unit_of(a, cid, ncl, 0); u < a.ntiles && live;
+         u = unit_of(a, cid, ncl, ++kq)) {
       int rg, ca0, nq, t, pidx;
       bool far;
       cur.seek(a, u, rg, ca0, nq, t, pidx, far);
@@ -1168,6 +1195,8 @@ cudaError_t plan_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
   a.seed = a.ctr_g = a.ctr_f = 0;
   a.m = 0;
   a.perm_d = 0;
+  a.pc = 0;
+  a.wa = a.wb = 1;
   // count the needed tiles on the host with the same rule the kernel walks
   int64_t total = 0;
   for (int g = 0; g * kcl < a.TR; ++g) {
@@ -1498,6 +1527,10 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
   }
   if (rec.C < 1) return cudaErrorNotSupported;
   rec.upd_groups = rec.margins ? 0 : update_groups(rec, grid - rec.C);
+  // the pairs whose CTAs also run the chain (CTAs 0 .. C-1) take fewer Gram items
+  P.a.pc = (rec.C + 1) / 2;
+  P.a.wa = kChainPairShare;
+  P.a.wb = kOtherPairShare;
   if (far_gram && next) {
     const int nfar = P.a.ntiles - P.a.n_stored;
     P.a.far_head = nfar < grid / 2 ? nfar : grid / 2;
