@@ -36,7 +36,6 @@ struct Resolved {
   int32_t* idx2;
   float* yY2;
   float* fpart;  // far partial sums of the far-forming Gram (null: not laid out)
-  float* w_acc;  // its update's running sum (null: not laid out)
   float* upd;
   double* loss_part;
   double* loss_slots;
@@ -95,7 +94,6 @@ Resolved resolve(void* ws, const Layout& L) {
   R.idx2 = L.off_idx2 ? reinterpret_cast<int32_t*>(base + L.off_idx2) : nullptr;
   R.yY2 = L.off_yY2 ? reinterpret_cast<float*>(base + L.off_yY2) : nullptr;
   R.fpart = L.off_fpart ? reinterpret_cast<float*>(base + L.off_fpart) : nullptr;
-  R.w_acc = L.off_wacc ? reinterpret_cast<float*>(base + L.off_wacc) : nullptr;
   R.upd = reinterpret_cast<float*>(base + L.off_upd);
   R.loss_part = reinterpret_cast<double*>(base + L.off_loss);
   R.loss_slots = R.loss_part + kLossCtas;
@@ -233,7 +231,7 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
     // on one GPU it is the identity.)
     CK(launch_gram_recur(R.Y, G, false, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss, p->flags,
                          G, R.Y, R.r, R.yY, R.alpha, R.far, R.slab, gp.far ? R.fpart : nullptr,
-                         R.upd, w, gp.far ? R.w_acc : nullptr, R.ctrl, p->timeout_us,
+                         R.upd, w, gp.far, R.ctrl, p->timeout_us,
                          /*g_band=*/G == R.G, gather ? &rs : nullptr, ctr, ctr, c));
     if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
   } else {
@@ -335,14 +333,14 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
       CK(launch_gram_recur(gather ? nullptr : (it + 1 < iters ? Yb[nxt] : nullptr), Gb[nxt],
                            true, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss, p->flags,
                            Gb[cur], gather ? nullptr : Yb[cur], R.r, yb[cur], R.alpha, R.far,
-                           R.slab, fpart, R.upd, w, R.w_acc, R.ctrl, p->timeout_us,
+                           R.slab, fpart, R.upd, w, true, R.ctrl, p->timeout_us,
                            /*g_band=*/true, rsp,
                            it + 1 < iters ? (k + 1) * (uint64_t)L.S : kNoRows,
                            k * (uint64_t)L.S, c));
     else if (it + 1 < iters)
       CK(launch_gram_recur(Yb[nxt], Gb[nxt], true, L.S, d->n, L.ldY, p->b, p->s, p->eta,
                            p->loss, p->flags, Gb[cur], Yb[cur], R.r, yb[cur], R.alpha, R.far,
-                           R.slab, nullptr, R.upd, w, nullptr, R.ctrl, p->timeout_us, false,
+                           R.slab, nullptr, R.upd, w, false, R.ctrl, p->timeout_us, false,
                            nullptr, 0, 0, c));
     else
       CK(launch_recur(Gb[cur], R.r, yb[cur], R.alpha, R.far, R.slab, p->b, p->s, p->eta,
@@ -526,12 +524,9 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms,
     L.off_G2 = off;  // the far-forming Gram stores the next iteration's band into it
     off += align_up((size_t)L.gram_elems * sizeof(float));
   }
-  L.off_wacc = 0;
   if (gp.far) {
     L.off_fpart = off;
     off += align_up((size_t)L.S * s * far_partials_per_block(b, s) * sizeof(float));
-    L.off_wacc = off;
-    off += align_up((size_t)n * sizeof(float));
   }
   L.total = off;
   return L;

@@ -75,7 +75,6 @@ struct Layout {
   size_t off_idx, off_r, off_yY, off_alpha, off_far, off_Y, off_G, off_upd, off_loss;
   size_t off_Y2, off_G2, off_idx2, off_yY2;  // 0: no second buffers
   size_t off_fpart;  // far partial sums FP32[S][s * npb] of the far-forming Gram (0: none)
-  size_t off_wacc;   // its update's running sum FP32[n] (0: none)
   size_t total;
 };
 
@@ -449,9 +448,8 @@ bool far_gram_supported(int64_t S, int64_t n, int b);
 cudaError_t launch_gram_band(const uint16_t* Y, float* G, int64_t S, int64_t n, int64_t ldY,
                              int b, int s, uint32_t flags, Ctrl* ctrl, uint32_t timeout_us,
                              const RowSource* rs, uint64_t ctr, Ctx& c);
-// w_acc (with fpart): FP32[n] scratch; the launch then forms the margins itself (r reset
-// to pending by launch_gather_reset) from Y and w, and w receives the update only with the
-// last block.  g_band (with fpart): Gg and G use the band layout (g_block_offset with
+// own_margins (with fpart): the launch forms the margins itself (r reset to pending by
+// launch_gather_reset) from Y and w; w receives the update once the last phase is done.  g_band (with fpart): Gg and G use the band layout (g_block_offset with
 // gB = band_width(b)), else the packed block-lower layout.  rs (non-null, with fpart):
 // every row is read from X instead of Yg / Y -- the Gram's own rows those of the
 // iteration starting at sampler counter ctr_g, this iteration's (far tiles, margins,
@@ -460,7 +458,7 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
                               int64_t ldY, int b, int s, float eta, int loss, uint32_t flags,
                               const float* G, const uint16_t* Y, float* r,
                               const float* yY, float* alpha, float* far, uint32_t* slab,
-                              float* fpart, float* part, float* w, float* w_acc, Ctrl* ctrl,
+                              float* fpart, float* part, float* w, bool own_margins, Ctrl* ctrl,
                               uint32_t timeout_us, bool g_band, const RowSource* rs,
                               uint64_t ctr_g, uint64_t ctr_f, Ctx& c);
 cudaError_t launch_update_reduce(const float* part, int upd_ctas, int64_t n, int64_t ldY,

@@ -73,6 +73,7 @@ struct TcArgs {
   bool stored_last;  // the stored units are the next iteration's band (see FarCursor)
   int n_stored;      // stored units in this launch
   int far_head;      // stored_last: far units before the stored ones
+  int store_tail;    // stored_last: stored units moved behind every far unit
   // Rows read straight from X (kernels with kGather): row p of the Gram's own rows is
   // row draw_row(seed, ctr_g + p) of X, row p of the far tiles' rows (this iteration's)
   // draw_row(seed, ctr_f + p) -- the sampler is a pure function of its counter, so the
@@ -251,8 +252,10 @@ struct TileCursor {
 // request) by phase.  Within a block t: column groups outer, row groups of block j inner.
 // Same iteration: every stored unit first (they wait on nothing and the recurrence
 // starts on them).  Band of the next iteration (stored_last): the first far_head far
-// units (one round over the pairs), then the stored units, which fill the MMAs while
-// the first far tiles wait for alpha, then the other far units.
+// units (one round over the pairs), then the stored units but the last store_tail, which
+// fill the MMAs while the first far tiles wait for alpha, then the other far units, then
+// those store_tail stored units (nothing in this launch waits for them, so they overlap
+// the recurrence's last phases).
 struct UnitWalk {  // forward walk over the far units (far) or the stored units
   int j = 0, base = 0, cnt = -1;
   __device__ int count(const TcArgs& a, bool far) const {
@@ -287,11 +290,14 @@ struct FarCursor {
       if (lf < 0) ls = u;
     } else if (u < a.far_head) {
       lf = u;
-    } else if (u < a.far_head + a.n_stored) {
+    } else if (u < a.far_head + a.n_stored - a.store_tail) {
       lf = -1;
       ls = u - a.far_head;
+    } else if (u < a.ntiles - a.store_tail) {
+      lf = u - (a.n_stored - a.store_tail);
     } else {
-      lf = u - a.n_stored;
+      lf = -1;
+      ls = u - (a.ntiles - a.n_stored);
     }
     far = lf >= 0;
     if (far)
@@ -614,6 +620,8 @@ constexpr int kFusedThreads = kThreads + kRecThreads;  // 6 Gram warps + 8 recur
 // Gram items per round of a pair that also runs the chain, and of the other pairs
 constexpr int kChainPairShare = 1;
 constexpr int kOtherPairShare = 1;
+// Share (percent) of the next iteration's band tiles computed after every far tile
+constexpr int kStoreTailPct = 50;
 constexpr uint32_t kIdesc2 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                              ((uint32_t)(256 >> 4) << 24);
 
@@ -1190,7 +1198,7 @@ cudaError_t plan_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
   a.npb = a.uq = 1;
   a.fs = s;
   a.stored_last = false;
-  a.n_stored = a.far_head = 0;
+  a.n_stored = a.far_head = a.store_tail = 0;
   a.gB = gB;
   a.seed = a.ctr_g = a.ctr_f = 0;
   a.m = 0;
@@ -1398,7 +1406,7 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
                               int64_t ldY, int b, int s, float eta, int loss, uint32_t flags,
                               const float* G, const uint16_t* Y, float* r,
                               const float* yY, float* alpha, float* far, uint32_t* slab,
-                              float* fpart, float* part, float* w, float* w_acc, Ctrl* ctrl,
+                              float* fpart, float* part, float* w, bool own_margins, Ctrl* ctrl,
                               uint32_t timeout_us, bool g_band, const RowSource* rs,
                               uint64_t ctr_g, uint64_t ctr_f, Ctx& c) {
   if (!gram_recur_fused_supported(S, n, b)) return cudaErrorNotSupported;
@@ -1447,6 +1455,7 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
     P.a.n_stored = (int)((!next || g_rows) ? nst : 0);
     P.a.ntiles = (int)(nfar + P.a.n_stored);
     P.a.far_head = 0;
+    P.a.store_tail = 0;
     rec.fpart = fpart;
     rec.fs = P.a.fs;
     rec.npb = P.a.npb;
@@ -1454,7 +1463,7 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
     rec.bulk_units = 0;  // no far units: the Gram forms the far sums
     rec.upd_R = upd_row_parts(b, ldY);  // the bulk groups only update: row parts
     rec.upd_units = s * (int)((ldY / 8 + 7) / 8) * rec.upd_R;
-    if (w_acc) {  // the bulk groups form the margins first (mG lanes per row, 2 passes)
+    if (own_margins) {  // the bulk groups form the margins first (mG lanes per row, 2 passes)
       int G = 1;
       while (G < ldY / 8 && G < 32) G <<= 1;
       rec.margins = true;
@@ -1464,7 +1473,6 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
       rec.r_w = r;
       rec.wm = w;
       rec.wm_vec = (reinterpret_cast<uintptr_t>(w) & 15u) == 0;
-      rec.w_acc = w_acc;
     }
   }
   // what Ctrl::band_done reaches once every stored tile is stored (8 warps per tile)
@@ -1534,6 +1542,7 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
   if (far_gram && next) {
     const int nfar = P.a.ntiles - P.a.n_stored;
     P.a.far_head = nfar < grid / 2 ? nfar : grid / 2;
+    P.a.store_tail = (int)((int64_t)P.a.n_stored * kStoreTailPct / 100);
   }
   cfg.gridDim = dim3((unsigned)grid);
   // Scheduled early behind the gather, a CTA waits in wait_prior_grid() (a hardware

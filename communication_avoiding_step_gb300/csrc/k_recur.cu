@@ -73,7 +73,6 @@ RecArgs make_rec_args(const float* G, const float* r, const float* yY, float* al
   a.mrows = a.mG = 0;
   a.r_w = nullptr;
   a.wm = nullptr;
-  a.w_acc = nullptr;
   a.far_gram = false;
   a.C = 0;
   a.upd_groups = 0;

@@ -94,13 +94,12 @@ struct RecArgs {
   uint32_t band_total;
   // Margins formed in this launch (with the far-forming Gram): the bulk groups' first
   // units (bulk_units of them, mrows rows each, mG lanes per row) write r (pending until
-  // then) from Y and w; the update then adds its block sums into w_acc and only the last
-  // block's into w, which the margins read.
+  // then) from Y and w.  The update writes w only once a column chunk's s block sums are
+  // all formed, which needs alpha_{s-1}, so after the chain has read every margin.
   bool margins, r_fp32, wm_vec;  // wm_vec: w 16-byte aligned
   int mrows, mG;
   float* r_w;
   const float* wm;  // w as the launch starts (w_k), read by the margin units
-  float* w_acc;
   bool far_gram;  // the Gram stores only the band (and diagonal) tiles
   int64_t S;
   Ctrl* ctrl;
@@ -537,27 +536,28 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
 
 // --------------------------------------------------------------- update units
 // Step a8, fused: unit (j, cc, rq) sums alpha_i * Y_i over row part rq (of R) of block j
-// for the 64 columns cc*64 .. cc*64+63 into partial row j*R + rq.  Two ways to finish:
-//  * modes 0-2 (R = 1; the bulk groups also stream G, so no unit may wait on another):
-//    the last of the s units of a column chunk adds the chunk's s partial rows to w,
-//    rows q, q+8, q+16, ... for each q < 8, then the eight sums in q order;
-//  * modes 3-4 (far sums from the Gram; the bulk groups only update): the last of the R
-//    units of (j, cc) sums the R partial rows (four interleaved sums) and adds the
-//    block's sum to w once block j-1's has been added (a per-chunk turn counter), so w
-//    receives the block sums in block order and only the last block's small addition
-//    follows the chain.
+// for the 64 columns cc*64 .. cc*64+63 into partial row j*R + rq.  With R > 1 the last of
+// the R units of (j, cc) sums the R partial rows (four interleaved sums) into row j*R,
+// the block's sum (R = 1: the unit's own row is).  The last of the s block sums of a
+// column chunk (a per-chunk counter) adds them to w: block rows q, q+8, q+16, ... for
+// each q < 8, then the eight sums in q order.  No unit waits on another (modes 0-2: the
+// bulk groups also stream G), and w receives one addition per iteration whatever order
+// the units finish in.
 // Threads: 32 row-lanes x 8 column vectors.  The unit issues its first rows of Y, then
 // waits as a whole for its rows of alpha_j: lane 0 of warp 0 polls one value with a
-// back-off (of phase j+1, or the part's last row for the last block), then warp 0 loads
+// back-off (of phase j+1; the part's last row for the last block and, in modes 3-4, the
+// last two), then warp 0 loads
 // the part's values until none is pending.  Fixed
 // order: rows ascending per row-lane, then row-lanes ascending in shared memory.  Y was
-// written by an earlier launch.
+// written by an earlier launch.  Returns, in thread 0 of the group, whether every update
+// unit had been dealt once alpha_j was final (the queue's counter, read then; it only
+// grows), so the group need not ask the queue again; false in the other threads.
 template <int kMode, bool kFromX>
-__device__ void update_unit(const RecArgs& a, int u, int rt) {
+__device__ bool update_unit(const RecArgs& a, int u, int rt) {
   __shared__ float red[32][64];
   // one flag per stage, each written by thread 0 and read by the group after a barrier;
   // the next write of a flag comes after at least two more barriers of the group
-  __shared__ int s_ready, s_last, s_turn;
+  __shared__ int s_ready, s_last;
   const int nchunk = (int)((a.ldY / 8 + 7) / 8);
   const int per_j = nchunk * a.upd_R;
   const int j = u / per_j, cc = (u - j * per_j) / a.upd_R;
@@ -572,6 +572,8 @@ __device__ void update_unit(const RecArgs& a, int u, int rt) {
   // (reading X: vectors from column n on are skipped, and the columns past n of the last
   // vector only reach partial-row columns that are never added to w)
   const bool xin = kFromX ? vec * 8 < a.n : vin;
+  uint32_t dealt = 0;
+  auto drained = [&]() { return rt == 0 && dealt >= (uint32_t)a.upd_units; };
   auto load_rows = [&](int i0) {
 #pragma unroll
     for (int k = 0; k < kUpdRows; ++k) {
@@ -590,9 +592,11 @@ __device__ void update_unit(const RecArgs& a, int u, int rt) {
     const uint64_t t_start = globaltimer_ns();
     if (rt == 0) {
       // one value polled with a back-off: of phase j+1 (final there implies alpha_j
-      // complete; the update of block j is off the critical path), or for the last
-      // block its own last row
-      const float* pv = j + 1 < a.s
+      // complete; the update of block j is off the critical path), or its own last row
+      // for the last block and, in modes 3-4 (which poll the part's own values next),
+      // for the last two: block s-2's sum is then formed before the last block's alpha
+      const int probe_ahead = kMode >= 3 ? j + 2 < a.s : j + 1 < a.s;
+      const float* pv = probe_ahead
                             ? a.alpha + (int64_t)(j + 1) * a.b + (int)((blockIdx.x * 37u) % (unsigned)a.b)
                             : al_j + r1 - 1;
       while (pending1(ld_volatile_f32(pv)) && ok) {
@@ -624,7 +628,10 @@ __device__ void update_unit(const RecArgs& a, int u, int rt) {
       }
     }
     ok = __all_sync(0xffffffffu, ok);
-    if (rt == 0) s_ready = ok ? 1 : 0;
+    if (rt == 0) {
+      s_ready = ok ? 1 : 0;
+      dealt = ld_volatile_u32(&a.ctrl->upd_next);  // used when the unit is done
+    }
   }
   group_sync<kMode != 0>();
   const bool ready = s_ready != 0;  // rewritten only after the group syncs below
@@ -648,79 +655,72 @@ __device__ void update_unit(const RecArgs& a, int u, int rt) {
   for (int e = 0; e < 8; ++e) red[tr][tv * 8 + e] = acc[e];
   group_sync<kMode != 0>();
   const int64_t c = (int64_t)cc * 64 + (rt & 63);
+  const int R = a.upd_R;                          // 1 in modes 0-2
+  float* brow = a.part + (int64_t)j * R * a.ldY;  // block j's partial rows
   if (rt < 64 && ready) {
     float sum = 0.0f;
     for (int r = 0; r < 32; ++r) sum += red[r][rt];
-    if (c < a.ldY) a.part[((int64_t)j * a.upd_R + rq) * a.ldY + c] = sum;
     if (rt == 0) stamp_last(a.trace, 2);
+    if (c < a.ldY) brow[(int64_t)rq * a.ldY + c] = sum;
     __threadfence();  // the partial row is visible before this unit is counted
   }
-  if (kMode <= 2) {
-    // the last of the s units of column chunk cc adds the chunk's s partial rows to w
+  if (R > 1) {
+    // the last of the R units of (j, cc): the block's sum (parts rq, rq+4, ... in four
+    // sums, then combined) into the block's first partial row
     group_sync<kMode != 0>();
     if (rt == 0)
-      s_last = ready && atomicAdd(a.upd_chunks + cc, 1u) == (unsigned)(a.s - 1) ? 1 : 0;
+      s_last = ready && atomicAdd(a.upd_blocks + (int64_t)j * nchunk + cc, 1u) ==
+                            (unsigned)(R - 1)
+                   ? 1
+                   : 0;
     group_sync<kMode != 0>();
-    if (s_last && rt < 64 && c < a.n) {
+    if (!s_last) return drained();  // group-uniform
+    if (rt < 64 && c < a.ldY) {
       __threadfence();
-      float sum = 0.0f;
-      for (int q8 = 0; q8 < 8; ++q8) {
-        float acc_q = 0.0f;
-        for (int pr = q8; pr < a.s; pr += 8) acc_q += __ldcg(a.part + (int64_t)pr * a.ldY + c);
-        sum += acc_q;
+      float p4[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int r0 = 0; r0 < R; r0 += 16) {  // 16 loads in flight, added in r order
+        float v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          v[k] = r0 + k < R ? __ldcg(brow + (int64_t)(r0 + k) * a.ldY + c) : 0.0f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) p4[k & 3] += v[k];
       }
-      const float v = a.w[c] + sum;
-      a.w[c] = v;
-      if (!isfinite(v)) atomicOr(&a.ctrl->status, ST_NONFINITE);
+      brow[c] = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+      __threadfence();
     }
-    return;
   }
-  // the last row part of (j, cc): the block's sum, then its turn to add to w
+  // the last of the s block sums of column chunk cc adds them to w: block rows q, q+8,
+  // q+16, ... for each q < 8, then the eight sums in q order
   group_sync<kMode != 0>();
   if (rt == 0)
-    s_last = ready && atomicAdd(a.upd_blocks + (int64_t)j * nchunk + cc, 1u) ==
-                          (unsigned)(a.upd_R - 1)
-                 ? 1
-                 : 0;
+    s_last = ready && atomicAdd(a.upd_chunks + cc, 1u) == (unsigned)(a.s - 1) ? 1 : 0;
   group_sync<kMode != 0>();
-  if (!s_last) return;  // group-uniform
-  float bsum = 0.0f;
-  if (rt < 64 && c < a.n) {
+  if (s_last && rt < 64 && c < a.n) {
     __threadfence();
-    float p4[4] = {0.f, 0.f, 0.f, 0.f};  // parts rq, rq+4, ... in four sums, then combined
-    for (int r = 0; r < a.upd_R; ++r)
-      p4[r & 3] += __ldcg(a.part + ((int64_t)j * a.upd_R + r) * a.ldY + c);
-    bsum = (p4[0] + p4[1]) + (p4[2] + p4[3]);
-  }
-  if (rt == 0) {  // wait for block j-1's addition to this chunk
-    bool ok = true;
-    const uint64_t t_start = globaltimer_ns();
-    while (ld_acquire_u32(a.upd_chunks + cc) != (uint32_t)j && ok) {
-      __nanosleep(64);
-      ok = keep_waiting(a, t_start, where_code(4, j));
+    float acc_q[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int p0 = 0; p0 < a.s; p0 += 16) {  // 16 loads in flight, added in row order
+      float v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        v[k] = p0 + k < a.s ? __ldcg(a.part + (int64_t)(p0 + k) * R * a.ldY + c) : 0.0f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) acc_q[k & 7] += v[k];
     }
-    s_turn = ok ? 1 : 0;
+    float sum = 0.0f;
+#pragma unroll
+    for (int q8 = 0; q8 < 8; ++q8) sum += acc_q[q8];
+    const float v = a.w[c] + sum;
+    a.w[c] = v;
+    if (!isfinite(v)) atomicOr(&a.ctrl->status, ST_NONFINITE);
   }
-  group_sync<kMode != 0>();
-  if (!s_turn) return;  // group-uniform
-  if (rt < 64 && c < a.n) {
-    // with the margins in this launch, w keeps w_k until the last block: the running
-    // sum lives in w_acc (block 0 starts from w)
-    const float* src = (a.w_acc && j > 0) ? a.w_acc : a.w;
-    float* dst = (a.w_acc && j + 1 < a.s) ? a.w_acc : a.w;
-    const float v = __ldcg(src + c) + bsum;
-    dst[c] = v;
-    if (j == a.s - 1 && !isfinite(v)) atomicOr(&a.ctrl->status, ST_NONFINITE);
-    __threadfence();
-  }
-  group_sync<kMode != 0>();
-  if (rt == 0) red_release_add_u32(a.upd_chunks + cc, 1u);  // block j+1's turn
+  return drained();
 }
 
 // -------------------------------------------------------------- margin units
 // Step a4 in the recurrence's launch (with the far-forming Gram): unit u forms the
-// margins of rows u*mrows .. of Y with w (the launch's w_k: the update writes w only with
-// the last block).  mG lanes per row (a power of two covering the row's 16-byte vectors
+// margins of rows u*mrows .. of Y with w (the launch's w_k: the update writes w only
+// after the last phase).  mG lanes per row (a power of two covering the row's 16-byte vectors
 // up to 32), 32/mG rows per warp and pass; lane g sums the vectors g, g+mG, ... in FP32,
 // eight elements each in column order, the row's lanes then add by a shuffle tree, and
 // its first lane stores the margin (rounded once to BF16, or FP32 with MARGINS_FP32).
@@ -822,7 +822,9 @@ __device__ void bulk_role(const RecArgs& a, int rt, bool upd_group) {
           far_left = false;
         }
       }
-      if (ld_volatile_u32(&a.ctrl->abort)) u = a.bulk_units + a.upd_units;
+      // (nothing dealt: the group leaves without reading the abort word)
+      if (u < a.bulk_units + a.upd_units && ld_volatile_u32(&a.ctrl->abort))
+        u = a.bulk_units + a.upd_units;
       s_unit = u;
     }
     group_sync<kMode != 0>();
@@ -830,7 +832,7 @@ __device__ void bulk_role(const RecArgs& a, int rt, bool upd_group) {
     group_sync<kMode != 0>();
     if (unit >= a.bulk_units) {
       if (unit < a.bulk_units + a.upd_units) {
-        update_unit<kMode, kFromX>(a, unit - a.bulk_units, rt);
+        if (update_unit<kMode, kFromX>(a, unit - a.bulk_units, rt)) upd_left = false;
         group_sync<kMode != 0>();
         continue;
       }
