@@ -205,6 +205,34 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// tcgen05.ld of 32 columns without the wait; the registers are valid only after
+// tmem_wait_ld on the same array (which takes them as operands, so no use of them can
+// be scheduled before the wait).
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+        "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+        "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+        "=r"(v[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
+                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
+                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]),
+                 "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                 "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]),
+                 "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+               :
+               : "memory");
+}
+
 // Number of needed column tiles in row tile `ra` (columns [0, count*BN) hold every
 // entry of a needed block in those rows).
 __device__ __forceinline__ int cols_needed(const TcArgs& a, int ra) {
@@ -354,11 +382,8 @@ __device__ __forceinline__ void bulk_wait_all() {  // every issued store has com
 
 // Epilogue of one tile for one warp: TMEM lanes 32*quarter.. hold rows ra*BM + 32*quarter
 // + lane of the tile; the 256 accumulator columns of buffer `acc` are read 32 at a time
-// and the entries that belong to needed blocks are stored into the packed G.
-// With a.tma_store (b a multiple of 32) every 32x32 chunk lies inside one block of G:
-// the warp writes it into one of its two 128-byte-swizzled staging buffers and lane 0
-// stores it with a TMA tensor store (whole 128-byte lines), through a 2D tensor map that
-// views the packed G as (blocks*b) rows of b columns.
+// and the entries that belong to needed blocks are stored into G (either layout) by
+// each lane, one row each.  Without a.tma_store only; store_tile_tma otherwise.
 __device__ __forceinline__ void store_tile_rows(const TcArgs& a, uint32_t tmem, int acc,
                                                 int quarter, int lane, int ra, int ca,
                                                 const CUtensorMap* tmG, uint8_t* stage,
@@ -378,27 +403,6 @@ __device__ __forceinline__ void store_tile_rows(const TcArgs& a, uint32_t tmem, 
       for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(round_bf16(__uint_as_float(v[e])));
     }
     const int64_t q0 = (int64_t)ca * BN + ch * 32;
-    if (a.tma_store) {  // warp-uniform
-      if (p0 >= a.S || q0 >= a.S) continue;
-      const int64_t j0 = p0 / a.b, t0b = q0 / a.b;
-      if (!(t0b < j0 || (a.diag && t0b == j0))) continue;
-      uint8_t* buf = stage + sbuf * (32 * 32 * 4);
-      if (lane == 0) bulk_wait_read1();  // the store issued two chunks ago has read buf
-      __syncwarp();
-#pragma unroll
-      for (int c = 0; c < 8; ++c)  // row `lane`, 16-byte chunk c at swizzled slot c ^ (row % 8)
-        *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) * 16)) =
-            make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        const int64_t grow = (g_block_offset(j0, t0b, a.b, a.diag, a.gB) / a.b) + (p0 - j0 * a.b);
-        tma_store_2d(tmG, smem_u32(buf), (int32_t)(q0 - t0b * a.b), (int32_t)grow);
-        bulk_commit();
-      }
-      sbuf ^= 1;
-      continue;
-    }
     if (!prow || q0 >= a.S) continue;
     const int64_t t0b = q0 / a.b;
     const int64_t q1 = q0 + 31;
@@ -422,6 +426,68 @@ __device__ __forceinline__ void store_tile_rows(const TcArgs& a, uint32_t tmem, 
               __uint_as_float(v[e]);
       }
     }
+  }
+}
+
+// One 32x32 chunk of store_tile_tma: columns q0.. of the warp's rows p0.. (block row j0),
+// stored if the chunk lies in a needed block.  The warp writes it into one of its two
+// 128-byte-swizzled staging buffers and lane 0 stores it with a TMA tensor store (whole
+// 128-byte lines) through a 2D tensor map that views G as (blocks*b) rows of b columns.
+__device__ __forceinline__ void store_chunk_tma(const TcArgs& a, const uint32_t (&v)[32],
+                                                int lane, int64_t p0, int64_t j0, int64_t q0,
+                                                const CUtensorMap* tmG, uint8_t* stage,
+                                                int& sbuf) {
+  if (q0 >= a.S) return;  // warp-uniform, as below
+  const int64_t t0b = q0 / a.b;
+  if (!(t0b < j0 || (a.diag && t0b == j0))) return;
+  uint8_t* buf = stage + sbuf * (32 * 32 * 4);
+  if (lane == 0) bulk_wait_read1();  // the store issued two chunks ago has read buf
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {  // row `lane`, 16-byte chunk c at swizzled slot c ^ (row % 8)
+    uint32_t x[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      x[e] = a.g_bf16 ? __float_as_uint(round_bf16(__uint_as_float(v[4 * c + e]))) : v[4 * c + e];
+    *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) * 16)) =
+        make_uint4(x[0], x[1], x[2], x[3]);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    const int64_t grow = (g_block_offset(j0, t0b, a.b, a.diag, a.gB) / a.b) + (p0 - j0 * a.b);
+    tma_store_2d(tmG, smem_u32(buf), (int32_t)(q0 - t0b * a.b), (int32_t)grow);
+    bulk_commit();
+  }
+  sbuf ^= 1;
+}
+
+// The epilogue of store_tile_rows with a.tma_store (b a multiple of 32, so every 32x32
+// chunk lies inside one block of G): the TMEM load of the next 32 columns is in flight
+// while a chunk is staged and stored.
+__device__ __forceinline__ void store_tile_tma(const TcArgs& a, uint32_t tmem, int acc,
+                                               int quarter, int lane, int ra, int ca,
+                                               const CUtensorMap* tmG, uint8_t* stage,
+                                               int& sbuf) {
+  const int64_t p0 = (int64_t)ra * BM + quarter * 32;  // the warp's first row
+  if (p0 >= a.S) return;                                // warp-uniform
+  const int64_t j0 = p0 / a.b;
+  const int64_t q00 = (int64_t)ca * BN;
+  const uint32_t base = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+  uint32_t va[32], vb[32];
+  __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
+  tmem_ld32_issue(base, va);
+  tmem_wait_ld(va);
+#pragma unroll 1
+  for (int ch = 0; ch < BN / 32; ch += 2) {
+    tmem_ld32_issue(base + (uint32_t)(ch + 1) * 32, vb);
+    store_chunk_tma(a, va, lane, p0, j0, q00 + ch * 32, tmG, stage, sbuf);
+    tmem_wait_ld(vb);
+    __syncwarp();
+    if (ch + 2 < BN / 32) tmem_ld32_issue(base + (uint32_t)(ch + 2) * 32, va);
+    store_chunk_tma(a, vb, lane, p0, j0, q00 + (ch + 1) * 32, tmG, stage, sbuf);
+    if (ch + 2 < BN / 32) tmem_wait_ld(va);
+    __syncwarp();
   }
 }
 
@@ -564,7 +630,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tphase[acc] ^= 1u;
       tc_fence_after();
-      store_tile_rows(a, tmem, acc, quarter, lane, ra, ca, &tmG, stage, sbuf);
+      if (a.tma_store)
+        store_tile_tma(a, tmem, acc, quarter, lane, ra, ca, &tmG, stage, sbuf);
+      else
+        store_tile_rows(a, tmem, acc, quarter, lane, ra, ca, &tmG, stage, sbuf);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sc->tempty[acc]);
@@ -770,33 +839,6 @@ __device__ bool stage_alpha(const TcArgs& a, const float* src, float* dst, int l
   return true;
 }
 
-// tcgen05.ld of 32 columns without the wait; the registers are valid only after
-// tmem_wait_ld on the same array (which takes them as operands, so no use of them can
-// be scheduled before the wait).
-__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-        "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
-        "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
-        "=r"(v[31])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
-                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
-                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]),
-                 "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
-                 "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]),
-                 "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
-               :
-               : "memory");
-}
 
 // An accumulator entry as the recurrence uses it: FP32, or rounded to BF16 (G_BF16).
 __device__ __forceinline__ float far_entry(uint32_t bits, bool g_bf16) {
@@ -1063,7 +1105,10 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
         if (kFar && far) {
           if (!dead) far_tile_dot(tmem, acc, quarter, al_s, a.g_bf16, sum);
         } else {
-          store_tile_rows(a, tmem, acc, quarter, lane, ra, ca, &tmG, stage, sbuf);
+          if (a.tma_store)
+            store_tile_tma(a, tmem, acc, quarter, lane, ra, ca, &tmG, stage, sbuf);
+          else
+            store_tile_rows(a, tmem, acc, quarter, lane, ra, ca, &tmG, stage, sbuf);
         }
         tc_fence_before();
         __syncwarp();

@@ -572,6 +572,15 @@ __device__ bool update_unit(const RecArgs& a, int u, int rt) {
   // (reading X: vectors from column n on are skipped, and the columns past n of the last
   // vector only reach partial-row columns that are never added to w)
   const bool xin = kFromX ? vec * 8 < a.n : vin;
+  // warp 0 polls the part's alpha values (all of them in modes 3-4 and for the last
+  // block) and then keeps them in red, which holds up to 2048
+  const bool polled = kMode >= 3 || j + 1 == a.s;
+  const bool al_sm = polled && r1 - r0 <= 32 * 64;
+  float* red_f = &red[0][0];
+  // w as the launch started (w_k): this column's value for the chunk's final sum, read
+  // now (w changes only with that sum)
+  const int64_t c = (int64_t)cc * 64 + (rt & 63);
+  const float w_k = (rt < 64 && c < a.n) ? a.w[c] : 0.0f;
   uint32_t dealt = 0;
   auto drained = [&]() { return rt == 0 && dealt >= (uint32_t)a.upd_units; };
   auto load_rows = [&](int i0) {
@@ -606,8 +615,9 @@ __device__ bool update_unit(const RecArgs& a, int u, int rt) {
     }
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     // the part's own values, four per lane in flight (modes 0-2 rely on the probe of
-    // phase j+1 for every block but the last, as the far units do)
-    if (kMode >= 3 || j + 1 == a.s) {
+    // phase j+1 for every block but the last, as the far units do), kept in shared
+    // memory for the sums (al_sm)
+    if (polled) {
       for (int i = r0 + rt; i < r1 && ok; i += 32 * 4) {
         float v[4];
 #pragma unroll
@@ -625,6 +635,11 @@ __device__ bool update_unit(const RecArgs& a, int u, int rt) {
             }
           if (pend) ok = keep_waiting(a, t_start, where_code(4, j));
         }
+        if (al_sm) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (i + 32 * k < r1) red_f[i + 32 * k - r0] = v[k];
+        }
       }
     }
     ok = __all_sync(0xffffffffu, ok);
@@ -641,7 +656,7 @@ __device__ bool update_unit(const RecArgs& a, int u, int rt) {
 #pragma unroll
       for (int k = 0; k < kUpdRows; ++k) {
         const int i = i0 + 32 * k;
-        const float al = i < r1 ? __ldcg(al_j + i) : 0.0f;
+        const float al = i < r1 ? (al_sm ? red_f[i - r0] : __ldcg(al_j + i)) : 0.0f;
         const uint32_t pw[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -651,10 +666,10 @@ __device__ bool update_unit(const RecArgs& a, int u, int rt) {
       }
     }
   }
+  group_sync<kMode != 0>();  // (red held alpha until here)
 #pragma unroll
   for (int e = 0; e < 8; ++e) red[tr][tv * 8 + e] = acc[e];
   group_sync<kMode != 0>();
-  const int64_t c = (int64_t)cc * 64 + (rt & 63);
   const int R = a.upd_R;                          // 1 in modes 0-2
   float* brow = a.part + (int64_t)j * R * a.ldY;  // block j's partial rows
   if (rt < 64 && ready) {
@@ -710,7 +725,7 @@ __device__ bool update_unit(const RecArgs& a, int u, int rt) {
     float sum = 0.0f;
 #pragma unroll
     for (int q8 = 0; q8 < 8; ++q8) sum += acc_q[q8];
-    const float v = a.w[c] + sum;
+    const float v = w_k + sum;
     a.w[c] = v;
     if (!isfinite(v)) atomicOr(&a.ctrl->status, ST_NONFINITE);
   }
