@@ -35,6 +35,10 @@ struct Resolved {
   float* G2;
   int32_t* idx2;
   float* yY2;
+  // third row buffers: the far-forming launch of iteration k gathers iteration k+2's rows
+  uint16_t* Y3;
+  int32_t* idx3;
+  float* yY3;
   float* fpart;  // far partial sums of the far-forming Gram (null: not laid out)
   float* upd;
   double* loss_part;
@@ -93,6 +97,9 @@ Resolved resolve(void* ws, const Layout& L) {
   R.G2 = L.off_G2 ? reinterpret_cast<float*>(base + L.off_G2) : nullptr;
   R.idx2 = L.off_idx2 ? reinterpret_cast<int32_t*>(base + L.off_idx2) : nullptr;
   R.yY2 = L.off_yY2 ? reinterpret_cast<float*>(base + L.off_yY2) : nullptr;
+  R.Y3 = L.off_Y3 ? reinterpret_cast<uint16_t*>(base + L.off_Y3) : nullptr;
+  R.idx3 = L.off_idx3 ? reinterpret_cast<int32_t*>(base + L.off_idx3) : nullptr;
+  R.yY3 = L.off_yY3 ? reinterpret_cast<float*>(base + L.off_yY3) : nullptr;
   R.fpart = L.off_fpart ? reinterpret_cast<float*>(base + L.off_fpart) : nullptr;
   R.upd = reinterpret_cast<float*>(base + L.off_upd);
   R.loss_part = reinterpret_cast<double*>(base + L.off_loss);
@@ -232,7 +239,7 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
     CK(launch_gram_recur(R.Y, G, false, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss, p->flags,
                          G, R.Y, R.r, R.yY, R.alpha, R.far, R.slab, gp.far ? R.fpart : nullptr,
                          R.upd, w, gp.far, R.ctrl, p->timeout_us,
-                         /*g_band=*/G == R.G, gather ? &rs : nullptr, ctr, ctr, c));
+                         /*g_band=*/G == R.G, gather ? &rs : nullptr, ctr, ctr, nullptr, c));
     if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
   } else {
     if (choice == 1)
@@ -300,52 +307,75 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   // and end (programmatic dependent launch); each waits for its predecessor's completion
   // before it touches memory, so the results are those of plain stream order
   c.pdl = true;
+  // With third row buffers (far-forming, not gathering, rows ahead_rows_supported) the
+  // launch of iteration k also gathers iteration k+2's rows (its producers, once their
+  // Gram work is done), so from the second iteration on the launch before it only
+  // gathers the iteration's indices and labels and resets the recurrence's state; the
+  // row buffers then rotate over three sets (the G buffers over two).
+  const bool ahead = far && !gather && R.Y3 != nullptr;
+  uint16_t* Yr[3] = {R.Y, R.Y2, R.Y3};
+  int32_t* Ir[3] = {R.idx, R.idx2, R.idx3};
+  float* yr[3] = {R.yY, R.yY2, R.yY3};
   for (int32_t it = 0; it < iters; ++it) {
     const int cur = it & 1, nxt = cur ^ 1;
     const uint64_t k = k0 + (uint64_t)it;
+    // rows, labels and indices of this iteration (c) and the next (n)
+    uint16_t* Yc = ahead ? Yr[it % 3] : Yb[cur];
+    uint16_t* Yn = ahead ? Yr[(it + 1) % 3] : Yb[nxt];
+    int32_t* Ic = ahead ? Ir[it % 3] : Ib[cur];
+    int32_t* In = ahead ? Ir[(it + 1) % 3] : Ib[nxt];
+    float* yc = ahead ? yr[it % 3] : yb[cur];
+    float* yn = ahead ? yr[(it + 1) % 3] : yb[nxt];
     if ((rc = record(prof, it, 0, st)) != CASGD_OK) return rc;
     if (it == 0) {  // prologue: this iteration's rows and its Gram (far: its band)
-      CK(launch_gather(*d, *p, w, k, nullptr, Ib[cur], gather ? nullptr : Yb[cur], L.ldY, R.r,
-                       yb[cur], R.alpha, R.far, nullptr, R.ctrl, R.slab, GATHER_ONLY, c));
+      CK(launch_gather(*d, *p, w, k, nullptr, Ic, gather ? nullptr : Yc, L.ldY, R.r, yc,
+                       R.alpha, R.far, nullptr, R.ctrl, R.slab, GATHER_ONLY, c));
       if (far)
-        CK(launch_gram_band(gather ? nullptr : Yb[cur], Gb[cur], L.S, d->n, L.ldY, p->b, p->s,
+        CK(launch_gram_band(gather ? nullptr : Yc, Gb[cur], L.S, d->n, L.ldY, p->b, p->s,
                             p->flags, R.ctrl, p->timeout_us, rsp, k * (uint64_t)L.S, c));
       else
-        CK(launch_gram_tc(Yb[cur], L.S, d->n, L.ldY, p->b, p->s, p->flags, 0, Gb[cur], R.ctrl,
+        CK(launch_gram_tc(Yc, L.S, d->n, L.ldY, p->b, p->s, p->flags, 0, Gb[cur], R.ctrl,
                           p->timeout_us, c));
     }
-    if (far)  // next iteration's rows (gathering: its indices and labels only) and this
-              // iteration's reset (margins in-launch)
-      CK(launch_gather_reset(*d, *p, k + 1, nullptr, Ib[nxt], gather ? nullptr : Yb[nxt],
-                             yb[nxt], it + 1 < iters, L.ldY, R.r, R.alpha, R.far, fpart, R.ctrl,
-                             R.slab, c));
+    if (far && (!ahead || it == 0))  // next iteration's rows (gathering: its indices and
+                                     // labels only) and this iteration's reset
+      CK(launch_gather_reset(*d, *p, k + 1, nullptr, In, gather ? nullptr : Yn, yn,
+                             it + 1 < iters, L.ldY, R.r, R.alpha, R.far, fpart, R.ctrl, R.slab,
+                             c));
+    else if (far)  // this iteration's rows came with the launch two back: its indices and
+                   // labels, and the reset
+      CK(launch_gather_reset(*d, *p, k, nullptr, Ic, nullptr, yc, true, L.ldY, R.r, R.alpha,
+                             R.far, fpart, R.ctrl, R.slab, c));
     else if (it + 1 < iters)  // next iteration's rows (into the buffers the last launch
                               // freed) and this iteration's margins, in one launch
-      CK(launch_gather_next_margins(*d, *p, w, k + 1, Ib[nxt], Yb[nxt], yb[nxt], Yb[cur],
-                                    L.ldY, R.r, R.alpha, R.far, fpart, R.ctrl, R.slab, c));
+      CK(launch_gather_next_margins(*d, *p, w, k + 1, In, Yn, yn, Yc, L.ldY, R.r, R.alpha,
+                                    R.far, fpart, R.ctrl, R.slab, c));
     else
-      CK(launch_gather(*d, *p, w, k, nullptr, Ib[cur], Yb[cur], L.ldY, R.r, yb[cur], R.alpha,
-                       R.far, fpart, R.ctrl, R.slab, MARGINS_ONLY, c));
+      CK(launch_gather(*d, *p, w, k, nullptr, Ic, Yc, L.ldY, R.r, yc, R.alpha, R.far, fpart,
+                       R.ctrl, R.slab, MARGINS_ONLY, c));
     if ((rc = record(prof, it, 1, st)) != CASGD_OK) return rc;
     // (The sum of G over processes would sit before this launch; on one GPU it is the
     // identity.)
-    if (far)  // this iteration's far sums; the next iteration's band (if any) into Gb[nxt]
-      CK(launch_gram_recur(gather ? nullptr : (it + 1 < iters ? Yb[nxt] : nullptr), Gb[nxt],
-                           true, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss, p->flags,
-                           Gb[cur], gather ? nullptr : Yb[cur], R.r, yb[cur], R.alpha, R.far,
-                           R.slab, fpart, R.upd, w, true, R.ctrl, p->timeout_us,
-                           /*g_band=*/true, rsp,
+    if (far) {  // this iteration's far sums; the next iteration's band (if any) into Gb[nxt]
+      AheadRows ah{};
+      if (ahead && it + 2 < iters)
+        ah = AheadRows{rs.X, rs.ld, rs.m, rs.seed, rs.perm_d, (k + 2) * (uint64_t)L.S,
+                       Yr[(it + 2) % 3]};
+      CK(launch_gram_recur(gather ? nullptr : (it + 1 < iters ? Yn : nullptr), Gb[nxt], true,
+                           L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss, p->flags, Gb[cur],
+                           gather ? nullptr : Yc, R.r, yc, R.alpha, R.far, R.slab, fpart, R.upd,
+                           w, true, R.ctrl, p->timeout_us, /*g_band=*/true, rsp,
                            it + 1 < iters ? (k + 1) * (uint64_t)L.S : kNoRows,
-                           k * (uint64_t)L.S, c));
-    else if (it + 1 < iters)
-      CK(launch_gram_recur(Yb[nxt], Gb[nxt], true, L.S, d->n, L.ldY, p->b, p->s, p->eta,
-                           p->loss, p->flags, Gb[cur], Yb[cur], R.r, yb[cur], R.alpha, R.far,
-                           R.slab, nullptr, R.upd, w, false, R.ctrl, p->timeout_us, false,
-                           nullptr, 0, 0, c));
-    else
-      CK(launch_recur(Gb[cur], R.r, yb[cur], R.alpha, R.far, R.slab, p->b, p->s, p->eta,
-                      p->loss, p->flags, p->timeout_us, R.ctrl, Yb[cur], L.ldY, d->n, R.upd, w,
-                      c));
+                           k * (uint64_t)L.S, ah.Y ? &ah : nullptr, c));
+    } else if (it + 1 < iters) {
+      CK(launch_gram_recur(Yn, Gb[nxt], true, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss,
+                           p->flags, Gb[cur], Yc, R.r, yc, R.alpha, R.far, R.slab, nullptr,
+                           R.upd, w, false, R.ctrl, p->timeout_us, false, nullptr, 0, 0,
+                           nullptr, c));
+    } else {
+      CK(launch_recur(Gb[cur], R.r, yc, R.alpha, R.far, R.slab, p->b, p->s, p->eta, p->loss,
+                      p->flags, p->timeout_us, R.ctrl, Yc, L.ldY, d->n, R.upd, w, c));
+    }
     // the update (a8) finished inside that launch
     if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
     if ((rc = record(prof, it, 3, st)) != CASGD_OK) return rc;
@@ -512,6 +542,7 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms,
   L.off_G = with_G ? off : 0;
   if (with_G) off += align_up((size_t)L.gram_elems * sizeof(float));
   L.off_Y2 = L.off_G2 = L.off_idx2 = L.off_yY2 = L.off_fpart = 0;
+  L.off_Y3 = L.off_idx3 = L.off_yY3 = 0;
   if (gp.fused) {  // casgd_train gathers the rows (and runs the Gram) one iteration ahead
     L.off_idx2 = off;
     off += align_up((size_t)L.S * sizeof(int32_t));
@@ -527,6 +558,14 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms,
   if (gp.far) {
     L.off_fpart = off;
     off += align_up((size_t)L.S * s * far_partials_per_block(b, s) * sizeof(float));
+  }
+  if (gp.fused && gp.far && !(flags & CASGD_FLAG_GATHER_ROWS) && ahead_rows_supported(n, L.ldY)) {
+    L.off_idx3 = off;
+    off += align_up((size_t)L.S * sizeof(int32_t));
+    L.off_yY3 = off;
+    off += align_up((size_t)L.S * sizeof(float));
+    L.off_Y3 = off;
+    off += align_up((size_t)L.S * L.ldY * sizeof(uint16_t));
   }
   L.total = off;
   return L;

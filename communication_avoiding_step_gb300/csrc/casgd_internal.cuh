@@ -64,7 +64,8 @@ struct Ctrl {
   uint32_t diag;          // which wait timed out last: kind << 24 | block << 12 | value seen
   uint32_t band_done;     // Gram in the recurrence's launch: tiles stored x 8 warps, as
                           // released by its epilogue warps (zeroed by the margins step)
-  uint32_t pad0;
+  uint32_t ahead_next;    // far-forming launch: chunks of the rows two iterations ahead
+                          // taken by its producers (zeroed by the gather kernel)
 };
 static_assert(sizeof(Ctrl) <= 512, "control block");
 
@@ -74,6 +75,7 @@ struct Layout {
   int upd_ctas;
   size_t off_idx, off_r, off_yY, off_alpha, off_far, off_Y, off_G, off_upd, off_loss;
   size_t off_Y2, off_G2, off_idx2, off_yY2;  // 0: no second buffers
+  size_t off_Y3, off_idx3, off_yY3;  // third row buffers (rows gathered two ahead; 0: none)
   size_t off_fpart;  // far partial sums FP32[S][s * npb] of the far-forming Gram (0: none)
   size_t total;
 };
@@ -448,19 +450,36 @@ bool far_gram_supported(int64_t S, int64_t n, int b);
 cudaError_t launch_gram_band(const uint16_t* Y, float* G, int64_t S, int64_t n, int64_t ldY,
                              int b, int s, uint32_t flags, Ctrl* ctrl, uint32_t timeout_us,
                              const RowSource* rs, uint64_t ctr, Ctx& c);
+// Rows that a far-forming launch gathers for a later iteration once its own Gram work is
+// done (launch_gram_recur's `ahead`): rows ctr .. ctr+S-1 of the sampler (draw_row with
+// seed, m, perm_d) of X (pitch ld) into Y (pitch ldY; columns n .. ldY-1 written as
+// zeros).  n % 8 == 0.  Their labels and indices are gathered separately.
+struct AheadRows {
+  const uint16_t* X;
+  int64_t ld;
+  uint32_t m;
+  uint64_t seed;
+  int perm_d;
+  uint64_t ctr;
+  uint16_t* Y;
+};
+// Whether launch_gram_recur can gather rows ahead for these shapes.
+bool ahead_rows_supported(int64_t n, int64_t ldY);
 // own_margins (with fpart): the launch forms the margins itself (r reset to pending by
-// launch_gather_reset) from Y and w; w receives the update once the last phase is done.  g_band (with fpart): Gg and G use the band layout (g_block_offset with
-// gB = band_width(b)), else the packed block-lower layout.  rs (non-null, with fpart):
-// every row is read from X instead of Yg / Y -- the Gram's own rows those of the
-// iteration starting at sampler counter ctr_g, this iteration's (far tiles, margins,
-// update) those starting at ctr_f.
+// launch_gather_reset) from Y and w; w receives the update once the last phase is done.
+// g_band (with fpart): Gg and G use the band layout (g_block_offset with gB =
+// band_width(b)), else the packed block-lower layout.  rs (non-null, with fpart): every
+// row is read from X instead of Yg / Y -- the Gram's own rows those of the iteration
+// starting at sampler counter ctr_g, this iteration's (far tiles, margins, update) those
+// starting at ctr_f.  ahead (non-null, with fpart and Yg, ahead_rows_supported): the
+// launch also gathers those rows (into buffers that none of its other work touches).
 cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t S, int64_t n,
                               int64_t ldY, int b, int s, float eta, int loss, uint32_t flags,
                               const float* G, const uint16_t* Y, float* r,
                               const float* yY, float* alpha, float* far, uint32_t* slab,
                               float* fpart, float* part, float* w, bool own_margins, Ctrl* ctrl,
                               uint32_t timeout_us, bool g_band, const RowSource* rs,
-                              uint64_t ctr_g, uint64_t ctr_f, Ctx& c);
+                              uint64_t ctr_g, uint64_t ctr_f, const AheadRows* ahead, Ctx& c);
 cudaError_t launch_update_reduce(const float* part, int upd_ctas, int64_t n, int64_t ldY,
                                  float* w, Ctrl* ctrl, Ctx& c);
 cudaError_t launch_update(const uint16_t* Y, const float* alpha, int64_t S, int64_t n,

@@ -81,6 +81,11 @@ struct TcArgs {
   uint64_t seed, ctr_g, ctr_f;
   uint32_t m;
   int perm_d;
+  // Rows gathered ahead once this CTA's Gram work is done (gather_ahead; far-forming
+  // launch with the next band only)
+  bool ahead_on;
+  int64_t ahead_ldY;
+  AheadRows ahead;
   // Weighted deal of the work items to the CTA pairs: the first pc pairs (those whose
   // CTAs also run the recurrence's chain) take wa items for every wb the other pairs
   // take (wa <= wb; wa == wb: plain round robin)
@@ -375,6 +380,9 @@ __device__ __forceinline__ void bulk_commit() {
 }
 __device__ __forceinline__ void bulk_wait_read1() {  // at most one group still reading smem
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read0() {  // no group still reading smem
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() {  // every issued store has completed
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -701,6 +709,7 @@ struct SharedCtl2 {
   uint64_t tfull[2];    // both CTAs: accumulator buffer complete
   uint64_t tempty[2];   // leader: both CTAs' epilogues done with a buffer (8 warps)
   uint64_t drain;       // leader: every MMA complete
+  uint64_t gfull[kSt];  // gather_ahead: a stage's row copies have landed
   uint32_t tmem_base;
   volatile uint32_t abort;
 };
@@ -781,6 +790,134 @@ __device__ bool mbar_wait2(uint64_t* bar, uint32_t parity, SharedCtl2<kSt>* sc, 
       return false;
     }
   }
+}
+
+// Waits for a phase ignoring the abort word, at most timeout_ns: copies already issued
+// into this CTA's shared memory land before it leaves.
+__device__ __forceinline__ bool mbar_wait_quiet(uint64_t* bar, uint32_t parity, uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > ns) return false;
+  return true;
+}
+
+// Rows gathered ahead (TcArgs::ahead) by the producer warp of each CTA once the MMAs
+// have read every stage of the CTA's ring, `stage`/`phase` being where the producer
+// stopped.  Chunks of rps rows (one stage each) are taken from Ctrl::ahead_next, so the
+// CTAs whose Gram work ends early take most of them.  For a chunk, lane r draws row r
+// from the sampler and copies its n*2 bytes from X into the stage (cp.async.bulk,
+// completion on the stage's gfull barrier); once landed the chunk goes out as
+// full-pitch bulk stores into Y (the stages' bytes from n*2 to the pitch are zeroed
+// once, so Y's padding stays zero).  The rows' labels and indices come with the launch
+// that resets the recurrence before the rows' own iteration.  Waits are bounded; after a
+// failed one the warp still lets the copies it issued land before it returns.
+template <int kSt>
+__device__ void gather_ahead(const TcArgs& a, SharedCtl2<kSt>* sc, uint8_t* smem, int lane,
+                             int stage, uint32_t phase) {
+  const AheadRows& h = a.ahead;
+  int ok = 1;
+  if (lane == 0) {  // every stage: the MMAs' reads of its last use are complete
+    for (int i = 0; i < kSt && ok; ++i) {
+      ok = mbar_wait2(&sc->empty[stage], phase ^ 1u, sc, a) ? 1 : 0;
+      if (++stage == kSt) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+  const uint32_t rowb = (uint32_t)a.n * 2;           // data bytes per row (n % 8 == 0)
+  const uint32_t pitch = (uint32_t)a.ahead_ldY * 2;  // bytes per row in Y and in a stage
+  const int rps = (int)(kStageBytes2 / pitch) < 32 ? (int)(kStageBytes2 / pitch) : 32;
+  const int64_t nch = (a.S + rps - 1) / rps;
+  for (int st = 0; st < kSt; ++st)
+    for (int r = 0; r < rps; ++r)
+      for (uint32_t o = rowb + (uint32_t)lane * 16; o < pitch; o += 32 * 16)
+        *reinterpret_cast<uint4*>(smem + (size_t)st * kStageBytes2 + (size_t)r * pitch + o) =
+            make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  __syncwarp();
+  // A ring over the stages: kSt-1 chunks' copies in flight while the oldest chunk is
+  // stored; a stage is refilled once the stores issued from it have read it (all but
+  // the newest store group).  Chunks enter the ring in stage order, so the first empty
+  // stage in that order ends it.
+  int64_t held[kSt];  // the chunk each stage holds (-1: none)
+  for (int st = 0; st < kSt; ++st) held[st] = -1;
+  // chunks are reserved kGrab at a time (one atomic per kGrab chunks)
+  constexpr int kGrab = 4;
+  int64_t res = 0;
+  int res_left = 0;
+  auto grab = [&]() -> int64_t {
+    if (res_left == 0) {
+      int64_t c = 0;
+      if (lane == 0) c = (int64_t)atomicAdd(&a.ctrl->ahead_next, (unsigned)kGrab);
+      res = __shfl_sync(0xffffffffu, c, 0);
+      res_left = kGrab;
+    }
+    --res_left;
+    return res++;
+  };
+  auto issue = [&](int st, int64_t c) {  // chunk c's copies
+    const int64_t p0 = c * rps;
+    const int nr = (int)(a.S - p0 < rps ? a.S - p0 : rps);
+    if (lane == 0) mbar_expect_tx(&sc->gfull[st], (uint32_t)nr * rowb);
+    __syncwarp();
+    if (lane < nr) {
+      const int32_t x = draw_row(h.seed, h.ctr + (uint64_t)(p0 + lane), h.m, h.perm_d);
+      bulk_load(smem + (size_t)st * kStageBytes2 + (size_t)lane * pitch, h.X + (int64_t)x * h.ld,
+                rowb, &sc->gfull[st]);
+    }
+    held[st] = c;
+  };
+  bool more = true;
+  for (int st = 0; st < kSt - 1 && more; ++st) {
+    const int64_t c = grab();
+    if (c >= nch)
+      more = false;
+    else
+      issue(st, c);
+  }
+  uint32_t gph = 0;  // parity of each stage's gfull barrier
+  bool live = true;
+  for (int i = 0;; ++i) {
+    const int st = i % kSt;
+    const int64_t c = held[st];
+    if (c < 0) break;
+    held[st] = -1;
+    const uint32_t par = (gph >> st) & 1u;
+    gph ^= 1u << st;
+    if (live) {
+      int got = 1;
+      if (lane == 0) got = mbar_wait2(&sc->gfull[st], par, sc, a) ? 1 : 0;
+      live = __shfl_sync(0xffffffffu, got, 0) != 0;
+      if (!live) more = false;
+    }
+    if (!live) {  // let the chunk's copies land, store nothing
+      if (lane == 0) mbar_wait_quiet(&sc->gfull[st], par, a.timeout_ns);
+      __syncwarp();
+      continue;
+    }
+    const int64_t p0 = c * rps;
+    const int nr = (int)(a.S - p0 < rps ? a.S - p0 : rps);
+    if (lane < nr)
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                       reinterpret_cast<uint64_t>(h.Y + (p0 + lane) * a.ahead_ldY)),
+                   "r"(smem_u32(smem + (size_t)st * kStageBytes2 + (size_t)lane * pitch)),
+                   "r"(pitch)
+                   : "memory");
+    bulk_commit();
+    if (more) {  // refill the stage stored last time
+      bulk_wait_read1();  // every store group but this chunk's has read shared memory
+      __syncwarp();
+      const int64_t cn = grab();
+      if (cn >= nch)
+        more = false;
+      else
+        issue((st + kSt - 1) % kSt, cn);
+    }
+  }
+  bulk_wait_all();  // this lane's stores are complete
+  __syncwarp();
 }
 
 // Far tiles: waits until the 256 values of alpha that multiply the tile's columns are
@@ -907,6 +1044,7 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
       mbar_init(&sc->tempty[i], 8);
     }
     mbar_init(&sc->drain, 1);
+    for (int i = 0; i < kSt; ++i) mbar_init(&sc->gfull[i], 1);
     sc->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -980,11 +1118,11 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
       }
     }
   } else if (warp == 0) {
+    int stage = 0;
+    uint32_t phase = 0;
     if (lane == 0) {
       // -------------------------------------------------------- TMA producer (both CTAs)
       WorkCursor<kFar> cur;
-      int stage = 0;
-      uint32_t phase = 0;
       for (int kq = 0, u = unit_of(a, cid, ncl, 0); u < a.ntiles && !sc->abort;
            u = unit_of(a, cid, ncl, ++kq)) {
         int rg, ca0, nq, t, pidx;
@@ -1010,6 +1148,12 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
           }
         }
       }
+    }
+    if (kFar && kNext && kRecV != 0 && a.ahead_on) {
+      __syncwarp();
+      const int st0 = __shfl_sync(0xffffffffu, stage, 0);
+      const uint32_t ph0 = __shfl_sync(0xffffffffu, phase, 0);
+      if (!__shfl_sync(0xffffffffu, sc->abort ? 1 : 0, 0)) gather_ahead<kSt>(a, sc, smem, lane, st0, ph0);
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
@@ -1244,6 +1388,9 @@ cudaError_t plan_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
   a.fs = s;
   a.stored_last = false;
   a.n_stored = a.far_head = a.store_tail = 0;
+  a.ahead_on = false;
+  a.ahead_ldY = 0;
+  memset(&a.ahead, 0, sizeof(a.ahead));
   a.gB = gB;
   a.seed = a.ctr_g = a.ctr_f = 0;
   a.m = 0;
@@ -1382,6 +1529,11 @@ bool far_gram_supported(int64_t S, int64_t n, int b) {
   return gram_recur_fused_supported(S, n, b) && b % 256 == 0;
 }
 
+bool ahead_rows_supported(int64_t n, int64_t ldY) {
+  // whole 16-byte row copies; rows of at least 512 bytes that fit a stage
+  return n % 8 == 0 && ldY * 2 >= 512 && ldY * 2 <= kStageBytes2;
+}
+
 namespace {
 
 // Units of the far-forming order: far (t < j-B) and stored (band, and the diagonal on
@@ -1453,7 +1605,7 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
                               const float* yY, float* alpha, float* far, uint32_t* slab,
                               float* fpart, float* part, float* w, bool own_margins, Ctrl* ctrl,
                               uint32_t timeout_us, bool g_band, const RowSource* rs,
-                              uint64_t ctr_g, uint64_t ctr_f, Ctx& c) {
+                              uint64_t ctr_g, uint64_t ctr_f, const AheadRows* ahead, Ctx& c) {
   if (!gram_recur_fused_supported(S, n, b)) return cudaErrorNotSupported;
   const bool far_gram = fpart != nullptr;
   if (far_gram && !far_gram_supported(S, n, b)) return cudaErrorNotSupported;
@@ -1496,6 +1648,11 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
     // next: the next iteration's band (none without its rows) after one round of far
     // units (far_head is set once the grid is known)
     P.a.stored_last = next;
+    if (ahead && next && !gather && ahead_rows_supported(n, ldY)) {
+      P.a.ahead_on = true;
+      P.a.ahead_ldY = ldY;
+      P.a.ahead = *ahead;
+    }
     const bool g_rows = gather ? ctr_g != kNoRows : Yg != nullptr;  // the Gram has rows
     P.a.n_stored = (int)((!next || g_rows) ? nst : 0);
     P.a.ntiles = (int)(nfar + P.a.n_stored);

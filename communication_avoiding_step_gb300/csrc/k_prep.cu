@@ -105,6 +105,7 @@ __device__ void reset_recurrence(const RowArgs& a) {
     a.ctrl->next_unit = 0;
     a.ctrl->upd_next = 0;
     a.ctrl->band_done = 0;
+    a.ctrl->ahead_next = 0;
     a.ctrl->abort = (a.ctrl->status & ST_TIMEOUT) ? 1u : 0u;  // stays set after a timeout
   }
   const int64_t nslab = (a.S + 255) / 256 * 8;  // the Gram's 32-row counters

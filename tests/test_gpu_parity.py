@@ -358,27 +358,33 @@ def test_far_from_gram_parity(gpu_lib, name, factory, override):
 
 
 FAR_PIPE_CASES = [
+    # rows of n % 8 == 0 columns (at least 256) are gathered two iterations ahead inside
+    # the far-forming launch; the others by a launch of their own
     ("recipe2_m20000", lambda: si.make_problem(2, m=20000), None),
+    ("recipe5_m20000", lambda: si.make_problem(5, m=20000), None),
     ("recipe3_m60000", lambda: si.make_problem(3, m=60000), None),
     ("ragged_3000x130_b256_s5", lambda: si.make_random(3000, 130, si.POISSON, seed=3),
      (256, 5, 0.02)),
+    ("ragged_3000x264_b256_s3", lambda: si.make_random(3000, 264, si.LOGISTIC, seed=4),
+     (256, 3, 0.1)),
 ]
 
 
 @pytest.mark.parametrize("name,factory,override", FAR_PIPE_CASES,
                          ids=[c[0] for c in FAR_PIPE_CASES])
 def test_far_from_gram_train_equals_outer_steps(gpu_lib, name, factory, override):
-    """casgd_train with the far-forming Gram gathers the next iteration's rows in the
-    launch that forms this iteration's margins and stores the next iteration's band in
-    the launch of this iteration's recurrence; the values are those of one outer
-    iteration at a time: bit-identical w after 3 iterations and after 1, and the same
-    again on a second run (the far sums are taken in a fixed order)."""
+    """casgd_train with the far-forming Gram stores the next iteration's band in the
+    launch of this iteration's recurrence, and gathers the rows two iterations ahead
+    there too (three row buffers in turn) or the next iteration's rows in a launch of
+    their own; the values are those of one outer iteration at a time: bit-identical w
+    after 5 iterations (every row buffer reused), after 2 and after 1, and the same again
+    on a second run (the far sums are taken in a fixed order)."""
     casgd = gpu_lib
     p = factory()
     data = _dev(p, casgd)
     params = _params(casgd, p, override, casgd.FLAG_FAR_FROM_GRAM)
     w0 = si.random_weights(p.n, seed=7)
-    for iters in (3, 1):
+    for iters in (5, 2, 1):
         ws = casgd.workspace(data, params)
         w_step = torch.from_numpy(w0.copy()).cuda()
         for k in range(iters):
@@ -391,6 +397,27 @@ def test_far_from_gram_train_equals_outer_steps(gpu_lib, name, factory, override
             assert kind == (6 if iters > 1 else 5)
             b_ = w_train.cpu().numpy()
             assert np.array_equal(a.view(np.uint32), b_.view(np.uint32)), (iters, _rel(b_, a))
+
+
+def test_far_train_rows_ahead_permuted_sampling(gpu_lib):
+    """The rows gathered two iterations ahead follow CASGD_FLAG_SAMPLE_PERMUTED's
+    sampler too: casgd_train over 4 iterations (crossing an epoch of the 20000 rows at
+    S = 8192) is bit-identical to 4 outer iterations one at a time."""
+    casgd = gpu_lib
+    p = si.make_problem(5, m=20000)
+    r = p.recipe
+    data = _dev(p, casgd)
+    params = casgd.Params(r.b, r.s, r.eta, r.loss, seed=3, flags=casgd.FLAG_SAMPLE_PERMUTED)
+    w0 = si.random_weights(p.n, seed=8)
+    ws = casgd.workspace(data, params)
+    w_step = torch.from_numpy(w0.copy()).cuda()
+    for k in range(4):
+        casgd.outer_step(data, params, w_step, 1 + k, ws)
+    w_train = torch.from_numpy(w0.copy()).cuda()
+    _, _, kind = casgd.train(data, params, w_train, 4, ws, k0=1)
+    assert kind == 6 and casgd.get_status(ws) == 0
+    a, b_ = w_step.cpu().numpy(), w_train.cpu().numpy()
+    assert np.array_equal(a.view(np.uint32), b_.view(np.uint32)), _rel(b_, a)
 
 
 def test_far_from_gram_is_the_default(gpu_lib):
