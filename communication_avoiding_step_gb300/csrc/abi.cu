@@ -39,6 +39,13 @@ struct Resolved {
   uint16_t* Y3;
   int32_t* idx3;
   float* yY3;
+  // second recurrence state (odd iterations of a run with the third row buffers)
+  Ctrl* ctrl2;
+  uint32_t* cnt2;
+  float* r2;
+  float* alpha2;
+  float* far2;
+  float* fpart2;
   float* fpart;  // far partial sums of the far-forming Gram (null: not laid out)
   float* upd;
   double* loss_part;
@@ -100,6 +107,12 @@ Resolved resolve(void* ws, const Layout& L) {
   R.Y3 = L.off_Y3 ? reinterpret_cast<uint16_t*>(base + L.off_Y3) : nullptr;
   R.idx3 = L.off_idx3 ? reinterpret_cast<int32_t*>(base + L.off_idx3) : nullptr;
   R.yY3 = L.off_yY3 ? reinterpret_cast<float*>(base + L.off_yY3) : nullptr;
+  R.ctrl2 = L.off_ctrl2 ? reinterpret_cast<Ctrl*>(base + L.off_ctrl2) : nullptr;
+  R.cnt2 = L.off_cnt2 ? reinterpret_cast<uint32_t*>(base + L.off_cnt2) : nullptr;
+  R.r2 = L.off_r2 ? reinterpret_cast<float*>(base + L.off_r2) : nullptr;
+  R.alpha2 = L.off_alpha2 ? reinterpret_cast<float*>(base + L.off_alpha2) : nullptr;
+  R.far2 = L.off_far2 ? reinterpret_cast<float*>(base + L.off_far2) : nullptr;
+  R.fpart2 = L.off_fpart2 ? reinterpret_cast<float*>(base + L.off_fpart2) : nullptr;
   R.fpart = L.off_fpart ? reinterpret_cast<float*>(base + L.off_fpart) : nullptr;
   R.upd = reinterpret_cast<float*>(base + L.off_upd);
   R.loss_part = reinterpret_cast<double*>(base + L.off_loss);
@@ -239,7 +252,8 @@ int outer_step_impl(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
     CK(launch_gram_recur(R.Y, G, false, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss, p->flags,
                          G, R.Y, R.r, R.yY, R.alpha, R.far, R.slab, gp.far ? R.fpart : nullptr,
                          R.upd, w, gp.far, R.ctrl, p->timeout_us,
-                         /*g_band=*/G == R.G, gather ? &rs : nullptr, ctr, ctr, nullptr, c));
+                         /*g_band=*/G == R.G, gather ? &rs : nullptr, ctr, ctr, nullptr,
+                         nullptr, nullptr, nullptr, c));
     if ((rc = record(prof, it, 2, st)) != CASGD_OK) return rc;
   } else {
     if (choice == 1)
@@ -309,13 +323,20 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
   c.pdl = true;
   // With third row buffers (far-forming, not gathering, rows ahead_rows_supported) the
   // launch of iteration k also gathers iteration k+2's rows (its producers, once their
-  // Gram work is done), so from the second iteration on the launch before it only
-  // gathers the iteration's indices and labels and resets the recurrence's state; the
-  // row buffers then rotate over three sets (the G buffers over two).
+  // Gram work is done), its indices and labels, and resets the recurrence state of
+  // iteration k+1, which alternates between two sets; from the second iteration on
+  // nothing runs between two such launches.  The row buffers rotate over three sets,
+  // the G buffers over two.
   const bool ahead = far && !gather && R.Y3 != nullptr;
   uint16_t* Yr[3] = {R.Y, R.Y2, R.Y3};
   int32_t* Ir[3] = {R.idx, R.idx2, R.idx3};
   float* yr[3] = {R.yY, R.yY2, R.yY3};
+  float* rS[2] = {R.r, R.r2};
+  float* aS[2] = {R.alpha, R.alpha2};
+  float* fS[2] = {R.far, R.far2};
+  float* fpS[2] = {fpart, R.fpart2};
+  Ctrl* qS[2] = {R.ctrl, R.ctrl2};
+  uint32_t* cS[2] = {R.slab, R.cnt2};
   for (int32_t it = 0; it < iters; ++it) {
     const int cur = it & 1, nxt = cur ^ 1;
     const uint64_t k = k0 + (uint64_t)it;
@@ -337,15 +358,14 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
         CK(launch_gram_tc(Yc, L.S, d->n, L.ldY, p->b, p->s, p->flags, 0, Gb[cur], R.ctrl,
                           p->timeout_us, c));
     }
+    const int cs = ahead ? (it & 1) : 0;  // this iteration's state set
     if (far && (!ahead || it == 0))  // next iteration's rows (gathering: its indices and
                                      // labels only) and this iteration's reset
       CK(launch_gather_reset(*d, *p, k + 1, nullptr, In, gather ? nullptr : Yn, yn,
                              it + 1 < iters, L.ldY, R.r, R.alpha, R.far, fpart, R.ctrl, R.slab,
                              c));
-    else if (far)  // this iteration's rows came with the launch two back: its indices and
-                   // labels, and the reset
-      CK(launch_gather_reset(*d, *p, k, nullptr, Ic, nullptr, yc, true, L.ldY, R.r, R.alpha,
-                             R.far, fpart, R.ctrl, R.slab, c));
+    else if (far)
+      ;  // (rows, indices, labels and state came with the launches before)
     else if (it + 1 < iters)  // next iteration's rows (into the buffers the last launch
                               // freed) and this iteration's margins, in one launch
       CK(launch_gather_next_margins(*d, *p, w, k + 1, In, Yn, yn, Yc, L.ldY, R.r, R.alpha,
@@ -358,20 +378,31 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
     // identity.)
     if (far) {  // this iteration's far sums; the next iteration's band (if any) into Gb[nxt]
       AheadRows ah{};
-      if (ahead && it + 2 < iters)
+      NextSet nx{};
+      const bool two = it + 2 < iters;
+      if (ahead && two)
         ah = AheadRows{rs.X, rs.ld, rs.m, rs.seed, rs.perm_d, (k + 2) * (uint64_t)L.S,
                        Yr[(it + 2) % 3]};
+      if (ahead && it + 1 < iters) {  // the next iteration's state; iteration k+2's labels
+        const int ns = cs ^ 1;
+        const int npb = far_partials_per_block(p->b, p->s);
+        nx = NextSet{rS[ns], aS[ns], fS[ns], fpS[ns], qS[ns], cS[ns], p->s * npb, p->b,
+                     band_width(p->b), npb, (int)((L.ldY + 63) / 64), p->s, d->y,
+                     two ? yr[(it + 2) % 3] : nullptr, two ? Ir[(it + 2) % 3] : nullptr,
+                     rs.seed, (k + 2) * (uint64_t)L.S, rs.m, rs.perm_d};
+      }
       CK(launch_gram_recur(gather ? nullptr : (it + 1 < iters ? Yn : nullptr), Gb[nxt], true,
                            L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss, p->flags, Gb[cur],
-                           gather ? nullptr : Yc, R.r, yc, R.alpha, R.far, R.slab, fpart, R.upd,
-                           w, true, R.ctrl, p->timeout_us, /*g_band=*/true, rsp,
+                           gather ? nullptr : Yc, rS[cs], yc, aS[cs], fS[cs], R.slab, fpS[cs],
+                           R.upd, w, true, R.ctrl, p->timeout_us, /*g_band=*/true, rsp,
                            it + 1 < iters ? (k + 1) * (uint64_t)L.S : kNoRows,
-                           k * (uint64_t)L.S, ah.Y ? &ah : nullptr, c));
+                           k * (uint64_t)L.S, ah.Y ? &ah : nullptr, qS[cs], cS[cs],
+                           nx.r ? &nx : nullptr, c));
     } else if (it + 1 < iters) {
       CK(launch_gram_recur(Yn, Gb[nxt], true, L.S, d->n, L.ldY, p->b, p->s, p->eta, p->loss,
                            p->flags, Gb[cur], Yc, R.r, yc, R.alpha, R.far, R.slab, nullptr,
                            R.upd, w, false, R.ctrl, p->timeout_us, false, nullptr, 0, 0,
-                           nullptr, c));
+                           nullptr, nullptr, nullptr, nullptr, c));
     } else {
       CK(launch_recur(Gb[cur], R.r, yc, R.alpha, R.far, R.slab, p->b, p->s, p->eta, p->loss,
                       p->flags, p->timeout_us, R.ctrl, Yc, L.ldY, d->n, R.upd, w, c));
@@ -543,6 +574,7 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms,
   if (with_G) off += align_up((size_t)L.gram_elems * sizeof(float));
   L.off_Y2 = L.off_G2 = L.off_idx2 = L.off_yY2 = L.off_fpart = 0;
   L.off_Y3 = L.off_idx3 = L.off_yY3 = 0;
+  L.off_ctrl2 = L.off_cnt2 = L.off_r2 = L.off_alpha2 = L.off_far2 = L.off_fpart2 = 0;
   if (gp.fused) {  // casgd_train gathers the rows (and runs the Gram) one iteration ahead
     L.off_idx2 = off;
     off += align_up((size_t)L.S * sizeof(int32_t));
@@ -566,6 +598,19 @@ Layout make_layout(int64_t n, int32_t b, int32_t s, uint32_t flags, int num_sms,
     off += align_up((size_t)L.S * sizeof(float));
     L.off_Y3 = off;
     off += align_up((size_t)L.S * L.ldY * sizeof(uint16_t));
+    L.off_ctrl2 = off;
+    off += align_up(sizeof(Ctrl));
+    L.off_cnt2 = off;
+    off += align_up((kMaxSlabs + kMaxUpdChunks + kMaxUpdBlocks) * sizeof(uint32_t) +
+                    (kMaxS + 1) * 4 * sizeof(uint64_t));
+    L.off_r2 = off;
+    off += align_up((size_t)L.S * sizeof(float));
+    L.off_alpha2 = off;
+    off += align_up((size_t)L.S * sizeof(float));
+    L.off_far2 = off;
+    off += align_up((size_t)L.S * sizeof(float));
+    L.off_fpart2 = off;
+    off += align_up((size_t)L.S * s * far_partials_per_block(b, s) * sizeof(float));
   }
   L.total = off;
   return L;

@@ -76,6 +76,9 @@ struct Layout {
   size_t off_idx, off_r, off_yY, off_alpha, off_far, off_Y, off_G, off_upd, off_loss;
   size_t off_Y2, off_G2, off_idx2, off_yY2;  // 0: no second buffers
   size_t off_Y3, off_idx3, off_yY3;  // third row buffers (rows gathered two ahead; 0: none)
+  // second recurrence state (with the third row buffers): control block, counters area,
+  // margins, alpha, far sums and far partials of the odd iterations of casgd_train
+  size_t off_ctrl2, off_cnt2, off_r2, off_alpha2, off_far2, off_fpart2;
   size_t off_fpart;  // far partial sums FP32[S][s * npb] of the far-forming Gram (0: none)
   size_t total;
 };
@@ -463,6 +466,29 @@ struct AheadRows {
   uint64_t ctr;
   uint16_t* Y;
 };
+// The state of the next outer iteration, which a far-forming launch of casgd_train
+// resets while it runs (the loop's launches alternate between two such sets, so no
+// launch between them is needed): margins r, alpha and far sums to pending (every row
+// p < S), far partials fpart to pending (row p's first ((p / fb) - fB) * fnp of fs),
+// the counters of q (next_unit, upd_next, band_done, ahead_next) and the update's
+// column and block counters (nchunk and s * nchunk from `counters`) to zero; and the
+// indices and labels of the iteration after it (sampler counters ctr .. ctr+S-1 of X's
+// m rows into idx and yY; none when yY is null).
+struct NextSet {
+  float* r;
+  float* alpha;
+  float* far;
+  float* fpart;
+  Ctrl* q;
+  uint32_t* counters;
+  int fs, fb, fB, fnp, nchunk, s;
+  const float* y;
+  float* yY;
+  int32_t* idx;
+  uint64_t seed, ctr;
+  uint32_t m;
+  int perm_d;
+};
 // Whether launch_gram_recur can gather rows ahead for these shapes.
 bool ahead_rows_supported(int64_t n, int64_t ldY);
 // own_margins (with fpart): the launch forms the margins itself (r reset to pending by
@@ -473,13 +499,17 @@ bool ahead_rows_supported(int64_t n, int64_t ldY);
 // starting at sampler counter ctr_g, this iteration's (far tiles, margins, update) those
 // starting at ctr_f.  ahead (non-null, with fpart and Yg, ahead_rows_supported): the
 // launch also gathers those rows (into buffers that none of its other work touches).
+// q / cnt (non-null): this iteration's counters and update counters area instead of
+// ctrl's and slab's (slab still holds the trace).  nx (non-null, with fpart and Yg): the
+// launch also resets that state set.
 cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t S, int64_t n,
                               int64_t ldY, int b, int s, float eta, int loss, uint32_t flags,
                               const float* G, const uint16_t* Y, float* r,
                               const float* yY, float* alpha, float* far, uint32_t* slab,
                               float* fpart, float* part, float* w, bool own_margins, Ctrl* ctrl,
                               uint32_t timeout_us, bool g_band, const RowSource* rs,
-                              uint64_t ctr_g, uint64_t ctr_f, const AheadRows* ahead, Ctx& c);
+                              uint64_t ctr_g, uint64_t ctr_f, const AheadRows* ahead, Ctrl* q,
+                              uint32_t* cnt, const NextSet* nx, Ctx& c);
 cudaError_t launch_update_reduce(const float* part, int upd_ctas, int64_t n, int64_t ldY,
                                  float* w, Ctrl* ctrl, Ctx& c);
 cudaError_t launch_update(const uint16_t* Y, const float* alpha, int64_t S, int64_t n,

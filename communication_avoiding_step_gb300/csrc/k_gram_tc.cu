@@ -52,7 +52,8 @@ constexpr size_t kSmemBytes =
 
 struct TcArgs {
   float* G;
-  Ctrl* ctrl;
+  Ctrl* ctrl;  // status and abort word
+  Ctrl* q;     // this iteration's counters (band_done, ahead_next)
   int64_t S;
   int n, b, nkb;
   int TR, TC, ntiles;  // ntiles: work items (tiles; units of nb tiles when fpart is set)
@@ -86,6 +87,9 @@ struct TcArgs {
   bool ahead_on;
   int64_t ahead_ldY;
   AheadRows ahead;
+  // The next iteration's state, reset during this launch (reset_next_set)
+  bool nx_on;
+  NextSet nx;
   // Weighted deal of the work items to the CTA pairs: the first pc pairs (those whose
   // CTAs also run the recurrence's chain) take wa items for every wb the other pairs
   // take (wa <= wb; wa == wb: plain round robin)
@@ -792,6 +796,40 @@ __device__ bool mbar_wait2(uint64_t* bar, uint32_t parity, SharedCtl2<kSt>* sc, 
   }
 }
 
+// Resets TcArgs::nx (see NextSet), by warp 1 of every CTA that does not lead its pair
+// (idle there: the leader's warp 1 issues the MMAs).  Pair cid's warp takes rows
+// cid*32 + lane, + ncl*32, ...; pair 0's also the counters.
+__device__ void reset_next_set(const NextSet& x, int64_t S, int cid, int ncl, int lane) {
+  const float pend = __uint_as_float(kAlphaPending);
+  if (cid == 0) {
+    if (lane == 0) {
+      x.q->next_unit = 0;
+      x.q->upd_next = 0;
+      x.q->band_done = 0;
+      x.q->ahead_next = 0;
+    }
+    uint32_t* chunks = upd_chunk_counters(x.counters);
+    for (int i = lane; i < x.nchunk; i += 32) chunks[i] = 0;
+    uint32_t* blocks = upd_block_counters(x.counters);
+    for (int i = lane; i < x.s * x.nchunk; i += 32) blocks[i] = 0;
+  }
+  for (int64_t p = (int64_t)cid * 32 + lane; p < S; p += (int64_t)ncl * 32) {
+    x.alpha[p] = pend;
+    x.far[p] = pend;
+    x.r[p] = pend;
+    if (x.fpart) {
+      const int nfar = ((int)(p / x.fb) - x.fB) * x.fnp;
+      float* row = x.fpart + p * x.fs;
+      for (int t = 0; t < nfar; ++t) row[t] = pend;
+    }
+    if (x.yY) {
+      const int32_t row = draw_row(x.seed, x.ctr + (uint64_t)p, x.m, x.perm_d);
+      x.idx[p] = row;
+      x.yY[p] = __ldg(x.y + row);
+    }
+  }
+}
+
 // Waits for a phase ignoring the abort word, at most timeout_ns: copies already issued
 // into this CTA's shared memory land before it leaves.
 __device__ __forceinline__ bool mbar_wait_quiet(uint64_t* bar, uint32_t parity, uint64_t ns) {
@@ -850,7 +888,7 @@ __device__ void gather_ahead(const TcArgs& a, SharedCtl2<kSt>* sc, uint8_t* smem
   auto grab = [&]() -> int64_t {
     if (res_left == 0) {
       int64_t c = 0;
-      if (lane == 0) c = (int64_t)atomicAdd(&a.ctrl->ahead_next, (unsigned)kGrab);
+      if (lane == 0) c = (int64_t)atomicAdd(&a.q->ahead_next, (unsigned)kGrab);
       res = __shfl_sync(0xffffffffu, c, 0);
       res_left = kGrab;
     }
@@ -1204,6 +1242,7 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
         }
       }
     }
+    if (kFar && kNext && kRecV != 0 && !leader && a.nx_on) reset_next_set(a.nx, a.S, cid, ncl, lane);
   } else if (warp < 6) {
     // ---------------------------------------------------------- epilogue (both CTAs)
     // Stored tiles: masked or TMA stores into G, then (recurrence in the same launch,
@@ -1272,7 +1311,7 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
           __syncwarp();
           if (lane == 0) {
             red_release_add_u32(a.slab + (int64_t)ra * 4 + quarter, (uint32_t)nq);
-            red_release_add_u32(&a.ctrl->band_done, (uint32_t)nq);
+            red_release_add_u32(&a.q->band_done, (uint32_t)nq);
             stamp_last(rec.trace, 0);
           }
         } else if (kRecV && lane == 0) {
@@ -1369,6 +1408,7 @@ cudaError_t plan_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
   TcArgs& a = P.a;
   a.G = G;
   a.ctrl = ctrl;
+  a.q = ctrl;
   a.S = S;
   a.n = (int)n;
   a.b = b;
@@ -1391,6 +1431,8 @@ cudaError_t plan_tc(const uint16_t* Y, int64_t S, int64_t n, int64_t ldY, int b,
   a.ahead_on = false;
   a.ahead_ldY = 0;
   memset(&a.ahead, 0, sizeof(a.ahead));
+  a.nx_on = false;
+  memset(&a.nx, 0, sizeof(a.nx));
   a.gB = gB;
   a.seed = a.ctr_g = a.ctr_f = 0;
   a.m = 0;
@@ -1605,7 +1647,8 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
                               const float* yY, float* alpha, float* far, uint32_t* slab,
                               float* fpart, float* part, float* w, bool own_margins, Ctrl* ctrl,
                               uint32_t timeout_us, bool g_band, const RowSource* rs,
-                              uint64_t ctr_g, uint64_t ctr_f, const AheadRows* ahead, Ctx& c) {
+                              uint64_t ctr_g, uint64_t ctr_f, const AheadRows* ahead, Ctrl* q,
+                              uint32_t* cnt, const NextSet* nx, Ctx& c) {
   if (!gram_recur_fused_supported(S, n, b)) return cudaErrorNotSupported;
   const bool far_gram = fpart != nullptr;
   if (far_gram && !far_gram_supported(S, n, b)) return cudaErrorNotSupported;
@@ -1632,6 +1675,14 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
   RecArgs rec = make_rec_args(G, r, yY, alpha, far, slab, b, s, eta, loss, flags, timeout_us,
                               ctrl, Y, ldY, n, part, w);
   rec.gB = gB;
+  if (q) {  // this iteration's counters (the trace stays in slab's area)
+    rec.q = q;
+    P.a.q = q;
+  }
+  if (cnt) {
+    rec.upd_chunks = upd_chunk_counters(cnt);
+    rec.upd_blocks = upd_block_counters(cnt);
+  }
   if (gather) {  // margins and update read this iteration's rows from X
     rec.X = rs->X;
     rec.ldx = rs->ld;
@@ -1652,6 +1703,10 @@ cudaError_t launch_gram_recur(const uint16_t* Yg, float* Gg, bool next, int64_t 
       P.a.ahead_on = true;
       P.a.ahead_ldY = ldY;
       P.a.ahead = *ahead;
+    }
+    if (nx && next && !gather) {
+      P.a.nx_on = true;
+      P.a.nx = *nx;
     }
     const bool g_rows = gather ? ctr_g != kNoRows : Yg != nullptr;  // the Gram has rows
     P.a.n_stored = (int)((!next || g_rows) ? nst : 0);

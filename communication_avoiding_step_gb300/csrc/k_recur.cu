@@ -45,6 +45,7 @@ RecArgs make_rec_args(const float* G, const float* r, const float* yY, float* al
   a.w = w;
   a.n = n;
   a.ctrl = ctrl;
+  a.q = ctrl;
   a.timeout_ns = (uint64_t)(timeout_us ? timeout_us : 1000000u) * 1000ull;
   a.b = b;
   a.s = s;

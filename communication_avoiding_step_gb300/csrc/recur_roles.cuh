@@ -102,7 +102,8 @@ struct RecArgs {
   const float* wm;  // w as the launch starts (w_k), read by the margin units
   bool far_gram;  // the Gram stores only the band (and diagonal) tiles
   int64_t S;
-  Ctrl* ctrl;
+  Ctrl* ctrl;  // status, abort word and diagnostics
+  Ctrl* q;     // this iteration's queues and counters (next_unit, upd_next, band_done)
   uint64_t timeout_ns;
   int b, s, loss, U, Uc, C, B, bulk_units;
   int upd_groups;  // bulk groups that serve the update queue first
@@ -325,7 +326,7 @@ __device__ void chain_role(const RecArgs& a, int c, int rt) {
     int ready = 1;
     if (!all_stored) {
       if (lane == 0) {
-        ready = ld_acquire_u32(&a.ctrl->band_done) >= a.band_total;
+        ready = ld_acquire_u32(&a.q->band_done) >= a.band_total;
         if (!ready) {
           const int64_t sl = ((int64_t)j * a.b + i) >> 5;
           ready = ld_acquire_u32(a.slab + sl) >= slab_need(a, sl) ? 2 : 0;
@@ -645,7 +646,7 @@ __device__ bool update_unit(const RecArgs& a, int u, int rt) {
     ok = __all_sync(0xffffffffu, ok);
     if (rt == 0) {
       s_ready = ok ? 1 : 0;
-      dealt = ld_volatile_u32(&a.ctrl->upd_next);  // used when the unit is done
+      dealt = ld_volatile_u32(&a.q->upd_next);  // used when the unit is done
     }
   }
   group_sync<kMode != 0>();
@@ -828,11 +829,11 @@ __device__ void bulk_role(const RecArgs& a, int rt, bool upd_group) {
       for (int pass = 0; pass < 2; ++pass) {
         const bool take_upd = (pass == 0) == upd_group;
         if (take_upd && upd_left) {
-          const int v = (int)atomicAdd(&a.ctrl->upd_next, 1u);
+          const int v = (int)atomicAdd(&a.q->upd_next, 1u);
           if (v < a.upd_units) { u = a.bulk_units + v; break; }
           upd_left = false;
         } else if (!take_upd && far_left) {
-          const int v = (int)atomicAdd(&a.ctrl->next_unit, 1u);
+          const int v = (int)atomicAdd(&a.q->next_unit, 1u);
           if (v < a.bulk_units) { u = v; break; }
           far_left = false;
         }

@@ -93,8 +93,10 @@ def test_workspace_sections_of_the_gram_paths(lib):
     # adds a second idx, y_Y, Y and G for casgd_train's iteration-ahead Gram; the
     # far-forming default keeps both G buffers in the band layout (the B = 3 blocks
     # below the diagonal of each block row: 90 of the 496 blocks) and adds the far
-    # partials (one column group per block: S x s floats) and a third set of row
-    # buffers (idx, y_Y, Y: the launch of iteration k gathers iteration k+2's rows)
+    # partials (one column group per block: S x s floats), a third set of row buffers
+    # (idx, y_Y, Y: the launch of iteration k gathers iteration k+2's rows) and a second
+    # recurrence state (control block, counters area, r, alpha, far sums, far partials:
+    # the launches alternate between two)
     n, b, s = 2000, 256, 32
     S, ld = b * s, 2048          # Y rows padded to whole 128-byte lines
     G = s * (s - 1) // 2 * b * b * 4
@@ -104,8 +106,10 @@ def test_workspace_sections_of_the_gram_paths(lib):
     full_g = _ws_bytes(lib, n, b, s, nat.FLAG_FULL_G)
     far = _ws_bytes(lib, n, b, s, 0)
     assert full_g - no_fuse == 2 * _a(S * 4) + _a(S * ld * 2) + _a(G)
+    counters = _a((65536 // 256 * 8 + 16384 // 64 + 64 * (16384 // 64)) * 4 + 65 * 4 * 8)
+    state2 = _a(32) + counters + 3 * _a(S * 4) + _a(S * s * 1 * 4)
     assert far - full_g == (2 * _a(Gb) - 2 * _a(G) + _a(S * s * 1 * 4)
-                            + _a(S * 4) + _a(S * 4) + _a(S * ld * 2))
+                            + _a(S * 4) + _a(S * 4) + _a(S * ld * 2) + state2)
     # b = 1024, s = 16, n = 18 (rows of 36 bytes: gathered by their own launch, no third
     # row buffers): the stored G is not shared with the recurrence there
     # (b > 512), so only the far-forming path has second buffers; its band is one block
