@@ -170,7 +170,8 @@ def train(data: Dataset, params: Params, w: torch.Tensor, iters: int, ws: torch.
     prof = _Profile()
     ev_arr = None
     if stage_events is not None:
-        ev_arr = (C.c_void_p * len(stage_events))(*[e.cuda_event for e in stage_events])
+        ev_arr = (C.c_void_p * len(stage_events))(
+            *[e.cuda_event if e is not None else None for e in stage_events])
         prof.stage_events = C.cast(ev_arr, C.POINTER(C.c_void_p))
         prof.n_events = len(stage_events)
     _check(load().casgd_train(C.byref(data.c()), C.byref(params.c()), _ptr(w), k0, iters,
@@ -348,7 +349,8 @@ def train_sharded(data: Dataset, params: Params, w: torch.Tensor, iters: int, ws
     prof = _Profile()
     ev_arr = None
     if stage_events is not None:
-        ev_arr = (C.c_void_p * len(stage_events))(*[e.cuda_event for e in stage_events])
+        ev_arr = (C.c_void_p * len(stage_events))(
+            *[e.cuda_event if e is not None else None for e in stage_events])
         prof.stage_events = C.cast(ev_arr, C.POINTER(C.c_void_p))
         prof.n_events = len(stage_events)
     _check(load().casgd_train_sharded(C.byref(data.c()), C.byref(params.c()), _ptr(w), k0, iters,

@@ -187,7 +187,7 @@ GramPlan gram_plan(int64_t n, int32_t b, int32_t s, uint32_t flags) {
 int record(casgd_profile_t* prof, int64_t it, int e, cudaStream_t st) {
   if (!prof || !prof->stage_events) return CASGD_OK;
   const int64_t i = it * CASGD_STAGE_EVENTS + e;
-  if (i >= prof->n_events) return CASGD_OK;
+  if (i >= prof->n_events || !prof->stage_events[i]) return CASGD_OK;  // (null: none here)
   if (cudaEventRecord(static_cast<cudaEvent_t>(prof->stage_events[i]), st) != cudaSuccess)
     return CASGD_ERR_CUDA;
   return CASGD_OK;

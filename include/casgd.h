@@ -199,10 +199,11 @@ typedef struct {
                             before stage e of outer iteration it (e = 0 gather,
                             1 Gram, 2 recurrence, 3 update, 4 after update;
                             when the Gram and the recurrence share one launch,
-                            events 2 and 3 are both recorded after it).  An
-                            event between two launches keeps them from
-                            overlapping (see casgd_train), so a timed loop
-                            with events runs slower than one without        */
+                            events 2 and 3 are both recorded after it); a NULL
+                            entry records nothing.  An event between two
+                            launches keeps them from overlapping (see
+                            casgd_train), so a timed loop with events runs
+                            slower than one without                          */
   int32_t n_events;      /* in: length of stage_events                          */
   int32_t gram_kind;     /* out: 1 = tcgen05 Gram kernel used, 2 = CUDA-core,
                             3 = paired-SM tcgen05 Gram and recurrence in one
