@@ -456,7 +456,8 @@ cudaError_t launch_gram_band(const uint16_t* Y, float* G, int64_t S, int64_t n, 
 // Rows that a far-forming launch gathers for a later iteration once its own Gram work is
 // done (launch_gram_recur's `ahead`): rows ctr .. ctr+S-1 of the sampler (draw_row with
 // seed, m, perm_d) of X (pitch ld) into Y (pitch ldY; columns n .. ldY-1 written as
-// zeros).  n % 8 == 0.  Their labels and indices are gathered separately.
+// zeros); n % 8 == 0 for rows wider than 64 columns (ahead_rows_supported).  Their
+// labels and indices are gathered separately.
 struct AheadRows {
   const uint16_t* X;
   int64_t ld;

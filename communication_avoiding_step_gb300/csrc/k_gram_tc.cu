@@ -788,6 +788,46 @@ __device__ bool mbar_wait2(uint64_t* bar, uint32_t parity, SharedCtl2<kSt>* sc, 
   }
 }
 
+// Narrow rows (ldY <= 64 columns) gathered ahead (TcArgs::ahead) by the producer warp
+// once its Gram work is issued, with plain 16-byte loads and stores: one row per lane,
+// chunks of 32 rows taken four at a time from Ctrl::ahead_next.  X's rows have at least
+// ldY/8 whole vectors (ld >= n, ld % 8 == 0); the columns from n on are stored as zeros.
+__device__ void gather_ahead_narrow(const TcArgs& a, int lane) {
+  const AheadRows& h = a.ahead;
+  const int ldv = (int)(a.ahead_ldY / 8);  // 16-byte vectors per row, at most 8
+  const int64_t nch = (a.S + 31) / 32;
+  constexpr int kGrab = 4;
+  while (true) {
+    int64_t c0 = 0;
+    if (lane == 0) c0 = (int64_t)atomicAdd(&a.q->ahead_next, (unsigned)kGrab);
+    c0 = __shfl_sync(0xffffffffu, c0, 0);
+    if (c0 >= nch) break;
+    for (int k = 0; k < kGrab; ++k) {
+      const int64_t p = (c0 + k) * 32 + lane;
+      if (c0 + k >= nch || p >= a.S) continue;
+      const int32_t x = draw_row(h.seed, h.ctr + (uint64_t)p, h.m, h.perm_d);
+      const uint4* src = reinterpret_cast<const uint4*>(h.X + (int64_t)x * h.ld);
+      uint4* dst = reinterpret_cast<uint4*>(h.Y + p * a.ahead_ldY);
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i < ldv) v[i] = __ldg(src + i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (i >= ldv) break;
+        uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {  // columns i*8 + 2e and i*8 + 2e + 1
+          const int c = i * 8 + 2 * e;
+          if (c >= a.n) w4[e] = 0u;
+          else if (c + 1 >= a.n) w4[e] &= 0xFFFFu;
+        }
+        dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+    }
+  }
+}
+
 // Resets TcArgs::nx (see NextSet), by warp 1 of every CTA that does not lead its pair
 // (idle there: the leader's warp 1 issues the MMAs).  Pair cid's warp takes rows
 // cid*32 + lane, + ncl*32, ...; pair 0's also the counters.
@@ -1183,7 +1223,12 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
       __syncwarp();
       const int st0 = __shfl_sync(0xffffffffu, stage, 0);
       const uint32_t ph0 = __shfl_sync(0xffffffffu, phase, 0);
-      if (!__shfl_sync(0xffffffffu, sc->abort ? 1 : 0, 0)) gather_ahead<kSt>(a, sc, smem, lane, st0, ph0);
+      if (!__shfl_sync(0xffffffffu, sc->abort ? 1 : 0, 0)) {
+        if (a.ahead_ldY <= 64)
+          gather_ahead_narrow(a, lane);
+        else
+          gather_ahead<kSt>(a, sc, smem, lane, st0, ph0);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
@@ -1564,8 +1609,9 @@ bool far_gram_supported(int64_t S, int64_t n, int b) {
 }
 
 bool ahead_rows_supported(int64_t n, int64_t ldY) {
-  // whole 16-byte row copies; rows of at least 512 bytes that fit a stage
-  return n % 8 == 0 && ldY * 2 >= 512 && ldY * 2 <= kStageBytes2;
+  // whole 16-byte row copies through the stages, rows of at least 512 bytes that fit a
+  // stage; or narrow rows (at most 64 columns) by plain vector loads
+  return (n % 8 == 0 && ldY * 2 >= 512 && ldY * 2 <= kStageBytes2) || ldY <= 64;
 }
 
 namespace {

@@ -110,8 +110,8 @@ def test_workspace_sections_of_the_gram_paths(lib):
     state2 = _a(32) + counters + 3 * _a(S * 4) + _a(S * s * 1 * 4)
     assert far - full_g == (2 * _a(Gb) - 2 * _a(G) + _a(S * s * 1 * 4)
                             + _a(S * 4) + _a(S * 4) + _a(S * ld * 2) + state2)
-    # b = 1024, s = 16, n = 18 (rows of 36 bytes: gathered by their own launch, no third
-    # row buffers): the stored G is not shared with the recurrence there
+    # b = 1024, s = 16, n = 18 (narrow rows, gathered ahead with plain loads: third row
+    # buffers and a second state too): the stored G is not shared with the recurrence there
     # (b > 512), so only the far-forming path has second buffers; its band is one block
     # wide; four column groups per block keep a row's far partials within 64
     n, b, s = 18, 1024, 16
@@ -120,8 +120,10 @@ def test_workspace_sections_of_the_gram_paths(lib):
     Gb = _band_blocks(s, 1) * b * b * 4
     full_g = _ws_bytes(lib, n, b, s, nat.FLAG_FULL_G)
     far = _ws_bytes(lib, n, b, s, 0)
+    state2 = _a(32) + counters + 3 * _a(S * 4) + _a(S * s * 4 * 4)
     assert far - full_g == (2 * _a(S * 4) + _a(S * ld * 2) + 2 * _a(Gb) - _a(G)
-                            + _a(S * s * 4 * 4))
+                            + _a(S * s * 4 * 4)
+                            + 2 * _a(S * 4) + _a(S * ld * 2) + state2)
     # least squares 11,000,000 x 28 at b = 2048, s = 32 (S = 65536): 31 band blocks of
     # 16 MiB per buffer instead of 496 (8.3 GB) in the packed block-lower layout
     far = _ws_bytes(lib, 28, 2048, 32, 0)
