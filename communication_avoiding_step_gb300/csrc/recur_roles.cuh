@@ -77,8 +77,9 @@ struct RecArgs {
   int64_t ldY;
   int upd_units;
   int upd_R;  // row parts per block (upd_row_parts)
-  // the update's last stage: the last row part of (block, column chunk) sums the parts
-  // and adds them to w in block order (upd_chunks: the next block per chunk)
+  // the update's counters: row parts of (block, column chunk) that have stored their
+  // partial row (upd_blocks), and block sums of a column chunk formed (upd_chunks; the
+  // last adds the chunk's s block sums to w)
   uint32_t* upd_chunks;
   uint32_t* upd_blocks;
   float* w;
