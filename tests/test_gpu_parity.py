@@ -399,6 +399,29 @@ def test_far_from_gram_train_equals_outer_steps(gpu_lib, name, factory, override
             assert np.array_equal(a.view(np.uint32), b_.view(np.uint32)), (iters, _rel(b_, a))
 
 
+@pytest.mark.parametrize("name,factory,override,per_iter", [
+    ("recipe2_m20000", lambda: si.make_problem(2, m=20000), None, 1),
+    ("recipe3_m60000", lambda: si.make_problem(3, m=60000), None, 1),
+    ("ragged_3000x130_b256_s5", lambda: si.make_random(3000, 130, si.POISSON, seed=3),
+     (256, 5, 0.02), 2),
+], ids=lambda v: v if isinstance(v, str) else "")
+def test_far_train_launches_per_iteration(gpu_lib, name, factory, override, per_iter):
+    """The far-forming casgd_train: a prologue (the first rows, the first band, the
+    second rows and the reset: four launches with the first shared launch), then one
+    launch per outer iteration where the launch gathers the rows two ahead itself (rows
+    of n % 8 == 0 and at least 512 bytes, or of at most 64 columns), else two."""
+    casgd = gpu_lib
+    p = factory()
+    data = _dev(p, casgd)
+    params = _params(casgd, p, override, 0)
+    ws = casgd.workspace(data, params)
+    w = torch.zeros(p.n, device="cuda")
+    iters = 6
+    _, launches, kind = casgd.train(data, params, w, iters, ws)
+    assert kind == 6 and casgd.get_status(ws) == 0
+    assert launches == 4 + per_iter * (iters - 1)
+
+
 def test_far_train_rows_ahead_permuted_sampling(gpu_lib):
     """The rows gathered two iterations ahead follow CASGD_FLAG_SAMPLE_PERMUTED's
     sampler too: casgd_train over 4 iterations (crossing an epoch of the 20000 rows at
