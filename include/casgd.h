@@ -282,7 +282,11 @@ int casgd_outer_step(const casgd_data_t* data, const casgd_params_t* params, flo
  * buffers that casgd_workspace_size includes for such parameters; with the far-
  * forming Gram (CASGD_FLAG_FAR_FROM_GRAM, the default for b a multiple of 256) the
  * launch of iteration k forms iteration k's far sums and margins and stores the band
- * of iteration k+1, after a launch that gathers iteration k+1's rows.  The loop's
+ * of iteration k+1, after a launch that gathers iteration k+1's rows.  Where n % 8 == 0
+ * with rows of at least 512 bytes, or n <= 64 (not with CASGD_FLAG_GATHER_ROWS), that
+ * launch also gathers iteration k+2's rows, indices and labels and resets iteration
+ * k+1's recurrence state (third row buffers and a second state in the workspace), so
+ * from the second iteration on one launch runs per iteration.  The loop's
  * launches use programmatic dependent launch: each may be scheduled while the one
  * before it ends and waits for that one's completion before it touches memory, so
  * work the caller enqueues on `stream` keeps plain stream order.  Either way the
