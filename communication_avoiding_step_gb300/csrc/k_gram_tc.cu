@@ -878,9 +878,9 @@ __device__ __forceinline__ bool mbar_wait_quiet(uint64_t* bar, uint32_t parity, 
 // from the sampler and copies its n*2 bytes from X into the stage (cp.async.bulk,
 // completion on the stage's gfull barrier); once landed the chunk goes out as
 // full-pitch bulk stores into Y (the stages' bytes from n*2 to the pitch are zeroed
-// once, so Y's padding stays zero).  The rows' labels and indices come with the launch
-// that resets the recurrence before the rows' own iteration.  Waits are bounded; after a
-// failed one the warp still lets the copies it issued land before it returns.
+// once, so Y's padding stays zero).  The rows' indices and labels are written by the
+// launch's reset of the next state (reset_next_set).  Waits are bounded; after a failed
+// one the warp still lets the copies it issued land before it returns.
 template <int kSt>
 __device__ void gather_ahead(const TcArgs& a, SharedCtl2<kSt>* sc, uint8_t* smem, int lane,
                              int stage, uint32_t phase) {
