@@ -580,10 +580,13 @@ def run_ours(args):
     value = samples / elapsed
     pk = peaks()
     work = alg_work(r.n, S, s, r.b, p.m)
-    # kind 3/4/5: the Gram (4: of the next iteration; 5: forming the far sums), the
+    # kind 3/4/5/6: the Gram (4: of the next iteration; 5/6: forming the far sums), the
     # recurrence and the update share one launch (its time is the "gram" stage; the
-    # "recurrence" stage is then empty)
+    # "recurrence" and "update" stages then hold only the gaps between events); kind 6
+    # also gathers the rows there, two iterations ahead, where the shapes allow (the
+    # "gather" stage then holds the prologue's gathers spread over the step)
     gram_name = GRAM_NAMES[kind]
+    fused_gather = kind == 6 and per_launch_ms["gather"] < 0.05 * per_launch_ms["gram"]
     stages_out = {}
     for st in STAGES:
         t = per_launch_ms[st] / 1e3
@@ -592,6 +595,10 @@ def run_ours(args):
         if st == "gram":
             ent["TFLOP/s"] = work[st]["flops"] / t / 1e12 if t > 0 else None
             ent["kernel"] = gram_name
+        elif (st in ("recurrence", "update") and kind in (3, 4, 5, 6)) or \
+                (st == "gather" and fused_gather):
+            ent["GB/s"] = None
+            ent["note"] = "runs inside the shared launch (the gram stage)"
         stages_out[st] = ent
     dom = max(STAGES, key=lambda st: per_launch_ms[st])
     t_dom = per_launch_ms[dom] / 1e3
