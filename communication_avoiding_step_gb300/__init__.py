@@ -180,6 +180,40 @@ def train(data: Dataset, params: Params, w: torch.Tensor, iters: int, ws: torch.
     return [hist[i] for i in range(nl)], int(prof.launches), int(prof.gram_kind)
 
 
+def _need_host(t: torch.Tensor, name: str, dtype, numel: int) -> None:
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name} must be a CPU tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{name} must hold at least {numel} elements, has {t.numel()}")
+
+
+def train_host(X_host: torch.Tensor, y_host: torch.Tensor, w_host: torch.Tensor,
+               data: Dataset, w_dev: torch.Tensor, params: Params, iters: int,
+               ws: torch.Tensor, k0: int = 0, loss_every: int = 0, stream=None):
+    """casgd_train on host inputs: X_host (CPU BF16, the layout of data.X), y_host and
+    w_host (CPU FP32; pin them for full-rate copies) are copied into data's device buffers
+    and w_dev, and w_host receives the result.  Returns (loss history, launches,
+    gram_kind).  Blocks."""
+    _need_host(X_host, "X_host", torch.bfloat16, data.X.numel())
+    _need_host(y_host, "y_host", torch.float32, data.m)
+    _need_host(w_host, "w_host", torch.float32, data.n)
+    _need_cuda(w_dev, "w_dev", torch.float32)
+    if w_dev.numel() < data.n:
+        raise ValueError(f"w_dev must hold at least {data.n} elements")
+    nl = iters // loss_every if loss_every > 0 else 0
+    hist = (C.c_double * max(nl, 1))()
+    prof = _Profile()
+    _check(load().casgd_train_host(_ptr(X_host), _ptr(y_host), _ptr(w_host), C.byref(data.c()),
+                                   _ptr(w_dev), C.byref(params.c()), k0, iters, _ptr(ws),
+                                   ws.numel(), _stream(stream), loss_every,
+                                   hist if nl > 0 else None, C.byref(prof)), "casgd_train_host")
+    return [hist[i] for i in range(nl)], int(prof.launches), int(prof.gram_kind)
+
+
 def loss(data: Dataset, kind: int, w: torch.Tensor, ws: torch.Tensor, stream=None) -> float:
     """Full-data loss f(w) (FP64 result).  Blocks."""
     out = C.c_double(0.0)

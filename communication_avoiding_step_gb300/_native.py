@@ -72,6 +72,9 @@ SIGNATURES = {
     "casgd_train": (C.c_int, [_P(Data), _P(Params), C.c_void_p, C.c_uint64, C.c_int32,
                               C.c_void_p, C.c_size_t, C.c_void_p, C.c_int32,
                               _P(C.c_double), _P(Profile)]),
+    "casgd_train_host": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, _P(Data), C.c_void_p,
+                                   _P(Params), C.c_uint64, C.c_int32, C.c_void_p, C.c_size_t,
+                                   C.c_void_p, C.c_int32, _P(C.c_double), _P(Profile)]),
     "casgd_loss": (C.c_int, [_P(Data), C.c_int32, C.c_void_p, C.c_void_p, C.c_size_t,
                              C.c_void_p, _P(C.c_double)]),
     "casgd_loss_async": (C.c_int, [_P(Data), C.c_int32, C.c_void_p, C.c_void_p, C.c_size_t,

@@ -731,6 +731,30 @@ int casgd_loss(const casgd_data_t* data, int32_t loss, const float* w, void* ws,
   return read_and_clear_status(R.ctrl, st);
 }
 
+int casgd_train_host(const void* X_host, const float* y_host, float* w_host,
+                     const casgd_data_t* data, float* w_dev, const casgd_params_t* params,
+                     uint64_t k0, int32_t iters, void* ws, size_t ws_bytes, void* stream,
+                     int32_t loss_every, double* loss_hist, casgd_profile_t* prof) {
+  if (!X_host || !y_host || !w_host || !w_dev || !check_data(data)) return CASGD_ERR_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t xbytes = (size_t)data->m * (size_t)data->ld * sizeof(uint16_t);
+  if (cudaMemcpyAsync(const_cast<void*>(data->X), X_host, xbytes, cudaMemcpyHostToDevice,
+                      st) != cudaSuccess ||
+      cudaMemcpyAsync(const_cast<float*>(data->y), y_host, (size_t)data->m * sizeof(float),
+                      cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(w_dev, w_host, (size_t)data->n * sizeof(float), cudaMemcpyHostToDevice,
+                      st) != cudaSuccess)
+    return CASGD_ERR_CUDA;
+  const int rc = casgd_train(data, params, w_dev, k0, iters, ws, ws_bytes, stream, loss_every,
+                             loss_hist, prof);
+  if (rc != CASGD_OK) return rc;
+  if (cudaMemcpyAsync(w_host, w_dev, (size_t)data->n * sizeof(float), cudaMemcpyDeviceToHost,
+                      st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return CASGD_ERR_CUDA;
+  return CASGD_OK;
+}
+
 int casgd_train(const casgd_data_t* data, const casgd_params_t* params, float* w,
                 uint64_t k0, int32_t iters, void* ws, size_t ws_bytes, void* stream,
                 int32_t loss_every, double* loss_hist, casgd_profile_t* prof) {

@@ -295,6 +295,21 @@ int casgd_train(const casgd_data_t* data, const casgd_params_t* params, float* w
                 uint64_t k0, int32_t iters, void* ws, size_t ws_bytes, void* stream,
                 int32_t loss_every, double* loss_hist, casgd_profile_t* prof);
 
+/* casgd_train on inputs that live in host memory: copies X_host (host, data->m rows of
+ * data->ld BF16 values, the layout of data->X) into data->X, y_host (host FP32[m]) into
+ * data->y and w_host (host FP32[n]) into w_dev on `stream`, runs casgd_train on the device
+ * buffers (data, w_dev, ws as there), and copies w_dev back into w_host.  Host buffers
+ * should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to run at full
+ * rate; pageable memory works but the copies then stage through the driver.  data->X,
+ * data->y and w_dev are caller-owned device buffers of those sizes (data->X 16-byte
+ * aligned, as for casgd_train).  Blocks until w_host holds the result; returns as
+ * casgd_train does, CASGD_ERR_ARG for a null host pointer or w_dev, CASGD_ERR_CUDA when a
+ * copy fails. */
+int casgd_train_host(const void* X_host, const float* y_host, float* w_host,
+                     const casgd_data_t* data, float* w_dev, const casgd_params_t* params,
+                     uint64_t k0, int32_t iters, void* ws, size_t ws_bytes, void* stream,
+                     int32_t loss_every, double* loss_hist, casgd_profile_t* prof);
+
 /* Step a9: f(w) = (1/m) sum_i l(x_i . w, y_i) with x_i the BF16 rows, each row's
  * dot product and loss in FP32, the sum in FP64.  Writes host *out; blocks. */
 int casgd_loss(const casgd_data_t* data, int32_t loss, const float* w, void* ws,

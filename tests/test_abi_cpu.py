@@ -161,6 +161,14 @@ def test_argument_errors_before_any_cuda_call(lib):
     rc = lib.casgd_sample_indices(0, 10, 0, 0, C.c_void_p(fake), None)
     assert rc == nat.CASGD_ERR_ARG
     assert lib.casgd_get_status(None, None) == nat.CASGD_ERR_WORKSPACE
+    # casgd_train_host: a null host buffer, a null w_dev or bad data, before any copy
+    hp = C.c_void_p(fake)
+    for args in ((None, hp, hp, good, hp), (hp, None, hp, good, hp), (hp, hp, None, good, hp),
+                 (hp, hp, hp, good, None), (hp, hp, hp, cases[0], hp)):
+        rc = lib.casgd_train_host(args[0], args[1], args[2], C.byref(args[3]), args[4],
+                                  C.byref(p), 0, 1, C.c_void_p(fake), 1 << 30, None, 0, None,
+                                  None)
+        assert rc == nat.CASGD_ERR_ARG
     # FP32 SGD: bad shapes, params and workspaces are rejected before any CUDA call
     nb = C.c_size_t(0)
     assert lib.casgd_sgd_workspace_size(256, C.byref(nb)) == 0 and nb.value >= 256 * 8

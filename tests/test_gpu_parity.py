@@ -422,6 +422,33 @@ def test_far_train_launches_per_iteration(gpu_lib, name, factory, override, per_
     assert launches == 4 + per_iter * (iters - 1)
 
 
+def test_train_host_equals_train_on_device_data(gpu_lib):
+    """casgd_train_host copies X, y and w0 from (pinned) host buffers into the caller's
+    device buffers, trains, and copies w back: bit-identical to casgd_train on the same
+    data already on the device, loss history included."""
+    casgd = gpu_lib
+    p = si.make_problem(5, m=20000)
+    r = p.recipe
+    data = _dev(p, casgd)
+    params = casgd.Params(r.b, r.s, r.eta, r.loss, seed=1)
+    Xh = data.X.cpu().pin_memory()
+    yh = data.y.cpu().pin_memory()
+    dset = casgd.Dataset(torch.empty_like(data.X), torch.empty_like(data.y), p.n)
+    w0 = si.random_weights(p.n, seed=12)
+    wh = torch.from_numpy(w0.copy()).pin_memory()
+    wdev = torch.empty(p.n, device="cuda")
+    hist, _, kind = casgd.train_host(Xh, yh, wh, dset, wdev, params, 3,
+                                     casgd.workspace(dset, params), k0=2, loss_every=3)
+    w_ref = torch.from_numpy(w0.copy()).cuda()
+    hist_ref, _, kind_ref = casgd.train(data, params, w_ref, 3, casgd.workspace(data, params),
+                                        k0=2, loss_every=3)
+    assert kind == kind_ref == 6
+    assert np.array_equal(wh.numpy().view(np.uint32), w_ref.cpu().numpy().view(np.uint32))
+    assert hist == hist_ref
+    with pytest.raises(ValueError):  # device tensors are not host buffers
+        casgd.train_host(data.X, yh, wh, dset, wdev, params, 1, casgd.workspace(dset, params))
+
+
 def test_far_train_rows_ahead_permuted_sampling(gpu_lib):
     """The rows gathered two iterations ahead follow CASGD_FLAG_SAMPLE_PERMUTED's
     sampler too: casgd_train over 4 iterations (crossing an epoch of the 20000 rows at
