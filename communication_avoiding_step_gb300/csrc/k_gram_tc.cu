@@ -927,6 +927,9 @@ __device__ void gather_ahead(const TcArgs& a, SharedCtl2<kSt>* sc, uint8_t* smem
     --res_left;
     return res++;
   };
+  // X's rows are read once here: evict them from L2 first (measured 126.3-128.1 ->
+  // 125.6 us per outer iteration on n = 2000)
+  const uint64_t pol = l2_evict_first_policy();
   auto issue = [&](int st, int64_t c) {  // chunk c's copies
     const int64_t p0 = c * rps;
     const int nr = (int)(a.S - p0 < rps ? a.S - p0 : rps);
@@ -934,8 +937,8 @@ __device__ void gather_ahead(const TcArgs& a, SharedCtl2<kSt>* sc, uint8_t* smem
     __syncwarp();
     if (lane < nr) {
       const int32_t x = draw_row(h.seed, h.ctr + (uint64_t)(p0 + lane), h.m, h.perm_d);
-      bulk_load(smem + (size_t)st * kStageBytes2 + (size_t)lane * pitch, h.X + (int64_t)x * h.ld,
-                rowb, &sc->gfull[st]);
+      bulk_load_hint(smem + (size_t)st * kStageBytes2 + (size_t)lane * pitch,
+                     h.X + (int64_t)x * h.ld, rowb, &sc->gfull[st], pol);
     }
     held[st] = c;
   };
