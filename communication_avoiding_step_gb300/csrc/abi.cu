@@ -359,20 +359,22 @@ int train_pipelined(const casgd_data_t* d, const casgd_params_t* p, float* w, ui
                           p->timeout_us, c));
     }
     const int cs = ahead ? (it & 1) : 0;  // this iteration's state set
-    if (far && (!ahead || it == 0))  // next iteration's rows (gathering: its indices and
-                                     // labels only) and this iteration's reset
-      CK(launch_gather_reset(*d, *p, k + 1, nullptr, In, gather ? nullptr : Yn, yn,
-                             it + 1 < iters, L.ldY, R.r, R.alpha, R.far, fpart, R.ctrl, R.slab,
-                             c));
-    else if (far)
-      ;  // (rows, indices, labels and state came with the launches before)
-    else if (it + 1 < iters)  // next iteration's rows (into the buffers the last launch
-                              // freed) and this iteration's margins, in one launch
+    if (far) {
+      // next iteration's rows (gathering: its indices and labels only) and this
+      // iteration's reset; with rows gathered ahead only in the first iteration (after
+      // it, rows, indices, labels and state come with the launches before)
+      if (!ahead || it == 0)
+        CK(launch_gather_reset(*d, *p, k + 1, nullptr, In, gather ? nullptr : Yn, yn,
+                               it + 1 < iters, L.ldY, R.r, R.alpha, R.far, fpart, R.ctrl,
+                               R.slab, c));
+    } else if (it + 1 < iters) {  // next iteration's rows (into the buffers the last launch
+                                  // freed) and this iteration's margins, in one launch
       CK(launch_gather_next_margins(*d, *p, w, k + 1, In, Yn, yn, Yc, L.ldY, R.r, R.alpha,
                                     R.far, fpart, R.ctrl, R.slab, c));
-    else
+    } else {
       CK(launch_gather(*d, *p, w, k, nullptr, Ic, Yc, L.ldY, R.r, yc, R.alpha, R.far, fpart,
                        R.ctrl, R.slab, MARGINS_ONLY, c));
+    }
     if ((rc = record(prof, it, 1, st)) != CASGD_OK) return rc;
     // (The sum of G over processes would sit before this launch; on one GPU it is the
     // identity.)
