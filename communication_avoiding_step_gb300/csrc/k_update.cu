@@ -126,225 +126,142 @@ __global__ void __launch_bounds__(256) update_reduce_kernel(const float* __restr
 }
 
 // Loss: the rows are streamed, never gathered -- each CTA owns a contiguous range of
-// rows, and because X is row-major with a 16-byte-multiple pitch, R consecutive rows are
-// one contiguous block that a single bulk copy (cp.async.bulk) moves into shared memory.
-// A producer lane keeps nst such stages in flight (a shared-memory ring with full/empty
-// barriers), so the bytes in flight per SM do not cost registers; eight consumer warps
-// take G lanes per row from the landed stage: lane g sums the row's 16-byte vectors g,
-// g+G, ... with w (staged in shared memory once), the row's lanes add by a shuffle tree,
-// and the row's loss is added in FP64.  Per row the FP32 dot product has the same order
-// as the margins.  Every wait is bounded; on expiry the CTA records ST_TIMEOUT, stops
-// consuming, and its producer waits (bounded) for its copies in flight before exiting.
-constexpr int kLossWarps = 16;                       // consumer warps
-constexpr int kLossThreads = 32 * (kLossWarps + 1);  // + one producer warp
-constexpr int kLossMaxStages = 8;
-constexpr uint32_t kLossStageBytes = 64 * 1024;
-constexpr int kLabelAhead = 8;                 // passes a label is copied ahead of its use
-constexpr int kLabelSlots = kLabelAhead + 1;   // ring slots per row slot of a pass
+// rows and reads each of its rows once, straight from HBM into registers.  G lanes per
+// row (a power of two; a lane holds at most eight of the row's 16-byte vectors for
+// n <= 2048): lane g takes the vectors g, g+G, ..., all of a lane's loads for a row
+// issued together.  For n <= 2048 (kPipe) a lane issues the loads of its next row
+// before it uses those of the current one, so each SM keeps about 128 KB of X in flight
+// without pause; wider rows are read eight vectors per lane at a time.  No staging in
+// shared memory and no hand-off between warps.  w is staged once in shared memory; the
+// row's label is loaded with its vectors.  Per row the FP32 dot product takes eight
+// sums (element e of every vector into sum e, vectors in increasing order), a fixed
+// tree, then a shuffle tree over the row's lanes -- the order of the margins; the row's
+// loss is added in FP64, the CTA's values in warp order, and the last CTA to finish
+// sums the CTA partials in CTA order.
+constexpr int kLossThreads = 256;
+constexpr int kLossV = 8;  // at most a lane's 16-byte loads per row (per batch of a wider row)
+// CTAs per SM the register budget is sized for (kV loads of two rows per lane in kPipe)
+constexpr int loss_min_ctas(int kV, bool pipe) { return pipe ? (kV >= 8 ? 2 : 4) : 3; }
 
 struct LossArgs {
   const uint16_t* X;
   const float* y;
   int64_t m, n, ld;
   int loss, G;
-  int R;            // rows per stage
-  int nst;          // stages in the ring
-  uint32_t stage;   // bytes per stage slot (multiple of 128)
-  uint32_t lring;   // bytes of the label ring (rows per pass x kLabelSlots floats)
   const float* w;
   double* part;
   double* out;
   Ctrl* ctrl;
-  uint64_t timeout_ns;
 };
 
-__device__ __forceinline__ bool loss_wait(uint64_t* bar, uint32_t parity, const LossArgs& a,
-                                          volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > a.timeout_ns) {
-      *abort_flag = 1;
-      atomicOr(&a.ctrl->status, ST_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-
-__global__ void __launch_bounds__(kLossThreads, 1) loss_kernel(LossArgs a) {
-  extern __shared__ __align__(128) uint8_t loss_smem[];
-  __shared__ uint64_t full[kLossMaxStages], empty[kLossMaxStages];
-  __shared__ double red[kLossWarps];
-  __shared__ volatile int s_abort;
+template <int kV, bool kPipe>
+__global__ void __launch_bounds__(kLossThreads, loss_min_ctas(kV, kPipe)) loss_kernel(LossArgs a) {
+  extern __shared__ __align__(16) float loss_w[];
+  __shared__ double red[kLossThreads / 32];
   __shared__ bool s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t ldv = a.ld / 8;                         // 16-byte vectors per row
   // w in two planes of ld/2 floats: plane 0 holds columns 8v..8v+3 of each 16-byte
   // vector v at 4v, plane 1 columns 8v+4..8v+7, so a warp's 16-byte reads of w for
   // consecutive vectors are contiguous (zero past n)
-  float* w_s = reinterpret_cast<float*>(loss_smem);
-  float* w_s1 = w_s + a.ld / 2;
-  float* label_ring = reinterpret_cast<float*>(loss_smem + ((a.ld * 4 + 127) / 128) * 128);
-  uint8_t* ring = reinterpret_cast<uint8_t*>(label_ring) + a.lring;
-  const int64_t r_lo = a.m * blockIdx.x / gridDim.x;
-  const int64_t r_hi = a.m * (blockIdx.x + 1) / gridDim.x;
-  const int64_t nchunk = (r_hi - r_lo + a.R - 1) / a.R;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < a.nst; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kLossWarps);
-    }
-    s_abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
+  float* w_s = loss_w;
+  float* w_s1 = loss_w + a.ld / 2;
   for (int64_t c = threadIdx.x; c < a.ld; c += blockDim.x)
     ((c & 4) ? w_s1 : w_s)[(c >> 3) * 4 + (c & 3)] = c < a.n ? a.w[c] : 0.0f;
   __syncthreads();
 
-  double mine = 0.0;
-  if (warp == kLossWarps) {
-    // ---------------------------------------------------------------- producer lane
-    if (lane == 0) {
-      int64_t issued = 0;
-      for (int64_t ch = 0; ch < nchunk && !s_abort; ++ch) {
-        const int st = (int)(ch % a.nst);
-        const uint32_t ph = (uint32_t)((ch / a.nst) & 1);
-        if (!loss_wait(&empty[st], ph ^ 1u, a, &s_abort)) break;
-        const int64_t row0 = r_lo + ch * a.R;
-        const int64_t rows = r_hi - row0 < a.R ? r_hi - row0 : a.R;
-        const uint32_t bytes = (uint32_t)(rows * a.ld * 2);
-        mbar_expect_tx(&full[st], bytes);
-        bulk_load(ring + (size_t)st * a.stage, a.X + row0 * a.ld, bytes, &full[st]);
-        issued = ch + 1;
-      }
-      // every copy issued has landed before the CTA may exit
-      for (int64_t ch = issued - a.nst < 0 ? 0 : issued - a.nst; ch < issued; ++ch) {
-        const int st = (int)(ch % a.nst);
-        const uint32_t ph = (uint32_t)((ch / a.nst) & 1);
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(&full[st], ph) && globaltimer_ns() - t0 < a.timeout_ns) {
+  const int G = a.G;
+  const int g = lane & (G - 1);
+  const int rows_per_pass = (kLossThreads / 32) * (32 / G);
+  const int my = warp * (32 / G) + lane / G;  // row slot within a pass
+  const int64_t r_lo = a.m * blockIdx.x / gridDim.x;
+  const int64_t r_hi = a.m * (blockIdx.x + 1) / gridDim.x;
+  const int nfull = (int)(a.n / 8);     // vectors wholly inside the n columns
+  const int nv = (int)((a.n + 7) / 8);  // vectors holding data
+
+  // the lane's vectors v0, v0+G, ... (at most kV) of row `row` (zeros if !live)
+  auto load = [&](int64_t row, bool live, int v0, uint4 (&xv)[kV]) {
+    const uint4* xr = reinterpret_cast<const uint4*>(a.X + (live ? row : 0) * a.ld);
+#pragma unroll
+    for (int k = 0; k < kV; ++k) {
+      const int v = v0 + k * G;
+      xv[k] = (live && v < nv) ? __ldg(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  // adds those vectors times w into the eight sums
+  auto add = [&](const uint4 (&xv)[kV], int v0, float (&sum)[8]) {
+#pragma unroll
+    for (int k = 0; k < kV; ++k) {
+      const int v = v0 + k * G;
+      if (v >= nv) break;
+      const float4 w0 = *reinterpret_cast<const float4*>(w_s + v * 4);
+      const float4 w1 = *reinterpret_cast<const float4*>(w_s1 + v * 4);
+      const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      uint32_t pw[4] = {xv[k].x, xv[k].y, xv[k].z, xv[k].w};
+      if (v >= nfull) {  // the partial last vector: columns from n on are not data
+        const int64_t c0 = (int64_t)v * 8;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int64_t cc = c0 + 2 * h;
+          if (cc >= a.n) pw[h] = 0;
+          else if (cc + 1 >= a.n) pw[h] &= 0xFFFFu;
         }
       }
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        sum[2 * h] = fmaf(__uint_as_float(pw[h] << 16), wv[2 * h], sum[2 * h]);
+        sum[2 * h + 1] = fmaf(__uint_as_float(pw[h] & 0xFFFF0000u), wv[2 * h + 1], sum[2 * h + 1]);
+      }
+    }
+  };
+  // the row's margin (eight sums, tree, shuffle tree) and, on its first lane, its loss
+  double mine = 0.0;
+  auto finish = [&](const float (&sum)[8], bool live, float label) {
+    float acc = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+    for (int off = G >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);
+    if (live && g == 0) mine += (double)loss_value(a.loss, acc, label);
+  };
+
+  if (kPipe) {  // one batch per row (nv <= kV * G); the next row's loads go first
+    int64_t row = r_lo + my;
+    bool live = row < r_hi;
+    uint4 xa[kV];
+    load(row, live, g, xa);
+    float la = (live && g == 0) ? __ldg(a.y + row) : 0.0f;
+    for (int64_t p0 = r_lo; p0 < r_hi; p0 += rows_per_pass) {  // CTA-uniform
+      const int64_t nrow = row + rows_per_pass;
+      const bool nlive = nrow < r_hi;
+      uint4 xb[kV];
+      load(nrow, nlive, g, xb);
+      const float lb = (nlive && g == 0) ? __ldg(a.y + nrow) : 0.0f;
+      float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      add(xa, g, sum);
+      finish(sum, live, la);
+#pragma unroll
+      for (int k = 0; k < kV; ++k) xa[k] = xb[k];
+      la = lb;
+      row = nrow;
+      live = nlive;
     }
   } else {
-    // ---------------------------------------------------------------- consumer warps
-    const int G = a.G;
-    const int g = lane & (G - 1);
-    const int rows_per_pass = kLossWarps * (32 / G);
-    const int my = warp * (32 / G) + lane / G;  // row slot within a pass
-    const int nfull = (int)(a.n / 8);             // vectors wholly inside the n columns
-    // Labels: pass P of the CTA is pass P % ppc of chunk P / ppc.  Lane g == 0 of each row
-    // slot copies its row's label kLabelAhead passes ahead into the slot's shared-memory
-    // ring with a 4-byte cp.async (one commit group per pass, empty where the row does
-    // not exist), so the label's memory latency never stalls a pass.  The ring has one
-    // slot more than the distance: the copy for pass P + kLabelAhead goes into the slot
-    // pass P - 1 read, never into the one the current pass is reading.
-    const int ppc = (a.R + rows_per_pass - 1) / rows_per_pass;
-    float* lring = label_ring + (size_t)my * kLabelSlots;
-    auto issue_label = [&](int64_t P) {
-      const int64_t ch = P / ppc;
-      const int64_t row = r_lo + ch * a.R + (P - ch * ppc) * rows_per_pass + my;
-      const int64_t end = r_lo + (ch + 1) * a.R < r_hi ? r_lo + (ch + 1) * a.R : r_hi;
-      if (g == 0 && ch < nchunk && row < end)
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
-                         smem_u32(lring + (P % kLabelSlots))),
-                     "l"(a.y + row)
-                     : "memory");
-      asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-    for (int64_t P = 0; P < kLabelAhead; ++P) issue_label(P);
-    for (int64_t ch = 0; ch < nchunk; ++ch) {
-      const int st = (int)(ch % a.nst);
-      const uint32_t ph = (uint32_t)((ch / a.nst) & 1);
-      int ok = 1;
-      if (lane == 0) ok = loss_wait(&full[st], ph, a, &s_abort) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      const int64_t row0 = r_lo + ch * a.R;
-      const int rows = (int)(r_hi - row0 < a.R ? r_hi - row0 : a.R);
-      const uint8_t* stg = ring + (size_t)st * a.stage;
-      for (int pp = 0; pp * rows_per_pass < rows; ++pp) {  // warp-uniform
-        const int64_t P = ch * ppc + pp;
-        const int q = pp * rows_per_pass + my;
-        const bool live = q < rows;
-        const uint4* xr = reinterpret_cast<const uint4*>(stg + (size_t)(live ? q : 0) * a.ld * 2);
-        // eight independent sums (element e of every vector into sum e), then a fixed tree
-        float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        auto add_full = [&](const uint4 xv, const float (&wv)[8]) {
-          const uint32_t pw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            sum[2 * h] = fmaf(__uint_as_float(pw[h] << 16), wv[2 * h], sum[2 * h]);
-            sum[2 * h + 1] = fmaf(__uint_as_float(pw[h] & 0xFFFF0000u), wv[2 * h + 1], sum[2 * h + 1]);
-          }
-        };
-        auto add_vec = [&](const uint4 xv, const float (&wv)[8], int64_t c0) {
-          uint32_t pw[4] = {xv.x, xv.y, xv.z, xv.w};
-          if (c0 + 8 > a.n) {  // columns from n on are not data: zero them
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const int64_t cc = c0 + 2 * h;
-              if (cc >= a.n) pw[h] = 0;
-              else if (cc + 1 >= a.n) pw[h] &= 0xFFFFu;
-            }
-          }
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            sum[2 * h] = fmaf(__uint_as_float(pw[h] << 16), wv[2 * h], sum[2 * h]);
-            sum[2 * h + 1] = fmaf(__uint_as_float(pw[h] & 0xFFFF0000u), wv[2 * h + 1], sum[2 * h + 1]);
-          }
-        };
-        // whole vectors (no masking), two at a time; then the partial last vector
-        if (live) {
-          int v = g;
-          for (; v + G < nfull; v += 2 * G) {
-            const uint4 x0 = xr[v], x1 = xr[v + G];
-            const float4 a0 = *reinterpret_cast<const float4*>(w_s + v * 4);
-            const float4 a1 = *reinterpret_cast<const float4*>(w_s1 + v * 4);
-            const float4 b0 = *reinterpret_cast<const float4*>(w_s + (v + G) * 4);
-            const float4 b1 = *reinterpret_cast<const float4*>(w_s1 + (v + G) * 4);
-            const float wva[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float wvb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-            add_full(x0, wva);
-            add_full(x1, wvb);
-          }
-          for (; v < nfull; v += G) {
-            const float4 a0 = *reinterpret_cast<const float4*>(w_s + v * 4);
-            const float4 a1 = *reinterpret_cast<const float4*>(w_s1 + v * 4);
-            const float wva[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            add_full(xr[v], wva);
-          }
-          if (v == nfull && nfull * 8 < a.n) {  // this lane holds the partial vector
-            const float4 a0 = *reinterpret_cast<const float4*>(w_s + v * 4);
-            const float4 a1 = *reinterpret_cast<const float4*>(w_s1 + v * 4);
-            const float wva[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            add_vec(xr[v], wva, (int64_t)v * 8);
-          }
-        }
-        float acc = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
-        for (int off = G >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, G);
-        // this pass's label: every group but the newest kLabelAhead - 1 has landed
-        asm volatile("cp.async.wait_group %0;" ::"n"(kLabelAhead - 1) : "memory");
-        if (live && g == 0) mine += (double)loss_value(a.loss, acc, lring[P % kLabelSlots]);
-        issue_label(P + kLabelAhead);  // into the slot pass P - 1 read
+    for (int64_t p0 = r_lo; p0 < r_hi; p0 += rows_per_pass) {  // CTA-uniform
+      const int64_t row = p0 + my;
+      const bool live = row < r_hi;
+      const float label = (live && g == 0) ? __ldg(a.y + row) : 0.0f;
+      float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int v0 = g; v0 < nv; v0 += kV * G) {
+        uint4 xv[kV];
+        load(row, live, v0, xv);
+        add(xv, v0, sum);
       }
-      // passes the last chunk does not have keep the pass count (and the ring) in step
-      for (int pp = (rows + rows_per_pass - 1) / rows_per_pass; pp < ppc; ++pp) {
-        asm volatile("cp.async.wait_group %0;" ::"n"(kLabelAhead - 1) : "memory");
-        issue_label(ch * ppc + pp + kLabelAhead);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
+      finish(sum, live, label);
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");  // no label copy outlives the CTA
-    for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
-    if (lane == 0) red[warp] = mine;
   }
+  for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
+  if (lane == 0) red[warp] = mine;
   __syncthreads();
   if (threadIdx.x == 0) {
     double t = 0.0;
-    for (int q = 0; q < kLossWarps; ++q) t += red[q];
+    for (int q = 0; q < kLossThreads / 32; ++q) t += red[q];
     a.part[blockIdx.x] = t;
     __threadfence();
     const uint32_t done = atomicAdd(&a.ctrl->loss_done, 1u);
@@ -399,7 +316,7 @@ cudaError_t launch_update_reduce(const float* part, int upd_ctas, int64_t n, int
 }
 
 int loss_ctas(int num_sms) {
-  int v = num_sms;
+  const int v = num_sms * loss_min_ctas(kLossV, false);
   return v > kLossCtas ? kLossCtas : v;
 }
 
@@ -415,36 +332,31 @@ cudaError_t launch_loss(const casgd_data_t& d, int loss, const float* w, double*
   // G lanes per row, each with at most eight of the row's 16-byte vectors where that
   // fits in 32 lanes
   const int64_t nv = (d.n + 7) / 8;
-  a.G = pow2_at_least((nv + 7) / 8, 32);
+  a.G = pow2_at_least((nv + kLossV - 1) / kLossV, 32);
   a.w = w;
   a.part = part;
   a.out = out_dev;
   a.ctrl = ctrl;
-  a.timeout_ns = 1000000000ull;
-  // stages of at least one row, 128-byte aligned slots; as many as fit beside w
-  const size_t row_bytes = (size_t)d.ld * 2;
-  size_t stage = row_bytes > kLossStageBytes ? row_bytes : kLossStageBytes;
-  stage = (stage + 127) / 128 * 128;
-  a.R = (int)(stage / row_bytes);
-  a.stage = (uint32_t)stage;
-  const size_t w_bytes = ((size_t)d.ld * 4 + 127) / 128 * 128;
-  const size_t rows_per_pass = (size_t)kLossWarps * (32 / a.G);
-  a.lring = (uint32_t)((rows_per_pass * kLabelSlots * 4 + 127) / 128 * 128);
-  const size_t budget = 216 * 1024;
-  int nst = (int)((budget - w_bytes - a.lring) / stage);
-  if (nst > 4) nst = 4;
-  if (nst < 2) return cudaErrorInvalidValue;  // (n <= 16384 keeps at least 2 stages)
-  a.nst = nst;
-  const size_t smem = w_bytes + a.lring + (size_t)nst * stage;
-  void (*const fn)(LossArgs) = loss_kernel;
+  // a lane's loads per row: kV (a power of two) covers its ceil(nv / G) vectors; wider
+  // rows (n > 2048) are read in batches of kLossV
+  const int64_t per_lane = (nv + a.G - 1) / a.G;
+  const bool pipe = per_lane <= kLossV;
+  const int kv = pipe ? pow2_at_least(per_lane, kLossV) : kLossV;
+  const size_t smem = (size_t)d.ld * 4;  // w's two planes (ld % 8 == 0)
+  void (*const fn)(LossArgs) = !pipe    ? loss_kernel<kLossV, false>
+                               : kv == 1 ? loss_kernel<1, true>
+                               : kv == 2 ? loss_kernel<2, true>
+                               : kv == 4 ? loss_kernel<4, true>
+                                         : loss_kernel<8, true>;
   int dummy = 0;
   cudaError_t e = cached_query(c, (const void*)fn, [&](int& v) {
     v = 1;
     return cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)(224 * 1024));
+                                (int)(64 * 1024));
   }, dummy);
   if (e != cudaSuccess) return e;
-  int64_t blocks = loss_ctas(c.num_sms);
+  int64_t blocks = (int64_t)c.num_sms * loss_min_ctas(kv, pipe);
+  if (blocks > kLossCtas) blocks = kLossCtas;
   if (blocks > d.m) blocks = d.m;
   fn<<<(unsigned)blocks, kLossThreads, smem, c.stream>>>(a);
   ++c.launches;

@@ -652,7 +652,8 @@ def test_deterministic(gpu_lib):
 # ---------------------------------------------------------------------- loss ----
 @pytest.mark.parametrize("kind,m,n", [(si.LOGISTIC, 10_001, 64), (si.LSQ, 5000, 28),
                                       (si.POISSON, 3001, 512), (si.LOGISTIC, 777, 2000),
-                                      (si.LSQ, 1, 3)])
+                                      (si.LSQ, 1, 3), (si.LSQ, 300, 4100),
+                                      (si.LOGISTIC, 4099, 12)])
 def test_loss_kernel_parity(gpu_lib, kind, m, n):
     casgd = gpu_lib
     p = si.make_random(m, n, kind, seed=11)
