@@ -314,6 +314,10 @@ FAR_CASES = [
     ("s40_b256_12000x64", lambda: si.make_random(12000, 64, si.LSQ, seed=9), (256, 40, 0.01)),
     # the largest S (65536) at recipe 4's shape
     ("max_S65536_recipe4_s32", lambda: si.make_problem(4, m=200_000), (2048, 32, 0.01)),
+    # one row part per update unit (at least 32 column chunks) with a partial last chunk
+    # and s not a multiple of 8: the last block's units add the block sums to w
+    ("ragged_3000x2056_b256_s5", lambda: si.make_random(3000, 2056, si.LOGISTIC, seed=5),
+     (256, 5, 0.1)),
 ]
 
 
@@ -367,6 +371,8 @@ FAR_PIPE_CASES = [
      (256, 5, 0.02)),
     ("ragged_3000x264_b256_s3", lambda: si.make_random(3000, 264, si.LOGISTIC, seed=4),
      (256, 3, 0.1)),
+    ("ragged_3000x2056_b256_s5", lambda: si.make_random(3000, 2056, si.LOGISTIC, seed=5),
+     (256, 5, 0.1)),
 ]
 
 
