@@ -1092,6 +1092,51 @@ __device__ __forceinline__ void far_tile_dot(uint32_t tmem, int acc, int quarter
   }
 }
 
+// The same with the choice as a template parameter, so the FP32 loop carries no
+// per-entry select: used by the launches with b >= 1024 (narrow n, where the far
+// tiles' epilogue paces the launch; measured on n = 28, b = 2048, s = 32: 1142 -> 998
+// us per outer iteration).  The other launches keep the form above (the change cost
+// the n = 2000 launch ~1 us through its register allocation).
+template <bool kGBf16>
+__device__ __forceinline__ float far_entry(uint32_t bits) {
+  const float g = __uint_as_float(bits);
+  return kGBf16 ? round_bf16(g) : g;
+}
+
+template <bool kGBf16>
+__device__ __forceinline__ void far_chunk(const uint32_t (&v)[32], const float* al,
+                                          float (&sum)[8]) {
+  const float4* a4 = reinterpret_cast<const float4*>(al);
+#pragma unroll
+  for (int e4 = 0; e4 < 8; ++e4) {
+    const float4 w = a4[e4];
+    const int o = (e4 & 1) * 4;
+    sum[o + 0] = fmaf(far_entry<kGBf16>(v[4 * e4 + 0]), w.x, sum[o + 0]);
+    sum[o + 1] = fmaf(far_entry<kGBf16>(v[4 * e4 + 1]), w.y, sum[o + 1]);
+    sum[o + 2] = fmaf(far_entry<kGBf16>(v[4 * e4 + 2]), w.z, sum[o + 2]);
+    sum[o + 3] = fmaf(far_entry<kGBf16>(v[4 * e4 + 3]), w.w, sum[o + 3]);
+  }
+}
+
+template <bool kGBf16>
+__device__ __forceinline__ void far_tile_dot(uint32_t tmem, int acc, int quarter,
+                                             const float* al, float (&sum)[8]) {
+  const uint32_t base = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+  uint32_t va[32], vb[32];
+  __syncwarp();
+  tmem_ld32_issue(base, va);
+  tmem_wait_ld(va);
+#pragma unroll
+  for (int ch = 0; ch < BN / 32; ch += 2) {
+    tmem_ld32_issue(base + (uint32_t)(ch + 1) * 32, vb);
+    far_chunk<kGBf16>(va, al + ch * 32, sum);
+    tmem_wait_ld(vb);
+    if (ch + 2 < BN / 32) tmem_ld32_issue(base + (uint32_t)(ch + 2) * 32, va);
+    far_chunk<kGBf16>(vb, al + (ch + 1) * 32, sum);
+    if (ch + 2 < BN / 32) tmem_wait_ld(va);
+  }
+}
+
 template <int kSt, int kRecV, bool kNext, bool kFar, bool kGather = false>
 __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
     gram_tc2sm_kernel(const __grid_constant__ CUtensorMap tmY,
@@ -1326,7 +1371,14 @@ __global__ void __launch_bounds__(kRecV ? kFusedThreads : kThreads, 1)
         tphase[acc] ^= 1u;
         tc_fence_after();
         if (kFar && far) {
-          if (!dead) far_tile_dot(tmem, acc, quarter, al_s, a.g_bf16, sum);
+          if (!dead) {
+            if constexpr (kRecV != 1)
+              far_tile_dot(tmem, acc, quarter, al_s, a.g_bf16, sum);
+            else if (a.g_bf16)
+              far_tile_dot<true>(tmem, acc, quarter, al_s, sum);
+            else
+              far_tile_dot<false>(tmem, acc, quarter, al_s, sum);
+          }
         } else {
           if (a.tma_store)
             store_tile_tma(a, tmem, acc, quarter, lane, ra, ca, &tmG, stage, sbuf);
